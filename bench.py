@@ -1,0 +1,548 @@
+#!/usr/bin/env python
+"""Throughput of the token early-exit step on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+  decode-1b (default): cosine gate (batch-min) -> compaction with gather ->
+      KV fill of 8 layers (identity map, int4 Wk/Wv) -> exit scatter, for a
+      64-token Llama-3.2-1B-shaped decode batch;
+  decode-tiny: the same on the tiny fp32 workload;
+  router-4096: router gate -> compaction with gather, 4096 tokens, d = 4096;
+  prefill-16k / prefill-120k: the RidgeFill KV fill of every layer after the
+      split for all filled rows.
+L2 is flushed (a write larger than L2) between timed steps, outside the timed
+events. Under torchrun each rank runs its own replica (independent batches,
+no collective on the data path: weak scaling); rank 0 prints one JSON line.
+The reference arm (--impl reference) times the CPU oracle on a bounded sample
+of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle is timed single-threaded; fix BLAS threads before numpy loads.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import configs, gen  # noqa: E402
+
+METRIC = "tokens/s through exit gate+compact+KV fill"
+WORKLOADS = ("decode-1b", "decode-tiny", "router-4096", "prefill-16k", "prefill-120k")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- workloads
+
+class Decode:
+    """gate -> compact (+gather) -> kv_fill -> scatter on one decode batch."""
+
+    def __init__(self, tee, cfg, dev, seed=0, case=None):
+        self.tee, self.cfg, self.dev = tee, cfg, dev
+        case = case or ("exit" if cfg.rule == "batch_all" else "default")
+        self.case = case
+        self.x = gen.decode_inputs(cfg, seed=seed, device=dev, case=case)
+        self.ws = tee.Workspace(dev)
+        self.fill = tee.KVFill(self.x["layers"], d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
+                               rope_base=cfg.rope_base, eps=cfg.eps, dtype=self.x["h_cur"].dtype,
+                               max_pos=cfg.cache_len, int4=cfg.weights == "int4", group=cfg.group)
+        n, d = cfg.batch, cfg.d
+        dt = self.x["h_cur"].dtype
+        self.g_out = {"score": torch.empty(n, device=dev), "mask": torch.empty(n, dtype=torch.uint8, device=dev),
+                      "flag": torch.empty(1, dtype=torch.int32, device=dev)}
+        self.c_out = {k: torch.empty(n, dtype=torch.int32, device=dev)
+                      for k in ("cont_rows", "exit_rows", "cont_pos", "exit_pos")}
+        self.c_out["counts"] = torch.empty(2, dtype=torch.int32, device=dev)
+        self.c_out["h_cont"] = torch.empty(n, d, dtype=dt, device=dev)
+        self.out = torch.zeros(n, d, dtype=dt, device=dev)
+        self.units = n
+        self.kernel = "kv_fill"
+        # algorithmic bytes of the fill call: weights + the h rows + K/V written
+        L = len(cfg.fill_layers)
+        kvw = cfg.kvw
+        if cfg.weights == "int4":
+            wbytes = 2 * (d * kvw // 2 + 2 * (d // cfg.group) * kvw * 2)
+        else:
+            wbytes = 2 * d * kvw * dt.itemsize
+        if cfg.map != "identity":
+            wbytes += d * d * dt.itemsize
+        wbytes += d * dt.itemsize  # gamma
+        self.n_exit_expected = None
+        self._fill_bytes_per_item_layer = 2 * kvw * dt.itemsize
+        self._fill_weight_bytes = L * wbytes
+        self._h_row_bytes = d * dt.itemsize
+        self.bound = "hbm"
+
+    def fill_bytes(self, n_exit):
+        L = len(self.cfg.fill_layers)
+        return self._fill_weight_bytes + n_exit * (self._h_row_bytes + L * self._fill_bytes_per_item_layer)
+
+    def step(self, ev=None):
+        tee, cfg, x = self.tee, self.cfg, self.x
+        tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule=cfg.rule, ws=self.ws, out=self.g_out)
+        tee.exit_compact(self.g_out["mask"], h=x["h_cur"], ws=self.ws, out=self.c_out)
+        if ev is not None:
+            ev[0].record()
+        self.fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=self.c_out["exit_rows"], pos=x["pos"],
+                  seq=x["seq"], n_dev=self.c_out["counts"][1:], n_max=cfg.batch, ws=self.ws)
+        if ev is not None:
+            ev[1].record()
+        tee.exit_scatter(self.c_out["counts"], self.c_out["exit_rows"], self.c_out["exit_pos"], x["h_cur"],
+                         self.out, ws=self.ws)
+
+    def host_io(self):
+        """Pinned host copies of the step's inputs and outputs for the end-to-end run."""
+        x = self.x
+        self.h_in = {k: x[k].cpu().pin_memory() for k in ("h_prev", "h_cur", "pos")}
+        self.h_out = {"score": torch.empty(self.cfg.batch).pin_memory(),
+                      "mask": torch.empty(self.cfg.batch, dtype=torch.uint8).pin_memory(),
+                      "counts": torch.empty(2, dtype=torch.int32).pin_memory(),
+                      "out": torch.empty_like(self.out, device="cpu").pin_memory()}
+        bi = sum(t.numel() * t.element_size() for t in self.h_in.values())
+        bo = sum(t.numel() * t.element_size() for t in self.h_out.values())
+        return bi, bo
+
+    def e2e_step(self):
+        x = self.x
+        for k, t in self.h_in.items():
+            x[k].copy_(t, non_blocking=True)
+        self.step()
+        self.h_out["score"].copy_(self.g_out["score"], non_blocking=True)
+        self.h_out["mask"].copy_(self.g_out["mask"], non_blocking=True)
+        self.h_out["counts"].copy_(self.c_out["counts"], non_blocking=True)
+        self.h_out["out"].copy_(self.out, non_blocking=True)
+
+    def n_exit(self):
+        return int(self.c_out["counts"][1].item())
+
+    def config(self):
+        c = self.cfg
+        return {"workload": c.name, "tokens_per_step": c.batch, "d": c.d, "fill_layers": len(c.fill_layers),
+                "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "cache_len": c.cache_len, "gate": "cosine",
+                "rule": c.rule, "tau": c.tau, "map": c.map, "weights": c.weights, "case": self.case,
+                "l2": "flushed between timed steps"}
+
+    # ---- the oracle on the host (reference arm and cpu_baseline)
+    def oracle_sample(self):
+        import oracle
+        from tests.parity import host
+        x = self.x
+        hp, hc = host(x["h_prev"]), host(x["h_cur"])
+        layers = host(x["layers"])
+        pos, cfg = x["pos"].cpu().numpy(), self.cfg
+
+        def run():
+            s, m, f = oracle.cosine_gate(hp, hc, cfg.tau, cfg.rule)
+            part = oracle.stable_partition(m)
+            oracle.gather_rows(hc, part["cont_rows"])
+            rows = part["exit_rows"]
+            for L in layers:
+                if len(rows):
+                    oracle.fill_rows(hc[rows], L, pos[rows], cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, cfg.eps,
+                                     cfg.group)
+            oracle.exit_scatter(np.zeros_like(hc), hc, rows, rows)
+            return cfg.batch
+        return run, "one full decode step (all tokens)"
+
+
+class Router:
+    """Router gate -> compaction with gather at one checkpoint."""
+
+    def __init__(self, tee, cfg, dev, seed=0, n=4096, theta=0.5):
+        self.tee, self.cfg, self.dev, self.n, self.theta = tee, cfg, dev, n, theta
+        k = cfg.checkpoints[0]
+        self.w = gen.router_weights(cfg, k, seed=seed, device=dev)
+        self.h = gen.router_hidden(cfg, n, k, seed=seed, device=dev)
+        self.ws = tee.Workspace(dev)
+        self.g_out = {"score": torch.empty(n, device=dev), "mask": torch.empty(n, dtype=torch.uint8, device=dev),
+                      "flag": torch.empty(1, dtype=torch.int32, device=dev)}
+        self.c_out = {k2: torch.empty(n, dtype=torch.int32, device=dev) for k2 in ("cont_rows", "exit_rows")}
+        self.c_out["counts"] = torch.empty(2, dtype=torch.int32, device=dev)
+        self.c_out["h_cont"] = torch.empty(n, cfg.d, dtype=self.h.dtype, device=dev)
+        self.units = n
+        self.kernel = "exit_gate(router)"
+        self.bound = "hbm"
+
+    def fill_bytes(self, n_exit):
+        d, b = self.cfg.d, self.cfg.bottleneck
+        return self.n * d * 2 + b * d * 2 + b * 2 + self.n * 5
+
+    def step(self, ev=None):
+        if ev is not None:
+            ev[0].record()
+        self.tee.exit_gate(self.h, self.theta, w_down=self.w["w_down"], w_up=self.w["w_up"], eps=self.cfg.eps,
+                           ws=self.ws, out=self.g_out)
+        if ev is not None:
+            ev[1].record()
+        self.tee.exit_compact(self.g_out["mask"], h=self.h, ws=self.ws, out=self.c_out, with_pos=False)
+
+    def host_io(self):
+        self.h_in = {"h": self.h.cpu().pin_memory()}
+        self.h_out = {"mask": torch.empty(self.n, dtype=torch.uint8).pin_memory(),
+                      "counts": torch.empty(2, dtype=torch.int32).pin_memory()}
+        return (sum(t.numel() * t.element_size() for t in self.h_in.values()),
+                sum(t.numel() * t.element_size() for t in self.h_out.values()))
+
+    def e2e_step(self):
+        self.h.copy_(self.h_in["h"], non_blocking=True)
+        self.step()
+        self.h_out["mask"].copy_(self.g_out["mask"], non_blocking=True)
+        self.h_out["counts"].copy_(self.c_out["counts"], non_blocking=True)
+
+    def n_exit(self):
+        return int(self.c_out["counts"][1].item())
+
+    def config(self):
+        c = self.cfg
+        return {"workload": f"{c.name}-n{self.n}", "tokens_per_step": self.n, "d": c.d, "bottleneck": c.bottleneck,
+                "theta": self.theta, "gate": "router", "rule": "per_token", "gather": True,
+                "l2": "flushed between timed steps"}
+
+    def oracle_sample(self):
+        import oracle
+        from tests.parity import host
+        m = 256
+        h, wd, wu = host(self.h[:m]), host(self.w["w_down"]), host(self.w["w_up"])
+
+        def run():
+            p, mask, _ = oracle.router_gate(h, wd, wu, self.theta, "per_token", eps=self.cfg.eps)
+            part = oracle.stable_partition(mask)
+            oracle.gather_rows(h, part["cont_rows"])
+            return m
+        return run, f"router gate + compaction with gather on the first {m} of {self.n} tokens"
+
+
+class Prefill:
+    """RidgeFill KV fill of every layer after the split, for all filled rows."""
+
+    def __init__(self, tee, cfg, dev, seed=0):
+        self.tee, self.cfg, self.dev = tee, cfg, dev
+        self.x = gen.prefill_inputs(cfg, seed=seed, device=dev)
+        self.ws = tee.Workspace(dev)
+        self.fill = tee.KVFill(self.x["layers"], d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
+                               rope_base=cfg.rope_base, eps=cfg.eps, dtype=torch.bfloat16, max_pos=cfg.tokens)
+        self.units = cfg.filled_rows
+        self.kernel = "kv_fill"
+        self.bound = "tensor"
+        d, kvw = cfg.d, cfg.kvw
+        self.flops = float(len(cfg.fill_layers)) * cfg.filled_rows * (2 * d * d + 4 * d * kvw)
+
+    def fill_bytes(self, n_exit):
+        return self.flops  # tensor-bound: FLOPs
+
+    def step(self, ev=None):
+        if ev is not None:
+            ev[0].record()
+        self.fill(self.x["h_split"], self.x["k_cache"], self.x["v_cache"], ws=self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    def host_io(self):
+        # inputs: the split-layer rows; output read back: the K/V of the last filled row of each layer
+        self.h_in = {"h_split": self.x["h_split"].cpu().pin_memory()}
+        kc = self.x["k_cache"]
+        self.h_out = {"k_last": torch.empty(kc.shape[0], kc.shape[2], kc.shape[4], dtype=kc.dtype).pin_memory()}
+        return (sum(t.numel() * t.element_size() for t in self.h_in.values()),
+                sum(t.numel() * t.element_size() for t in self.h_out.values()))
+
+    def e2e_step(self):
+        self.x["h_split"].copy_(self.h_in["h_split"], non_blocking=True)
+        self.step()
+        self.h_out["k_last"].copy_(self.x["k_cache"][:, 0, :, self.cfg.filled_rows - 1], non_blocking=True)
+
+    def n_exit(self):
+        return self.cfg.filled_rows
+
+    def config(self):
+        c = self.cfg
+        return {"workload": c.name, "tokens_per_step": c.filled_rows, "d": c.d, "fill_layers": len(c.fill_layers),
+                "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "prompt_tokens": c.tokens,
+                "exact_tail": c.exact_tail, "map": "ridge (N(0,1/d)+0.5I)", "weights": "bf16 dense",
+                "l2": "inputs larger than L2; flushed between timed steps"}
+
+    def oracle_sample(self):
+        import oracle
+        from tests.parity import host
+        rows = np.arange(16) * (self.cfg.filled_rows // 16)
+        h = host(self.x["h_split"][torch.as_tensor(rows, device=self.dev)])
+        layers = host(self.x["layers"])
+        cfg = self.cfg
+
+        def run():
+            for L in layers:
+                oracle.fill_rows(h, L, rows, cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, cfg.eps)
+            return len(rows)
+        return run, f"fill of 16 evenly spaced rows across all {len(layers)} layers (per-row time extrapolated)"
+
+
+def make(name, tee, dev, seed):
+    if name == "decode-1b":
+        return Decode(tee, configs.LLAMA1B_DECODE, dev, seed)
+    if name == "decode-tiny":
+        return Decode(tee, configs.TINY_DECODE, dev, seed)
+    if name == "router-4096":
+        return Router(tee, configs.ROUTER_4096, dev, seed)
+    if name == "prefill-16k":
+        return Prefill(tee, configs.PREFILL_16K, dev, seed)
+    if name == "prefill-120k":
+        return Prefill(tee, configs.PREFILL_120K, dev, seed)
+    raise SystemExit(f"unknown workload {name}")
+
+
+# --------------------------------------------------------------------------- helpers
+
+class Clocks:
+    """nvidia-smi samples (every 200 ms) taken during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.index}.csv")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ln in open(self.path):
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        mx = max(r[1] for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def time_oracle(run, budget_s):
+    """Repeat the oracle sample until ``budget_s`` of CPU time; units/s."""
+    run()  # warm
+    units, t0 = 0, time.perf_counter()
+    while True:
+        units += run()
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return units / el, el
+
+
+# --------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    # The oracle runs on the host; inputs come from the same seeded generator.
+    tee = None
+    if dev.type == "cuda":
+        import __graft_entry__
+        __graft_entry__.build()
+        import token_early_exit_gb300 as tee
+    w = make(args.workload, tee, dev, args.seed) if tee is not None else None
+    if w is None:
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm needs the seeded inputs on a GPU"}))
+        return 0
+    run, sample = w.oracle_sample()
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    units = 0
+    for _ in range(args.steps):
+        units += run()
+    el = time.perf_counter() - t0
+    v = units / el
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": w.config(),
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_gpu(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import token_early_exit_gb300 as tee
+    from token_early_exit_gb300 import _lib
+    lib = _lib.load()
+
+    w = make(args.workload, tee, dev, args.seed + rank)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        w.step()
+    torch.cuda.synchronize(dev)
+    n_exit = w.n_exit()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = Clocks(dev.index)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    l0 = lib.tee_launch_count()
+    for i in range(args.steps):
+        flush.zero_()                      # evict L2 (outside the timed events)
+        ev[i][0].record(stream)
+        w.step(kev[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = lib.tee_launch_count() - l0
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    t_step = statistics.mean(step_ms)
+    t_step = max_over_ranks(t_step, world, dev)
+    value = world * w.units / (t_step * 1e-3)
+
+    # end to end: pinned host inputs -> device -> step -> result back to the host, per step
+    bi, bo = w.host_io()
+    for _ in range(2):
+        w.e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        w.e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+
+    pk = peaks()
+    k_ms = statistics.mean(kern_ms)
+    work = w.fill_bytes(n_exit)
+    if w.bound == "hbm":
+        achieved = work / (k_ms * 1e-3) / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "kernel": w.kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None, "algorithmic_bytes": work, "kernel_ms": k_ms,
+                "peak_source": pk["source"]}
+    else:
+        achieved = work / (k_ms * 1e-3) / 1e12
+        peak = pk["bf16_tflops_sustained"] if k_ms > 50 else pk["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": w.kernel, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "algorithmic_flops": work, "kernel_ms": k_ms,
+                "peak_source": pk["source"]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        run, sample = w.oracle_sample()
+        v, el = time_oracle(run, args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+               "seconds": round(el, 2)}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.config().get("workload") != configs.TINY_DECODE.name else "f32",
+            "data": "synthetic", "config": w.config(), "exits_per_step": n_exit,
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": world * w.units / (t_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                    "d2h_bytes_per_step": bo, "ms_per_step": t_e2e},
+            "gpu_launches": int(launches), "clocks": clk,
+            "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)}}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("tee", "reference"), default="tee")
+    ap.add_argument("--workload", choices=WORKLOADS, default="decode-1b")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

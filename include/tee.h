@@ -1,0 +1,284 @@
+/*
+ * tee.h - token early exit on one GPU: exit gate, compaction, exit scatter and
+ * KV fill, as a plain C ABI (libtee.so, built for sm_103a).
+ *
+ * The four operations follow three write-ups of token-level early exit in
+ * decoder-only LLM inference:
+ *   - "River-LLM: Large Language Model Seamless Exit Based on KV Share"
+ *     (state-transition cosine gate, batch-min rule, KV-shared exit layers
+ *     with W4A16 weights that write the skipped layers' cache slots);
+ *   - "TIDE: Token-Informed Depth Execution for Per-Token Early Exit in LLM
+ *     Inference" (RMSNorm -> router MLP -> sigmoid gate, batch compaction
+ *     by warp ballot / prefix sum, exit scatter, exit projection);
+ *   - "RidgeFill: training-free later-layer cache fill" (per-layer linear map
+ *     from the split state to each later layer's input; that layer's own
+ *     norm and K/V projection write the cache).
+ *
+ * Conventions shared by every call
+ *   Ownership: the caller allocates every buffer (device memory unless stated)
+ *     and keeps it alive until the work on `stream` has finished. The library
+ *     allocates no device memory inside a call.
+ *   Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *     default stream). All calls are asynchronous: a call only enqueues
+ *     kernels on `stream`, and no call synchronises the host except
+ *     tee_get_device_error. Counts stay on the device, so gate -> compact ->
+ *     fill -> scatter needs no host round trip.
+ *   Layouts: matrices are row-major with a leading dimension `ld` in
+ *     elements; device pointers of activations and weights must be 16-byte
+ *     aligned and `ld * element size` a multiple of 16 bytes (the kernels use
+ *     128-bit loads), and `d` a multiple of 8.
+ *   Workspace: each call takes a device scratch buffer `ws` of at least the
+ *     size its *_workspace_size query returns. It begins with a 256-byte
+ *     header holding a sticky device error word. The caller zero-fills a new
+ *     workspace once (tee_workspace_init); every call leaves it reusable.
+ *     Calls that share one workspace must not overlap on the GPU.
+ *   Errors: every call returns a tee_status. Host-side checks (null required
+ *     pointer, bad size, misalignment, unsupported format) return before any
+ *     launch. Faults that only the device can see (a row, position, sequence
+ *     or destination index out of range) skip the offending write and record
+ *     the first such fault in the workspace header; tee_get_device_error
+ *     reads it. No kernel traps, and no kernel waits without an iteration
+ *     limit.
+ */
+#ifndef TEE_H
+#define TEE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TEE_API __attribute__((visibility("default")))
+#else
+#define TEE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TEE_OK = 0,
+    TEE_ERR_INVALID_ARG = 1,   /* null required pointer, bad size, misaligned pointer or ld, NaN threshold */
+    TEE_ERR_UNSUPPORTED = 2,   /* dtype / format combination not built */
+    TEE_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed; see tee_last_cuda_error */
+    TEE_ERR_WORKSPACE = 4,     /* ws (or prep) missing or smaller than its size query */
+    TEE_ERR_DEVICE = 5         /* returned by tee_get_device_error when a device fault was recorded */
+} tee_status;
+
+/* Element types. */
+enum { TEE_F32 = 0, TEE_F16 = 1, TEE_BF16 = 2 };
+/* Gate kinds and exit rules. */
+enum { TEE_GATE_COSINE = 0, TEE_GATE_ROUTER = 1 };
+enum { TEE_RULE_PER_TOKEN = 0, TEE_RULE_BATCH_ALL = 1 };
+/* Weight formats of the fill's K/V projection. */
+enum { TEE_W_DENSE = 0, TEE_W_INT4 = 1 };
+/* Device fault codes recorded in the workspace header. */
+enum {
+    TEE_DEVERR_NONE = 0,
+    TEE_DEVERR_ROW = 1,        /* a row index outside the source rows */
+    TEE_DEVERR_POS = 2,        /* a cache position outside [0, max_pos) */
+    TEE_DEVERR_SEQ = 3,        /* a cache sequence outside [0, n_seq) */
+    TEE_DEVERR_COUNT = 4,      /* a device-side count larger than its host-side bound */
+    TEE_DEVERR_DEST = 5        /* a scatter destination outside [0, n_out) */
+};
+
+#define TEE_WS_HEADER_BYTES 256
+
+/* ------------------------------------------------------------------ misc */
+
+TEE_API const char* tee_version(void);
+TEE_API const char* tee_status_string(tee_status s);
+/* The cudaError_t (as int) behind the last TEE_ERR_CUDA of this thread. */
+TEE_API int tee_last_cuda_error(void);
+/* Zero-fill `bytes` of a workspace on `stream` (needed once per new workspace). */
+TEE_API tee_status tee_workspace_init(void* ws, size_t bytes, void* stream);
+/* Synchronise `stream`, then report the first device fault recorded in `ws`:
+ * *code gets a TEE_DEVERR_* value, *detail the offending index (either may be
+ * NULL). Returns TEE_ERR_DEVICE if a fault was recorded, else TEE_OK. */
+TEE_API tee_status tee_get_device_error(const void* ws, int32_t* code, int32_t* detail, void* stream);
+/* Clear the device fault word of `ws` on `stream`. */
+TEE_API tee_status tee_clear_device_error(void* ws, void* stream);
+/* Number of kernels this library has launched in this process (all threads). */
+TEE_API uint64_t tee_launch_count(void);
+
+/* ------------------------------------------------------------- exit gate */
+
+typedef struct {
+    int32_t mode;        /* TEE_GATE_COSINE or TEE_GATE_ROUTER */
+    int32_t rule;        /* TEE_RULE_PER_TOKEN or TEE_RULE_BATCH_ALL */
+    int32_t dtype;       /* element type of h_cur, h_prev, gamma, w_down, w_up */
+    int32_t d;           /* hidden size */
+    int32_t bottleneck;  /* router width b (128 in TIDE); ignored by the cosine gate */
+    float threshold;     /* tau (cosine) or theta (router); exit iff score > threshold */
+    float eps;           /* RMSNorm epsilon of the router */
+} tee_gate_desc;
+
+TEE_API size_t tee_exit_gate_workspace_size(const tee_gate_desc* desc, int32_t n);
+
+/*
+ * Exit gate for n tokens (one row each).
+ *
+ * Cosine (River-LLM, background "state transition similarity" and method
+ * step 3): score[t] = <h_prev[t], h_cur[t]> / (|h_prev[t]| |h_cur[t]|), the
+ * similarity of one decoder block's input and output; a zero row scores 0.
+ * Router (TIDE, formula 3 and module 4 "Fused LayerNorm + Route"):
+ * score[t] = sigmoid(w_up . SiLU(w_down . (g * h_cur[t] / rms(h_cur[t])) +
+ * b_down) + b_up), rms(x) = sqrt(mean(x^2) + eps).
+ *
+ * Rule TEE_RULE_PER_TOKEN: mask[t] = score[t] > threshold. Rule
+ * TEE_RULE_BATCH_ALL (River-LLM's min over the batch > tau; TIDE module 3's
+ * "for all tokens in the batch"): every mask[t] = (min_t score[t] > threshold).
+ * batch_flag (nullable) gets that all-tokens flag under either rule; it is 0
+ * for n = 0. Scores accumulate in fp32 and the comparison is taken in fp32.
+ *
+ *   h_cur   [n][ld_cur]  dtype                    (the block output / router input)
+ *   h_prev  [n][ld_prev] dtype                    (cosine only, else NULL)
+ *   gamma   [d] dtype, nullable (= 1)             (router only)
+ *   w_down  [bottleneck][d] dtype                 (router only)
+ *   b_down  [bottleneck] f32, nullable (= 0)      (router only)
+ *   w_up    [bottleneck] dtype                    (router only)
+ *   b_up    [1] f32, nullable (= 0)               (router only)
+ *   score   [n] f32 out;  mask [n] u8 out (1 = exit);  batch_flag [1] i32 out
+ */
+TEE_API tee_status tee_exit_gate(const tee_gate_desc* desc, int32_t n,
+                         const void* h_cur, int64_t ld_cur,
+                         const void* h_prev, int64_t ld_prev,
+                         const void* gamma, const void* w_down, const float* b_down,
+                         const void* w_up, const float* b_up,
+                         float* score, uint8_t* mask, int32_t* batch_flag,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* -------------------------------------------------------- exit compaction */
+
+TEE_API size_t tee_exit_compact_workspace_size(int32_t n);
+
+/*
+ * Stable split of n tokens into continuing (mask 0) and exiting (mask != 0)
+ * ones (TIDE module 4 "Batch Compact": warp ballot for small batches, a
+ * prefix-sum scatter for large ones).
+ *
+ *   mask      [n] u8 in
+ *   pos_in    [n] i32 in, nullable (= row index): original slot of each row
+ *   cont_rows [n] i32 out: the first counts[0] entries are the continuing
+ *             rows in increasing order; exit_rows likewise for the exiting
+ *             rows (first counts[1] entries). Entries past the count are not
+ *             written.
+ *   cont_pos, exit_pos [n] i32 out, nullable: pos_in of those rows
+ *   counts    [2] i32 out (device): {n_cont, n_exit}
+ *   h_in      [n][ld_in] dtype, nullable: when given, the continuing rows are
+ *             gathered into h_cont [n_cont][ld_cont] (the compacted buffer the
+ *             next layer runs on).
+ */
+TEE_API tee_status tee_exit_compact(int32_t n, const uint8_t* mask, const int32_t* pos_in,
+                            const void* h_in, int64_t ld_in, int32_t d, int32_t dtype,
+                            int32_t* cont_rows, int32_t* exit_rows,
+                            int32_t* cont_pos, int32_t* exit_pos,
+                            void* h_cont, int64_t ld_cont, int32_t* counts,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ exit scatter */
+
+TEE_API size_t tee_exit_scatter_workspace_size(int32_t n_max);
+
+/*
+ * Exit scatter (TIDE module 4): for i < counts[1],
+ * out[exit_pos[i]] = h_src[exit_rows[i]]; with final_gamma (the "Exit
+ * Projection" kernel, RMSNorm fused with the scatter) the row is written as
+ * h / sqrt(mean(h^2) + eps) * final_gamma instead. Other rows of `out` are
+ * left as they are.
+ *
+ *   n_max     host bound on counts[1] and on the rows of h_src
+ *   counts    [2] i32 device; counts[1] = number of exiting rows
+ *   exit_rows, exit_pos [n_max] i32; h_src [n_max][ld_src]; out [n_out][ld_out]
+ *   final_gamma [d] dtype, nullable
+ * A destination outside [0, n_out) or a source row outside [0, n_max) is
+ * skipped and recorded (TEE_DEVERR_DEST / TEE_DEVERR_ROW).
+ */
+TEE_API tee_status tee_exit_scatter(int32_t n_max, const int32_t* counts,
+                            const int32_t* exit_rows, const int32_t* exit_pos,
+                            const void* h_src, int64_t ld_src,
+                            void* out, int64_t ld_out, int64_t n_out,
+                            int32_t d, int32_t dtype, const void* final_gamma, float eps,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------- KV fill */
+
+typedef struct {
+    int32_t d;            /* hidden size */
+    int32_t n_kv_heads;   /* KV heads written per layer */
+    int32_t head_dim;     /* width of one head (even) */
+    float rope_base;      /* RoPE base */
+    float eps;            /* epsilon of each filled layer's RMSNorm */
+    int32_t dtype;        /* h_split, w_map, gamma, dense wk/wv and the caches */
+    int32_t wfmt;         /* TEE_W_DENSE or TEE_W_INT4 for wk/wv */
+    int32_t group;        /* int4 group length along d (multiple of 16) */
+} tee_fill_desc;
+
+/* Weights of one filled layer j (device pointers). kvw = n_kv_heads*head_dim. */
+typedef struct {
+    const void* w_map;    /* [d][d] dtype: x_j = h_split . w_map; NULL = identity (state propagation) */
+    const void* gamma;    /* [d] dtype: layer j's RMSNorm weight */
+    const void* wk;       /* dense [d][kvw] dtype, or int4 [d/2][kvw] u8 (even k in the low nibble) */
+    const void* wv;       /* same as wk */
+    const void* k_scale;  /* int4 only: [d/group][kvw] f16; W = (q - zero) * scale */
+    const void* k_zero;   /* int4 only: [d/group][kvw] f16 */
+    const void* v_scale;
+    const void* v_zero;
+    int32_t cache_layer;  /* layer index into the caches */
+    int32_t reserved;
+} tee_fill_layer;
+
+/* Cache geometry, shared by k_cache and v_cache. Strides are in elements;
+ * head_dim is contiguous. Slot (layer, seq, head, pos) starts at
+ * layer*s_layer + seq*s_seq + head*s_head + pos*s_pos and holds head_dim
+ * elements. n_heads must be at least the descriptor's n_kv_heads. */
+typedef struct {
+    int64_t s_layer, s_seq, s_head, s_pos;
+    int32_t n_layers, n_seq, n_heads, max_pos;
+} tee_cache_layout;
+
+/* Size of the prepared-state buffer `prep` (RoPE table and repacked weights). */
+TEE_API size_t tee_kv_fill_prep_size(const tee_fill_desc* desc, int32_t n_layers, int32_t max_pos);
+/* Fill `prep` for these layers and positions [0, max_pos). Run once, and again
+ * whenever the weights behind `layers` change; tee_kv_fill reads it. */
+TEE_API tee_status tee_kv_fill_prepare(const tee_fill_desc* desc, int32_t n_layers, const tee_fill_layer* layers,
+                               int32_t max_pos, void* prep, size_t prep_bytes, void* stream);
+
+TEE_API size_t tee_kv_fill_workspace_size(const tee_fill_desc* desc, int32_t n_layers, int32_t n_max);
+
+/*
+ * KV fill for the layers an exiting token skips.
+ *
+ * RidgeFill: x_j = h_split . W_j, the split-layer state mapped to filled
+ * layer j's input by a per-layer ridge map (identity = River-LLM's State
+ * Propagation); then layer j's own RMSNorm x^ = x_j / rms(x_j) * gamma_j and
+ * projections k = x^ . Wk_j, v = x^ . Wv_j (dense, or River-LLM's W4A16 int4
+ * weights); RoPE (rotate-half pairs i, i + head_dim/2, angle
+ * pos * rope_base^(-2i/head_dim)) on each K head; K and V stored in the slot
+ * the backbone would have written (River-LLM method step 1: identical
+ * position index, head split and dimension layout).
+ *
+ * Items: n = *n_dev if n_dev is given (a device count, e.g. counts + 1 of
+ * tee_exit_compact), else n_max; n must not exceed n_max. Item i uses
+ *   row r = rows ? rows[i] : i            of h_split (r < h_rows),
+ *   position p = pos ? pos[r] : pos0 + r  (0 <= p < cache->max_pos),
+ *   sequence s = seq ? seq[r] : 0         (0 <= s < cache->n_seq),
+ * and writes every kv head of every listed layer.
+ *
+ *   layers     host array of n_layers descriptors (device weight pointers)
+ *   prep       prepared by tee_kv_fill_prepare for the same desc and layers
+ *   h_split    [h_rows][ld_h] dtype
+ *   k_cache, v_cache  caches of `dtype` laid out as `cache` says
+ */
+TEE_API tee_status tee_kv_fill(const tee_fill_desc* desc, int32_t n_layers, const tee_fill_layer* layers,
+                       const void* prep, size_t prep_bytes,
+                       int32_t n_max, const int32_t* n_dev,
+                       const void* h_split, int64_t ld_h, int32_t h_rows,
+                       const int32_t* rows, const int32_t* pos, int32_t pos0, const int32_t* seq,
+                       void* k_cache, void* v_cache, const tee_cache_layout* cache,
+                       void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TEE_H */

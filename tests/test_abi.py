@@ -1,0 +1,110 @@
+"""The C ABI library loads and exports every symbol include/tee.h declares,
+and host-side argument checks answer before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from token_early_exit_gb300 import build
+    build.build()
+    from token_early_exit_gb300 import _lib
+    return _lib.load()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^TEE_API\s+[\w\s\*]+?\b(tee_\w+)\s*\(", text, re.M))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from token_early_exit_gb300 import _lib
+    names = declared_symbols()
+    assert len(names) >= 16
+    for name in names:
+        assert hasattr(lib, name), name
+    # the binding declares a signature for each of them, and for nothing else
+    assert names == set(_lib.SIGNATURES)
+
+
+def test_only_the_abi_is_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    syms = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert syms == declared_symbols()
+
+
+def test_version_and_status_strings(lib):
+    assert b"sm_103a" in lib.tee_version()
+    assert lib.tee_status_string(0) == b"ok"
+    assert lib.tee_status_string(4) == b"workspace too small"
+
+
+def test_host_side_checks_need_no_gpu(lib):
+    from token_early_exit_gb300 import _lib
+    g = _lib.GateDesc(mode=0, rule=0, dtype=_lib.TEE_BF16, d=2048, bottleneck=0, threshold=0.97, eps=1e-5)
+    assert lib.tee_exit_gate_workspace_size(ctypes.byref(g), 64) >= _lib.WS_HEADER_BYTES
+    fake = ctypes.c_void_p(16)  # never dereferenced: every call below fails its checks first
+    # null descriptor
+    assert lib.tee_exit_gate(None, 4, fake, 2048, fake, 2048, None, None, None, None, None, fake, fake, None,
+                             fake, 1 << 20, None) == _lib.TEE_ERR_INVALID_ARG
+    # workspace too small
+    assert lib.tee_exit_gate(ctypes.byref(g), 4, fake, 2048, fake, 2048, None, None, None, None, None, fake,
+                             fake, None, fake, 8, None) == _lib.TEE_ERR_WORKSPACE
+    # d not a multiple of 8
+    g.d = 2047
+    assert lib.tee_exit_gate(ctypes.byref(g), 4, fake, 2048, fake, 2048, None, None, None, None, None, fake,
+                             fake, None, fake, 1 << 20, None) == _lib.TEE_ERR_INVALID_ARG
+    # NaN threshold
+    g.d, g.threshold = 2048, float("nan")
+    assert lib.tee_exit_gate(ctypes.byref(g), 4, fake, 2048, fake, 2048, None, None, None, None, None, fake,
+                             fake, None, fake, 1 << 20, None) == _lib.TEE_ERR_INVALID_ARG
+    # misaligned row pitch (ld * 2 bytes not a multiple of 16)
+    g.threshold = 0.97
+    assert lib.tee_exit_gate(ctypes.byref(g), 4, fake, 2049, fake, 2048, None, None, None, None, None, fake,
+                             fake, None, fake, 1 << 20, None) == _lib.TEE_ERR_INVALID_ARG
+    # unsupported dtype
+    g.dtype = 7
+    assert lib.tee_exit_gate(ctypes.byref(g), 4, fake, 2048, fake, 2048, None, None, None, None, None, fake,
+                             fake, None, fake, 1 << 20, None) == _lib.TEE_ERR_UNSUPPORTED
+    # compaction: null mask / negative n / small workspace
+    assert lib.tee_exit_compact(-1, fake, None, None, 0, 0, 0, fake, fake, None, None, None, 0, fake, fake,
+                                1 << 20, None) == _lib.TEE_ERR_INVALID_ARG
+    assert lib.tee_exit_compact(8, None, None, None, 0, 0, 0, fake, fake, None, None, None, 0, fake, fake,
+                                1 << 20, None) == _lib.TEE_ERR_INVALID_ARG
+    assert lib.tee_exit_compact(8, fake, None, None, 0, 0, 0, fake, fake, None, None, None, 0, fake, fake,
+                                16, None) == _lib.TEE_ERR_WORKSPACE
+    # scatter with d not a multiple of 8
+    assert lib.tee_exit_scatter(4, fake, fake, fake, fake, 12, fake, 12, 4, 12, _lib.TEE_BF16, None, 1e-5, fake,
+                                1 << 20, None) == _lib.TEE_ERR_INVALID_ARG
+
+
+def test_fill_descriptor_checks(lib):
+    from token_early_exit_gb300 import _lib
+    D = _lib.FillDesc(d=4096, n_kv_heads=8, head_dim=128, rope_base=5e5, eps=1e-5, dtype=_lib.TEE_BF16,
+                      wfmt=_lib.TEE_W_DENSE, group=64)
+    assert lib.tee_kv_fill_prep_size(ctypes.byref(D), 16, 16384) > 16384 * 64 * 8
+    assert lib.tee_kv_fill_workspace_size(ctypes.byref(D), 16, 14336) > 0
+    D.head_dim = 7  # odd head_dim: no rotate-half pairing
+    assert lib.tee_kv_fill_prep_size(ctypes.byref(D), 16, 16384) == 0
+    D.head_dim, D.wfmt, D.group = 128, _lib.TEE_W_INT4, 48  # group must divide d and be a multiple of 16
+    assert lib.tee_kv_fill_prep_size(ctypes.byref(D), 16, 16384) == 0
+    D.group = 64
+    fake = ctypes.c_void_p(16)
+    layout = _lib.CacheLayout(8 * 16 * 128, 8 * 16 * 128, 16 * 128, 128, 1, 1, 8, 16)
+    arr = (_lib.FillLayer * 1)()
+    # workspace too small
+    assert lib.tee_kv_fill(ctypes.byref(D), 1, arr, fake, 1 << 30, 4, None, fake, 4096, 4, None, None, 0, None,
+                           fake, fake, ctypes.byref(layout), fake, 8, None) == _lib.TEE_ERR_WORKSPACE
+    # a layer without weights
+    assert lib.tee_kv_fill(ctypes.byref(D), 1, arr, fake, 1 << 30, 4, None, fake, 4096, 4, None, None, 0, None,
+                           fake, fake, ctypes.byref(layout), fake, 1 << 40, None) == _lib.TEE_ERR_INVALID_ARG

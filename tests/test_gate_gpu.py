@@ -1,0 +1,125 @@
+"""Exit gate on the GPU (through the C ABI) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity import check_mask, check_scores, f64
+from workloads import configs, gen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tee():
+    import __graft_entry__
+    __graft_entry__.build()
+    import token_early_exit_gb300 as t
+    return t
+
+
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_cosine_tiny_fp32_per_token(tee, seed):
+    cfg = configs.TINY_DECODE
+    x = gen.decode_inputs(cfg, seed=seed, device=DEV, with_cache=False)
+    score, mask, flag = tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule="per_token")
+    s_ref, m_ref, f_ref = oracle.cosine_gate(f64(x["h_prev"]), f64(x["h_cur"]), cfg.tau, "per_token")
+    check_scores(score, s_ref)
+    check_mask(mask, s_ref, cfg.tau)
+    if np.all(np.abs(s_ref - cfg.tau) > 1e-3):
+        assert int(flag.item()) == f_ref
+
+
+@pytest.mark.parametrize("case,want", [("exit", 1), ("stay", 0)])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_cosine_bf16_batch_min(tee, case, want, seed):
+    cfg = configs.LLAMA1B_DECODE
+    x = gen.decode_inputs(cfg, seed=seed, device=DEV, case=case, with_cache=False)
+    score, mask, flag = tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule="batch_all")
+    s_ref, m_ref, f_ref = oracle.cosine_gate(f64(x["h_prev"]), f64(x["h_cur"]), cfg.tau, "batch_all")
+    check_scores(score, s_ref)
+    assert f_ref == want and int(flag.item()) == want
+    assert np.array_equal(mask.cpu().numpy(), m_ref)
+
+
+@pytest.mark.parametrize("n", [1, 7, 31, 32, 33, 255, 4095, 4096, 4097, 9000])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+def test_cosine_sizes_and_dtypes(tee, n, dtype):
+    cfg = configs.DecodeConfig(**{**configs.TINY_DECODE.__dict__, "batch": n, "d": 264})
+    x = gen.decode_inputs(cfg, seed=n, device=DEV, with_cache=False)
+    hp, hc = x["h_prev"].to(dtype), x["h_cur"].to(dtype)
+    for rule in ("per_token", "batch_all"):
+        score, mask, flag = tee.exit_gate(hc, 0.9, h_prev=hp, rule=rule)
+        s_ref, m_ref, f_ref = oracle.cosine_gate(f64(hp), f64(hc), 0.9, rule)
+        check_scores(score, s_ref)
+        if rule == "per_token":
+            check_mask(mask, s_ref, 0.9)
+        elif np.abs(s_ref.min() - 0.9) > 1e-3:
+            assert int(flag.item()) == f_ref and np.array_equal(mask.cpu().numpy(), m_ref)
+
+
+def test_cosine_strided_rows_and_zero_rows(tee):
+    base = torch.randn(40, 512, device=DEV, dtype=torch.bfloat16)
+    hp, hc = base[:, :256], base[:, 256:]           # ld = 512
+    hp[3].zero_()
+    score, mask, flag = tee.exit_gate(hc, -0.5, h_prev=hp)
+    s_ref, _, _ = oracle.cosine_gate(f64(hp), f64(hc), -0.5)
+    check_scores(score, s_ref)
+    assert float(score[3]) == 0.0 and int(mask[3]) == 1   # 0 > -0.5
+
+
+def test_gate_empty_batch(tee):
+    h = torch.empty(0, 256, device=DEV)
+    score, mask, flag = tee.exit_gate(h, 0.5, h_prev=h, rule="batch_all")
+    assert int(flag.item()) == 0 and score.numel() == 0
+
+
+def _router_ref(h, w, theta, rule, **kw):
+    return oracle.router_gate(f64(h), f64(w["w_down"]), f64(w["w_up"]), theta, rule,
+                              **{k: (f64(v) if torch.is_tensor(v) else v) for k, v in kw.items()})
+
+
+@pytest.mark.parametrize("n", [32, 4096])
+@pytest.mark.parametrize("theta", configs.ROUTER_4096.thetas)
+def test_router_workload(tee, n, theta):
+    cfg = configs.ROUTER_4096
+    k = cfg.checkpoints[n % len(cfg.checkpoints)]
+    w = gen.router_weights(cfg, k, seed=0, device=DEV)
+    h = gen.router_hidden(cfg, n, k, seed=0, device=DEV)
+    score, mask, flag = tee.exit_gate(h, theta, w_down=w["w_down"], w_up=w["w_up"], eps=cfg.eps)
+    p_ref, m_ref, _ = _router_ref(h, w, theta, "per_token", eps=cfg.eps)
+    check_scores(score, p_ref)
+    excluded = check_mask(mask, p_ref, theta)
+    assert excluded <= max(2, n // 20)
+
+
+@pytest.mark.parametrize("n", [1, 5, 33, 300])
+def test_router_biases_gamma_and_batch_rule(tee, n):
+    cfg = configs.ROUTER_4096
+    d = 1024
+    torch.manual_seed(n)
+    h = torch.randn(n, d, device=DEV, dtype=torch.bfloat16)
+    w = {"w_down": (0.02 * torch.randn(128, d, device=DEV)).bfloat16(),
+         "w_up": (0.02 * torch.randn(128, device=DEV)).bfloat16()}
+    gamma = (1 + 0.1 * torch.randn(d, device=DEV)).bfloat16()
+    b_down = 0.1 * torch.randn(128, device=DEV)
+    b_up = torch.tensor([2.0], device=DEV)  # p well above 0.5 for every token
+    for rule in ("per_token", "batch_all"):
+        score, mask, flag = tee.exit_gate(h, 0.6, w_down=w["w_down"], w_up=w["w_up"], gamma=gamma, b_down=b_down,
+                                          b_up=b_up, rule=rule, eps=cfg.eps)
+        p_ref, m_ref, f_ref = _router_ref(h, w, 0.6, rule, gamma=gamma, b_down=b_down, b_up=b_up, eps=cfg.eps)
+        check_scores(score, p_ref)
+        assert int(flag.item()) == f_ref == 1
+        assert np.array_equal(mask.cpu().numpy(), m_ref)
+
+
+def test_router_zero_weights_give_sigmoid_bias(tee):
+    n, d = 64, 512
+    h = torch.randn(n, d, device=DEV, dtype=torch.bfloat16)
+    z = torch.zeros(128, d, device=DEV, dtype=torch.bfloat16)
+    score, _, _ = tee.exit_gate(h, 0.5, w_down=z, w_up=torch.zeros(128, device=DEV, dtype=torch.bfloat16),
+                                b_up=torch.tensor([np.log(3.0)], device=DEV, dtype=torch.float32))
+    assert torch.allclose(score, torch.full_like(score, 0.75), atol=1e-6)

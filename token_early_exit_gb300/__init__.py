@@ -1,0 +1,10 @@
+"""Token-level early exit on one GB300: exit gate, compaction, exit scatter and
+KV fill, as hand-written CUDA for sm_103a behind the C ABI in include/tee.h.
+
+The Python side only marshals arguments; see ``ops``.
+"""
+from . import _lib  # noqa: F401
+from .ops import (KVFill, Workspace, cache_layout, exit_compact, exit_gate, exit_scatter,  # noqa: F401
+                  kv_fill)
+
+__all__ = ["exit_gate", "exit_compact", "exit_scatter", "kv_fill", "KVFill", "Workspace", "cache_layout"]

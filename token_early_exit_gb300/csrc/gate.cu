@@ -1,0 +1,299 @@
+// Exit gate: River-LLM's state-transition cosine and TIDE's RMSNorm router.
+//
+// Cosine (River-LLM, background "state transition similarity"; method step 3):
+// one warp per token streams h_prev and h_cur with 128-bit loads, accumulates
+// <a,b>, |a|^2 and |b|^2 in fp32 and reduces them with __shfl_xor_sync.
+//
+// Router (TIDE formula 3; module 4 "Fused LayerNorm + Route"): the d -> b
+// contraction is split over (token tile, channel group) blocks that stage the
+// token rows in shared memory as fp32; a finalize kernel then applies the
+// per-token 1/rms, b_down, SiLU, the b -> 1 projection and the sigmoid. Large
+// batches take the tensor-core path in router_tc.cu instead.
+//
+// Both end in the same decision, score > threshold in fp32, and the same
+// "last block" reduction of the all-tokens flag (River-LLM's min over the
+// batch; TIDE module 3's "for every token in the batch").
+#include "common.cuh"
+
+namespace tee {
+
+namespace {
+
+constexpr int GATE_WARPS = 8;
+constexpr int GATE_MAX_BLOCKS = 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(GATE_WARPS * 32)
+cosine_gate_kernel(int n, int d, const T* __restrict__ hc, int64_t ldc, const T* __restrict__ hp,
+                   int64_t ldp, float thr, int rule, bool need_flag, float* __restrict__ score,
+                   uint8_t* __restrict__ mask, int32_t* __restrict__ flag, void* ws) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float wmin = INFINITY;
+    for (int t = blockIdx.x * GATE_WARPS + warp; t < n; t += gridDim.x * GATE_WARPS) {
+        const T* a = hp + static_cast<int64_t>(t) * ldp;
+        const T* b = hc + static_cast<int64_t>(t) * ldc;
+        float dot = 0.f, na = 0.f, nb = 0.f;
+        for (int i = lane * 8; i < d; i += 256) {
+            float x[8], y[8];
+            load8(a + i, x);
+            load8(b + i, y);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                dot = fmaf(x[k], y[k], dot);
+                na = fmaf(x[k], x[k], na);
+                nb = fmaf(y[k], y[k], nb);
+            }
+        }
+        dot = warp_sum(dot);
+        na = warp_sum(na);
+        nb = warp_sum(nb);
+        const float den = sqrtf(na) * sqrtf(nb);
+        const float s = den > 0.f ? dot / den : 0.f;
+        if (lane == 0) {
+            score[t] = s;
+            if (rule == TEE_RULE_PER_TOKEN) mask[t] = exits(s, thr);
+        }
+        wmin = fminf(wmin, s == s ? s : -INFINITY);
+    }
+    if (!need_flag) return;
+    __shared__ float s_min[GATE_WARPS];
+    if (lane == 0) s_min[warp] = wmin;
+    __syncthreads();
+    float bmin = INFINITY;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < GATE_WARPS; ++w) bmin = fminf(bmin, s_min[w]);
+    batch_flag_tail(bmin, n, thr, rule, mask, flag, ws_at<float>(ws, TEE_WS_HEADER_BYTES),
+                    ws_counter(ws, WS_CNT_GATE));
+}
+
+// ---------------------------------------------------------------- router
+constexpr int RT_TOK = 4;        // tokens per block
+constexpr int RT_CH_WARP = 1;    // channels per warp
+constexpr int RT_WARPS = 8;
+
+// dots[t][c] = sum_i w_down[c][i] * gamma[i] * h[t][i]; sumsq[t] = sum_i h[t][i]^2.
+template <typename T>
+__global__ void __launch_bounds__(RT_WARPS * 32)
+router_dot_kernel(int n, int d, int b, const T* __restrict__ h, int64_t ldh, const T* __restrict__ gamma,
+                  const T* __restrict__ wd, float* __restrict__ dots, float* __restrict__ sumsq) {
+    extern __shared__ float s_h[];  // [RT_TOK][d], gamma applied
+    const int t0 = blockIdx.x * RT_TOK;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Stage the token rows; the blocks of channel group 0 also report sumsq.
+    float ss[RT_TOK];
+#pragma unroll
+    for (int tt = 0; tt < RT_TOK; ++tt) {
+        const int t = t0 + tt;
+        ss[tt] = 0.f;
+        for (int i = threadIdx.x * 8; i < d; i += blockDim.x * 8) {
+            float x[8], g[8];
+            if (t < n) {
+                load8(h + static_cast<int64_t>(t) * ldh + i, x);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x[k] = 0.f;
+            }
+            if (gamma) {
+                load8(gamma + i, g);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) g[k] = 1.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                ss[tt] = fmaf(x[k], x[k], ss[tt]);
+                s_h[tt * d + i + k] = x[k] * g[k];
+            }
+        }
+    }
+    __shared__ float s_red[RT_TOK][RT_WARPS];
+    if (blockIdx.y == 0) {
+#pragma unroll
+        for (int tt = 0; tt < RT_TOK; ++tt) {
+            const float v = warp_sum(ss[tt]);
+            if (lane == 0) s_red[tt][warp] = v;
+        }
+    }
+    __syncthreads();
+    if (blockIdx.y == 0 && threadIdx.x < RT_TOK && t0 + threadIdx.x < n) {
+        float tot = 0.f;
+        for (int w = 0; w < RT_WARPS; ++w) tot += s_red[threadIdx.x][w];
+        sumsq[t0 + threadIdx.x] = tot;
+    }
+    for (int cc = 0; cc < RT_CH_WARP; ++cc) {
+        const int c = (blockIdx.y * RT_WARPS + warp) * RT_CH_WARP + cc;
+        if (c >= b) break;
+        float acc[RT_TOK];
+#pragma unroll
+        for (int tt = 0; tt < RT_TOK; ++tt) acc[tt] = 0.f;
+        const T* wrow = wd + static_cast<int64_t>(c) * d;
+        for (int i = lane * 8; i < d; i += 256) {
+            float w[8];
+            load8(wrow + i, w);
+#pragma unroll
+            for (int tt = 0; tt < RT_TOK; ++tt) {
+                const float4 x0 = *reinterpret_cast<const float4*>(s_h + tt * d + i);
+                const float4 x1 = *reinterpret_cast<const float4*>(s_h + tt * d + i + 4);
+                acc[tt] = fmaf(w[0], x0.x, acc[tt]);
+                acc[tt] = fmaf(w[1], x0.y, acc[tt]);
+                acc[tt] = fmaf(w[2], x0.z, acc[tt]);
+                acc[tt] = fmaf(w[3], x0.w, acc[tt]);
+                acc[tt] = fmaf(w[4], x1.x, acc[tt]);
+                acc[tt] = fmaf(w[5], x1.y, acc[tt]);
+                acc[tt] = fmaf(w[6], x1.z, acc[tt]);
+                acc[tt] = fmaf(w[7], x1.w, acc[tt]);
+            }
+        }
+#pragma unroll
+        for (int tt = 0; tt < RT_TOK; ++tt) {
+            const float v = warp_sum(acc[tt]);
+            if (lane == 0 && t0 + tt < n) dots[static_cast<int64_t>(t0 + tt) * b + c] = v;
+        }
+    }
+}
+
+}  // namespace
+
+// p[t] = sigmoid(sum_c w_up[c] * SiLU(dots[t][c] / rms_t + b_down[c]) + b_up),
+// rms_t = sqrt(sumsq[t] / d + eps): one warp per token. Shared with the
+// tensor-core path, which produces the same dots/sumsq.
+template <typename T>
+__global__ void __launch_bounds__(GATE_WARPS * 32)
+router_finalize_kernel(int n, int d, int b, float eps, const float* __restrict__ dots,
+                       const float* __restrict__ sumsq, const float* __restrict__ b_down,
+                       const T* __restrict__ w_up, const float* __restrict__ b_up, float thr, int rule,
+                       bool need_flag, float* __restrict__ score, uint8_t* __restrict__ mask,
+                       int32_t* __restrict__ flag, void* ws) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float wmin = INFINITY;
+    for (int t = blockIdx.x * GATE_WARPS + warp; t < n; t += gridDim.x * GATE_WARPS) {
+        const float r = 1.0f / sqrtf(sumsq[t] / static_cast<float>(d) + eps);
+        float z = 0.f;
+        for (int c = lane; c < b; c += 32) {
+            float u = dots[static_cast<int64_t>(t) * b + c] * r;
+            if (b_down) u += b_down[c];
+            const float silu = u / (1.0f + expf(-u));
+            z = fmaf(to_f32(w_up[c]), silu, z);
+        }
+        z = warp_sum(z);
+        if (b_up) z += b_up[0];
+        const float p = 1.0f / (1.0f + expf(-z));
+        if (lane == 0) {
+            score[t] = p;
+            if (rule == TEE_RULE_PER_TOKEN) mask[t] = exits(p, thr);
+        }
+        wmin = fminf(wmin, p == p ? p : -INFINITY);
+    }
+    if (!need_flag) return;
+    __shared__ float s_min[GATE_WARPS];
+    if (lane == 0) s_min[warp] = wmin;
+    __syncthreads();
+    float bmin = INFINITY;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < GATE_WARPS; ++w) bmin = fminf(bmin, s_min[w]);
+    batch_flag_tail(bmin, n, thr, rule, mask, flag, ws_at<float>(ws, TEE_WS_HEADER_BYTES),
+                    ws_counter(ws, WS_CNT_ROUTER));
+}
+
+// Tensor-core router contraction (router_tc.cu). Returns TEE_ERR_UNSUPPORTED
+// when the shape does not fit it, so that the CUDA-core kernel runs instead.
+tee_status router_dots_tc(int n, int d, int b, int dtype, const void* h, int64_t ldh, const void* gamma,
+                          const void* w_down, float* dots, float* sumsq, void* ws, size_t ws_off,
+                          size_t ws_bytes, cudaStream_t stream);
+
+static size_t gate_blocks(int n) {
+    size_t blocks = (static_cast<size_t>(n) + GATE_WARPS - 1) / GATE_WARPS;
+    return blocks < 1 ? 1 : (blocks > GATE_MAX_BLOCKS ? GATE_MAX_BLOCKS : blocks);
+}
+
+// Workspace: header | block minima (GATE_MAX_BLOCKS f32) | router dots [n][b] f32 | sumsq [n] f32 | tc scratch
+static size_t router_dots_off() { return TEE_WS_HEADER_BYTES + GATE_MAX_BLOCKS * sizeof(float); }
+static size_t router_sumsq_off(int n, int b) { return round_up(router_dots_off() + static_cast<size_t>(n) * b * 4, 256); }
+static size_t router_tc_off(int n, int b) { return round_up(router_sumsq_off(n, b) + static_cast<size_t>(n) * 4, 256); }
+size_t router_tc_scratch_bytes(int n, int d, int b);
+
+template <typename T>
+static tee_status run_gate(const tee_gate_desc* g, int n, const void* h_cur, int64_t ld_cur, const void* h_prev,
+                           int64_t ld_prev, const void* gamma, const void* w_down, const float* b_down,
+                           const void* w_up, const float* b_up, float* score, uint8_t* mask, int32_t* flag,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+    const bool need_flag = flag != nullptr || g->rule == TEE_RULE_BATCH_ALL;
+    const int blocks = static_cast<int>(gate_blocks(n));
+    if (g->mode == TEE_GATE_COSINE) {
+        cosine_gate_kernel<T><<<blocks, GATE_WARPS * 32, 0, stream>>>(
+            n, g->d, static_cast<const T*>(h_cur), ld_cur, static_cast<const T*>(h_prev), ld_prev, g->threshold,
+            g->rule, need_flag, score, mask, flag, ws);
+        return launch_status();
+    }
+    const int b = g->bottleneck;
+    float* dots = ws_at<float>(ws, router_dots_off());
+    float* sumsq = ws_at<float>(ws, router_sumsq_off(n, b));
+    tee_status st = router_dots_tc(n, g->d, b, g->dtype, h_cur, ld_cur, gamma, w_down, dots, sumsq, ws,
+                                   router_tc_off(n, b), ws_bytes, stream);
+    if (st == TEE_ERR_UNSUPPORTED) {
+        dim3 grid((n + RT_TOK - 1) / RT_TOK, (b + RT_WARPS * RT_CH_WARP - 1) / (RT_WARPS * RT_CH_WARP));
+        const size_t smem = static_cast<size_t>(RT_TOK) * g->d * sizeof(float);
+        if (smem > 48 * 1024) {
+            st = cuda_status(cudaFuncSetAttribute(router_dot_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(smem)));
+            if (st != TEE_OK) return st;
+        }
+        router_dot_kernel<T><<<grid, RT_WARPS * 32, smem, stream>>>(
+            n, g->d, b, static_cast<const T*>(h_cur), ld_cur, static_cast<const T*>(gamma),
+            static_cast<const T*>(w_down), dots, sumsq);
+        st = launch_status();
+    }
+    if (st != TEE_OK) return st;
+    router_finalize_kernel<T><<<blocks, GATE_WARPS * 32, 0, stream>>>(
+        n, g->d, b, g->eps, dots, sumsq, b_down, static_cast<const T*>(w_up), b_up, g->threshold, g->rule,
+        need_flag, score, mask, flag, ws);
+    return launch_status();
+}
+
+}  // namespace tee
+
+using namespace tee;
+
+extern "C" size_t tee_exit_gate_workspace_size(const tee_gate_desc* g, int32_t n) {
+    if (!g || n < 0) return 0;
+    if (g->mode == TEE_GATE_COSINE) return TEE_WS_HEADER_BYTES + GATE_MAX_BLOCKS * sizeof(float);
+    const int b = g->bottleneck > 0 ? g->bottleneck : 128;
+    return router_tc_off(n, b) + router_tc_scratch_bytes(n, g->d, b);
+}
+
+extern "C" tee_status tee_exit_gate(const tee_gate_desc* g, int32_t n, const void* h_cur, int64_t ld_cur,
+                                    const void* h_prev, int64_t ld_prev, const void* gamma, const void* w_down,
+                                    const float* b_down, const void* w_up, const float* b_up, float* score,
+                                    uint8_t* mask, int32_t* batch_flag, void* ws, size_t ws_bytes, void* stream) {
+    if (!g || n < 0 || g->d <= 0 || g->d % 8 != 0) return TEE_ERR_INVALID_ARG;
+    if (g->mode != TEE_GATE_COSINE && g->mode != TEE_GATE_ROUTER) return TEE_ERR_INVALID_ARG;
+    if (g->rule != TEE_RULE_PER_TOKEN && g->rule != TEE_RULE_BATCH_ALL) return TEE_ERR_INVALID_ARG;
+    if (g->threshold != g->threshold) return TEE_ERR_INVALID_ARG;
+    const size_t es = dtype_bytes(g->dtype);
+    if (es == 0) return TEE_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < tee_exit_gate_workspace_size(g, n)) return TEE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n == 0) {
+        if (batch_flag) return cuda_status(cudaMemsetAsync(batch_flag, 0, sizeof(int32_t), s));
+        return TEE_OK;
+    }
+    if (!h_cur || !score || !mask || ld_cur < g->d || !aligned16(h_cur) || (ld_cur * es) % 16) return TEE_ERR_INVALID_ARG;
+    if (g->mode == TEE_GATE_COSINE) {
+        if (!h_prev || ld_prev < g->d || !aligned16(h_prev) || (ld_prev * es) % 16) return TEE_ERR_INVALID_ARG;
+    } else {
+        if (!w_down || !w_up || g->bottleneck <= 0 || !aligned16(w_down)) return TEE_ERR_INVALID_ARG;
+        if (gamma && !aligned16(gamma)) return TEE_ERR_INVALID_ARG;
+        if (!(g->eps >= 0.f)) return TEE_ERR_INVALID_ARG;
+    }
+    switch (g->dtype) {
+        case TEE_F32:
+            return run_gate<float>(g, n, h_cur, ld_cur, h_prev, ld_prev, gamma, w_down, b_down, w_up, b_up, score,
+                                   mask, batch_flag, ws, ws_bytes, s);
+        case TEE_F16:
+            return run_gate<__half>(g, n, h_cur, ld_cur, h_prev, ld_prev, gamma, w_down, b_down, w_up, b_up, score,
+                                    mask, batch_flag, ws, ws_bytes, s);
+        default:
+            return run_gate<__nv_bfloat16>(g, n, h_cur, ld_cur, h_prev, ld_prev, gamma, w_down, b_down, w_up, b_up,
+                                           score, mask, batch_flag, ws, ws_bytes, s);
+    }
+}

@@ -1,0 +1,240 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Each function takes CUDA tensors, passes their device pointers, leading
+dimensions and the current torch stream to libtee.so, and returns the output
+tensors. No step of the computation runs in Python or PyTorch: the library
+kernels do all of it, and a missing library raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import (CacheLayout, FillDesc, FillLayer, GateDesc, check, load)
+
+_DT = {torch.float32: _lib.TEE_F32, torch.float16: _lib.TEE_F16, torch.bfloat16: _lib.TEE_BF16}
+_RULE = {"per_token": _lib.TEE_RULE_PER_TOKEN, "batch_all": _lib.TEE_RULE_BATCH_ALL}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _mat(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with contiguous rows")
+    return t
+
+
+def _vec(t: Optional[torch.Tensor], name: str) -> Optional[torch.Tensor]:
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t
+
+
+class Workspace:
+    """Device scratch for the calls. Grows on demand; a new buffer is
+    zero-filled once through tee_workspace_init, as the ABI requires."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf: Optional[torch.Tensor] = None
+
+    def get(self, nbytes: int):
+        nbytes = max(int(nbytes), _lib.WS_HEADER_BYTES)
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            check("tee_workspace_init", load().tee_workspace_init(_ptr(self.buf), nbytes, _stream(self.device)))
+        return _ptr(self.buf), self.buf.numel()
+
+    def device_error(self):
+        """(code, detail) of the first device fault recorded; synchronises the stream."""
+        if self.buf is None:
+            return 0, 0
+        code, detail = ctypes.c_int32(0), ctypes.c_int32(0)
+        st = load().tee_get_device_error(_ptr(self.buf), ctypes.byref(code), ctypes.byref(detail),
+                                         _stream(self.device))
+        if st not in (_lib.TEE_OK, _lib.TEE_ERR_DEVICE):
+            check("tee_get_device_error", st)
+        return code.value, detail.value
+
+    def clear_error(self):
+        if self.buf is not None:
+            check("tee_clear_device_error", load().tee_clear_device_error(_ptr(self.buf), _stream(self.device)))
+
+
+def exit_gate(h_cur: torch.Tensor, threshold: float, *, h_prev: Optional[torch.Tensor] = None,
+              w_down: Optional[torch.Tensor] = None, w_up: Optional[torch.Tensor] = None,
+              gamma: Optional[torch.Tensor] = None, b_down: Optional[torch.Tensor] = None,
+              b_up: Optional[torch.Tensor] = None, rule: str = "per_token", eps: float = 1e-5,
+              ws: Optional[Workspace] = None, out: Optional[Dict[str, torch.Tensor]] = None):
+    """Cosine gate when ``h_prev`` is given, else TIDE router gate (``w_down``,
+    ``w_up``). Returns (score f32[n], mask u8[n], batch_flag i32[1])."""
+    lib = load()
+    h_cur = _mat(h_cur, "h_cur")
+    n, d = h_cur.shape
+    cosine = h_prev is not None
+    desc = GateDesc(mode=_lib.TEE_GATE_COSINE if cosine else _lib.TEE_GATE_ROUTER, rule=_RULE[rule],
+                    dtype=_DT[h_cur.dtype], d=d, bottleneck=0 if cosine else int(w_down.shape[0]),
+                    threshold=float(threshold), eps=float(eps))
+    if cosine:
+        _mat(h_prev, "h_prev")
+    else:
+        _mat(w_down, "w_down")
+        _vec(w_up, "w_up")
+    out = out or {}
+    score = out.get("score", torch.empty(n, dtype=torch.float32, device=h_cur.device))
+    mask = out.get("mask", torch.empty(n, dtype=torch.uint8, device=h_cur.device))
+    flag = out.get("flag", torch.empty(1, dtype=torch.int32, device=h_cur.device))
+    ws = ws or Workspace(h_cur.device)
+    wp, wn = ws.get(lib.tee_exit_gate_workspace_size(ctypes.byref(desc), n))
+    st = lib.tee_exit_gate(ctypes.byref(desc), n, _ptr(h_cur), h_cur.stride(0),
+                           _ptr(h_prev), h_prev.stride(0) if cosine else 0,
+                           _ptr(_vec(gamma, "gamma")), _ptr(w_down), _ptr(_vec(b_down, "b_down")),
+                           _ptr(w_up), _ptr(_vec(b_up, "b_up")), _ptr(score), _ptr(mask), _ptr(flag),
+                           wp, wn, _stream(h_cur.device))
+    check("tee_exit_gate", st)
+    return score, mask, flag
+
+
+def exit_compact(mask: torch.Tensor, *, pos_in: Optional[torch.Tensor] = None, h: Optional[torch.Tensor] = None,
+                 ws: Optional[Workspace] = None, out: Optional[Dict[str, torch.Tensor]] = None,
+                 with_pos: bool = True) -> Dict[str, torch.Tensor]:
+    """Stable split by ``mask``; gathers the continuing rows of ``h`` when given."""
+    lib = load()
+    mask = _vec(mask, "mask")
+    n = mask.numel()
+    dev = mask.device
+    out = dict(out or {})
+    for k in ("cont_rows", "exit_rows") + (("cont_pos", "exit_pos") if with_pos else ()):
+        out.setdefault(k, torch.empty(n, dtype=torch.int32, device=dev))
+    out.setdefault("counts", torch.empty(2, dtype=torch.int32, device=dev))
+    d, dt, ldi, ldc = 0, _lib.TEE_BF16, 0, 0
+    if h is not None:
+        _mat(h, "h")
+        d = h.shape[1]
+        dt = _DT[h.dtype]
+        out.setdefault("h_cont", torch.empty((n, d), dtype=h.dtype, device=dev))
+        ldi, ldc = h.stride(0), out["h_cont"].stride(0)
+    ws = ws or Workspace(dev)
+    wp, wn = ws.get(lib.tee_exit_compact_workspace_size(n))
+    st = lib.tee_exit_compact(n, _ptr(mask), _ptr(_vec(pos_in, "pos_in")), _ptr(h), ldi, d, dt,
+                              _ptr(out["cont_rows"]), _ptr(out["exit_rows"]), _ptr(out.get("cont_pos")),
+                              _ptr(out.get("exit_pos")), _ptr(out.get("h_cont")), ldc, _ptr(out["counts"]),
+                              wp, wn, _stream(dev))
+    check("tee_exit_compact", st)
+    return out
+
+
+def exit_scatter(counts: torch.Tensor, exit_rows: torch.Tensor, exit_pos: torch.Tensor, h_src: torch.Tensor,
+                 out: torch.Tensor, *, final_gamma: Optional[torch.Tensor] = None, eps: float = 1e-5,
+                 n_max: Optional[int] = None, ws: Optional[Workspace] = None) -> torch.Tensor:
+    """out[exit_pos[i]] = h_src[exit_rows[i]] (optionally RMSNorm * final_gamma) for i < counts[1]."""
+    lib = load()
+    _mat(h_src, "h_src")
+    _mat(out, "out")
+    n_max = h_src.shape[0] if n_max is None else int(n_max)
+    ws = ws or Workspace(out.device)
+    wp, wn = ws.get(lib.tee_exit_scatter_workspace_size(n_max))
+    st = lib.tee_exit_scatter(n_max, _ptr(_vec(counts, "counts")), _ptr(_vec(exit_rows, "exit_rows")),
+                              _ptr(_vec(exit_pos, "exit_pos")), _ptr(h_src), h_src.stride(0), _ptr(out),
+                              out.stride(0), out.shape[0], h_src.shape[1], _DT[h_src.dtype],
+                              _ptr(_vec(final_gamma, "final_gamma")), float(eps), wp, wn, _stream(out.device))
+    check("tee_exit_scatter", st)
+    return out
+
+
+def cache_layout(cache: torch.Tensor) -> CacheLayout:
+    """Layout of a [layers][seqs][kv_heads][positions][head_dim] cache tensor."""
+    if cache.dim() != 5 or cache.stride(4) != 1:
+        raise ValueError("cache must be 5-D [layers][seqs][kv_heads][positions][head_dim] with contiguous head_dim")
+    s = cache.stride()
+    L, S, H, P, _ = cache.shape
+    return CacheLayout(s_layer=s[0], s_seq=s[1], s_head=s[2], s_pos=s[3], n_layers=L, n_seq=S, n_heads=H, max_pos=P)
+
+
+class KVFill:
+    """Prepared KV fill for a fixed set of filled layers.
+
+    ``layers`` holds one dict per filled layer with CUDA tensors ``gamma``,
+    ``wk``, ``wv`` (dense [d][kvw] or packed int4 [d/2][kvw]), optionally
+    ``w_map`` [d][d] and, for int4, ``k_scale``, ``k_zero``, ``v_scale``,
+    ``v_zero`` [d/group][kvw] fp16, plus the int ``cache_layer``.
+    """
+
+    def __init__(self, layers: Sequence[Dict], *, d: int, n_kv_heads: int, head_dim: int, rope_base: float,
+                 eps: float, dtype: torch.dtype, max_pos: int, int4: bool = False, group: int = 64):
+        self.lib = load()
+        self.desc = FillDesc(d=d, n_kv_heads=n_kv_heads, head_dim=head_dim, rope_base=float(rope_base),
+                             eps=float(eps), dtype=_DT[dtype], wfmt=_lib.TEE_W_INT4 if int4 else _lib.TEE_W_DENSE,
+                             group=group)
+        self.keep: List[torch.Tensor] = []
+        arr = (FillLayer * max(1, len(layers)))()
+        dev = None
+        for i, L in enumerate(layers):
+            def p(k):
+                t = L.get(k)
+                if t is None:
+                    return None
+                _vec(t, k)
+                self.keep.append(t)
+                return t.data_ptr()
+            arr[i].w_map, arr[i].gamma, arr[i].wk, arr[i].wv = p("w_map"), p("gamma"), p("wk"), p("wv")
+            arr[i].k_scale, arr[i].k_zero = p("k_scale"), p("k_zero")
+            arr[i].v_scale, arr[i].v_zero = p("v_scale"), p("v_zero")
+            arr[i].cache_layer = int(L["cache_layer"])
+            dev = L["gamma"].device
+        self.layers = arr
+        self.n_layers = len(layers)
+        self.max_pos = int(max_pos)
+        self.device = dev or torch.device("cuda")
+        nbytes = self.lib.tee_kv_fill_prep_size(ctypes.byref(self.desc), self.n_layers, self.max_pos)
+        if nbytes == 0:
+            raise ValueError("invalid KV fill descriptor")
+        self.prep = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        st = self.lib.tee_kv_fill_prepare(ctypes.byref(self.desc), self.n_layers, self.layers, self.max_pos,
+                                          _ptr(self.prep), nbytes, _stream(self.device))
+        check("tee_kv_fill_prepare", st)
+
+    def workspace_bytes(self, n_max: int) -> int:
+        return self.lib.tee_kv_fill_workspace_size(ctypes.byref(self.desc), self.n_layers, int(n_max))
+
+    def __call__(self, h_split: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+                 rows: Optional[torch.Tensor] = None, pos: Optional[torch.Tensor] = None, pos0: int = 0,
+                 seq: Optional[torch.Tensor] = None, n_dev: Optional[torch.Tensor] = None,
+                 n_max: Optional[int] = None, ws: Optional[Workspace] = None) -> None:
+        _mat(h_split, "h_split")
+        if k_cache.stride() != v_cache.stride() or k_cache.shape != v_cache.shape:
+            raise ValueError("k_cache and v_cache must share one layout")
+        layout = cache_layout(k_cache)
+        if n_max is None:
+            n_max = rows.numel() if rows is not None else h_split.shape[0]
+        ws = ws or Workspace(h_split.device)
+        wp, wn = ws.get(self.workspace_bytes(n_max))
+        st = self.lib.tee_kv_fill(ctypes.byref(self.desc), self.n_layers, self.layers, _ptr(self.prep),
+                                  self.prep.numel(), int(n_max), _ptr(_vec(n_dev, "n_dev")), _ptr(h_split),
+                                  h_split.stride(0), h_split.shape[0], _ptr(_vec(rows, "rows")),
+                                  _ptr(_vec(pos, "pos")), int(pos0), _ptr(_vec(seq, "seq")), _ptr(k_cache),
+                                  _ptr(v_cache), ctypes.byref(layout), wp, wn, _stream(h_split.device))
+        check("tee_kv_fill", st)
+
+
+def kv_fill(h_split: torch.Tensor, layers: Sequence[Dict], k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+            n_kv_heads: int, head_dim: int, rope_base: float, eps: float = 1e-5, int4: bool = False,
+            group: int = 64, **kw) -> KVFill:
+    """One-shot convenience: prepare for these layers and fill; returns the prepared object."""
+    f = KVFill(layers, d=h_split.shape[1], n_kv_heads=n_kv_heads, head_dim=head_dim, rope_base=rope_base, eps=eps,
+               dtype=h_split.dtype, max_pos=k_cache.shape[3], int4=int4, group=group)
+    f(h_split, k_cache, v_cache, **kw)
+    return f
