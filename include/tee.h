@@ -148,6 +148,40 @@ TEE_API tee_status tee_exit_gate(const tee_gate_desc* desc, int32_t n,
                          float* score, uint8_t* mask, int32_t* batch_flag,
                          void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Router gate that needs no workspace (no counterpart on the source pages; it
+ * exists for callers that cannot provide device scratch).
+ *
+ * Meant for callers that cannot allocate device memory when they call the
+ * gate: for example a plugin whose host owns all device memory through its
+ * own pool and passes in only the call's inputs and outputs, or a
+ * latency-critical loop where cudaMalloc is not allowed because it can block
+ * or synchronise the device. It computes exactly what tee_exit_gate computes
+ * in router mode (same kernels, same arguments without h_prev and without a
+ * workspace), taking its scratch from a 4 MiB array compiled into the
+ * library; every GPU that loads the library keeps that array until the
+ * process exits. The call itself allocates nothing.
+ *
+ * Limit: the call is rejected with TEE_ERR_WORKSPACE when its scratch need,
+ * tee_exit_gate_workspace_size(desc, n), exceeds
+ * tee_exit_gate_router_static_max_bytes() (4 MiB), e.g. for more than about
+ * 8,000 tokens at bottleneck 128; desc->mode must be TEE_GATE_ROUTER.
+ * Set-up: the first call on each device (the device current on the calling
+ * thread) looks up the array's device address; make that first call before
+ * any stream capture. Sharing: all calls on a device use the same array and
+ * it keeps the previous call's contents (each call clears the part that must
+ * start at zero), so two calls that overlap on the GPU, on different streams
+ * or threads, race and may return wrong results. The device fault word lives
+ * in the array too; tee_get_device_error cannot read it.
+ */
+TEE_API size_t tee_exit_gate_router_static_max_bytes(void);
+TEE_API tee_status tee_exit_gate_router_static(const tee_gate_desc* desc, int32_t n,
+                                               const void* h, int64_t ld,
+                                               const void* gamma, const void* w_down, const float* b_down,
+                                               const void* w_up, const float* b_up,
+                                               float* score, uint8_t* mask, int32_t* batch_flag,
+                                               void* stream);
+
 /* -------------------------------------------------------- exit compaction */
 
 TEE_API size_t tee_exit_compact_workspace_size(int32_t n);

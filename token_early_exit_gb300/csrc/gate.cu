@@ -13,6 +13,8 @@
 // Both end in the same decision, score > threshold in fp32, and the same
 // "last block" reduction of the all-tokens flag (River-LLM's min over the
 // batch; TIDE module 3's "for every token in the batch").
+#include <mutex>
+
 #include "common.cuh"
 
 namespace tee {
@@ -296,4 +298,62 @@ extern "C" tee_status tee_exit_gate(const tee_gate_desc* g, int32_t n, const voi
             return run_gate<__nv_bfloat16>(g, n, h_cur, ld_cur, h_prev, ld_prev, gamma, w_down, b_down, w_up, b_up,
                                            score, mask, batch_flag, ws, ws_bytes, s);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Router gate without a caller workspace.
+//
+// Some callers cannot hand the library any device scratch: a plugin whose host
+// owns all device memory through its own pool and passes the plugin nothing but
+// the call's inputs and outputs, or a latency-critical loop where cudaMalloc is
+// ruled out because it can block or synchronise the device. For them the
+// router gate can take its scratch (per-token channel sums and sum of squares,
+// per-block minima, the last-block counter) from a fixed array compiled into
+// the library. Every GPU that loads the library holds this array until the
+// process exits.
+constexpr size_t ROUTER_STATIC_SCRATCH_BYTES = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_router_scratch[ROUTER_STATIC_SCRATCH_BYTES];
+
+constexpr int STATIC_MAX_DEVICES = 64;
+static std::mutex g_router_scratch_mu;
+static void* g_router_scratch_addr[STATIC_MAX_DEVICES] = {};
+
+// Device address of the array on the current device. Host code only knows a
+// host-side stand-in for it, so the address comes from cudaGetSymbolAddress,
+// looked up once per device with that device current.
+static tee_status router_static_scratch(void** out) {
+    int dev = 0;
+    tee_status st = cuda_status(cudaGetDevice(&dev));
+    if (st != TEE_OK) return st;
+    if (dev < 0 || dev >= STATIC_MAX_DEVICES) return TEE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_router_scratch_mu);
+    if (!g_router_scratch_addr[dev]) {
+        void* p = nullptr;
+        st = cuda_status(cudaGetSymbolAddress(&p, g_router_scratch));
+        if (st != TEE_OK) return st;
+        g_router_scratch_addr[dev] = p;
+    }
+    *out = g_router_scratch_addr[dev];
+    return TEE_OK;
+}
+
+extern "C" size_t tee_exit_gate_router_static_max_bytes(void) { return ROUTER_STATIC_SCRATCH_BYTES; }
+
+extern "C" tee_status tee_exit_gate_router_static(const tee_gate_desc* g, int32_t n, const void* h, int64_t ld,
+                                                  const void* gamma, const void* w_down, const float* b_down,
+                                                  const void* w_up, const float* b_up, float* score,
+                                                  uint8_t* mask, int32_t* batch_flag, void* stream) {
+    if (!g || g->mode != TEE_GATE_ROUTER) return TEE_ERR_INVALID_ARG;
+    if (n < 0) return TEE_ERR_INVALID_ARG;
+    const size_t need = tee_exit_gate_workspace_size(g, n);
+    if (need == 0 || need > ROUTER_STATIC_SCRATCH_BYTES) return TEE_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    tee_status st = router_static_scratch(&scratch);
+    if (st != TEE_OK) return st;
+    // The array keeps the previous call's contents; the header (fault word and
+    // the last-block counter) must start at zero.
+    st = cuda_status(cudaMemsetAsync(scratch, 0, TEE_WS_HEADER_BYTES, static_cast<cudaStream_t>(stream)));
+    if (st != TEE_OK) return st;
+    return tee_exit_gate(g, n, h, ld, nullptr, 0, gamma, w_down, b_down, w_up, b_up, score, mask, batch_flag,
+                         scratch, ROUTER_STATIC_SCRATCH_BYTES, stream);
 }
