@@ -79,7 +79,8 @@ enum {
     TEE_DEVERR_POS = 2,        /* a cache position outside [0, max_pos) */
     TEE_DEVERR_SEQ = 3,        /* a cache sequence outside [0, n_seq) */
     TEE_DEVERR_COUNT = 4,      /* a device-side count larger than its host-side bound */
-    TEE_DEVERR_DEST = 5        /* a scatter destination outside [0, n_out) */
+    TEE_DEVERR_DEST = 5,       /* a scatter destination outside [0, n_out) */
+    TEE_DEVERR_TIMEOUT = 6     /* a pipeline wait ran out of time; the kernel stopped early (detail: where) */
 };
 
 #define TEE_WS_HEADER_BYTES 256

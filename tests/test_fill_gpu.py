@@ -109,3 +109,116 @@ def test_bad_positions_are_recorded_and_skipped(tee):
     assert code == 2 and detail == cfg.cache_len + 5   # TEE_DEVERR_POS
     good = np.array([r for r in range(cfg.batch) if r != 2], dtype=np.int32)
     _check_decode(cfg, x, good, pos.cpu().numpy(), x["seq"].cpu().numpy())
+
+
+# ---------------------------------------------------------------- tensor-core path
+# bf16 fills of at least 256 rows with dense weights run on tcgen05 (128 x 256 tiles).
+
+def _layers_for(cfg, d, kvw, n_layers, seed, identity=False):
+    import math
+    out = []
+    for i in range(n_layers):
+        w = None if identity else (gen.normal((d, d), 1.0 / math.sqrt(d), seed, f"W{i}", DEV) +
+                                   0.5 * torch.eye(d, device=DEV)).bfloat16()
+        out.append({"cache_layer": i, "w_map": w,
+                    "gamma": gen.normal((d,), 0.1, seed, f"g{i}", DEV, torch.bfloat16, mean=1.0),
+                    "wk": gen.normal((d, kvw), math.sqrt(0.25 / d), seed, f"wk{i}", DEV, torch.bfloat16),
+                    "wv": gen.normal((d, kvw), math.sqrt(0.25 / d), seed, f"wv{i}", DEV, torch.bfloat16)})
+    return out
+
+
+@pytest.mark.parametrize("rows", [256, 257, 383, 640, 4109])
+def test_tc_fill_ragged_tails(tee, rows):
+    cfg = configs.PREFILL_16K
+    x = gen.prefill_inputs(cfg, seed=rows, device=DEV, rows=rows, layers=2)
+    f = _make(tee, cfg, x["layers"], torch.bfloat16, cfg.tokens)
+    f(x["h_split"], x["k_cache"], x["v_cache"])
+    rng = np.random.default_rng(rows)
+    check = np.unique(np.concatenate([np.arange(40), np.arange(rows - 40, rows), rng.integers(0, rows, 48)]))
+    _prefill_check(cfg, x, check.astype(np.int64), rows)
+
+
+@pytest.mark.parametrize("identity", [True, False])
+def test_tc_fill_head_dim_64_and_identity_map(tee, identity):
+    cfg = configs.PrefillFillConfig(name="hd64", d=2048, n_layers=4, n_q_heads=32, n_kv_heads=8, head_dim=64,
+                                    rope_base=5e5, split=2, tokens=1024, exact_tail=0)
+    rows = 700
+    h = gen.normal((rows, cfg.d), 1.0, 3, "h", DEV, torch.bfloat16)
+    layers = _layers_for(cfg, cfg.d, cfg.kvw, 2, 3, identity)
+    shape = (2, 1, cfg.n_kv_heads, cfg.tokens, cfg.head_dim)
+    x = {"h_split": h, "layers": layers,
+         "k_cache": torch.full(shape, gen.CACHE_SENTINEL, dtype=torch.bfloat16, device=DEV),
+         "v_cache": torch.full(shape, gen.CACHE_SENTINEL, dtype=torch.bfloat16, device=DEV)}
+    f = _make(tee, cfg, layers, torch.bfloat16, cfg.tokens)
+    f(h, x["k_cache"], x["v_cache"], pos0=100)
+    _prefill_check(cfg, x, np.arange(0, rows, 7).astype(np.int64), rows, pos0=100)
+
+
+def test_tc_fill_scattered_positions_sequences_and_device_count(tee):
+    # A large batch of decode tokens: each row has its own sequence and position.
+    cfg = configs.PrefillFillConfig(name="scatter", d=1024, n_layers=2, n_q_heads=8, n_kv_heads=4, head_dim=128,
+                                    rope_base=1e4, split=0, tokens=2048, exact_tail=0)
+    n_max, n = 600, 517
+    h = gen.normal((n_max, cfg.d), 1.0, 5, "h", DEV, torch.bfloat16)
+    layers = _layers_for(cfg, cfg.d, cfg.kvw, 2, 5)
+    n_seq = 40
+    # distinct (seq, pos) slots, so that no slot is written twice
+    slots = torch.randperm(n_seq * cfg.tokens, generator=torch.Generator().manual_seed(5))[:n_max].to(DEV)
+    seq, pos = (slots // cfg.tokens).int(), (slots % cfg.tokens).int()
+    shape = (2, n_seq, cfg.n_kv_heads, cfg.tokens, cfg.head_dim)
+    x = {"h_cur": h, "layers": layers,
+         "k_cache": torch.full(shape, gen.CACHE_SENTINEL, dtype=torch.bfloat16, device=DEV),
+         "v_cache": torch.full(shape, gen.CACHE_SENTINEL, dtype=torch.bfloat16, device=DEV)}
+    f = _make(tee, cfg, layers, torch.bfloat16, cfg.tokens)
+    n_dev = torch.tensor([n], dtype=torch.int32, device=DEV)
+    f(h, x["k_cache"], x["v_cache"], pos=pos, seq=seq, n_dev=n_dev, n_max=n_max)
+    cfg2 = configs.DecodeConfig(name="scatter", d=cfg.d, n_layers=2, n_q_heads=8, n_kv_heads=cfg.n_kv_heads,
+                                head_dim=cfg.head_dim, batch=n_max, cache_len=cfg.tokens, gate_layer=0,
+                                fill_layers=(0, 1), tau=0.5, rule="per_token", weights="dense", map="ridge",
+                                rope_base=cfg.rope_base, dtype="bf16")
+    check_decode_fill(cfg2, x, np.arange(n), pos.cpu().numpy(), seq.cpu().numpy(), gen.CACHE_SENTINEL)
+
+
+def test_tc_fill_records_bad_positions(tee):
+    cfg = configs.PREFILL_16K
+    rows = 300
+    x = gen.prefill_inputs(cfg, seed=4, device=DEV, rows=rows, layers=1)
+    ws = tee.Workspace(DEV)
+    f = _make(tee, cfg, x["layers"], torch.bfloat16, cfg.tokens)
+    pos = torch.arange(rows, dtype=torch.int32, device=DEV)
+    pos[17] = cfg.tokens + 3
+    f(x["h_split"], x["k_cache"], x["v_cache"], pos=pos, ws=ws)
+    code, detail = ws.device_error()
+    assert code == 2 and detail == cfg.tokens + 3
+    good = np.array([r for r in range(rows) if r != 17], dtype=np.int64)
+    _prefill_check(cfg, {**x, "k_cache": x["k_cache"], "v_cache": x["v_cache"]}, good[::5], rows)
+    assert bool((x["k_cache"][:, 0, :, 17] == gen.CACHE_SENTINEL).all())
+
+
+def _sampled_rows(n, seed, k=48):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([np.arange(16), np.arange(n - 16, n), rng.integers(0, n, k)])).astype(np.int64)
+
+
+@pytest.mark.parametrize("cfg", [configs.PREFILL_16K, configs.PREFILL_120K], ids=["16k", "120k"])
+def test_tc_fill_full_prefill_workload(tee, cfg):
+    """The full workload in the launch configuration the bench times, checked on
+    sampled rows (all layers) and, everywhere, on the slots that must stay untouched."""
+    x = gen.prefill_inputs(cfg, seed=0, device=DEV)
+    f = _make(tee, cfg, x["layers"], torch.bfloat16, cfg.tokens)
+    f(x["h_split"], x["k_cache"], x["v_cache"])
+    torch.cuda.synchronize()
+    rows = _sampled_rows(cfg.filled_rows, 1)
+    h = f64(x["h_split"][torch.as_tensor(rows, device=DEV)])
+    for L in x["layers"]:
+        Lh = host(L)
+        k_ref, v_ref = oracle.fill_rows(h, Lh, rows, cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, cfg.eps)
+        j = L["cache_layer"]
+        p = torch.as_tensor(rows, device=DEV)
+        check_kv(x["k_cache"][j, 0].index_select(1, p).permute(1, 0, 2), k_ref, f"K layer {j}")
+        check_kv(x["v_cache"][j, 0].index_select(1, p).permute(1, 0, 2), v_ref, f"V layer {j}")
+        del Lh
+    for c in (x["k_cache"], x["v_cache"]):
+        assert bool((c[:, :, :, cfg.filled_rows:] == gen.CACHE_SENTINEL).all())   # exact tail untouched
+        assert bool(torch.isfinite(c[:, :, :, :cfg.filled_rows]).all())
+        assert not bool((c[:, :, :, :cfg.filled_rows] == gen.CACHE_SENTINEL).any())  # every filled slot written

@@ -16,7 +16,8 @@ TEE_F32, TEE_F16, TEE_BF16 = 0, 1, 2
 TEE_GATE_COSINE, TEE_GATE_ROUTER = 0, 1
 TEE_RULE_PER_TOKEN, TEE_RULE_BATCH_ALL = 0, 1
 TEE_W_DENSE, TEE_W_INT4 = 0, 1
-TEE_DEVERR_NONE, TEE_DEVERR_ROW, TEE_DEVERR_POS, TEE_DEVERR_SEQ, TEE_DEVERR_COUNT, TEE_DEVERR_DEST = range(6)
+(TEE_DEVERR_NONE, TEE_DEVERR_ROW, TEE_DEVERR_POS, TEE_DEVERR_SEQ, TEE_DEVERR_COUNT, TEE_DEVERR_DEST,
+ TEE_DEVERR_TIMEOUT) = range(7)
 WS_HEADER_BYTES = 256
 
 
