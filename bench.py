@@ -98,18 +98,27 @@ class Decode:
         L = len(self.cfg.fill_layers)
         return self._fill_weight_bytes + n_exit * (self._h_row_bytes + L * self._fill_bytes_per_item_layer)
 
-    def step(self, ev=None):
+    def parts(self):
         tee, cfg, x = self.tee, self.cfg, self.x
-        tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule=cfg.rule, ws=self.ws, out=self.g_out)
-        tee.exit_compact(self.g_out["mask"], h=x["h_cur"], ws=self.ws, out=self.c_out)
-        if ev is not None:
-            ev[0].record()
-        self.fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=self.c_out["exit_rows"], pos=x["pos"],
-                  seq=x["seq"], n_dev=self.c_out["counts"][1:], n_max=cfg.batch, ws=self.ws)
-        if ev is not None:
-            ev[1].record()
-        tee.exit_scatter(self.c_out["counts"], self.c_out["exit_rows"], self.c_out["exit_pos"], x["h_cur"],
-                         self.out, ws=self.ws)
+
+        def gate():
+            tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule=cfg.rule, ws=self.ws, out=self.g_out)
+
+        def compact():
+            tee.exit_compact(self.g_out["mask"], h=x["h_cur"], ws=self.ws, out=self.c_out)
+
+        def fill():
+            self.fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=self.c_out["exit_rows"], pos=x["pos"],
+                      seq=x["seq"], n_dev=self.c_out["counts"][1:], n_max=cfg.batch, ws=self.ws)
+
+        def scatter():
+            tee.exit_scatter(self.c_out["counts"], self.c_out["exit_rows"], self.c_out["exit_pos"], x["h_cur"],
+                             self.out, ws=self.ws)
+        return [gate, compact, fill, scatter], 2
+
+    def step(self):
+        for f in self.parts()[0]:
+            f()
 
     def host_io(self):
         """Pinned host copies of the step's inputs and outputs for the end-to-end run."""
@@ -188,14 +197,18 @@ class Router:
         d, b = self.cfg.d, self.cfg.bottleneck
         return self.n * d * 2 + b * d * 2 + b * 2 + self.n * 5
 
-    def step(self, ev=None):
-        if ev is not None:
-            ev[0].record()
-        self.tee.exit_gate(self.h, self.theta, w_down=self.w["w_down"], w_up=self.w["w_up"], eps=self.cfg.eps,
-                           ws=self.ws, out=self.g_out)
-        if ev is not None:
-            ev[1].record()
-        self.tee.exit_compact(self.g_out["mask"], h=self.h, ws=self.ws, out=self.c_out, with_pos=False)
+    def parts(self):
+        def gate():
+            self.tee.exit_gate(self.h, self.theta, w_down=self.w["w_down"], w_up=self.w["w_up"], eps=self.cfg.eps,
+                               ws=self.ws, out=self.g_out)
+
+        def compact():
+            self.tee.exit_compact(self.g_out["mask"], h=self.h, ws=self.ws, out=self.c_out, with_pos=False)
+        return [gate, compact], 0
+
+    def step(self):
+        for f in self.parts()[0]:
+            f()
 
     def host_io(self):
         self.h_in = {"h": self.h.cpu().pin_memory()}
@@ -236,27 +249,31 @@ class Router:
 class Prefill:
     """RidgeFill KV fill of every layer after the split, for all filled rows."""
 
-    def __init__(self, tee, cfg, dev, seed=0):
+    def __init__(self, tee, cfg, dev, seed=0, rows=None, layers=None):
         self.tee, self.cfg, self.dev = tee, cfg, dev
-        self.x = gen.prefill_inputs(cfg, seed=seed, device=dev)
+        self.rows = cfg.filled_rows if rows is None else rows
+        self.x = gen.prefill_inputs(cfg, seed=seed, device=dev, rows=rows, layers=layers)
+        self.n_layers = len(self.x["layers"])
         self.ws = tee.Workspace(dev)
         self.fill = tee.KVFill(self.x["layers"], d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
                                rope_base=cfg.rope_base, eps=cfg.eps, dtype=torch.bfloat16, max_pos=cfg.tokens)
-        self.units = cfg.filled_rows
+        self.units = self.rows
         self.kernel = "kv_fill"
         self.bound = "tensor"
         d, kvw = cfg.d, cfg.kvw
-        self.flops = float(len(cfg.fill_layers)) * cfg.filled_rows * (2 * d * d + 4 * d * kvw)
+        self.flops = float(self.n_layers) * self.rows * (2 * d * d + 4 * d * kvw)
 
     def fill_bytes(self, n_exit):
         return self.flops  # tensor-bound: FLOPs
 
-    def step(self, ev=None):
-        if ev is not None:
-            ev[0].record()
-        self.fill(self.x["h_split"], self.x["k_cache"], self.x["v_cache"], ws=self.ws)
-        if ev is not None:
-            ev[1].record()
+    def parts(self):
+        def fill():
+            self.fill(self.x["h_split"], self.x["k_cache"], self.x["v_cache"], ws=self.ws)
+        return [fill], 0
+
+    def step(self):
+        for f in self.parts()[0]:
+            f()
 
     def host_io(self):
         # inputs: the split-layer rows; output read back: the K/V of the last filled row of each layer
@@ -269,14 +286,16 @@ class Prefill:
     def e2e_step(self):
         self.x["h_split"].copy_(self.h_in["h_split"], non_blocking=True)
         self.step()
-        self.h_out["k_last"].copy_(self.x["k_cache"][:, 0, :, self.cfg.filled_rows - 1], non_blocking=True)
+        self.h_out["k_last"].copy_(self.x["k_cache"][:, 0, :, self.rows - 1], non_blocking=True)
 
     def n_exit(self):
-        return self.cfg.filled_rows
+        return self.rows
 
     def config(self):
         c = self.cfg
-        return {"workload": c.name, "tokens_per_step": c.filled_rows, "d": c.d, "fill_layers": len(c.fill_layers),
+        name = c.name if (self.rows, self.n_layers) == (c.filled_rows, len(c.fill_layers)) else \
+            f"{c.name}-reduced-{self.rows}rows-{self.n_layers}layers"
+        return {"workload": name, "tokens_per_step": self.rows, "d": c.d, "fill_layers": self.n_layers,
                 "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "prompt_tokens": c.tokens,
                 "exact_tail": c.exact_tail, "map": "ridge (N(0,1/d)+0.5I)", "weights": "bf16 dense",
                 "l2": "inputs larger than L2; flushed between timed steps"}
@@ -284,7 +303,7 @@ class Prefill:
     def oracle_sample(self):
         import oracle
         from tests.parity import host
-        rows = np.arange(16) * (self.cfg.filled_rows // 16)
+        rows = np.arange(16) * (self.rows // 16)
         h = host(self.x["h_split"][torch.as_tensor(rows, device=self.dev)])
         layers = host(self.x["layers"])
         cfg = self.cfg
@@ -296,7 +315,7 @@ class Prefill:
         return run, f"fill of 16 evenly spaced rows across all {len(layers)} layers (per-row time extrapolated)"
 
 
-def make(name, tee, dev, seed):
+def make(name, tee, dev, seed, rows=None, layers=None):
     if name == "decode-1b":
         return Decode(tee, configs.LLAMA1B_DECODE, dev, seed)
     if name == "decode-tiny":
@@ -304,9 +323,9 @@ def make(name, tee, dev, seed):
     if name == "router-4096":
         return Router(tee, configs.ROUTER_4096, dev, seed)
     if name == "prefill-16k":
-        return Prefill(tee, configs.PREFILL_16K, dev, seed)
+        return Prefill(tee, configs.PREFILL_16K, dev, seed, rows, layers)
     if name == "prefill-120k":
-        return Prefill(tee, configs.PREFILL_120K, dev, seed)
+        return Prefill(tee, configs.PREFILL_120K, dev, seed, rows, layers)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -404,7 +423,7 @@ def run_reference(args):
         import __graft_entry__
         __graft_entry__.build()
         import token_early_exit_gb300 as tee
-    w = make(args.workload, tee, dev, args.seed) if tee is not None else None
+    w = make(args.workload, tee, dev, args.seed, args.rows, args.layers) if tee is not None else None
     if w is None:
         print(json.dumps({"impl": "reference", "unavailable": "the reference arm needs the seeded inputs on a GPU"}))
         return 0
@@ -440,7 +459,7 @@ def run_gpu(args):
     from token_early_exit_gb300 import _lib
     lib = _lib.load()
 
-    w = make(args.workload, tee, dev, args.seed + rank)
+    w = make(args.workload, tee, dev, args.seed + rank, args.rows, args.layers)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -450,24 +469,50 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     n_exit = w.n_exit()
 
+    # The step (and, separately, the dominant call) replay as CUDA graphs, so that
+    # the GPU is not left waiting for Python between kernels.
+    fns, kidx = w.parts()
+    l0 = lib.tee_launch_count()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        for f in fns:
+            f()
+    k_step = lib.tee_launch_count() - l0
+    g_kern, k_kern = g_step, 0
+    if len(fns) > 1:
+        l0 = lib.tee_launch_count()
+        g_kern = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_kern):
+            fns[kidx]()
+        k_kern = lib.tee_launch_count() - l0
+    for _ in range(2):
+        g_step.replay()
+        if g_kern is not g_step:
+            g_kern.replay()
+    torch.cuda.synchronize(dev)
+
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = Clocks(dev.index)
     barrier(world)
     torch.cuda.synchronize(dev)
     clocks.start()
-    l0 = lib.tee_launch_count()
     for i in range(args.steps):
         flush.zero_()                      # evict L2 (outside the timed events)
         ev[i][0].record(stream)
-        w.step(kev[i])
+        g_step.replay()
         ev[i][1].record(stream)
+        if g_kern is not g_step:
+            flush.zero_()
+            kev[i][0].record(stream)
+            g_kern.replay()
+            kev[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    launches = lib.tee_launch_count() - l0
+    launches = args.steps * (k_step + k_kern)
     barrier(world)
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev] if g_kern is not g_step else step_ms
     t_step = statistics.mean(step_ms)
     t_step = max_over_ranks(t_step, world, dev)
     value = world * w.units / (t_step * 1e-3)
@@ -516,7 +561,8 @@ def run_gpu(args):
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": world * w.units / (t_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": t_e2e},
-            "gpu_launches": int(launches), "clocks": clk,
+            "gpu_launches": int(launches), "launches_per_step": int(k_step), "clocks": clk,
+            "timing": "CUDA-graph replay per step; L2 flushed before each replay",
             "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)}}
     if rank == 0:
         print(json.dumps(line))
@@ -536,6 +582,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=None, help="prefill workloads: fewer filled rows (profiling)")
+    ap.add_argument("--layers", type=int, default=None, help="prefill workloads: fewer filled layers (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

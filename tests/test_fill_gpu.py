@@ -222,3 +222,48 @@ def test_tc_fill_full_prefill_workload(tee, cfg):
         assert bool((c[:, :, :, cfg.filled_rows:] == gen.CACHE_SENTINEL).all())   # exact tail untouched
         assert bool(torch.isfinite(c[:, :, :, :cfg.filled_rows]).all())
         assert not bool((c[:, :, :, :cfg.filled_rows] == gen.CACHE_SENTINEL).any())  # every filled slot written
+
+
+# ---------------------------------------------------------------- decode path
+# int4 fills of up to 128 items with an identity map run as one tcgen05 launch
+# (dequantised weights as the A operand, K split across blocks).
+
+@pytest.mark.parametrize("n,hd", [(1, 64), (17, 64), (100, 64), (128, 64), (48, 128)])
+def test_decode_int4_fill_item_counts(tee, n, hd):
+    base = configs.LLAMA1B_DECODE
+    cfg = configs.DecodeConfig(**{**base.__dict__, "batch": n, "head_dim": hd, "n_kv_heads": 512 // hd})
+    x = gen.decode_inputs(cfg, seed=n + hd, device=DEV, case="exit")
+    f = _make(tee, cfg, x["layers"], torch.bfloat16, cfg.cache_len, int4=True)
+    rng = np.random.default_rng(n)
+    rows = rng.permutation(n).astype(np.int32)   # gathered in a scrambled order
+    f(x["h_cur"], x["k_cache"], x["v_cache"], rows=torch.from_numpy(rows).to(DEV), pos=x["pos"], seq=x["seq"])
+    check_decode_fill(cfg, x, rows, x["pos"].cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL)
+
+
+def test_decode_int4_fill_twice_reuses_the_workspace(tee):
+    # the K-split partial tiles are cleared by the block that finishes each tile
+    cfg = configs.LLAMA1B_DECODE
+    ws = tee.Workspace(DEV)
+    for seed in (7, 8):
+        x = gen.decode_inputs(cfg, seed=seed, device=DEV, case="exit")
+        f = _make(tee, cfg, x["layers"], torch.bfloat16, cfg.cache_len, int4=True)
+        rows = np.arange(cfg.batch, dtype=np.int32)
+        f(x["h_cur"], x["k_cache"], x["v_cache"], rows=torch.from_numpy(rows).to(DEV), pos=x["pos"], seq=x["seq"],
+          ws=ws)
+        check_decode_fill(cfg, x, rows, x["pos"].cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL)
+    assert ws.device_error() == (0, 0)
+
+
+def test_decode_int4_fill_records_bad_positions(tee):
+    cfg = configs.LLAMA1B_DECODE
+    x = gen.decode_inputs(cfg, seed=9, device=DEV, case="exit")
+    ws = tee.Workspace(DEV)
+    f = _make(tee, cfg, x["layers"], torch.bfloat16, cfg.cache_len, int4=True)
+    pos = x["pos"].clone()
+    pos[5] = -1
+    rows = torch.arange(cfg.batch, dtype=torch.int32, device=DEV)
+    f(x["h_cur"], x["k_cache"], x["v_cache"], rows=rows, pos=pos, seq=x["seq"], ws=ws)
+    code, detail = ws.device_error()
+    assert code == 2 and detail == -1
+    good = np.array([r for r in range(cfg.batch) if r != 5], dtype=np.int32)
+    check_decode_fill(cfg, x, good, pos.cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL)

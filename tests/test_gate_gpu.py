@@ -123,3 +123,32 @@ def test_router_zero_weights_give_sigmoid_bias(tee):
     score, _, _ = tee.exit_gate(h, 0.5, w_down=z, w_up=torch.zeros(128, device=DEV, dtype=torch.bfloat16),
                                 b_up=torch.tensor([np.log(3.0)], device=DEV, dtype=torch.float32))
     assert torch.allclose(score, torch.full_like(score, 0.75), atol=1e-6)
+
+
+# ------------------------------------------------------------ router on tcgen05
+# bf16 batches of at least 256 tokens without gamma run the d -> 128 contraction
+# on the tensor cores (K split across CTAs, partial sums accumulated in the workspace).
+
+@pytest.mark.parametrize("n", [256, 300, 1000, 8192])
+def test_router_tc_batch_sizes(tee, n):
+    cfg = configs.ROUTER_4096
+    w = gen.router_weights(cfg, 7, seed=n, device=DEV)
+    h = gen.router_hidden(cfg, n, 7, seed=n, device=DEV)
+    b_down = 0.05 * torch.randn(128, device=DEV)
+    score, mask, flag = tee.exit_gate(h, 0.5, w_down=w["w_down"], w_up=w["w_up"], b_down=b_down, eps=cfg.eps)
+    p_ref, _, _ = _router_ref(h, w, 0.5, "per_token", b_down=b_down, eps=cfg.eps)
+    check_scores(score, p_ref)
+    check_mask(mask, p_ref, 0.5)
+
+
+def test_router_calls_share_a_workspace(tee):
+    # tensor-core and CUDA-core calls alternate on one workspace: each must see clean sums
+    cfg = configs.ROUTER_4096
+    ws = tee.Workspace(DEV)
+    w = gen.router_weights(cfg, 11, seed=1, device=DEV)
+    for n in (4096, 64, 4096, 300, 300):
+        h = gen.router_hidden(cfg, n, 11, seed=n, device=DEV)
+        score, mask, _ = tee.exit_gate(h, 0.5, w_down=w["w_down"], w_up=w["w_up"], eps=cfg.eps, ws=ws)
+        p_ref, _, _ = _router_ref(h, w, 0.5, "per_token", eps=cfg.eps)
+        check_scores(score, p_ref)
+    assert ws.device_error() == (0, 0)

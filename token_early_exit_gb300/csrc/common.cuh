@@ -97,6 +97,21 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
     reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 
+// Copy nv 16-byte vectors by one warp, eight loads per lane in flight.
+__device__ __forceinline__ void warp_copy16(uint4* __restrict__ dst, const uint4* __restrict__ src, int nv,
+                                            int lane) {
+    constexpr int U = 8;
+    for (int k0 = lane; k0 < nv; k0 += 32 * U) {
+        uint4 t[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (k0 + 32 * u < nv) t[u] = __ldg(src + k0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (k0 + 32 * u < nv) dst[k0 + 32 * u] = t[u];
+    }
+}
+
 // ------------------------------------------------------------ reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

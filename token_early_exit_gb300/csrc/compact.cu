@@ -146,7 +146,7 @@ compact_kernel(int n, int R, const uint8_t* __restrict__ mask, const int32_t* __
     for (int j = warp; j < n_cont_chunk; j += CP_WARPS) {
         const uint4* src = reinterpret_cast<const uint4*>(h_in + static_cast<int64_t>(s_src[j]) * ld_in);
         uint4* dst = reinterpret_cast<uint4*>(h_cont + static_cast<int64_t>(dst0 + j) * ld_cont);
-        for (int i = lane; i < d / V; i += 32) dst[i] = src[i];
+        warp_copy16(dst, src, d / V, lane);
     }
 }
 
@@ -177,9 +177,7 @@ scatter_kernel(int n_max, const int32_t* __restrict__ counts, const int32_t* __r
         T* o = out + dst * ld_out;
         if (!gamma) {
             constexpr int V = 16 / sizeof(T);
-            const uint4* sv = reinterpret_cast<const uint4*>(s);
-            uint4* ov = reinterpret_cast<uint4*>(o);
-            for (int k = lane; k < d / V; k += 32) ov[k] = sv[k];
+            warp_copy16(reinterpret_cast<uint4*>(o), reinterpret_cast<const uint4*>(s), d / V, lane);
             continue;
         }
         float ss = 0.f;

@@ -35,16 +35,27 @@ cosine_gate_kernel(int n, int d, const T* __restrict__ hc, int64_t ldc, const T*
         const T* a = hp + static_cast<int64_t>(t) * ldp;
         const T* b = hc + static_cast<int64_t>(t) * ldc;
         float dot = 0.f, na = 0.f, nb = 0.f;
-        for (int i = lane * 8; i < d; i += 256) {
-            float x[8], y[8];
-            load8(a + i, x);
-            load8(b + i, y);
+        // Four 16-byte chunks of each row per lane in flight at once.
+        for (int i0 = lane * 8; i0 < d; i0 += 4 * 256) {
+            float x[4][8], y[4][8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                dot = fmaf(x[k], y[k], dot);
-                na = fmaf(x[k], x[k], na);
-                nb = fmaf(y[k], y[k], nb);
+            for (int u = 0; u < 4; ++u) {
+                if (i0 + u * 256 < d) {
+                    load8(a + i0 + u * 256, x[u]);
+                    load8(b + i0 + u * 256, y[u]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) x[u][k] = y[u][k] = 0.f;
+                }
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    dot = fmaf(x[u][k], y[u][k], dot);
+                    na = fmaf(x[u][k], x[u][k], na);
+                    nb = fmaf(y[u][k], y[u][k], nb);
+                }
         }
         dot = warp_sum(dot);
         na = warp_sum(na);
@@ -158,11 +169,12 @@ router_dot_kernel(int n, int d, int b, const T* __restrict__ h, int64_t ldh, con
 
 // p[t] = sigmoid(sum_c w_up[c] * SiLU(dots[t][c] / rms_t + b_down[c]) + b_up),
 // rms_t = sqrt(sumsq[t] / d + eps): one warp per token. Shared with the
-// tensor-core path, which produces the same dots/sumsq.
+// tensor-core path, which accumulates into dots/sumsq: both are cleared here
+// after use, so that the workspace is ready for the next call.
 template <typename T>
 __global__ void __launch_bounds__(GATE_WARPS * 32)
-router_finalize_kernel(int n, int d, int b, float eps, const float* __restrict__ dots,
-                       const float* __restrict__ sumsq, const float* __restrict__ b_down,
+router_finalize_kernel(int n, int d, int b, float eps, float* __restrict__ dots,
+                       float* __restrict__ sumsq, const float* __restrict__ b_down,
                        const T* __restrict__ w_up, const float* __restrict__ b_up, float thr, int rule,
                        bool need_flag, float* __restrict__ score, uint8_t* __restrict__ mask,
                        int32_t* __restrict__ flag, void* ws) {
@@ -170,9 +182,12 @@ router_finalize_kernel(int n, int d, int b, float eps, const float* __restrict__
     float wmin = INFINITY;
     for (int t = blockIdx.x * GATE_WARPS + warp; t < n; t += gridDim.x * GATE_WARPS) {
         const float r = 1.0f / sqrtf(sumsq[t] / static_cast<float>(d) + eps);
+        __syncwarp();
+        if (lane == 0) sumsq[t] = 0.f;
         float z = 0.f;
         for (int c = lane; c < b; c += 32) {
             float u = dots[static_cast<int64_t>(t) * b + c] * r;
+            dots[static_cast<int64_t>(t) * b + c] = 0.f;
             if (b_down) u += b_down[c];
             const float silu = u / (1.0f + expf(-u));
             z = fmaf(to_f32(w_up[c]), silu, z);

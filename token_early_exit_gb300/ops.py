@@ -94,9 +94,9 @@ def exit_gate(h_cur: torch.Tensor, threshold: float, *, h_prev: Optional[torch.T
         _mat(w_down, "w_down")
         _vec(w_up, "w_up")
     out = out or {}
-    score = out.get("score", torch.empty(n, dtype=torch.float32, device=h_cur.device))
-    mask = out.get("mask", torch.empty(n, dtype=torch.uint8, device=h_cur.device))
-    flag = out.get("flag", torch.empty(1, dtype=torch.int32, device=h_cur.device))
+    score = out["score"] if "score" in out else torch.empty(n, dtype=torch.float32, device=h_cur.device)
+    mask = out["mask"] if "mask" in out else torch.empty(n, dtype=torch.uint8, device=h_cur.device)
+    flag = out["flag"] if "flag" in out else torch.empty(1, dtype=torch.int32, device=h_cur.device)
     ws = ws or Workspace(h_cur.device)
     wp, wn = ws.get(lib.tee_exit_gate_workspace_size(ctypes.byref(desc), n))
     st = lib.tee_exit_gate(ctypes.byref(desc), n, _ptr(h_cur), h_cur.stride(0),
@@ -118,14 +118,17 @@ def exit_compact(mask: torch.Tensor, *, pos_in: Optional[torch.Tensor] = None, h
     dev = mask.device
     out = dict(out or {})
     for k in ("cont_rows", "exit_rows") + (("cont_pos", "exit_pos") if with_pos else ()):
-        out.setdefault(k, torch.empty(n, dtype=torch.int32, device=dev))
-    out.setdefault("counts", torch.empty(2, dtype=torch.int32, device=dev))
+        if k not in out:
+            out[k] = torch.empty(n, dtype=torch.int32, device=dev)
+    if "counts" not in out:
+        out["counts"] = torch.empty(2, dtype=torch.int32, device=dev)
     d, dt, ldi, ldc = 0, _lib.TEE_BF16, 0, 0
     if h is not None:
         _mat(h, "h")
         d = h.shape[1]
         dt = _DT[h.dtype]
-        out.setdefault("h_cont", torch.empty((n, d), dtype=h.dtype, device=dev))
+        if "h_cont" not in out:
+            out["h_cont"] = torch.empty((n, d), dtype=h.dtype, device=dev)
         ldi, ldc = h.stride(0), out["h_cont"].stride(0)
     ws = ws or Workspace(dev)
     wp, wn = ws.get(lib.tee_exit_compact_workspace_size(n))
