@@ -109,7 +109,7 @@ typedef struct {
     int32_t rule;        /* TEE_RULE_PER_TOKEN or TEE_RULE_BATCH_ALL */
     int32_t dtype;       /* element type of h_cur, h_prev, gamma, w_down, w_up */
     int32_t d;           /* hidden size */
-    int32_t bottleneck;  /* router width b (128 in TIDE); ignored by the cosine gate */
+    int32_t bottleneck;  /* router width b (128 in TIDE, at most 256); ignored by the cosine gate */
     float threshold;     /* tau (cosine) or theta (router); exit iff score > threshold */
     float eps;           /* RMSNorm epsilon of the router */
 } tee_gate_desc;

@@ -225,8 +225,8 @@ def test_tc_fill_full_prefill_workload(tee, cfg):
 
 
 # ---------------------------------------------------------------- decode path
-# int4 fills of up to 128 items with an identity map run as one tcgen05 launch
-# (dequantised weights as the A operand, K split across blocks).
+# int4 fills of up to 128 items with an identity map run as one tcgen05 launch:
+# one block per (64 output columns, layer), weights dequantised into the B operand.
 
 @pytest.mark.parametrize("n,hd", [(1, 64), (17, 64), (100, 64), (128, 64), (48, 128)])
 def test_decode_int4_fill_item_counts(tee, n, hd):
@@ -267,3 +267,20 @@ def test_decode_int4_fill_records_bad_positions(tee):
     assert code == 2 and detail == -1
     good = np.array([r for r in range(cfg.batch) if r != 5], dtype=np.int32)
     check_decode_fill(cfg, x, good, pos.cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL)
+
+
+# Shapes around the decode kernel's limits: d a multiple of 512 (one staged chunk of
+# codes) takes the tcgen05 launch, fewer or more chunks than its four-chunk ring; other
+# d go to the generic path. Same results either way.
+@pytest.mark.parametrize("S,d,hd,n", [(8, 2048, 64, 64), (4, 1024, 128, 33), (1, 256, 64, 5), (3, 768, 64, 64),
+                                      (8, 512, 128, 1), (2, 512, 64, 64), (2, 4096, 128, 128), (1, 5120, 128, 77),
+                                      (2, 1536, 64, 100)])
+def test_decode_shapes(tee, S, d, hd, n):
+    base = configs.LLAMA1B_DECODE
+    cfg = configs.DecodeConfig(**{**base.__dict__, "d": d, "batch": n, "head_dim": hd, "n_kv_heads": 512 // hd,
+                                  "n_layers": S, "fill_layers": tuple(range(S))})
+    x = gen.decode_inputs(cfg, seed=S * 100 + n, device=DEV, case="exit")
+    f = _make(tee, cfg, x["layers"], torch.bfloat16, cfg.cache_len, int4=True)
+    rows = np.random.default_rng(n).permutation(n).astype(np.int32)
+    f(x["h_cur"], x["k_cache"], x["v_cache"], rows=torch.from_numpy(rows).to(DEV), pos=x["pos"], seq=x["seq"])
+    check_decode_fill(cfg, x, rows, x["pos"].cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL)

@@ -2,23 +2,26 @@
 // group-64 weights (River-LLM's W4A16 exit layers), identity map (the
 // "State Propagation" / identity-fill input).
 //
-// One launch, one CTA per (head of K or V, filled layer). On tcgen05:
-//   D[item][c] = sum_k h[row(item)][k] * W'[k][c],  M = 128 item rows,
-//   N = head_dim columns, K = d,   W'[k][c] = (q - zero) * scale * g_j[k]
-// so that D / rms(h) is layer j's K (or V) head for each item; the RMSNorm
-// weight g_j is folded into the dequantised weights.
-//
-// Shared memory holds an 8-slot ring of raw inputs per 64-wide K block, filled
-// six blocks ahead with cp.async: the gathered h rows land directly in the
-// 128-byte-swizzled K-major A operand layout (rows past the items read as
-// zero), next to the block's int4 codes, fp16 scales/zeros and g_j. Per block,
-// warps 0-3 dequantise the codes into the B operand (bf16, swizzled, double
-// buffered) while warps 4-7 add up sum(h^2) of their item row from the staged
-// A tile; one thread then issues four tcgen05.mma (K = 16) and commits to the
-// slot's barrier, which frees both the slot and the B buffer. After the last
-// block each epilogue thread owns one item row of the TMEM accumulator, i.e. a
-// whole head: it applies 1/rms and RoPE (pairs i, i + hd/2) in registers and
-// stores the head row into the backbone's cache slot.
+// One launch, one CTA per (group of 64 output columns, filled layer). The 64
+// columns are two 32-wide segments [i, i+32) and [i+hd/2, i+hd/2+32) of one K
+// or V head, so that RoPE pairs stay inside the CTA. On tcgen05:
+//   D[item][c] = sum_k h[row(item)][k] * W'[k][c],  M = 128 item rows (rows
+//   past the items are zero), N = 64 columns, K = d, with
+//   W'[k][c] = (q - zero) * scale * g_j[k]
+// so that D / rms(h) is layer j's K or V for each item (RMSNorm weight folded
+// into the dequantised weights). Warp roles, synchronised by mbarriers only:
+//   warps 0-7  stream the int4 codes, fp16 scales/zeros and g_j in 512-k chunks
+//              (cp.async, a 4-chunk ring: for d <= 2048 everything is in
+//              flight at once) and dequantise each 64-k block into a ring of
+//              bf16 B operands (128-byte swizzle), running ahead of the MMAs;
+//   warp 8     streams the gathered h rows of each 64-k block into a ring of A
+//              operands three blocks ahead, releases a block once its copies
+//              have landed (and are fenced for the tensor core), adds up
+//              sum(h^2) per item, and fetches the items' RoPE rows;
+//   warp 9     issues tcgen05.mma into a 64-column TMEM accumulator and frees
+//              the ring slots with tcgen05.commit.
+// Epilogue (warps 0-3, one item row each): 1/rms, RoPE in registers, store of
+// the two 32-wide segments into the backbone's cache slot.
 #include "fill.cuh"
 #include "tc.cuh"
 
@@ -28,17 +31,45 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int DKB = 64;            // K per block: one int4 group, one 128-byte swizzle row of bf16
-constexpr int RING = 8;            // raw-input slots
-constexpr int AHEAD = RING - 2;    // blocks in flight ahead of the one being consumed
-constexpr int THREADS_D = 256;
-constexpr int MAX_ITEMS = 128;     // MMA M
-constexpr uint32_t A_SLOT = MAX_ITEMS * DKB * 2;   // 16 KB
+constexpr int D_COLS = 64;           // output columns per CTA
+constexpr int D_KB = 64;             // K per MMA block (one int4 group)
+constexpr int D_CHUNK = 512;         // K per staged chunk of codes
+constexpr int D_RA = 4;              // A operand slots (h rows)
+constexpr int D_LAG = D_RA - 1;      // blocks in flight ahead of the one released
+constexpr int D_RB = 3;              // B operand slots (dequantised weights)
+constexpr int D_RC = 4;              // code chunks in the ring
+constexpr int D_MAX_ITEMS = 128;
+constexpr int D_DEQ_WARPS = 8, D_HROW_WARP = 8, D_MMA_WARP = 9;
+constexpr int D_THREADS = 10 * 32;
+constexpr int D_CROW = D_COLS + 16;  // staged bytes per packed-code row (padding spreads the banks)
 
+constexpr uint32_t A_SLOT = 128 * 128;                                   // 16 KB
+constexpr uint32_t B_SLOT = D_COLS * 128;                                // 8 KB
+constexpr uint32_t CHUNK_CODES = (D_CHUNK / 2) * D_CROW;                 // 20 KB
+constexpr uint32_t CHUNK_SZ = (D_CHUNK / D_KB) * 256;                    // scale[64], zero[64] per group: 2 KB
+constexpr uint32_t CHUNK_G = D_CHUNK * 2;                                // 1 KB
+constexpr uint32_t CHUNK_BYTES = CHUNK_CODES + CHUNK_SZ + CHUNK_G;
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + D_RA * A_SLOT;
+constexpr uint32_t OFF_C = OFF_B + D_RB * B_SLOT;
+constexpr uint32_t OFF_ROPE = OFF_C + D_RC * CHUNK_BYTES;                // float2 [item][32]
+constexpr uint32_t OFF_SMALL = OFF_ROPE + D_MAX_ITEMS * 256;
+constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * D_RB + 2) * 8 + D_MAX_ITEMS * (8 + 4 + 4 + 4) + 16;
+constexpr size_t D_SMEM = 1024 + OFF_SMALL + SMALL_BYTES;
+static_assert(D_SMEM <= 232448, "decode fill shared memory");
+
+struct DecodeLayer {
+    const uint8_t* codes[2];   // wk, wv
+    const __half* scale[2];
+    const __half* zero[2];
+    const bf16* gamma;
+    int cache_layer;
+};
+constexpr int MAX_DECODE_LAYERS = 64;
 struct DecodeArgs {
-    int n_max;
+    DecodeLayer l[MAX_DECODE_LAYERS];
+    int n_max, d, kvw, hd, half, n_kv, groups_per_head;
     const int32_t* n_dev;
-    int d, kvw, hd, half, group, n_kv;
     float inv_d, eps;
     const bf16* h;
     int64_t ld_h;
@@ -52,23 +83,6 @@ struct DecodeArgs {
     bf16* kc;
     bf16* vc;
     tee_cache_layout cl;
-    uint32_t slot_bytes, codes_off, sz_off, g_off;   // layout of one ring slot
-};
-
-struct DecodeLayer {
-    const uint8_t* wk;
-    const uint8_t* wv;
-    const __half* k_scale;
-    const __half* k_zero;
-    const __half* v_scale;
-    const __half* v_zero;
-    const bf16* gamma;
-    int cache_layer;
-};
-
-constexpr int MAX_DECODE_LAYERS = 64;
-struct DecodeLayers {
-    DecodeLayer l[MAX_DECODE_LAYERS];
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -81,63 +95,101 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-
+__device__ __forceinline__ void deq_bar_sync() {   // the eight dequantising warps only
+    asm volatile("bar.sync 1, %0;" ::"n"(D_DEQ_WARPS * 32) : "memory");
+}
 __device__ __forceinline__ float nibble_f32(uint32_t q) {
     // exact small integer as fp32: (2^23 + q) - 2^23
     return __uint_as_float(0x4B000000u | q) - 8388608.0f;
 }
 
-__global__ void __launch_bounds__(THREADS_D, 1)
-fill_decode_kernel(DecodeArgs a, const __grid_constant__ DecodeLayers layers, void* ws) {
+__global__ void __launch_bounds__(D_THREADS, 1)
+fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int N = a.hd;                                   // columns of this CTA (one head)
-    uint8_t* ring = smem;                                 // RING slots of a.slot_bytes
-    uint8_t* wb[2] = {smem + RING * a.slot_bytes, smem + RING * a.slot_bytes + N * 128};
-    // Small arrays after the operands, widest first so that each stays aligned.
-    uint64_t* done = reinterpret_cast<uint64_t*>(wb[1] + N * 128);       // [RING]
-    int64_t* s_off = reinterpret_cast<int64_t*>(done + RING);            // [MAX_ITEMS] cache offset or -1
-    int* s_row = reinterpret_cast<int*>(s_off + MAX_ITEMS);              // [MAX_ITEMS] source row or -1
-    int* s_pos = s_row + MAX_ITEMS;                                      // [MAX_ITEMS]
-    float* s_ss = reinterpret_cast<float*>(s_pos + MAX_ITEMS);           // [MAX_ITEMS]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_ss + MAX_ITEMS);
-    int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);                // [0] abort
+    uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + OFF_SMALL);
+    uint64_t* a_empty = a_full + D_RA;
+    uint64_t* b_full = a_empty + D_RA;
+    uint64_t* b_empty = b_full + D_RB;
+    uint64_t* acc_full = b_empty + D_RB;
+    uint64_t* ss_ready = acc_full + 1;
+    int64_t* s_off = reinterpret_cast<int64_t*>(ss_ready + 1);        // cache offset of the item row or -1
+    int* s_row = reinterpret_cast<int*>(s_off + D_MAX_ITEMS);
+    int* s_pos = s_row + D_MAX_ITEMS;
+    float* s_ss = reinterpret_cast<float*>(s_pos + D_MAX_ITEMS);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_ss + D_MAX_ITEMS);
+    int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);
     volatile int* abort = s_flags;
 
-    const int head2 = blockIdx.x, li = blockIdx.y;
-    const DecodeLayer& L = layers.l[li];
-    const bool is_k = head2 < a.n_kv;
-    const int head = is_k ? head2 : head2 - a.n_kv;
-    const int col0 = head * a.hd;
-    const uint8_t* codes = is_k ? L.wk : L.wv;
-    const __half* scale = is_k ? L.k_scale : L.v_scale;
-    const __half* zero = is_k ? L.k_zero : L.v_zero;
+    const int grp = blockIdx.x, li = blockIdx.y;
+    const DecodeLayer& L = a.l[li];
+    const bool is_k = grp < a.n_kv * a.groups_per_head;
+    const int kv = is_k ? 0 : 1;
+    const int gi = is_k ? grp : grp - a.n_kv * a.groups_per_head;
+    const int head = gi / a.groups_per_head, seg = gi % a.groups_per_head;
+    const int col_lo = head * a.hd + 32 * seg, col_hi = col_lo + a.half;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = min(item_count(a.n_max, a.n_dev), MAX_ITEMS);
-    const uint32_t tmem_cols = N <= 64 ? 64 : 128;
-    const int nkb = a.d / DKB;
+    const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
+    const int nkb = a.d / D_KB, nchunks = a.d / D_CHUNK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < RING; ++s) tc::mbar_init(&done[s], 1);
+        for (int s = 0; s < D_RA; ++s) {
+            tc::mbar_init(&a_full[s], 1);
+            tc::mbar_init(&a_empty[s], 1);
+        }
+        for (int s = 0; s < D_RB; ++s) {
+            tc::mbar_init(&b_full[s], D_DEQ_WARPS);
+            tc::mbar_init(&b_empty[s], 1);
+        }
+        tc::mbar_init(acc_full, 1);
+        tc::mbar_init(ss_ready, 1);
         s_flags[0] = 0;
         tc::fence_barrier_init();
     }
-    // Per-item metadata: source row, cache offset (validated once per item).
-    for (int i = threadIdx.x; i < MAX_ITEMS; i += THREADS_D) {
+    // Chunk c of codes / scales / zeros / g into ring slot c % D_RC (dequant warps).
+    auto load_chunk = [&](int c) {
+        uint8_t* base = smem + OFF_C + (c % D_RC) * CHUNK_BYTES;
+        const int kp0 = c * (D_CHUNK / 2), g0 = c * (D_CHUNK / D_KB);
+        for (int u = threadIdx.x; u < (D_CHUNK / 2) * 4; u += D_DEQ_WARPS * 32) {
+            const int r = u >> 2, part = u & 3;        // packed row, 16-byte piece (lo 2, hi 2)
+            const int col = (part < 2 ? col_lo : col_hi) + (part & 1) * 16;
+            cp_async16(base + r * D_CROW + part * 16, L.codes[kv] + static_cast<int64_t>(kp0 + r) * a.kvw + col, true);
+        }
+        for (int u = threadIdx.x; u < (D_CHUNK / D_KB) * 16 + D_CHUNK / 8; u += D_DEQ_WARPS * 32) {
+            if (u < (D_CHUNK / D_KB) * 16) {
+                const int g = u >> 4, part = u & 15, which = part >> 3, p = part & 7;
+                const int col = (p < 4 ? col_lo : col_hi) + (p & 3) * 8;
+                const __half* src = (which ? L.zero[kv] : L.scale[kv]) + static_cast<int64_t>(g0 + g) * a.kvw + col;
+                cp_async16(base + CHUNK_CODES + g * 256 + which * 128 + p * 16, src, true);
+            } else {
+                const int p = u - (D_CHUNK / D_KB) * 16;
+                cp_async16(base + CHUNK_CODES + CHUNK_SZ + p * 16, L.gamma + c * D_CHUNK + p * 8, true);
+            }
+        }
+    };
+    if (warp < D_DEQ_WARPS) {
+        for (int c = 0; c < D_RC; ++c) {
+            if (c < nchunks) load_chunk(c);
+            cp_async_commit();
+        }
+    }
+    // Per-item metadata: source row, position, cache offset (validated once per item).
+    for (int i = threadIdx.x; i < D_MAX_ITEMS; i += D_THREADS) {
         int r = -1, p = 0;
         int64_t off = -1;
         if (i < n) {
             r = a.rows ? a.rows[i] : i;
             if (r < 0 || r >= a.h_rows) {
-                if (head2 == 0 && li == 0) record_fault(ws, TEE_DEVERR_ROW, r);
+                if (grp == 0 && li == 0) record_fault(ws, TEE_DEVERR_ROW, r);
                 r = -1;
             } else {
                 p = a.pos ? a.pos[r] : a.pos0 + r;
                 const int sq = a.seq ? a.seq[r] : 0;
                 if (!pos_ok(p, a.cl.max_pos, a.hdr)) {
-                    if (head2 == 0 && li == 0) record_fault(ws, TEE_DEVERR_POS, p);
+                    if (grp == 0 && li == 0) record_fault(ws, TEE_DEVERR_POS, p);
+                    p = 0;
                 } else if (sq < 0 || sq >= a.cl.n_seq) {
-                    if (head2 == 0 && li == 0) record_fault(ws, TEE_DEVERR_SEQ, sq);
+                    if (grp == 0 && li == 0) record_fault(ws, TEE_DEVERR_SEQ, sq);
                 } else {
                     off = L.cache_layer * a.cl.s_layer + sq * a.cl.s_seq + head * a.cl.s_head +
                           static_cast<int64_t>(p) * a.cl.s_pos;
@@ -148,173 +200,187 @@ fill_decode_kernel(DecodeArgs a, const __grid_constant__ DecodeLayers layers, vo
         s_pos[i] = p;
         s_off[i] = off;
     }
-    if (warp == 0) tc::tmem_alloc(tmem_slot, tmem_cols);
+    // A rows past the items stay zero in every slot (the MMA reads 128 rows).
+    for (int u = threadIdx.x; u < D_RA * (128 - n) * 8; u += D_THREADS) {
+        const int s = u / ((128 - n) * 8), rem = u % ((128 - n) * 8);
+        *reinterpret_cast<uint4*>(smem + OFF_A + s * A_SLOT + (n + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
+            make_uint4(0, 0, 0, 0);
+    }
+    if (warp == D_MMA_WARP) tc::tmem_alloc(tmem_slot, D_COLS);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // Issue the cp.async copies of K block kb into its ring slot.
-    auto prefetch = [&](int kb) {
-        uint8_t* slot = ring + (kb % RING) * a.slot_bytes;
-        // A: the item rows x 8 chunks of 16 bytes, swizzled (chunk j of row r at j ^ (r & 7)).
-        // Rows from n to 127 were zeroed once and are never written.
-        for (int u = threadIdx.x; u < n * 8; u += THREADS_D) {
-            const int r = u >> 3, j = u & 7;
-            const int src_row = s_row[r];
-            const bf16* src = a.h + static_cast<int64_t>(src_row < 0 ? 0 : src_row) * a.ld_h + kb * DKB + j * 8;
-            cp_async16(slot + r * 128 + ((j ^ (r & 7)) << 4), src, src_row >= 0);
-        }
-        // int4 codes: 32 packed rows x N bytes.
-        const int cchunks = N / 16;
-        for (int u = threadIdx.x; u < 32 * cchunks; u += THREADS_D) {
-            const int r = u / cchunks, j = u % cchunks;
-            cp_async16(slot + a.codes_off + r * N + j * 16,
-                       codes + static_cast<int64_t>(kb * 32 + r) * a.kvw + col0 + j * 16, true);
-        }
-        // scale and zero of this group (N fp16 each), g_j for these 64 k.
-        const int schunks = N * 2 / 16;
-        const int64_t gi = static_cast<int64_t>(kb * DKB / a.group) * a.kvw + col0;
-        for (int u = threadIdx.x; u < 2 * schunks + 8; u += THREADS_D) {
-            if (u < schunks)
-                cp_async16(slot + a.sz_off + u * 16, scale + gi + u * 8, true);
-            else if (u < 2 * schunks)
-                cp_async16(slot + a.sz_off + N * 2 + (u - schunks) * 16, zero + gi + (u - schunks) * 8, true);
-            else
-                cp_async16(slot + a.g_off + (u - 2 * schunks) * 16, L.gamma + kb * DKB + (u - 2 * schunks) * 8, true);
-        }
-    };
-
-    // Zero the A rows past the items in every ring slot (the MMA always reads 128 rows).
-    for (int u = threadIdx.x; u < RING * (MAX_ITEMS - n) * 8; u += THREADS_D) {
-        const int slot = u / ((MAX_ITEMS - n) * 8), rem = u % ((MAX_ITEMS - n) * 8);
-        *reinterpret_cast<uint4*>(ring + slot * a.slot_bytes + (n + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
-            make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
-    for (int kb = 0; kb < AHEAD; ++kb) {
-        if (kb < nkb) prefetch(kb);
-        cp_async_commit();
-    }
-    float ss = 0.f;                       // partial sum(h^2): item row threadIdx.x >> 1, chunks of one half
-    const uint32_t idesc = tc::idesc_bf16(MAX_ITEMS, N);
-    bool ok = true;
-    for (int kb = 0; kb < nkb; ++kb) {
-        // Refill the slot of block kb-2 with block kb+AHEAD once the MMA of kb-2 is done.
-        bool w = true;
-        if (kb >= 2) w = tc::mbar_wait(&done[(kb - 2) % RING], ((kb - 2) / RING) & 1, abort, ws, 21);
-        if (w && kb + AHEAD < nkb) prefetch(kb + AHEAD);
-        cp_async_commit();
-        cp_async_wait<AHEAD>();           // block kb has landed (this thread's copies)
-        if (!__syncthreads_and(w)) {      // ... and everyone else's; leave together on a timeout
-            ok = false;
-            break;
-        }
-        const uint8_t* slot = ring + (kb % RING) * a.slot_bytes;
-        {
-            // Dequantise N columns x 64 k into the B operand: unit = 4 columns x 8 k, all warps.
-            const int units = N / 4 * 8;
-            for (int u = threadIdx.x; u < units; u += THREADS_D) {
-                const int cg = (u >> 5) * 4 + (u & 3);     // column group (4 columns)
-                const int kc = (u & 31) >> 2;              // 8 k values
-                uint32_t w4[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    w4[r] = *reinterpret_cast<const uint32_t*>(slot + a.codes_off + (4 * kc + r) * N + 4 * cg);
-                const uint2 s4 = *reinterpret_cast<const uint2*>(slot + a.sz_off + cg * 8);
-                const uint2 z4 = *reinterpret_cast<const uint2*>(slot + a.sz_off + N * 2 + cg * 8);
-                const uint4 g8 = *reinterpret_cast<const uint4*>(slot + a.g_off + kc * 16);
-                float sc[4], zs[4], g[8];
+    if (warp < D_DEQ_WARPS) {
+        // ---- dequantise: unit = 4 columns x 4 k, 256 units per 64-k block
+        const int v = threadIdx.x;
+        const int cg = ((v >> 5) & 3) * 4 + (v & 3);              // column group (4 columns)
+        const int kq = (v >> 7) * 8 + ((v >> 2) & 7);             // k quad: 4kq .. 4kq+3
+        bool ok = true;
+        // Every dequantising warp runs every chunk iteration (the named barriers must
+        // match); after a timed-out wait a warp only skips the work.
+        for (int c = 0; c < nchunks; ++c) {
+            cp_async_wait<D_RC - 1>();                            // chunk c has landed (own copies)
+            deq_bar_sync();                                       // ... and everyone's
+            const uint8_t* base = smem + OFF_C + (c % D_RC) * CHUNK_BYTES;
+            for (int b = 0; b < D_CHUNK / D_KB && ok; ++b) {
+                const int kb = c * (D_CHUNK / D_KB) + b, s = kb % D_RB;
+                if (kb >= D_RB && !tc::mbar_wait(&b_empty[s], ((kb / D_RB) - 1) & 1, abort, ws, 51)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* crow = base + (b * 32 + 2 * kq) * D_CROW + 4 * cg;
+                const uint32_t w0 = *reinterpret_cast<const uint32_t*>(crow);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t*>(crow + D_CROW);
+                const uint8_t* szp = base + CHUNK_CODES + b * 256;
+                const uint2 s4 = *reinterpret_cast<const uint2*>(szp + cg * 8);
+                const uint2 z4 = *reinterpret_cast<const uint2*>(szp + 128 + cg * 8);
+                const uint2 g4 = *reinterpret_cast<const uint2*>(base + CHUNK_CODES + CHUNK_SZ + (b * D_KB + 4 * kq) * 2);
+                float sc[4], zs[4], g[4];
                 unpack_f16x2(s4.x, sc[0], sc[1]);
                 unpack_f16x2(s4.y, sc[2], sc[3]);
                 unpack_f16x2(z4.x, zs[0], zs[1]);
                 unpack_f16x2(z4.y, zs[2], zs[3]);
-                unpack_bf16x2(g8.x, g[0], g[1]);
-                unpack_bf16x2(g8.y, g[2], g[3]);
-                unpack_bf16x2(g8.z, g[4], g[5]);
-                unpack_bf16x2(g8.w, g[6], g[7]);
+                unpack_bf16x2(g4.x, g[0], g[1]);
+                unpack_bf16x2(g4.y, g[2], g[3]);
+                uint8_t* bslot = smem + OFF_B + s * B_SLOT;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float szj = zs[j] * sc[j];
-                    uint32_t packed[4];
+                    const uint32_t b0 = (w0 >> (8 * j)) & 0xFFu, b1 = (w1 >> (8 * j)) & 0xFFu;
+                    // (q - z) * s * g  as  (q * s - z * s) * g
+                    const float x0 = fmaf(nibble_f32(b0 & 0xFu), sc[j], -szj) * g[0];
+                    const float x1 = fmaf(nibble_f32(b0 >> 4), sc[j], -szj) * g[1];
+                    const float x2 = fmaf(nibble_f32(b1 & 0xFu), sc[j], -szj) * g[2];
+                    const float x3 = fmaf(nibble_f32(b1 >> 4), sc[j], -szj) * g[3];
+                    const int col = 4 * cg + j, kc = kq >> 1;
+                    *reinterpret_cast<uint2*>(bslot + col * 128 + ((kc ^ (col & 7)) << 4) + ((kq & 1) << 3)) =
+                        make_uint2(pack_bf16x2(x0, x1), pack_bf16x2(x2, x3));
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&b_full[s]);
+            }
+            deq_bar_sync();                                       // everyone is done with chunk c
+            if (c + D_RC < nchunks) load_chunk(c + D_RC);
+            cp_async_commit();
+        }
+    } else if (warp == D_HROW_WARP) {
+        // ---- h rows: block kb into A slot kb % D_RA; release block kb - D_LAG.
+        if (is_k)
+            for (int u = lane; u < n * 16; u += 32) {
+                const int i = u >> 4, p = u & 15;
+                cp_async16(smem + OFF_ROPE + i * 256 + p * 16,
+                           a.rope + static_cast<int64_t>(s_pos[i]) * a.half + 32 * seg + p * 2, true);
+            }
+        cp_async_commit();
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};   // items lane + 32q
+        auto release = [&](int j) {
+            // Block j's copies (and everything before them) have landed for this warp.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            const uint8_t* slot = smem + OFF_A + (j % D_RA) * A_SLOT;
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const uint32_t byte = (w4[r] >> (8 * j)) & 0xFFu;
-                        // (q - z) * s * g  as  (q * s - z * s) * g
-                        const float lo = fmaf(nibble_f32(byte & 0xFu), sc[j], -szj) * g[2 * r];
-                        const float hi = fmaf(nibble_f32(byte >> 4), sc[j], -szj) * g[2 * r + 1];
-                        packed[r] = pack_bf16x2(lo, hi);
-                    }
-                    const int c = 4 * cg + j;
-                    *reinterpret_cast<uint4*>(wb[kb & 1] + c * 128 + ((kc ^ (c & 7)) << 4)) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            for (int q = 0; q < 4; ++q) {
+                const int i = lane + 32 * q;
+                if (i >= n) break;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(slot + i * 128 + (((jj + i) & 7) << 4));
+                    float f[8];
+                    unpack_bf16x2(x.x, f[0], f[1]);
+                    unpack_bf16x2(x.y, f[2], f[3]);
+                    unpack_bf16x2(x.z, f[4], f[5]);
+                    unpack_bf16x2(x.w, f[6], f[7]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss[q] = fmaf(f[e], f[e], ss[q]);
                 }
             }
-            // sum(h^2): two threads per item row, four 16-byte chunks each.
-            const int r = threadIdx.x >> 1;
-            if (r < n) {
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int j = (threadIdx.x & 1) * 4 + jj;
-                    const uint4 v = *reinterpret_cast<const uint4*>(slot + r * 128 + (j << 4));
-                    float x[8];
-                    unpack_bf16x2(v.x, x[0], x[1]);
-                    unpack_bf16x2(v.y, x[2], x[3]);
-                    unpack_bf16x2(v.z, x[4], x[5]);
-                    unpack_bf16x2(v.w, x[6], x[7]);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) ss = fmaf(x[q], x[q], ss);
-                }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&a_full[j % D_RA]);
+        };
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % D_RA;
+            if (kb >= D_RA && !tc::mbar_wait(&a_empty[s], ((kb / D_RA) - 1) & 1, abort, ws, 52)) {
+                ok = false;
+                break;
+            }
+            uint8_t* slot = smem + OFF_A + s * A_SLOT;
+            for (int u = lane; u < n * 8; u += 32) {
+                const int r = u >> 3, j = u & 7;
+                const int src = s_row[r];
+                cp_async16(slot + r * 128 + ((j ^ (r & 7)) << 4),
+                           a.h + static_cast<int64_t>(src < 0 ? 0 : src) * a.ld_h + kb * D_KB + j * 8, src >= 0);
+            }
+            cp_async_commit();
+            if (kb >= D_LAG) {
+                cp_async_wait<D_LAG>();
+                release(kb - D_LAG);
             }
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            tc::tc_fence_after();
-            const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(slot));
-            const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(wb[kb & 1]));
+        cp_async_wait<0>();
+        if (ok)
+            for (int j = max(0, nkb - D_LAG); j < nkb; ++j) release(j);
 #pragma unroll
-            for (int kk = 0; kk < DKB / 16; ++kk) tc::umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, kb | kk);
-            tc::umma_commit(&done[kb % RING]);
+        for (int q = 0; q < 4; ++q)
+            if (lane + 32 * q < D_MAX_ITEMS) s_ss[lane + 32 * q] = ss[q];
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_ss and the RoPE rows are ready
+    } else {
+        // ---- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_bf16(128, D_COLS);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int sa = kb % D_RA, sb = kb % D_RB;
+                if (!tc::mbar_wait(&a_full[sa], (kb / D_RA) & 1, abort, ws, 53)) break;
+                if (!tc::mbar_wait(&b_full[sb], (kb / D_RB) & 1, abort, ws, 54)) break;
+                tc::tc_fence_after();
+                const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(smem + OFF_A + sa * A_SLOT));
+                const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + OFF_B + sb * B_SLOT));
+#pragma unroll
+                for (int kk = 0; kk < D_KB / 16; ++kk) tc::umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, kb | kk);
+                tc::umma_commit(&a_empty[sa]);
+                tc::umma_commit(&b_empty[sb]);
+            }
+            tc::umma_commit(acc_full);
         }
     }
-    cp_async_wait<0>();
-    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
-    if ((threadIdx.x & 1) == 0 && (threadIdx.x >> 1) < MAX_ITEMS) s_ss[threadIdx.x >> 1] = ss;
-    if (ok && nkb > 0) ok = tc::mbar_wait(&done[(nkb - 1) % RING], ((nkb - 1) / RING) & 1, abort, ws, 22);
-    ok = __syncthreads_and(ok);
-    tc::tc_fence_after();
 
-    // Epilogue: warps 0-3, thread = item row = TMEM lane, one whole head in its columns.
-    if (warp < 4 && ok) {
+    // ---- epilogue: warps 0-3, thread = item row = TMEM lane
+    if (warp < 4) {
+        bool ok = tc::mbar_wait(acc_full, 0, abort, ws, 55);
+        ok = ok && tc::mbar_wait(ss_ready, 0, abort, ws, 56);
+        tc::tc_fence_after();
         const int i = warp * 32 + lane;
-        const bool valid = i < n && s_off[i] >= 0;
-        const float rs = valid ? 1.0f / sqrtf(s_ss[i] * a.inv_d + a.eps) : 0.f;
+        const bool valid = ok && i < n && s_off[i] >= 0;
         const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        bf16* dst = (is_k ? a.kc : a.vc) + (valid ? s_off[i] : 0);
-        const float2* cs = a.rope + static_cast<int64_t>(valid ? s_pos[i] : 0) * a.half;
-        for (int c = 0; c < a.half; c += 32) {
-            float lo[32], hi[32];
-            tc::tmem_ld32(tb + c, lo);
-            tc::tmem_ld32(tb + a.half + c, hi);
-            if (!valid) continue;
+        float lo[32], hi[32];
+        tc::tmem_ld32(tb, lo);
+        tc::tmem_ld32(tb + 32, hi);
+        if (valid) {
+            const float rs = 1.0f / sqrtf(s_ss[i] * a.inv_d + a.eps);
             if (is_k) {
+                const float2* cs = reinterpret_cast<const float2*>(smem + OFF_ROPE + i * 256);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float2 e = cs[c + j];
-                    const float x1 = lo[j] * rs, x2 = hi[j] * rs;
-                    lo[j] = x1 * e.x - x2 * e.y;
-                    hi[j] = x2 * e.x + x1 * e.y;
+                for (int c = 0; c < 32; ++c) {
+                    const float2 e = cs[c];
+                    const float x1 = lo[c] * rs, x2 = hi[c] * rs;
+                    lo[c] = x1 * e.x - x2 * e.y;
+                    hi[c] = x2 * e.x + x1 * e.y;
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    lo[j] *= rs;
-                    hi[j] *= rs;
+                for (int c = 0; c < 32; ++c) {
+                    lo[c] *= rs;
+                    hi[c] *= rs;
                 }
             }
-            uint4* o = reinterpret_cast<uint4*>(dst + c);
-            uint4* o2 = reinterpret_cast<uint4*>(dst + a.half + c);
+            bf16* dst = (is_k ? a.kc : a.vc) + s_off[i] + 32 * seg;
+            uint4* o = reinterpret_cast<uint4*>(dst);
+            uint4* o2 = reinterpret_cast<uint4*>(dst + a.half);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 o[q] = make_uint4(pack_bf16x2(lo[8 * q], lo[8 * q + 1]), pack_bf16x2(lo[8 * q + 2], lo[8 * q + 3]),
@@ -324,20 +390,23 @@ fill_decode_kernel(DecodeArgs a, const __grid_constant__ DecodeLayers layers, vo
             }
         }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
+    if (warp == D_MMA_WARP) tc::tmem_dealloc(tmem, D_COLS);
 }
 
 bool decode_eligible(const FillCall& fc) {
     const tee_fill_desc& D = *fc.desc;
-    if (D.dtype != TEE_BF16 || D.wfmt != TEE_W_INT4 || D.group != DKB) return false;
-    if (fc.n_max > MAX_ITEMS || fc.n_layers > MAX_DECODE_LAYERS) return false;
-    if (D.d % DKB || (D.head_dim != 64 && D.head_dim != 128)) return false;
+    if (D.dtype != TEE_BF16 || D.wfmt != TEE_W_INT4 || D.group != D_KB) return false;
+    if (fc.n_max > D_MAX_ITEMS || fc.n_layers > MAX_DECODE_LAYERS) return false;
+    if (D.d % D_CHUNK || (D.head_dim != 64 && D.head_dim != 128)) return false;
     if ((fc.ld_h * 2) % 16 || !aligned16(fc.h) || !aligned16(fc.k_cache) || !aligned16(fc.v_cache)) return false;
     const tee_cache_layout& cl = *fc.cache;
     if (cl.s_layer % 8 || cl.s_seq % 8 || cl.s_head % 8 || cl.s_pos % 8) return false;
+    const int kvw = D.n_kv_heads * D.head_dim;
+    if (kvw % 16) return false;
     for (int l = 0; l < fc.n_layers; ++l) {
         const tee_fill_layer& L = fc.layers[l];
         if (L.w_map) return false;
@@ -345,9 +414,7 @@ bool decode_eligible(const FillCall& fc) {
             !aligned16(L.v_scale) || !aligned16(L.v_zero) || !aligned16(L.gamma))
             return false;
     }
-    // 16-byte copies of codes rows (kvw bytes apart) and of fp16 scale rows (2*kvw bytes apart)
-    const int kvw = D.n_kv_heads * D.head_dim;
-    return kvw % 16 == 0;
+    return true;
 }
 
 }  // namespace
@@ -369,8 +436,8 @@ tee_status fill_decode_run(const FillCall& fc) {
     a.kvw = D.n_kv_heads * D.head_dim;
     a.hd = D.head_dim;
     a.half = D.head_dim / 2;
-    a.group = D.group;
     a.n_kv = D.n_kv_heads;
+    a.groups_per_head = a.half / 32;
     a.inv_d = 1.0f / static_cast<float>(D.d);
     a.eps = D.eps;
     a.h = static_cast<const bf16*>(fc.h);
@@ -386,27 +453,22 @@ tee_status fill_decode_run(const FillCall& fc) {
     a.kc = static_cast<bf16*>(fc.k_cache);
     a.vc = static_cast<bf16*>(fc.v_cache);
     a.cl = *fc.cache;
-    // ring slot: A operand (1024-aligned) | codes 32 x N | scale N, zero N (fp16) | g 64 (bf16)
-    a.codes_off = A_SLOT;
-    a.sz_off = a.codes_off + 32 * a.hd;
-    a.g_off = a.sz_off + 4 * a.hd;
-    a.slot_bytes = static_cast<uint32_t>(round_up(a.g_off + DKB * 2, 1024));
-    DecodeLayers ls{};
     for (int l = 0; l < fc.n_layers; ++l) {
         const tee_fill_layer& L = fc.layers[l];
-        ls.l[l] = DecodeLayer{static_cast<const uint8_t*>(L.wk), static_cast<const uint8_t*>(L.wv),
-                              static_cast<const __half*>(L.k_scale), static_cast<const __half*>(L.k_zero),
-                              static_cast<const __half*>(L.v_scale), static_cast<const __half*>(L.v_zero),
-                              static_cast<const bf16*>(L.gamma), L.cache_layer};
+        a.l[l] = DecodeLayer{{static_cast<const uint8_t*>(L.wk), static_cast<const uint8_t*>(L.wv)},
+                             {static_cast<const __half*>(L.k_scale), static_cast<const __half*>(L.v_scale)},
+                             {static_cast<const __half*>(L.k_zero), static_cast<const __half*>(L.v_zero)},
+                             static_cast<const bf16*>(L.gamma), L.cache_layer};
     }
-    // alignment slack | ring | two B buffers | small arrays (see the kernel's layout)
-    const size_t small = RING * 8 + MAX_ITEMS * (8 + 4 + 4 + 4) + 4 + 4 * 4;
-    const size_t smem = 1024 + RING * size_t(a.slot_bytes) + 2 * size_t(a.hd) * 128 + round_up(small, 16);
-    tee_status st = cuda_status(
-        cudaFuncSetAttribute(fill_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
-    if (st != TEE_OK) return st;
-    dim3 grid(2 * D.n_kv_heads, fc.n_layers);
-    fill_decode_kernel<<<grid, THREADS_D, smem, fc.stream>>>(a, ls, fc.ws);
+    static bool attr = false;
+    if (!attr) {
+        tee_status st = cuda_status(cudaFuncSetAttribute(fill_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         static_cast<int>(D_SMEM)));
+        if (st != TEE_OK) return st;
+        attr = true;
+    }
+    dim3 grid(2 * a.n_kv * a.groups_per_head, fc.n_layers);
+    fill_decode_kernel<<<grid, D_THREADS, D_SMEM, fc.stream>>>(a, fc.ws);
     return launch_status();
 }
 

@@ -180,17 +180,30 @@ router_finalize_kernel(int n, int d, int b, float eps, float* __restrict__ dots,
                        int32_t* __restrict__ flag, void* ws) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float wmin = INFINITY;
+    constexpr int MAXC = 8;  // channels per lane held in registers (b <= 256)
     for (int t = blockIdx.x * GATE_WARPS + warp; t < n; t += gridDim.x * GATE_WARPS) {
-        const float r = 1.0f / sqrtf(sumsq[t] / static_cast<float>(d) + eps);
+        // Issue every load of this token before using any of them.
+        float* row = dots + static_cast<int64_t>(t) * b;
+        const float ssq = sumsq[t];
+        float u[MAXC], wu[MAXC], bd[MAXC];
+#pragma unroll
+        for (int j = 0; j < MAXC; ++j) {
+            const int c = lane + 32 * j;
+            u[j] = c < b ? row[c] : 0.f;
+            wu[j] = c < b ? to_f32(w_up[c]) : 0.f;
+            bd[j] = (c < b && b_down) ? b_down[c] : 0.f;
+        }
         __syncwarp();
+#pragma unroll
+        for (int j = 0; j < MAXC; ++j)
+            if (lane + 32 * j < b) row[lane + 32 * j] = 0.f;   // leave the sums cleared for the next call
         if (lane == 0) sumsq[t] = 0.f;
+        const float r = 1.0f / sqrtf(ssq / static_cast<float>(d) + eps);
         float z = 0.f;
-        for (int c = lane; c < b; c += 32) {
-            float u = dots[static_cast<int64_t>(t) * b + c] * r;
-            dots[static_cast<int64_t>(t) * b + c] = 0.f;
-            if (b_down) u += b_down[c];
-            const float silu = u / (1.0f + expf(-u));
-            z = fmaf(to_f32(w_up[c]), silu, z);
+#pragma unroll
+        for (int j = 0; j < MAXC; ++j) {
+            const float x = u[j] * r + bd[j];
+            z = fmaf(wu[j], x / (1.0f + expf(-x)), z);
         }
         z = warp_sum(z);
         if (b_up) z += b_up[0];
@@ -298,7 +311,8 @@ extern "C" tee_status tee_exit_gate(const tee_gate_desc* g, int32_t n, const voi
     if (g->mode == TEE_GATE_COSINE) {
         if (!h_prev || ld_prev < g->d || !aligned16(h_prev) || (ld_prev * es) % 16) return TEE_ERR_INVALID_ARG;
     } else {
-        if (!w_down || !w_up || g->bottleneck <= 0 || !aligned16(w_down)) return TEE_ERR_INVALID_ARG;
+        if (!w_down || !w_up || g->bottleneck <= 0 || g->bottleneck > 256 || !aligned16(w_down))
+            return TEE_ERR_INVALID_ARG;
         if (gamma && !aligned16(gamma)) return TEE_ERR_INVALID_ARG;
         if (!(g->eps >= 0.f)) return TEE_ERR_INVALID_ARG;
     }

@@ -23,7 +23,9 @@ using bf16 = __nv_bfloat16;
 constexpr int RBM = 128, RBN = 128, RBK = 64, RSTAGES = 4;
 constexpr int RTHREADS = 6 * 32;
 constexpr uint32_t RA_BYTES = RBM * RBK * 2, RB_BYTES = RBN * RBK * 2, RSTAGE = RA_BYTES + RB_BYTES;
-constexpr size_t RSMEM = 1024 + size_t(RSTAGES) * RSTAGE + 256;
+constexpr int RSTAGE_LD = 132;  // floats per staged row (conflict-free 16-byte stores)
+constexpr uint32_t RSTAGING = 4 * 32 * RSTAGE_LD * 4;   // epilogue staging, its own region
+constexpr size_t RSMEM = 1024 + size_t(RSTAGES) * RSTAGE + RSTAGING + 256;
 // Smallest batch that goes to the tensor cores.
 constexpr int RTC_MIN_TOKENS = 256;
 
@@ -37,7 +39,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                  int kb_per_split, float* __restrict__ dots, float* __restrict__ sumsq, void* ws) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RSTAGES * RSTAGE);
+    float* staging = reinterpret_cast<float*>(smem + RSTAGES * RSTAGE);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RSTAGES * RSTAGE + RSTAGING);
     uint64_t* empty = full + RSTAGES;
     uint64_t* acc_full = empty + RSTAGES;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
@@ -130,7 +133,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const uint8_t* row = smem + stage * RSTAGE + r * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint4 v = *reinterpret_cast<const uint4*>(row + j * 16);
+                // rotate the chunk order by row: lanes of a warp hit 8 different bank groups
+                const uint4 v = *reinterpret_cast<const uint4*>(row + (((j + r) & 7) << 4));
                 float x[8];
                 unpack_bf16x2(v.x, x[0], x[1]);
                 unpack_bf16x2(v.y, x[2], x[3]);
@@ -152,16 +156,26 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         tc::tc_fence_after();
         const int t = m0 + r;
         if (ok) {
+            // Stage this warp's 32 rows in shared memory (row stride 132 floats keeps
+            // the 16-byte stores conflict-free), then add each row into dots with
+            // one 512-byte vector reduction per warp instruction.
+            float* stage = staging + warp * (32 * RSTAGE_LD);
             const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < RBN; c += 32) {
                 float v[32];
                 tc::tmem_ld32(tb + c, v);
-                if (t < n) {
-                    float* dst = dots + static_cast<int64_t>(t) * RBN + c;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) red_add_v4(dst + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                }
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4*>(stage + lane * RSTAGE_LD + c + 4 * q) =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+            __syncwarp();
+            for (int rr = 0; rr < 32; ++rr) {
+                const int tt = m0 + warp * 32 + rr;
+                if (tt >= n) break;
+                const float4 v = *reinterpret_cast<const float4*>(stage + rr * RSTAGE_LD + lane * 4);
+                red_add_v4(dots + static_cast<int64_t>(tt) * RBN + lane * 4, v.x, v.y, v.z, v.w);
             }
             if (t < n) atomicAdd(sumsq + t, ss);
         }
@@ -201,7 +215,8 @@ tee_status router_dots_tc(int n, int d, int b, int dtype, const void* h, int64_t
         attr = true;
     }
     const int m_tiles = (n + RBM - 1) / RBM, nkb = d / RBK;
-    int splits = (sm_count() + m_tiles - 1) / m_tiles;
+    // One wave: m_tiles * splits <= SMs (a second partial wave doubles the time).
+    int splits = sm_count() / m_tiles;
     if (splits > nkb) splits = nkb;
     if (splits > 16) splits = 16;
     if (splits < 1) splits = 1;
