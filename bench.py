@@ -469,50 +469,51 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     n_exit = w.n_exit()
 
-    # The step (and, separately, the dominant call) replay as CUDA graphs, so that
-    # the GPU is not left waiting for Python between kernels.
+    # The step (and, separately, the dominant call) replay as CUDA graphs. Each graph
+    # holds the L2 flush, then a timing event, the work, and a second timing event:
+    # the events run on the device inside the graph, so the interval is the work
+    # alone (kernels and the gaps between them), without the graph's own launch.
     fns, kidx = w.parts()
-    l0 = lib.tee_launch_count()
-    g_step = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_step):
-        for f in fns:
-            f()
-    k_step = lib.tee_launch_count() - l0
-    g_kern, k_kern = g_step, 0
-    if len(fns) > 1:
+
+    def capture(calls):
+        a = torch.cuda.Event(enable_timing=True, external=True)
+        b = torch.cuda.Event(enable_timing=True, external=True)
+        g = torch.cuda.CUDAGraph()
         l0 = lib.tee_launch_count()
-        g_kern = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_kern):
-            fns[kidx]()
-        k_kern = lib.tee_launch_count() - l0
+        with torch.cuda.graph(g):
+            flush.zero_()
+            a.record()
+            for f in calls:
+                f()
+            b.record()
+        return g, a, b, lib.tee_launch_count() - l0
+
+    g_step, sa, sb, k_step = capture(fns)
+    g_kern, ka, kb, k_kern = (capture([fns[kidx]]) if len(fns) > 1 else (None, None, None, 0))
     for _ in range(2):
         g_step.replay()
-        if g_kern is not g_step:
+        if g_kern is not None:
             g_kern.replay()
     torch.cuda.synchronize(dev)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = Clocks(dev.index)
     barrier(world)
     torch.cuda.synchronize(dev)
     clocks.start()
+    step_ms, kern_ms = [], []
     for i in range(args.steps):
-        flush.zero_()                      # evict L2 (outside the timed events)
-        ev[i][0].record(stream)
         g_step.replay()
-        ev[i][1].record(stream)
-        if g_kern is not g_step:
-            flush.zero_()
-            kev[i][0].record(stream)
+        torch.cuda.synchronize(dev)
+        step_ms.append(sa.elapsed_time(sb))
+        if g_kern is not None:
             g_kern.replay()
-            kev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+            torch.cuda.synchronize(dev)
+            kern_ms.append(ka.elapsed_time(kb))
     launches = args.steps * (k_step + k_kern)
     barrier(world)
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    kern_ms = [a.elapsed_time(b) for a, b in kev] if g_kern is not g_step else step_ms
+    if g_kern is None:
+        kern_ms = step_ms
     t_step = statistics.mean(step_ms)
     t_step = max_over_ranks(t_step, world, dev)
     value = world * w.units / (t_step * 1e-3)
@@ -562,7 +563,8 @@ def run_gpu(args):
             "e2e": {"value": world * w.units / (t_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": t_e2e},
             "gpu_launches": int(launches), "launches_per_step": int(k_step), "clocks": clk,
-            "timing": "CUDA-graph replay per step; L2 flushed before each replay",
+            "timing": "CUDA-graph replay per step; L2 flushed inside the graph before the step; "
+                      "timed by device events recorded inside the graph around the step",
             "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)}}
     if rank == 0:
         print(json.dumps(line))

@@ -6,20 +6,23 @@
 // columns are two 32-wide segments [i, i+32) and [i+hd/2, i+hd/2+32) of one K
 // or V head, so that RoPE pairs stay inside the CTA. On tcgen05:
 //   D[item][c] = sum_k h[row(item)][k] * W'[k][c],  M = 128 item rows (rows
-//   past the items are zero), N = 64 columns, K = d, with
+//   past the items hold whatever; their D rows are never stored), N = 64
+//   columns, K = d, with
 //   W'[k][c] = (q - zero) * scale * g_j[k]
 // so that D / rms(h) is layer j's K or V for each item (RMSNorm weight folded
 // into the dequantised weights). Warp roles, synchronised by mbarriers only:
-//   warps 0-7  stream the int4 codes, fp16 scales/zeros and g_j in 512-k chunks
-//              (cp.async, a 4-chunk ring: for d <= 2048 everything is in
-//              flight at once) and dequantise each 64-k block into a ring of
-//              bf16 B operands (128-byte swizzle), running ahead of the MMAs;
-//   warp 8     streams the gathered h rows of each 64-k block into a ring of A
-//              operands three blocks ahead, releases a block once its copies
-//              have landed (and are fenced for the tensor core), adds up
-//              sum(h^2) per item, and fetches the items' RoPE rows;
-//   warp 9     issues tcgen05.mma into a 64-column TMEM accumulator and frees
-//              the ring slots with tcgen05.commit.
+//   warps 0-7   stream the int4 codes, fp16 scales/zeros and g_j in 512-k
+//               chunks (cp.async, a 3-chunk ring) and dequantise each 64-k
+//               block into a ring of bf16 B operands (128-byte swizzle);
+//   warp 8      issues tcgen05.mma into a 64-column TMEM accumulator and frees
+//               the ring slots with tcgen05.commit;
+//   warps 9-12  gather the items' h rows of each 64-k block into a ring of A
+//               operands (cp.async, 128-byte swizzle), two blocks in flight,
+//               after asking L2 for the whole rows at the start; once a
+//               thread's copies of a block have landed it fences them for the
+//               tensor core and releases the block. They also fetch the
+//               items' positions, cache slots and RoPE rows;
+//   warps 13-14 add up sum(h^2) per item from each landed A block.
 // Epilogue (warps 0-3, one item row each): 1/rms, RoPE in registers, store of
 // the two 32-wide segments into the backbone's cache slot.
 #include "fill.cuh"
@@ -34,14 +37,19 @@ using bf16 = __nv_bfloat16;
 constexpr int D_COLS = 64;           // output columns per CTA
 constexpr int D_KB = 64;             // K per MMA block (one int4 group)
 constexpr int D_CHUNK = 512;         // K per staged chunk of codes
-constexpr int D_RA = 4;              // A operand slots (h rows)
-constexpr int D_LAG = D_RA - 1;      // blocks in flight ahead of the one released
+constexpr int D_RA = 6;              // A operand slots (h rows)
+constexpr int D_LAG = 2;             // blocks of h copies in flight
 constexpr int D_RB = 3;              // B operand slots (dequantised weights)
-constexpr int D_RC = 4;              // code chunks in the ring
+constexpr int D_RC = 3;              // code chunks in the ring
 constexpr int D_MAX_ITEMS = 128;
-constexpr int D_DEQ_WARPS = 8, D_HROW_WARP = 8, D_MMA_WARP = 9;
-constexpr int D_THREADS = 10 * 32;
+constexpr int D_DEQ_WARPS = 8, D_MMA_WARP = 8, D_CP_WARP0 = 9, D_CP_WARPS = 4, D_SS_WARP0 = 13, D_SS_WARPS = 2;
+constexpr int D_CP_THREADS = D_CP_WARPS * 32;
+constexpr int D_ITEMS_PER_CP = D_MAX_ITEMS * 8 / D_CP_THREADS;   // 16-byte pieces per thread and block
+constexpr int D_THREADS = (D_SS_WARP0 + D_SS_WARPS) * 32;
 constexpr int D_CROW = D_COLS + 16;  // staged bytes per packed-code row (padding spreads the banks)
+// A slot is refilled D_RA - D_LAG - 1 iterations after its release: slack for the MMA
+// and sum(h^2) round trip (mbarrier hand-offs cost ~0.1 us each).
+static_assert(D_LAG + 2 < D_RA, "the A ring needs slack beyond the blocks in flight");
 
 constexpr uint32_t A_SLOT = 128 * 128;                                   // 16 KB
 constexpr uint32_t B_SLOT = D_COLS * 128;                                // 8 KB
@@ -54,9 +62,10 @@ constexpr uint32_t OFF_B = OFF_A + D_RA * A_SLOT;
 constexpr uint32_t OFF_C = OFF_B + D_RB * B_SLOT;
 constexpr uint32_t OFF_ROPE = OFF_C + D_RC * CHUNK_BYTES;                // float2 [item][32]
 constexpr uint32_t OFF_SMALL = OFF_ROPE + D_MAX_ITEMS * 256;
-constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * D_RB + 2) * 8 + D_MAX_ITEMS * (8 + 4 + 4 + 4) + 16;
+constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * D_RB + 2) * 8 + D_MAX_ITEMS * (8 + 4) + 16;
 constexpr size_t D_SMEM = 1024 + OFF_SMALL + SMALL_BYTES;
 static_assert(D_SMEM <= 232448, "decode fill shared memory");
+static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_ROPE % 16 == 0 && OFF_SMALL % 8 == 0, "alignment");
 
 struct DecodeLayer {
     const uint8_t* codes[2];   // wk, wv
@@ -85,10 +94,8 @@ struct DecodeArgs {
     tee_cache_layout cl;
 };
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -102,6 +109,25 @@ __device__ __forceinline__ float nibble_f32(uint32_t q) {
     // exact small integer as fp32: (2^23 + q) - 2^23
     return __uint_as_float(0x4B000000u | q) - 8388608.0f;
 }
+// Lane 0 waits for the phase, the warp follows: every lane sees the same outcome,
+// so a timed-out wait cannot split a warp at a later __syncwarp or named barrier.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, void* ws, int where) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, abort, ws, where);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
+}
+__device__ __forceinline__ float sumsq8(uint4 x, float acc) {
+    float f[8];
+    unpack_bf16x2(x.x, f[0], f[1]);
+    unpack_bf16x2(x.y, f[2], f[3]);
+    unpack_bf16x2(x.z, f[4], f[5]);
+    unpack_bf16x2(x.w, f[6], f[7]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc = fmaf(f[e], f[e], acc);
+    return acc;
+}
 
 __global__ void __launch_bounds__(D_THREADS, 1)
 fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
@@ -114,12 +140,9 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     uint64_t* acc_full = b_empty + D_RB;
     uint64_t* ss_ready = acc_full + 1;
     int64_t* s_off = reinterpret_cast<int64_t*>(ss_ready + 1);        // cache offset of the item row or -1
-    int* s_row = reinterpret_cast<int*>(s_off + D_MAX_ITEMS);
-    int* s_pos = s_row + D_MAX_ITEMS;
-    float* s_ss = reinterpret_cast<float*>(s_pos + D_MAX_ITEMS);
+    float* s_ss = reinterpret_cast<float*>(s_off + D_MAX_ITEMS);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_ss + D_MAX_ITEMS);
-    int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);
-    volatile int* abort = s_flags;
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int grp = blockIdx.x, li = blockIdx.y;
     const DecodeLayer& L = a.l[li];
@@ -129,21 +152,21 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     const int head = gi / a.groups_per_head, seg = gi % a.groups_per_head;
     const int col_lo = head * a.hd + 32 * seg, col_hi = col_lo + a.half;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
     const int nkb = a.d / D_KB, nchunks = a.d / D_CHUNK;
+    const bool reporter = grp == 0 && li == 0;   // one block records bad rows / positions
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < D_RA; ++s) {
-            tc::mbar_init(&a_full[s], 1);
-            tc::mbar_init(&a_empty[s], 1);
+            tc::mbar_init(&a_full[s], D_CP_WARPS);
+            tc::mbar_init(&a_empty[s], 1 + D_SS_WARPS);   // MMA commit + the sum(h^2) warps
         }
         for (int s = 0; s < D_RB; ++s) {
             tc::mbar_init(&b_full[s], D_DEQ_WARPS);
             tc::mbar_init(&b_empty[s], 1);
         }
         tc::mbar_init(acc_full, 1);
-        tc::mbar_init(ss_ready, 1);
-        s_flags[0] = 0;
+        tc::mbar_init(ss_ready, D_CP_WARPS + D_SS_WARPS);
+        *abort = 0;
         tc::fence_barrier_init();
     }
     // Chunk c of codes / scales / zeros / g into ring slot c % D_RC (dequant warps).
@@ -153,17 +176,17 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         for (int u = threadIdx.x; u < (D_CHUNK / 2) * 4; u += D_DEQ_WARPS * 32) {
             const int r = u >> 2, part = u & 3;        // packed row, 16-byte piece (lo 2, hi 2)
             const int col = (part < 2 ? col_lo : col_hi) + (part & 1) * 16;
-            cp_async16(base + r * D_CROW + part * 16, L.codes[kv] + static_cast<int64_t>(kp0 + r) * a.kvw + col, true);
+            cp_async16(base + r * D_CROW + part * 16, L.codes[kv] + static_cast<int64_t>(kp0 + r) * a.kvw + col);
         }
         for (int u = threadIdx.x; u < (D_CHUNK / D_KB) * 16 + D_CHUNK / 8; u += D_DEQ_WARPS * 32) {
             if (u < (D_CHUNK / D_KB) * 16) {
                 const int g = u >> 4, part = u & 15, which = part >> 3, p = part & 7;
                 const int col = (p < 4 ? col_lo : col_hi) + (p & 3) * 8;
                 const __half* src = (which ? L.zero[kv] : L.scale[kv]) + static_cast<int64_t>(g0 + g) * a.kvw + col;
-                cp_async16(base + CHUNK_CODES + g * 256 + which * 128 + p * 16, src, true);
+                cp_async16(base + CHUNK_CODES + g * 256 + which * 128 + p * 16, src);
             } else {
                 const int p = u - (D_CHUNK / D_KB) * 16;
-                cp_async16(base + CHUNK_CODES + CHUNK_SZ + p * 16, L.gamma + c * D_CHUNK + p * 8, true);
+                cp_async16(base + CHUNK_CODES + CHUNK_SZ + p * 16, L.gamma + c * D_CHUNK + p * 8);
             }
         }
     };
@@ -173,41 +196,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             cp_async_commit();
         }
     }
-    // Per-item metadata: source row, position, cache offset (validated once per item).
-    for (int i = threadIdx.x; i < D_MAX_ITEMS; i += D_THREADS) {
-        int r = -1, p = 0;
-        int64_t off = -1;
-        if (i < n) {
-            r = a.rows ? a.rows[i] : i;
-            if (r < 0 || r >= a.h_rows) {
-                if (grp == 0 && li == 0) record_fault(ws, TEE_DEVERR_ROW, r);
-                r = -1;
-            } else {
-                p = a.pos ? a.pos[r] : a.pos0 + r;
-                const int sq = a.seq ? a.seq[r] : 0;
-                if (!pos_ok(p, a.cl.max_pos, a.hdr)) {
-                    if (grp == 0 && li == 0) record_fault(ws, TEE_DEVERR_POS, p);
-                    p = 0;
-                } else if (sq < 0 || sq >= a.cl.n_seq) {
-                    if (grp == 0 && li == 0) record_fault(ws, TEE_DEVERR_SEQ, sq);
-                } else {
-                    off = L.cache_layer * a.cl.s_layer + sq * a.cl.s_seq + head * a.cl.s_head +
-                          static_cast<int64_t>(p) * a.cl.s_pos;
-                }
-            }
-        }
-        s_row[i] = r;
-        s_pos[i] = p;
-        s_off[i] = off;
-    }
-    // A rows past the items stay zero in every slot (the MMA reads 128 rows).
-    for (int u = threadIdx.x; u < D_RA * (128 - n) * 8; u += D_THREADS) {
-        const int s = u / ((128 - n) * 8), rem = u % ((128 - n) * 8);
-        *reinterpret_cast<uint4*>(smem + OFF_A + s * A_SLOT + (n + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
-            make_uint4(0, 0, 0, 0);
-    }
     if (warp == D_MMA_WARP) tc::tmem_alloc(tmem_slot, D_COLS);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -227,7 +216,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             const uint8_t* base = smem + OFF_C + (c % D_RC) * CHUNK_BYTES;
             for (int b = 0; b < D_CHUNK / D_KB && ok; ++b) {
                 const int kb = c * (D_CHUNK / D_KB) + b, s = kb % D_RB;
-                if (kb >= D_RB && !tc::mbar_wait(&b_empty[s], ((kb / D_RB) - 1) & 1, abort, ws, 51)) {
+                if (kb >= D_RB && !warp_wait(&b_empty[s], ((kb / D_RB) - 1) & 1, abort, ws, 51)) {
                     ok = false;
                     break;
                 }
@@ -267,69 +256,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             if (c + D_RC < nchunks) load_chunk(c + D_RC);
             cp_async_commit();
         }
-    } else if (warp == D_HROW_WARP) {
-        // ---- h rows: block kb into A slot kb % D_RA; release block kb - D_LAG.
-        if (is_k)
-            for (int u = lane; u < n * 16; u += 32) {
-                const int i = u >> 4, p = u & 15;
-                cp_async16(smem + OFF_ROPE + i * 256 + p * 16,
-                           a.rope + static_cast<int64_t>(s_pos[i]) * a.half + 32 * seg + p * 2, true);
-            }
-        cp_async_commit();
-        float ss[4] = {0.f, 0.f, 0.f, 0.f};   // items lane + 32q
-        auto release = [&](int j) {
-            // Block j's copies (and everything before them) have landed for this warp.
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            const uint8_t* slot = smem + OFF_A + (j % D_RA) * A_SLOT;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int i = lane + 32 * q;
-                if (i >= n) break;
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(slot + i * 128 + (((jj + i) & 7) << 4));
-                    float f[8];
-                    unpack_bf16x2(x.x, f[0], f[1]);
-                    unpack_bf16x2(x.y, f[2], f[3]);
-                    unpack_bf16x2(x.z, f[4], f[5]);
-                    unpack_bf16x2(x.w, f[6], f[7]);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ss[q] = fmaf(f[e], f[e], ss[q]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&a_full[j % D_RA]);
-        };
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % D_RA;
-            if (kb >= D_RA && !tc::mbar_wait(&a_empty[s], ((kb / D_RA) - 1) & 1, abort, ws, 52)) {
-                ok = false;
-                break;
-            }
-            uint8_t* slot = smem + OFF_A + s * A_SLOT;
-            for (int u = lane; u < n * 8; u += 32) {
-                const int r = u >> 3, j = u & 7;
-                const int src = s_row[r];
-                cp_async16(slot + r * 128 + ((j ^ (r & 7)) << 4),
-                           a.h + static_cast<int64_t>(src < 0 ? 0 : src) * a.ld_h + kb * D_KB + j * 8, src >= 0);
-            }
-            cp_async_commit();
-            if (kb >= D_LAG) {
-                cp_async_wait<D_LAG>();
-                release(kb - D_LAG);
-            }
-        }
-        cp_async_wait<0>();
-        if (ok)
-            for (int j = max(0, nkb - D_LAG); j < nkb; ++j) release(j);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (lane + 32 * q < D_MAX_ITEMS) s_ss[lane + 32 * q] = ss[q];
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_ss and the RoPE rows are ready
-    } else {
+    } else if (warp == D_MMA_WARP) {
         // ---- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_bf16(128, D_COLS);
@@ -345,16 +272,124 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                 tc::umma_commit(&a_empty[sa]);
                 tc::umma_commit(&b_empty[sb]);
             }
-            tc::umma_commit(acc_full);
+            tc::umma_commit(acc_full);   // also when stopped early: every issued MMA finishes first
         }
+    } else if (warp < D_SS_WARP0) {
+        // ---- h rows. Thread ct copies 16-byte piece j = ct % 8 of items ct / 8 + 16 m,
+        // m = 0..7, of every block.
+        const int ct = threadIdx.x - D_CP_WARP0 * 32;
+        const int j = ct & 7, ib = ct >> 3;
+        const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
+        // Item ct's h row, pulled into L2 whole (every block of it is read by every CTA).
+        int r_ct = -1;
+        if (ct < n) {
+            const int r = a.rows ? a.rows[ct] : ct;
+            if (r >= 0 && r < a.h_rows) {
+                r_ct = r;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.h + static_cast<int64_t>(r) * a.ld_h),
+                             "r"(a.d * 2)
+                             : "memory");
+            } else if (reporter) {
+                record_fault(ws, TEE_DEVERR_ROW, r);
+            }
+        }
+        const bf16* src[D_ITEMS_PER_CP];
+#pragma unroll
+        for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
+            const int i = ib + 16 * m;
+            const int r = i < n ? (a.rows ? a.rows[i] : i) : -1;
+            src[m] = (r >= 0 && r < a.h_rows) ? a.h + static_cast<int64_t>(r) * a.ld_h + j * 8 : nullptr;
+        }
+        auto issue = [&](int kb) {
+            uint8_t* slot = smem + OFF_A + (kb % D_RA) * A_SLOT;
+#pragma unroll
+            for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
+                const int i = ib + 16 * m;
+                if (src[m]) cp_async16(slot + i * 128 + ((j ^ (i & 7)) << 4), src[m] + kb * D_KB);
+            }
+        };
+        // Block kb's copies (and all older ones) of this thread have landed: order them
+        // for the tensor core and release the block.
+        auto release = [&](int kb) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&a_full[kb % D_RA]);
+        };
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % D_RA;
+            if (kb >= D_RA && !warp_wait(&a_empty[s], ((kb / D_RA) - 1) & 1, abort, ws, 52)) {
+                ok = false;
+                break;
+            }
+            issue(kb);
+            if (kb == 0) {
+                // Item ct's position, cache slot and RoPE row (the RoPE copies ride in block 0's group).
+                int64_t off = -1;
+                if (r_ct >= 0) {
+                    const int p = a.pos ? a.pos[r_ct] : a.pos0 + r_ct;
+                    const int sq = a.seq ? a.seq[r_ct] : 0;
+                    if (!pos_ok(p, a.cl.max_pos, a.hdr)) {
+                        if (reporter) record_fault(ws, TEE_DEVERR_POS, p);
+                    } else if (sq < 0 || sq >= a.cl.n_seq) {
+                        if (reporter) record_fault(ws, TEE_DEVERR_SEQ, sq);
+                    } else {
+                        off = L.cache_layer * a.cl.s_layer + sq * a.cl.s_seq + head * a.cl.s_head +
+                              static_cast<int64_t>(p) * a.cl.s_pos;
+                        if (is_k)
+                            for (int u = 0; u < 16; ++u)
+                                cp_async16(smem + OFF_ROPE + ct * 256 + u * 16,
+                                           a.rope + static_cast<int64_t>(p) * a.half + 32 * seg + u * 2);
+                    }
+                }
+                s_off[ct] = off;
+            }
+            cp_async_commit();
+            if (kb >= D_LAG) {
+                cp_async_wait<D_LAG>();
+                release(kb - D_LAG);
+            }
+        }
+        cp_async_wait<0>();
+        if (ok)
+            for (int b = max(0, nkb - D_LAG); b < nkb; ++b) release(b);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_off and the RoPE rows are ready
+    } else {
+        // ---- sum(h^2): warp w takes items 32 (2q + w) + lane, q = 0, 1, from each landed block.
+        const int w = warp - D_SS_WARP0;
+        const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
+        float ss[2] = {0.f, 0.f};
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % D_RA;
+            if (!warp_wait(&a_full[s], (kb / D_RA) & 1, abort, ws, 55)) break;
+            const uint8_t* slot = smem + OFF_A + s * A_SLOT;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int i = 32 * (2 * q + w) + lane;
+                if (i >= n) continue;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)   // chunk order rotated by row: conflict-free across the warp
+                    ss[q] = sumsq8(*reinterpret_cast<const uint4*>(slot + i * 128 + (((jj + i) & 7) << 4)), ss[q]);
+            }
+            // Order these reads before the refill of the slot.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&a_empty[s]);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) s_ss[32 * (2 * q + w) + lane] = ss[q];
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_ss is ready
     }
 
     // ---- epilogue: warps 0-3, thread = item row = TMEM lane
     if (warp < 4) {
-        bool ok = tc::mbar_wait(acc_full, 0, abort, ws, 55);
-        ok = ok && tc::mbar_wait(ss_ready, 0, abort, ws, 56);
+        bool ok = warp_wait(acc_full, 0, abort, ws, 56);
+        ok = ok && warp_wait(ss_ready, 0, abort, ws, 57);
         tc::tc_fence_after();
         const int i = warp * 32 + lane;
+        const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
         const bool valid = ok && i < n && s_off[i] >= 0;
         const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         float lo[32], hi[32];

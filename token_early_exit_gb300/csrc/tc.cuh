@@ -55,23 +55,53 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking probe: true if the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// As above, but a thread whose phase is still open is suspended (it takes no
+// issue slots) until the phase completes or suspend_ns have passed.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
 
 // Wait until the phase with the given parity has completed. Bounded: returns
 // false (and raises *abort, records the fault) after WAIT_LIMIT_NS, or as soon
-// as another role of the block has raised *abort.
+// as another role of the block has raised *abort. Waiting threads sleep in
+// mbarrier.try_wait (up to 20 us per attempt) instead of spinning, so that the
+// warps doing the work keep the issue slots.
+constexpr uint32_t WAIT_SUSPEND_NS = 20000;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, void* ws,
                                           int where) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 63) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-                *abort = 1;
-                record_fault(ws, TEE_DEVERR_TIMEOUT, where);
-                return false;
-            }
+        if (mbar_try_wait_sleep(bar, parity, WAIT_SUSPEND_NS)) return true;
+        if (*abort) return false;
+        if ((i & 7) == 7 && globaltimer() - t0 > WAIT_LIMIT_NS) {
+            *abort = 1;
+            record_fault(ws, TEE_DEVERR_TIMEOUT, where);
+            return false;
         }
     }
 }
