@@ -26,6 +26,7 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse  # noqa: E402
+import hashlib  # noqa: E402
 import json  # noqa: E402
 import statistics  # noqa: E402
 import subprocess  # noqa: E402
@@ -53,6 +54,24 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def traffic(key):
+    """DRAM bytes per call of the dominant kernel, from the ncu capture recorded in
+    profiles/traffic.json, or None when there is none or the kernel's source has
+    changed since it was taken."""
+    if key is None:
+        return None
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    e = json.load(open(p)).get(key)
+    if not e:
+        return None
+    src = os.path.join(ROOT, e["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != e["sha256"]:
+        return None
+    return int(e["dram_bytes_per_launch"]) * int(e.get("launches_per_call", 1))
+
+
 # --------------------------------------------------------------------------- workloads
 
 class Decode:
@@ -78,6 +97,9 @@ class Decode:
         self.out = torch.zeros(n, d, dtype=dt, device=dev)
         self.units = n
         self.kernel = "kv_fill"
+        # the decode kernel (int4, identity map, bf16) has a recorded ncu capture
+        self.traffic_key = ("kv_fill/decode" if cfg.weights == "int4" and cfg.map == "identity" and cfg.dtype == "bf16"
+                            else None)
         # algorithmic bytes of the fill call: weights + the h rows + K/V written
         L = len(cfg.fill_layers)
         kvw = cfg.kvw
@@ -191,6 +213,7 @@ class Router:
         self.c_out["h_cont"] = torch.empty(n, cfg.d, dtype=self.h.dtype, device=dev)
         self.units = n
         self.kernel = "exit_gate(router)"
+        self.traffic_key = None
         self.bound = "hbm"
 
     def fill_bytes(self, n_exit):
@@ -259,6 +282,7 @@ class Prefill:
                                rope_base=cfg.rope_base, eps=cfg.eps, dtype=torch.bfloat16, max_pos=cfg.tokens)
         self.units = self.rows
         self.kernel = "kv_fill"
+        self.traffic_key = None
         self.bound = "tensor"
         d, kvw = cfg.d, cfg.kvw
         self.flops = float(self.n_layers) * self.rows * (2 * d * d + 4 * d * kvw)
@@ -539,13 +563,13 @@ def run_gpu(args):
         achieved = work / (k_ms * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "kernel": w.kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None, "algorithmic_bytes": work, "kernel_ms": k_ms,
+                "frac": achieved / peak, "traffic": traffic(w.traffic_key), "algorithmic_bytes": work, "kernel_ms": k_ms,
                 "peak_source": pk["source"]}
     else:
         achieved = work / (k_ms * 1e-3) / 1e12
         peak = pk["bf16_tflops_sustained"] if k_ms > 50 else pk["bf16_tflops"]
         roof = {"bound": "tensor", "kernel": w.kernel, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None, "algorithmic_flops": work, "kernel_ms": k_ms,
+                "frac": achieved / peak, "traffic": traffic(w.traffic_key), "algorithmic_flops": work, "kernel_ms": k_ms,
                 "peak_source": pk["source"]}
 
     cpu = None

@@ -2,29 +2,34 @@
 // group-64 weights (River-LLM's W4A16 exit layers), identity map (the
 // "State Propagation" / identity-fill input).
 //
-// One launch, one CTA per (group of 64 output columns, filled layer). The 64
-// columns are two 32-wide segments [i, i+32) and [i+hd/2, i+hd/2+32) of one K
-// or V head, so that RoPE pairs stay inside the CTA. On tcgen05:
-//   D[item][c] = sum_k h[row(item)][k] * W'[k][c],  M = 128 item rows (rows
-//   past the items hold whatever; their D rows are never stored), N = 64
-//   columns, K = d, with
-//   W'[k][c] = (q - zero) * scale * g_j[k]
-// so that D / rms(h) is layer j's K or V for each item (RMSNorm weight folded
-// into the dequantised weights). Warp roles, synchronised by mbarriers only:
-//   warps 0-7   stream the int4 codes, fp16 scales/zeros and g_j in 512-k
-//               chunks (cp.async, a 3-chunk ring) and dequantise each 64-k
-//               block into a ring of bf16 B operands (128-byte swizzle);
-//   warp 8      issues tcgen05.mma into a 64-column TMEM accumulator and frees
-//               the ring slots with tcgen05.commit;
+// Work split. The K and V projections of one filled layer are cut into groups
+// of 256 output columns, and the reduction dimension d into KS equal ranges.
+// One cluster of KS CTAs per (group, layer): CTA r computes, on tcgen05,
+//   P_r[item][c] = sum_{k in range r} h[row(item)][k] * W'[k][c],
+//   W'[k][c] = (q - zero) * scale * g_j[k]     (M = 128 item rows, N = 256, K = d / KS)
+// and the partial sums of h^2 over its range; the CTAs then add their partials
+// through distributed shared memory. A group is four units of 64 columns, each
+// unit the two 32-wide halves [i, i+32) and [i+hd/2, i+hd/2+32) of one head,
+// so that RoPE pairs stay inside a unit; unit u is finished by the CTA of rank
+// u % KS: sum of the KS partials, 1/rms over the whole d, RoPE, bf16 store
+// into the backbone's cache slot.
+//
+// Warp roles in a CTA (mbarriers between roles):
+//   warps 0-7   stream the CTA's int4 codes, fp16 scales/zeros and g_j (cp.async,
+//               256-k chunks, two in flight) and dequantise each 64-k block
+//               into a ring of bf16 B operands (256 rows of 128 bytes, 128-byte
+//               swizzle), packed f32x2 arithmetic;
+//   warp 8      issues tcgen05.mma (N = 256) into a 256-column TMEM accumulator;
 //   warps 9-12  gather the items' h rows of each 64-k block into a ring of A
-//               operands (cp.async, 128-byte swizzle), two blocks in flight,
-//               after asking L2 for the whole rows at the start; once a
-//               thread's copies of a block have landed it fences them for the
-//               tensor core and releases the block. They also fetch the
-//               items' positions, cache slots and RoPE rows;
-//   warps 13-14 add up sum(h^2) per item from each landed A block.
-// Epilogue (warps 0-3, one item row each): 1/rms, RoPE in registers, store of
-// the two 32-wide segments into the backbone's cache slot.
+//               operands (cp.async, 128-byte swizzle), after asking L2 for the
+//               rows' slices at the start, and fetch positions and cache slots;
+//   warps 13-14 add up the partial sum(h^2) per item from each landed A block.
+// After the last MMA, in rounds of 64 item rows: warps 0-7 copy the accumulator
+// rows (thread = item row) into shared memory per unit, with the row's partial
+// sum of h^2 in the padding; a cluster barrier; one thread sends each unit's
+// rows to its finishing CTA with a bulk shared::cluster copy that completes on
+// the receiver's mbarrier; the receivers add the partials and finish; a
+// cluster barrier closes the round.
 #include "fill.cuh"
 #include "tc.cuh"
 
@@ -34,38 +39,50 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int D_COLS = 64;           // output columns per CTA
+constexpr int D_GCOLS = 256;         // output columns per group (MMA N)
+constexpr int D_UNITS = 4;           // 64-column units per group
 constexpr int D_KB = 64;             // K per MMA block (one int4 group)
-constexpr int D_CHUNK = 512;         // K per staged chunk of codes
-constexpr int D_RA = 6;              // A operand slots (h rows)
+constexpr int D_CH = 256;            // K per staged chunk of codes
+constexpr int D_BPC = D_CH / D_KB;   // blocks per chunk
+constexpr int D_RA = 5;              // A operand slots (h rows)
 constexpr int D_LAG = 2;             // blocks of h copies in flight
-constexpr int D_RB = 3;              // B operand slots (dequantised weights)
-constexpr int D_RC = 3;              // code chunks in the ring
+constexpr int D_RB = 2;              // B operand slots (dequantised weights)
+constexpr int D_RC = 2;              // code chunks in flight
 constexpr int D_MAX_ITEMS = 128;
 constexpr int D_DEQ_WARPS = 8, D_MMA_WARP = 8, D_CP_WARP0 = 9, D_CP_WARPS = 4, D_SS_WARP0 = 13, D_SS_WARPS = 2;
+constexpr int D_DEQ_THREADS = D_DEQ_WARPS * 32;
 constexpr int D_CP_THREADS = D_CP_WARPS * 32;
 constexpr int D_ITEMS_PER_CP = D_MAX_ITEMS * 8 / D_CP_THREADS;   // 16-byte pieces per thread and block
 constexpr int D_THREADS = (D_SS_WARP0 + D_SS_WARPS) * 32;
-constexpr int D_CROW = D_COLS + 16;  // staged bytes per packed-code row (padding spreads the banks)
-// A slot is refilled D_RA - D_LAG - 1 iterations after its release: slack for the MMA
-// and sum(h^2) round trip (mbarrier hand-offs cost ~0.1 us each).
+// A slot is refilled D_RA - D_LAG - 1 iterations after its release: slack for the
+// MMA and sum(h^2) round trip (an mbarrier hand-off costs ~0.1 us).
 static_assert(D_LAG + 2 < D_RA, "the A ring needs slack beyond the blocks in flight");
 
-constexpr uint32_t A_SLOT = 128 * 128;                                   // 16 KB
-constexpr uint32_t B_SLOT = D_COLS * 128;                                // 8 KB
-constexpr uint32_t CHUNK_CODES = (D_CHUNK / 2) * D_CROW;                 // 20 KB
-constexpr uint32_t CHUNK_SZ = (D_CHUNK / D_KB) * 256;                    // scale[64], zero[64] per group: 2 KB
-constexpr uint32_t CHUNK_G = D_CHUNK * 2;                                // 1 KB
-constexpr uint32_t CHUNK_BYTES = CHUNK_CODES + CHUNK_SZ + CHUNK_G;
+constexpr uint32_t A_SLOT = 128 * 128;                  // 16 KB: 128 item rows x 64 k
+constexpr uint32_t B_SLOT = D_GCOLS * 128;              // 32 KB: 256 columns x 64 k
+constexpr uint32_t CH_CODES = (D_CH / 2) * D_GCOLS;     // 32 KB: 128 packed rows x 256 columns
+constexpr uint32_t CH_SZ = (D_CH / D_KB) * D_GCOLS * 4; // 4 KB: scale[256], zero[256] (fp16) per group
+constexpr uint32_t CH_G = D_CH * 2;                     // g_j for the chunk's k
+constexpr uint32_t CH_BYTES = CH_CODES + CH_SZ + CH_G;
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + D_RA * A_SLOT;
 constexpr uint32_t OFF_C = OFF_B + D_RB * B_SLOT;
-constexpr uint32_t OFF_ROPE = OFF_C + D_RC * CHUNK_BYTES;                // float2 [item][32]
-constexpr uint32_t OFF_SMALL = OFF_ROPE + D_MAX_ITEMS * 256;
-constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * D_RB + 2) * 8 + D_MAX_ITEMS * (8 + 4) + 16;
+constexpr uint32_t OFF_SMALL = OFF_C + D_RC * CH_BYTES;
+constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * D_RB + 3) * 8 + D_MAX_ITEMS * (8 + 4 + 4) + 16;
 constexpr size_t D_SMEM = 1024 + OFF_SMALL + SMALL_BYTES;
+// After the main loop the A and B rings hold, per round of 64 item rows, this CTA's
+// partials [unit][row][P_LD floats] (64 unit columns, then the row's partial sum of
+// h^2, padding) and the partials received for the units it finishes
+// [slot = source rank * units per CTA + owned unit][row][P_LD floats].
+constexpr int P_LD = 68;
+constexpr int P_ROWS = 64;
+constexpr uint32_t P_ROW_BYTES = P_LD * 4;
+constexpr uint32_t P_TILE = P_ROWS * P_ROW_BYTES;
+constexpr uint32_t OFF_STG = 0;
+constexpr uint32_t OFF_RCV = OFF_STG + D_UNITS * P_TILE;
+static_assert(OFF_RCV + D_UNITS * P_TILE <= OFF_C, "the partials fit in the operand rings");
 static_assert(D_SMEM <= 232448, "decode fill shared memory");
-static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_ROPE % 16 == 0 && OFF_SMALL % 8 == 0, "alignment");
+static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_SMALL % 8 == 0, "alignment");
 
 struct DecodeLayer {
     const uint8_t* codes[2];   // wk, wv
@@ -77,7 +94,7 @@ struct DecodeLayer {
 constexpr int MAX_DECODE_LAYERS = 64;
 struct DecodeArgs {
     DecodeLayer l[MAX_DECODE_LAYERS];
-    int n_max, d, kvw, hd, half, n_kv, groups_per_head;
+    int n_max, d, kvw, hd, half, groups_kv, ks;
     const int32_t* n_dev;
     float inv_d, eps;
     const bf16* h;
@@ -103,11 +120,10 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void deq_bar_sync() {   // the eight dequantising warps only
-    asm volatile("bar.sync 1, %0;" ::"n"(D_DEQ_WARPS * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(D_DEQ_THREADS) : "memory");
 }
-__device__ __forceinline__ float nibble_f32(uint32_t q) {
-    // exact small integer as fp32: (2^23 + q) - 2^23
-    return __uint_as_float(0x4B000000u | q) - 8388608.0f;
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 // Lane 0 waits for the phase, the warp follows: every lane sees the same outcome,
 // so a timed-out wait cannot split a warp at a later __syncwarp or named barrier.
@@ -128,6 +144,59 @@ __device__ __forceinline__ float sumsq8(uint4 x, float acc) {
     for (int e = 0; e < 8; ++e) acc = fmaf(f[e], f[e], acc);
     return acc;
 }
+// Nibble q of a packed word, as the fp32 value 1 + q/16: sign 0, exponent 127,
+// q in mantissa bits 19..22. SH moves the nibble's lowest bit to bit 19.
+template <int SH>
+__device__ __forceinline__ uint32_t nib_one_plus(uint32_t w) {
+    const uint32_t x = SH >= 0 ? (w << (SH >= 0 ? SH : 0)) : (w >> (SH < 0 ? -SH : 0));
+    return (x & 0x00780000u) | 0x3F800000u;
+}
+// Two consecutive k of one column: ((1 + q/16) * 16 s - (16 + z) s) * g = (q - z) s g,
+// as one packed f32x2 fma and mul, rounded to bf16x2 (lower k in the low half).
+__device__ __forceinline__ uint32_t deq2(uint32_t f0, uint32_t f1, float s16, float nz16, float g0, float g1) {
+    uint32_t out;
+    asm("{\n"
+        ".reg .b64 f, s, z, g, r;\n"
+        ".reg .f32 lo, hi;\n"
+        "mov.b64 f, {%1, %2};\n"
+        "mov.b64 s, {%3, %3};\n"
+        "mov.b64 z, {%4, %4};\n"
+        "mov.b64 g, {%5, %6};\n"
+        "fma.rn.f32x2 r, f, s, z;\n"
+        "mul.rn.f32x2 r, r, g;\n"
+        "mov.b64 {lo, hi}, r;\n"
+        "cvt.rn.bf16x2.f32 %0, hi, lo;\n"
+        "}"
+        : "=r"(out)
+        : "r"(f0), "r"(f1), "f"(s16), "f"(nz16), "f"(g0), "f"(g1));
+    return out;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// Bulk copy of bytes from this CTA's shared memory to a cluster peer's, completing
+// on the peer's mbarrier (both given as shared::cluster addresses).
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "r"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+
+// First column of unit u's low and high halves within the K (or V) projection.
+__device__ __forceinline__ int unit_col_lo(int gk, int u, int hd) {
+    const int uph = hd / 64;   // units per head
+    return (D_GCOLS * gk / hd + u / uph) * hd + 32 * (u % uph);
+}
 
 __global__ void __launch_bounds__(D_THREADS, 1)
 fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
@@ -139,21 +208,25 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     uint64_t* b_empty = b_full + D_RB;
     uint64_t* acc_full = b_empty + D_RB;
     uint64_t* ss_ready = acc_full + 1;
-    int64_t* s_off = reinterpret_cast<int64_t*>(ss_ready + 1);        // cache offset of the item row or -1
-    float* s_ss = reinterpret_cast<float*>(s_off + D_MAX_ITEMS);
+    uint64_t* recv_full = ss_ready + 1;
+    int64_t* s_ioff = reinterpret_cast<int64_t*>(recv_full + 1);   // item part of the cache offset, or -1
+    int* s_pos = reinterpret_cast<int*>(s_ioff + D_MAX_ITEMS);
+    float* s_ss = reinterpret_cast<float*>(s_pos + D_MAX_ITEMS);  // partial sum(h^2) over this CTA's k
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_ss + D_MAX_ITEMS);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-    const int grp = blockIdx.x, li = blockIdx.y;
+    const int ks = a.ks;
+    const int rank = static_cast<int>(cluster_rank());
+    const int gq = blockIdx.x / ks, li = blockIdx.y;
     const DecodeLayer& L = a.l[li];
-    const bool is_k = grp < a.n_kv * a.groups_per_head;
+    const bool is_k = gq < a.groups_kv;
     const int kv = is_k ? 0 : 1;
-    const int gi = is_k ? grp : grp - a.n_kv * a.groups_per_head;
-    const int head = gi / a.groups_per_head, seg = gi % a.groups_per_head;
-    const int col_lo = head * a.hd + 32 * seg, col_hi = col_lo + a.half;
+    const int gk = is_k ? gq : gq - a.groups_kv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nkb = a.d / D_KB, nchunks = a.d / D_CHUNK;
-    const bool reporter = grp == 0 && li == 0;   // one block records bad rows / positions
+    const int kc = a.d / ks, k0 = rank * kc;     // this CTA's k range
+    const int nkb = kc / D_KB, nch = kc / D_CH;
+    const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
+    const bool reporter = blockIdx.x == 0 && li == 0;   // one CTA records bad rows / positions
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < D_RA; ++s) {
@@ -166,100 +239,118 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         }
         tc::mbar_init(acc_full, 1);
         tc::mbar_init(ss_ready, D_CP_WARPS + D_SS_WARPS);
+        tc::mbar_init(recv_full, 1);
         *abort = 0;
         tc::fence_barrier_init();
     }
-    // Chunk c of codes / scales / zeros / g into ring slot c % D_RC (dequant warps).
+    // Chunk c of the CTA's codes / scales / zeros / g into ring slot c % D_RC. Staged
+    // column order: unit u's low half, then its high half (64 u .. 64 u + 63).
     auto load_chunk = [&](int c) {
-        uint8_t* base = smem + OFF_C + (c % D_RC) * CHUNK_BYTES;
-        const int kp0 = c * (D_CHUNK / 2), g0 = c * (D_CHUNK / D_KB);
-        for (int u = threadIdx.x; u < (D_CHUNK / 2) * 4; u += D_DEQ_WARPS * 32) {
-            const int r = u >> 2, part = u & 3;        // packed row, 16-byte piece (lo 2, hi 2)
-            const int col = (part < 2 ? col_lo : col_hi) + (part & 1) * 16;
-            cp_async16(base + r * D_CROW + part * 16, L.codes[kv] + static_cast<int64_t>(kp0 + r) * a.kvw + col);
+        uint8_t* base = smem + OFF_C + (c % D_RC) * CH_BYTES;
+        const int kg = k0 + c * D_CH;             // first k of the chunk
+        for (int v = threadIdx.x; v < (D_CH / 2) * 16; v += D_DEQ_THREADS) {
+            const int r = v >> 4, p = v & 15, u = p >> 2, part = p & 3;
+            const int col = unit_col_lo(gk, u, a.hd) + (part >= 2 ? a.half : 0) + (part & 1) * 16;
+            cp_async16(base + r * D_GCOLS + p * 16, L.codes[kv] + static_cast<int64_t>(kg / 2 + r) * a.kvw + col);
         }
-        for (int u = threadIdx.x; u < (D_CHUNK / D_KB) * 16 + D_CHUNK / 8; u += D_DEQ_WARPS * 32) {
-            if (u < (D_CHUNK / D_KB) * 16) {
-                const int g = u >> 4, part = u & 15, which = part >> 3, p = part & 7;
-                const int col = (p < 4 ? col_lo : col_hi) + (p & 3) * 8;
-                const __half* src = (which ? L.zero[kv] : L.scale[kv]) + static_cast<int64_t>(g0 + g) * a.kvw + col;
-                cp_async16(base + CHUNK_CODES + g * 256 + which * 128 + p * 16, src);
+        for (int v = threadIdx.x; v < D_BPC * 64 + D_CH / 8; v += D_DEQ_THREADS) {
+            if (v < D_BPC * 64) {
+                // group g, scale or zero, unit u, half: 32 fp16 = 4 pieces
+                const int g = v >> 6, which = (v >> 5) & 1, p = v & 31, u = p >> 3, hp = (p >> 2) & 1, q = p & 3;
+                const int col = unit_col_lo(gk, u, a.hd) + (hp ? a.half : 0) + q * 8;
+                const __half* src = (which ? L.zero[kv] : L.scale[kv]) + static_cast<int64_t>(kg / D_KB + g) * a.kvw + col;
+                cp_async16(base + CH_CODES + g * (D_GCOLS * 4) + which * (D_GCOLS * 2) + (u * 64 + hp * 32 + q * 8) * 2, src);
             } else {
-                const int p = u - (D_CHUNK / D_KB) * 16;
-                cp_async16(base + CHUNK_CODES + CHUNK_SZ + p * 16, L.gamma + c * D_CHUNK + p * 8);
+                const int p = v - D_BPC * 64;
+                cp_async16(base + CH_CODES + CH_SZ + p * 16, L.gamma + kg + p * 8);
             }
         }
     };
     if (warp < D_DEQ_WARPS) {
         for (int c = 0; c < D_RC; ++c) {
-            if (c < nchunks) load_chunk(c);
+            if (c < nch) load_chunk(c);
             cp_async_commit();
         }
     }
-    if (warp == D_MMA_WARP) tc::tmem_alloc(tmem_slot, D_COLS);
+    if (warp == D_MMA_WARP) tc::tmem_alloc(tmem_slot, D_GCOLS);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp < D_DEQ_WARPS) {
-        // ---- dequantise: unit = 4 columns x 4 k, 256 units per 64-k block
-        const int v = threadIdx.x;
-        const int cg = ((v >> 5) & 3) * 4 + (v & 3);              // column group (4 columns)
-        const int kq = (v >> 7) * 8 + ((v >> 2) & 7);             // k quad: 4kq .. 4kq+3
+        // ---- dequantise. Thread t: staged columns 4 cg .. 4 cg + 3 (cg = t % 64), k
+        // 16 kq .. 16 kq + 15 of each block (kq = t / 64). Staged column 4 cg + j goes
+        // to B row (= accumulator column) cg + 64 j: consecutive lanes hit different
+        // swizzle rows, so the 16-byte stores are conflict-free.
+        const int t = threadIdx.x;
+        const int cg = t & 63, kq = t >> 6;
         bool ok = true;
-        // Every dequantising warp runs every chunk iteration (the named barriers must
-        // match); after a timed-out wait a warp only skips the work.
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = 0; c < nch; ++c) {
             cp_async_wait<D_RC - 1>();                            // chunk c has landed (own copies)
             deq_bar_sync();                                       // ... and everyone's
-            const uint8_t* base = smem + OFF_C + (c % D_RC) * CHUNK_BYTES;
-            for (int b = 0; b < D_CHUNK / D_KB && ok; ++b) {
-                const int kb = c * (D_CHUNK / D_KB) + b, s = kb % D_RB;
+            const uint8_t* base = smem + OFF_C + (c % D_RC) * CH_BYTES;
+            for (int b = 0; b < D_BPC && ok; ++b) {
+                const int kb = c * D_BPC + b, s = kb % D_RB;
                 if (kb >= D_RB && !warp_wait(&b_empty[s], ((kb / D_RB) - 1) & 1, abort, ws, 51)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* crow = base + (b * 32 + 2 * kq) * D_CROW + 4 * cg;
-                const uint32_t w0 = *reinterpret_cast<const uint32_t*>(crow);
-                const uint32_t w1 = *reinterpret_cast<const uint32_t*>(crow + D_CROW);
-                const uint8_t* szp = base + CHUNK_CODES + b * 256;
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    w[i] = *reinterpret_cast<const uint32_t*>(base + (b * 32 + kq * 8 + i) * D_GCOLS + 4 * cg);
+                const uint8_t* szp = base + CH_CODES + b * (D_GCOLS * 4);
                 const uint2 s4 = *reinterpret_cast<const uint2*>(szp + cg * 8);
-                const uint2 z4 = *reinterpret_cast<const uint2*>(szp + 128 + cg * 8);
-                const uint2 g4 = *reinterpret_cast<const uint2*>(base + CHUNK_CODES + CHUNK_SZ + (b * D_KB + 4 * kq) * 2);
-                float sc[4], zs[4], g[4];
+                const uint2 z4 = *reinterpret_cast<const uint2*>(szp + D_GCOLS * 2 + cg * 8);
+                const uint4 ga = *reinterpret_cast<const uint4*>(base + CH_CODES + CH_SZ + (b * D_KB + kq * 16) * 2);
+                const uint4 gb = *reinterpret_cast<const uint4*>(base + CH_CODES + CH_SZ + (b * D_KB + kq * 16 + 8) * 2);
+                float g[16];
+                unpack_bf16x2(ga.x, g[0], g[1]);
+                unpack_bf16x2(ga.y, g[2], g[3]);
+                unpack_bf16x2(ga.z, g[4], g[5]);
+                unpack_bf16x2(ga.w, g[6], g[7]);
+                unpack_bf16x2(gb.x, g[8], g[9]);
+                unpack_bf16x2(gb.y, g[10], g[11]);
+                unpack_bf16x2(gb.z, g[12], g[13]);
+                unpack_bf16x2(gb.w, g[14], g[15]);
+                float sc[4], zr[4];
                 unpack_f16x2(s4.x, sc[0], sc[1]);
                 unpack_f16x2(s4.y, sc[2], sc[3]);
-                unpack_f16x2(z4.x, zs[0], zs[1]);
-                unpack_f16x2(z4.y, zs[2], zs[3]);
-                unpack_bf16x2(g4.x, g[0], g[1]);
-                unpack_bf16x2(g4.y, g[2], g[3]);
+                unpack_f16x2(z4.x, zr[0], zr[1]);
+                unpack_f16x2(z4.y, zr[2], zr[3]);
                 uint8_t* bslot = smem + OFF_B + s * B_SLOT;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float szj = zs[j] * sc[j];
-                    const uint32_t b0 = (w0 >> (8 * j)) & 0xFFu, b1 = (w1 >> (8 * j)) & 0xFFu;
-                    // (q - z) * s * g  as  (q * s - z * s) * g
-                    const float x0 = fmaf(nibble_f32(b0 & 0xFu), sc[j], -szj) * g[0];
-                    const float x1 = fmaf(nibble_f32(b0 >> 4), sc[j], -szj) * g[1];
-                    const float x2 = fmaf(nibble_f32(b1 & 0xFu), sc[j], -szj) * g[2];
-                    const float x3 = fmaf(nibble_f32(b1 >> 4), sc[j], -szj) * g[3];
-                    const int col = 4 * cg + j, kc = kq >> 1;
-                    *reinterpret_cast<uint2*>(bslot + col * 128 + ((kc ^ (col & 7)) << 4) + ((kq & 1) << 3)) =
-                        make_uint2(pack_bf16x2(x0, x1), pack_bf16x2(x2, x3));
+                    const float s16 = 16.0f * sc[j], nz16 = -(16.0f + zr[j]) * sc[j];
+                    uint32_t o[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        uint32_t flo, fhi;
+                        // byte j of w[i]: low nibble = k 16 kq + 2 i, high nibble = the next k
+                        if (j == 0) { flo = nib_one_plus<19>(w[i]); fhi = nib_one_plus<15>(w[i]); }
+                        else if (j == 1) { flo = nib_one_plus<11>(w[i]); fhi = nib_one_plus<7>(w[i]); }
+                        else if (j == 2) { flo = nib_one_plus<3>(w[i]); fhi = nib_one_plus<-1>(w[i]); }
+                        else { flo = nib_one_plus<-5>(w[i]); fhi = nib_one_plus<-9>(w[i]); }
+                        o[i] = deq2(flo, fhi, s16, nz16, g[2 * i], g[2 * i + 1]);
+                    }
+                    const int row = cg + 64 * j;
+                    uint8_t* rp = bslot + row * 128;
+                    *reinterpret_cast<uint4*>(rp + (((2 * kq) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(rp + (((2 * kq + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&b_full[s]);
             }
             deq_bar_sync();                                       // everyone is done with chunk c
-            if (c + D_RC < nchunks) load_chunk(c + D_RC);
+            if (c + D_RC < nch) load_chunk(c + D_RC);
             cp_async_commit();
         }
     } else if (warp == D_MMA_WARP) {
         // ---- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_bf16(128, D_COLS);
+            const uint32_t idesc = tc::idesc_bf16(128, D_GCOLS);
             for (int kb = 0; kb < nkb; ++kb) {
                 const int sa = kb % D_RA, sb = kb % D_RB;
                 if (!tc::mbar_wait(&a_full[sa], (kb / D_RA) & 1, abort, ws, 53)) break;
@@ -276,19 +367,17 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         }
     } else if (warp < D_SS_WARP0) {
         // ---- h rows. Thread ct copies 16-byte piece j = ct % 8 of items ct / 8 + 16 m,
-        // m = 0..7, of every block.
+        // m = 0..7, of every block of this CTA's k range.
         const int ct = threadIdx.x - D_CP_WARP0 * 32;
         const int j = ct & 7, ib = ct >> 3;
-        const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
-        // Item ct's h row, pulled into L2 whole (every block of it is read by every CTA).
+        // Item ct's h row slice, pulled into L2 whole (every CTA of the column groups
+        // reads it).
         int r_ct = -1;
         if (ct < n) {
             const int r = a.rows ? a.rows[ct] : ct;
             if (r >= 0 && r < a.h_rows) {
                 r_ct = r;
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.h + static_cast<int64_t>(r) * a.ld_h),
-                             "r"(a.d * 2)
-                             : "memory");
+                prefetch_l2(a.h + static_cast<int64_t>(r) * a.ld_h + k0, static_cast<uint32_t>(kc * 2));
             } else if (reporter) {
                 record_fault(ws, TEE_DEVERR_ROW, r);
             }
@@ -298,7 +387,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
             const int i = ib + 16 * m;
             const int r = i < n ? (a.rows ? a.rows[i] : i) : -1;
-            src[m] = (r >= 0 && r < a.h_rows) ? a.h + static_cast<int64_t>(r) * a.ld_h + j * 8 : nullptr;
+            src[m] = (r >= 0 && r < a.h_rows) ? a.h + static_cast<int64_t>(r) * a.ld_h + k0 + j * 8 : nullptr;
         }
         auto issue = [&](int kb) {
             uint8_t* slot = smem + OFF_A + (kb % D_RA) * A_SLOT;
@@ -323,27 +412,6 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                 break;
             }
             issue(kb);
-            if (kb == 0) {
-                // Item ct's position, cache slot and RoPE row (the RoPE copies ride in block 0's group).
-                int64_t off = -1;
-                if (r_ct >= 0) {
-                    const int p = a.pos ? a.pos[r_ct] : a.pos0 + r_ct;
-                    const int sq = a.seq ? a.seq[r_ct] : 0;
-                    if (!pos_ok(p, a.cl.max_pos, a.hdr)) {
-                        if (reporter) record_fault(ws, TEE_DEVERR_POS, p);
-                    } else if (sq < 0 || sq >= a.cl.n_seq) {
-                        if (reporter) record_fault(ws, TEE_DEVERR_SEQ, sq);
-                    } else {
-                        off = L.cache_layer * a.cl.s_layer + sq * a.cl.s_seq + head * a.cl.s_head +
-                              static_cast<int64_t>(p) * a.cl.s_pos;
-                        if (is_k)
-                            for (int u = 0; u < 16; ++u)
-                                cp_async16(smem + OFF_ROPE + ct * 256 + u * 16,
-                                           a.rope + static_cast<int64_t>(p) * a.half + 32 * seg + u * 2);
-                    }
-                }
-                s_off[ct] = off;
-            }
             cp_async_commit();
             if (kb >= D_LAG) {
                 cp_async_wait<D_LAG>();
@@ -353,12 +421,31 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         cp_async_wait<0>();
         if (ok)
             for (int b = max(0, nkb - D_LAG); b < nkb; ++b) release(b);
+        // Item ct's position and cache slot (dependent loads: kept off the copies' path).
+        {
+            int64_t ioff = -1;
+            int p = 0;
+            if (r_ct >= 0) {
+                p = a.pos ? a.pos[r_ct] : a.pos0 + r_ct;
+                const int sq = a.seq ? a.seq[r_ct] : 0;
+                if (!pos_ok(p, a.cl.max_pos, a.hdr)) {
+                    if (reporter) record_fault(ws, TEE_DEVERR_POS, p);
+                    p = 0;
+                } else if (sq < 0 || sq >= a.cl.n_seq) {
+                    if (reporter) record_fault(ws, TEE_DEVERR_SEQ, sq);
+                } else {
+                    ioff = L.cache_layer * a.cl.s_layer + sq * a.cl.s_seq + static_cast<int64_t>(p) * a.cl.s_pos;
+                    if (is_k) prefetch_l2(a.rope + static_cast<int64_t>(p) * a.half, static_cast<uint32_t>(a.half * 8));
+                }
+            }
+            s_ioff[ct] = ioff;
+            s_pos[ct] = p;
+        }
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_off and the RoPE rows are ready
+        if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_ioff, s_pos are ready
     } else {
-        // ---- sum(h^2): warp w takes items 32 (2q + w) + lane, q = 0, 1, from each landed block.
+        // ---- partial sum(h^2): warp w takes items 32 (2q + w) + lane, q = 0, 1.
         const int w = warp - D_SS_WARP0;
-        const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
         float ss[2] = {0.f, 0.f};
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % D_RA;
@@ -383,65 +470,131 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_ss is ready
     }
 
-    // ---- epilogue: warps 0-3, thread = item row = TMEM lane
-    if (warp < 4) {
-        bool ok = warp_wait(acc_full, 0, abort, ws, 56);
-        ok = ok && warp_wait(ss_ready, 0, abort, ws, 57);
+    // ---- the reduction across the cluster, in rounds of 64 item rows.
+    // Accumulator column cg + 64 j holds staged column 4 cg + j, i.e. unit cg / 16,
+    // unit column 4 (cg % 16) + j.
+    bool acc_ok = true;
+    if (warp < D_DEQ_WARPS) {
+        acc_ok = warp_wait(acc_full, 0, abort, ws, 56);
+        acc_ok = warp_wait(ss_ready, 0, abort, ws, 57) && acc_ok;   // the A ring is free
         tc::tc_fence_after();
-        const int i = warp * 32 + lane;
-        const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
-        const bool valid = ok && i < n && s_off[i] >= 0;
-        const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        float lo[32], hi[32];
-        tc::tmem_ld32(tb, lo);
-        tc::tmem_ld32(tb + 32, hi);
-        if (valid) {
-            const float rs = 1.0f / sqrtf(s_ss[i] * a.inv_d + a.eps);
-            if (is_k) {
-                const float2* cs = reinterpret_cast<const float2*>(smem + OFF_ROPE + i * 256);
+    }
+    const int upr = D_UNITS / ks;   // units finished per CTA
+    const uint32_t stg_s = tc::smem_u32(smem + OFF_STG), rcv_s = tc::smem_u32(smem + OFF_RCV);
+    const float* stg = reinterpret_cast<const float*>(smem + OFF_STG);
+    const float* rcv = reinterpret_cast<const float*>(smem + OFF_RCV);
+    const int rounds = (n + P_ROWS - 1) / P_ROWS;
+    for (int round = 0; round < rounds; ++round) {
+        const int r0 = round * P_ROWS, nr = min(P_ROWS, n - r0);
+        if (threadIdx.x == 0 && ks > 1)
+            tc::mbar_arrive_expect_tx(recv_full, static_cast<uint32_t>(upr * (ks - 1) * nr) * P_ROW_BYTES);
+        // Rows r0 .. r0 + 63 sit in TMEM lane quarters 2 round, 2 round + 1: warps w with
+        // w % 4 in those quarters read them, units 0-1 (w < 4) or 2-3 (w >= 4).
+        if (warp < D_DEQ_WARPS && (warp & 3) / 2 == round) {
+            const int r = (warp & 3) * 32 + lane, rl = r - r0;
+            const uint32_t tb = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+#pragma unroll 1
+            for (int u = 2 * (warp >> 2); u < 2 * (warp >> 2) + 2; ++u) {
+                float v[4][16];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float2 e = cs[c];
-                    const float x1 = lo[c] * rs, x2 = hi[c] * rs;
-                    lo[c] = x1 * e.x - x2 * e.y;
-                    hi[c] = x2 * e.x + x1 * e.y;
-                }
-            } else {
+                for (int j = 0; j < 4; ++j) tc::tmem_ld16(tb + 16 * u + 64 * j, v[j]);   // warp-wide
+                if (rl < nr) {
+                    float* row = reinterpret_cast<float*>(smem + OFF_STG + u * P_TILE + rl * P_ROW_BYTES);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    lo[c] *= rs;
-                    hi[c] *= rs;
+                    for (int m = 0; m < 16; ++m)
+                        *reinterpret_cast<float4*>(row + 4 * m) = make_float4(v[0][m], v[1][m], v[2][m], v[3][m]);
+                    row[64] = s_ss[r];
                 }
             }
-            bf16* dst = (is_k ? a.kc : a.vc) + s_off[i] + 32 * seg;
-            uint4* o = reinterpret_cast<uint4*>(dst);
-            uint4* o2 = reinterpret_cast<uint4*>(dst + a.half);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read next by the bulk copies
+        }
+        tc::tc_fence_before();
+        __syncthreads();
+        cluster_sync();   // partials staged everywhere; every receiver's rings are free
+        tc::tc_fence_after();
+        if (threadIdx.x == 0)
+            for (int u = 0; u < D_UNITS; ++u) {
+                const int owner = u % ks;
+                if (owner == rank) continue;
+                const int slot = rank * upr + u / ks;
+                bulk_to_peer(map_rank(rcv_s + slot * P_TILE, owner), stg_s + u * P_TILE,
+                             static_cast<uint32_t>(nr) * P_ROW_BYTES, map_rank(tc::smem_u32(recv_full), owner));
+            }
+        // ---- finish the units of this rank: warps 0-7, thread = (item, 8 column pairs).
+        if (warp < D_DEQ_WARPS) {
+            const bool got = ks == 1 || warp_wait(recv_full, round & 1, abort, ws, 58);
+            const int t = threadIdx.x, q = t & 3, il = t >> 2, i = r0 + il;
+            if (got && acc_ok && !*abort && il < nr && s_ioff[i] >= 0) {
+                const int64_t ioff = s_ioff[i];
+                for (int ul = 0; ul < upr; ++ul) {
+                    const int u = rank + ul * ks;
+                    const int col_lo = unit_col_lo(gk, u, a.hd);
+                    const int head = col_lo / a.hd, seg_off = col_lo - head * a.hd;   // 32 * segment
+                    float lo[8], hi[8], ss = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                o[q] = make_uint4(pack_bf16x2(lo[8 * q], lo[8 * q + 1]), pack_bf16x2(lo[8 * q + 2], lo[8 * q + 3]),
-                                  pack_bf16x2(lo[8 * q + 4], lo[8 * q + 5]), pack_bf16x2(lo[8 * q + 6], lo[8 * q + 7]));
-                o2[q] = make_uint4(pack_bf16x2(hi[8 * q], hi[8 * q + 1]), pack_bf16x2(hi[8 * q + 2], hi[8 * q + 3]),
-                                   pack_bf16x2(hi[8 * q + 4], hi[8 * q + 5]), pack_bf16x2(hi[8 * q + 6], hi[8 * q + 7]));
+                    for (int e = 0; e < 8; ++e) lo[e] = hi[e] = 0.f;
+                    for (int src = 0; src < ks; ++src) {
+                        const float* row = (src == rank ? stg + (u * P_ROWS + il) * P_LD
+                                                        : rcv + ((src * upr + ul) * P_ROWS + il) * P_LD);
+                        const float4 l0 = *reinterpret_cast<const float4*>(row + 8 * q);
+                        const float4 l1 = *reinterpret_cast<const float4*>(row + 8 * q + 4);
+                        const float4 h0 = *reinterpret_cast<const float4*>(row + 32 + 8 * q);
+                        const float4 h1 = *reinterpret_cast<const float4*>(row + 32 + 8 * q + 4);
+                        lo[0] += l0.x; lo[1] += l0.y; lo[2] += l0.z; lo[3] += l0.w;
+                        lo[4] += l1.x; lo[5] += l1.y; lo[6] += l1.z; lo[7] += l1.w;
+                        hi[0] += h0.x; hi[1] += h0.y; hi[2] += h0.z; hi[3] += h0.w;
+                        hi[4] += h1.x; hi[5] += h1.y; hi[6] += h1.z; hi[7] += h1.w;
+                        ss += row[64];
+                    }
+                    const float rs = 1.0f / sqrtf(ss * a.inv_d + a.eps);
+                    if (is_k) {
+                        const float4* cs = reinterpret_cast<const float4*>(
+                            a.rope + static_cast<int64_t>(s_pos[i]) * a.half + seg_off + 8 * q);
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const float4 c2 = __ldg(cs + e2);   // {cos, sin} of two pairs
+                            const float x1 = lo[2 * e2] * rs, x2 = hi[2 * e2] * rs;
+                            const float y1 = lo[2 * e2 + 1] * rs, y2 = hi[2 * e2 + 1] * rs;
+                            lo[2 * e2] = x1 * c2.x - x2 * c2.y;
+                            hi[2 * e2] = x2 * c2.x + x1 * c2.y;
+                            lo[2 * e2 + 1] = y1 * c2.z - y2 * c2.w;
+                            hi[2 * e2 + 1] = y2 * c2.z + y1 * c2.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            lo[e] *= rs;
+                            hi[e] *= rs;
+                        }
+                    }
+                    bf16* dst = (is_k ? a.kc : a.vc) + ioff + static_cast<int64_t>(head) * a.cl.s_head + seg_off + 8 * q;
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                                                                pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+                    *reinterpret_cast<uint4*>(dst + a.half) =
+                        make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]), pack_bf16x2(hi[4], hi[5]),
+                                   pack_bf16x2(hi[6], hi[7]));
+                }
             }
         }
+        cluster_sync();   // the round's copies have landed and been read: buffers reusable, peers may exit
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == D_MMA_WARP) tc::tmem_dealloc(tmem, D_COLS);
+    if (warp == D_MMA_WARP) tc::tmem_dealloc(tmem, D_GCOLS);
 }
 
 bool decode_eligible(const FillCall& fc) {
     const tee_fill_desc& D = *fc.desc;
     if (D.dtype != TEE_BF16 || D.wfmt != TEE_W_INT4 || D.group != D_KB) return false;
     if (fc.n_max > D_MAX_ITEMS || fc.n_layers > MAX_DECODE_LAYERS) return false;
-    if (D.d % D_CHUNK || (D.head_dim != 64 && D.head_dim != 128)) return false;
+    if (D.d % D_CH || (D.head_dim != 64 && D.head_dim != 128)) return false;
+    const int kvw = D.n_kv_heads * D.head_dim;
+    if (kvw % D_GCOLS) return false;
     if ((fc.ld_h * 2) % 16 || !aligned16(fc.h) || !aligned16(fc.k_cache) || !aligned16(fc.v_cache)) return false;
     const tee_cache_layout& cl = *fc.cache;
     if (cl.s_layer % 8 || cl.s_seq % 8 || cl.s_head % 8 || cl.s_pos % 8) return false;
-    const int kvw = D.n_kv_heads * D.head_dim;
-    if (kvw % 16) return false;
     for (int l = 0; l < fc.n_layers; ++l) {
         const tee_fill_layer& L = fc.layers[l];
         if (L.w_map) return false;
@@ -450,6 +603,52 @@ bool decode_eligible(const FillCall& fc) {
             return false;
     }
     return true;
+}
+
+// K split: the largest of 4, 2, 1 that divides d into whole chunks and keeps the
+// grid within the clusters that can be resident at once.
+int choose_ks(int d, int ctas_per_split, int max_clusters_4, int max_clusters_2) {
+    const int sms = sm_count();
+    if (d % (4 * D_CH) == 0 && ctas_per_split * 4 <= sms && ctas_per_split <= max_clusters_4) return 4;
+    if (d % (2 * D_CH) == 0 && ctas_per_split * 2 <= sms && ctas_per_split <= max_clusters_2) return 2;
+    return 1;
+}
+
+tee_status launch(const DecodeArgs& a, dim3 grid, int ks, void* ws, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(D_THREADS);
+    cfg.dynamicSmemBytes = D_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, fill_decode_kernel, a, ws));
+    return st != TEE_OK ? st : launch_status();   // counts the launch
+}
+
+int max_clusters(int ks) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(ks * 64, 1);
+    cfg.blockDim = dim3(D_THREADS);
+    cfg.dynamicSmemBytes = D_SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fill_decode_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace
@@ -464,6 +663,16 @@ size_t fill_decode_ws_bytes(const tee_fill_desc& D, int n_layers, int n_max) {
 tee_status fill_decode_run(const FillCall& fc) {
     if (!decode_eligible(fc)) return TEE_ERR_UNSUPPORTED;
     const tee_fill_desc& D = *fc.desc;
+    static bool attr_set = false;
+    static int mc4 = 0, mc2 = 0;
+    if (!attr_set) {
+        tee_status st = cuda_status(cudaFuncSetAttribute(fill_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         static_cast<int>(D_SMEM)));
+        if (st != TEE_OK) return st;
+        mc4 = max_clusters(4);
+        mc2 = max_clusters(2);
+        attr_set = true;
+    }
     DecodeArgs a{};
     a.n_max = fc.n_max;
     a.n_dev = fc.n_dev;
@@ -471,8 +680,7 @@ tee_status fill_decode_run(const FillCall& fc) {
     a.kvw = D.n_kv_heads * D.head_dim;
     a.hd = D.head_dim;
     a.half = D.head_dim / 2;
-    a.n_kv = D.n_kv_heads;
-    a.groups_per_head = a.half / 32;
+    a.groups_kv = a.kvw / D_GCOLS;
     a.inv_d = 1.0f / static_cast<float>(D.d);
     a.eps = D.eps;
     a.h = static_cast<const bf16*>(fc.h);
@@ -495,16 +703,9 @@ tee_status fill_decode_run(const FillCall& fc) {
                              {static_cast<const __half*>(L.k_zero), static_cast<const __half*>(L.v_zero)},
                              static_cast<const bf16*>(L.gamma), L.cache_layer};
     }
-    static bool attr = false;
-    if (!attr) {
-        tee_status st = cuda_status(cudaFuncSetAttribute(fill_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         static_cast<int>(D_SMEM)));
-        if (st != TEE_OK) return st;
-        attr = true;
-    }
-    dim3 grid(2 * a.n_kv * a.groups_per_head, fc.n_layers);
-    fill_decode_kernel<<<grid, D_THREADS, D_SMEM, fc.stream>>>(a, fc.ws);
-    return launch_status();
+    const int splits = 2 * a.groups_kv * fc.n_layers;   // (group, layer) pairs
+    a.ks = choose_ks(D.d, splits, mc4, mc2);
+    return launch(a, dim3(2 * a.groups_kv * a.ks, fc.n_layers), a.ks, fc.ws, fc.stream);
 }
 
 }  // namespace tee
