@@ -5,8 +5,8 @@
 // Work split. The K and V projections of one filled layer are cut into groups
 // of 256 output columns, and the reduction dimension d into KS equal ranges.
 // One cluster of KS CTAs per (group, layer): CTA r computes, on tcgen05,
-//   P_r[item][c] = sum_{k in range r} h[row(item)][k] * W'[k][c],
-//   W'[k][c] = (q - zero) * scale * g_j[k]     (M = 128 item rows, N = 256, K = d / KS)
+//   P_r[item][c] = sum_{k in range r} (h[row(item)][k] g_j[k]) * W[k][c],
+//   W[k][c] = (q - zero) * scale     (M = 128 item rows, N = 256, K = d / KS)
 // and the partial sums of h^2 over its range; the CTAs then add their partials
 // through distributed shared memory. A group is four units of 64 columns, each
 // unit the two 32-wide halves [i, i+32) and [i+hd/2, i+hd/2+32) of one head,
@@ -15,15 +15,17 @@
 // into the backbone's cache slot.
 //
 // Warp roles in a CTA (mbarriers between roles):
-//   warps 0-7   stream the CTA's int4 codes, fp16 scales/zeros and g_j (cp.async,
-//               256-k chunks, two in flight) and dequantise each 64-k block
-//               into a ring of bf16 B operands (256 rows of 128 bytes, 128-byte
-//               swizzle), packed f32x2 arithmetic;
+//   warps 0-7   stream the CTA's int4 codes and fp16 scales/zeros (cp.async, 256-k
+//               chunks, two in flight) and dequantise each 64-k block into a ring
+//               of bf16 B operands (256 rows of 128 bytes, 128-byte swizzle):
+//               W[k][c] = (q - z) s, in packed bf16x2 arithmetic;
 //   warp 8      issues tcgen05.mma (N = 256) into a 256-column TMEM accumulator;
 //   warps 9-12  gather the items' h rows of each 64-k block into a ring of A
 //               operands (cp.async, 128-byte swizzle), after asking L2 for the
-//               rows' slices at the start, and fetch positions and cache slots;
-//   warps 13-14 add up the partial sum(h^2) per item from each landed A block.
+//               rows' slices at the start. Once a thread's pieces of a block have
+//               landed it adds their squares into per-item sums of h^2 and scales
+//               them by the RMSNorm gain g_j in place (A = h * g_j), then releases
+//               the block; they also fetch positions and cache slots.
 // After the last MMA, in rounds of 64 item rows: warps 0-7 copy the accumulator
 // rows (thread = item row) into shared memory per unit, with the row's partial
 // sum of h^2 in the padding; a cluster barrier; one thread sends each unit's
@@ -49,28 +51,29 @@ constexpr int D_LAG = 2;             // blocks of h copies in flight
 constexpr int D_RB = 2;              // B operand slots (dequantised weights)
 constexpr int D_RC = 2;              // code chunks in flight
 constexpr int D_MAX_ITEMS = 128;
-constexpr int D_DEQ_WARPS = 8, D_MMA_WARP = 8, D_CP_WARP0 = 9, D_CP_WARPS = 4, D_SS_WARP0 = 13, D_SS_WARPS = 2;
+constexpr int D_DEQ_WARPS = 8, D_MMA_WARP = 8, D_CP_WARP0 = 9, D_CP_WARPS = 4;
 constexpr int D_DEQ_THREADS = D_DEQ_WARPS * 32;
 constexpr int D_CP_THREADS = D_CP_WARPS * 32;
 constexpr int D_ITEMS_PER_CP = D_MAX_ITEMS * 8 / D_CP_THREADS;   // 16-byte pieces per thread and block
-constexpr int D_THREADS = (D_SS_WARP0 + D_SS_WARPS) * 32;
+constexpr int D_THREADS = (D_CP_WARP0 + D_CP_WARPS) * 32;
+constexpr int D_MAX_KC = 2048;       // largest k range of one CTA (its g_j slice sits in shared memory)
 // A slot is refilled D_RA - D_LAG - 1 iterations after its release: slack for the
-// MMA and sum(h^2) round trip (an mbarrier hand-off costs ~0.1 us).
+// MMA round trip (an mbarrier hand-off costs ~0.1 us).
 static_assert(D_LAG + 2 < D_RA, "the A ring needs slack beyond the blocks in flight");
 
 constexpr uint32_t A_SLOT = 128 * 128;                  // 16 KB: 128 item rows x 64 k
 constexpr uint32_t B_SLOT = D_GCOLS * 128;              // 32 KB: 256 columns x 64 k
 constexpr uint32_t CH_CODES = (D_CH / 2) * D_GCOLS;     // 32 KB: 128 packed rows x 256 columns
 constexpr uint32_t CH_SZ = (D_CH / D_KB) * D_GCOLS * 4; // 4 KB: scale[256], zero[256] (fp16) per group
-constexpr uint32_t CH_G = D_CH * 2;                     // g_j for the chunk's k
-constexpr uint32_t CH_BYTES = CH_CODES + CH_SZ + CH_G;
+constexpr uint32_t CH_BYTES = CH_CODES + CH_SZ;
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + D_RA * A_SLOT;
 constexpr uint32_t OFF_C = OFF_B + D_RB * B_SLOT;
-constexpr uint32_t OFF_SMALL = OFF_C + D_RC * CH_BYTES;
+constexpr uint32_t OFF_G = OFF_C + D_RC * CH_BYTES;               // g_j over this CTA's k range (bf16)
+constexpr uint32_t OFF_SMALL = OFF_G + D_MAX_KC * 2;
 constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * D_RB + 3) * 8 + D_MAX_ITEMS * (8 + 4 + 4) + 16;
 constexpr size_t D_SMEM = 1024 + OFF_SMALL + SMALL_BYTES;
-// After the main loop the A and B rings hold, per round of 64 item rows, this CTA's
+// After the main loop the operand and code rings hold, per round of 64 item rows, this CTA's
 // partials [unit][row][P_LD floats] (64 unit columns, then the row's partial sum of
 // h^2, padding) and the partials received for the units it finishes
 // [slot = source rank * units per CTA + owned unit][row][P_LD floats].
@@ -80,9 +83,9 @@ constexpr uint32_t P_ROW_BYTES = P_LD * 4;
 constexpr uint32_t P_TILE = P_ROWS * P_ROW_BYTES;
 constexpr uint32_t OFF_STG = 0;
 constexpr uint32_t OFF_RCV = OFF_STG + D_UNITS * P_TILE;
-static_assert(OFF_RCV + D_UNITS * P_TILE <= OFF_C, "the partials fit in the operand rings");
+static_assert(OFF_RCV + D_UNITS * P_TILE <= OFF_G, "the partials fit in the operand and code rings");
 static_assert(D_SMEM <= 232448, "decode fill shared memory");
-static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_SMALL % 8 == 0, "alignment");
+static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_G % 16 == 0 && OFF_SMALL % 8 == 0, "alignment");
 
 struct DecodeLayer {
     const uint8_t* codes[2];   // wk, wv
@@ -144,32 +147,17 @@ __device__ __forceinline__ float sumsq8(uint4 x, float acc) {
     for (int e = 0; e < 8; ++e) acc = fmaf(f[e], f[e], acc);
     return acc;
 }
-// Nibble q of a packed word, as the fp32 value 1 + q/16: sign 0, exponent 127,
-// q in mantissa bits 19..22. SH moves the nibble's lowest bit to bit 19.
-template <int SH>
-__device__ __forceinline__ uint32_t nib_one_plus(uint32_t w) {
-    const uint32_t x = SH >= 0 ? (w << (SH >= 0 ? SH : 0)) : (w >> (SH < 0 ? -SH : 0));
-    return (x & 0x00780000u) | 0x3F800000u;
-}
-// Two consecutive k of one column: ((1 + q/16) * 16 s - (16 + z) s) * g = (q - z) s g,
-// as one packed f32x2 fma and mul, rounded to bf16x2 (lower k in the low half).
-__device__ __forceinline__ uint32_t deq2(uint32_t f0, uint32_t f1, float s16, float nz16, float g0, float g1) {
-    uint32_t out;
-    asm("{\n"
-        ".reg .b64 f, s, z, g, r;\n"
-        ".reg .f32 lo, hi;\n"
-        "mov.b64 f, {%1, %2};\n"
-        "mov.b64 s, {%3, %3};\n"
-        "mov.b64 z, {%4, %4};\n"
-        "mov.b64 g, {%5, %6};\n"
-        "fma.rn.f32x2 r, f, s, z;\n"
-        "mul.rn.f32x2 r, r, g;\n"
-        "mov.b64 {lo, hi}, r;\n"
-        "cvt.rn.bf16x2.f32 %0, hi, lo;\n"
-        "}"
-        : "=r"(out)
-        : "r"(f0), "r"(f1), "f"(s16), "f"(nz16), "f"(g0), "f"(g1));
-    return out;
+// Two consecutive k of one column from byte b of a packed word (low nibble = the
+// lower k): x = (b & 0xF) | (b >> 4) << 16 | 0x43004300 is the bf16 pair 128 + q;
+// subtracting 136 leaves q - 8 exactly, and one bf16x2 fma gives
+// (q - 8) s + (8 - z) s = (q - z) s, rounded once. wl / wh: the packed word and the
+// word shifted right by 4; sel picks byte b of each into bytes 0 and 2.
+__device__ __forceinline__ uint32_t deq_pair(uint32_t wl, uint32_t wh, uint32_t sel, __nv_bfloat162 s2,
+                                             __nv_bfloat162 zs2) {
+    const uint32_t x = (__byte_perm(wl, wh, sel) & 0x000F000Fu) | 0x43004300u;
+    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&x);
+    v = __hfma2(__hsub2(v, __floats2bfloat162_rn(136.0f, 136.0f)), s2, zs2);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -231,19 +219,19 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < D_RA; ++s) {
             tc::mbar_init(&a_full[s], D_CP_WARPS);
-            tc::mbar_init(&a_empty[s], 1 + D_SS_WARPS);   // MMA commit + the sum(h^2) warps
+            tc::mbar_init(&a_empty[s], 1);                // MMA commit
         }
         for (int s = 0; s < D_RB; ++s) {
             tc::mbar_init(&b_full[s], D_DEQ_WARPS);
             tc::mbar_init(&b_empty[s], 1);
         }
         tc::mbar_init(acc_full, 1);
-        tc::mbar_init(ss_ready, D_CP_WARPS + D_SS_WARPS);
+        tc::mbar_init(ss_ready, D_CP_WARPS);
         tc::mbar_init(recv_full, 1);
         *abort = 0;
         tc::fence_barrier_init();
     }
-    // Chunk c of the CTA's codes / scales / zeros / g into ring slot c % D_RC. Staged
+    // Chunk c of the CTA's codes / scales / zeros into ring slot c % D_RC. Staged
     // column order: unit u's low half, then its high half (64 u .. 64 u + 63).
     auto load_chunk = [&](int c) {
         uint8_t* base = smem + OFF_C + (c % D_RC) * CH_BYTES;
@@ -253,17 +241,12 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             const int col = unit_col_lo(gk, u, a.hd) + (part >= 2 ? a.half : 0) + (part & 1) * 16;
             cp_async16(base + r * D_GCOLS + p * 16, L.codes[kv] + static_cast<int64_t>(kg / 2 + r) * a.kvw + col);
         }
-        for (int v = threadIdx.x; v < D_BPC * 64 + D_CH / 8; v += D_DEQ_THREADS) {
-            if (v < D_BPC * 64) {
-                // group g, scale or zero, unit u, half: 32 fp16 = 4 pieces
-                const int g = v >> 6, which = (v >> 5) & 1, p = v & 31, u = p >> 3, hp = (p >> 2) & 1, q = p & 3;
-                const int col = unit_col_lo(gk, u, a.hd) + (hp ? a.half : 0) + q * 8;
-                const __half* src = (which ? L.zero[kv] : L.scale[kv]) + static_cast<int64_t>(kg / D_KB + g) * a.kvw + col;
-                cp_async16(base + CH_CODES + g * (D_GCOLS * 4) + which * (D_GCOLS * 2) + (u * 64 + hp * 32 + q * 8) * 2, src);
-            } else {
-                const int p = v - D_BPC * 64;
-                cp_async16(base + CH_CODES + CH_SZ + p * 16, L.gamma + kg + p * 8);
-            }
+        for (int v = threadIdx.x; v < D_BPC * 64; v += D_DEQ_THREADS) {
+            // group g, scale or zero, unit u, half: 32 fp16 = 4 pieces
+            const int g = v >> 6, which = (v >> 5) & 1, p = v & 31, u = p >> 3, hp = (p >> 2) & 1, q = p & 3;
+            const int col = unit_col_lo(gk, u, a.hd) + (hp ? a.half : 0) + q * 8;
+            const __half* src = (which ? L.zero[kv] : L.scale[kv]) + static_cast<int64_t>(kg / D_KB + g) * a.kvw + col;
+            cp_async16(base + CH_CODES + g * (D_GCOLS * 4) + which * (D_GCOLS * 2) + (u * 64 + hp * 32 + q * 8) * 2, src);
         }
     };
     if (warp < D_DEQ_WARPS) {
@@ -296,24 +279,15 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                     ok = false;
                     break;
                 }
-                uint32_t w[8];
+                uint32_t w[8], wh[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 8; ++i) {
                     w[i] = *reinterpret_cast<const uint32_t*>(base + (b * 32 + kq * 8 + i) * D_GCOLS + 4 * cg);
+                    wh[i] = w[i] >> 4;
+                }
                 const uint8_t* szp = base + CH_CODES + b * (D_GCOLS * 4);
                 const uint2 s4 = *reinterpret_cast<const uint2*>(szp + cg * 8);
                 const uint2 z4 = *reinterpret_cast<const uint2*>(szp + D_GCOLS * 2 + cg * 8);
-                const uint4 ga = *reinterpret_cast<const uint4*>(base + CH_CODES + CH_SZ + (b * D_KB + kq * 16) * 2);
-                const uint4 gb = *reinterpret_cast<const uint4*>(base + CH_CODES + CH_SZ + (b * D_KB + kq * 16 + 8) * 2);
-                float g[16];
-                unpack_bf16x2(ga.x, g[0], g[1]);
-                unpack_bf16x2(ga.y, g[2], g[3]);
-                unpack_bf16x2(ga.z, g[4], g[5]);
-                unpack_bf16x2(ga.w, g[6], g[7]);
-                unpack_bf16x2(gb.x, g[8], g[9]);
-                unpack_bf16x2(gb.y, g[10], g[11]);
-                unpack_bf16x2(gb.z, g[12], g[13]);
-                unpack_bf16x2(gb.w, g[14], g[15]);
                 float sc[4], zr[4];
                 unpack_f16x2(s4.x, sc[0], sc[1]);
                 unpack_f16x2(s4.y, sc[2], sc[3]);
@@ -322,18 +296,13 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                 uint8_t* bslot = smem + OFF_B + s * B_SLOT;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float s16 = 16.0f * sc[j], nz16 = -(16.0f + zr[j]) * sc[j];
+                    const __nv_bfloat162 s2 = __floats2bfloat162_rn(sc[j], sc[j]);
+                    const float zs = (8.0f - zr[j]) * sc[j];
+                    const __nv_bfloat162 zs2 = __floats2bfloat162_rn(zs, zs);
+                    const uint32_t sel = (j | (j << 4) | ((j + 4) << 8) | ((j + 4) << 12));
                     uint32_t o[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        uint32_t flo, fhi;
-                        // byte j of w[i]: low nibble = k 16 kq + 2 i, high nibble = the next k
-                        if (j == 0) { flo = nib_one_plus<19>(w[i]); fhi = nib_one_plus<15>(w[i]); }
-                        else if (j == 1) { flo = nib_one_plus<11>(w[i]); fhi = nib_one_plus<7>(w[i]); }
-                        else if (j == 2) { flo = nib_one_plus<3>(w[i]); fhi = nib_one_plus<-1>(w[i]); }
-                        else { flo = nib_one_plus<-5>(w[i]); fhi = nib_one_plus<-9>(w[i]); }
-                        o[i] = deq2(flo, fhi, s16, nz16, g[2 * i], g[2 * i + 1]);
-                    }
+                    for (int i = 0; i < 8; ++i) o[i] = deq_pair(w[i], wh[i], sel, s2, zs2);   // k 16 kq + 2i, +1
                     const int row = cg + 64 * j;
                     uint8_t* rp = bslot + row * 128;
                     *reinterpret_cast<uint4*>(rp + (((2 * kq) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -365,11 +334,16 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             }
             tc::umma_commit(acc_full);   // also when stopped early: every issued MMA finishes first
         }
-    } else if (warp < D_SS_WARP0) {
-        // ---- h rows. Thread ct copies 16-byte piece j = ct % 8 of items ct / 8 + 16 m,
-        // m = 0..7, of every block of this CTA's k range.
+    } else {
+        // ---- h rows. Thread ct copies 16-byte piece j = ct % 8 (k 8 j .. 8 j + 7 of
+        // each block) of items ct / 8 + 16 m, m = 0..7, of every block of this CTA's
+        // k range; it alone touches those pieces, so once they have landed it adds
+        // their squares and scales them by g_j in place.
         const int ct = threadIdx.x - D_CP_WARP0 * 32;
         const int j = ct & 7, ib = ct >> 3;
+        // This CTA's slice of g_j (landed before the first release, see below).
+        for (int v = ct; v < kc / 8; v += D_CP_THREADS) cp_async16(smem + OFF_G + v * 16, L.gamma + k0 + v * 8);
+        cp_async_commit();   // the oldest group
         // Item ct's h row slice, pulled into L2 whole (every CTA of the column groups
         // reads it).
         int r_ct = -1;
@@ -397,14 +371,36 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                 if (src[m]) cp_async16(slot + i * 128 + ((j ^ (i & 7)) << 4), src[m] + kb * D_KB);
             }
         };
-        // Block kb's copies (and all older ones) of this thread have landed: order them
-        // for the tensor core and release the block.
+        float ss[D_ITEMS_PER_CP];
+#pragma unroll
+        for (int m = 0; m < D_ITEMS_PER_CP; ++m) ss[m] = 0.f;
+        // Block kb's pieces of this thread have landed: add their squares, scale them
+        // by g_j (bf16 x bf16 -> bf16, one rounding), order them for the tensor core,
+        // and release the block once the whole warp is done.
         auto release = [&](int kb) {
+            uint8_t* slot = smem + OFF_A + (kb % D_RA) * A_SLOT;
+            const uint4 gp = *reinterpret_cast<const uint4*>(smem + OFF_G + (kb * D_KB + 8 * j) * 2);
+            const __nv_bfloat162* gv = reinterpret_cast<const __nv_bfloat162*>(&gp);
+#pragma unroll
+            for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
+                if (!src[m]) continue;
+                const int i = ib + 16 * m;
+                uint4* pp = reinterpret_cast<uint4*>(slot + i * 128 + ((j ^ (i & 7)) << 4));
+                uint4 x = *pp;
+                ss[m] = sumsq8(x, ss[m]);
+                __nv_bfloat162* xv = reinterpret_cast<__nv_bfloat162*>(&x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) xv[e] = __hmul2(xv[e], gv[e]);
+                *pp = x;
+            }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&a_full[kb % D_RA]);
         };
+        // The g_j slice comes from every copier: they meet once, after their first wait.
+        auto g_ready = [&]() { asm volatile("bar.sync 2, %0;" ::"n"(D_CP_THREADS) : "memory"); };
         bool ok = true;
+        int waited = 0;
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % D_RA;
             if (kb >= D_RA && !warp_wait(&a_empty[s], ((kb / D_RA) - 1) & 1, abort, ws, 52)) {
@@ -415,12 +411,26 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             cp_async_commit();
             if (kb >= D_LAG) {
                 cp_async_wait<D_LAG>();
+                if (!waited) {
+                    g_ready();
+                    waited = 1;
+                }
                 release(kb - D_LAG);
             }
         }
         cp_async_wait<0>();
+        if (!waited) g_ready();   // every copier reaches the meeting exactly once
         if (ok)
             for (int b = max(0, nkb - D_LAG); b < nkb; ++b) release(b);
+        // Per-item totals: the eight threads of an item are consecutive lanes.
+#pragma unroll
+        for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
+            float t = ss[m];
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            t += __shfl_xor_sync(0xffffffffu, t, 4);
+            if (j == 0) s_ss[ib + 16 * m] = t;
+        }
         // Item ct's position and cache slot (dependent loads: kept off the copies' path).
         {
             int64_t ioff = -1;
@@ -442,32 +452,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             s_pos[ct] = p;
         }
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_ioff, s_pos are ready
-    } else {
-        // ---- partial sum(h^2): warp w takes items 32 (2q + w) + lane, q = 0, 1.
-        const int w = warp - D_SS_WARP0;
-        float ss[2] = {0.f, 0.f};
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % D_RA;
-            if (!warp_wait(&a_full[s], (kb / D_RA) & 1, abort, ws, 55)) break;
-            const uint8_t* slot = smem + OFF_A + s * A_SLOT;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int i = 32 * (2 * q + w) + lane;
-                if (i >= n) continue;
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj)   // chunk order rotated by row: conflict-free across the warp
-                    ss[q] = sumsq8(*reinterpret_cast<const uint4*>(slot + i * 128 + (((jj + i) & 7) << 4)), ss[q]);
-            }
-            // Order these reads before the refill of the slot.
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&a_empty[s]);
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) s_ss[32 * (2 * q + w) + lane] = ss[q];
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_ss is ready
+        if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_ss, s_ioff, s_pos are ready
     }
 
     // ---- the reduction across the cluster, in rounds of 64 item rows.
@@ -476,7 +461,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     bool acc_ok = true;
     if (warp < D_DEQ_WARPS) {
         acc_ok = warp_wait(acc_full, 0, abort, ws, 56);
-        acc_ok = warp_wait(ss_ready, 0, abort, ws, 57) && acc_ok;   // the A ring is free
+        acc_ok = warp_wait(ss_ready, 0, abort, ws, 57) && acc_ok;   // s_ss, s_ioff, s_pos
         tc::tc_fence_after();
     }
     const int upr = D_UNITS / ks;   // units finished per CTA
@@ -705,6 +690,7 @@ tee_status fill_decode_run(const FillCall& fc) {
     }
     const int splits = 2 * a.groups_kv * fc.n_layers;   // (group, layer) pairs
     a.ks = choose_ks(D.d, splits, mc4, mc2);
+    if (D.d / a.ks > D_MAX_KC) return TEE_ERR_UNSUPPORTED;
     return launch(a, dim3(2 * a.groups_kv * a.ks, fc.n_layers), a.ks, fc.ws, fc.stream);
 }
 
