@@ -157,14 +157,19 @@ scatter_kernel(int n_max, const int32_t* __restrict__ counts, const int32_t* __r
                T* __restrict__ out, int64_t ld_out, int64_t n_out, int d, const T* __restrict__ gamma, float eps,
                void* ws) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The row lists hold n_max entries: read this warp's first entries together with
+    // the count instead of after it (one dependent load fewer on the critical path).
+    const int i_first = blockIdx.x * 8 + warp;
+    const int src_first = i_first < n_max ? exit_rows[i_first] : 0;
+    const int64_t dst_first = i_first < n_max ? exit_pos[i_first] : 0;
     int n_exit = counts[1];
     if (n_exit > n_max) {
         if (blockIdx.x == 0 && threadIdx.x == 0) record_fault(ws, TEE_DEVERR_COUNT, n_exit);
         n_exit = n_max;
     }
-    for (int i = blockIdx.x * 8 + warp; i < n_exit; i += gridDim.x * 8) {
-        const int src = exit_rows[i];
-        const int64_t dst = exit_pos[i];
+    for (int i = i_first; i < n_exit; i += gridDim.x * 8) {
+        const int src = i == i_first ? src_first : exit_rows[i];
+        const int64_t dst = i == i_first ? dst_first : exit_pos[i];
         if (src < 0 || src >= n_max) {
             if (lane == 0) record_fault(ws, TEE_DEVERR_ROW, src);
             continue;

@@ -1,8 +1,9 @@
 // Exit gate: River-LLM's state-transition cosine and TIDE's RMSNorm router.
 //
 // Cosine (River-LLM, background "state transition similarity"; method step 3):
-// one warp per token streams h_prev and h_cur with 128-bit loads, accumulates
-// <a,b>, |a|^2 and |b|^2 in fp32 and reduces them with __shfl_xor_sync.
+// h_prev and h_cur stream in with 128-bit loads, <a,b>, |a|^2 and |b|^2 are
+// accumulated in fp32 and reduced with __shfl_xor_sync: one block per token up
+// to 1024 tokens (decode batches), one warp per token beyond.
 //
 // Router (TIDE formula 3; module 4 "Fused LayerNorm + Route"): the d -> b
 // contraction is split over (token tile, channel group) blocks that stage the
@@ -77,6 +78,68 @@ cosine_gate_kernel(int n, int d, const T* __restrict__ hc, int64_t ldc, const T*
         for (int w = 0; w < GATE_WARPS; ++w) bmin = fminf(bmin, s_min[w]);
     batch_flag_tail(bmin, n, thr, rule, mask, flag, ws_at<float>(ws, TEE_WS_HEADER_BYTES),
                     ws_counter(ws, WS_CNT_GATE));
+}
+
+// Small batches: one block per token, the row split over the block's eight warps,
+// so that a decode batch of tens of tokens still spreads over as many SMs and
+// each thread issues its loads of both rows at once.
+template <typename T>
+__global__ void __launch_bounds__(GATE_WARPS * 32)
+cosine_gate_row_kernel(int n, int d, const T* __restrict__ hc, int64_t ldc, const T* __restrict__ hp, int64_t ldp,
+                       float thr, int rule, bool need_flag, float* __restrict__ score, uint8_t* __restrict__ mask,
+                       int32_t* __restrict__ flag, void* ws) {
+    const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const T* a = hp + static_cast<int64_t>(t) * ldp;
+    const T* b = hc + static_cast<int64_t>(t) * ldc;
+    float dot = 0.f, na = 0.f, nb = 0.f;
+    for (int i0 = threadIdx.x * 8; i0 < d; i0 += 2 * GATE_WARPS * 32 * 8) {
+        float x[2][8], y[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = i0 + u * GATE_WARPS * 32 * 8;
+            if (i < d) {
+                load8(a + i, x[u]);
+                load8(b + i, y[u]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x[u][k] = y[u][k] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                dot = fmaf(x[u][k], y[u][k], dot);
+                na = fmaf(x[u][k], x[u][k], na);
+                nb = fmaf(y[u][k], y[u][k], nb);
+            }
+    }
+    __shared__ float s_part[3][GATE_WARPS];
+    dot = warp_sum(dot);
+    na = warp_sum(na);
+    nb = warp_sum(nb);
+    if (lane == 0) {
+        s_part[0][warp] = dot;
+        s_part[1][warp] = na;
+        s_part[2][warp] = nb;
+    }
+    __syncthreads();
+    float s = 0.f;
+    if (threadIdx.x == 0) {
+        dot = na = nb = 0.f;
+        for (int w = 0; w < GATE_WARPS; ++w) {
+            dot += s_part[0][w];
+            na += s_part[1][w];
+            nb += s_part[2][w];
+        }
+        const float den = sqrtf(na) * sqrtf(nb);
+        s = den > 0.f ? dot / den : 0.f;
+        score[t] = s;
+        if (rule == TEE_RULE_PER_TOKEN) mask[t] = exits(s, thr);
+        s = s == s ? s : -INFINITY;
+    }
+    if (!need_flag) return;
+    batch_flag_tail(s, n, thr, rule, mask, flag, ws_at<float>(ws, TEE_WS_HEADER_BYTES), ws_counter(ws, WS_CNT_GATE));
 }
 
 // ---------------------------------------------------------------- router
@@ -250,6 +313,12 @@ static tee_status run_gate(const tee_gate_desc* g, int n, const void* h_cur, int
     const bool need_flag = flag != nullptr || g->rule == TEE_RULE_BATCH_ALL;
     const int blocks = static_cast<int>(gate_blocks(n));
     if (g->mode == TEE_GATE_COSINE) {
+        if (n >= 1 && n <= GATE_MAX_BLOCKS) {   // one block per token (its score is the block minimum)
+            cosine_gate_row_kernel<T><<<n, GATE_WARPS * 32, 0, stream>>>(
+                n, g->d, static_cast<const T*>(h_cur), ld_cur, static_cast<const T*>(h_prev), ld_prev, g->threshold,
+                g->rule, need_flag, score, mask, flag, ws);
+            return launch_status();
+        }
         cosine_gate_kernel<T><<<blocks, GATE_WARPS * 32, 0, stream>>>(
             n, g->d, static_cast<const T*>(h_cur), ld_cur, static_cast<const T*>(h_prev), ld_prev, g->threshold,
             g->rule, need_flag, score, mask, flag, ws);
