@@ -85,7 +85,8 @@ class Decode:
         self.ws = tee.Workspace(dev)
         self.fill = tee.KVFill(self.x["layers"], d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
                                rope_base=cfg.rope_base, eps=cfg.eps, dtype=self.x["h_cur"].dtype,
-                               max_pos=cfg.cache_len, int4=cfg.weights == "int4", group=cfg.group)
+                               max_pos=cfg.cache_len, int4=cfg.weights == "int4", group=cfg.group,
+                               early_weights=True)   # the step's kernels never write the weights
         n, d = cfg.batch, cfg.d
         dt = self.x["h_cur"].dtype
         self.g_out = {"score": torch.empty(n, device=dev), "mask": torch.empty(n, dtype=torch.uint8, device=dev),
@@ -136,7 +137,9 @@ class Decode:
         def scatter():
             tee.exit_scatter(self.c_out["counts"], self.c_out["exit_rows"], self.c_out["exit_pos"], x["h_cur"],
                              self.out, ws=self.ws)
-        return [gate, compact, fill, scatter], 2
+        # The scatter does not need the fill's output: it runs before the fill, whose
+        # early launch (TEE_FILL_EARLY_WEIGHTS) streams the weights during the scatter.
+        return [gate, compact, scatter, fill], 3
 
     def step(self):
         for f in self.parts()[0]:

@@ -247,7 +247,16 @@ typedef struct {
     int32_t dtype;        /* h_split, w_map, gamma, dense wk/wv and the caches */
     int32_t wfmt;         /* TEE_W_DENSE or TEE_W_INT4 for wk/wv */
     int32_t group;        /* int4 group length along d (multiple of 16) */
+    int32_t flags;        /* 0, or TEE_FILL_EARLY_WEIGHTS */
 } tee_fill_desc;
+
+/* tee_fill_desc.flags. TEE_FILL_EARLY_WEIGHTS: the decode kernel may start while
+ * the kernel enqueued just before it on the stream is still running, and read
+ * the layers' weights (wk, wv, scales, zeros, gamma) and `prep` at once; it
+ * reads h_split, rows, pos, seq, n_dev, the caches and the workspace only after
+ * that kernel has completed (programmatic dependent launch). Set it only when
+ * that kernel does not write the weights. Ignored by the other paths. */
+#define TEE_FILL_EARLY_WEIGHTS 1
 
 /* Weights of one filled layer j (device pointers). kvw = n_kv_heads*head_dim. */
 typedef struct {

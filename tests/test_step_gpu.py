@@ -20,25 +20,39 @@ def tee():
     return t
 
 
-def run_step(tee, cfg, x, fill, ws):
+def run_step(tee, cfg, x, fill, ws, scatter_first=False):
     score, mask, flag = tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule=cfg.rule, ws=ws)
     comp = tee.exit_compact(mask, h=x["h_cur"], ws=ws)
-    fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=comp["exit_rows"], pos=x["pos"], seq=x["seq"],
-         n_dev=comp["counts"][1:], n_max=cfg.batch, ws=ws)
     out = torch.full_like(x["h_cur"], -3.0)
-    tee.exit_scatter(comp["counts"], comp["exit_rows"], comp["exit_pos"], x["h_cur"], out, ws=ws)
+
+    def do_fill():
+        fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=comp["exit_rows"], pos=x["pos"], seq=x["seq"],
+             n_dev=comp["counts"][1:], n_max=cfg.batch, ws=ws)
+
+    def do_scatter():
+        tee.exit_scatter(comp["counts"], comp["exit_rows"], comp["exit_pos"], x["h_cur"], out, ws=ws)
+
+    if scatter_first:   # the fill then follows the scatter kernel directly (early launch)
+        do_scatter()
+        do_fill()
+    else:
+        do_fill()
+        do_scatter()
     return score, mask, flag, comp, out
 
 
-@pytest.mark.parametrize("cfg,case,seed", [(configs.TINY_DECODE, "default", s) for s in range(4)] +
-                         [(configs.LLAMA1B_DECODE, c, s) for c in ("exit", "stay") for s in range(2)])
-def test_decode_step(tee, cfg, case, seed):
+@pytest.mark.parametrize("cfg,case,seed,early", [(configs.TINY_DECODE, "default", s, False) for s in range(4)] +
+                         [(configs.LLAMA1B_DECODE, c, s, False) for c in ("exit", "stay") for s in range(2)] +
+                         [(configs.LLAMA1B_DECODE, c, s, True) for c in ("exit", "stay") for s in range(2)])
+def test_decode_step(tee, cfg, case, seed, early):
+    # early: the fill launches while the scatter runs and reads h, rows, counts only
+    # after it completes (TEE_FILL_EARLY_WEIGHTS)
     x = gen.decode_inputs(cfg, seed=seed, device=DEV, case=case)
     ws = tee.Workspace(DEV)
     fill = tee.KVFill(x["layers"], d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
                       rope_base=cfg.rope_base, eps=cfg.eps, dtype=x["h_cur"].dtype, max_pos=cfg.cache_len,
-                      int4=cfg.weights == "int4", group=cfg.group)
-    score, mask, flag, comp, out = run_step(tee, cfg, x, fill, ws)
+                      int4=cfg.weights == "int4", group=cfg.group, early_weights=early)
+    score, mask, flag, comp, out = run_step(tee, cfg, x, fill, ws, scatter_first=early)
     assert ws.device_error() == (0, 0)
     hp, hc = f64(x["h_prev"]), f64(x["h_cur"])
     s_ref, m_ref, f_ref = oracle.cosine_gate(hp, hc, cfg.tau, cfg.rule)

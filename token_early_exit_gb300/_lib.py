@@ -26,9 +26,12 @@ class GateDesc(ctypes.Structure):
                 ("bottleneck", c_int32), ("threshold", c_float), ("eps", c_float)]
 
 
+TEE_FILL_EARLY_WEIGHTS = 1
+
+
 class FillDesc(ctypes.Structure):
     _fields_ = [("d", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32), ("rope_base", c_float),
-                ("eps", c_float), ("dtype", c_int32), ("wfmt", c_int32), ("group", c_int32)]
+                ("eps", c_float), ("dtype", c_int32), ("wfmt", c_int32), ("group", c_int32), ("flags", c_int32)]
 
 
 class FillLayer(ctypes.Structure):

@@ -112,6 +112,17 @@ __device__ __forceinline__ void warp_copy16(uint4* __restrict__ dst, const uint4
     }
 }
 
+// ------------------------------------------------------------ dependent launches
+// Let a kernel enqueued after this one with programmatic stream serialization
+// start now; it waits for this grid to complete before reading what it writes.
+__device__ __forceinline__ void allow_dependents() {
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// In a kernel launched with programmatic stream serialization: wait until the
+// kernel enqueued before it has completed and its writes are visible (returns
+// at once otherwise).
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------ reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

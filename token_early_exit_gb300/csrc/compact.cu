@@ -77,6 +77,7 @@ compact_kernel(int n, int R, const uint8_t* __restrict__ mask, const int32_t* __
                int32_t* __restrict__ cont_rows, int32_t* __restrict__ exit_rows, int32_t* __restrict__ cont_pos,
                int32_t* __restrict__ exit_pos, T* __restrict__ h_cont, int64_t ld_cont,
                int32_t* __restrict__ counts) {
+    allow_dependents();
     __shared__ unsigned s_red[CP_WARPS];
     __shared__ unsigned s_wexit[CP_WARPS];
     __shared__ int s_src[256];
@@ -156,6 +157,7 @@ scatter_kernel(int n_max, const int32_t* __restrict__ counts, const int32_t* __r
                const int32_t* __restrict__ exit_pos, const T* __restrict__ h_src, int64_t ld_src,
                T* __restrict__ out, int64_t ld_out, int64_t n_out, int d, const T* __restrict__ gamma, float eps,
                void* ws) {
+    allow_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // The row lists hold n_max entries: read this warp's first entries together with
     // the count instead of after it (one dependent load fewer on the critical path).

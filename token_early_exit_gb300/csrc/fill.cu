@@ -287,6 +287,7 @@ static tee_status check_fill_desc(const tee_fill_desc* D) {
     if (dtype_bytes(D->dtype) == 0) return TEE_ERR_UNSUPPORTED;
     if (D->wfmt != TEE_W_DENSE && D->wfmt != TEE_W_INT4) return TEE_ERR_UNSUPPORTED;
     if (D->wfmt == TEE_W_INT4 && (D->group <= 0 || D->group % 16 || D->d % D->group)) return TEE_ERR_INVALID_ARG;
+    if (D->flags & ~TEE_FILL_EARLY_WEIGHTS) return TEE_ERR_INVALID_ARG;
     return TEE_OK;
 }
 

@@ -5,10 +5,10 @@
 // Work split. The K and V projections of one filled layer are cut into groups
 // of 256 output columns, and the reduction dimension d into KS equal ranges.
 // One cluster of KS CTAs per (group, layer): CTA r computes, on tcgen05,
-//   P_r[item][c] = sum_{k in range r} (h[row(item)][k] g_j[k]) * W[k][c],
-//   W[k][c] = (q - zero) * scale     (M = 128 item rows, N = 256, K = d / KS)
+//   P_r[item][c] = sum_{k in range r} h[row(item)][k] * W'[k][c],
+//   W'[k][c] = (q - zero) * scale * g_j[k]     (M = 128 item rows, N = 256, K = d / KS)
 // and the partial sums of h^2 over its range; the CTAs then add their partials
-// through distributed shared memory. A group is four units of 64 columns, each
+// through the workspace (L2). A group is four units of 64 columns, each
 // unit the two 32-wide halves [i, i+32) and [i+hd/2, i+hd/2+32) of one head,
 // so that RoPE pairs stay inside a unit; unit u is finished by the CTA of rank
 // u % KS: sum of the KS partials, 1/rms over the whole d, RoPE, bf16 store
@@ -18,20 +18,18 @@
 //   warps 0-7   stream the CTA's int4 codes and fp16 scales/zeros (cp.async, 256-k
 //               chunks, two in flight) and dequantise each 64-k block into a ring
 //               of bf16 B operands (256 rows of 128 bytes, 128-byte swizzle):
-//               W[k][c] = (q - z) s, in packed bf16x2 arithmetic;
+//               W'[k][c] = (q - z) s g_j[k], in packed bf16x2 arithmetic;
 //   warp 8      issues tcgen05.mma (N = 256) into a 256-column TMEM accumulator;
 //   warps 9-12  gather the items' h rows of each 64-k block into a ring of A
 //               operands (cp.async, 128-byte swizzle), after asking L2 for the
 //               rows' slices at the start. Once a thread's pieces of a block have
-//               landed it adds their squares into per-item sums of h^2 and scales
-//               them by the RMSNorm gain g_j in place (A = h * g_j), then releases
-//               the block; they also fetch positions and cache slots.
-// After the last MMA, in rounds of 64 item rows: warps 0-7 copy the accumulator
-// rows (thread = item row) into shared memory per unit, with the row's partial
-// sum of h^2 in the padding; a cluster barrier; one thread sends each unit's
-// rows to its finishing CTA with a bulk shared::cluster copy that completes on
-// the receiver's mbarrier; the receivers add the partials and finish; a
-// cluster barrier closes the round.
+//               landed it adds their squares into per-item sums of h^2 and
+//               releases the block; they also fetch positions and cache slots.
+// After the last MMA warps 0-7 store the accumulator rows (thread = item row,
+// TMEM lane quarter = warp % 4) and the partial sums of h^2 into this CTA's slot
+// of the workspace with coalesced 16-byte stores; one cluster barrier (release /
+// acquire at cluster scope); then warps 0-7 of each CTA read the KS partials of
+// their units from L2, add them and finish.
 #include "fill.cuh"
 #include "tc.cuh"
 
@@ -71,19 +69,8 @@ constexpr uint32_t OFF_B = OFF_A + D_RA * A_SLOT;
 constexpr uint32_t OFF_C = OFF_B + D_RB * B_SLOT;
 constexpr uint32_t OFF_G = OFF_C + D_RC * CH_BYTES;               // g_j over this CTA's k range (bf16)
 constexpr uint32_t OFF_SMALL = OFF_G + D_MAX_KC * 2;
-constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * D_RB + 3) * 8 + D_MAX_ITEMS * (8 + 4 + 4) + 16;
+constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * D_RB + 2) * 8 + D_MAX_ITEMS * (8 + 4 + 4) + 16;
 constexpr size_t D_SMEM = 1024 + OFF_SMALL + SMALL_BYTES;
-// After the main loop the operand and code rings hold, per round of 64 item rows, this CTA's
-// partials [unit][row][P_LD floats] (64 unit columns, then the row's partial sum of
-// h^2, padding) and the partials received for the units it finishes
-// [slot = source rank * units per CTA + owned unit][row][P_LD floats].
-constexpr int P_LD = 68;
-constexpr int P_ROWS = 64;
-constexpr uint32_t P_ROW_BYTES = P_LD * 4;
-constexpr uint32_t P_TILE = P_ROWS * P_ROW_BYTES;
-constexpr uint32_t OFF_STG = 0;
-constexpr uint32_t OFF_RCV = OFF_STG + D_UNITS * P_TILE;
-static_assert(OFF_RCV + D_UNITS * P_TILE <= OFF_G, "the partials fit in the operand and code rings");
 static_assert(D_SMEM <= 232448, "decode fill shared memory");
 static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_G % 16 == 0 && OFF_SMALL % 8 == 0, "alignment");
 
@@ -112,6 +99,8 @@ struct DecodeArgs {
     bf16* kc;
     bf16* vc;
     tee_cache_layout cl;
+    float4* part;   // workspace: [cluster][rank][unit][16][n_max] float4 partial accumulators
+    float* part_ss; // workspace: [cluster][rank][n_max] partial sums of h^2
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -150,13 +139,14 @@ __device__ __forceinline__ float sumsq8(uint4 x, float acc) {
 // Two consecutive k of one column from byte b of a packed word (low nibble = the
 // lower k): x = (b & 0xF) | (b >> 4) << 16 | 0x43004300 is the bf16 pair 128 + q;
 // subtracting 136 leaves q - 8 exactly, and one bf16x2 fma gives
-// (q - 8) s + (8 - z) s = (q - z) s, rounded once. wl / wh: the packed word and the
-// word shifted right by 4; sel picks byte b of each into bytes 0 and 2.
+// (q - 8) s + (8 - z) s = (q - z) s, rounded once, then the RMSNorm gains of the
+// two k (rounded again). wl / wh: the packed word and the word shifted right by 4;
+// sel picks byte b of each into bytes 0 and 2.
 __device__ __forceinline__ uint32_t deq_pair(uint32_t wl, uint32_t wh, uint32_t sel, __nv_bfloat162 s2,
-                                             __nv_bfloat162 zs2) {
+                                             __nv_bfloat162 zs2, __nv_bfloat162 g2) {
     const uint32_t x = (__byte_perm(wl, wh, sel) & 0x000F000Fu) | 0x43004300u;
     __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&x);
-    v = __hfma2(__hsub2(v, __floats2bfloat162_rn(136.0f, 136.0f)), s2, zs2);
+    v = __hmul2(__hfma2(__hsub2(v, __floats2bfloat162_rn(136.0f, 136.0f)), s2, zs2), g2);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -167,17 +157,17 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
+// L2-only loads of what peer CTAs wrote before the cluster barrier (that barrier's
+// asm carries the memory clobber, so these cannot move above it).
+__device__ __forceinline__ float4 ld_l2_f4(const float4* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
 }
-// Bulk copy of bytes from this CTA's shared memory to a cluster peer's, completing
-// on the peer's mbarrier (both given as shared::cluster addresses).
-__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
-    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "r"(src), "r"(bytes), "r"(mbar)
-                 : "memory");
+__device__ __forceinline__ float ld_l2_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
 }
 
 // First column of unit u's low and high halves within the K (or V) projection.
@@ -196,8 +186,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     uint64_t* b_empty = b_full + D_RB;
     uint64_t* acc_full = b_empty + D_RB;
     uint64_t* ss_ready = acc_full + 1;
-    uint64_t* recv_full = ss_ready + 1;
-    int64_t* s_ioff = reinterpret_cast<int64_t*>(recv_full + 1);   // item part of the cache offset, or -1
+    int64_t* s_ioff = reinterpret_cast<int64_t*>(ss_ready + 1);   // item part of the cache offset, or -1
     int* s_pos = reinterpret_cast<int*>(s_ioff + D_MAX_ITEMS);
     float* s_ss = reinterpret_cast<float*>(s_pos + D_MAX_ITEMS);  // partial sum(h^2) over this CTA's k
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_ss + D_MAX_ITEMS);
@@ -213,7 +202,9 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kc = a.d / ks, k0 = rank * kc;     // this CTA's k range
     const int nkb = kc / D_KB, nch = kc / D_CH;
-    const int n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
+    // The item count (and everything else a previous kernel may produce) is read only
+    // after wait_prior_grid(): with an early launch the weights stream in before that.
+    int n = 0;
     const bool reporter = blockIdx.x == 0 && li == 0;   // one CTA records bad rows / positions
 
     if (threadIdx.x == 0) {
@@ -227,29 +218,35 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         }
         tc::mbar_init(acc_full, 1);
         tc::mbar_init(ss_ready, D_CP_WARPS);
-        tc::mbar_init(recv_full, 1);
         *abort = 0;
         tc::fence_barrier_init();
     }
     // Chunk c of the CTA's codes / scales / zeros into ring slot c % D_RC. Staged
     // column order: unit u's low half, then its high half (64 u .. 64 u + 63).
+    // Per-thread pieces of a chunk (dequant warps): code piece p = t % 16 of packed
+    // rows t / 16 + 16 i, and scale/zero piece t (group, which, unit, half, quarter).
+    const int p_code = threadIdx.x & 15, r_code = threadIdx.x >> 4;
+    const int col_code = unit_col_lo(gk, p_code >> 2, a.hd) + ((p_code & 3) >= 2 ? a.half : 0) + (p_code & 1) * 16;
+    const int g_sz = (threadIdx.x >> 6) & 3, which_sz = (threadIdx.x >> 5) & 1, p_sz = threadIdx.x & 31;
+    const int col_sz = unit_col_lo(gk, p_sz >> 3, a.hd) + (((p_sz >> 2) & 1) ? a.half : 0) + (p_sz & 3) * 8;
+    const uint32_t off_sz = CH_CODES + g_sz * (D_GCOLS * 4) + which_sz * (D_GCOLS * 2) +
+                            ((p_sz >> 3) * 64 + ((p_sz >> 2) & 1) * 32 + (p_sz & 3) * 8) * 2;
+    // Chunk c of the CTA's codes / scales / zeros into ring slot c % D_RC. Staged
+    // column order: unit u's low half, then its high half (64 u .. 64 u + 63).
     auto load_chunk = [&](int c) {
         uint8_t* base = smem + OFF_C + (c % D_RC) * CH_BYTES;
         const int kg = k0 + c * D_CH;             // first k of the chunk
-        for (int v = threadIdx.x; v < (D_CH / 2) * 16; v += D_DEQ_THREADS) {
-            const int r = v >> 4, p = v & 15, u = p >> 2, part = p & 3;
-            const int col = unit_col_lo(gk, u, a.hd) + (part >= 2 ? a.half : 0) + (part & 1) * 16;
-            cp_async16(base + r * D_GCOLS + p * 16, L.codes[kv] + static_cast<int64_t>(kg / 2 + r) * a.kvw + col);
-        }
-        for (int v = threadIdx.x; v < D_BPC * 64; v += D_DEQ_THREADS) {
-            // group g, scale or zero, unit u, half: 32 fp16 = 4 pieces
-            const int g = v >> 6, which = (v >> 5) & 1, p = v & 31, u = p >> 3, hp = (p >> 2) & 1, q = p & 3;
-            const int col = unit_col_lo(gk, u, a.hd) + (hp ? a.half : 0) + q * 8;
-            const __half* src = (which ? L.zero[kv] : L.scale[kv]) + static_cast<int64_t>(kg / D_KB + g) * a.kvw + col;
-            cp_async16(base + CH_CODES + g * (D_GCOLS * 4) + which * (D_GCOLS * 2) + (u * 64 + hp * 32 + q * 8) * 2, src);
-        }
+        const uint8_t* src = L.codes[kv] + static_cast<int64_t>(kg / 2 + r_code) * a.kvw + col_code;
+#pragma unroll
+        for (int i = 0; i < (D_CH / 2) / 16; ++i)
+            cp_async16(base + (r_code + 16 * i) * D_GCOLS + p_code * 16, src + static_cast<int64_t>(16 * i) * a.kvw);
+        static_assert(D_BPC * 64 == D_DEQ_THREADS, "one scale/zero piece per thread");
+        cp_async16(base + off_sz,
+                   (which_sz ? L.zero[kv] : L.scale[kv]) + static_cast<int64_t>(kg / D_KB + g_sz) * a.kvw + col_sz);
     };
     if (warp < D_DEQ_WARPS) {
+        // g_j over this CTA's k range rides in chunk 0's group.
+        for (int v = threadIdx.x; v < kc / 8; v += D_DEQ_THREADS) cp_async16(smem + OFF_G + v * 16, L.gamma + k0 + v * 8);
         for (int c = 0; c < D_RC; ++c) {
             if (c < nch) load_chunk(c);
             cp_async_commit();
@@ -293,6 +290,10 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                 unpack_f16x2(s4.y, sc[2], sc[3]);
                 unpack_f16x2(z4.x, zr[0], zr[1]);
                 unpack_f16x2(z4.y, zr[2], zr[3]);
+                // g_j of the thread's 16 k, as 8 bf16 pairs (k 16 kq + 2i, +1)
+                const uint4 ga = *reinterpret_cast<const uint4*>(smem + OFF_G + (kb * D_KB + kq * 16) * 2);
+                const uint4 gb = *reinterpret_cast<const uint4*>(smem + OFF_G + (kb * D_KB + kq * 16 + 8) * 2);
+                const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
                 uint8_t* bslot = smem + OFF_B + s * B_SLOT;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -302,7 +303,8 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                     const uint32_t sel = (j | (j << 4) | ((j + 4) << 8) | ((j + 4) << 12));
                     uint32_t o[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) o[i] = deq_pair(w[i], wh[i], sel, s2, zs2);   // k 16 kq + 2i, +1
+                    for (int i = 0; i < 8; ++i)   // k 16 kq + 2i, +1
+                        o[i] = deq_pair(w[i], wh[i], sel, s2, zs2, *reinterpret_cast<const __nv_bfloat162*>(&gw[i]));
                     const int row = cg + 64 * j;
                     uint8_t* rp = bslot + row * 128;
                     *reinterpret_cast<uint4*>(rp + (((2 * kq) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -341,9 +343,8 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         // their squares and scales them by g_j in place.
         const int ct = threadIdx.x - D_CP_WARP0 * 32;
         const int j = ct & 7, ib = ct >> 3;
-        // This CTA's slice of g_j (landed before the first release, see below).
-        for (int v = ct; v < kc / 8; v += D_CP_THREADS) cp_async16(smem + OFF_G + v * 16, L.gamma + k0 + v * 8);
-        cp_async_commit();   // the oldest group
+        wait_prior_grid();
+        n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
         // Item ct's h row slice, pulled into L2 whole (every CTA of the column groups
         // reads it).
         int r_ct = -1;
@@ -374,33 +375,21 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         float ss[D_ITEMS_PER_CP];
 #pragma unroll
         for (int m = 0; m < D_ITEMS_PER_CP; ++m) ss[m] = 0.f;
-        // Block kb's pieces of this thread have landed: add their squares, scale them
-        // by g_j (bf16 x bf16 -> bf16, one rounding), order them for the tensor core,
-        // and release the block once the whole warp is done.
+        // Block kb's pieces of this thread have landed: add their squares, order them
+        // for the tensor core, and release the block once the whole warp is done.
         auto release = [&](int kb) {
-            uint8_t* slot = smem + OFF_A + (kb % D_RA) * A_SLOT;
-            const uint4 gp = *reinterpret_cast<const uint4*>(smem + OFF_G + (kb * D_KB + 8 * j) * 2);
-            const __nv_bfloat162* gv = reinterpret_cast<const __nv_bfloat162*>(&gp);
+            const uint8_t* slot = smem + OFF_A + (kb % D_RA) * A_SLOT;
 #pragma unroll
             for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
                 if (!src[m]) continue;
                 const int i = ib + 16 * m;
-                uint4* pp = reinterpret_cast<uint4*>(slot + i * 128 + ((j ^ (i & 7)) << 4));
-                uint4 x = *pp;
-                ss[m] = sumsq8(x, ss[m]);
-                __nv_bfloat162* xv = reinterpret_cast<__nv_bfloat162*>(&x);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) xv[e] = __hmul2(xv[e], gv[e]);
-                *pp = x;
+                ss[m] = sumsq8(*reinterpret_cast<const uint4*>(slot + i * 128 + ((j ^ (i & 7)) << 4)), ss[m]);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&a_full[kb % D_RA]);
         };
-        // The g_j slice comes from every copier: they meet once, after their first wait.
-        auto g_ready = [&]() { asm volatile("bar.sync 2, %0;" ::"n"(D_CP_THREADS) : "memory"); };
         bool ok = true;
-        int waited = 0;
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % D_RA;
             if (kb >= D_RA && !warp_wait(&a_empty[s], ((kb / D_RA) - 1) & 1, abort, ws, 52)) {
@@ -411,15 +400,10 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             cp_async_commit();
             if (kb >= D_LAG) {
                 cp_async_wait<D_LAG>();
-                if (!waited) {
-                    g_ready();
-                    waited = 1;
-                }
                 release(kb - D_LAG);
             }
         }
         cp_async_wait<0>();
-        if (!waited) g_ready();   // every copier reaches the meeting exactly once
         if (ok)
             for (int b = max(0, nkb - D_LAG); b < nkb; ++b) release(b);
         // Per-item totals: the eight threads of an item are consecutive lanes.
@@ -455,113 +439,113 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         if (lane == 0) tc::mbar_arrive(ss_ready);   // release: s_ss, s_ioff, s_pos are ready
     }
 
-    // ---- the reduction across the cluster, in rounds of 64 item rows.
+    wait_prior_grid();
+    n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
+    // ---- the reduction across the cluster, through this call's workspace slots.
     // Accumulator column cg + 64 j holds staged column 4 cg + j, i.e. unit cg / 16,
-    // unit column 4 (cg % 16) + j.
+    // unit column 4 (cg % 16) + j: float4 m = cg % 16 of a unit row holds its
+    // unit columns 4m .. 4m + 3.
+    const int cluster = blockIdx.y * (gridDim.x / ks) + gq;
+    float4* part = a.part + static_cast<int64_t>(cluster) * ks * D_UNITS * 16 * a.n_max;
+    float* part_ss = a.part_ss + static_cast<int64_t>(cluster) * ks * a.n_max;
     bool acc_ok = true;
     if (warp < D_DEQ_WARPS) {
         acc_ok = warp_wait(acc_full, 0, abort, ws, 56);
         acc_ok = warp_wait(ss_ready, 0, abort, ws, 57) && acc_ok;   // s_ss, s_ioff, s_pos
         tc::tc_fence_after();
-    }
-    const int upr = D_UNITS / ks;   // units finished per CTA
-    const uint32_t stg_s = tc::smem_u32(smem + OFF_STG), rcv_s = tc::smem_u32(smem + OFF_RCV);
-    const float* stg = reinterpret_cast<const float*>(smem + OFF_STG);
-    const float* rcv = reinterpret_cast<const float*>(smem + OFF_RCV);
-    const int rounds = (n + P_ROWS - 1) / P_ROWS;
-    for (int round = 0; round < rounds; ++round) {
-        const int r0 = round * P_ROWS, nr = min(P_ROWS, n - r0);
-        if (threadIdx.x == 0 && ks > 1)
-            tc::mbar_arrive_expect_tx(recv_full, static_cast<uint32_t>(upr * (ks - 1) * nr) * P_ROW_BYTES);
-        // Rows r0 .. r0 + 63 sit in TMEM lane quarters 2 round, 2 round + 1: warps w with
-        // w % 4 in those quarters read them, units 0-1 (w < 4) or 2-3 (w >= 4).
-        if (warp < D_DEQ_WARPS && (warp & 3) / 2 == round) {
-            const int r = (warp & 3) * 32 + lane, rl = r - r0;
-            const uint32_t tb = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        // Warp w reads TMEM lane quarter w % 4 (item rows 32 (w % 4) + lane), units
+        // 2 (w / 4) and 2 (w / 4) + 1; consecutive lanes store consecutive rows.
+        const int r = (warp & 3) * 32 + lane;
+        const uint32_t tb = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 #pragma unroll 1
-            for (int u = 2 * (warp >> 2); u < 2 * (warp >> 2) + 2; ++u) {
-                float v[4][16];
+        for (int u = 2 * (warp >> 2); u < 2 * (warp >> 2) + 2; ++u) {
+            float v[4][16];
+            tc::tmem_ld16x4(tb + 16 * u, 64, v);   // warp-wide
+            if (acc_ok && r < n) {
+                float4* dst = part + static_cast<int64_t>((rank * D_UNITS + u) * 16) * a.n_max + r;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) tc::tmem_ld16(tb + 16 * u + 64 * j, v[j]);   // warp-wide
-                if (rl < nr) {
-                    float* row = reinterpret_cast<float*>(smem + OFF_STG + u * P_TILE + rl * P_ROW_BYTES);
-#pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        *reinterpret_cast<float4*>(row + 4 * m) = make_float4(v[0][m], v[1][m], v[2][m], v[3][m]);
-                    row[64] = s_ss[r];
-                }
+                for (int m = 0; m < 16; ++m) dst[static_cast<int64_t>(m) * a.n_max] = make_float4(v[0][m], v[1][m], v[2][m], v[3][m]);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read next by the bulk copies
         }
-        tc::tc_fence_before();
-        __syncthreads();
-        cluster_sync();   // partials staged everywhere; every receiver's rings are free
-        tc::tc_fence_after();
-        if (threadIdx.x == 0)
-            for (int u = 0; u < D_UNITS; ++u) {
-                const int owner = u % ks;
-                if (owner == rank) continue;
-                const int slot = rank * upr + u / ks;
-                bulk_to_peer(map_rank(rcv_s + slot * P_TILE, owner), stg_s + u * P_TILE,
-                             static_cast<uint32_t>(nr) * P_ROW_BYTES, map_rank(tc::smem_u32(recv_full), owner));
-            }
-        // ---- finish the units of this rank: warps 0-7, thread = (item, 8 column pairs).
-        if (warp < D_DEQ_WARPS) {
-            const bool got = ks == 1 || warp_wait(recv_full, round & 1, abort, ws, 58);
-            const int t = threadIdx.x, q = t & 3, il = t >> 2, i = r0 + il;
-            if (got && acc_ok && !*abort && il < nr && s_ioff[i] >= 0) {
-                const int64_t ioff = s_ioff[i];
-                for (int ul = 0; ul < upr; ++ul) {
-                    const int u = rank + ul * ks;
-                    const int col_lo = unit_col_lo(gk, u, a.hd);
-                    const int head = col_lo / a.hd, seg_off = col_lo - head * a.hd;   // 32 * segment
-                    float lo[8], hi[8], ss = 0.f;
+        if (warp < 4 && acc_ok && r < n) part_ss[rank * a.n_max + r] = s_ss[r];
+    }
+    tc::tc_fence_before();
+    cluster_sync();   // every CTA's partials are visible to the cluster
+    tc::tc_fence_after();
+
+    // ---- finish the units of this rank: warps 0-7, thread = (item, 8 column pairs).
+    if (warp < D_DEQ_WARPS && acc_ok && !*abort) {
+        const int t = threadIdx.x, q = t & 3;
+        const int upr = D_UNITS / ks;   // units finished per CTA
+        for (int i = t >> 2; i < n; i += D_DEQ_THREADS / 4) {
+            const int64_t ioff = s_ioff[i];
+            if (ioff < 0) continue;
+            // Every load of the item is issued before any of them is used (one L2
+            // round trip), then the sums.
+            float ssv[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) lo[e] = hi[e] = 0.f;
-                    for (int src = 0; src < ks; ++src) {
-                        const float* row = (src == rank ? stg + (u * P_ROWS + il) * P_LD
-                                                        : rcv + ((src * upr + ul) * P_ROWS + il) * P_LD);
-                        const float4 l0 = *reinterpret_cast<const float4*>(row + 8 * q);
-                        const float4 l1 = *reinterpret_cast<const float4*>(row + 8 * q + 4);
-                        const float4 h0 = *reinterpret_cast<const float4*>(row + 32 + 8 * q);
-                        const float4 h1 = *reinterpret_cast<const float4*>(row + 32 + 8 * q + 4);
-                        lo[0] += l0.x; lo[1] += l0.y; lo[2] += l0.z; lo[3] += l0.w;
-                        lo[4] += l1.x; lo[5] += l1.y; lo[6] += l1.z; lo[7] += l1.w;
-                        hi[0] += h0.x; hi[1] += h0.y; hi[2] += h0.z; hi[3] += h0.w;
-                        hi[4] += h1.x; hi[5] += h1.y; hi[6] += h1.z; hi[7] += h1.w;
-                        ss += row[64];
-                    }
-                    const float rs = 1.0f / sqrtf(ss * a.inv_d + a.eps);
-                    if (is_k) {
-                        const float4* cs = reinterpret_cast<const float4*>(
-                            a.rope + static_cast<int64_t>(s_pos[i]) * a.half + seg_off + 8 * q);
+            for (int src = 0; src < 4; ++src) ssv[src] = src < ks ? ld_l2_f32(part_ss + src * a.n_max + i) : 0.f;
+            for (int ul = 0; ul < upr; ++ul) {
+                const int u = rank + ul * ks;
+                const int col_lo = unit_col_lo(gk, u, a.hd);
+                const int head = col_lo / a.hd, seg_off = col_lo - head * a.hd;   // 32 * segment
+                float4 pv[4][4];
 #pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const float4 c2 = __ldg(cs + e2);   // {cos, sin} of two pairs
-                            const float x1 = lo[2 * e2] * rs, x2 = hi[2 * e2] * rs;
-                            const float y1 = lo[2 * e2 + 1] * rs, y2 = hi[2 * e2 + 1] * rs;
-                            lo[2 * e2] = x1 * c2.x - x2 * c2.y;
-                            hi[2 * e2] = x2 * c2.x + x1 * c2.y;
-                            lo[2 * e2 + 1] = y1 * c2.z - y2 * c2.w;
-                            hi[2 * e2 + 1] = y2 * c2.z + y1 * c2.w;
-                        }
+                for (int src = 0; src < 4; ++src) {
+                    if (src < ks) {
+                        const float4* row = part + static_cast<int64_t>((src * D_UNITS + u) * 16) * a.n_max + i;
+                        pv[src][0] = ld_l2_f4(row + static_cast<int64_t>(2 * q) * a.n_max);
+                        pv[src][1] = ld_l2_f4(row + static_cast<int64_t>(2 * q + 1) * a.n_max);
+                        pv[src][2] = ld_l2_f4(row + static_cast<int64_t>(8 + 2 * q) * a.n_max);
+                        pv[src][3] = ld_l2_f4(row + static_cast<int64_t>(9 + 2 * q) * a.n_max);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            lo[e] *= rs;
-                            hi[e] *= rs;
-                        }
+                        for (int e = 0; e < 4; ++e) pv[src][e] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    bf16* dst = (is_k ? a.kc : a.vc) + ioff + static_cast<int64_t>(head) * a.cl.s_head + seg_off + 8 * q;
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
-                                                                pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
-                    *reinterpret_cast<uint4*>(dst + a.half) =
-                        make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]), pack_bf16x2(hi[4], hi[5]),
-                                   pack_bf16x2(hi[6], hi[7]));
                 }
+                float4 c2[4];   // {cos, sin} of the 8 pairs (K only), with the partials
+                if (is_k) {
+                    const float4* cs = reinterpret_cast<const float4*>(a.rope + static_cast<int64_t>(s_pos[i]) * a.half +
+                                                                       seg_off + 8 * q);
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) c2[e2] = __ldg(cs + e2);
+                }
+                const float rs = 1.0f / sqrtf((ssv[0] + ssv[1] + ssv[2] + ssv[3]) * a.inv_d + a.eps);
+                float lo[8], hi[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) lo[e] = hi[e] = 0.f;
+#pragma unroll
+                for (int src = 0; src < 4; ++src) {
+                    const float4 l0 = pv[src][0], l1 = pv[src][1], h0 = pv[src][2], h1 = pv[src][3];
+                    lo[0] += l0.x; lo[1] += l0.y; lo[2] += l0.z; lo[3] += l0.w;
+                    lo[4] += l1.x; lo[5] += l1.y; lo[6] += l1.z; lo[7] += l1.w;
+                    hi[0] += h0.x; hi[1] += h0.y; hi[2] += h0.z; hi[3] += h0.w;
+                    hi[4] += h1.x; hi[5] += h1.y; hi[6] += h1.z; hi[7] += h1.w;
+                }
+                if (is_k) {
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const float x1 = lo[2 * e2] * rs, x2 = hi[2 * e2] * rs;
+                        const float y1 = lo[2 * e2 + 1] * rs, y2 = hi[2 * e2 + 1] * rs;
+                        lo[2 * e2] = x1 * c2[e2].x - x2 * c2[e2].y;
+                        hi[2 * e2] = x2 * c2[e2].x + x1 * c2[e2].y;
+                        lo[2 * e2 + 1] = y1 * c2[e2].z - y2 * c2[e2].w;
+                        hi[2 * e2 + 1] = y2 * c2[e2].z + y1 * c2[e2].w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        lo[e] *= rs;
+                        hi[e] *= rs;
+                    }
+                }
+                bf16* dst = (is_k ? a.kc : a.vc) + ioff + static_cast<int64_t>(head) * a.cl.s_head + seg_off + 8 * q;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                                                            pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+                *reinterpret_cast<uint4*>(dst + a.half) = make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]),
+                                                                     pack_bf16x2(hi[4], hi[5]), pack_bf16x2(hi[6], hi[7]));
             }
         }
-        cluster_sync();   // the round's copies have landed and been read: buffers reusable, peers may exit
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     tc::tc_fence_before();
@@ -599,19 +583,21 @@ int choose_ks(int d, int ctas_per_split, int max_clusters_4, int max_clusters_2)
     return 1;
 }
 
-tee_status launch(const DecodeArgs& a, dim3 grid, int ks, void* ws, cudaStream_t stream) {
+tee_status launch(const DecodeArgs& a, dim3 grid, int ks, bool early, void* ws, cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(D_THREADS);
     cfg.dynamicSmemBytes = D_SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = ks;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = early ? 2 : 1;
     const tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, fill_decode_kernel, a, ws));
     return st != TEE_OK ? st : launch_status();   // counts the launch
 }
@@ -636,12 +622,23 @@ int max_clusters(int ks) {
     return n;
 }
 
+// Workspace of the cross-CTA reduction: per cluster and rank, 64 float4 and one
+// float per item row.
+constexpr size_t D_PART_BUDGET = size_t(64) << 20;
+size_t part_bytes(int groups_kv, int n_layers, int ks, int n_max) {
+    const size_t rows = static_cast<size_t>(2 * groups_kv) * n_layers * ks * n_max;
+    return round_up(rows * D_UNITS * 16 * sizeof(float4), 256) + round_up(rows * sizeof(float), 256);
+}
+
 }  // namespace
 
 size_t fill_decode_ws_bytes(const tee_fill_desc& D, int n_layers, int n_max) {
-    (void)D;
-    (void)n_layers;
-    (void)n_max;
+    const int kvw = D.n_kv_heads * D.head_dim;
+    if (kvw <= 0 || kvw % D_GCOLS || n_max <= 0 || n_max > D_MAX_ITEMS) return TEE_WS_HEADER_BYTES;
+    for (int ks = 4; ks >= 1; ks >>= 1) {   // the largest split whose partials fit the budget
+        const size_t b = part_bytes(kvw / D_GCOLS, n_layers, ks, n_max);
+        if (b <= D_PART_BUDGET) return TEE_WS_HEADER_BYTES + b;
+    }
     return TEE_WS_HEADER_BYTES;
 }
 
@@ -690,8 +687,22 @@ tee_status fill_decode_run(const FillCall& fc) {
     }
     const int splits = 2 * a.groups_kv * fc.n_layers;   // (group, layer) pairs
     a.ks = choose_ks(D.d, splits, mc4, mc2);
-    if (D.d / a.ks > D_MAX_KC) return TEE_ERR_UNSUPPORTED;
-    return launch(a, dim3(2 * a.groups_kv * a.ks, fc.n_layers), a.ks, fc.ws, fc.stream);
+    while (a.ks > 1 && TEE_WS_HEADER_BYTES + part_bytes(a.groups_kv, fc.n_layers, a.ks, fc.n_max) > fc.ws_bytes)
+        a.ks >>= 1;   // a smaller split needs smaller partials
+    if (TEE_WS_HEADER_BYTES + part_bytes(a.groups_kv, fc.n_layers, a.ks, fc.n_max) > fc.ws_bytes ||
+        D.d / a.ks > D_MAX_KC)
+        return TEE_ERR_UNSUPPORTED;
+    {
+        char* p = static_cast<char*>(fc.ws) + TEE_WS_HEADER_BYTES;
+        const size_t rows = static_cast<size_t>(2 * a.groups_kv) * fc.n_layers * a.ks * fc.n_max;
+        a.part = reinterpret_cast<float4*>(p);
+        a.part_ss = reinterpret_cast<float*>(p + round_up(rows * D_UNITS * 16 * sizeof(float4), 256));
+    }
+    const dim3 grid(2 * a.groups_kv * a.ks, fc.n_layers);
+    // An early launch parks the grid's CTAs on their SMs until the previous kernel
+    // completes: only when the grid leaves SMs free for that kernel to finish on.
+    const bool early = (D.flags & TEE_FILL_EARLY_WEIGHTS) && static_cast<int>(grid.x * grid.y) + 4 <= sm_count();
+    return launch(a, grid, a.ks, early, fc.ws, fc.stream);
 }
 
 }  // namespace tee

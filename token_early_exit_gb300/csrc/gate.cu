@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(GATE_WARPS * 32)
 cosine_gate_kernel(int n, int d, const T* __restrict__ hc, int64_t ldc, const T* __restrict__ hp,
                    int64_t ldp, float thr, int rule, bool need_flag, float* __restrict__ score,
                    uint8_t* __restrict__ mask, int32_t* __restrict__ flag, void* ws) {
+    allow_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float wmin = INFINITY;
     for (int t = blockIdx.x * GATE_WARPS + warp; t < n; t += gridDim.x * GATE_WARPS) {
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(GATE_WARPS * 32)
 cosine_gate_row_kernel(int n, int d, const T* __restrict__ hc, int64_t ldc, const T* __restrict__ hp, int64_t ldp,
                        float thr, int rule, bool need_flag, float* __restrict__ score, uint8_t* __restrict__ mask,
                        int32_t* __restrict__ flag, void* ws) {
+    allow_dependents();
     const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const T* a = hp + static_cast<int64_t>(t) * ldp;
     const T* b = hc + static_cast<int64_t>(t) * ldc;

@@ -166,6 +166,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Four 16-column loads (columns c, c + step, c + 2 step, c + 3 step of the
+// warp's lanes) behind a single wait.
+__device__ __forceinline__ void tmem_ld16x4(uint32_t taddr, uint32_t step, float (&v)[4][16]) {
+    uint32_t r[4][16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+            "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+            : "=r"(r[j][0]), "=r"(r[j][1]), "=r"(r[j][2]), "=r"(r[j][3]), "=r"(r[j][4]), "=r"(r[j][5]),
+              "=r"(r[j][6]), "=r"(r[j][7]), "=r"(r[j][8]), "=r"(r[j][9]), "=r"(r[j][10]), "=r"(r[j][11]),
+              "=r"(r[j][12]), "=r"(r[j][13]), "=r"(r[j][14]), "=r"(r[j][15])
+            : "r"(taddr + j * step));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[j][i] = __uint_as_float(r[j][i]);
+}
+
 // ------------------------------------------------------------------ UMMA
 // Shared-memory matrix descriptor, K-major operand stored as 128-byte rows
 // (64 bf16) with the 128-byte swizzle, 8-row groups 1024 bytes apart.

@@ -177,11 +177,12 @@ class KVFill:
     """
 
     def __init__(self, layers: Sequence[Dict], *, d: int, n_kv_heads: int, head_dim: int, rope_base: float,
-                 eps: float, dtype: torch.dtype, max_pos: int, int4: bool = False, group: int = 64):
+                 eps: float, dtype: torch.dtype, max_pos: int, int4: bool = False, group: int = 64,
+                 early_weights: bool = False):
         self.lib = load()
         self.desc = FillDesc(d=d, n_kv_heads=n_kv_heads, head_dim=head_dim, rope_base=float(rope_base),
                              eps=float(eps), dtype=_DT[dtype], wfmt=_lib.TEE_W_INT4 if int4 else _lib.TEE_W_DENSE,
-                             group=group)
+                             group=group, flags=_lib.TEE_FILL_EARLY_WEIGHTS if early_weights else 0)
         self.keep: List[torch.Tensor] = []
         arr = (FillLayer * max(1, len(layers)))()
         dev = None
