@@ -114,6 +114,10 @@ typedef struct {
     float eps;           /* RMSNorm epsilon of the router */
 } tee_gate_desc;
 
+/* Workspace for tee_exit_gate: the size at which the router's tensor-core path
+ * splits d across the most CTAs. The call also accepts less, down to the size
+ * its single-split path needs (about n * 516 bytes + 4 KiB at b = 128); below
+ * that it returns TEE_ERR_WORKSPACE. */
 TEE_API size_t tee_exit_gate_workspace_size(const tee_gate_desc* desc, int32_t n);
 
 /*
@@ -159,13 +163,14 @@ TEE_API tee_status tee_exit_gate(const tee_gate_desc* desc, int32_t n,
  * latency-critical loop where cudaMalloc is not allowed because it can block
  * or synchronise the device. It computes exactly what tee_exit_gate computes
  * in router mode (same kernels, same arguments without h_prev and without a
- * workspace), taking its scratch from a 4 MiB array compiled into the
+ * workspace; the tensor-core path splits d across fewer CTAs when the array is
+ * smaller than the size it would ask for), taking its scratch from a 4 MiB array compiled into the
  * library; every GPU that loads the library keeps that array until the
  * process exits. The call itself allocates nothing.
  *
- * Limit: the call is rejected with TEE_ERR_WORKSPACE when its scratch need,
- * tee_exit_gate_workspace_size(desc, n), exceeds
- * tee_exit_gate_router_static_max_bytes() (4 MiB), e.g. for more than about
+ * Limit: the call is rejected with TEE_ERR_WORKSPACE when the smallest scratch
+ * it can run with (see tee_exit_gate_workspace_size) exceeds
+ * tee_exit_gate_router_static_max_bytes() (4 MiB), i.e. for more than about
  * 8,000 tokens at bottleneck 128; desc->mode must be TEE_GATE_ROUTER.
  * Set-up: the first call on each device (the device current on the calling
  * thread) looks up the array's device address; make that first call before

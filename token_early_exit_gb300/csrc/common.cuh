@@ -22,7 +22,7 @@ __device__ __forceinline__ void record_fault(void* ws, int code, int detail) {
     if (atomicCAS(h + WS_ERR, 0, code) == 0) h[WS_DETAIL] = detail;
 }
 
-__device__ __forceinline__ uint32_t* ws_counter(void* ws, int idx) {
+__host__ __device__ __forceinline__ uint32_t* ws_counter(void* ws, int idx) {
     return reinterpret_cast<uint32_t*>(ws) + idx;
 }
 

@@ -268,11 +268,11 @@ router_finalize_kernel(int n, int d, int b, float eps, float* __restrict__ dots,
 #pragma unroll
         for (int j = 0; j < MAXC; ++j) {
             const float x = u[j] * r + bd[j];
-            z = fmaf(wu[j], x / (1.0f + expf(-x)), z);
+            z = fmaf(wu[j], __fdividef(x, 1.0f + __expf(-x)), z);   // SiLU (fast exp and divide: ~1e-6 relative)
         }
         z = warp_sum(z);
         if (b_up) z += b_up[0];
-        const float p = 1.0f / (1.0f + expf(-z));
+        const float p = __fdividef(1.0f, 1.0f + __expf(-z));
         if (lane == 0) {
             score[t] = p;
             if (rule == TEE_RULE_PER_TOKEN) mask[t] = exits(p, thr);
@@ -290,22 +290,26 @@ router_finalize_kernel(int n, int d, int b, float eps, float* __restrict__ dots,
                     ws_counter(ws, WS_CNT_ROUTER));
 }
 
-// Tensor-core router contraction (router_tc.cu). Returns TEE_ERR_UNSUPPORTED
-// when the shape does not fit it, so that the CUDA-core kernel runs instead.
-tee_status router_dots_tc(int n, int d, int b, int dtype, const void* h, int64_t ldh, const void* gamma,
-                          const void* w_down, float* dots, float* sumsq, void* ws, size_t ws_off,
-                          size_t ws_bytes, cudaStream_t stream);
+// Whole router gate on the tensor cores (router_tc.cu). Returns TEE_ERR_UNSUPPORTED
+// when the shape does not fit it, so that the CUDA-core kernels run instead.
+tee_status router_gate_tc(int n, int d, int b, int dtype, const void* h, int64_t ldh, const void* gamma,
+                          const void* w_down, const float* b_down, const void* w_up, const float* b_up, float eps,
+                          float thr, int rule, bool need_flag, float* score, uint8_t* mask, int32_t* flag,
+                          float* block_mins, uint32_t* counter, void* ws, size_t ws_off, size_t ws_bytes,
+                          cudaStream_t stream);
+size_t router_tc_scratch_bytes(int n, int d, int b);
+size_t router_tc_scratch_bytes_at(int n, int splits);
 
 static size_t gate_blocks(int n) {
     size_t blocks = (static_cast<size_t>(n) + GATE_WARPS - 1) / GATE_WARPS;
     return blocks < 1 ? 1 : (blocks > GATE_MAX_BLOCKS ? GATE_MAX_BLOCKS : blocks);
 }
 
-// Workspace: header | block minima (GATE_MAX_BLOCKS f32) | router dots [n][b] f32 | sumsq [n] f32 | tc scratch
+// Workspace: header | block minima (GATE_MAX_BLOCKS f32) | then either the CUDA-core
+// path's dots [n][b] f32 and sumsq [n] f32, or the tensor-core path's partials.
 static size_t router_dots_off() { return TEE_WS_HEADER_BYTES + GATE_MAX_BLOCKS * sizeof(float); }
 static size_t router_sumsq_off(int n, int b) { return round_up(router_dots_off() + static_cast<size_t>(n) * b * 4, 256); }
-static size_t router_tc_off(int n, int b) { return round_up(router_sumsq_off(n, b) + static_cast<size_t>(n) * 4, 256); }
-size_t router_tc_scratch_bytes(int n, int d, int b);
+static size_t router_core_end(int n, int b) { return round_up(router_sumsq_off(n, b) + static_cast<size_t>(n) * 4, 256); }
 
 template <typename T>
 static tee_status run_gate(const tee_gate_desc* g, int n, const void* h_cur, int64_t ld_cur, const void* h_prev,
@@ -329,9 +333,12 @@ static tee_status run_gate(const tee_gate_desc* g, int n, const void* h_cur, int
     const int b = g->bottleneck;
     float* dots = ws_at<float>(ws, router_dots_off());
     float* sumsq = ws_at<float>(ws, router_sumsq_off(n, b));
-    tee_status st = router_dots_tc(n, g->d, b, g->dtype, h_cur, ld_cur, gamma, w_down, dots, sumsq, ws,
-                                   router_tc_off(n, b), ws_bytes, stream);
-    if (st == TEE_ERR_UNSUPPORTED) {
+    tee_status st = router_gate_tc(n, g->d, b, g->dtype, h_cur, ld_cur, gamma, w_down, b_down, w_up, b_up, g->eps,
+                                   g->threshold, g->rule, need_flag, score, mask, flag,
+                                   ws_at<float>(ws, TEE_WS_HEADER_BYTES), ws_counter(ws, WS_CNT_ROUTER), ws,
+                                   router_dots_off(), ws_bytes, stream);
+    if (st != TEE_ERR_UNSUPPORTED) return st;   // the tensor-core kernel did the whole gate
+    {
         dim3 grid((n + RT_TOK - 1) / RT_TOK, (b + RT_WARPS * RT_CH_WARP - 1) / (RT_WARPS * RT_CH_WARP));
         const size_t smem = static_cast<size_t>(RT_TOK) * g->d * sizeof(float);
         if (smem > 48 * 1024) {
@@ -355,11 +362,25 @@ static tee_status run_gate(const tee_gate_desc* g, int n, const void* h_cur, int
 
 using namespace tee;
 
-extern "C" size_t tee_exit_gate_workspace_size(const tee_gate_desc* g, int32_t n) {
-    if (!g || n < 0) return 0;
+// Smallest workspace a call accepts: the router's tensor-core path then splits K
+// least (the size asked for by tee_exit_gate_workspace_size lets it split most).
+static size_t gate_min_workspace(const tee_gate_desc* g, int n) {
     if (g->mode == TEE_GATE_COSINE) return TEE_WS_HEADER_BYTES + GATE_MAX_BLOCKS * sizeof(float);
     const int b = g->bottleneck > 0 ? g->bottleneck : 128;
-    return router_tc_off(n, b) + router_tc_scratch_bytes(n, g->d, b);
+    const size_t core = router_core_end(n, b);
+    const size_t tc = router_dots_off() + router_tc_scratch_bytes_at(n, 1);
+    return core > tc ? core : tc;
+}
+
+extern "C" size_t tee_exit_gate_workspace_size(const tee_gate_desc* g, int32_t n) {
+    if (!g || n < 0) return 0;
+    if (g->mode == TEE_GATE_COSINE) return gate_min_workspace(g, n);
+    const int b = g->bottleneck > 0 ? g->bottleneck : 128;
+    const size_t core = router_core_end(n, b);
+    const size_t tc = router_dots_off() + router_tc_scratch_bytes(n, g->d, b);
+    const size_t m = core > tc ? core : tc;
+    const size_t lo = gate_min_workspace(g, n);
+    return m > lo ? m : lo;
 }
 
 extern "C" tee_status tee_exit_gate(const tee_gate_desc* g, int32_t n, const void* h_cur, int64_t ld_cur,
@@ -372,7 +393,7 @@ extern "C" tee_status tee_exit_gate(const tee_gate_desc* g, int32_t n, const voi
     if (g->threshold != g->threshold) return TEE_ERR_INVALID_ARG;
     const size_t es = dtype_bytes(g->dtype);
     if (es == 0) return TEE_ERR_UNSUPPORTED;
-    if (!ws || ws_bytes < tee_exit_gate_workspace_size(g, n)) return TEE_ERR_WORKSPACE;
+    if (!ws || ws_bytes < gate_min_workspace(g, n)) return TEE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (n == 0) {
         if (batch_flag) return cuda_status(cudaMemsetAsync(batch_flag, 0, sizeof(int32_t), s));
@@ -445,8 +466,8 @@ extern "C" tee_status tee_exit_gate_router_static(const tee_gate_desc* g, int32_
                                                   uint8_t* mask, int32_t* batch_flag, void* stream) {
     if (!g || g->mode != TEE_GATE_ROUTER) return TEE_ERR_INVALID_ARG;
     if (n < 0) return TEE_ERR_INVALID_ARG;
-    const size_t need = tee_exit_gate_workspace_size(g, n);
-    if (need == 0 || need > ROUTER_STATIC_SCRATCH_BYTES) return TEE_ERR_WORKSPACE;
+    const size_t need = gate_min_workspace(g, n);
+    if (need > ROUTER_STATIC_SCRATCH_BYTES) return TEE_ERR_WORKSPACE;
     void* scratch = nullptr;
     tee_status st = router_static_scratch(&scratch);
     if (st != TEE_OK) return st;
