@@ -8,7 +8,7 @@
 // M = 128 tokens x N = 128 router channels per tile; K = d split over KS CTAs so
 // that the batch spreads over the SMs. The KS CTAs of a token tile form a
 // cluster. In each CTA, warp 4 streams 128x64 tiles of h and W_down (already
-// K-major: TMA reads the caller's array) into a 4-stage ring (128-byte swizzle),
+// K-major: TMA reads the caller's array) into a 6-stage ring (128-byte swizzle),
 // one thread of warp 5 issues tcgen05.mma into a 128-column TMEM accumulator,
 // and warps 0-3 add up sum(h^2) of their token row from each staged h tile (the
 // fused RMSNorm; a ring slot is freed by the MMA commit plus the four warps).
@@ -26,13 +26,14 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int RBM = 128, RBN = 128, RBK = 64, RSTAGES = 4;
+constexpr int RBM = 128, RBN = 128, RBK = 64, RSTAGES = 6;
 constexpr int RTHREADS = 6 * 32;
 constexpr int RMAX_SPLIT = 4;   // K split and cluster size at most (keeps the finishing loads in registers)
 constexpr uint32_t RA_BYTES = RBM * RBK * 2, RB_BYTES = RBN * RBK * 2, RSTAGE = RA_BYTES + RB_BYTES;
 constexpr int RSTAGE_LD = 132;  // floats per staged row (conflict-free 16-byte stores)
-constexpr uint32_t RSTAGING = 4 * 32 * RSTAGE_LD * 4;   // epilogue staging, its own region
-constexpr size_t RSMEM = 1024 + size_t(RSTAGES) * RSTAGE + RSTAGING + 256;
+constexpr uint32_t RSTAGING = 4 * 32 * RSTAGE_LD * 4;   // epilogue staging: reuses the ring once the MMAs are done
+static_assert(RSTAGING <= RSTAGES * RSTAGE, "staging must fit in the ring");
+constexpr size_t RSMEM = 1024 + size_t(RSTAGES) * RSTAGE + 256;
 // Smallest batch that goes to the tensor cores.
 constexpr int RTC_MIN_TOKENS = 256;
 
@@ -78,8 +79,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                  const __grid_constant__ RouterArgs a, void* ws) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* staging = reinterpret_cast<float*>(smem + RSTAGES * RSTAGE);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RSTAGES * RSTAGE + RSTAGING);
+    float* staging = reinterpret_cast<float*>(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RSTAGES * RSTAGE);
     uint64_t* empty = full + RSTAGES;
     uint64_t* acc_full = empty + RSTAGES;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
@@ -192,6 +193,10 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
         if (ok) ok = tc::mbar_wait(acc_full, 0, abort, ws, 34);
         tc::tc_fence_after();
+        // The staging area overlays the ring: every MMA has read its operands
+        // (acc_full), and this barrier waits until the four warps are done with
+        // their last tiles. Not .aligned: lanes may leave the loop on a timeout apart.
+        asm volatile("barrier.sync 1, 128;" ::: "memory");
         if (ok) {
             // Stage this warp's 32 rows in shared memory (row stride 132 floats keeps
             // the 16-byte stores conflict-free), then store each row with one 512-byte
