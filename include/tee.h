@@ -29,9 +29,13 @@
  *     128-bit loads), and `d` a multiple of 8.
  *   Workspace: each call takes a device scratch buffer `ws` of at least the
  *     size its *_workspace_size query returns. It begins with a 256-byte
- *     header holding a sticky device error word. The caller zero-fills a new
- *     workspace once (tee_workspace_init); every call leaves it reusable.
- *     Calls that share one workspace must not overlap on the GPU.
+ *     header holding a sticky device error word and the counters of the
+ *     kernels' "last block" reductions, which every call leaves at zero. The
+ *     caller zero-fills a new workspace once (tee_workspace_init); every call
+ *     leaves it reusable. A call that stopped on a wait time-out
+ *     (TEE_DEVERR_TIMEOUT) may leave a counter set: tee_clear_device_error
+ *     zeroes the whole header again. Calls that share one workspace must not
+ *     overlap on the GPU.
  *   Errors: every call returns a tee_status. Host-side checks (null required
  *     pointer, bad size, misalignment, unsupported format) return before any
  *     launch. Faults that only the device can see (a row, position, sequence
@@ -97,7 +101,8 @@ TEE_API tee_status tee_workspace_init(void* ws, size_t bytes, void* stream);
  * *code gets a TEE_DEVERR_* value, *detail the offending index (either may be
  * NULL). Returns TEE_ERR_DEVICE if a fault was recorded, else TEE_OK. */
 TEE_API tee_status tee_get_device_error(const void* ws, int32_t* code, int32_t* detail, void* stream);
-/* Clear the device fault word of `ws` on `stream`. */
+/* Clear the device fault word of `ws` on `stream`, and every counter of the
+ * header with it (the whole TEE_WS_HEADER_BYTES). */
 TEE_API tee_status tee_clear_device_error(void* ws, void* stream);
 /* Number of kernels this library has launched in this process (all threads). */
 TEE_API uint64_t tee_launch_count(void);

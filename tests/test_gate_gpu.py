@@ -141,12 +141,79 @@ def test_router_tc_batch_sizes(tee, n):
     check_mask(mask, p_ref, 0.5)
 
 
+# Above 76 token tiles (on 152 SMs) the gate runs one persistent CTA per SM over
+# the tiles, two TMEM accumulators, no K split: 9729 tokens = 77 tiles with a
+# one-token tail; 40000 tokens = 313 tiles, two or three per CTA, a 64-token tail.
+@pytest.mark.parametrize("n,rule", [(9729, "per_token"), (40000, "per_token"), (40000, "batch_all")])
+def test_router_tc_persistent(tee, n, rule):
+    cfg = configs.ROUTER_4096
+    w = gen.router_weights(cfg, 3, seed=n, device=DEV)
+    h = gen.router_hidden(cfg, n, 3, seed=n, device=DEV)
+    b_down = 0.05 * torch.randn(128, device=DEV)
+    b_up = torch.full((1,), 0.3, device=DEV)
+    ws = tee.Workspace(DEV)
+    score, mask, flag = tee.exit_gate(h, 0.5, w_down=w["w_down"], w_up=w["w_up"], b_down=b_down, b_up=b_up,
+                                      rule=rule, eps=cfg.eps, ws=ws)
+    p_ref, m_ref, f_ref = _router_ref(h, w, 0.5, rule, b_down=b_down, b_up=b_up, eps=cfg.eps)
+    check_scores(score, p_ref)
+    if rule == "per_token":
+        check_mask(mask, p_ref, 0.5)
+    elif np.abs(p_ref.min() - 0.5) > 1e-3:
+        assert int(flag.item()) == int(f_ref)
+        assert bool((mask == int(f_ref)).all())
+    assert ws.device_error() == (0, 0)
+
+
+# d that is not a whole number of two-block stages (the trailing block reads as
+# zero), with the K split (4096 tokens) and the persistent kernel (20000 tokens).
+@pytest.mark.parametrize("d,n", [(576, 4096), (576, 20000), (64, 300), (192, 9729)])
+def test_router_tc_odd_k_blocks(tee, d, n):
+    import dataclasses
+    cfg = dataclasses.replace(configs.ROUTER_4096, d=d)
+    w = gen.router_weights(cfg, 1, seed=d, device=DEV)
+    w["w_down"] = (w["w_down"].float() * 6.0).to(torch.bfloat16)   # keep the scores spread at small d
+    h = gen.router_hidden(cfg, n, 1, seed=d, device=DEV)
+    b_down = 0.05 * torch.randn(128, device=DEV)
+    score, mask, _ = tee.exit_gate(h, 0.5, w_down=w["w_down"], w_up=w["w_up"], b_down=b_down, eps=cfg.eps)
+    p_ref, _, _ = _router_ref(h, w, 0.5, "per_token", b_down=b_down, eps=cfg.eps)
+    check_scores(score, p_ref)
+    check_mask(mask, p_ref, 0.5)
+
+
+def test_router_tc_persistent_on_the_exact_workspace(tee):
+    # The persistent kernel needs no scratch beyond the header: the call runs on a
+    # buffer of exactly the queried size, through the C ABI.
+    import ctypes
+    from token_early_exit_gb300 import _lib
+    cfg = configs.ROUTER_4096
+    n = 20000
+    w = gen.router_weights(cfg, 7, seed=5, device=DEV)
+    h = gen.router_hidden(cfg, n, 7, seed=5, device=DEV)
+    lib = _lib.load()
+    desc = _lib.GateDesc(mode=_lib.TEE_GATE_ROUTER, rule=_lib.TEE_RULE_PER_TOKEN, dtype=_lib.TEE_BF16, d=cfg.d,
+                         bottleneck=cfg.bottleneck, threshold=0.5, eps=cfg.eps)
+    size = lib.tee_exit_gate_workspace_size(ctypes.byref(desc), n)
+    ws = torch.zeros(size, dtype=torch.uint8, device=DEV)
+    score = torch.full((n,), -1.0, device=DEV)
+    mask = torch.full((n,), 7, dtype=torch.uint8, device=DEV)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = lib.tee_exit_gate(ctypes.byref(desc), n, p(h), h.stride(0), None, 0, None, p(w["w_down"]), None,
+                           p(w["w_up"]), None, p(score), p(mask), None, p(ws), size, stream)
+    assert st == _lib.TEE_OK
+    torch.cuda.synchronize()
+    p_ref, _, _ = _router_ref(h, w, 0.5, "per_token", eps=cfg.eps)
+    check_scores(score, p_ref)
+    check_mask(mask, p_ref, 0.5)
+    assert int(ws[:8].view(torch.int32)[0].item()) == 0
+
+
 def test_router_calls_share_a_workspace(tee):
     # tensor-core and CUDA-core calls alternate on one workspace: each must see clean sums
     cfg = configs.ROUTER_4096
     ws = tee.Workspace(DEV)
     w = gen.router_weights(cfg, 11, seed=1, device=DEV)
-    for n in (4096, 64, 4096, 300, 300):
+    for n in (4096, 64, 20000, 4096, 300, 20000, 300):
         h = gen.router_hidden(cfg, n, 11, seed=n, device=DEV)
         score, mask, _ = tee.exit_gate(h, 0.5, w_down=w["w_down"], w_up=w["w_up"], eps=cfg.eps, ws=ws)
         p_ref, _, _ = _router_ref(h, w, 0.5, "per_token", eps=cfg.eps)

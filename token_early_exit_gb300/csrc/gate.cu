@@ -15,6 +15,7 @@
 // "last block" reduction of the all-tokens flag (River-LLM's min over the
 // batch; TIDE module 3's "for every token in the batch").
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -25,40 +26,71 @@ namespace {
 constexpr int GATE_WARPS = 8;
 constexpr int GATE_MAX_BLOCKS = 1024;
 
+// 16 bytes of a row that is read once: not kept in L1.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+// <a,b>, |a|^2, |b|^2 over the elements of one 16-byte chunk of each row.
 template <typename T>
-__global__ void __launch_bounds__(GATE_WARPS * 32)
+__device__ __forceinline__ void cos_acc16(uint4 a, uint4 b, float& dot, float& na, float& nb) {
+    const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if constexpr (sizeof(T) == 4) {
+            const float x = __uint_as_float(ua[q]), y = __uint_as_float(ub[q]);
+            dot = fmaf(x, y, dot);
+            na = fmaf(x, x, na);
+            nb = fmaf(y, y, nb);
+        } else {
+            float x0, x1, y0, y1;
+            if constexpr (std::is_same<T, __half>::value) {
+                unpack_f16x2(ua[q], x0, x1);
+                unpack_f16x2(ub[q], y0, y1);
+            } else {
+                unpack_bf16x2(ua[q], x0, x1);
+                unpack_bf16x2(ub[q], y0, y1);
+            }
+            dot = fmaf(x0, y0, dot);
+            dot = fmaf(x1, y1, dot);
+            na = fmaf(x0, x0, na);
+            na = fmaf(x1, x1, na);
+            nb = fmaf(y0, y0, nb);
+            nb = fmaf(y1, y1, nb);
+        }
+    }
+}
+
+// Large batches: one warp per token, eight 16-byte chunks of each row per lane
+// in flight at once (4 KB per row per warp), loads that bypass L1.
+constexpr int COS_U = 8;
+template <typename T>
+__global__ void __launch_bounds__(GATE_WARPS * 32, 3)   // room for the 16 loads in flight
 cosine_gate_kernel(int n, int d, const T* __restrict__ hc, int64_t ldc, const T* __restrict__ hp,
                    int64_t ldp, float thr, int rule, bool need_flag, float* __restrict__ score,
                    uint8_t* __restrict__ mask, int32_t* __restrict__ flag, void* ws) {
     allow_dependents();
+    constexpr int V = 16 / sizeof(T);   // elements per chunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float wmin = INFINITY;
     for (int t = blockIdx.x * GATE_WARPS + warp; t < n; t += gridDim.x * GATE_WARPS) {
         const T* a = hp + static_cast<int64_t>(t) * ldp;
         const T* b = hc + static_cast<int64_t>(t) * ldc;
         float dot = 0.f, na = 0.f, nb = 0.f;
-        // Four 16-byte chunks of each row per lane in flight at once.
-        for (int i0 = lane * 8; i0 < d; i0 += 4 * 256) {
-            float x[4][8], y[4][8];
+        int i0 = lane * V;
+        for (; i0 + (COS_U - 1) * 32 * V < d; i0 += COS_U * 32 * V) {   // whole steps
+            uint4 xa[COS_U], xb[COS_U];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (i0 + u * 256 < d) {
-                    load8(a + i0 + u * 256, x[u]);
-                    load8(b + i0 + u * 256, y[u]);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) x[u][k] = y[u][k] = 0.f;
-                }
+            for (int u = 0; u < COS_U; ++u) {
+                xa[u] = ld_stream16(a + i0 + u * 32 * V);
+                xb[u] = ld_stream16(b + i0 + u * 32 * V);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    dot = fmaf(x[u][k], y[u][k], dot);
-                    na = fmaf(x[u][k], x[u][k], na);
-                    nb = fmaf(y[u][k], y[u][k], nb);
-                }
+            for (int u = 0; u < COS_U; ++u) cos_acc16<T>(xa[u], xb[u], dot, na, nb);
         }
+        for (; i0 < d; i0 += 32 * V) cos_acc16<T>(ld_stream16(a + i0), ld_stream16(b + i0), dot, na, nb);   // the rest
         dot = warp_sum(dot);
         na = warp_sum(na);
         nb = warp_sum(nb);
@@ -325,7 +357,17 @@ static tee_status run_gate(const tee_gate_desc* g, int n, const void* h_cur, int
                 g->rule, need_flag, score, mask, flag, ws);
             return launch_status();
         }
-        cosine_gate_kernel<T><<<blocks, GATE_WARPS * 32, 0, stream>>>(
+        // No more blocks than are resident at once: each warp then streams its
+        // tokens back to back instead of a second wave starting late.
+        static int per_sm = 0;
+        if (per_sm == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cosine_gate_kernel<T>,
+                                                                           GATE_WARPS * 32, 0) != cudaSuccess ||
+                            per_sm < 1)) {
+            (void)cudaGetLastError();
+            per_sm = 1;
+        }
+        const int resident = per_sm * sm_count();
+        cosine_gate_kernel<T><<<blocks < resident ? blocks : resident, GATE_WARPS * 32, 0, stream>>>(
             n, g->d, static_cast<const T*>(h_cur), ld_cur, static_cast<const T*>(h_prev), ld_prev, g->threshold,
             g->rule, need_flag, score, mask, flag, ws);
         return launch_status();

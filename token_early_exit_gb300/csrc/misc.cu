@@ -71,7 +71,7 @@ tee_status tee_get_device_error(const void* ws, int32_t* code, int32_t* detail, 
 
 tee_status tee_clear_device_error(void* ws, void* stream) {
     if (!ws) return TEE_ERR_WORKSPACE;
-    return cuda_status(cudaMemsetAsync(ws, 0, 2 * sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+    return cuda_status(cudaMemsetAsync(ws, 0, TEE_WS_HEADER_BYTES, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -113,6 +113,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -233,5 +239,11 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // Out-of-range rows/columns read as zero.
 tee_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                           uint32_t box_inner, uint32_t box_rows);
+// The same matrix ([rows][n_kb * 64]) as n_kb blocks of 64 columns: a box brings
+// box_kb consecutive blocks, each as its own swizzled [box_rows][64] tile, in one
+// copy (a TMA copy costs about the same time whatever its size, so larger boxes
+// move more per SM). Blocks past n_kb read as zero.
+tee_status make_tmap_bf16_kblocks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes,
+                                  uint64_t n_kb, uint32_t box_rows, uint32_t box_kb);
 
 }  // namespace tee
