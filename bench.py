@@ -9,10 +9,12 @@ A step is one pass of the whole hot path over one batch of synthetic input:
       64-token Llama-3.2-1B-shaped decode batch;
   decode-tiny: the same on the tiny fp32 workload;
   router-4096: router gate -> compaction with gather, 4096 tokens, d = 4096;
+  router-65536: the same at 65,536 tokens (inputs far larger than L2), with the
+      cosine gate and the exit scatter at that batch timed alongside;
   prefill-16k / prefill-120k: the RidgeFill KV fill of every layer after the
       split for all filled rows.
 L2 is flushed (a write larger than L2) between timed steps, outside the timed
-events. Under torchrun each rank runs its own replica (independent batches,
+events, except where every input is larger than L2 (router-65536). Under torchrun each rank runs its own replica (independent batches,
 no collective on the data path: weak scaling); rank 0 prints one JSON line.
 The reference arm (--impl reference) times the CPU oracle on a bounded sample
 of the same workload on the host cores.
@@ -42,7 +44,7 @@ sys.path.insert(0, ROOT)
 from workloads import configs, gen  # noqa: E402
 
 METRIC = "tokens/s through exit gate+compact+KV fill"
-WORKLOADS = ("decode-1b", "decode-tiny", "router-4096", "prefill-16k", "prefill-120k")
+WORKLOADS = ("decode-1b", "decode-tiny", "router-4096", "router-65536", "prefill-16k", "prefill-120k")
 
 
 def peaks():
@@ -218,10 +220,48 @@ class Router:
         self.kernel = "exit_gate(router)"
         self.traffic_key = None
         self.bound = "hbm"
+        # h alone is twice L2 or more: no flush between steps (its lines are gone anyway)
+        self.flush = n * cfg.d * 2 < 2 * torch.cuda.get_device_properties(dev).L2_cache_size
 
     def fill_bytes(self, n_exit):
         d, b = self.cfg.d, self.cfg.bottleneck
         return self.n * d * 2 + b * d * 2 + b * 2 + self.n * 5
+
+    def kernels(self):
+        """Each kernel of the path at this batch as its own call: (name, call, algorithmic bytes).
+        Besides the step's router gate and compaction, the cosine gate (a second
+        hidden state of the same shape) and the exit scatter of the exiting rows."""
+        if self.n < 65536:
+            return []
+        tee, n, d = self.tee, self.n, self.cfg.d
+        gen_ = torch.Generator(device=self.dev)
+        gen_.manual_seed(1)
+        h_prev = (self.h.float() + 0.3 * torch.randn(n, d, device=self.dev, generator=gen_)).to(self.h.dtype)
+        c_out = dict(self.c_out)
+        pos = torch.arange(n, dtype=torch.int32, device=self.dev)
+        c_out["cont_pos"] = torch.empty(n, dtype=torch.int32, device=self.dev)
+        c_out["exit_pos"] = torch.empty(n, dtype=torch.int32, device=self.dev)
+        self.tee.exit_gate(self.h, self.theta, w_down=self.w["w_down"], w_up=self.w["w_up"], eps=self.cfg.eps,
+                           ws=self.ws, out=self.g_out)
+        tee.exit_compact(self.g_out["mask"], pos_in=pos, h=self.h, ws=self.ws, out=c_out)
+        torch.cuda.synchronize(self.dev)
+        n_cont, n_exit = [int(v) for v in c_out["counts"].tolist()]
+        out = torch.empty(n, d, dtype=self.h.dtype, device=self.dev)
+        g_out = {k: torch.empty_like(v) for k, v in self.g_out.items()}
+        self._keep = (h_prev, c_out, pos, out, g_out)
+        return [
+            ("exit_gate(cosine, per_token)",
+             lambda: tee.exit_gate(self.h, 0.95, h_prev=h_prev, ws=self.ws, out=g_out), 2 * n * d * 2 + 5 * n),
+            ("exit_gate(router)",
+             lambda: tee.exit_gate(self.h, self.theta, w_down=self.w["w_down"], w_up=self.w["w_up"],
+                                   eps=self.cfg.eps, ws=self.ws, out=g_out), self.fill_bytes(0)),
+            ("exit_compact(gather, positions)",
+             lambda: tee.exit_compact(self.g_out["mask"], pos_in=pos, h=self.h, ws=self.ws, out=c_out),
+             n + 4 * n + 16 * n + 8 + 2 * n_cont * d * 2),
+            ("exit_scatter",
+             lambda: tee.exit_scatter(c_out["counts"], c_out["exit_rows"], c_out["exit_pos"], self.h, out,
+                                      ws=self.ws), 2 * n_exit * d * 2 + 8 * n_exit + 8),
+        ]
 
     def parts(self):
         def gate():
@@ -256,7 +296,7 @@ class Router:
         c = self.cfg
         return {"workload": f"{c.name}-n{self.n}", "tokens_per_step": self.n, "d": c.d, "bottleneck": c.bottleneck,
                 "theta": self.theta, "gate": "router", "rule": "per_token", "gather": True,
-                "l2": "flushed between timed steps"}
+                "l2": "flushed between timed steps" if self.flush else "inputs larger than L2 (no flush)"}
 
     def oracle_sample(self):
         import oracle
@@ -349,6 +389,8 @@ def make(name, tee, dev, seed, rows=None, layers=None):
         return Decode(tee, configs.TINY_DECODE, dev, seed)
     if name == "router-4096":
         return Router(tee, configs.ROUTER_4096, dev, seed)
+    if name == "router-65536":
+        return Router(tee, configs.ROUTER_4096, dev, seed, n=65536)
     if name == "prefill-16k":
         return Prefill(tee, configs.PREFILL_16K, dev, seed, rows, layers)
     if name == "prefill-120k":
@@ -508,7 +550,8 @@ def run_gpu(args):
         g = torch.cuda.CUDAGraph()
         l0 = lib.tee_launch_count()
         with torch.cuda.graph(g):
-            flush.zero_()
+            if getattr(w, "flush", True):
+                flush.zero_()
             a.record()
             for f in calls:
                 f()
@@ -541,6 +584,21 @@ def run_gpu(args):
     clk = clocks.stop()
     if g_kern is None:
         kern_ms = step_ms
+    # each kernel of the path as its own call, where the workload lists them
+    per_kernel = {}
+    for name, call, nbytes in (w.kernels() if hasattr(w, "kernels") else []):
+        g1, a1, b1, k1 = capture([call])
+        g1.replay()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(args.steps):
+            g1.replay()
+            torch.cuda.synchronize(dev)
+            ts.append(a1.elapsed_time(b1))
+        km = statistics.median(ts)
+        gbs = nbytes / (km * 1e-3) / 1e9
+        per_kernel[name] = {"us": km * 1e3, "algorithmic_bytes": nbytes, "GB/s": gbs,
+                            "frac": gbs / peaks()["hbm_gbs"], "launches": int(k1)}
     t_step = statistics.mean(step_ms)
     t_step = max_over_ranks(t_step, world, dev)
     value = world * w.units / (t_step * 1e-3)
@@ -590,7 +648,10 @@ def run_gpu(args):
             "e2e": {"value": world * w.units / (t_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": t_e2e},
             "gpu_launches": int(launches), "launches_per_step": int(k_step), "clocks": clk,
-            "timing": "CUDA-graph replay per step; L2 flushed inside the graph before the step; "
+            **({"kernels": per_kernel} if per_kernel else {}),
+            "timing": "CUDA-graph replay per step; " + ("L2 flushed inside the graph before the step; "
+                                                           if getattr(w, "flush", True) else
+                                                           "no flush (every input is larger than L2); ") +
                       "timed by device events recorded inside the graph around the step",
             "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)}}
     if rank == 0:
