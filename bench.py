@@ -218,7 +218,7 @@ class Router:
         self.c_out["h_cont"] = torch.empty(n, cfg.d, dtype=self.h.dtype, device=dev)
         self.units = n
         self.kernel = "exit_gate(router)"
-        self.traffic_key = None
+        self.traffic_key = f"exit_gate(router)/n{n}"   # recorded ncu captures: 4096 and 65,536 tokens
         self.bound = "hbm"
         # h alone is twice L2 or more: no flush between steps (its lines are gone anyway)
         self.flush = n * cfg.d * 2 < 2 * torch.cuda.get_device_properties(dev).L2_cache_size
@@ -231,7 +231,7 @@ class Router:
         """Each kernel of the path at this batch as its own call: (name, call, algorithmic bytes).
         Besides the step's router gate and compaction, the cosine gate (a second
         hidden state of the same shape) and the exit scatter of the exiting rows."""
-        if self.n < 65536:
+        if self.n < 16384:
             return []
         tee, n, d = self.tee, self.n, self.cfg.d
         gen_ = torch.Generator(device=self.dev)
@@ -390,7 +390,7 @@ def make(name, tee, dev, seed, rows=None, layers=None):
     if name == "router-4096":
         return Router(tee, configs.ROUTER_4096, dev, seed)
     if name == "router-65536":
-        return Router(tee, configs.ROUTER_4096, dev, seed, n=65536)
+        return Router(tee, configs.ROUTER_4096, dev, seed, n=rows or 65536)
     if name == "prefill-16k":
         return Prefill(tee, configs.PREFILL_16K, dev, seed, rows, layers)
     if name == "prefill-120k":
@@ -672,7 +672,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--rows", type=int, default=None, help="prefill workloads: fewer filled rows (profiling)")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="prefill workloads: fewer filled rows; router-65536: fewer tokens (profiling)")
     ap.add_argument("--layers", type=int, default=None, help="prefill workloads: fewer filled layers (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
