@@ -221,6 +221,28 @@ TEE_API tee_status tee_exit_compact(int32_t n, const uint8_t* mask, const int32_
                             void* h_cont, int64_t ld_cont, int32_t* counts,
                             void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Compaction and exit scatter in one launch: tee_exit_compact (same arguments
+ * and results; the gather into h_cont is optional here, h_cont nullable) and,
+ * for every exiting row r, out[p] = h_in[r] with p = pos_in ? pos_in[r] : r,
+ * i.e. what tee_exit_scatter(n, counts, exit_rows, exit_pos, h_in, ...) writes
+ * without final_gamma. The blocks that rank the rows also copy them, so a
+ * decode step saves a launch.
+ *
+ *   h_in      [n][ld_in] dtype, required
+ *   out       [n_out][ld_out] dtype, required; rows other than the exiting
+ *             rows' slots are left as they are
+ * A slot outside [0, n_out) is skipped and recorded (TEE_DEVERR_DEST).
+ * Workspace: tee_exit_compact_workspace_size(n).
+ */
+TEE_API tee_status tee_exit_compact_scatter(int32_t n, const uint8_t* mask, const int32_t* pos_in,
+                            const void* h_in, int64_t ld_in, int32_t d, int32_t dtype,
+                            int32_t* cont_rows, int32_t* exit_rows,
+                            int32_t* cont_pos, int32_t* exit_pos,
+                            void* h_cont, int64_t ld_cont,
+                            void* out, int64_t ld_out, int64_t n_out, int32_t* counts,
+                            void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------ exit scatter */
 
 TEE_API size_t tee_exit_scatter_workspace_size(int32_t n_max);

@@ -118,3 +118,59 @@ def test_scatter_records_bad_destinations(tee):
     assert torch.equal(out[5], h[0]) and torch.equal(out[6], h[2])
     ws.clear_error()
     assert ws.device_error() == (0, 0)
+
+
+# ------------------------------------------------------------ compaction + scatter in one launch
+
+@pytest.mark.parametrize("n,d,dtype,gather", [(1, 256, torch.bfloat16, True), (8, 2048, torch.bfloat16, False),
+                                              (33, 256, torch.float32, True), (64, 2048, torch.bfloat16, True),
+                                              (300, 520, torch.float16, False), (4097, 256, torch.bfloat16, True),
+                                              (70000, 64, torch.bfloat16, True)])
+def test_compaction_with_scatter(tee, n, d, dtype, gather):
+    rng = np.random.default_rng(n + d)
+    h = torch.randn(n, d, device=DEV).to(dtype)
+    n_out = 3 * n
+    pos_in = torch.from_numpy(rng.permutation(n_out)[:n].astype(np.int32)).to(DEV)
+    for name, m in _masks(n, rng):
+        out = torch.full((n_out, d), -7.0, device=DEV).to(dtype)
+        ws = tee.Workspace(DEV)
+        res = tee.exit_compact_scatter(torch.from_numpy(m).to(DEV), h, out, pos_in=pos_in, gather=gather, ws=ws)
+        ref = oracle.stable_partition(m, pos_in.cpu().numpy())
+        _check(res, ref, n, h if gather else None)
+        want = oracle.exit_scatter(np.full((n_out, d), -7.0), f64(h), ref["exit_rows"], ref["exit_pos"])
+        assert torch.equal(out.cpu(), torch.from_numpy(want).to(dtype)), name
+        assert ws.device_error() == (0, 0)
+
+
+def test_compaction_with_scatter_matches_the_two_calls(tee):
+    # the decode-step shape: 64 tokens of a 1B model, identity slots
+    n, d = 64, 2048
+    h = torch.randn(n, d, device=DEV).to(torch.bfloat16)
+    m = torch.from_numpy((np.random.default_rng(3).random(n) < 0.5).astype(np.uint8)).to(DEV)
+    out1 = torch.zeros(n, d, device=DEV, dtype=torch.bfloat16)
+    out2 = torch.zeros(n, d, device=DEV, dtype=torch.bfloat16)
+    r1 = tee.exit_compact(m, h=h)
+    tee.exit_scatter(r1["counts"], r1["exit_rows"], r1["exit_pos"], h, out1)
+    r2 = tee.exit_compact_scatter(m, h, out2)
+    assert torch.equal(out1, out2)
+    for k in ("counts", "cont_rows", "exit_rows", "h_cont"):
+        c = int(r1["counts"][0]) if k in ("cont_rows", "h_cont") else int(r1["counts"][1]) if k == "exit_rows" else 2
+        assert torch.equal(r1[k][:c], r2[k][:c]), k
+
+
+def test_compaction_with_scatter_records_bad_slots(tee):
+    n, d = 40, 256
+    h = torch.randn(n, d, device=DEV).to(torch.bfloat16)
+    m = torch.ones(n, dtype=torch.uint8, device=DEV)
+    pos_in = torch.arange(n, dtype=torch.int32, device=DEV)
+    pos_in[5] = n + 3     # outside out's rows: skipped and recorded
+    pos_in[9] = -1
+    out = torch.zeros(n, d, device=DEV, dtype=torch.bfloat16)
+    ws = tee.Workspace(DEV)
+    tee.exit_compact_scatter(m, h, out, pos_in=pos_in, gather=False, ws=ws)
+    code, detail = ws.device_error()
+    assert code == 5 and detail in (n + 3, -1)
+    keep = [i for i in range(n) if i not in (5, 9)]
+    assert torch.equal(out[keep], h[keep])
+    assert torch.equal(out[5], torch.zeros(d, device=DEV, dtype=torch.bfloat16))
+    assert torch.equal(out[9], torch.zeros(d, device=DEV, dtype=torch.bfloat16))

@@ -20,10 +20,15 @@ def tee():
     return t
 
 
-def run_step(tee, cfg, x, fill, ws, scatter_first=False):
+def run_step(tee, cfg, x, fill, ws, scatter_first=False, fused=False):
     score, mask, flag = tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule=cfg.rule, ws=ws)
-    comp = tee.exit_compact(mask, h=x["h_cur"], ws=ws)
     out = torch.full_like(x["h_cur"], -3.0)
+    if fused:   # compaction and scatter in one launch, then the fill
+        comp = tee.exit_compact_scatter(mask, x["h_cur"], out, ws=ws)
+        fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=comp["exit_rows"], pos=x["pos"], seq=x["seq"],
+             n_dev=comp["counts"][1:], n_max=cfg.batch, ws=ws)
+        return score, mask, flag, comp, out
+    comp = tee.exit_compact(mask, h=x["h_cur"], ws=ws)
 
     def do_fill():
         fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=comp["exit_rows"], pos=x["pos"], seq=x["seq"],
@@ -41,18 +46,22 @@ def run_step(tee, cfg, x, fill, ws, scatter_first=False):
     return score, mask, flag, comp, out
 
 
-@pytest.mark.parametrize("cfg,case,seed,early", [(configs.TINY_DECODE, "default", s, False) for s in range(4)] +
-                         [(configs.LLAMA1B_DECODE, c, s, False) for c in ("exit", "stay") for s in range(2)] +
-                         [(configs.LLAMA1B_DECODE, c, s, True) for c in ("exit", "stay") for s in range(2)])
-def test_decode_step(tee, cfg, case, seed, early):
-    # early: the fill launches while the scatter runs and reads h, rows, counts only
-    # after it completes (TEE_FILL_EARLY_WEIGHTS)
+@pytest.mark.parametrize("cfg,case,seed,early,fused",
+                         [(configs.TINY_DECODE, "default", s, False, False) for s in range(4)] +
+                         [(configs.TINY_DECODE, "default", s, False, True) for s in range(2)] +
+                         [(configs.LLAMA1B_DECODE, c, s, False, False) for c in ("exit", "stay") for s in range(2)] +
+                         [(configs.LLAMA1B_DECODE, c, s, True, False) for c in ("exit", "stay") for s in range(2)] +
+                         [(configs.LLAMA1B_DECODE, c, s, True, True) for c in ("exit", "stay") for s in range(2)])
+def test_decode_step(tee, cfg, case, seed, early, fused):
+    # early: the fill launches while the previous kernel runs and reads h, rows, counts
+    # only after it completes (TEE_FILL_EARLY_WEIGHTS); fused: compaction and scatter
+    # in one launch (the bench's step)
     x = gen.decode_inputs(cfg, seed=seed, device=DEV, case=case)
     ws = tee.Workspace(DEV)
     fill = tee.KVFill(x["layers"], d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
                       rope_base=cfg.rope_base, eps=cfg.eps, dtype=x["h_cur"].dtype, max_pos=cfg.cache_len,
                       int4=cfg.weights == "int4", group=cfg.group, early_weights=early)
-    score, mask, flag, comp, out = run_step(tee, cfg, x, fill, ws, scatter_first=early)
+    score, mask, flag, comp, out = run_step(tee, cfg, x, fill, ws, scatter_first=early, fused=fused)
     assert ws.device_error() == (0, 0)
     hp, hc = f64(x["h_prev"]), f64(x["h_cur"])
     s_ref, m_ref, f_ref = oracle.cosine_gate(hp, hc, cfg.tau, cfg.rule)

@@ -4,7 +4,8 @@ KV fill, as hand-written CUDA for sm_103a behind the C ABI in include/tee.h.
 The Python side only marshals arguments; see ``ops``.
 """
 from . import _lib  # noqa: F401
-from .ops import (KVFill, Workspace, cache_layout, exit_compact, exit_gate, exit_scatter,  # noqa: F401
-                  kv_fill)
+from .ops import (KVFill, Workspace, cache_layout, exit_compact, exit_compact_scatter,  # noqa: F401
+                  exit_gate, exit_scatter, kv_fill)
 
-__all__ = ["exit_gate", "exit_compact", "exit_scatter", "kv_fill", "KVFill", "Workspace", "cache_layout"]
+__all__ = ["exit_gate", "exit_compact", "exit_compact_scatter", "exit_scatter", "kv_fill", "KVFill", "Workspace",
+           "cache_layout"]

@@ -13,6 +13,9 @@
 //
 // The exit scatter copies each exiting row back to its original slot; with a
 // final RMSNorm weight it is TIDE's "Exit Projection" (norm fused with scatter).
+// Without that norm the scatter can also run inside the compaction launch: the
+// blocks that rank the rows copy their exiting rows to `out` beside the gather of
+// the continuing rows (one launch fewer on a decode step).
 #include "common.cuh"
 
 namespace tee {
@@ -76,11 +79,13 @@ compact_kernel(int n, int R, const uint8_t* __restrict__ mask, const int32_t* __
                const uint32_t* __restrict__ chunk_exits, const T* __restrict__ h_in, int64_t ld_in, int d,
                int32_t* __restrict__ cont_rows, int32_t* __restrict__ exit_rows, int32_t* __restrict__ cont_pos,
                int32_t* __restrict__ exit_pos, T* __restrict__ h_cont, int64_t ld_cont,
-               int32_t* __restrict__ counts) {
+               int32_t* __restrict__ counts, T* __restrict__ out, int64_t ld_out, int64_t n_out, void* ws) {
     allow_dependents();
     __shared__ unsigned s_red[CP_WARPS];
     __shared__ unsigned s_wexit[CP_WARPS];
-    __shared__ int s_src[256];
+    __shared__ int s_src[256];     // the chunk's continuing rows, in order
+    __shared__ int s_xsrc[256];    // its exiting rows, in order, and their slots in `out`
+    __shared__ int s_xdst[256];
     const int r0 = blockIdx.x * R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -100,10 +105,10 @@ compact_kernel(int n, int R, const uint8_t* __restrict__ mask, const int32_t* __
         prefix = block_count_exits(mask, r0, s_red);
     }
 
-    // Warp ballots inside the chunk.
+    // Warp ballots inside the chunk (R may be below 32: lanes past it sit out).
     const int row = r0 + warp * 32 + lane;
     const bool active = warp * 32 < R;
-    const bool in = active && row < n;
+    const bool in = active && warp * 32 + lane < R && row < n;
     const bool is_exit = in && mask[row] != 0;
     const unsigned ball = __ballot_sync(0xFFFFFFFFu, is_exit);
     if (lane == 0) s_wexit[warp] = active ? __popc(ball) : 0u;
@@ -126,6 +131,11 @@ compact_kernel(int n, int R, const uint8_t* __restrict__ mask, const int32_t* __
                 exit_rows[e_idx] = row;
                 if (exit_pos) exit_pos[e_idx] = p;
             }
+            const int xl = e_idx - static_cast<int>(prefix);   // exiting rows of this chunk before it
+            if (xl >= 0 && xl < 256) {
+                s_xsrc[xl] = row;
+                s_xdst[xl] = p;
+            }
         } else if (c_idx >= 0 && c_idx < n && local >= 0 && local < 256) {
             cont_rows[c_idx] = row;
             if (cont_pos) cont_pos[c_idx] = p;
@@ -140,14 +150,28 @@ compact_kernel(int n, int R, const uint8_t* __restrict__ mask, const int32_t* __
     }
     if (!h_in) return;
     __syncthreads();
-    // Gather the chunk's continuing rows, one warp per row, 16 bytes per lane.
-    const int n_cont_chunk = min(chunk_rows - static_cast<int>(chunk_total), R);
+    // Copy the chunk's rows, one warp per row, 16 bytes per lane: the continuing
+    // rows into h_cont (gather), then the exiting rows to their slots of `out`
+    // (scatter), in one sequence of jobs over the block's warps.
+    const int n_cont_chunk = h_cont ? min(chunk_rows - static_cast<int>(chunk_total), R) : 0;
+    const int n_exit_chunk = out ? min(static_cast<int>(chunk_total), R) : 0;
     const int dst0 = r0 - static_cast<int>(prefix);
     constexpr int V = 16 / sizeof(T);
-    for (int j = warp; j < n_cont_chunk; j += CP_WARPS) {
-        const uint4* src = reinterpret_cast<const uint4*>(h_in + static_cast<int64_t>(s_src[j]) * ld_in);
-        uint4* dst = reinterpret_cast<uint4*>(h_cont + static_cast<int64_t>(dst0 + j) * ld_cont);
-        warp_copy16(dst, src, d / V, lane);
+    for (int j = warp; j < n_cont_chunk + n_exit_chunk; j += CP_WARPS) {
+        if (j < n_cont_chunk) {
+            const uint4* src = reinterpret_cast<const uint4*>(h_in + static_cast<int64_t>(s_src[j]) * ld_in);
+            uint4* dst = reinterpret_cast<uint4*>(h_cont + static_cast<int64_t>(dst0 + j) * ld_cont);
+            warp_copy16(dst, src, d / V, lane);
+        } else {
+            const int x = j - n_cont_chunk;
+            const int64_t slot = s_xdst[x];
+            if (slot < 0 || slot >= n_out) {
+                if (lane == 0) record_fault(ws, TEE_DEVERR_DEST, static_cast<int>(slot));
+                continue;
+            }
+            const uint4* src = reinterpret_cast<const uint4*>(h_in + static_cast<int64_t>(s_xsrc[x]) * ld_in);
+            warp_copy16(reinterpret_cast<uint4*>(out + slot * ld_out), src, d / V, lane);
+        }
     }
 }
 
@@ -207,10 +231,12 @@ scatter_kernel(int n_max, const int32_t* __restrict__ counts, const int32_t* __r
     }
 }
 
-int chunk_rows_for(int n, bool gather) {
+// Rows per block: about one block per SM. Calls that copy rows start from 8 rows a
+// block (one row per warp), so that a small batch's copies spread over SMs.
+int chunk_rows_for(int n, bool copies) {
     if (n > PREFIX_DIRECT_MAX) return 256;
-    const int target = gather ? (n + 147) / 148 : (n + 147) / 148 * 4;
-    int R = 32;
+    const int target = copies ? (n + 147) / 148 : (n + 147) / 148 * 4;
+    int R = copies ? 8 : 32;
     while (R < target && R < 256) R <<= 1;
     return R;
 }
@@ -218,7 +244,8 @@ int chunk_rows_for(int n, bool gather) {
 template <typename T>
 tee_status run_compact(int n, const uint8_t* mask, const int32_t* pos_in, const void* h_in, int64_t ld_in, int d,
                        int32_t* cont_rows, int32_t* exit_rows, int32_t* cont_pos, int32_t* exit_pos, void* h_cont,
-                       int64_t ld_cont, int32_t* counts, void* ws, cudaStream_t s) {
+                       int64_t ld_cont, int32_t* counts, void* out, int64_t ld_out, int64_t n_out, void* ws,
+                       cudaStream_t s) {
     const int R = chunk_rows_for(n, h_in != nullptr);
     const int chunks = (n + R - 1) / R;
     uint32_t* chunk_exits = nullptr;
@@ -230,7 +257,8 @@ tee_status run_compact(int n, const uint8_t* mask, const int32_t* pos_in, const 
     }
     compact_kernel<T><<<chunks, CP_THREADS, 0, s>>>(n, R, mask, pos_in, chunk_exits, static_cast<const T*>(h_in),
                                                     ld_in, d, cont_rows, exit_rows, cont_pos, exit_pos,
-                                                    static_cast<T*>(h_cont), ld_cont, counts);
+                                                    static_cast<T*>(h_cont), ld_cont, counts, static_cast<T*>(out),
+                                                    ld_out, n_out, ws);
     return launch_status();
 }
 
@@ -245,10 +273,11 @@ extern "C" size_t tee_exit_compact_workspace_size(int32_t n) {
     return TEE_WS_HEADER_BYTES + (n > PREFIX_DIRECT_MAX ? round_up((static_cast<size_t>(n) + 255) / 256 * 4, 256) : 0);
 }
 
-extern "C" tee_status tee_exit_compact(int32_t n, const uint8_t* mask, const int32_t* pos_in, const void* h_in,
-                                       int64_t ld_in, int32_t d, int32_t dtype, int32_t* cont_rows,
-                                       int32_t* exit_rows, int32_t* cont_pos, int32_t* exit_pos, void* h_cont,
-                                       int64_t ld_cont, int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
+static tee_status compact_call(int32_t n, const uint8_t* mask, const int32_t* pos_in, const void* h_in,
+                               int64_t ld_in, int32_t d, int32_t dtype, int32_t* cont_rows, int32_t* exit_rows,
+                               int32_t* cont_pos, int32_t* exit_pos, void* h_cont, int64_t ld_cont, void* out,
+                               int64_t ld_out, int64_t n_out, int32_t* counts, void* ws, size_t ws_bytes,
+                               void* stream) {
     if (n < 0 || !counts) return TEE_ERR_INVALID_ARG;
     if (!ws || ws_bytes < tee_exit_compact_workspace_size(n)) return TEE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -257,21 +286,42 @@ extern "C" tee_status tee_exit_compact(int32_t n, const uint8_t* mask, const int
     if (h_in) {
         const size_t es = dtype_bytes(dtype);
         if (es == 0) return TEE_ERR_UNSUPPORTED;
-        if (!h_cont || d <= 0 || (d * es) % 16 || ld_in < d || ld_cont < d || (ld_in * es) % 16 ||
-            (ld_cont * es) % 16 || !aligned16(h_in) || !aligned16(h_cont))
+        if ((!h_cont && !out) || d <= 0 || (d * es) % 16 || ld_in < d || (ld_in * es) % 16 || !aligned16(h_in))
             return TEE_ERR_INVALID_ARG;
+        if (h_cont && (ld_cont < d || (ld_cont * es) % 16 || !aligned16(h_cont))) return TEE_ERR_INVALID_ARG;
+        if (out && (n_out < 0 || ld_out < d || (ld_out * es) % 16 || !aligned16(out))) return TEE_ERR_INVALID_ARG;
     }
     switch (h_in ? dtype : TEE_BF16) {
         case TEE_F32:
             return run_compact<float>(n, mask, pos_in, h_in, ld_in, d, cont_rows, exit_rows, cont_pos, exit_pos,
-                                      h_cont, ld_cont, counts, ws, s);
+                                      h_cont, ld_cont, counts, out, ld_out, n_out, ws, s);
         case TEE_F16:
             return run_compact<__half>(n, mask, pos_in, h_in, ld_in, d, cont_rows, exit_rows, cont_pos, exit_pos,
-                                       h_cont, ld_cont, counts, ws, s);
+                                       h_cont, ld_cont, counts, out, ld_out, n_out, ws, s);
         default:
             return run_compact<__nv_bfloat16>(n, mask, pos_in, h_in, ld_in, d, cont_rows, exit_rows, cont_pos,
-                                              exit_pos, h_cont, ld_cont, counts, ws, s);
+                                              exit_pos, h_cont, ld_cont, counts, out, ld_out, n_out, ws, s);
     }
+}
+
+extern "C" tee_status tee_exit_compact(int32_t n, const uint8_t* mask, const int32_t* pos_in, const void* h_in,
+                                       int64_t ld_in, int32_t d, int32_t dtype, int32_t* cont_rows,
+                                       int32_t* exit_rows, int32_t* cont_pos, int32_t* exit_pos, void* h_cont,
+                                       int64_t ld_cont, int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
+    if (h_in && !h_cont) return TEE_ERR_INVALID_ARG;
+    return compact_call(n, mask, pos_in, h_in, ld_in, d, dtype, cont_rows, exit_rows, cont_pos, exit_pos, h_cont,
+                        ld_cont, nullptr, 0, 0, counts, ws, ws_bytes, stream);
+}
+
+extern "C" tee_status tee_exit_compact_scatter(int32_t n, const uint8_t* mask, const int32_t* pos_in,
+                                               const void* h_in, int64_t ld_in, int32_t d, int32_t dtype,
+                                               int32_t* cont_rows, int32_t* exit_rows, int32_t* cont_pos,
+                                               int32_t* exit_pos, void* h_cont, int64_t ld_cont, void* out,
+                                               int64_t ld_out, int64_t n_out, int32_t* counts, void* ws,
+                                               size_t ws_bytes, void* stream) {
+    if (n > 0 && (!h_in || !out)) return TEE_ERR_INVALID_ARG;
+    return compact_call(n, mask, pos_in, h_in, ld_in, d, dtype, cont_rows, exit_rows, cont_pos, exit_pos, h_cont,
+                        ld_cont, out, ld_out, n_out, counts, ws, ws_bytes, stream);
 }
 
 extern "C" size_t tee_exit_scatter_workspace_size(int32_t n_max) {

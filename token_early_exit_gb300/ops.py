@@ -140,6 +140,39 @@ def exit_compact(mask: torch.Tensor, *, pos_in: Optional[torch.Tensor] = None, h
     return out
 
 
+def exit_compact_scatter(mask: torch.Tensor, h: torch.Tensor, out: torch.Tensor, *,
+                         pos_in: Optional[torch.Tensor] = None, gather: bool = True,
+                         ws: Optional[Workspace] = None, res: Optional[Dict[str, torch.Tensor]] = None,
+                         with_pos: bool = True) -> Dict[str, torch.Tensor]:
+    """exit_compact (gathering the continuing rows of ``h`` when ``gather``) and the
+    exit scatter out[pos_in[r] or r] = h[r] of every exiting row r, in one launch."""
+    lib = load()
+    mask = _vec(mask, "mask")
+    n = mask.numel()
+    dev = mask.device
+    _mat(h, "h")
+    _mat(out, "out")
+    d = h.shape[1]
+    res = dict(res or {})
+    for k in ("cont_rows", "exit_rows") + (("cont_pos", "exit_pos") if with_pos else ()):
+        if k not in res:
+            res[k] = torch.empty(n, dtype=torch.int32, device=dev)
+    if "counts" not in res:
+        res["counts"] = torch.empty(2, dtype=torch.int32, device=dev)
+    if gather and "h_cont" not in res:
+        res["h_cont"] = torch.empty((n, d), dtype=h.dtype, device=dev)
+    h_cont = res.get("h_cont") if gather else None
+    ws = ws or Workspace(dev)
+    wp, wn = ws.get(lib.tee_exit_compact_workspace_size(n))
+    st = lib.tee_exit_compact_scatter(n, _ptr(mask), _ptr(_vec(pos_in, "pos_in")), _ptr(h), h.stride(0), d,
+                                      _DT[h.dtype], _ptr(res["cont_rows"]), _ptr(res["exit_rows"]),
+                                      _ptr(res.get("cont_pos")), _ptr(res.get("exit_pos")), _ptr(h_cont),
+                                      h_cont.stride(0) if h_cont is not None else 0, _ptr(out), out.stride(0),
+                                      out.shape[0], _ptr(res["counts"]), wp, wn, _stream(dev))
+    check("tee_exit_compact_scatter", st)
+    return res
+
+
 def exit_scatter(counts: torch.Tensor, exit_rows: torch.Tensor, exit_pos: torch.Tensor, h_src: torch.Tensor,
                  out: torch.Tensor, *, final_gamma: Optional[torch.Tensor] = None, eps: float = 1e-5,
                  n_max: Optional[int] = None, ws: Optional[Workspace] = None) -> torch.Tensor:
