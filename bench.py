@@ -4,9 +4,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 A step is one pass of the whole hot path over one batch of synthetic input:
-  decode-1b (default): cosine gate (batch-min) -> compaction with gather and
-      the exit scatter (one launch) -> KV fill of 8 layers (identity map, int4
-      Wk/Wv), for a 64-token Llama-3.2-1B-shaped decode batch;
+  decode-1b (default): cosine gate (batch-min) -> compaction with gather ->
+      exit scatter (the three in one launch) -> KV fill of 8 layers (identity
+      map, int4 Wk/Wv), for a 64-token Llama-3.2-1B-shaped decode batch;
   decode-tiny: the same on the tiny fp32 workload;
   router-4096: router gate -> compaction with gather, 4096 tokens, d = 4096;
   router-65536: the same at 65,536 tokens (inputs far larger than L2), with the
@@ -97,6 +97,7 @@ class Decode:
                       for k in ("cont_rows", "exit_rows", "cont_pos", "exit_pos")}
         self.c_out["counts"] = torch.empty(2, dtype=torch.int32, device=dev)
         self.c_out["h_cont"] = torch.empty(n, d, dtype=dt, device=dev)
+        self.c_out.update(self.g_out)   # the front writes score, mask and flag into the same dict
         self.out = torch.zeros(n, d, dtype=dt, device=dev)
         self.units = n
         self.kernel = "kv_fill"
@@ -126,20 +127,18 @@ class Decode:
     def parts(self):
         tee, cfg, x = self.tee, self.cfg, self.x
 
-        def gate():
-            tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule=cfg.rule, ws=self.ws, out=self.g_out)
-
-        def compact_scatter():
-            # compaction (continuing rows gathered) and the exit scatter of the
-            # exiting rows to their slots of the output, in one launch
-            tee.exit_compact_scatter(self.g_out["mask"], x["h_cur"], self.out, ws=self.ws, res=self.c_out)
+        def front():
+            # cosine gate, compaction (continuing rows gathered) and the exit scatter
+            # of the exiting rows to their slots of the output: one launch
+            tee.exit_gate_compact_scatter(x["h_cur"], x["h_prev"], cfg.tau, self.out, rule=cfg.rule, ws=self.ws,
+                                          res=self.c_out)
 
         def fill():
             self.fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=self.c_out["exit_rows"], pos=x["pos"],
                       seq=x["seq"], n_dev=self.c_out["counts"][1:], n_max=cfg.batch, ws=self.ws)
         # The fill's early launch (TEE_FILL_EARLY_WEIGHTS) streams its weights while the
-        # compaction and scatter run.
-        return [gate, compact_scatter, fill], 2
+        # front runs.
+        return [front, fill], 1
 
     def step(self):
         for f in self.parts()[0]:

@@ -243,6 +243,33 @@ TEE_API tee_status tee_exit_compact_scatter(int32_t n, const uint8_t* mask, cons
                             void* out, int64_t ld_out, int64_t n_out, int32_t* counts,
                             void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------- gate, compaction and scatter */
+
+TEE_API size_t tee_exit_gate_compact_scatter_workspace_size(const tee_gate_desc* desc, int32_t n);
+
+/*
+ * The front of a decode step: tee_exit_gate, then tee_exit_compact_scatter on
+ * its mask with h = h_cur (continuing rows gathered into h_cont when it is not
+ * null, exiting rows scattered to out[pos_in[r] or r]). Arguments and results
+ * are those of the two calls. A cosine gate over 1..128 tokens runs as one
+ * cluster launch that reads each row once (River-LLM's state-transition cosine
+ * with its batch minimum, TIDE module 4's compaction and exit scatter); other
+ * calls run the two calls' kernels in turn. out and h_cont must not overlap
+ * h_cur. Workspace: tee_exit_gate_compact_scatter_workspace_size.
+ */
+TEE_API tee_status tee_exit_gate_compact_scatter(const tee_gate_desc* desc, int32_t n,
+                            const void* h_cur, int64_t ld_cur,
+                            const void* h_prev, int64_t ld_prev,
+                            const void* gamma, const void* w_down, const float* b_down,
+                            const void* w_up, const float* b_up,
+                            const int32_t* pos_in,
+                            float* score, uint8_t* mask, int32_t* batch_flag,
+                            int32_t* cont_rows, int32_t* exit_rows,
+                            int32_t* cont_pos, int32_t* exit_pos,
+                            void* h_cont, int64_t ld_cont,
+                            void* out, int64_t ld_out, int64_t n_out, int32_t* counts,
+                            void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------ exit scatter */
 
 TEE_API size_t tee_exit_scatter_workspace_size(int32_t n_max);

@@ -21,8 +21,13 @@ def tee():
 
 
 def run_step(tee, cfg, x, fill, ws, scatter_first=False, fused=False):
-    score, mask, flag = tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule=cfg.rule, ws=ws)
     out = torch.full_like(x["h_cur"], -3.0)
+    if fused == "front":   # gate, compaction and scatter in one launch, then the fill
+        comp = tee.exit_gate_compact_scatter(x["h_cur"], x["h_prev"], cfg.tau, out, rule=cfg.rule, ws=ws)
+        fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=comp["exit_rows"], pos=x["pos"], seq=x["seq"],
+             n_dev=comp["counts"][1:], n_max=cfg.batch, ws=ws)
+        return comp["score"], comp["mask"], comp["flag"], comp, out
+    score, mask, flag = tee.exit_gate(x["h_cur"], cfg.tau, h_prev=x["h_prev"], rule=cfg.rule, ws=ws)
     if fused:   # compaction and scatter in one launch, then the fill
         comp = tee.exit_compact_scatter(mask, x["h_cur"], out, ws=ws)
         fill(x["h_cur"], x["k_cache"], x["v_cache"], rows=comp["exit_rows"], pos=x["pos"], seq=x["seq"],
@@ -51,11 +56,13 @@ def run_step(tee, cfg, x, fill, ws, scatter_first=False, fused=False):
                          [(configs.TINY_DECODE, "default", s, False, True) for s in range(2)] +
                          [(configs.LLAMA1B_DECODE, c, s, False, False) for c in ("exit", "stay") for s in range(2)] +
                          [(configs.LLAMA1B_DECODE, c, s, True, False) for c in ("exit", "stay") for s in range(2)] +
-                         [(configs.LLAMA1B_DECODE, c, s, True, True) for c in ("exit", "stay") for s in range(2)])
+                         [(configs.LLAMA1B_DECODE, c, s, True, True) for c in ("exit", "stay") for s in range(2)] +
+                         [(configs.TINY_DECODE, "default", s, False, "front") for s in range(2)] +
+                         [(configs.LLAMA1B_DECODE, c, s, True, "front") for c in ("exit", "stay") for s in range(2)])
 def test_decode_step(tee, cfg, case, seed, early, fused):
     # early: the fill launches while the previous kernel runs and reads h, rows, counts
     # only after it completes (TEE_FILL_EARLY_WEIGHTS); fused: compaction and scatter
-    # in one launch (the bench's step)
+    # in one launch; "front": gate, compaction and scatter in one launch (the bench's step)
     x = gen.decode_inputs(cfg, seed=seed, device=DEV, case=case)
     ws = tee.Workspace(DEV)
     fill = tee.KVFill(x["layers"], d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,

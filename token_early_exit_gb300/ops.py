@@ -173,6 +173,48 @@ def exit_compact_scatter(mask: torch.Tensor, h: torch.Tensor, out: torch.Tensor,
     return res
 
 
+def exit_gate_compact_scatter(h_cur: torch.Tensor, h_prev: torch.Tensor, threshold: float, out: torch.Tensor, *,
+                              rule: str = "per_token", pos_in: Optional[torch.Tensor] = None, gather: bool = True,
+                              ws: Optional[Workspace] = None, res: Optional[Dict[str, torch.Tensor]] = None,
+                              with_pos: bool = True) -> Dict[str, torch.Tensor]:
+    """Cosine exit gate, compaction (continuing rows of ``h_cur`` gathered when
+    ``gather``) and the exit scatter out[pos_in[r] or r] = h_cur[r], one launch for
+    up to 128 tokens. Returns score, mask, flag, counts and the row lists."""
+    lib = load()
+    h_cur = _mat(h_cur, "h_cur")
+    _mat(h_prev, "h_prev")
+    _mat(out, "out")
+    n, d = h_cur.shape
+    dev = h_cur.device
+    desc = GateDesc(mode=_lib.TEE_GATE_COSINE, rule=_RULE[rule], dtype=_DT[h_cur.dtype], d=d, bottleneck=0,
+                    threshold=float(threshold), eps=1e-5)
+    res = dict(res or {})
+    if "score" not in res:
+        res["score"] = torch.empty(n, dtype=torch.float32, device=dev)
+    if "mask" not in res:
+        res["mask"] = torch.empty(n, dtype=torch.uint8, device=dev)
+    if "flag" not in res:
+        res["flag"] = torch.empty(1, dtype=torch.int32, device=dev)
+    for k in ("cont_rows", "exit_rows") + (("cont_pos", "exit_pos") if with_pos else ()):
+        if k not in res:
+            res[k] = torch.empty(n, dtype=torch.int32, device=dev)
+    if "counts" not in res:
+        res["counts"] = torch.empty(2, dtype=torch.int32, device=dev)
+    if gather and "h_cont" not in res:
+        res["h_cont"] = torch.empty((n, d), dtype=h_cur.dtype, device=dev)
+    h_cont = res.get("h_cont") if gather else None
+    ws = ws or Workspace(dev)
+    wp, wn = ws.get(lib.tee_exit_gate_compact_scatter_workspace_size(ctypes.byref(desc), n))
+    st = lib.tee_exit_gate_compact_scatter(
+        ctypes.byref(desc), n, _ptr(h_cur), h_cur.stride(0), _ptr(h_prev), h_prev.stride(0), None, None, None, None,
+        None, _ptr(_vec(pos_in, "pos_in")), _ptr(res["score"]), _ptr(res["mask"]), _ptr(res["flag"]),
+        _ptr(res["cont_rows"]), _ptr(res["exit_rows"]), _ptr(res.get("cont_pos")), _ptr(res.get("exit_pos")),
+        _ptr(h_cont), h_cont.stride(0) if h_cont is not None else 0, _ptr(out), out.stride(0), out.shape[0],
+        _ptr(res["counts"]), wp, wn, _stream(dev))
+    check("tee_exit_gate_compact_scatter", st)
+    return res
+
+
 def exit_scatter(counts: torch.Tensor, exit_rows: torch.Tensor, exit_pos: torch.Tensor, h_src: torch.Tensor,
                  out: torch.Tensor, *, final_gamma: Optional[torch.Tensor] = None, eps: float = 1e-5,
                  n_max: Optional[int] = None, ws: Optional[Workspace] = None) -> torch.Tensor:
