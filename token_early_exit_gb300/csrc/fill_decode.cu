@@ -46,33 +46,45 @@ constexpr int D_CH = 256;            // K per staged chunk of codes
 constexpr int D_BPC = D_CH / D_KB;   // blocks per chunk
 constexpr int D_RA = 5;              // A operand slots (h rows)
 constexpr int D_LAG = 2;             // blocks of h copies in flight
-constexpr int D_RB = 2;              // B operand slots (dequantised weights)
 constexpr int D_RC = 2;              // code chunks in flight
 constexpr int D_MAX_ITEMS = 128;
 constexpr int D_DEQ_WARPS = 8, D_MMA_WARP = 8, D_CP_WARP0 = 9, D_CP_WARPS = 4;
 constexpr int D_DEQ_THREADS = D_DEQ_WARPS * 32;
 constexpr int D_CP_THREADS = D_CP_WARPS * 32;
-constexpr int D_ITEMS_PER_CP = D_MAX_ITEMS * 8 / D_CP_THREADS;   // 16-byte pieces per thread and block
 constexpr int D_THREADS = (D_CP_WARP0 + D_CP_WARPS) * 32;
 constexpr int D_MAX_KC = 2048;       // largest k range of one CTA (its g_j slice sits in shared memory)
 // A slot is refilled D_RA - D_LAG - 1 iterations after its release: slack for the
 // MMA round trip (an mbarrier hand-off costs ~0.1 us).
 static_assert(D_LAG + 2 < D_RA, "the A ring needs slack beyond the blocks in flight");
 
-constexpr uint32_t A_SLOT = 128 * 128;                  // 16 KB: 128 item rows x 64 k
 constexpr uint32_t B_SLOT = D_GCOLS * 128;              // 32 KB: 256 columns x 64 k
 constexpr uint32_t CH_CODES = (D_CH / 2) * D_GCOLS;     // 32 KB: 128 packed rows x 256 columns
 constexpr uint32_t CH_SZ = (D_CH / D_KB) * D_GCOLS * 4; // 4 KB: scale[256], zero[256] (fp16) per group
 constexpr uint32_t CH_BYTES = CH_CODES + CH_SZ;
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + D_RA * A_SLOT;
-constexpr uint32_t OFF_C = OFF_B + D_RB * B_SLOT;
-constexpr uint32_t OFF_G = OFF_C + D_RC * CH_BYTES;               // g_j over this CTA's k range (bf16)
-constexpr uint32_t OFF_SMALL = OFF_G + D_MAX_KC * 2;
-constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * D_RB + 2) * 8 + D_MAX_ITEMS * (8 + 4 + 4) + 16;
-constexpr size_t D_SMEM = 1024 + OFF_SMALL + SMALL_BYTES;
-static_assert(D_SMEM <= 232448, "decode fill shared memory");
-static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_G % 16 == 0 && OFF_SMALL % 8 == 0, "alignment");
+
+// Shared-memory layout. Up to 128 items the A slots hold 128 item rows and the B
+// ring two dequantised blocks. Up to 64 items ("narrow") the A slots hold 64 rows:
+// the M = 128 MMA then also reads the next 64 rows (the following slot, or after
+// the last slot an 8 KB guard), which only feed accumulator rows >= 64 that are
+// never stored; the space saved gives the B ring a third slot, so that the
+// dequantising warps do not wait for the MMA of two blocks back.
+template <bool NARROW>
+struct DLayout {
+    static constexpr int ITEMS = NARROW ? 64 : 128;
+    static constexpr int RB = NARROW ? 3 : 2;             // B operand slots (dequantised weights)
+    static constexpr uint32_t A_SLOT = ITEMS * 128;       // item rows x 64 k
+    static constexpr uint32_t A_GUARD = NARROW ? 64 * 128 : 0;
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + D_RA * A_SLOT + A_GUARD;
+    static constexpr uint32_t OFF_C = OFF_B + RB * B_SLOT;
+    static constexpr uint32_t OFF_G = OFF_C + D_RC * CH_BYTES;    // g_j over this CTA's k range (bf16)
+    static constexpr uint32_t OFF_SMALL = OFF_G + D_MAX_KC * 2;
+    static constexpr uint32_t SMALL_BYTES = (2 * D_RA + 2 * RB + 2) * 8 + D_MAX_ITEMS * (8 + 4 + 4) + 16;
+    static constexpr size_t SMEM = 1024 + OFF_SMALL + SMALL_BYTES;
+    static constexpr int IPC = ITEMS * 8 / D_CP_THREADS;  // 16-byte h pieces per copy thread and block
+    static_assert(SMEM <= 232448, "decode fill shared memory");
+    static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_G % 16 == 0 && OFF_SMALL % 8 == 0, "alignment");
+};
 
 struct DecodeLayer {
     const uint8_t* codes[2];   // wk, wv
@@ -176,15 +188,17 @@ __device__ __forceinline__ int unit_col_lo(int gk, int u, int hd) {
     return (D_GCOLS * gk / hd + u / uph) * hd + 32 * (u % uph);
 }
 
+template <bool NARROW>
 __global__ void __launch_bounds__(D_THREADS, 1)
 fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
+    using Lay = DLayout<NARROW>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + OFF_SMALL);
+    uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + Lay::OFF_SMALL);
     uint64_t* a_empty = a_full + D_RA;
     uint64_t* b_full = a_empty + D_RA;
-    uint64_t* b_empty = b_full + D_RB;
-    uint64_t* acc_full = b_empty + D_RB;
+    uint64_t* b_empty = b_full + Lay::RB;
+    uint64_t* acc_full = b_empty + Lay::RB;
     uint64_t* ss_ready = acc_full + 1;
     int64_t* s_ioff = reinterpret_cast<int64_t*>(ss_ready + 1);   // item part of the cache offset, or -1
     int* s_pos = reinterpret_cast<int*>(s_ioff + D_MAX_ITEMS);
@@ -212,7 +226,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             tc::mbar_init(&a_full[s], D_CP_WARPS);
             tc::mbar_init(&a_empty[s], 1);                // MMA commit
         }
-        for (int s = 0; s < D_RB; ++s) {
+        for (int s = 0; s < Lay::RB; ++s) {
             tc::mbar_init(&b_full[s], D_DEQ_WARPS);
             tc::mbar_init(&b_empty[s], 1);
         }
@@ -234,7 +248,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     // Chunk c of the CTA's codes / scales / zeros into ring slot c % D_RC. Staged
     // column order: unit u's low half, then its high half (64 u .. 64 u + 63).
     auto load_chunk = [&](int c) {
-        uint8_t* base = smem + OFF_C + (c % D_RC) * CH_BYTES;
+        uint8_t* base = smem + Lay::OFF_C + (c % D_RC) * CH_BYTES;
         const int kg = k0 + c * D_CH;             // first k of the chunk
         const uint8_t* src = L.codes[kv] + static_cast<int64_t>(kg / 2 + r_code) * a.kvw + col_code;
 #pragma unroll
@@ -246,7 +260,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     };
     if (warp < D_DEQ_WARPS) {
         // g_j over this CTA's k range rides in chunk 0's group.
-        for (int v = threadIdx.x; v < kc / 8; v += D_DEQ_THREADS) cp_async16(smem + OFF_G + v * 16, L.gamma + k0 + v * 8);
+        for (int v = threadIdx.x; v < kc / 8; v += D_DEQ_THREADS) cp_async16(smem + Lay::OFF_G + v * 16, L.gamma + k0 + v * 8);
         for (int c = 0; c < D_RC; ++c) {
             if (c < nch) load_chunk(c);
             cp_async_commit();
@@ -269,10 +283,10 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         for (int c = 0; c < nch; ++c) {
             cp_async_wait<D_RC - 1>();                            // chunk c has landed (own copies)
             deq_bar_sync();                                       // ... and everyone's
-            const uint8_t* base = smem + OFF_C + (c % D_RC) * CH_BYTES;
+            const uint8_t* base = smem + Lay::OFF_C + (c % D_RC) * CH_BYTES;
             for (int b = 0; b < D_BPC && ok; ++b) {
-                const int kb = c * D_BPC + b, s = kb % D_RB;
-                if (kb >= D_RB && !warp_wait(&b_empty[s], ((kb / D_RB) - 1) & 1, abort, ws, 51)) {
+                const int kb = c * D_BPC + b, s = kb % Lay::RB;
+                if (kb >= Lay::RB && !warp_wait(&b_empty[s], ((kb / Lay::RB) - 1) & 1, abort, ws, 51)) {
                     ok = false;
                     break;
                 }
@@ -291,10 +305,10 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                 unpack_f16x2(z4.x, zr[0], zr[1]);
                 unpack_f16x2(z4.y, zr[2], zr[3]);
                 // g_j of the thread's 16 k, as 8 bf16 pairs (k 16 kq + 2i, +1)
-                const uint4 ga = *reinterpret_cast<const uint4*>(smem + OFF_G + (kb * D_KB + kq * 16) * 2);
-                const uint4 gb = *reinterpret_cast<const uint4*>(smem + OFF_G + (kb * D_KB + kq * 16 + 8) * 2);
+                const uint4 ga = *reinterpret_cast<const uint4*>(smem + Lay::OFF_G + (kb * D_KB + kq * 16) * 2);
+                const uint4 gb = *reinterpret_cast<const uint4*>(smem + Lay::OFF_G + (kb * D_KB + kq * 16 + 8) * 2);
                 const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                uint8_t* bslot = smem + OFF_B + s * B_SLOT;
+                uint8_t* bslot = smem + Lay::OFF_B + s * B_SLOT;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const __nv_bfloat162 s2 = __floats2bfloat162_rn(sc[j], sc[j]);
@@ -323,12 +337,12 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_bf16(128, D_GCOLS);
             for (int kb = 0; kb < nkb; ++kb) {
-                const int sa = kb % D_RA, sb = kb % D_RB;
+                const int sa = kb % D_RA, sb = kb % Lay::RB;
                 if (!tc::mbar_wait(&a_full[sa], (kb / D_RA) & 1, abort, ws, 53)) break;
-                if (!tc::mbar_wait(&b_full[sb], (kb / D_RB) & 1, abort, ws, 54)) break;
+                if (!tc::mbar_wait(&b_full[sb], (kb / Lay::RB) & 1, abort, ws, 54)) break;
                 tc::tc_fence_after();
-                const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(smem + OFF_A + sa * A_SLOT));
-                const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + OFF_B + sb * B_SLOT));
+                const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(smem + Lay::OFF_A + sa * Lay::A_SLOT));
+                const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + Lay::OFF_B + sb * B_SLOT));
 #pragma unroll
                 for (int kk = 0; kk < D_KB / 16; ++kk) tc::umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, kb | kk);
                 tc::umma_commit(&a_empty[sa]);
@@ -344,7 +358,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
         const int ct = threadIdx.x - D_CP_WARP0 * 32;
         const int j = ct & 7, ib = ct >> 3;
         wait_prior_grid();
-        n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
+        n = min(item_count(a.n_max, a.n_dev), Lay::ITEMS);
         // Item ct's h row slice, pulled into L2 whole (every CTA of the column groups
         // reads it).
         int r_ct = -1;
@@ -357,30 +371,30 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                 record_fault(ws, TEE_DEVERR_ROW, r);
             }
         }
-        const bf16* src[D_ITEMS_PER_CP];
+        const bf16* src[Lay::IPC];
 #pragma unroll
-        for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
+        for (int m = 0; m < Lay::IPC; ++m) {
             const int i = ib + 16 * m;
             const int r = i < n ? (a.rows ? a.rows[i] : i) : -1;
             src[m] = (r >= 0 && r < a.h_rows) ? a.h + static_cast<int64_t>(r) * a.ld_h + k0 + j * 8 : nullptr;
         }
         auto issue = [&](int kb) {
-            uint8_t* slot = smem + OFF_A + (kb % D_RA) * A_SLOT;
+            uint8_t* slot = smem + Lay::OFF_A + (kb % D_RA) * Lay::A_SLOT;
 #pragma unroll
-            for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
+            for (int m = 0; m < Lay::IPC; ++m) {
                 const int i = ib + 16 * m;
                 if (src[m]) cp_async16(slot + i * 128 + ((j ^ (i & 7)) << 4), src[m] + kb * D_KB);
             }
         };
-        float ss[D_ITEMS_PER_CP];
+        float ss[Lay::IPC];
 #pragma unroll
-        for (int m = 0; m < D_ITEMS_PER_CP; ++m) ss[m] = 0.f;
+        for (int m = 0; m < Lay::IPC; ++m) ss[m] = 0.f;
         // Block kb's pieces of this thread have landed: add their squares, order them
         // for the tensor core, and release the block once the whole warp is done.
         auto release = [&](int kb) {
-            const uint8_t* slot = smem + OFF_A + (kb % D_RA) * A_SLOT;
+            const uint8_t* slot = smem + Lay::OFF_A + (kb % D_RA) * Lay::A_SLOT;
 #pragma unroll
-            for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
+            for (int m = 0; m < Lay::IPC; ++m) {
                 if (!src[m]) continue;
                 const int i = ib + 16 * m;
                 ss[m] = sumsq8(*reinterpret_cast<const uint4*>(slot + i * 128 + ((j ^ (i & 7)) << 4)), ss[m]);
@@ -408,7 +422,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
             for (int b = max(0, nkb - D_LAG); b < nkb; ++b) release(b);
         // Per-item totals: the eight threads of an item are consecutive lanes.
 #pragma unroll
-        for (int m = 0; m < D_ITEMS_PER_CP; ++m) {
+        for (int m = 0; m < Lay::IPC; ++m) {
             float t = ss[m];
             t += __shfl_xor_sync(0xffffffffu, t, 1);
             t += __shfl_xor_sync(0xffffffffu, t, 2);
@@ -440,7 +454,7 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     }
 
     wait_prior_grid();
-    n = min(item_count(a.n_max, a.n_dev), D_MAX_ITEMS);
+    n = min(item_count(a.n_max, a.n_dev), Lay::ITEMS);
     // ---- the reduction across the cluster, through this call's workspace slots.
     // Accumulator column cg + 64 j holds staged column 4 cg + j, i.e. unit cg / 16,
     // unit column 4 (cg % 16) + j: float4 m = cg % 16 of a unit row holds its
@@ -583,11 +597,12 @@ int choose_ks(int d, int ctas_per_split, int max_clusters_4, int max_clusters_2)
     return 1;
 }
 
+template <bool NARROW>
 tee_status launch(const DecodeArgs& a, dim3 grid, int ks, bool early, void* ws, cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(D_THREADS);
-    cfg.dynamicSmemBytes = D_SMEM;
+    cfg.dynamicSmemBytes = DLayout<NARROW>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -598,15 +613,16 @@ tee_status launch(const DecodeArgs& a, dim3 grid, int ks, bool early, void* ws, 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = early ? 2 : 1;
-    const tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, fill_decode_kernel, a, ws));
+    const tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, fill_decode_kernel<NARROW>, a, ws));
     return st != TEE_OK ? st : launch_status();   // counts the launch
 }
 
+// Clusters of ks CTAs that can be resident at once (both layouts take one CTA per SM).
 int max_clusters(int ks) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(ks * 64, 1);
     cfg.blockDim = dim3(D_THREADS);
-    cfg.dynamicSmemBytes = D_SMEM;
+    cfg.dynamicSmemBytes = DLayout<false>::SMEM;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = ks;
@@ -615,7 +631,7 @@ int max_clusters(int ks) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fill_decode_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, fill_decode_kernel<false>, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
@@ -648,8 +664,11 @@ tee_status fill_decode_run(const FillCall& fc) {
     static bool attr_set = false;
     static int mc4 = 0, mc2 = 0;
     if (!attr_set) {
-        tee_status st = cuda_status(cudaFuncSetAttribute(fill_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         static_cast<int>(D_SMEM)));
+        tee_status st = cuda_status(cudaFuncSetAttribute(
+            fill_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(DLayout<false>::SMEM)));
+        if (st != TEE_OK) return st;
+        st = cuda_status(cudaFuncSetAttribute(fill_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(DLayout<true>::SMEM)));
         if (st != TEE_OK) return st;
         mc4 = max_clusters(4);
         mc2 = max_clusters(2);
@@ -702,7 +721,8 @@ tee_status fill_decode_run(const FillCall& fc) {
     // An early launch parks the grid's CTAs on their SMs until the previous kernel
     // completes: only when the grid leaves SMs free for that kernel to finish on.
     const bool early = (D.flags & TEE_FILL_EARLY_WEIGHTS) && static_cast<int>(grid.x * grid.y) + 4 <= sm_count();
-    return launch(a, grid, a.ks, early, fc.ws, fc.stream);
+    return fc.n_max <= DLayout<true>::ITEMS ? launch<true>(a, grid, a.ks, early, fc.ws, fc.stream)
+                                            : launch<false>(a, grid, a.ks, early, fc.ws, fc.stream);
 }
 
 }  // namespace tee

@@ -2,7 +2,8 @@
 // "state transition similarity"; method step 3), TIDE's batch compaction and
 // exit scatter (core module 4), for batches of up to 128 tokens.
 //
-// One cluster of C = ceil(n / 16) CTAs (C <= 8), a warp per token. Each warp
+// One cluster of C <= 8 CTAs of W = ceil(n / 8) warps (W <= 16), a warp per
+// token, so that even a small batch spreads over eight SMs. Each warp
 // streams its token's rows of h_prev and h_cur (16-byte loads, eight chunks of
 // each row per lane in flight; the h_cur chunks stay in registers), reduces
 // <a,b>, |a|^2, |b|^2 in fp32 and forms the score. Each CTA publishes, in its
@@ -23,7 +24,7 @@ namespace tee {
 
 namespace {
 
-constexpr int FW = 16;                 // warps (tokens) per CTA
+constexpr int FW = 16;                 // warps (tokens) per CTA at most
 constexpr int F_THREADS = FW * 32;
 constexpr int F_MAX_CTAS = 8;          // portable cluster size
 constexpr int F_MAX_TOKENS = FW * F_MAX_CTAS;
@@ -113,7 +114,8 @@ __global__ void __launch_bounds__(F_THREADS, 1) front_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t cta = cluster_rank();
     const int n_ctas = static_cast<int>(gridDim.x);   // the grid is one cluster
-    const int t = static_cast<int>(cta) * FW + warp;
+    const int fw = static_cast<int>(blockDim.x) >> 5;   // tokens per CTA
+    const int t = static_cast<int>(cta) * fw + warp;
     const bool live = t < a.n;
     constexpr int V = 16 / sizeof(T);
     const int nch = a.d / V;
@@ -162,8 +164,8 @@ __global__ void __launch_bounds__(F_THREADS, 1) front_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         float m = INFINITY;
         uint32_t bits = 0;
-        for (int w = 0; w < FW; ++w) {
-            if (static_cast<int>(cta) * FW + w >= a.n) break;
+        for (int w = 0; w < fw; ++w) {
+            if (static_cast<int>(cta) * fw + w >= a.n) break;
             const float sw = s_score[w];
             m = fminf(m, sw == sw ? sw : -INFINITY);   // a NaN score never lets the batch exit
             if (exits(sw, a.thr)) bits |= 1u << w;
@@ -191,9 +193,9 @@ __global__ void __launch_bounds__(F_THREADS, 1) front_kernel(const __grid_consta
     const bool all_exit = a.n > 0 && gmin > a.thr;
     uint32_t bits = s_exit_bits;
     if (a.rule == TEE_RULE_BATCH_ALL) {
-        const int live_here = min(max(a.n - static_cast<int>(cta) * FW, 0), FW);
-        bits = all_exit ? (live_here == 32 ? 0xFFFFFFFFu : (1u << live_here) - 1u) : 0u;
-        before = all_exit ? min(static_cast<int>(cta) * FW, a.n) : 0;
+        const int live_here = min(max(a.n - static_cast<int>(cta) * fw, 0), fw);
+        bits = all_exit ? (1u << live_here) - 1u : 0u;   // live_here <= 16
+        before = all_exit ? min(static_cast<int>(cta) * fw, a.n) : 0;
         total = all_exit ? a.n : 0;
     }
     const bool ex = live && ((bits >> warp) & 1u);
@@ -244,10 +246,11 @@ __global__ void __launch_bounds__(F_THREADS, 1) front_kernel(const __grid_consta
 
 template <typename T>
 tee_status launch_front(const FrontArgs& a, cudaStream_t stream) {
-    const int ctas = (a.n + FW - 1) / FW;
+    const int fw = (a.n + F_MAX_CTAS - 1) / F_MAX_CTAS;   // 1..16 tokens per CTA
+    const int ctas = (a.n + fw - 1) / fw;                 // <= 8
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(ctas);
-    cfg.blockDim = dim3(F_THREADS);
+    cfg.blockDim = dim3(fw * 32);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
