@@ -105,7 +105,10 @@ generic_gemm_kernel(int n_max, const int32_t* __restrict__ n_dev, int K, int N, 
     const float rs = (m < n && A.rowscale) ? A.rowscale[m] : 1.f;
     const int bk = tid / 16, bc = (tid % 16) * 4;
     float acc[4][4] = {};
-    for (int k0 = 0; k0 < K; k0 += GB_K) {
+    // The next k tile is loaded into registers while the current one is multiplied
+    // from shared memory, so that a k step does not wait for its loads.
+    float ra[4], rb[4];
+    auto load_tile = [&](int k0) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int k = k0 + ak + q;
@@ -115,14 +118,23 @@ generic_gemm_kernel(int n_max, const int32_t* __restrict__ n_dev, int K, int N, 
                 if (A.colscale) v *= to_f32(A.colscale[k]);
                 v *= rs;
             }
-            As[ak + q][am] = v;
+            ra[q] = v;
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int k = k0 + bk, c = c0 + bc + q;
-            Bs[bk][bc + q] = (k < K && c < N) ? load_b(B, k, c) : 0.f;
+            rb[q] = (k < K && c < N) ? load_b(B, k, c) : 0.f;
+        }
+    };
+    load_tile(0);
+    for (int k0 = 0; k0 < K; k0 += GB_K) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            As[ak + q][am] = ra[q];
+            Bs[bk][bc + q] = rb[q];
         }
         __syncthreads();
+        if (k0 + GB_K < K) load_tile(k0 + GB_K);
 #pragma unroll
         for (int kk = 0; kk < GB_K; ++kk) {
             float a[4], b[4];
