@@ -84,7 +84,8 @@ enum {
     TEE_DEVERR_SEQ = 3,        /* a cache sequence outside [0, n_seq) */
     TEE_DEVERR_COUNT = 4,      /* a device-side count larger than its host-side bound */
     TEE_DEVERR_DEST = 5,       /* a scatter destination outside [0, n_out) */
-    TEE_DEVERR_TIMEOUT = 6     /* a pipeline wait ran out of time; the kernel stopped early (detail: where) */
+    TEE_DEVERR_TIMEOUT = 6,    /* a pipeline wait ran out of time; the kernel stopped early (detail: where) */
+    TEE_DEVERR_NOT_SPD = 7     /* the ridge fit met a pivot <= 0 (detail: the column); the map is NaN */
 };
 
 #define TEE_WS_HEADER_BYTES 256
@@ -380,6 +381,28 @@ TEE_API tee_status tee_kv_fill(const tee_fill_desc* desc, int32_t n_layers, cons
                        const int32_t* rows, const int32_t* pos, int32_t pos0, const int32_t* seq,
                        void* k_cache, void* v_cache, const tee_cache_layout* cache,
                        void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------- ridge fit (next) */
+
+TEE_API size_t tee_ridge_fit_workspace_size(int32_t n, int32_t d, int32_t d_out);
+
+/*
+ * RidgeFill's per-layer map, fitted on the GPU (RidgeFill, "closed-form ridge
+ * regression" note): W = (X^T X + lambda I)^-1 X^T Y over n calibration rows.
+ *
+ *   x     [n][ld_x] bf16: split-layer states;  y [n][ld_y] bf16: the true
+ *         inputs of the filled layer
+ *   w     [d][ld_w] f32 out: the map, for x_j = h W (tee_kv_fill's w_map
+ *         after a conversion to the fill's dtype)
+ *   d, d_out multiples of 256; lambda >= 0
+ * X^T X and X^T Y accumulate in fp32 on the tensor cores; the Cholesky
+ * factorisation and the two triangular solves run in fp32. A pivot <= 0
+ * (X^T X + lambda I not positive definite in fp32) records
+ * TEE_DEVERR_NOT_SPD and leaves NaN in w.
+ */
+TEE_API tee_status tee_ridge_fit(int32_t n, int32_t d, int32_t d_out, const void* x, int64_t ld_x,
+                                 const void* y, int64_t ld_y, int32_t dtype, float lambda,
+                                 float* w, int64_t ld_w, void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -108,3 +108,27 @@ def test_fill_descriptor_checks(lib):
     # a layer without weights
     assert lib.tee_kv_fill(ctypes.byref(D), 1, arr, fake, 1 << 30, 4, None, fake, 4096, 4, None, None, 0, None,
                            fake, fake, ctypes.byref(layout), fake, 1 << 40, None) == _lib.TEE_ERR_INVALID_ARG
+
+
+def test_fused_and_ridge_entry_points_check_on_the_host(lib):
+    from token_early_exit_gb300 import _lib
+    fake = ctypes.c_void_p(16)  # never dereferenced: every call below fails its checks first
+    # compaction + scatter: h without an output to scatter into
+    assert lib.tee_exit_compact_scatter(8, fake, None, fake, 256, 256, _lib.TEE_BF16, fake, fake, None, None, None, 0,
+                                        None, 0, 0, fake, fake, 1 << 20, None) == _lib.TEE_ERR_INVALID_ARG
+    # gate + compaction + scatter: too small a workspace, then a misaligned output row
+    g = _lib.GateDesc(mode=_lib.TEE_GATE_COSINE, rule=_lib.TEE_RULE_PER_TOKEN, dtype=_lib.TEE_BF16, d=256,
+                      bottleneck=0, threshold=0.9, eps=1e-5)
+    args = [ctypes.byref(g), 8, fake, 256, fake, 256, None, None, None, None, None, None, fake, fake, None, fake,
+            fake, None, None, None, 0, fake, 256, 8, fake, fake]
+    assert lib.tee_exit_gate_compact_scatter(*args, 8, None) == _lib.TEE_ERR_WORKSPACE
+    args[22] = 257
+    assert lib.tee_exit_gate_compact_scatter(*args, 1 << 20, None) == _lib.TEE_ERR_INVALID_ARG
+    # ridge fit: widths off the 256-column tiles, a negative lambda, a short workspace
+    assert lib.tee_ridge_fit(64, 200, 256, fake, 200, fake, 256, _lib.TEE_BF16, 0.1, fake, 256, fake, 1 << 30,
+                             None) == _lib.TEE_ERR_UNSUPPORTED
+    assert lib.tee_ridge_fit(64, 256, 256, fake, 256, fake, 256, _lib.TEE_BF16, -1.0, fake, 256, fake, 1 << 30,
+                             None) == _lib.TEE_ERR_INVALID_ARG
+    assert lib.tee_ridge_fit(64, 256, 256, fake, 256, fake, 256, _lib.TEE_BF16, 0.1, fake, 256, fake, 1024,
+                             None) == _lib.TEE_ERR_WORKSPACE
+    assert lib.tee_ridge_fit_workspace_size(64, 256, 256) > 256 * 256 * 4

@@ -5,7 +5,7 @@ The Python side only marshals arguments; see ``ops``.
 """
 from . import _lib  # noqa: F401
 from .ops import (KVFill, Workspace, cache_layout, exit_compact, exit_compact_scatter,  # noqa: F401
-                  exit_gate, exit_gate_compact_scatter, exit_scatter, kv_fill)
+                  exit_gate, exit_gate_compact_scatter, exit_scatter, kv_fill, ridge_fit)
 
-__all__ = ["exit_gate", "exit_compact", "exit_compact_scatter", "exit_gate_compact_scatter", "exit_scatter", "kv_fill", "KVFill", "Workspace",
+__all__ = ["exit_gate", "exit_compact", "exit_compact_scatter", "exit_gate_compact_scatter", "exit_scatter", "ridge_fit", "kv_fill", "KVFill", "Workspace",
            "cache_layout"]

@@ -69,6 +69,9 @@ SIGNATURES = {
     "tee_exit_gate_compact_scatter": (c_int, [POINTER(GateDesc), c_int32, _P, c_int64, _P, c_int64, _P, _P, _P, _P,
                                               _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, c_int64, _P, c_int64,
                                               c_int64, _P, _P, c_size_t, _P]),
+    "tee_ridge_fit_workspace_size": (c_size_t, [c_int32, c_int32, c_int32]),
+    "tee_ridge_fit": (c_int, [c_int32, c_int32, c_int32, _P, c_int64, _P, c_int64, c_int32, c_float, _P, c_int64, _P,
+                              c_size_t, _P]),
     "tee_exit_scatter_workspace_size": (c_size_t, [c_int32]),
     "tee_exit_scatter": (c_int, [c_int32, _P, _P, _P, _P, c_int64, _P, c_int64, c_int64, c_int32, c_int32, _P,
                                  c_float, _P, c_size_t, _P]),

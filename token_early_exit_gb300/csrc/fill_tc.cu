@@ -85,7 +85,7 @@ constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
 
-enum { EPI_MAP = 0, EPI_KV = 1 };
+enum { EPI_MAP = 0, EPI_KV = 1, EPI_F32 = 2 };
 // Where a pipeline wait gave up (detail of TEE_DEVERR_TIMEOUT).
 enum { W_EMPTY = 1, W_ACC_EMPTY = 2, W_FULL = 3, W_ACC_FULL = 4, W_DRAIN = 5, W_TEARDOWN = 6 };
 
@@ -106,6 +106,11 @@ struct EpiArgs {
     bf16* vc;
     tee_cache_layout cl;
     int layer, kvw, hd, half, h_rows;
+    // fp32 output (the ridge fit's Gram matrices): C, its row stride, and a value
+    // added where row == column
+    float* c32;
+    int64_t ldc32;
+    float diag;
 };
 
 __device__ __forceinline__ void store32_bf16(bf16* dst, const float (&v)[32]) {
@@ -130,6 +135,25 @@ __device__ __forceinline__ void epi_map(const EpiArgs& ep, int row, int n, int c
         if (ok) store32_bf16(dst + c * 32, v);
     }
     if (ok) atomicAdd(ep.sumsq_out + row, ss);
+}
+
+// fp32 epilogue: the tile row as it accumulated, plus ep.diag on the diagonal.
+__device__ __forceinline__ void epi_f32(const EpiArgs& ep, int row, int n, int c0, uint32_t t_base) {
+    const bool ok = row < n;
+    float* dst = ep.c32 + static_cast<int64_t>(row) * ep.ldc32 + c0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tc::tmem_ld32(t_base + c * 32, v);
+        if (!ok) continue;
+        const int dc = row - (c0 + c * 32);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j == dc) v[j] += ep.diag;
+        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
 }
 
 // K/V epilogue: 1/rms row scale, RoPE on K heads, store into the cache slot.
@@ -326,8 +350,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t t_base = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
             if (EPI == EPI_MAP)
                 epi_map(ep, row, n, c0, t_base);
-            else
+            else if (EPI == EPI_KV)
                 epi_kv(ep, row, n, c0, t_base, ws);
+            else
+                epi_f32(ep, row, n, c0, t_base);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty[acc]);
@@ -426,6 +452,46 @@ tee_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int n_max, co
 }
 
 }  // namespace
+
+// ---- the ridge fit's Gram matrices (RidgeFill's closed-form fit) on the same GEMM:
+// G = X^T X + lambda I [d][d] and R = X^T Y [d][d_out], fp32, from bf16 X [n][ld_x]
+// and Y [n][ld_y]. X and Y are first transposed into K-major copies [d][n_pad] and
+// [d_out][n_pad] (n_pad = n rounded up to 64, zero columns past n).
+size_t ridge_gram_ws_bytes(int n, int d, int d_out) {
+    const size_t n_pad = round_up(static_cast<size_t>(n), BK);
+    return round_up(static_cast<size_t>(d) * n_pad * 2, 1024) + round_up(static_cast<size_t>(d_out) * n_pad * 2, 1024);
+}
+
+tee_status ridge_gram(int n, int d, int d_out, const void* x, int64_t ld_x, const void* y, int64_t ld_y, float lambda,
+                      float* g, float* r, int64_t ld_r, char* scratch, void* ws, cudaStream_t s) {
+    if (d % BN || d_out % BN) return TEE_ERR_UNSUPPORTED;
+    const int n_pad = static_cast<int>(round_up(static_cast<size_t>(n), BK));
+    bf16* xt = reinterpret_cast<bf16*>(scratch);
+    bf16* yt = reinterpret_cast<bf16*>(scratch + round_up(static_cast<size_t>(d) * n_pad * 2, 1024));
+    tee_status st = cuda_status(cudaMemsetAsync(scratch, 0, ridge_gram_ws_bytes(n, d, d_out), s));
+    if (st != TEE_OK) return st;
+    dim3 blk(32, 8);
+    transpose_scale_kernel<<<dim3((d + 31) / 32, (n + 31) / 32), blk, 0, s>>>(static_cast<const bf16*>(x), n, d, ld_x,
+                                                                            nullptr, xt, n_pad);
+    if ((st = launch_status()) != TEE_OK) return st;
+    transpose_scale_kernel<<<dim3((d_out + 31) / 32, (n + 31) / 32), blk, 0, s>>>(static_cast<const bf16*>(y), n, d_out,
+                                                                                ld_y, nullptr, yt, n_pad);
+    if ((st = launch_status()) != TEE_OK) return st;
+    CUtensorMap tx, ty;
+    if ((st = make_tmap_bf16(&tx, xt, n_pad, d, static_cast<uint64_t>(n_pad) * 2, BK, BM)) != TEE_OK) return st;
+    CUtensorMap txb;
+    if ((st = make_tmap_bf16(&txb, xt, n_pad, d, static_cast<uint64_t>(n_pad) * 2, BK, BN)) != TEE_OK) return st;
+    if ((st = make_tmap_bf16(&ty, yt, n_pad, d_out, static_cast<uint64_t>(n_pad) * 2, BK, BN)) != TEE_OK) return st;
+    EpiArgs ep{};
+    ep.c32 = g;
+    ep.ldc32 = d;
+    ep.diag = lambda;
+    if ((st = launch_gemm<EPI_F32>(tx, txb, d, nullptr, d, n_pad, ep, ws, s)) != TEE_OK) return st;
+    ep.c32 = r;
+    ep.ldc32 = ld_r;
+    ep.diag = 0.f;
+    return launch_gemm<EPI_F32>(tx, ty, d, nullptr, d_out, n_pad, ep, ws, s);
+}
 
 size_t fill_tc_prep_bytes(const tee_fill_desc& D, int n_layers) {
     if (!desc_eligible(D)) return 0;

@@ -1,0 +1,260 @@
+// RidgeFill's per-layer linear map, fitted on the GPU (RidgeFill, "closed-form
+// ridge regression" note): W = (X^T X + lambda I)^-1 X^T Y, with X the split-layer
+// states and Y the true inputs of the filled layer over the calibration rows.
+//
+// The Gram matrices G = X^T X + lambda I and R = X^T Y come from the tcgen05 GEMM
+// (fp32 accumulate; ridge_gram in fill_tc.cu). G is then factorised in place as
+// L L^T (blocked right-looking Cholesky in fp32, 64 x 64 tiles: the diagonal tile
+// in one CTA's shared memory, the panel below it by substitution, the trailing
+// lower triangle updated tile by tile), and W = L^-T L^-1 R is solved in place in
+// the output by block forward and backward substitution.
+#include "common.cuh"
+
+namespace tee {
+
+size_t ridge_gram_ws_bytes(int n, int d, int d_out);
+tee_status ridge_gram(int n, int d, int d_out, const void* x, int64_t ld_x, const void* y, int64_t ld_y, float lambda,
+                      float* g, float* r, int64_t ld_r, char* scratch, void* ws, cudaStream_t s);
+
+namespace {
+
+constexpr int NB = 64;           // tile
+constexpr int NT = 256;          // threads of the tile kernels
+constexpr int TLD = NB + 1;      // shared-memory row stride of a tile (conflict-free columns)
+
+// Factor the diagonal tile k of G (lower triangle) in shared memory. A pivot that
+// is not positive records TEE_DEVERR_NOT_SPD with its column and leaves NaN.
+__global__ void __launch_bounds__(NT) potrf_tile_kernel(float* __restrict__ G, int64_t ld, int k, void* ws) {
+    __shared__ float t[NB][TLD];
+    float* base = G + static_cast<int64_t>(k) * NB * ld + static_cast<int64_t>(k) * NB;
+    for (int e = threadIdx.x; e < NB * NB; e += NT) t[e / NB][e % NB] = base[static_cast<int64_t>(e / NB) * ld + e % NB];
+    __syncthreads();
+    for (int j = 0; j < NB; ++j) {
+        if (threadIdx.x == 0) {
+            const float p = t[j][j];
+            if (!(p > 0.f)) record_fault(ws, TEE_DEVERR_NOT_SPD, k * NB + j);
+            t[j][j] = sqrtf(p);   // NaN for a pivot <= 0, which then spreads to the solution
+        }
+        __syncthreads();
+        const float dj = t[j][j];
+        for (int i = j + 1 + threadIdx.x; i < NB; i += NT) t[i][j] /= dj;
+        __syncthreads();
+        // trailing update of the tile's lower triangle: t[i][c] -= t[i][j] t[c][j], j < c <= i
+        for (int i = j + 1 + (threadIdx.x >> 4); i < NB; i += NT / 16)
+            for (int c = j + 1 + (threadIdx.x & 15); c <= i; c += 16) t[i][c] -= t[i][j] * t[c][j];
+        __syncthreads();
+    }
+    for (int e = threadIdx.x; e < NB * NB; e += NT) {
+        const int i = e / NB, c = e % NB;
+        base[static_cast<int64_t>(i) * ld + c] = c <= i ? t[i][c] : 0.f;
+    }
+}
+
+// Panel below the diagonal tile k: 16-row slice blockIdx.x % 4 of block row
+// i = k + 1 + blockIdx.x / 4 becomes A_ik L_kk^-T (each row solved forward over the
+// columns, its dot products split over 16 threads).
+constexpr int RPC = 16;   // rows (or right-hand-side columns) per CTA, 16 threads each
+__global__ void __launch_bounds__(NT) trsm_panel_kernel(float* __restrict__ G, int64_t ld, int k) {
+    __shared__ float l[NB][TLD];
+    __shared__ float a[RPC][TLD];
+    const int i = k + 1 + blockIdx.x / (NB / RPC), r0 = (blockIdx.x % (NB / RPC)) * RPC;
+    const float* lk = G + static_cast<int64_t>(k) * NB * ld + static_cast<int64_t>(k) * NB;
+    float* ai = G + (static_cast<int64_t>(i) * NB + r0) * ld + static_cast<int64_t>(k) * NB;
+    for (int e = threadIdx.x; e < NB * NB; e += NT) l[e / NB][e % NB] = lk[static_cast<int64_t>(e / NB) * ld + e % NB];
+    for (int e = threadIdx.x; e < RPC * NB; e += NT) a[e / NB][e % NB] = ai[static_cast<int64_t>(e / NB) * ld + e % NB];
+    __syncthreads();
+    const int row = threadIdx.x >> 4, sub = threadIdx.x & 15;   // 16 rows x 16 threads
+    for (int c = 0; c < NB; ++c) {
+        float s = 0.f;
+        for (int cc = sub; cc < c; cc += 16) s = fmaf(a[row][cc], l[c][cc], s);
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (sub == 0) a[row][c] = (a[row][c] - s) / l[c][c];
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < RPC * NB; e += NT) ai[static_cast<int64_t>(e / NB) * ld + e % NB] = a[e / NB][e % NB];
+}
+
+// C -= A B^T on one 64 x 64 tile, K = 64, fp32; 16 outputs a thread.
+__device__ __forceinline__ void tile_update(float* __restrict__ C, int64_t ldc, const float* __restrict__ A,
+                                            int64_t lda, const float* __restrict__ B, int64_t ldb,
+                                            float (&sa)[NB][TLD], float (&sb)[NB][TLD]) {
+    // sa[kk][m] = A(m, kk), sb[kk][c] = B(c, kk)
+    for (int e = threadIdx.x; e < NB * NB; e += NT) {
+        const int r = e / NB, c = e % NB;
+        sa[c][r] = A[static_cast<int64_t>(r) * lda + c];
+        sb[c][r] = B[static_cast<int64_t>(r) * ldb + c];
+    }
+    __syncthreads();
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4] = {};
+#pragma unroll 8
+    for (int kk = 0; kk < NB; ++kk) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            av[q] = sa[kk][ty * 4 + q];
+            bv[q] = sb[kk][tx * 4 + q];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) acc[q][w] = fmaf(av[q], bv[w], acc[q][w]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) C[static_cast<int64_t>(ty * 4 + q) * ldc + tx * 4 + w] -= acc[q][w];
+}
+
+// Trailing lower triangle after panel k: tile (i, j), k < j <= i, gets -= L_ik L_jk^T.
+__global__ void __launch_bounds__(NT) syrk_kernel(float* __restrict__ G, int64_t ld, int k, int nb) {
+    __shared__ float sa[NB][TLD];
+    __shared__ float sb[NB][TLD];
+    // blockIdx.x -> (i, j) over the lower triangle of the trailing tiles, row by row
+    int e = blockIdx.x, i = 0;
+    while (e > i) {
+        e -= i + 1;
+        ++i;
+    }
+    const int j = e;   // 0 <= j <= i
+    const int ti = k + 1 + i, tj = k + 1 + j;
+    if (ti >= nb) return;
+    float* c = G + static_cast<int64_t>(ti) * NB * ld + static_cast<int64_t>(tj) * NB;
+    const float* a = G + static_cast<int64_t>(ti) * NB * ld + static_cast<int64_t>(k) * NB;
+    const float* b = G + static_cast<int64_t>(tj) * NB * ld + static_cast<int64_t>(k) * NB;
+    tile_update(c, ld, a, ld, b, ld, sa, sb);
+}
+
+// Forward substitution on block row k of the right-hand sides: R_k <- L_kk^-1 R_k,
+// 16 columns per CTA (16 threads per column, rows in order).
+// Backward (upper = true): R_k <- L_kk^-T R_k, rows in reverse.
+__global__ void __launch_bounds__(NT) trsm_rhs_kernel(const float* __restrict__ G, int64_t ld, float* __restrict__ R,
+                                                      int64_t ldr, int k, bool upper) {
+    __shared__ float l[NB][TLD];
+    __shared__ float x[NB][RPC + 1];   // x[row][col]
+    const float* lk = G + static_cast<int64_t>(k) * NB * ld + static_cast<int64_t>(k) * NB;
+    float* rk = R + static_cast<int64_t>(k) * NB * ldr + static_cast<int64_t>(blockIdx.x) * RPC;
+    for (int e = threadIdx.x; e < NB * NB; e += NT) l[e / NB][e % NB] = lk[static_cast<int64_t>(e / NB) * ld + e % NB];
+    for (int e = threadIdx.x; e < NB * RPC; e += NT) x[e / RPC][e % RPC] = rk[static_cast<int64_t>(e / RPC) * ldr + e % RPC];
+    __syncthreads();
+    const int col = threadIdx.x >> 4, sub = threadIdx.x & 15;
+    for (int step = 0; step < NB; ++step) {
+        const int r = upper ? NB - 1 - step : step;
+        float s = 0.f;
+        if (!upper) {
+            for (int rr = sub; rr < r; rr += 16) s = fmaf(l[r][rr], x[rr][col], s);   // L[r][rr], rr < r
+        } else {
+            for (int rr = r + 1 + sub; rr < NB; rr += 16) s = fmaf(l[rr][r], x[rr][col], s);   // L^T[r][rr] = L[rr][r]
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (sub == 0) x[r][col] = (x[r][col] - s) / l[r][r];
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < NB * RPC; e += NT) rk[static_cast<int64_t>(e / RPC) * ldr + e % RPC] = x[e / RPC][e % RPC];
+}
+
+// Right-hand-side update after block row k was solved. Forward: R_i -= L_ik R_k for
+// i > k. Backward: R_i -= L_ki^T R_k for i < k. Tile (i, column tile c) per CTA.
+__global__ void __launch_bounds__(NT) rhs_update_kernel(const float* __restrict__ G, int64_t ld, float* __restrict__ R,
+                                                        int64_t ldr, int k, int nb, bool upper) {
+    __shared__ float sa[NB][TLD];
+    __shared__ float sb[NB][TLD];
+    const int m = upper ? k : nb - 1 - k;   // block rows to update
+    const int bi = blockIdx.x % m, ct = blockIdx.x / m;
+    const int i = upper ? bi : k + 1 + bi;
+    float* c = R + static_cast<int64_t>(i) * NB * ldr + static_cast<int64_t>(ct) * NB;
+    const float* rk = R + static_cast<int64_t>(k) * NB * ldr + static_cast<int64_t>(ct) * NB;
+    const float* a = upper ? G + static_cast<int64_t>(k) * NB * ld + static_cast<int64_t>(i) * NB      // L_ki, used as A^T
+                           : G + static_cast<int64_t>(i) * NB * ld + static_cast<int64_t>(k) * NB;     // L_ik
+    // sa[kk][m] = the left factor's (m, kk); sb[kk][c] = R_k[kk][c]
+    for (int e = threadIdx.x; e < NB * NB; e += NT) {
+        const int r = e / NB, cc = e % NB;
+        const float va = a[static_cast<int64_t>(r) * ld + cc];
+        if (upper)
+            sa[r][cc] = va;   // A^T: sa[kk][m] = L_ki[kk][m]
+        else
+            sa[cc][r] = va;   // sa[kk][m] = L_ik[m][kk]
+        sb[r][cc] = rk[static_cast<int64_t>(r) * ldr + cc];   // sb[kk][c] = R_k[kk][c]
+    }
+    __syncthreads();
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4] = {};
+#pragma unroll 8
+    for (int kk = 0; kk < NB; ++kk) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            av[q] = sa[kk][ty * 4 + q];
+            bv[q] = sb[kk][tx * 4 + q];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) acc[q][w] = fmaf(av[q], bv[w], acc[q][w]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) c[static_cast<int64_t>(ty * 4 + q) * ldr + tx * 4 + w] -= acc[q][w];
+}
+
+}  // namespace
+
+}  // namespace tee
+
+using namespace tee;
+
+extern "C" size_t tee_ridge_fit_workspace_size(int32_t n, int32_t d, int32_t d_out) {
+    if (n <= 0 || d <= 0 || d_out <= 0) return TEE_WS_HEADER_BYTES;
+    return TEE_WS_HEADER_BYTES + round_up(static_cast<size_t>(d) * d * 4, 1024) + ridge_gram_ws_bytes(n, d, d_out);
+}
+
+extern "C" tee_status tee_ridge_fit(int32_t n, int32_t d, int32_t d_out, const void* x, int64_t ld_x, const void* y,
+                                    int64_t ld_y, int32_t dtype, float lambda, float* w, int64_t ld_w, void* ws,
+                                    size_t ws_bytes, void* stream) {
+    if (n <= 0 || d <= 0 || d_out <= 0 || !x || !y || !w) return TEE_ERR_INVALID_ARG;
+    if (dtype != TEE_BF16) return TEE_ERR_UNSUPPORTED;
+    if (d % 256 || d_out % 256) return TEE_ERR_UNSUPPORTED;   // the GEMM's 256-column tiles
+    if (!(lambda >= 0.f) || ld_x < d || ld_y < d_out || ld_w < d_out || (ld_x * 2) % 16 || (ld_y * 2) % 16 ||
+        (ld_w * 4) % 16 || !aligned16(x) || !aligned16(y) || !aligned16(w))
+        return TEE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < tee_ridge_fit_workspace_size(n, d, d_out)) return TEE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws) + TEE_WS_HEADER_BYTES;
+    float* g = reinterpret_cast<float*>(base);
+    char* scratch = base + round_up(static_cast<size_t>(d) * d * 4, 1024);
+    tee_status st = ridge_gram(n, d, d_out, x, ld_x, y, ld_y, lambda, g, w, ld_w, scratch, ws, s);
+    if (st != TEE_OK) return st;
+    const int nb = d / NB, ncol = d_out / NB;
+    for (int k = 0; k < nb; ++k) {   // G = L L^T, in place
+        potrf_tile_kernel<<<1, NT, 0, s>>>(g, d, k, ws);
+        if ((st = launch_status()) != TEE_OK) return st;
+        const int m = nb - 1 - k;
+        if (m == 0) break;
+        trsm_panel_kernel<<<m * (NB / RPC), NT, 0, s>>>(g, d, k);
+        if ((st = launch_status()) != TEE_OK) return st;
+        syrk_kernel<<<m * (m + 1) / 2, NT, 0, s>>>(g, d, k, nb);
+        if ((st = launch_status()) != TEE_OK) return st;
+    }
+    for (int k = 0; k < nb; ++k) {   // L Z = R
+        trsm_rhs_kernel<<<d_out / RPC, NT, 0, s>>>(g, d, w, ld_w, k, false);
+        if ((st = launch_status()) != TEE_OK) return st;
+        if (k + 1 < nb) {
+            rhs_update_kernel<<<(nb - 1 - k) * ncol, NT, 0, s>>>(g, d, w, ld_w, k, nb, false);
+            if ((st = launch_status()) != TEE_OK) return st;
+        }
+    }
+    for (int k = nb - 1; k >= 0; --k) {   // L^T W = Z
+        trsm_rhs_kernel<<<d_out / RPC, NT, 0, s>>>(g, d, w, ld_w, k, true);
+        if ((st = launch_status()) != TEE_OK) return st;
+        if (k > 0) {
+            rhs_update_kernel<<<k * ncol, NT, 0, s>>>(g, d, w, ld_w, k, nb, true);
+            if ((st = launch_status()) != TEE_OK) return st;
+        }
+    }
+    return TEE_OK;
+}

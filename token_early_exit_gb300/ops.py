@@ -317,3 +317,23 @@ def kv_fill(h_split: torch.Tensor, layers: Sequence[Dict], k_cache: torch.Tensor
                dtype=h_split.dtype, max_pos=k_cache.shape[3], int4=int4, group=group)
     f(h_split, k_cache, v_cache, **kw)
     return f
+
+
+def ridge_fit(x: torch.Tensor, y: torch.Tensor, lam: float, *, ws: Optional[Workspace] = None,
+              out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """RidgeFill's map W = (X^T X + lam I)^-1 X^T Y on the GPU: x [n][d], y [n][d_out]
+    bf16 calibration rows; returns W [d][d_out] fp32."""
+    lib = load()
+    x = _mat(x, "x")
+    _mat(y, "y")
+    n, d = x.shape
+    d_out = y.shape[1]
+    if y.shape[0] != n:
+        raise ValueError("x and y need the same rows")
+    w = out if out is not None else torch.empty(d, d_out, dtype=torch.float32, device=x.device)
+    ws = ws or Workspace(x.device)
+    wp, wn = ws.get(lib.tee_ridge_fit_workspace_size(n, d, d_out))
+    st = lib.tee_ridge_fit(n, d, d_out, _ptr(x), x.stride(0), _ptr(y), y.stride(0), _DT[x.dtype], float(lam), _ptr(w),
+                           w.stride(0), wp, wn, _stream(x.device))
+    check("tee_ridge_fit", st)
+    return w
