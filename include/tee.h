@@ -329,8 +329,21 @@ typedef struct {
     const void* v_scale;
     const void* v_zero;
     int32_t cache_layer;  /* layer index into the caches */
-    int32_t reserved;
+    int32_t writes;       /* caches this layer writes: 0 (both), TEE_FILL_WRITE_K, TEE_FILL_WRITE_V */
+    /* Model-family variants (RidgeFill's per-model notes); all nullable:
+     * k = x^ Wk + k_bias, v = x^ Wv + v_bias (QKV-bias models); with k_norm,
+     * each head of k is RMS-normalised over head_dim (eps = desc->eps) and
+     * multiplied by k_norm before RoPE (QK-norm models). dtype of h. */
+    const void* k_bias;   /* [kvw] */
+    const void* v_bias;   /* [kvw] */
+    const void* k_norm;   /* [head_dim] */
 } tee_fill_layer;
+
+/* tee_fill_layer.writes: fill only the K cache (V kept as the backbone wrote
+ * it) or only the V cache: RidgeFill finds the fill's error in K on one model
+ * family and in V on another. */
+#define TEE_FILL_WRITE_K 1
+#define TEE_FILL_WRITE_V 2
 
 /* Cache geometry, shared by k_cache and v_cache. Strides are in elements;
  * head_dim is contiguous. Slot (layer, seq, head, pos) starts at

@@ -82,7 +82,10 @@ def fill_rows(h_rows, layer: Dict, pos, n_kv_heads: int, head_dim: int, rope_bas
     """K and V that filled layer j writes for the given split-layer rows.
 
     x_j = h W_j (identity when ``w_map`` is None); x^ = RMSNorm_j(x_j);
-    k = x^ Wk_j, v = x^ Wv_j; k gets RoPE at each row's position, per kv head.
+    k = x^ Wk_j (+ k_bias), v = x^ Wv_j (+ v_bias); with ``k_norm`` every head of
+    k is RMS-normalised over head_dim (same eps) and scaled by k_norm; then k
+    gets RoPE at each row's position, per kv head. The bias and the K norm are
+    the QKV-bias and QK-norm model families that RidgeFill's notes cover.
     Returns K, V of shape [rows][n_kv_heads][head_dim] in float64.
     """
     h = _f64(h_rows)
@@ -90,8 +93,16 @@ def fill_rows(h_rows, layer: Dict, pos, n_kv_heads: int, head_dim: int, rope_bas
     xn = rms_norm(x, layer["gamma"], eps)
     wk, wv = layer_weights(layer, group)
     t = h.shape[0]
-    k = (xn @ wk).reshape(t, n_kv_heads, head_dim)
-    v = (xn @ wv).reshape(t, n_kv_heads, head_dim)
+    k = xn @ wk
+    v = xn @ wv
+    if layer.get("k_bias") is not None:
+        k = k + _f64(layer["k_bias"])
+    if layer.get("v_bias") is not None:
+        v = v + _f64(layer["v_bias"])
+    k = k.reshape(t, n_kv_heads, head_dim)
+    v = v.reshape(t, n_kv_heads, head_dim)
+    if layer.get("k_norm") is not None:
+        k = rms_norm(k, layer["k_norm"], eps)
     k = rope_rotate_half(k, np.asarray(pos, dtype=np.float64)[:, None], rope_base)
     return k, v
 
@@ -106,7 +117,8 @@ def kv_fill(h_split, layers: Sequence[Dict], k_cache, v_cache, n_kv_heads: int, 
     p = pos[r] (or pos0 + r) and sequence s = seq[r] (or 0), and writes
     cache[layer.cache_layer][s][head][p][:] for every kv head, in both caches.
     Caches are [layers][seqs][kv_heads][positions][head_dim]; every other slot
-    keeps its value. Returns float64 copies of the two caches.
+    keeps its value. A layer with ``writes`` = "k" (or 1) fills only the K cache,
+    "v" (or 2) only the V cache. Returns float64 copies of the two caches.
     """
     h = _f64(h_split)
     kc = np.array(k_cache, dtype=np.float64, copy=True)
@@ -118,7 +130,12 @@ def kv_fill(h_split, layers: Sequence[Dict], k_cache, v_cache, n_kv_heads: int, 
     for layer in layers:
         k, v = fill_rows(h[rr], layer, pp, n_kv_heads, head_dim, rope_base, eps, group)
         L = int(layer["cache_layer"])
+        w = layer.get("writes")
+        write_k = w in (None, 0, "kv", 1, "k")
+        write_v = w in (None, 0, "kv", 2, "v")
         for i in range(n):
-            kc[L, ss[i], :, pp[i], :] = k[i]
-            vc[L, ss[i], :, pp[i], :] = v[i]
+            if write_k:
+                kc[L, ss[i], :, pp[i], :] = k[i]
+            if write_v:
+                vc[L, ss[i], :, pp[i], :] = v[i]
     return kc, vc

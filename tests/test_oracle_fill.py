@@ -179,6 +179,57 @@ def test_kv_fill_writes_exactly_the_backbone_slots():
     np.testing.assert_array_equal(k3[1, 0, :, 4], k_ref[1])
 
 
+# ------------------------------------------------------------------ model-family variants
+
+def test_fill_bias_with_zero_weights_is_the_bias():
+    # Wk = Wv = 0: k = k_bias, v = v_bias; at position 0 RoPE leaves k as it is
+    d, nkv, hd = 4, 2, 2
+    kb, vb = np.array([1.0, -2.0, 0.5, 3.0]), np.array([-1.0, 0.25, 2.0, 7.0])
+    L = _layer(d, nkv * hd, wk=np.zeros((d, nkv * hd)), wv=np.zeros((d, nkv * hd)))
+    L["k_bias"], L["v_bias"] = kb, vb
+    k, v = oracle.fill_rows(RNG.standard_normal((1, d)), L, [0], nkv, hd, 1e4, 1e-5)
+    np.testing.assert_array_equal(k[0].ravel(), kb)
+    np.testing.assert_array_equal(v[0].ravel(), vb)
+    # at position p the bias is rotated like any k: head (1, -2) by angle p (i = 0, hd = 2)
+    k, _ = oracle.fill_rows(RNG.standard_normal((1, d)), L, [1], nkv, hd, 1e4, 1e-5)
+    c, sn = math.cos(1.0), math.sin(1.0)
+    np.testing.assert_allclose(k[0, 0], [1.0 * c + 2.0 * sn, -2.0 * c + 1.0 * sn], atol=1e-15)
+
+
+def test_qk_norm_normalises_each_head_before_rope():
+    # worked example: one head k = (3, 4) at position 0, k_norm = (1, 1), eps = 0:
+    # mean square 12.5, k -> (3, 4)/sqrt(12.5)
+    d = 2
+    L = _layer(d, 2, wk=np.eye(2), wv=np.eye(2))
+    L["k_norm"] = np.ones(2)
+    h = np.array([[3.0, 4.0]])
+    k, v = oracle.fill_rows(h, L, [0], 1, 2, 1e4, eps=0.0)
+    xn = h / math.sqrt(12.5)   # the layer norm already gives unit mean square
+    np.testing.assert_allclose(k[0, 0], xn[0], atol=1e-15)
+    np.testing.assert_allclose(v[0, 0], xn[0], atol=1e-15)   # v is not normalised by k_norm
+    # any head: mean square 1 before RoPE (which keeps pair norms, so also after), scaled by k_norm
+    d, nkv, hd = 16, 2, 8
+    L = _layer(d, nkv * hd)
+    L["k_bias"] = RNG.standard_normal(nkv * hd)
+    L["k_norm"] = np.full(hd, 2.0)
+    k, _ = oracle.fill_rows(RNG.standard_normal((3, d)), L, [0, 5, 9], nkv, hd, 1e4, eps=0.0)
+    np.testing.assert_allclose(np.mean(k * k, axis=-1), 4.0, rtol=1e-12)
+
+
+def test_k_only_and_v_only_fills_keep_the_other_cache():
+    d, nkv, hd = 8, 2, 4
+    kc = np.full((1, 1, nkv, 4, hd), -3.0)
+    vc = np.full((1, 1, nkv, 4, hd), -5.0)
+    h = RNG.standard_normal((2, d))
+    for w, k_written, v_written in (("k", True, False), ("v", False, True), (1, True, False), (2, False, True),
+                                    (None, True, True)):
+        L = _layer(d, nkv * hd, cache_layer=0)
+        L["writes"] = w
+        k2, v2 = oracle.kv_fill(h, [L], kc, vc, nkv, hd, 1e4, 1e-5)
+        assert bool(np.any(k2 != -3.0)) == k_written
+        assert bool(np.any(v2 != -5.0)) == v_written
+
+
 # ------------------------------------------------------------------ ridge
 
 def test_ridge_with_orthonormal_columns():

@@ -27,6 +27,8 @@ class GateDesc(ctypes.Structure):
 
 
 TEE_FILL_EARLY_WEIGHTS = 1
+TEE_FILL_WRITE_K = 1
+TEE_FILL_WRITE_V = 2
 
 
 class FillDesc(ctypes.Structure):
@@ -37,7 +39,8 @@ class FillDesc(ctypes.Structure):
 class FillLayer(ctypes.Structure):
     _fields_ = [("w_map", c_void_p), ("gamma", c_void_p), ("wk", c_void_p), ("wv", c_void_p),
                 ("k_scale", c_void_p), ("k_zero", c_void_p), ("v_scale", c_void_p), ("v_zero", c_void_p),
-                ("cache_layer", c_int32), ("reserved", c_int32)]
+                ("cache_layer", c_int32), ("writes", c_int32),
+                ("k_bias", c_void_p), ("v_bias", c_void_p), ("k_norm", c_void_p)]
 
 
 class CacheLayout(ctypes.Structure):

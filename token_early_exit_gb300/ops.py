@@ -248,7 +248,9 @@ class KVFill:
     ``layers`` holds one dict per filled layer with CUDA tensors ``gamma``,
     ``wk``, ``wv`` (dense [d][kvw] or packed int4 [d/2][kvw]), optionally
     ``w_map`` [d][d] and, for int4, ``k_scale``, ``k_zero``, ``v_scale``,
-    ``v_zero`` [d/group][kvw] fp16, plus the int ``cache_layer``.
+    ``v_zero`` [d/group][kvw] fp16, plus the int ``cache_layer``. Model-family
+    variants: ``k_bias``, ``v_bias`` [kvw] and ``k_norm`` [head_dim] tensors, and
+    ``writes`` = "k" or "v" to fill only one of the caches.
     """
 
     def __init__(self, layers: Sequence[Dict], *, d: int, n_kv_heads: int, head_dim: int, rope_base: float,
@@ -273,6 +275,8 @@ class KVFill:
             arr[i].k_scale, arr[i].k_zero = p("k_scale"), p("k_zero")
             arr[i].v_scale, arr[i].v_zero = p("v_scale"), p("v_zero")
             arr[i].cache_layer = int(L["cache_layer"])
+            arr[i].k_bias, arr[i].v_bias, arr[i].k_norm = p("k_bias"), p("v_bias"), p("k_norm")
+            arr[i].writes = {None: 0, "kv": 0, "k": _lib.TEE_FILL_WRITE_K, "v": _lib.TEE_FILL_WRITE_V}[L.get("writes")]
             dev = L["gamma"].device
         self.layers = arr
         self.n_layers = len(layers)
