@@ -13,6 +13,11 @@ SCORE_TOL = 1e-4
 NEAR_BAND = 1e-3
 KV_MAX_ABS = 2e-2
 KV_REL_L2 = 1e-2
+# RMS of K and V at which KV_MAX_ABS holds (projection weights N(0, 0.25/d)): the
+# fill's roundings are relative errors, so for larger values (a per-head K norm
+# gives K an RMS near its norm weight, a bias adds to both) the bound grows with
+# the reference's RMS.
+KV_REF_RMS = 0.5
 
 
 def f64(t) -> np.ndarray:
@@ -52,7 +57,9 @@ def check_kv(gpu, ref, what="kv"):
     diff = np.abs(g - ref)
     mx = diff.max(initial=0.0)
     rel = np.linalg.norm((g - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-30)
-    assert mx <= KV_MAX_ABS and rel <= KV_REL_L2, f"{what}: max-abs {mx:.3e}, rel-L2 {rel:.3e}"
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    lim = KV_MAX_ABS * max(1.0, rms / KV_REF_RMS)
+    assert mx <= lim and rel <= KV_REL_L2, f"{what}: max-abs {mx:.3e} (bound {lim:.3e}), rel-L2 {rel:.3e}"
     return mx, rel
 
 
@@ -63,7 +70,7 @@ def check_decode_fill(cfg, x, rows, pos, seq, sentinel):
     h = f64(x["h_cur"])
     layers = host(x["layers"])
     k_all, v_all = x["k_cache"], x["v_cache"]
-    written = torch.zeros(k_all.shape[:4], dtype=torch.bool, device=k_all.device)
+    written = {c: torch.zeros(k_all.shape[:4], dtype=torch.bool, device=k_all.device) for c in "kv"}
     dev = k_all.device
     for L in layers:
         if len(rows) == 0:
@@ -73,8 +80,9 @@ def check_decode_fill(cfg, x, rows, pos, seq, sentinel):
         j = L["cache_layer"]
         idx_s = torch.as_tensor(seq[rows], device=dev).long()
         idx_p = torch.as_tensor(pos[rows], device=dev).long()
-        check_kv(k_all[j, idx_s, :, idx_p], k_ref, f"K layer {j}")
-        check_kv(v_all[j, idx_s, :, idx_p], v_ref, f"V layer {j}")
-        written[j, idx_s, :, idx_p] = True
-    for c in (k_all, v_all):
-        assert bool((c[~written] == sentinel).all())
+        for c, cache, ref in (("k", k_all, k_ref), ("v", v_all, v_ref)):
+            if L.get("writes") in (None, "kv", c):   # a K-only / V-only layer leaves the other cache
+                check_kv(cache[j, idx_s, :, idx_p], ref, f"{c.upper()} layer {j}")
+                written[c][j, idx_s, :, idx_p] = True
+    for c, cache in (("k", k_all), ("v", v_all)):
+        assert bool((cache[~written[c]] == sentinel).all())

@@ -188,44 +188,73 @@ generic_rms_kernel(int n_max, const int32_t* __restrict__ n_dev, int d, float ep
     if (lane == 0) rowscale[m] = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
 }
 
-// RoPE on K and the store of K and V into the backbone's slots.
+// Bias, the optional per-head K norm, RoPE on K, and the store of K and V into
+// the backbone's slots: a warp per (item, kv head), lanes over the rotation pairs.
 template <typename T>
 __global__ void __launch_bounds__(256)
 generic_rope_store_kernel(int n_max, const int32_t* __restrict__ n_dev, int n_kv, int hd, const float* __restrict__ kv,
                           int h_rows, const int32_t* __restrict__ rows, const int32_t* __restrict__ pos, int pos0,
                           const int32_t* __restrict__ seq, const PrepHeader* __restrict__ hdr,
                           const float2* __restrict__ rope, T* __restrict__ kc, T* __restrict__ vc,
-                          tee_cache_layout cl, int layer, void* ws) {
+                          tee_cache_layout cl, int layer, const T* __restrict__ kb, const T* __restrict__ vb,
+                          const T* __restrict__ kn, float eps, int writes, void* ws) {
     const int n = item_count(n_max, n_dev);
     const int half = hd / 2, kvw = n_kv * hd;
-    const int64_t total = static_cast<int64_t>(n) * n_kv * half;
-    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int m = static_cast<int>(idx / (n_kv * half));
-        const int rem = static_cast<int>(idx % (n_kv * half));
-        const int h = rem / half, i = rem % half;
+    const int lane = threadIdx.x & 31;
+    const bool write_k = writes != TEE_FILL_WRITE_V, write_v = writes != TEE_FILL_WRITE_K;
+    const int64_t total = static_cast<int64_t>(n) * n_kv;
+    for (int64_t w = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; w < total;
+         w += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+        const int m = static_cast<int>(w / n_kv), h = static_cast<int>(w % n_kv);
         const int r = rows ? rows[m] : m;
         if (r < 0 || r >= h_rows) continue;  // recorded by the GEMM's row check
         const int p = pos ? pos[r] : pos0 + r;
         const int s = seq ? seq[r] : 0;
         if (!pos_ok(p, cl.max_pos, hdr)) {
-            if (h == 0 && i == 0) record_fault(ws, TEE_DEVERR_POS, p);
+            if (h == 0 && lane == 0) record_fault(ws, TEE_DEVERR_POS, p);
             continue;
         }
         if (s < 0 || s >= cl.n_seq) {
-            if (h == 0 && i == 0) record_fault(ws, TEE_DEVERR_SEQ, s);
+            if (h == 0 && lane == 0) record_fault(ws, TEE_DEVERR_SEQ, s);
             continue;
         }
         const float* row = kv + static_cast<int64_t>(m) * 2 * kvw;
-        const float k1 = row[h * hd + i], k2 = row[h * hd + i + half];
-        const float v1 = row[kvw + h * hd + i], v2 = row[kvw + h * hd + i + half];
-        const float2 cs = rope[static_cast<int64_t>(p) * half + i];
-        const float c = cs.x, sn = cs.y;
         const int64_t off = layer * cl.s_layer + s * cl.s_seq + h * cl.s_head + static_cast<int64_t>(p) * cl.s_pos;
-        kc[off + i] = from_f32<T>(k1 * c - k2 * sn);
-        kc[off + i + half] = from_f32<T>(k2 * c + k1 * sn);
-        vc[off + i] = from_f32<T>(v1);
-        vc[off + i + half] = from_f32<T>(v2);
+        // K: bias, then the head's RMS (when normalised) over all hd values
+        float krs = 1.f;
+        if (kn) {
+            float ss = 0.f;
+            for (int i = lane; i < hd; i += 32) {
+                const float k = row[h * hd + i] + (kb ? to_f32(kb[h * hd + i]) : 0.f);
+                ss = fmaf(k, k, ss);
+            }
+            krs = 1.0f / sqrtf(warp_sum(ss) / static_cast<float>(hd) + eps);
+        }
+        for (int i = lane; i < half; i += 32) {
+            if (write_k) {
+                float k1 = row[h * hd + i], k2 = row[h * hd + i + half];
+                if (kb) {
+                    k1 += to_f32(kb[h * hd + i]);
+                    k2 += to_f32(kb[h * hd + i + half]);
+                }
+                if (kn) {
+                    k1 *= krs * to_f32(kn[i]);
+                    k2 *= krs * to_f32(kn[i + half]);
+                }
+                const float2 cs = rope[static_cast<int64_t>(p) * half + i];
+                kc[off + i] = from_f32<T>(k1 * cs.x - k2 * cs.y);
+                kc[off + i + half] = from_f32<T>(k2 * cs.x + k1 * cs.y);
+            }
+            if (write_v) {
+                float v1 = row[kvw + h * hd + i], v2 = row[kvw + h * hd + i + half];
+                if (vb) {
+                    v1 += to_f32(vb[h * hd + i]);
+                    v2 += to_f32(vb[h * hd + i + half]);
+                }
+                vc[off + i] = from_f32<T>(v1);
+                vc[off + i + half] = from_f32<T>(v2);
+            }
+        }
     }
 }
 
@@ -262,13 +291,15 @@ tee_status run_generic(const FillCall& fc) {
                                                                    2 * kvw, fc.ws);
         st = launch_status();
         if (st != TEE_OK) return st;
-        const int64_t total = static_cast<int64_t>(fc.n_max) * kvw / 2;
-        int blocks = static_cast<int>((total + 255) / 256);
+        const int64_t warps = static_cast<int64_t>(fc.n_max) * D.n_kv_heads;
+        int blocks = static_cast<int>((warps + 7) / 8);
         if (blocks > 4 * 1024) blocks = 4 * 1024;
         if (blocks < 1) blocks = 1;
         generic_rope_store_kernel<T><<<blocks, 256, 0, fc.stream>>>(
             fc.n_max, fc.n_dev, D.n_kv_heads, D.head_dim, KV, fc.h_rows, fc.rows, fc.pos, fc.pos0, fc.seq, pv.hdr, pv.rope,
-            static_cast<T*>(fc.k_cache), static_cast<T*>(fc.v_cache), *fc.cache, L.cache_layer, fc.ws);
+            static_cast<T*>(fc.k_cache), static_cast<T*>(fc.v_cache), *fc.cache, L.cache_layer,
+            static_cast<const T*>(L.k_bias), static_cast<const T*>(L.v_bias), static_cast<const T*>(L.k_norm), D.eps,
+            L.writes, fc.ws);
         st = launch_status();
         if (st != TEE_OK) return st;
     }
@@ -373,6 +404,9 @@ extern "C" tee_status tee_kv_fill(const tee_fill_desc* D, int32_t n_layers, cons
         if (!L.gamma || !L.wk || !L.wv || L.cache_layer < 0 || L.cache_layer >= cache->n_layers)
             return TEE_ERR_INVALID_ARG;
         if (D->wfmt == TEE_W_INT4 && (!L.k_scale || !L.k_zero || !L.v_scale || !L.v_zero)) return TEE_ERR_INVALID_ARG;
+        if (L.writes != 0 && L.writes != TEE_FILL_WRITE_K && L.writes != TEE_FILL_WRITE_V) return TEE_ERR_INVALID_ARG;
+        if ((L.k_bias && !aligned16(L.k_bias)) || (L.v_bias && !aligned16(L.v_bias)) || (L.k_norm && !aligned16(L.k_norm)))
+            return TEE_ERR_INVALID_ARG;
     }
     FillCall fc{D, n_layers, layers, prep, prep_bytes, n_max, n_dev, h_split, ld_h, h_rows, rows, pos, pos0, seq,
                 k_cache, v_cache, cache, ws, ws_bytes, static_cast<cudaStream_t>(stream)};

@@ -91,7 +91,10 @@ struct DecodeLayer {
     const __half* scale[2];
     const __half* zero[2];
     const bf16* gamma;
+    const bf16* bias[2];   // k_bias, v_bias (nullable)
+    const bf16* k_norm;    // per-head K norm weight (nullable)
     int cache_layer;
+    int writes;            // 0, TEE_FILL_WRITE_K or TEE_FILL_WRITE_V
 };
 constexpr int MAX_DECODE_LAYERS = 64;
 struct DecodeArgs {
@@ -182,6 +185,46 @@ __device__ __forceinline__ float ld_l2_f32(const float* p) {
     return v;
 }
 
+__device__ __forceinline__ void load8_bf16(const bf16* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    unpack_bf16x2(u.x, v[0], v[1]);
+    unpack_bf16x2(u.y, v[2], v[3]);
+    unpack_bf16x2(u.z, v[4], v[5]);
+    unpack_bf16x2(u.w, v[6], v[7]);
+}
+
+// One thread's 8 low and 8 high output columns (columns col, col + half of the
+// projection): the partial accumulators of the ks split CTAs summed, times the
+// row's 1/rms, plus the bias.
+__device__ __forceinline__ void sum_partials(const float4 (&pv)[4][4], int ks, float rs, const bf16* bias, int col,
+                                             int half, float (&lo)[8], float (&hi)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) lo[e] = hi[e] = 0.f;
+#pragma unroll
+    for (int src = 0; src < 4; ++src) {
+        if (src >= ks) continue;
+        const float4 l0 = pv[src][0], l1 = pv[src][1], h0 = pv[src][2], h1 = pv[src][3];
+        lo[0] += l0.x; lo[1] += l0.y; lo[2] += l0.z; lo[3] += l0.w;
+        lo[4] += l1.x; lo[5] += l1.y; lo[6] += l1.z; lo[7] += l1.w;
+        hi[0] += h0.x; hi[1] += h0.y; hi[2] += h0.z; hi[3] += h0.w;
+        hi[4] += h1.x; hi[5] += h1.y; hi[6] += h1.z; hi[7] += h1.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        lo[e] *= rs;
+        hi[e] *= rs;
+    }
+    if (bias) {
+        float b[8];
+        load8_bf16(bias + col, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) lo[e] += b[e];
+        load8_bf16(bias + col + half, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) hi[e] += b[e];
+    }
+}
+
 // First column of unit u's low and high halves within the K (or V) projection.
 __device__ __forceinline__ int unit_col_lo(int gk, int u, int hd) {
     const int uph = hd / 64;   // units per head
@@ -213,13 +256,16 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     const bool is_k = gq < a.groups_kv;
     const int kv = is_k ? 0 : 1;
     const int gk = is_k ? gq : gq - a.groups_kv;
+    // A K-only or V-only layer: the other kind's clusters leave before any shared state.
+    if (L.writes == (is_k ? TEE_FILL_WRITE_V : TEE_FILL_WRITE_K)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kc = a.d / ks, k0 = rank * kc;     // this CTA's k range
     const int nkb = kc / D_KB, nch = kc / D_CH;
     // The item count (and everything else a previous kernel may produce) is read only
     // after wait_prior_grid(): with an early launch the weights stream in before that.
     int n = 0;
-    const bool reporter = blockIdx.x == 0 && li == 0;   // one CTA records bad rows / positions
+    // one CTA (the first that runs for layer 0) records bad rows / positions
+    const bool reporter = li == 0 && blockIdx.x == (a.l[0].writes == TEE_FILL_WRITE_V ? a.groups_kv * ks : 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < D_RA; ++s) {
@@ -491,6 +537,8 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
     if (warp < D_DEQ_WARPS && acc_ok && !*abort) {
         const int t = threadIdx.x, q = t & 3;
         const int upr = D_UNITS / ks;   // units finished per CTA
+        const bf16* bias = L.bias[kv];
+        const bool knorm = is_k && L.k_norm;
         for (int i = t >> 2; i < n; i += D_DEQ_THREADS / 4) {
             const int64_t ioff = s_ioff[i];
             if (ioff < 0) continue;
@@ -526,31 +574,66 @@ fill_decode_kernel(const __grid_constant__ DecodeArgs a, void* ws) {
                 }
                 const float rs = 1.0f / sqrtf((ssv[0] + ssv[1] + ssv[2] + ssv[3]) * a.inv_d + a.eps);
                 float lo[8], hi[8];
+                sum_partials(pv, ks, rs, bias, head * a.hd + seg_off + 8 * q, a.half, lo, hi);
+                if (knorm) {
+                    // the head's RMS: this unit's 64 columns over the item's four
+                    // threads, plus (head_dim 128) the partner unit's, summed the same way
+                    float hss = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) lo[e] = hi[e] = 0.f;
+                    for (int e = 0; e < 8; ++e) hss = fmaf(lo[e], lo[e], fmaf(hi[e], hi[e], hss));
+                    if (a.hd == 128) {
+                        // the partner unit's totals, one split at a time (registers)
+                        float4 t4[4] = {};
+#pragma unroll 1
+                        for (int src = 0; src < ks; ++src) {
+                            const float4* row = part + static_cast<int64_t>((src * D_UNITS + (u ^ 1)) * 16) * a.n_max + i;
 #pragma unroll
-                for (int src = 0; src < 4; ++src) {
-                    const float4 l0 = pv[src][0], l1 = pv[src][1], h0 = pv[src][2], h1 = pv[src][3];
-                    lo[0] += l0.x; lo[1] += l0.y; lo[2] += l0.z; lo[3] += l0.w;
-                    lo[4] += l1.x; lo[5] += l1.y; lo[6] += l1.z; lo[7] += l1.w;
-                    hi[0] += h0.x; hi[1] += h0.y; hi[2] += h0.z; hi[3] += h0.w;
-                    hi[4] += h1.x; hi[5] += h1.y; hi[6] += h1.z; hi[7] += h1.w;
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 v = ld_l2_f4(row + static_cast<int64_t>((e >> 1) * 8 + 2 * q + (e & 1)) * a.n_max);
+                                t4[e].x += v.x;
+                                t4[e].y += v.y;
+                                t4[e].z += v.z;
+                                t4[e].w += v.w;
+                            }
+                        }
+                        float lo2[8] = {t4[0].x, t4[0].y, t4[0].z, t4[0].w, t4[1].x, t4[1].y, t4[1].z, t4[1].w};
+                        float hi2[8] = {t4[2].x, t4[2].y, t4[2].z, t4[2].w, t4[3].x, t4[3].y, t4[3].z, t4[3].w};
+                        float b[8] = {};
+                        const int col2 = head * a.hd + (32 - seg_off) + 8 * q;
+                        if (bias) load8_bf16(bias + col2, b);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float x = fmaf(lo2[e], rs, b[e]);
+                            hss = fmaf(x, x, hss);
+                        }
+                        if (bias) load8_bf16(bias + col2 + a.half, b);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float x = fmaf(hi2[e], rs, b[e]);
+                            hss = fmaf(x, x, hss);
+                        }
+                    }
+                    const unsigned quad = 0xFu << (threadIdx.x & 28);
+                    hss += __shfl_xor_sync(quad, hss, 1);
+                    hss += __shfl_xor_sync(quad, hss, 2);
+                    const float hs = 1.0f / sqrtf(hss / static_cast<float>(a.hd) + a.eps);
+                    float g[8];
+                    load8_bf16(L.k_norm + seg_off + 8 * q, g);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) lo[e] *= hs * g[e];
+                    load8_bf16(L.k_norm + a.half + seg_off + 8 * q, g);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) hi[e] *= hs * g[e];
                 }
                 if (is_k) {
 #pragma unroll
                     for (int e2 = 0; e2 < 4; ++e2) {
-                        const float x1 = lo[2 * e2] * rs, x2 = hi[2 * e2] * rs;
-                        const float y1 = lo[2 * e2 + 1] * rs, y2 = hi[2 * e2 + 1] * rs;
+                        const float x1 = lo[2 * e2], x2 = hi[2 * e2];
+                        const float y1 = lo[2 * e2 + 1], y2 = hi[2 * e2 + 1];
                         lo[2 * e2] = x1 * c2[e2].x - x2 * c2[e2].y;
                         hi[2 * e2] = x2 * c2[e2].x + x1 * c2[e2].y;
                         lo[2 * e2 + 1] = y1 * c2[e2].z - y2 * c2[e2].w;
                         hi[2 * e2 + 1] = y2 * c2[e2].z + y1 * c2[e2].w;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        lo[e] *= rs;
-                        hi[e] *= rs;
                     }
                 }
                 bf16* dst = (is_k ? a.kc : a.vc) + ioff + static_cast<int64_t>(head) * a.cl.s_head + seg_off + 8 * q;
@@ -702,7 +785,9 @@ tee_status fill_decode_run(const FillCall& fc) {
         a.l[l] = DecodeLayer{{static_cast<const uint8_t*>(L.wk), static_cast<const uint8_t*>(L.wv)},
                              {static_cast<const __half*>(L.k_scale), static_cast<const __half*>(L.v_scale)},
                              {static_cast<const __half*>(L.k_zero), static_cast<const __half*>(L.v_zero)},
-                             static_cast<const bf16*>(L.gamma), L.cache_layer};
+                             static_cast<const bf16*>(L.gamma),
+                             {static_cast<const bf16*>(L.k_bias), static_cast<const bf16*>(L.v_bias)},
+                             static_cast<const bf16*>(L.k_norm), L.cache_layer, L.writes};
     }
     const int splits = 2 * a.groups_kv * fc.n_layers;   // (group, layer) pairs
     a.ks = choose_ks(D.d, splits, mc4, mc2);

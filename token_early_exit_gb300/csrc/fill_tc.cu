@@ -106,6 +106,12 @@ struct EpiArgs {
     bf16* vc;
     tee_cache_layout cl;
     int layer, kvw, hd, half, h_rows;
+    // the GEMM's column 0 is output column col_off of [K|V] (kvw for a V-only layer);
+    // per-layer bias of K and V and per-head K norm weight (all nullable)
+    int col_off;
+    const bf16* kb;
+    const bf16* vb;
+    const bf16* kn;
     // fp32 output (the ridge fit's Gram matrices): C, its row stride, and a value
     // added where row == column
     float* c32;
@@ -156,7 +162,20 @@ __device__ __forceinline__ void epi_f32(const EpiArgs& ep, int row, int n, int c
     }
 }
 
-// K/V epilogue: 1/rms row scale, RoPE on K heads, store into the cache slot.
+__device__ __forceinline__ void load32_bf16(const bf16* src, float (&v)[32]) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 u = s4[q];
+        unpack_bf16x2(u.x, v[8 * q + 0], v[8 * q + 1]);
+        unpack_bf16x2(u.y, v[8 * q + 2], v[8 * q + 3]);
+        unpack_bf16x2(u.z, v[8 * q + 4], v[8 * q + 5]);
+        unpack_bf16x2(u.w, v[8 * q + 6], v[8 * q + 7]);
+    }
+}
+
+// K/V epilogue: 1/rms row scale, bias, the per-head K norm, RoPE on K heads,
+// store into the cache slot.
 __device__ __forceinline__ void epi_kv(const EpiArgs& ep, int row, int n, int c0, uint32_t t_base, void* ws) {
     bool ok = row < n;
     float r = 0.f;
@@ -178,33 +197,72 @@ __device__ __forceinline__ void epi_kv(const EpiArgs& ep, int row, int n, int c0
             }
         }
     }
-    const bool is_k = c0 < ep.kvw;
-    const int col0 = is_k ? c0 : c0 - ep.kvw;
+    const int cg = c0 + ep.col_off;
+    const bool is_k = cg < ep.kvw;
+    const int col0 = is_k ? cg : cg - ep.kvw;
     bf16* cache = is_k ? ep.kc : ep.vc;
+    const bf16* bias = is_k ? ep.kb : ep.vb;
+    const bool knorm = is_k && ep.kn;
     const int64_t base = ep.layer * ep.cl.s_layer + s * ep.cl.s_seq + static_cast<int64_t>(p) * ep.cl.s_pos;
     const float2* cs = ep.rope + static_cast<int64_t>(p) * ep.half;
 #pragma unroll 1
     for (int hb = 0; hb < BN; hb += ep.hd) {
         bf16* dst = cache + base + static_cast<int64_t>((col0 + hb) / ep.hd) * ep.cl.s_head;
+        const bf16* bh = bias ? bias + col0 + hb : nullptr;
+        // QK-norm: a first pass over the head for the RMS of r * acc + bias
+        float hs = 1.f;
+        if (knorm) {
+            float ss = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < ep.hd; c += 32) {
+                float v[32], b[32];
+                tc::tmem_ld32(t_base + hb + c, v);
+                if (bh) load32_bf16(bh + c, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float a = bh ? fmaf(v[j], r, b[j]) : v[j] * r;
+                    ss = fmaf(a, a, ss);
+                }
+            }
+            hs = 1.0f / sqrtf(ss / static_cast<float>(ep.hd) + ep.eps);
+        }
 #pragma unroll 1
         for (int c = 0; c < ep.half; c += 32) {
             float lo[32], hi[32];
             tc::tmem_ld32(t_base + hb + c, lo);
             tc::tmem_ld32(t_base + hb + ep.half + c, hi);
             if (!ok) continue;
-            if (is_k) {
+            if (bh) {
+                float b[32];
+                load32_bf16(bh + c, b);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float2 e = cs[c + j];
-                    const float a = lo[j] * r, b = hi[j] * r;
-                    lo[j] = a * e.x - b * e.y;
-                    hi[j] = b * e.x + a * e.y;
-                }
+                for (int j = 0; j < 32; ++j) lo[j] = fmaf(lo[j], r, b[j]);
+                load32_bf16(bh + ep.half + c, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) hi[j] = fmaf(hi[j], r, b[j]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     lo[j] *= r;
                     hi[j] *= r;
+                }
+            }
+            if (knorm) {
+                float g[32];
+                load32_bf16(ep.kn + c, g);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) lo[j] *= hs * g[j];
+                load32_bf16(ep.kn + ep.half + c, g);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) hi[j] *= hs * g[j];
+            }
+            if (is_k) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float2 e = cs[c + j];
+                    const float a = lo[j], b = hi[j];
+                    lo[j] = a * e.x - b * e.y;
+                    hi[j] = b * e.x + a * e.y;
                 }
             }
             store32_bf16(dst + c, lo);
@@ -600,11 +658,18 @@ tee_status fill_tc_run(const FillCall& fc) {
             st = launch_status();
             if (st != TEE_OK) return st;
         }
-        st = make_tmap_bf16(&tm_b, wkv_t, d, 2 * kvw, static_cast<uint64_t>(d) * 2, BK, BN);
+        // a K-only or V-only layer multiplies by its half of [Wk|Wv] alone
+        const int n_cols = L.writes ? kvw : 2 * kvw;
+        ep.col_off = L.writes == TEE_FILL_WRITE_V ? kvw : 0;
+        st = make_tmap_bf16(&tm_b, wkv_t + static_cast<size_t>(ep.col_off) * d, d, n_cols,
+                            static_cast<uint64_t>(d) * 2, BK, BN);
         if (st != TEE_OK) return st;
         ep.sumsq_in = sumsq;
         ep.layer = L.cache_layer;
-        st = launch_gemm<EPI_KV>(*a2, tm_b, n_max, fc.n_dev, 2 * kvw, d, ep, fc.ws, fc.stream);
+        ep.kb = static_cast<const bf16*>(L.k_bias);
+        ep.vb = static_cast<const bf16*>(L.v_bias);
+        ep.kn = static_cast<const bf16*>(L.k_norm);
+        st = launch_gemm<EPI_KV>(*a2, tm_b, n_max, fc.n_dev, n_cols, d, ep, fc.ws, fc.stream);
         if (st != TEE_OK) return st;
     }
     return TEE_OK;
