@@ -4,7 +4,9 @@ A plain, slow, obviously correct float64 restatement of what the three source
 pages define: River-LLM's state-transition cosine gate, TIDE's RMSNorm router
 gate and its compaction / exit scatter, and RidgeFill's KV fill (per-layer
 linear map, that layer's own RMSNorm and K/V projection, RoPE on K, store into
-the backbone's cache slot). Inputs stored in bf16/fp16/fp32 are widened to
+the backbone's cache slot), and River-LLM's Exit River (the W4A16 copies of
+the remaining decoder layers: attention over the shared cache and the FFN).
+Inputs stored in bf16/fp16/fp32 are widened to
 float64 exactly; nothing is rounded on the way except where a page fixes a
 precision (the exit decision, taken in fp32 like the kernels the TIDE notes
 describe).
@@ -22,3 +24,4 @@ from .gate import (cosine_similarity, cosine_gate, router_probability, router_ga
 from .compact import stable_partition, gather_rows, exit_scatter  # noqa: F401
 from .fill import dequant_int4, rms_norm, rope_rotate_half, fill_rows, kv_fill  # noqa: F401
 from .ridge import ridge_fit  # noqa: F401
+from .river import silu, attention, exit_layer, exit_river  # noqa: F401

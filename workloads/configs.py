@@ -86,6 +86,45 @@ class PrefillFillConfig:
         return self.tokens - self.exact_tail
 
 
+@dataclass(frozen=True)
+class RiverConfig:
+    """The Exit River of one decode step: the exited tokens through the W4A16
+    copies of layers river_layers (River-LLM)."""
+    name: str
+    d: int
+    n_layers: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    d_ff: int
+    batch: int                 # exited tokens, one per sequence
+    cache_len: int
+    river_layers: Tuple[int, ...]
+    rope_base: float
+    group: int = 64
+    eps: float = 1e-5
+
+    @property
+    def kvw(self) -> int:
+        return self.n_kv_heads * self.head_dim
+
+    @property
+    def qw(self) -> int:
+        return self.n_q_heads * self.head_dim
+
+
+# Tiny Exit River: two layers of a d=256 model, 8 tokens, 128 cache positions.
+TINY_RIVER = RiverConfig(
+    name="tiny-river", d=256, n_layers=4, n_q_heads=4, n_kv_heads=2, head_dim=64, d_ff=512,
+    batch=8, cache_len=128, river_layers=(2, 3), rope_base=1.0e4)
+
+# Llama-3.2-1B-shaped Exit River: 64 tokens that exited after layer 8 run the
+# W4A16 copies of layers 9-16 (0-based 8-15), 4096 cache positions.
+LLAMA1B_RIVER = RiverConfig(
+    name="llama3.2-1b-exit-river-w4a16", d=2048, n_layers=16, n_q_heads=32, n_kv_heads=8, head_dim=64,
+    d_ff=8192, batch=64, cache_len=4096, river_layers=tuple(range(8, 16)), rope_base=5.0e5)
+
+
 # Tiny fp32 decode step: exit after 1-based layer 2, fill 1-based layers 3-4.
 TINY_DECODE = DecodeConfig(
     name="tiny-fp32-decode", d=256, n_layers=4, n_q_heads=4, n_kv_heads=2,
@@ -118,4 +157,4 @@ PREFILL_120K = PrefillFillConfig(
     head_dim=128, rope_base=1.0e6, split=32, tokens=122880, exact_tail=4096)
 
 ALL = {c.name: c for c in (TINY_DECODE, LLAMA1B_DECODE, ROUTER_4096,
-                           PREFILL_16K, PREFILL_120K)}
+                           PREFILL_16K, PREFILL_120K, TINY_RIVER, LLAMA1B_RIVER)}

@@ -21,7 +21,9 @@ Distributions (the pages give none; these are the readings used):
   * int4 Wk, Wv: codes q ~ U{0..15}, fp16 zero z = 7.5 + U(-0.5, 0.5) and fp16
     scale s = sqrt(0.25/d)/sqrt(21.25) * (1 + 0.1*N(0, 1)) per group of 64
     input rows, which gives the dequantised weights about the dense spread;
-  * router weights ~ N(0, 0.02^2), gamma = 1, no biases.
+  * router weights ~ N(0, 0.02^2), gamma = 1, no biases;
+  * Exit River layers: every weight int4 as above (spread sqrt(0.25/d_in)),
+    norm weights 1 + 0.1*N(0, 1); cache history K, V ~ N(0, 0.5^2).
 """
 from __future__ import annotations
 
@@ -31,7 +33,7 @@ from typing import Dict, List, Optional
 
 import torch
 
-from .configs import DecodeConfig, PrefillFillConfig, RouterConfig
+from .configs import DecodeConfig, PrefillFillConfig, RiverConfig, RouterConfig
 
 _DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
@@ -167,4 +169,30 @@ def prefill_inputs(cfg: PrefillFillConfig, seed: int = 0, device="cpu", rows: Op
         shape = (len(fill), 1, cfg.n_kv_heads, cfg.tokens, cfg.head_dim)
         out["k_cache"] = torch.full(shape, CACHE_SENTINEL, dtype=dt, device=device)
         out["v_cache"] = torch.full(shape, CACHE_SENTINEL, dtype=dt, device=device)
+    return out
+
+
+def river_inputs(cfg: RiverConfig, seed: int = 0, device="cpu", with_cache: bool = True,
+                 dtype=torch.bfloat16) -> Dict[str, object]:
+    """Inputs of one Exit River pass: the exited tokens' hidden states, their
+    positions and sequences, the W4A16 layers, and caches whose history
+    (every slot) holds random values that the attention reads."""
+    n, d, f = cfg.batch, cfg.d, cfg.d_ff
+    h = normal((n, d), 1.0, seed, "h_exit", device, dtype)
+    pos = randint((n,), 0, cfg.cache_len, seed, "pos", device)
+    layers: List[Dict[str, object]] = []
+    for j in cfg.river_layers:
+        L: Dict[str, object] = {"cache_layer": j}
+        L["attn_norm"] = normal((d,), 0.1, seed, f"an{j}", device, dtype, mean=1.0)
+        L["ffn_norm"] = normal((d,), 0.1, seed, f"fn{j}", device, dtype, mean=1.0)
+        for m, (k_in, n_out) in {"q": (d, cfg.qw), "k": (d, cfg.kvw), "v": (d, cfg.kvw), "o": (cfg.qw, d),
+                                 "g": (d, f), "u": (d, f), "d": (f, d)}.items():
+            w = int4_weight(k_in, n_out, cfg.group, seed, f"w{m}{j}", device)
+            L[f"w{m}"], L[f"{m}_scale"], L[f"{m}_zero"] = w["packed"], w["scale"], w["zero"]
+        layers.append(L)
+    out = {"h": h, "pos": pos, "seq": torch.arange(n, dtype=torch.int32, device=device), "layers": layers}
+    if with_cache:
+        shape = (cfg.n_layers, n, cfg.n_kv_heads, cfg.cache_len, cfg.head_dim)
+        out["k_cache"] = normal(shape, 0.5, seed, "k_hist", device, dtype)
+        out["v_cache"] = normal(shape, 0.5, seed, "v_hist", device, dtype)
     return out
