@@ -417,6 +417,89 @@ TEE_API tee_status tee_ridge_fit(int32_t n, int32_t d, int32_t d_out, const void
                                  const void* y, int64_t ld_y, int32_t dtype, float lambda,
                                  float* w, int64_t ld_w, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------ Exit River (next) */
+
+/* One int4 weight matrix W [k_in][n_out] in the fill's W4A16 format: codes
+ * [k_in/2][n_out] u8 (two per byte along k, even k in the low nibble), f16
+ * scale and zero [k_in/group][n_out]; W = (q - zero) * scale. */
+typedef struct {
+    const void* codes;
+    const void* scale;
+    const void* zero;
+} tee_w4;
+
+typedef struct {
+    int32_t d;            /* hidden size (multiple of 128) */
+    int32_t n_q_heads;    /* query heads (a multiple of n_kv_heads) */
+    int32_t n_kv_heads;   /* KV heads */
+    int32_t head_dim;     /* 64 or 128 */
+    int32_t d_ff;         /* FFN width (multiple of 64) */
+    float rope_base;      /* RoPE base (q and k) */
+    float eps;            /* epsilon of both RMSNorms */
+    int32_t group;        /* int4 group length: 64 */
+    int32_t flags;        /* 0 */
+} tee_river_desc;
+
+/* One exit layer: the W4A16 copy of decoder layer `cache_layer` (device
+ * pointers). qw = n_q_heads*head_dim, kvw = n_kv_heads*head_dim. */
+typedef struct {
+    const void* attn_norm;  /* [d] bf16: RMSNorm weight before attention */
+    const void* ffn_norm;   /* [d] bf16: RMSNorm weight before the FFN */
+    tee_w4 wq;              /* [d][qw] */
+    tee_w4 wk;              /* [d][kvw] */
+    tee_w4 wv;              /* [d][kvw] */
+    tee_w4 wo;              /* [qw][d] */
+    tee_w4 wg;              /* [d][d_ff] gate */
+    tee_w4 wu;              /* [d][d_ff] up */
+    tee_w4 wd;              /* [d_ff][d] down */
+    int32_t cache_layer;    /* layer index into the caches */
+    int32_t reserved;       /* 0 */
+} tee_river_layer;
+
+/* Size of `prep` (the RoPE table for positions [0, max_pos)). */
+TEE_API size_t tee_exit_river_prep_size(const tee_river_desc* desc, int32_t max_pos);
+TEE_API tee_status tee_exit_river_prepare(const tee_river_desc* desc, int32_t max_pos, void* prep,
+                                          size_t prep_bytes, void* stream);
+/* Workspace of a call with up to n_max items over caches of cache->max_pos
+ * positions. */
+TEE_API size_t tee_exit_river_workspace_size(const tee_river_desc* desc, int32_t n_max, int32_t max_pos);
+
+/*
+ * River-LLM's Exit River (core method; method steps 1 and 3): the tokens that
+ * left the backbone continue through the W4A16 copies of the remaining
+ * layers, each of which writes the skipped layer's K/V into the backbone's
+ * own slots and passes its output to the next; the last output goes to the
+ * LM head. Per exit layer, for every item:
+ *   x = RMSNorm(h) * attn_norm;  q, k, v = x Wq, x Wk, x Wv;
+ *   RoPE (rotate-half, as tee_kv_fill) on every head of q and k at the item's
+ *   position; k, v stored at (cache_layer, seq, head, pos) -- every item's
+ *   before any attention of the layer;
+ *   o_h = softmax(q_h . K^T / sqrt(head_dim)) . V over positions 0..pos of the
+ *   item's sequence, q head h reading kv head h / (n_q_heads / n_kv_heads);
+ *   h1 = h + o . Wo;  x2 = RMSNorm(h1) * ffn_norm;
+ *   h <- h1 + (SiLU(x2 Wg) * (x2 Wu)) . Wd.
+ * The residual stream stays in fp32 between layers; contractions take bf16
+ * operands (int4 weights dequantised to bf16) and accumulate in fp32.
+ *
+ * Items: n = *n_dev if n_dev is given, else n_max (n_max <= 128). Item i uses
+ *   row r = rows ? rows[i] : i of h (r < h_rows), position pos[r] and
+ *   sequence seq ? seq[r] : 0, and writes h_out[i] (item order, ready for
+ *   tee_exit_scatter). An item with a bad row, position or sequence is
+ *   recorded (TEE_DEVERR_ROW / POS / SEQ) and skipped: no cache write, and
+ *   h_out[i] is left as it was.
+ *
+ *   layers     host array of n_layers exit layers, in order
+ *   prep       prepared by tee_exit_river_prepare (RoPE table)
+ *   h          [h_rows][ld_h] bf16;  h_out [n_max][ld_out] bf16
+ *   k_cache, v_cache  bf16 caches laid out as `cache` says
+ */
+TEE_API tee_status tee_exit_river(const tee_river_desc* desc, int32_t n_layers, const tee_river_layer* layers,
+                                  const void* prep, size_t prep_bytes, int32_t n_max, const int32_t* n_dev,
+                                  const void* h, int64_t ld_h, int32_t h_rows, const int32_t* rows,
+                                  const int32_t* pos, const int32_t* seq,
+                                  void* k_cache, void* v_cache, const tee_cache_layout* cache,
+                                  void* h_out, int64_t ld_out, void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

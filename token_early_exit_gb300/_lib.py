@@ -48,6 +48,20 @@ class CacheLayout(ctypes.Structure):
                 ("n_layers", c_int32), ("n_seq", c_int32), ("n_heads", c_int32), ("max_pos", c_int32)]
 
 
+class W4(ctypes.Structure):
+    _fields_ = [("codes", c_void_p), ("scale", c_void_p), ("zero", c_void_p)]
+
+
+class RiverDesc(ctypes.Structure):
+    _fields_ = [("d", c_int32), ("n_q_heads", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32),
+                ("d_ff", c_int32), ("rope_base", c_float), ("eps", c_float), ("group", c_int32), ("flags", c_int32)]
+
+
+class RiverLayer(ctypes.Structure):
+    _fields_ = [("attn_norm", c_void_p), ("ffn_norm", c_void_p), ("wq", W4), ("wk", W4), ("wv", W4), ("wo", W4),
+                ("wg", W4), ("wu", W4), ("wd", W4), ("cache_layer", c_int32), ("reserved", c_int32)]
+
+
 _P = c_void_p
 SIGNATURES = {
     "tee_version": (c_char_p, []),
@@ -75,6 +89,12 @@ SIGNATURES = {
     "tee_ridge_fit_workspace_size": (c_size_t, [c_int32, c_int32, c_int32]),
     "tee_ridge_fit": (c_int, [c_int32, c_int32, c_int32, _P, c_int64, _P, c_int64, c_int32, c_float, _P, c_int64, _P,
                               c_size_t, _P]),
+    "tee_exit_river_prep_size": (c_size_t, [POINTER(RiverDesc), c_int32]),
+    "tee_exit_river_prepare": (c_int, [POINTER(RiverDesc), c_int32, _P, c_size_t, _P]),
+    "tee_exit_river_workspace_size": (c_size_t, [POINTER(RiverDesc), c_int32, c_int32]),
+    "tee_exit_river": (c_int, [POINTER(RiverDesc), c_int32, POINTER(RiverLayer), _P, c_size_t, c_int32, _P, _P,
+                               c_int64, c_int32, _P, _P, _P, _P, _P, POINTER(CacheLayout), _P, c_int64, _P,
+                               c_size_t, _P]),
     "tee_exit_scatter_workspace_size": (c_size_t, [c_int32]),
     "tee_exit_scatter": (c_int, [c_int32, _P, _P, _P, _P, c_int64, _P, c_int64, c_int64, c_int32, c_int32, _P,
                                  c_float, _P, c_size_t, _P]),

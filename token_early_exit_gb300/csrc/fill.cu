@@ -319,6 +319,15 @@ GenericWs generic_ws(const tee_fill_desc& D, int n_max) {
     return w;
 }
 
+tee_status build_rope_table(float2* table, int max_pos, int half, double base, cudaStream_t s) {
+    const int64_t total = static_cast<int64_t>(max_pos) * half;
+    int blocks = static_cast<int>((total + 255) / 256);
+    if (blocks > 8192) blocks = 8192;
+    if (blocks < 1) blocks = 1;
+    rope_table_kernel<<<blocks, 256, 0, s>>>(max_pos, half, base, table);
+    return launch_status();
+}
+
 }  // namespace tee
 
 using namespace tee;
@@ -358,13 +367,7 @@ extern "C" tee_status tee_kv_fill_prepare(const tee_fill_desc* D, int32_t n_laye
     st = cuda_status(cudaMemcpyAsync(prep, &h, sizeof(h), cudaMemcpyHostToDevice, s));
     if (st != TEE_OK) return st;
     const PrepView pv = prep_view(prep, *D, n_layers);
-    const int half = D->head_dim / 2;
-    const int64_t total = static_cast<int64_t>(max_pos) * half;
-    int blocks = static_cast<int>((total + 255) / 256);
-    if (blocks > 8192) blocks = 8192;
-    rope_table_kernel<<<blocks, 256, 0, s>>>(max_pos, half, static_cast<double>(D->rope_base),
-                                             const_cast<float2*>(pv.rope));
-    st = launch_status();
+    st = build_rope_table(const_cast<float2*>(pv.rope), max_pos, D->head_dim / 2, D->rope_base, s);
     if (st != TEE_OK) return st;
     return fill_tc_prepare(*D, n_layers, layers, const_cast<char*>(pv.tc), s);
 }

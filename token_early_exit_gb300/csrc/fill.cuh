@@ -58,6 +58,9 @@ inline PrepView prep_view(const void* prep, const tee_fill_desc& D, int n_layers
     return v;
 }
 
+// {cos, sin} of pos * base^(-2i/(2 half)) for pos < max_pos, i < half, computed in float64.
+tee_status build_rope_table(float2* table, int max_pos, int half, double base, cudaStream_t s);
+
 // Position check shared by every store: 0 <= p < min(cache max_pos, table length).
 __device__ __forceinline__ bool pos_ok(int p, int cache_max, const PrepHeader* hdr) {
     return p >= 0 && p < cache_max && p < hdr->max_pos;

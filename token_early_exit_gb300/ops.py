@@ -341,3 +341,74 @@ def ridge_fit(x: torch.Tensor, y: torch.Tensor, lam: float, *, ws: Optional[Work
                            w.stride(0), wp, wn, _stream(x.device))
     check("tee_ridge_fit", st)
     return w
+
+
+class ExitRiver:
+    """Prepared Exit River: the W4A16 copies of the layers an exited token
+    still runs (River-LLM), for a fixed set of layers and cache length.
+
+    ``layers`` holds one dict per exit layer, in order: bf16 CUDA tensors
+    ``attn_norm``, ``ffn_norm`` [d]; for each of q k v o g u d the packed int4
+    codes ``w{m}`` [k_in/2][n_out] u8 and fp16 ``{m}_scale``, ``{m}_zero``
+    [k_in/64][n_out]; and the int ``cache_layer``.
+    """
+
+    def __init__(self, layers: Sequence[Dict], *, d: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                 d_ff: int, rope_base: float, eps: float, max_pos: int, group: int = 64):
+        self.lib = load()
+        self.desc = _lib.RiverDesc(d=d, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=head_dim, d_ff=d_ff,
+                                   rope_base=float(rope_base), eps=float(eps), group=group, flags=0)
+        self.keep: List[torch.Tensor] = []
+        arr = (_lib.RiverLayer * max(1, len(layers)))()
+
+        def p(L, k):
+            t = _vec(L[k], k)
+            self.keep.append(t)
+            return t.data_ptr()
+
+        dev = None
+        for i, L in enumerate(layers):
+            arr[i].attn_norm, arr[i].ffn_norm = p(L, "attn_norm"), p(L, "ffn_norm")
+            for m in "qkvougd":
+                w = getattr(arr[i], f"w{m}")
+                w.codes, w.scale, w.zero = p(L, f"w{m}"), p(L, f"{m}_scale"), p(L, f"{m}_zero")
+            arr[i].cache_layer = int(L["cache_layer"])
+            dev = L["attn_norm"].device
+        self.layers = arr
+        self.n_layers = len(layers)
+        self.max_pos = int(max_pos)
+        self.device = dev or torch.device("cuda")
+        nbytes = self.lib.tee_exit_river_prep_size(ctypes.byref(self.desc), self.max_pos)
+        if nbytes == 0:
+            raise ValueError("invalid Exit River descriptor")
+        self.prep = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        check("tee_exit_river_prepare", self.lib.tee_exit_river_prepare(ctypes.byref(self.desc), self.max_pos,
+                                                                        _ptr(self.prep), nbytes, _stream(self.device)))
+
+    def workspace_bytes(self, n_max: int, max_pos: Optional[int] = None) -> int:
+        return self.lib.tee_exit_river_workspace_size(ctypes.byref(self.desc), int(n_max),
+                                                      int(max_pos or self.max_pos))
+
+    def __call__(self, h: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pos: torch.Tensor, *,
+                 seq: Optional[torch.Tensor] = None, rows: Optional[torch.Tensor] = None,
+                 n_dev: Optional[torch.Tensor] = None, n_max: Optional[int] = None,
+                 out: Optional[torch.Tensor] = None, ws: Optional[Workspace] = None) -> torch.Tensor:
+        """Runs the items through every exit layer; returns h_out [n_max][d] (bf16)."""
+        _mat(h, "h")
+        if k_cache.stride() != v_cache.stride() or k_cache.shape != v_cache.shape:
+            raise ValueError("k_cache and v_cache must share one layout")
+        layout = cache_layout(k_cache)
+        if n_max is None:
+            n_max = rows.numel() if rows is not None else h.shape[0]
+        if out is None:
+            out = torch.empty(int(n_max), h.shape[1], dtype=h.dtype, device=h.device)
+        _mat(out, "out")
+        ws = ws or Workspace(h.device)
+        wp, wn = ws.get(self.workspace_bytes(n_max, layout.max_pos))
+        st = self.lib.tee_exit_river(ctypes.byref(self.desc), self.n_layers, self.layers, _ptr(self.prep),
+                                     self.prep.numel(), int(n_max), _ptr(_vec(n_dev, "n_dev")), _ptr(h), h.stride(0),
+                                     h.shape[0], _ptr(_vec(rows, "rows")), _ptr(_vec(pos, "pos")),
+                                     _ptr(_vec(seq, "seq")), _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
+                                     _ptr(out), out.stride(0), wp, wn, _stream(h.device))
+        check("tee_exit_river", st)
+        return out
