@@ -12,7 +12,10 @@ A step is one pass of the whole hot path over one batch of synthetic input:
   router-65536: the same at 65,536 tokens (inputs far larger than L2), with the
       cosine gate and the exit scatter at that batch timed alongside;
   prefill-16k / prefill-120k: the RidgeFill KV fill of every layer after the
-      split for all filled rows.
+      split for all filled rows;
+  river-1b / river-tiny: River-LLM's Exit River -- 64 exited tokens through the
+      W4A16 copies of 8 Llama-3.2-1B-shaped layers (attention over a 4096-slot
+      cache, FFN), one call.
 L2 is flushed (a write larger than L2) between timed steps, outside the timed
 events, except where every input is larger than L2 (router-65536). Under torchrun each rank runs its own replica (independent batches,
 no collective on the data path: weak scaling); rank 0 prints one JSON line.
@@ -44,7 +47,8 @@ sys.path.insert(0, ROOT)
 from workloads import configs, gen  # noqa: E402
 
 METRIC = "tokens/s through exit gate+compact+KV fill"
-WORKLOADS = ("decode-1b", "decode-tiny", "router-4096", "router-65536", "prefill-16k", "prefill-120k")
+WORKLOADS = ("decode-1b", "decode-tiny", "router-4096", "router-65536", "prefill-16k", "prefill-120k", "river-1b",
+             "river-tiny")
 
 
 def peaks():
@@ -379,7 +383,100 @@ class Prefill:
         return run, f"fill of 16 evenly spaced rows across all {len(layers)} layers (per-row time extrapolated)"
 
 
+class River:
+    """The Exit River: the exited tokens through the W4A16 copies of the
+    remaining layers (attention over the shared cache + FFN), one call."""
+
+    def __init__(self, tee, cfg, dev, seed=0, rows=None, layers=None):
+        import dataclasses
+        if rows or layers:   # a reduced case (profiling)
+            cfg = dataclasses.replace(cfg, batch=rows or cfg.batch,
+                                      river_layers=cfg.river_layers[:layers] if layers else cfg.river_layers,
+                                      name=f"{cfg.name}-reduced-{rows or cfg.batch}tokens-{layers or len(cfg.river_layers)}layers")
+        self.tee, self.cfg, self.dev = tee, cfg, dev
+        self.x = gen.river_inputs(cfg, seed, dev)
+        self.ws = tee.Workspace(dev)
+        self.river = tee.ExitRiver(self.x["layers"], d=cfg.d, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
+                                   head_dim=cfg.head_dim, d_ff=cfg.d_ff, rope_base=cfg.rope_base, eps=cfg.eps,
+                                   max_pos=cfg.cache_len)
+        self.out = torch.empty(cfg.batch, cfg.d, dtype=torch.bfloat16, device=dev)
+        self.units = cfg.batch
+        self.kernel = "exit_river (all launches of the call)"
+        self.metric = "tokens/s through the Exit River (W4A16 exit layers)"
+        self.traffic_key = None
+        self.bound = "hbm"
+        L = len(cfg.river_layers)
+        d, f, qw, kvw, g = cfg.d, cfg.d_ff, cfg.qw, cfg.kvw, cfg.group
+        mats = [(d, qw), (d, kvw), (d, kvw), (qw, d), (d, f), (d, f), (f, d)]
+        w_layer = sum(k * n // 2 + 2 * (k // g) * n * 2 for k, n in mats) + 2 * d * 2
+        pos = self.x["pos"].cpu().numpy().astype(np.int64)
+        kv_read = int((pos + 1).sum()) * kvw * 2 * 2         # K and V rows 0..pos of every item
+        kv_write = cfg.batch * kvw * 2 * 2
+        self._bytes = L * (w_layer + kv_read + kv_write) + 2 * cfg.batch * d * 2
+
+    def fill_bytes(self, n_exit):
+        return self._bytes
+
+    def parts(self):
+        x = self.x
+
+        def river():
+            self.river(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"], out=self.out, ws=self.ws)
+        return [river], 0
+
+    def step(self):
+        for f in self.parts()[0]:
+            f()
+
+    def host_io(self):
+        x = self.x
+        self.h_in = {k: x[k].cpu().pin_memory() for k in ("h", "pos", "seq")}
+        self.h_out = {"out": torch.empty_like(self.out, device="cpu").pin_memory()}
+        return (sum(t.numel() * t.element_size() for t in self.h_in.values()),
+                sum(t.numel() * t.element_size() for t in self.h_out.values()))
+
+    def e2e_step(self):
+        for k, t in self.h_in.items():
+            self.x[k].copy_(t, non_blocking=True)
+        self.step()
+        self.h_out["out"].copy_(self.out, non_blocking=True)
+
+    def n_exit(self):
+        return self.cfg.batch
+
+    def config(self):
+        c = self.cfg
+        return {"workload": c.name, "tokens_per_step": c.batch, "d": c.d, "river_layers": len(c.river_layers),
+                "q_heads": c.n_q_heads, "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "d_ff": c.d_ff,
+                "cache_len": c.cache_len, "positions": "U[0, cache_len) per sequence",
+                "weights": "int4 group-64 (W4A16), every matrix", "algorithmic_bytes_per_step": self._bytes,
+                "l2": "inputs larger than L2 (the KV cache read); flushed between timed steps"}
+
+    def oracle_sample(self):
+        from oracle import river
+        from tests.parity import host
+        cfg, x = self.cfg, self.x
+        L = host(x["layers"][0])
+        L["cache_layer"] = 0
+        p = int(x["pos"][0].item())
+        kc = host(x["k_cache"][cfg.river_layers[0]:cfg.river_layers[0] + 1, :1, :, :p + 1])
+        vc = host(x["v_cache"][cfg.river_layers[0]:cfg.river_layers[0] + 1, :1, :, :p + 1])
+        h = host(x["h"][:1])
+        frac = 1.0 / len(cfg.river_layers)
+
+        def run():
+            river.exit_layer(h, L, [p], [0], kc, vc, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.rope_base,
+                             cfg.eps, cfg.group)
+            return frac
+        return run, (f"one token through one of the {len(cfg.river_layers)} exit layers "
+                     f"(position {p}; counted as 1/{len(cfg.river_layers)} token)")
+
+
 def make(name, tee, dev, seed, rows=None, layers=None):
+    if name == "river-1b":
+        return River(tee, configs.LLAMA1B_RIVER, dev, seed, rows, layers)
+    if name == "river-tiny":
+        return River(tee, configs.TINY_RIVER, dev, seed, rows, layers)
     if name == "decode-1b":
         return Decode(tee, configs.LLAMA1B_DECODE, dev, seed)
     if name == "decode-tiny":
@@ -502,7 +599,7 @@ def run_reference(args):
         units += run()
     el = time.perf_counter() - t0
     v = units / el
-    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
+    line = {"metric": getattr(w, "metric", METRIC), "value": v, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": w.config(),
@@ -637,7 +734,7 @@ def run_gpu(args):
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
                "seconds": round(el, 2)}
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+    line = {"metric": getattr(w, "metric", METRIC), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.config().get("workload") != configs.TINY_DECODE.name else "f32",
             "data": "synthetic", "config": w.config(), "exits_per_step": n_exit,

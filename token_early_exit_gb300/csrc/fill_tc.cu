@@ -58,6 +58,20 @@ tee_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, ui
     return r == CUDA_SUCCESS ? TEE_OK : TEE_ERR_INVALID_ARG;
 }
 
+tee_status make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_rows) {
+    if (!encoder_ready()) return TEE_ERR_UNSUPPORTED;
+    if (inner == 0 || rows == 0) return TEE_ERR_INVALID_ARG;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TEE_OK : TEE_ERR_INVALID_ARG;
+}
+
 // A K-major bf16 matrix [rows][n_kb * 64] seen as n_kb blocks of 64 columns: one
 // box brings box_kb consecutive blocks of box_rows rows, each block landing as its
 // own 128-byte-swizzled [box_rows][64] tile (block stride 128 bytes in the source).

@@ -43,27 +43,37 @@ constexpr uint32_t RIVER_MAGIC = 0x54455256u;  // "TERV"
 
 // ------------------------------------------------------------------ workspace
 struct RiverWs {
-    size_t resid, abuf, qbuf, obuf, act, ss_a, ss_f, ipos, iseq, gcnt, acnt, part, apart, end;
+    size_t resid, abuf, qbuf, obuf, act, ss_a, ss_f, ipos, iseq, gcnt, acnt, apart, end;
 };
 
 constexpr int GT_N = 128;        // output columns per GEMM tile
 constexpr int GT_K = 64;         // inputs per k block
-constexpr int G_THREADS = 256;
-constexpr int G_CS = 8;          // code / scale ring depth (blocks)
-constexpr int G_AS = 4;          // A ring depth
-constexpr uint32_t G_A_BYTES = 128 * GT_K * 2;       // 16 KB: 128 rows x 64 bf16
+constexpr int G_DQ_WARPS = 8;    // dequantising warps (then the epilogue)
+constexpr int G_PROD_WARP = 8;   // issues the TMA / bulk copies
+constexpr int G_MMA_WARP = 9;    // issues the MMAs, owns TMEM
+constexpr int G_THREADS = 320;
+constexpr int G_EPI_THREADS = G_DQ_WARPS * 32;
+constexpr int G_S = 6;           // stages of A + codes + scales/zeros
+constexpr int G_RB = 3;          // dequantised B buffers
+constexpr int G_A_ROWS = 128;    // A tile rows (TMEM lanes); A buffers hold 128 rows
+constexpr uint32_t G_A_BYTES = G_A_ROWS * GT_K * 2;  // 16 KB: 128 rows x 64 bf16, 128-byte swizzle
 constexpr uint32_t G_B_BYTES = GT_N * GT_K * 2;      // 16 KB
 constexpr uint32_t G_C_BYTES = 32 * GT_N;            // 4 KB: 32 packed rows x 128 columns
 constexpr uint32_t G_SZ_BYTES = 2 * GT_N * 2;        // 512 B: scales, zeros
+constexpr uint32_t G_STAGE_TX = G_A_BYTES + G_C_BYTES + G_SZ_BYTES;
 constexpr uint32_t G_OFF_A = 0;
-constexpr uint32_t G_OFF_B = G_OFF_A + G_AS * G_A_BYTES;
-constexpr uint32_t G_OFF_C = G_OFF_B + 2 * G_B_BYTES;
-constexpr uint32_t G_OFF_SZ = G_OFF_C + G_CS * G_C_BYTES;
-constexpr uint32_t G_OFF_BAR = G_OFF_SZ + G_CS * G_SZ_BYTES;
-constexpr size_t G_SMEM = 1024 + G_OFF_BAR + 64;
+constexpr uint32_t G_OFF_B = G_OFF_A + G_S * G_A_BYTES;
+constexpr uint32_t G_OFF_C = G_OFF_B + G_RB * G_B_BYTES;
+constexpr uint32_t G_OFF_SZ = G_OFF_C + G_S * G_C_BYTES;
+constexpr uint32_t G_OFF_BAR = G_OFF_SZ + G_S * G_SZ_BYTES;
+constexpr size_t G_SMEM = 1024 + G_OFF_BAR + (2 * G_S + 2 * G_RB + 1) * 8 + 16;
+// the CTA's partial tile after the loop: [128 rows][GT_N + 4] fp32, over the A ring
+constexpr int G_P_PITCH = GT_N + 4;
+static_assert(G_A_ROWS * G_P_PITCH * 4 <= G_S * G_A_BYTES, "partial tile fits the A ring");
 static_assert(G_OFF_B % 1024 == 0 && G_OFF_C % 16 == 0 && G_OFF_BAR % 8 == 0, "alignment");
+static_assert(G_SMEM <= 232448, "shared memory");
 
-constexpr int MAX_KS = 16;
+constexpr int MAX_KS = 8;        // K splits = CTAs of a cluster (portable size)
 constexpr int MAX_ITEMS = 128;
 
 int max_tiles(const tee_river_desc& D) {
@@ -75,25 +85,18 @@ int max_tiles(const tee_river_desc& D) {
 
 int at_chunk(int hd) { return hd == 64 ? 256 : 128; }
 
-// K splits: the largest power of two that keeps tiles * ks within the SMs and
-// leaves each split at least two 64-input blocks.
+int max_clusters(int ks);
+
+// K splits (the CTAs of one cluster): the largest power of two that keeps every
+// cluster resident at once, tiles * ks within the SMs, and each split at least
+// two 64-input blocks.
 int choose_ks(int tiles, int K) {
     const int sms = sm_count();
     int ks = 1;
-    while (ks * 2 <= MAX_KS && tiles * ks * 2 <= sms && K % (ks * 2 * GT_K) == 0 && K / (ks * 2) >= 2 * GT_K)
+    while (ks * 2 <= MAX_KS && tiles * ks * 2 <= sms && K % (ks * 2 * GT_K) == 0 && K / (ks * 2) >= 2 * GT_K &&
+           tiles <= max_clusters(ks * 2))
         ks *= 2;
     return ks;
-}
-
-// Largest ks * N of the layer's four GEMMs (the split-K partials).
-size_t part_cols(const tee_river_desc& D) {
-    const size_t qw = static_cast<size_t>(D.n_q_heads) * D.head_dim, kvw = static_cast<size_t>(D.n_kv_heads) * D.head_dim;
-    const size_t nq = qw + 2 * kvw, nf = 2 * static_cast<size_t>(D.d_ff);
-    size_t m = nq * choose_ks(static_cast<int>(nq / GT_N), D.d);
-    m = std::max(m, static_cast<size_t>(D.d) * choose_ks(D.d / GT_N, static_cast<int>(qw)));
-    m = std::max(m, nf * choose_ks(static_cast<int>(nf / GT_N), D.d));
-    m = std::max(m, static_cast<size_t>(D.d) * choose_ks(D.d / GT_N, D.d_ff));
-    return m;
 }
 
 RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
@@ -109,17 +112,17 @@ RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
         return at;
     };
     w.resid = take(n * d * 4);
-    w.abuf = take(n * d * 2);
+    const size_t na = G_A_ROWS;   // the GEMMs' A operands: 128 rows, the TMA box
+    w.abuf = take(na * d * 2);
     w.qbuf = take(n * qw * 2);
-    w.obuf = take(n * qw * 2);
-    w.act = take(n * f * 2);
+    w.obuf = take(na * qw * 2);
+    w.act = take(na * f * 2);
     w.ss_a = take(n * 4);
     w.ss_f = take(n * 4);
     w.ipos = take(n * 4);
     w.iseq = take(n * 4);
     w.gcnt = take(static_cast<size_t>(max_tiles(D)) * 4);
     w.acnt = take(n * D.n_kv_heads * 4);
-    w.part = take(n * part_cols(D) * 4);
     w.apart = take(n * D.n_kv_heads * chunks * rep * (D.head_dim + 2) * 4);
     w.end = o;
     return w;
@@ -224,14 +227,14 @@ struct W4Seg {
 };
 
 struct GemmArgs {
+    CUtensorMap tm_a;       // A [128][K] bf16, box 128 x 64, 128-byte swizzle
+    CUtensorMap tm_c[3];    // codes of each segment, box 32 x 128 (GU: 32 x 64 of gate and up)
     W4Seg seg[3];
     int n_seg, K, N, ks;
     int n_max;
     const int32_t* n_dev;
-    const bf16* a;          // [n][lda]
+    const bf16* a;          // [128][lda]
     int64_t lda;
-    float* part;            // [ks][n_max][N]
-    int32_t* cnt;           // [tiles]
     float* ss_zero;         // cleared by CTA (0, 0): the next producer accumulates into it
     // row scale of the normalised input: rs = 1 / sqrt(ss_in / width + eps)
     const float* ss_in;
@@ -268,6 +271,11 @@ __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(tc::smem_u32(dst)), "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+                 : "memory");
+}
 
 // Column c (0..127) of tile t -> (segment, column within it).
 template <int MODE>
@@ -290,200 +298,270 @@ __device__ __forceinline__ float row_scale(const GemmArgs& g, int m) {
     return g.ss_in ? 1.0f / sqrtf(g.ss_in[m] * g.inv_width + g.eps) : 1.f;
 }
 
-// Split-K partial sum of (item m, tile column c), in split order.
-__device__ __forceinline__ float part_sum(const GemmArgs& g, int m, int col) {
-    float v = 0.f;
-    for (int s = 0; s < g.ks; ++s) v += __ldcg(g.part + (static_cast<int64_t>(s) * g.n_max + m) * g.N + col);
-    return v;
+__device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d) {
+    return make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
 }
 
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Sum over the cluster's ks partial tiles of (row m, columns col .. col + 3), in
+// rank order; every CTA's load is issued before the first add.
+__device__ __forceinline__ float4 tile_sum4(const float* P, int ks, int m, int col) {
+    const uint32_t laddr = tc::smem_u32(P + m * G_P_PITCH + col);
+    if (ks == 1) return *reinterpret_cast<const float4*>(P + m * G_P_PITCH + col);
+    float4 v[MAX_KS];
+#pragma unroll
+    for (int r = 0; r < MAX_KS; ++r)
+        if (r < ks) {
+            uint32_t ra;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(laddr), "r"(r));
+            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v[r].x), "=f"(v[r].y), "=f"(v[r].z), "=f"(v[r].w)
+                         : "r"(ra)
+                         : "memory");
+        }
+    float4 a = v[0];
+#pragma unroll
+    for (int r = 1; r < MAX_KS; ++r)
+        if (r < ks) {
+            a.x += v[r].x;
+            a.y += v[r].y;
+            a.z += v[r].z;
+            a.w += v[r].w;
+        }
+    return a;
+}
+
+// The tile's epilogue for this CTA's share of it (groups [rank * gpr, (rank + 1) * gpr)
+// of four consecutive columns, pairs or units); a thread takes one group of one item.
 template <int MODE>
-__device__ void finish_tile(const GemmArgs& g, int t, int n, void* ws) {
+__device__ void finish_tile(const GemmArgs& g, const float* P, int t, int n, int rank) {
     const int tid = threadIdx.x;
     const int c0 = t * GT_N;
-    if (MODE == M_QKV) {
-        const int pairs = GT_N / 2;
-        for (int idx = tid; idx < n * pairs; idx += G_THREADS) {
-            const int m = idx / pairs, p = idx % pairs;
+    constexpr int G = MODE == M_QKV || MODE == M_GU ? 16 : 32;   // groups per tile
+    const int gpr = G / g.ks;
+    for (int idx = tid; idx < n * gpr; idx += G_EPI_THREADS) {
+        const int m = idx / gpr, grp = rank * gpr + idx % gpr;
+        if (MODE == M_QKV) {
+            const int p = 4 * grp;   // four pairs (i, i + half)
             const int ht = p / g.half, i = p % g.half;
-            const int lo = c0 + ht * g.hd + i, hi = lo + g.half;
+            const int lo = ht * g.hd + i, hi = lo + g.half;   // tile columns
             const int pm = g.ipos[m];
             if (pm < 0) continue;
             const float rs = row_scale(g, m);
-            float x1 = part_sum(g, m, lo) * rs, x2 = part_sum(g, m, hi) * rs;
-            const bool is_v = lo >= g.qw + g.kvw;
+            const float4 a = tile_sum4(P, g.ks, m, lo), b = tile_sum4(P, g.ks, m, hi);
+            float x1[4] = {a.x * rs, a.y * rs, a.z * rs, a.w * rs}, x2[4] = {b.x * rs, b.y * rs, b.z * rs, b.w * rs};
+            const int glo = c0 + lo;
+            const bool is_v = glo >= g.qw + g.kvw;
             if (!is_v) {
-                const float2 cs = g.rope[static_cast<int64_t>(pm) * g.half + i];
-                const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
-                x1 = y1;
-                x2 = y2;
+                const float4* cs = reinterpret_cast<const float4*>(g.rope + static_cast<int64_t>(pm) * g.half + i);
+                const float4 e01 = cs[0], e23 = cs[1];
+                const float c[4] = {e01.x, e01.z, e23.x, e23.z}, sn[4] = {e01.y, e01.w, e23.y, e23.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float y1 = x1[e] * c[e] - x2[e] * sn[e], y2 = x2[e] * c[e] + x1[e] * sn[e];
+                    x1[e] = y1;
+                    x2[e] = y2;
+                }
             }
-            if (lo < g.qw) {
-                bf16* q = g.qbuf + static_cast<int64_t>(m) * g.qw;
-                q[lo] = __float2bfloat16_rn(x1);
-                q[hi] = __float2bfloat16_rn(x2);
+            const uint2 plo = pack4_bf16(x1[0], x1[1], x1[2], x1[3]), phi = pack4_bf16(x2[0], x2[1], x2[2], x2[3]);
+            bf16* dst;
+            if (glo < g.qw) {
+                dst = g.qbuf + static_cast<int64_t>(m) * g.qw + glo;
             } else {
-                const int cc = is_v ? lo - g.qw - g.kvw : lo - g.qw;
-                const int head = cc / g.hd, e = cc % g.hd;
-                bf16* dst = (is_v ? g.vc : g.kc) + g.layer * g.cl.s_layer + g.iseq[m] * g.cl.s_seq +
-                            head * g.cl.s_head + static_cast<int64_t>(pm) * g.cl.s_pos + e;
-                dst[0] = __float2bfloat16_rn(x1);
-                dst[g.half] = __float2bfloat16_rn(x2);
+                const int cc = is_v ? glo - g.qw - g.kvw : glo - g.qw;
+                dst = (is_v ? g.vc : g.kc) + g.layer * g.cl.s_layer + g.iseq[m] * g.cl.s_seq +
+                      (cc / g.hd) * g.cl.s_head + static_cast<int64_t>(pm) * g.cl.s_pos + cc % g.hd;
             }
-        }
-    } else if (MODE == M_GU) {
-        for (int idx = tid; idx < n * 64; idx += G_THREADS) {
-            const int m = idx >> 6, u = idx & 63;
+            *reinterpret_cast<uint2*>(dst) = plo;
+            *reinterpret_cast<uint2*>(dst + g.half) = phi;
+        } else if (MODE == M_GU) {
+            const int u = 4 * grp;
             const float rs = row_scale(g, m);
-            const float gate = part_sum(g, m, c0 + u) * rs, up = part_sum(g, m, c0 + 64 + u) * rs;
-            const float a = gate / (1.0f + expf(-gate)) * up;
-            g.act[static_cast<int64_t>(m) * g.d_ff + 64 * t + u] = __float2bfloat16_rn(a);
-        }
-    } else {   // M_O, M_DOWN: residual update
-        for (int idx = tid; idx < n * GT_N; idx += G_THREADS) {
-            const int m = idx / GT_N, c = idx % GT_N;   // a warp: one item, 32 columns
-            const int col = c0 + c;
-            float* rp = g.resid + static_cast<int64_t>(m) * g.d + col;
-            const float v = *rp + part_sum(g, m, col);
+            const float4 ga = tile_sum4(P, g.ks, m, u), up = tile_sum4(P, g.ks, m, 64 + u);
+            const float gv[4] = {ga.x * rs, ga.y * rs, ga.z * rs, ga.w * rs};
+            const float uv[4] = {up.x * rs, up.y * rs, up.z * rs, up.w * rs};
+            float a[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] = gv[e] / (1.0f + expf(-gv[e])) * uv[e];
+            *reinterpret_cast<uint2*>(g.act + static_cast<int64_t>(m) * g.d_ff + 64 * t + u) =
+                pack4_bf16(a[0], a[1], a[2], a[3]);
+        } else {   // M_O, M_DOWN: residual update
+            const int lc = 4 * grp, col = c0 + lc;
+            float4* rp = reinterpret_cast<float4*>(g.resid + static_cast<int64_t>(m) * g.d + col);
+            const float4 sum = tile_sum4(P, g.ks, m, lc);
+            float4 v = *rp;
+            v.x += sum.x;
+            v.y += sum.y;
+            v.z += sum.z;
+            v.w += sum.w;
             *rp = v;
             if (g.h_out) {
-                if (g.ipos[m] >= 0) g.h_out[static_cast<int64_t>(m) * g.ld_out + col] = __float2bfloat16_rn(v);
+                if (g.ipos[m] >= 0)
+                    *reinterpret_cast<uint2*>(g.h_out + static_cast<int64_t>(m) * g.ld_out + col) =
+                        pack4_bf16(v.x, v.y, v.z, v.w);
             } else {
-                g.next_a[static_cast<int64_t>(m) * g.d + col] = __float2bfloat16_rn(v * __bfloat162float(g.next_gain[col]));
-                const float sq = warp_sum(v * v);
-                if ((threadIdx.x & 31) == 0) atomicAdd(g.ss_out + m, sq);
+                const uint2 gg = *reinterpret_cast<const uint2*>(g.next_gain + col);
+                float g0, g1, g2, g3;
+                unpack_bf16x2(gg.x, g0, g1);
+                unpack_bf16x2(gg.y, g2, g3);
+                *reinterpret_cast<uint2*>(g.next_a + static_cast<int64_t>(m) * g.d + col) =
+                    pack4_bf16(v.x * g0, v.y * g1, v.z * g2, v.w * g3);
+                // the item's gpr consecutive lanes (gpr a power of two <= 32) sum their squares
+                float sq = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                const int lane = tid & 31;
+                const unsigned seg = gpr >= 32 ? 0xFFFFFFFFu : ((1u << gpr) - 1u) << (lane & ~(gpr - 1));
+                for (int o = 1; o < gpr; o <<= 1) sq += __shfl_xor_sync(seg, sq, o);
+                if ((lane & (gpr - 1)) == 0) atomicAdd(g.ss_out + m, sq);
             }
         }
     }
-    (void)ws;
 }
 
+// One 128-column tile over a 1/ks slice of the inputs; the ks CTAs of a tile are a
+// cluster. Warp 8 streams A (TMA), the int4 codes (TMA) and scales/zeros (bulk)
+// into a G_S-stage ring; warps 0-7 dequantise each block into one of G_RB B
+// buffers; warp 9 issues the MMAs. Then every CTA stages its fp32 partial tile in
+// shared memory and, after a cluster barrier, finishes its share of the tile's
+// columns from the ks partials (DSMEM reads).
 template <int MODE>
 __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_constant__ GemmArgs g, void* ws) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + G_OFF_BAR);   // [2]
-    uint64_t* acc_bar = mma_bar + 2;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + G_OFF_BAR);   // [G_S]
+    uint64_t* empty = full + G_S;                                       // [G_S]
+    uint64_t* bfull = empty + G_S;                                      // [G_RB]
+    uint64_t* bempty = bfull + G_RB;                                    // [G_RB]
+    uint64_t* acc_bar = bempty + G_RB;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t = blockIdx.x, sp = blockIdx.y;
+    const int t = blockIdx.x, sp = blockIdx.y;   // sp: the CTA's rank in its cluster
     const int n = item_count(g.n_max, g.n_dev);
     if (g.ss_zero && t == 0 && sp == 0)
         for (int i = tid; i < g.n_max; i += G_THREADS) g.ss_zero[i] = 0.f;
-    if (n == 0) return;
+    if (n == 0) return;   // every CTA of the cluster leaves here
     const int kc = g.K / g.ks, k0 = sp * kc, nkb = kc / GT_K;
 
     if (tid == 0) {
-        tc::mbar_init(&mma_bar[0], 1);
-        tc::mbar_init(&mma_bar[1], 1);
+        for (int i = 0; i < G_S; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < G_RB; ++i) {
+            tc::mbar_init(&bfull[i], G_DQ_WARPS);
+            tc::mbar_init(&bempty[i], 1);
+        }
         tc::mbar_init(acc_bar, 1);
         *abort = 0;
         tc::fence_barrier_init();
     }
-    if (warp == 0) tc::tmem_alloc(tmem_slot, GT_N);
+    if (warp == G_MMA_WARP) tc::tmem_alloc(tmem_slot, GT_N);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // this thread's pieces of a block: one 16-byte code chunk (packed row tid / 8,
-    // columns 16 (tid % 8) ...), and for tid < 32 one scale / zero chunk
-    const int c_row = tid >> 3, c_chunk = tid & 7;
-    int c_seg, c_col;
-    tile_col<MODE>(g, t, c_chunk * 16, c_seg, c_col);
-    const uint8_t* c_src = g.seg[c_seg].codes + static_cast<int64_t>(k0 / 2 + c_row) * g.seg[c_seg].n + c_col;
-    const int64_t c_step = static_cast<int64_t>(GT_K / 2) * g.seg[c_seg].n;
-    int z_seg = 0, z_col = 0;
-    const bool z_thread = tid < 32;
-    if (z_thread) tile_col<MODE>(g, t, (tid & 15) * 8, z_seg, z_col);
-    const __half* z_src = (tid < 16 ? g.seg[z_seg].scale : g.seg[z_seg].zero) +
-                          static_cast<int64_t>(k0 / GT_K) * g.seg[z_seg].n + z_col;
-    const int64_t z_step = g.seg[z_seg].n;
-
-    auto load_codes = [&](int kb) {
-        if (kb >= nkb) return;
-        const int st = kb % G_CS;
-        cp_async16(smem + G_OFF_C + st * G_C_BYTES + c_row * GT_N + c_chunk * 16, c_src + kb * c_step);
-        if (z_thread) cp_async16(smem + G_OFF_SZ + st * G_SZ_BYTES + tid * 16, z_src + kb * z_step);
-    };
-    auto load_a = [&](int kb) {
-        if (kb >= nkb) return;
-        uint8_t* dst = smem + G_OFF_A + (kb % G_AS) * G_A_BYTES;
-        const bf16* src = g.a + k0 + kb * GT_K;
-        for (int c = tid; c < n * 8; c += G_THREADS) {
-            const int m = c >> 3, j = c & 7;
-            cp_async16(dst + m * 128 + ((j ^ (m & 7)) << 4), src + static_cast<int64_t>(m) * g.lda + 8 * j);
+    if (warp == G_PROD_WARP) {
+        // Block kb -> stage kb % G_S: the A tile (TMA, swizzled), the codes (TMA:
+        // one 32 x 128 box, or 32 x 64 of gate and of up) and the scale / zero rows
+        // (bulk copies), all completing on full[stage].
+        if (lane == 0) {
+            int seg0 = 0, col0 = 0;
+            tile_col<MODE>(g, t, 0, seg0, col0);
+            int kb = 0;
+            for (; kb < nkb; ++kb) {
+                const int st = kb % G_S;
+                if (kb >= G_S && !tc::mbar_wait(&empty[st], ((kb / G_S) - 1) & 1, abort, ws, 81)) break;
+                uint64_t* bar = &full[st];
+                tc::mbar_arrive_expect_tx(bar, G_STAGE_TX);
+                const int kg = k0 + kb * GT_K;
+                tc::tma_load_2d(smem + G_OFF_A + st * G_A_BYTES, &g.tm_a, kg, 0, bar);
+                uint8_t* cdst = smem + G_OFF_C + st * G_C_BYTES;
+                __half* zdst = reinterpret_cast<__half*>(smem + G_OFF_SZ + st * G_SZ_BYTES);
+                const int64_t grow = kg / GT_K;
+                if (MODE == M_GU) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        tc::tma_load_2d(cdst + h * (G_C_BYTES / 2), &g.tm_c[h], 64 * t, kg / 2, bar);
+                        const W4Seg& sg = g.seg[h];
+                        bulk_load(zdst + 64 * h, sg.scale + grow * sg.n + 64 * t, 128, bar);
+                        bulk_load(zdst + GT_N + 64 * h, sg.zero + grow * sg.n + 64 * t, 128, bar);
+                    }
+                } else {
+                    tc::tma_load_2d(cdst, &g.tm_c[seg0], col0, kg / 2, bar);
+                    const W4Seg& sg = g.seg[seg0];
+                    bulk_load(zdst, sg.scale + grow * sg.n + col0, 256, bar);
+                    bulk_load(zdst + GT_N, sg.zero + grow * sg.n + col0, 256, bar);
+                }
+            }
+            // stopped early: let the copies in flight land before the CTA moves on
+            const uint64_t t0 = tc::globaltimer();
+            for (int j = max(0, kb - G_S); j < kb; ++j)
+                while (!tc::mbar_test_wait(&full[j % G_S], (j / G_S) & 1) && tc::globaltimer() - t0 < 200000000ull) {
+                }
         }
-    };
-
-    // prologue: codes of blocks 0 .. CS-2 and A of block 0 (one group), A of block 1
-    for (int kb = 0; kb < G_CS - 1; ++kb) load_codes(kb);
-    load_a(0);
-    cp_commit();
-    load_a(1);
-    cp_commit();
-
-    const int dq_n = tid & 127, dq_h = tid >> 7;   // dequantiser: column, half of the k block
-    const uint32_t idesc = tc::idesc_bf16(128, GT_N);
-    bool ok = true;
-    for (int kb = 0; kb < nkb; ++kb) {
-        if (tid == 0 && kb >= 2) {
-            if (!tc::mbar_wait(&mma_bar[kb & 1], ((kb - 2) >> 1) & 1, abort, ws, 81)) *abort = 1;
+    } else if (warp == G_MMA_WARP) {
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_bf16(128, GT_N);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int st = kb % G_S, b = kb % G_RB;
+                if (!tc::mbar_wait(&full[st], (kb / G_S) & 1, abort, ws, 82)) break;
+                if (!tc::mbar_wait(&bfull[b], (kb / G_RB) & 1, abort, ws, 83)) break;
+                tc::tc_fence_after();
+                const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_A + st * G_A_BYTES));
+                const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_B + b * G_B_BYTES));
+#pragma unroll
+                for (int kk = 0; kk < GT_K / 16; ++kk) tc::umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, kb | kk);
+                tc::umma_commit(&bempty[b]);
+                tc::umma_commit(&empty[st]);
+            }
+            tc::umma_commit(acc_bar);   // every MMA issued has finished (also after a stop)
         }
-        __syncthreads();   // MMA kb-2 finished: its A stage and this B buffer are free
-        if (*abort) {
-            ok = false;
-            break;
-        }
-        load_codes(kb + G_CS - 1);
-        load_a(kb + 2);
-        cp_commit();
-        cp_wait<2>();      // block kb's codes and A have landed (this thread's copies)
-        fence_async_smem();
-        __syncthreads();
-        {
-            const uint8_t* cs = smem + G_OFF_C + (kb % G_CS) * G_C_BYTES;
-            const __half* sz = reinterpret_cast<const __half*>(smem + G_OFF_SZ + (kb % G_CS) * G_SZ_BYTES);
-            const float s = __half2float(sz[dq_n]);
-            const float zs = -__half2float(sz[GT_N + dq_n]) * s;
+    } else {
+        // dequantiser: column dq_n, half dq_h of each k block
+        const int dq_n = tid & 127, dq_h = tid >> 7;
+        // code byte (packed row r, column dq_n) of a stage: rows 128 bytes apart, or
+        // (GU) gate columns then up columns, each [32][64]
+        const int c_off = MODE == M_GU ? (dq_n >> 6) * (G_C_BYTES / 2) + (dq_n & 63) : dq_n;
+        const int c_pitch = MODE == M_GU ? 64 : GT_N;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int st = kb % G_S, b = kb % G_RB;
+            if (kb >= G_RB && !tc::mbar_wait(&bempty[b], ((kb / G_RB) - 1) & 1, abort, ws, 84)) break;
+            if (!tc::mbar_wait(&full[st], (kb / G_S) & 1, abort, ws, 85)) break;
+            const uint8_t* cs = smem + G_OFF_C + st * G_C_BYTES + c_off;
+            const __half* sz = reinterpret_cast<const __half*>(smem + G_OFF_SZ + st * G_SZ_BYTES);
+            const float sc = __half2float(sz[dq_n]);
+            const float zs = -__half2float(sz[GT_N + dq_n]) * sc;
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const uint32_t b = cs[(dq_h * 16 + i) * GT_N + dq_n];
-                w[i] = pack_bf16x2(fmaf(static_cast<float>(b & 15u), s, zs), fmaf(static_cast<float>(b >> 4), s, zs));
+                const uint32_t cb = cs[(dq_h * 16 + i) * c_pitch];
+                w[i] = pack_bf16x2(fmaf(static_cast<float>(cb & 15u), sc, zs), fmaf(static_cast<float>(cb >> 4), sc, zs));
             }
-            uint8_t* row = smem + G_OFF_B + (kb & 1) * G_B_BYTES + dq_n * 128;
+            uint8_t* row = smem + G_OFF_B + b * G_B_BYTES + dq_n * 128;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int jj = dq_h * 4 + q;
                 *reinterpret_cast<uint4*>(row + ((jj ^ (dq_n & 7)) << 4)) =
                     make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
-        }
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            tc::tc_fence_after();
-            const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_A + (kb % G_AS) * G_A_BYTES));
-            const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_B + (kb & 1) * G_B_BYTES));
-#pragma unroll
-            for (int kk = 0; kk < GT_K / 16; ++kk) tc::umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, kb | kk);
-            tc::umma_commit(&mma_bar[kb & 1]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bfull[b]);
         }
     }
-    if (tid == 0) {
-        tc::umma_commit(acc_bar);   // every MMA issued has finished (also after a stop)
-        if (!tc::mbar_wait(acc_bar, 0, abort, ws, 82)) *abort = 1;
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    // the accumulator is final
+    if (warp < G_DQ_WARPS && !tc::mbar_wait(acc_bar, 0, abort, ws, 86)) *abort = 1;
     __syncthreads();
-    ok = ok && !*abort;
+    const bool ok = !*abort;
     tc::tc_fence_after();
-    // partial tile -> workspace: warp w reads lanes 32 (w % 4).., columns 64 (w / 4)..
-    if (ok) {
+    // partial tile -> shared memory (over the A ring, idle now): warp w reads TMEM
+    // lanes 32 (w % 4).., columns 64 (w / 4)..
+    float* P = reinterpret_cast<float*>(smem + G_OFF_A);
+    if (ok && warp < G_DQ_WARPS) {
         const int m = (warp & 3) * 32 + lane;
         const int cb = (warp >> 2) * 64;
 #pragma unroll 1
@@ -491,27 +569,25 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
             float v[32];
             tc::tmem_ld32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + cb + c, v);
             if (m < n) {
-                float4* dst = reinterpret_cast<float4*>(g.part + (static_cast<int64_t>(sp) * g.n_max + m) * g.N +
-                                                        t * GT_N + cb + c);
+                float4* dst = reinterpret_cast<float4*>(P + m * G_P_PITCH + cb + c);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         }
     }
     tc::tc_fence_before();
-    __threadfence();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, GT_N);
-    if (!ok) return;
-    if (tid == 0) {
-        const int prev = atomicAdd(g.cnt + t, 1);
-        s_last = prev == g.ks - 1;
-        if (s_last) g.cnt[t] = 0;
+    if (warp == G_MMA_WARP) tc::tmem_dealloc(tmem, GT_N);
+    // every CTA of the cluster reaches both barriers (also after a stop)
+    if (g.ks > 1) {
+        cluster_arrive();
+        cluster_wait();
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    finish_tile<MODE>(g, t, n, ws);
+    if (ok && warp < G_DQ_WARPS) finish_tile<MODE>(g, P, t, n, sp);
+    if (g.ks > 1) {   // no CTA leaves while a peer may still read its partial tile
+        cluster_arrive();
+        cluster_wait();
+    }
 }
 
 // ------------------------------------------------------------------ attention
@@ -526,24 +602,48 @@ struct AttnArgs {
     const bf16* vc;
     tee_cache_layout cl;
     int layer;
+    int contig;            // s_pos == head_dim: a chunk of one head is one contiguous block
     float qscale;          // log2(e) / sqrt(head_dim)
     float* part;           // [n][n_kv][chunks][REP][HD + 2]
     int32_t* cnt;          // [n][n_kv]
     bf16* obuf;            // [n][qw]
+    void* ws;
 };
 
 constexpr int AT_THREADS = 128;
 
 template <int HD, int REP>
+struct AttnSmem {
+    static constexpr int RPT = 128 / HD;             // K rows per thread in the score pass
+    static constexpr int CHUNK = AT_THREADS * RPT;   // positions per CTA
+    static constexpr int PC = HD / 8;                // 16-byte pieces per row
+    static constexpr int RG = AT_THREADS / PC;       // row groups of the P.V pass
+    static constexpr uint32_t OFF_V = 0;             // V chunk [CHUNK][HD] bf16
+    static constexpr uint32_t OFF_P = OFF_V + CHUNK * HD * 2;
+    static constexpr uint32_t OFF_RED = OFF_P + REP * CHUNK * 4;
+    static constexpr uint32_t OFF_Q = OFF_RED + (AT_THREADS / 32) * REP * HD * 4;
+    static constexpr uint32_t OFF_BAR = OFF_Q + REP * HD * 4;
+    static constexpr size_t BYTES = OFF_BAR + 64;
+};
+
+// One (chunk, kv head, item): the chunk's V is copied into shared memory at once
+// (one bulk copy when the head's positions are contiguous) while the scores are
+// computed from K rows held in registers; then softmax statistics and P.V from
+// shared memory. The last chunk of an (item, kv head) to finish merges the
+// chunks' partials.
+template <int HD, int REP>
 __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_constant__ AttnArgs a) {
-    constexpr int RPT = 128 / HD;                 // K rows per thread in the score pass
-    constexpr int CHUNK = AT_THREADS * RPT;       // positions per CTA
-    constexpr int PC = HD / 8;                    // 16-byte pieces per row
-    constexpr int RG = AT_THREADS / PC;           // row groups of the P.V pass
-    __shared__ float s_q[REP][HD];
-    __shared__ float s_p[REP][CHUNK];
-    __shared__ float s_red[RG][REP][HD];
-    __shared__ float s_mx[REP][AT_THREADS / 32], s_l[REP][AT_THREADS / 32];
+    using S = AttnSmem<HD, REP>;
+    constexpr int RPT = S::RPT, CHUNK = S::CHUNK, PC = S::PC, RG = S::RG;
+    constexpr int NW = AT_THREADS / 32;
+    extern __shared__ __align__(128) uint8_t at_smem[];
+    bf16* s_v = reinterpret_cast<bf16*>(at_smem + S::OFF_V);
+    float (*s_p)[CHUNK] = reinterpret_cast<float (*)[CHUNK]>(at_smem + S::OFF_P);
+    float (*s_red)[REP][HD] = reinterpret_cast<float (*)[REP][HD]>(at_smem + S::OFF_RED);
+    float (*s_q)[HD] = reinterpret_cast<float (*)[HD]>(at_smem + S::OFF_Q);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(at_smem + S::OFF_BAR);
+    volatile int* abort = reinterpret_cast<volatile int*>(bar + 1);
+    __shared__ float s_mx[REP][NW], s_l[REP][NW];
     __shared__ float s_m[REP], s_sum[REP];
     __shared__ int s_last;
 
@@ -563,6 +663,23 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
     const int t0 = c * CHUNK, cnt = min(CHUNK, pm + 1 - t0);
     const int64_t base = a.layer * a.cl.s_layer + a.iseq[m] * a.cl.s_seq + static_cast<int64_t>(g) * a.cl.s_head +
                          static_cast<int64_t>(t0) * a.cl.s_pos;
+    // V chunk -> shared memory
+    if (a.contig) {
+        if (tid == 0) {
+            tc::mbar_init(bar, 1);
+            *abort = 0;
+            tc::fence_barrier_init();
+            tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * HD * 2);
+            bulk_load(s_v, a.vc + base, static_cast<uint32_t>(cnt) * HD * 2, bar);
+        }
+    } else {
+        if (tid == 0) *abort = 0;
+        for (int i = tid; i < cnt * PC; i += AT_THREADS) {
+            const int tt = i / PC, pc = i % PC;
+            cp_async16(s_v + tt * HD + 8 * pc, a.vc + base + static_cast<int64_t>(tt) * a.cl.s_pos + 8 * pc);
+        }
+        cp_commit();
+    }
     for (int i = tid; i < REP * HD; i += AT_THREADS)
         s_q[i / HD][i % HD] = __bfloat162float(a.qbuf[static_cast<int64_t>(m) * a.qw + g * REP * HD + i]) * a.qscale;
     __syncthreads();
@@ -580,31 +697,46 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
                 const uint4* src = reinterpret_cast<const uint4*>(a.kc + base + static_cast<int64_t>(tt) * a.cl.s_pos);
 #pragma unroll
                 for (int q = 0; q < PC; ++q) kr[j][q] = __ldcs(src + q);
+            } else {
+#pragma unroll
+                for (int q = 0; q < PC; ++q) kr[j][q] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        // q is read as float4 pairs once per 8 columns and used for every row
+        float acc[RPT][REP];
+#pragma unroll
+        for (int j = 0; j < RPT; ++j)
+#pragma unroll
+            for (int r = 0; r < REP; ++r) acc[j][r] = 0.f;
+#pragma unroll
+        for (int q = 0; q < PC; ++q) {
+            float k8[RPT][8];
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) {
+                unpack_bf16x2(kr[j][q].x, k8[j][0], k8[j][1]);
+                unpack_bf16x2(kr[j][q].y, k8[j][2], k8[j][3]);
+                unpack_bf16x2(kr[j][q].z, k8[j][4], k8[j][5]);
+                unpack_bf16x2(kr[j][q].w, k8[j][6], k8[j][7]);
+            }
+#pragma unroll
+            for (int r = 0; r < REP; ++r) {
+                const float4 qa = *reinterpret_cast<const float4*>(&s_q[r][8 * q]);
+                const float4 qb = *reinterpret_cast<const float4*>(&s_q[r][8 * q + 4]);
+                const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                for (int j = 0; j < RPT; ++j)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[j][r] = fmaf(qv[e], k8[j][e], acc[j][r]);
             }
         }
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {
             const int tt = tid + j * AT_THREADS;
             if (tt >= cnt) continue;
-            float acc[REP];
-#pragma unroll
-            for (int r = 0; r < REP; ++r) acc[r] = 0.f;
-#pragma unroll
-            for (int q = 0; q < PC; ++q) {
-                float k8[8];
-                unpack_bf16x2(kr[j][q].x, k8[0], k8[1]);
-                unpack_bf16x2(kr[j][q].y, k8[2], k8[3]);
-                unpack_bf16x2(kr[j][q].z, k8[4], k8[5]);
-                unpack_bf16x2(kr[j][q].w, k8[6], k8[7]);
-#pragma unroll
-                for (int r = 0; r < REP; ++r)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[r] = fmaf(s_q[r][8 * q + e], k8[e], acc[r]);
-            }
 #pragma unroll
             for (int r = 0; r < REP; ++r) {
-                s_p[r][tt] = acc[r];
-                mx[r] = fmaxf(mx[r], acc[r]);
+                s_p[r][tt] = acc[j][r];
+                mx[r] = fmaxf(mx[r], acc[j][r]);
             }
         }
     }
@@ -618,7 +750,7 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
     __syncthreads();
     if (tid < REP) {
         float v = -INFINITY;
-        for (int w = 0; w < AT_THREADS / 32; ++w) v = fmaxf(v, s_mx[tid][w]);
+        for (int w = 0; w < NW; ++w) v = fmaxf(v, s_mx[tid][w]);
         s_m[tid] = v;
     }
     __syncthreads();
@@ -643,10 +775,17 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
             if (lane == 0) s_l[r][warp] = v;
         }
     }
+    // the V chunk has landed
+    if (a.contig) {
+        if (tid == 0 && !tc::mbar_wait(bar, 0, abort, a.ws, 91)) *abort = 1;
+    } else {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    }
     __syncthreads();
+    if (*abort) return;
     if (tid < REP) {
         float v = 0.f;
-        for (int w = 0; w < AT_THREADS / 32; ++w) v += s_l[tid][w];
+        for (int w = 0; w < NW; ++w) v += s_l[tid][w];
         s_sum[tid] = v;
     }
     // P.V: thread (row group rg, piece pc): rows rg, rg + RG, ...; 8 columns
@@ -657,45 +796,41 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
         for (int r = 0; r < REP; ++r)
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[r][e] = 0.f;
-        constexpr int ROWS = CHUNK / RG;
-        constexpr int BATCH = 8;
-#pragma unroll 1
-        for (int b0 = 0; b0 < ROWS; b0 += BATCH) {
-            uint4 vr[BATCH];
+#pragma unroll 4
+        for (int tt = rg; tt < cnt; tt += RG) {
+            const uint4 vr = *reinterpret_cast<const uint4*>(s_v + tt * HD + 8 * pc);
+            float v8[8];
+            unpack_bf16x2(vr.x, v8[0], v8[1]);
+            unpack_bf16x2(vr.y, v8[2], v8[3]);
+            unpack_bf16x2(vr.z, v8[4], v8[5]);
+            unpack_bf16x2(vr.w, v8[6], v8[7]);
 #pragma unroll
-            for (int j = 0; j < BATCH; ++j) {
-                const int tt = rg + (b0 + j) * RG;
-                if (tt < cnt)
-                    vr[j] = __ldcs(reinterpret_cast<const uint4*>(a.vc + base + static_cast<int64_t>(tt) * a.cl.s_pos) + pc);
-            }
+            for (int r = 0; r < REP; ++r) {
+                const float p = s_p[r][tt];
 #pragma unroll
-            for (int j = 0; j < BATCH; ++j) {
-                const int tt = rg + (b0 + j) * RG;
-                if (tt >= cnt) continue;
-                float v8[8];
-                unpack_bf16x2(vr[j].x, v8[0], v8[1]);
-                unpack_bf16x2(vr[j].y, v8[2], v8[3]);
-                unpack_bf16x2(vr[j].z, v8[4], v8[5]);
-                unpack_bf16x2(vr[j].w, v8[6], v8[7]);
-#pragma unroll
-                for (int r = 0; r < REP; ++r) {
-                    const float p = s_p[r][tt];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[r][e] = fmaf(p, v8[e], o[r][e]);
-                }
+                for (int e = 0; e < 8; ++e) o[r][e] = fmaf(p, v8[e], o[r][e]);
             }
         }
+        // the row groups of a warp, then the warps
 #pragma unroll
         for (int r = 0; r < REP; ++r)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) s_red[rg][r][8 * pc + e] = o[r][e];
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                for (int sh = PC; sh < 32; sh <<= 1) o[r][e] += __shfl_xor_sync(0xFFFFFFFFu, o[r][e], sh);
+        if (lane < PC)
+#pragma unroll
+            for (int r = 0; r < REP; ++r)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s_red[warp][r][8 * pc + e] = o[r][e];
     }
     __syncthreads();
     if (nch == 1) {   // the whole range in this CTA: normalise and store
         for (int i = tid; i < REP * HD; i += AT_THREADS) {
             const int r = i / HD, e = i % HD;
             float v = 0.f;
-            for (int w = 0; w < RG; ++w) v += s_red[w][r][e];
+#pragma unroll
+            for (int w = 0; w < NW; ++w) v += s_red[w][r][e];
             out[i] = __float2bfloat16_rn(v / s_sum[r]);
         }
         return;
@@ -704,7 +839,8 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
     for (int i = tid; i < REP * HD; i += AT_THREADS) {
         const int r = i / HD, e = i % HD;
         float v = 0.f;
-        for (int w = 0; w < RG; ++w) v += s_red[w][r][e];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) v += s_red[w][r][e];
         pp[r * (HD + 2) + e] = v;
     }
     if (tid < REP) {
@@ -722,33 +858,72 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    // merge the chunks: O = sum_c o_c 2^(m_c - M) / sum_c l_c 2^(m_c - M)
-    const float* p0 = a.part + (static_cast<int64_t>(m) * a.n_kv + g) * a.chunks * (REP * (HD + 2));
+    // merge the chunks: O = sum_c o_c 2^(m_c - M) / sum_c l_c 2^(m_c - M). The
+    // chunks' (m_c, l_c) go to shared memory first (one load per thread; the V
+    // buffer is free by now), then a column's o_c are loaded 16 at a time.
+    const int nc = a.chunks;
+    const float* p0 = a.part + (static_cast<int64_t>(m) * a.n_kv + g) * nc * (REP * (HD + 2));
+    float* s_ml = reinterpret_cast<float*>(s_v);   // [REP][nc][2]
+    float* s_w = s_ml + 2 * REP * nc;              // [REP][nc]: 2^(m_c - M) / L
+    for (int i = tid; i < REP * nch; i += AT_THREADS) {
+        const int r = i / nch, cc = i % nch;
+        const float* q = p0 + cc * (REP * (HD + 2)) + r * (HD + 2) + HD;
+        s_ml[(r * nc + cc) * 2] = __ldcg(q);
+        s_ml[(r * nc + cc) * 2 + 1] = __ldcg(q + 1);
+    }
+    __syncthreads();
+    if (tid < REP) {
+        float M = -INFINITY;
+        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, s_ml[(tid * nc + cc) * 2]);
+        float L = 0.f;
+        for (int cc = 0; cc < nch; ++cc) {
+            const float w = exp2f(s_ml[(tid * nc + cc) * 2] - M);
+            s_w[tid * nc + cc] = w;
+            L = fmaf(s_ml[(tid * nc + cc) * 2 + 1], w, L);
+        }
+        for (int cc = 0; cc < nch; ++cc) s_w[tid * nc + cc] /= L;
+    }
+    __syncthreads();
     for (int i = tid; i < REP * HD; i += AT_THREADS) {
         const int r = i / HD, e = i % HD;
-        float M = -INFINITY;
-        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(p0 + cc * (REP * (HD + 2)) + r * (HD + 2) + HD));
-        float L = 0.f, O = 0.f;
-        for (int cc = 0; cc < nch; ++cc) {
-            const float* q = p0 + cc * (REP * (HD + 2)) + r * (HD + 2);
-            const float w = exp2f(__ldcg(q + HD) - M);
-            L = fmaf(__ldcg(q + HD + 1), w, L);
-            O = fmaf(__ldcg(q + e), w, O);
+        float O = 0.f;
+        for (int c0 = 0; c0 < nch; c0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < nch) v[j] = __ldcg(p0 + (c0 + j) * (REP * (HD + 2)) + r * (HD + 2) + e);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < nch) O = fmaf(v[j], s_w[r * nc + c0 + j], O);
         }
-        out[i] = __float2bfloat16_rn(O / L);
+        out[i] = __float2bfloat16_rn(O);
     }
+}
+
+template <int HD, int REP>
+tee_status launch_attn_rep(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+    static bool attr = false;
+    constexpr size_t bytes = AttnSmem<HD, REP>::BYTES;
+    if (!attr) {
+        tee_status st = cuda_status(cudaFuncSetAttribute(river_attn_kernel<HD, REP>,
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         static_cast<int>(bytes)));
+        if (st != TEE_OK) return st;
+        attr = true;
+    }
+    river_attn_kernel<HD, REP><<<grid, AT_THREADS, bytes, s>>>(a);
+    return launch_status();
 }
 
 template <int HD>
 tee_status launch_attn(const AttnArgs& a, int rep, dim3 grid, cudaStream_t s) {
     switch (rep) {
-        case 1: river_attn_kernel<HD, 1><<<grid, AT_THREADS, 0, s>>>(a); break;
-        case 2: river_attn_kernel<HD, 2><<<grid, AT_THREADS, 0, s>>>(a); break;
-        case 4: river_attn_kernel<HD, 4><<<grid, AT_THREADS, 0, s>>>(a); break;
-        case 8: river_attn_kernel<HD, 8><<<grid, AT_THREADS, 0, s>>>(a); break;
+        case 1: return launch_attn_rep<HD, 1>(a, grid, s);
+        case 2: return launch_attn_rep<HD, 2>(a, grid, s);
+        case 4: return launch_attn_rep<HD, 4>(a, grid, s);
+        case 8: return launch_attn_rep<HD, 8>(a, grid, s);
         default: return TEE_ERR_UNSUPPORTED;
     }
-    return launch_status();
 }
 
 // ------------------------------------------------------------------ host
@@ -776,18 +951,66 @@ W4Seg seg_of(const tee_w4& w, int n) {
                  static_cast<const __half*>(w.zero), n};
 }
 
+// Clusters of ks GEMM CTAs that can be resident at once (one CTA per SM).
+int max_clusters(int ks) {
+    static int cache[MAX_KS + 1] = {};
+    if (ks <= 1) return 1 << 20;
+    if (cache[ks]) return cache[ks];
+    if (cudaFuncSetAttribute(w4_gemm_kernel<M_O>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(G_SMEM)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1, ks * 64);
+    cfg.blockDim = dim3(G_THREADS);
+    cfg.dynamicSmemBytes = G_SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = ks;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, w4_gemm_kernel<M_O>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        c = 0;
+    }
+    cache[ks] = c > 0 ? c : -1;
+    return c;
+}
+
 template <int MODE>
-tee_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
+tee_status launch_gemm(const GemmArgs& g0, cudaStream_t s) {
+    GemmArgs g = g0;
+    tee_status st = make_tmap_bf16(&g.tm_a, g.a, g.K, G_A_ROWS, static_cast<uint64_t>(g.lda) * 2, GT_K, G_A_ROWS);
+    if (st != TEE_OK) return st;
+    for (int i = 0; i < g.n_seg; ++i) {
+        st = make_tmap_u8(&g.tm_c[i], g.seg[i].codes, g.seg[i].n, g.K / 2, g.seg[i].n, MODE == M_GU ? 64 : GT_N, 32);
+        if (st != TEE_OK) return st;
+    }
     static bool attr = false;
     if (!attr) {
-        tee_status st = cuda_status(cudaFuncSetAttribute(w4_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         static_cast<int>(G_SMEM)));
+        st = cuda_status(cudaFuncSetAttribute(w4_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(G_SMEM)));
         if (st != TEE_OK) return st;
         attr = true;
     }
-    const int tiles = g.N / GT_N;
-    w4_gemm_kernel<MODE><<<dim3(tiles, g.ks), G_THREADS, G_SMEM, s>>>(g, nullptr);
-    return launch_status();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(g.N / GT_N, g.ks);
+    cfg.blockDim = dim3(G_THREADS);
+    cfg.dynamicSmemBytes = G_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = g.ks;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = g.ks > 1 ? 1 : 0;
+    st = cuda_status(cudaLaunchKernelEx(&cfg, w4_gemm_kernel<MODE>, g, static_cast<void*>(nullptr)));
+    return st != TEE_OK ? st : launch_status();
 }
 
 }  // namespace
@@ -898,8 +1121,6 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     GemmArgs g{};
     g.n_max = n_max;
     g.n_dev = n_dev;
-    g.part = ws_at<float>(ws, w.part);
-    g.cnt = gcnt;
     g.eps = D->eps;
     g.qw = qw;
     g.kvw = kvw;
@@ -934,7 +1155,12 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     at.part = ws_at<float>(ws, w.apart);
     at.cnt = acnt;
     at.obuf = obuf;
+    at.contig = cl.s_pos == hd;
+    at.ws = ws;
     const int rep = D->n_q_heads / D->n_kv_heads;
+    // the merge keeps 3 floats per (q head of a group, chunk) in the 32 KB V buffer
+    if (static_cast<size_t>(at.chunks) * rep * 3 * 4 > static_cast<size_t>(at_chunk(hd)) * hd * 2)
+        return TEE_ERR_UNSUPPORTED;
 
     for (int l = 0; l < n_layers; ++l) {
         const tee_river_layer& L = layers[l];

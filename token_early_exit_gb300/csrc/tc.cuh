@@ -239,6 +239,10 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // Out-of-range rows/columns read as zero.
 tee_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                           uint32_t box_inner, uint32_t box_rows);
+// Host: a 2-D u8 tensor map over [rows][inner] bytes, box [box_rows][box_inner],
+// no swizzle (rows land box_inner bytes apart).
+tee_status make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_rows);
 // The same matrix ([rows][n_kb * 64]) as n_kb blocks of 64 columns: a box brings
 // box_kb consecutive blocks, each as its own swizzled [box_rows][64] tile, in one
 // copy (a TMA copy costs about the same time whatever its size, so larger boxes
