@@ -72,6 +72,22 @@ tee_status make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint
     return r == CUDA_SUCCESS ? TEE_OK : TEE_ERR_INVALID_ARG;
 }
 
+tee_status make_tmap_cache(CUtensorMap* map, const void* base, int head_dim, const tee_cache_layout& cl,
+                           uint32_t box_rows) {
+    if (!encoder_ready()) return TEE_ERR_UNSUPPORTED;
+    cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(cl.max_pos),
+                          static_cast<cuuint64_t>(cl.n_heads), static_cast<cuuint64_t>(cl.n_seq),
+                          static_cast<cuuint64_t>(cl.n_layers)};
+    cuuint64_t strides[4] = {static_cast<cuuint64_t>(cl.s_pos) * 2, static_cast<cuuint64_t>(cl.s_head) * 2,
+                             static_cast<cuuint64_t>(cl.s_seq) * 2, static_cast<cuuint64_t>(cl.s_layer) * 2};
+    cuuint32_t box[5] = {64, box_rows, 1, 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TEE_OK : TEE_ERR_INVALID_ARG;
+}
+
 // A K-major bf16 matrix [rows][n_kb * 64] seen as n_kb blocks of 64 columns: one
 // box brings box_kb consecutive blocks of box_rows rows, each block landing as its
 // own 128-byte-swizzled [box_rows][64] tile (block stride 128 bytes in the source).

@@ -592,17 +592,14 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
 
 // ------------------------------------------------------------------ attention
 struct AttnArgs {
+    CUtensorMap kmap, vmap;   // the caches, 5-D (head_dim, pos, head, seq, layer), box 64 x 64, 128-byte swizzle
     int n_max;
     const int32_t* n_dev;
     int n_kv, qw, chunks;
     const bf16* qbuf;
     const int32_t* ipos;
     const int32_t* iseq;
-    const bf16* kc;
-    const bf16* vc;
-    tee_cache_layout cl;
     int layer;
-    int contig;            // s_pos == head_dim: a chunk of one head is one contiguous block
     float qscale;          // log2(e) / sqrt(head_dim)
     float* part;           // [n][n_kv][chunks][REP][HD + 2]
     int32_t* cnt;          // [n][n_kv]
@@ -611,6 +608,7 @@ struct AttnArgs {
 };
 
 constexpr int AT_THREADS = 128;
+constexpr int AT_BOX = 64;   // positions per TMA box
 
 template <int HD, int REP>
 struct AttnSmem {
@@ -618,31 +616,42 @@ struct AttnSmem {
     static constexpr int CHUNK = AT_THREADS * RPT;   // positions per CTA
     static constexpr int PC = HD / 8;                // 16-byte pieces per row
     static constexpr int RG = AT_THREADS / PC;       // row groups of the P.V pass
-    static constexpr uint32_t OFF_V = 0;             // V chunk [CHUNK][HD] bf16
-    static constexpr uint32_t OFF_P = OFF_V + CHUNK * HD * 2;
+    static constexpr uint32_t KV_BYTES = CHUNK * HD * 2;   // 32 KB: halves of 64 columns, rows of 128 bytes
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+    static constexpr uint32_t OFF_P = OFF_V + KV_BYTES;
     static constexpr uint32_t OFF_RED = OFF_P + REP * CHUNK * 4;
     static constexpr uint32_t OFF_Q = OFF_RED + (AT_THREADS / 32) * REP * HD * 4;
     static constexpr uint32_t OFF_BAR = OFF_Q + REP * HD * 4;
-    static constexpr size_t BYTES = OFF_BAR + 64;
+    static constexpr size_t BYTES = 1024 + OFF_BAR + 64;
 };
 
-// One (chunk, kv head, item): the chunk's V is copied into shared memory at once
-// (one bulk copy when the head's positions are contiguous) while the scores are
-// computed from K rows held in registers; then softmax statistics and P.V from
-// shared memory. The last chunk of an (item, kv head) to finish merges the
+// Byte offset of 16-byte piece q of row t in a swizzled K or V chunk: 64-column
+// halves of CHUNK rows x 128 bytes, piece j of row t at j ^ (t % 8).
+template <int CHUNK>
+__device__ __forceinline__ uint32_t sw_off(int t, int q) {
+    return (q >> 3) * (CHUNK * 128) + t * 128 + (((q & 7) ^ (t & 7)) << 4);
+}
+
+// One (chunk, kv head, item): TMA brings the chunk's K and V (swizzled) into
+// shared memory; scores, softmax statistics and P.V are computed from there on
+// the CUDA cores. The last chunk of an (item, kv head) to finish merges the
 // chunks' partials.
 template <int HD, int REP>
 __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_constant__ AttnArgs a) {
     using S = AttnSmem<HD, REP>;
     constexpr int RPT = S::RPT, CHUNK = S::CHUNK, PC = S::PC, RG = S::RG;
     constexpr int NW = AT_THREADS / 32;
-    extern __shared__ __align__(128) uint8_t at_smem[];
-    bf16* s_v = reinterpret_cast<bf16*>(at_smem + S::OFF_V);
-    float (*s_p)[CHUNK] = reinterpret_cast<float (*)[CHUNK]>(at_smem + S::OFF_P);
-    float (*s_red)[REP][HD] = reinterpret_cast<float (*)[REP][HD]>(at_smem + S::OFF_RED);
-    float (*s_q)[HD] = reinterpret_cast<float (*)[HD]>(at_smem + S::OFF_Q);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(at_smem + S::OFF_BAR);
-    volatile int* abort = reinterpret_cast<volatile int*>(bar + 1);
+    extern __shared__ uint8_t at_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
+    const uint8_t* s_k = sm + S::OFF_K;
+    uint8_t* s_v = sm + S::OFF_V;
+    float (*s_p)[CHUNK] = reinterpret_cast<float (*)[CHUNK]>(sm + S::OFF_P);
+    float (*s_red)[REP][HD] = reinterpret_cast<float (*)[REP][HD]>(sm + S::OFF_RED);
+    float (*s_q)[HD] = reinterpret_cast<float (*)[HD]>(sm + S::OFF_Q);
+    uint64_t* kbar = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);
+    uint64_t* vbar = kbar + 1;
+    volatile int* abort = reinterpret_cast<volatile int*>(vbar + 1);
     __shared__ float s_mx[REP][NW], s_l[REP][NW];
     __shared__ float s_m[REP], s_sum[REP];
     __shared__ int s_last;
@@ -661,48 +670,35 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
     const int nch = pm / CHUNK + 1;
     if (c >= nch) return;
     const int t0 = c * CHUNK, cnt = min(CHUNK, pm + 1 - t0);
-    const int64_t base = a.layer * a.cl.s_layer + a.iseq[m] * a.cl.s_seq + static_cast<int64_t>(g) * a.cl.s_head +
-                         static_cast<int64_t>(t0) * a.cl.s_pos;
-    // V chunk -> shared memory
-    if (a.contig) {
-        if (tid == 0) {
-            tc::mbar_init(bar, 1);
-            *abort = 0;
-            tc::fence_barrier_init();
-            tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * HD * 2);
-            bulk_load(s_v, a.vc + base, static_cast<uint32_t>(cnt) * HD * 2, bar);
-        }
-    } else {
-        if (tid == 0) *abort = 0;
-        for (int i = tid; i < cnt * PC; i += AT_THREADS) {
-            const int tt = i / PC, pc = i % PC;
-            cp_async16(s_v + tt * HD + 8 * pc, a.vc + base + static_cast<int64_t>(tt) * a.cl.s_pos + 8 * pc);
-        }
-        cp_commit();
+    if (tid == 0) {
+        tc::mbar_init(kbar, 1);
+        tc::mbar_init(vbar, 1);
+        *abort = 0;
+        tc::fence_barrier_init();
+        const int nb = (cnt + AT_BOX - 1) / AT_BOX;
+        const uint32_t bytes = static_cast<uint32_t>(nb) * (HD / 64) * AT_BOX * 128;
+        const int sq = a.iseq[m];
+        tc::mbar_arrive_expect_tx(kbar, bytes);
+        for (int b = 0; b < nb; ++b)
+            for (int h = 0; h < HD / 64; ++h)
+                tc::tma_load_5d(sm + S::OFF_K + h * (CHUNK * 128) + b * (AT_BOX * 128), &a.kmap, 64 * h,
+                                t0 + b * AT_BOX, g, sq, a.layer, kbar);
+        tc::mbar_arrive_expect_tx(vbar, bytes);
+        for (int b = 0; b < nb; ++b)
+            for (int h = 0; h < HD / 64; ++h)
+                tc::tma_load_5d(s_v + h * (CHUNK * 128) + b * (AT_BOX * 128), &a.vmap, 64 * h, t0 + b * AT_BOX, g,
+                                sq, a.layer, vbar);
     }
     for (int i = tid; i < REP * HD; i += AT_THREADS)
         s_q[i / HD][i % HD] = __bfloat162float(a.qbuf[static_cast<int64_t>(m) * a.qw + g * REP * HD + i]) * a.qscale;
     __syncthreads();
+    if (!tc::mbar_wait(kbar, 0, abort, a.ws, 91)) *abort = 1;
 
-    // scores: thread -> RPT rows; every load of the rows issued before the sums
+    // scores: thread -> rows tid + 128 j
     float mx[REP];
 #pragma unroll
     for (int r = 0; r < REP; ++r) mx[r] = -INFINITY;
     {
-        uint4 kr[RPT][PC];
-#pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            const int tt = tid + j * AT_THREADS;
-            if (tt < cnt) {
-                const uint4* src = reinterpret_cast<const uint4*>(a.kc + base + static_cast<int64_t>(tt) * a.cl.s_pos);
-#pragma unroll
-                for (int q = 0; q < PC; ++q) kr[j][q] = __ldcs(src + q);
-            } else {
-#pragma unroll
-                for (int q = 0; q < PC; ++q) kr[j][q] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        // q is read as float4 pairs once per 8 columns and used for every row
         float acc[RPT][REP];
 #pragma unroll
         for (int j = 0; j < RPT; ++j)
@@ -713,10 +709,11 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
             float k8[RPT][8];
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
-                unpack_bf16x2(kr[j][q].x, k8[j][0], k8[j][1]);
-                unpack_bf16x2(kr[j][q].y, k8[j][2], k8[j][3]);
-                unpack_bf16x2(kr[j][q].z, k8[j][4], k8[j][5]);
-                unpack_bf16x2(kr[j][q].w, k8[j][6], k8[j][7]);
+                const uint4 u = *reinterpret_cast<const uint4*>(s_k + sw_off<CHUNK>(tid + j * AT_THREADS, q));
+                unpack_bf16x2(u.x, k8[j][0], k8[j][1]);
+                unpack_bf16x2(u.y, k8[j][2], k8[j][3]);
+                unpack_bf16x2(u.z, k8[j][4], k8[j][5]);
+                unpack_bf16x2(u.w, k8[j][6], k8[j][7]);
             }
 #pragma unroll
             for (int r = 0; r < REP; ++r) {
@@ -775,12 +772,7 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
             if (lane == 0) s_l[r][warp] = v;
         }
     }
-    // the V chunk has landed
-    if (a.contig) {
-        if (tid == 0 && !tc::mbar_wait(bar, 0, abort, a.ws, 91)) *abort = 1;
-    } else {
-        asm volatile("cp.async.wait_all;" ::: "memory");
-    }
+    if (!tc::mbar_wait(vbar, 0, abort, a.ws, 92)) *abort = 1;
     __syncthreads();
     if (*abort) return;
     if (tid < REP) {
@@ -798,7 +790,7 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
             for (int e = 0; e < 8; ++e) o[r][e] = 0.f;
 #pragma unroll 4
         for (int tt = rg; tt < cnt; tt += RG) {
-            const uint4 vr = *reinterpret_cast<const uint4*>(s_v + tt * HD + 8 * pc);
+            const uint4 vr = *reinterpret_cast<const uint4*>(s_v + sw_off<CHUNK>(tt, pc));
             float v8[8];
             unpack_bf16x2(vr.x, v8[0], v8[1]);
             unpack_bf16x2(vr.y, v8[2], v8[3]);
@@ -863,7 +855,7 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
     // buffer is free by now), then a column's o_c are loaded 16 at a time.
     const int nc = a.chunks;
     const float* p0 = a.part + (static_cast<int64_t>(m) * a.n_kv + g) * nc * (REP * (HD + 2));
-    float* s_ml = reinterpret_cast<float*>(s_v);   // [REP][nc][2]
+    float* s_ml = reinterpret_cast<float*>(s_v);   // [REP][nc][2] (the V chunk is no longer needed)
     float* s_w = s_ml + 2 * REP * nc;              // [REP][nc]: 2^(m_c - M) / L
     for (int i = tid; i < REP * nch; i += AT_THREADS) {
         const int r = i / nch, cc = i % nch;
@@ -1148,14 +1140,12 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     at.qbuf = qbuf;
     at.ipos = ipos;
     at.iseq = iseq;
-    at.kc = static_cast<const bf16*>(k_cache);
-    at.vc = static_cast<const bf16*>(v_cache);
-    at.cl = cl;
+    if ((st = make_tmap_cache(&at.kmap, k_cache, hd, cl, AT_BOX)) != TEE_OK) return st;
+    if ((st = make_tmap_cache(&at.vmap, v_cache, hd, cl, AT_BOX)) != TEE_OK) return st;
     at.qscale = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
     at.part = ws_at<float>(ws, w.apart);
     at.cnt = acnt;
     at.obuf = obuf;
-    at.contig = cl.s_pos == hd;
     at.ws = ws;
     const int rep = D->n_q_heads / D->n_kv_heads;
     // the merge keeps 3 floats per (q head of a group, chunk) in the 32 KB V buffer

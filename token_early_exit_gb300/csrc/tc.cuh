@@ -119,6 +119,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int x, int y, int z, int w, int v,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], "
+        "[%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -239,6 +247,11 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // Out-of-range rows/columns read as zero.
 tee_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                           uint32_t box_inner, uint32_t box_rows);
+// Host: a 5-D bf16 tensor map over a KV cache [layer][seq][head][pos][head_dim]
+// with the layout's strides; box 64 (of head_dim) x box_rows positions, 128-byte
+// swizzle (head_dim 128 takes two boxes, x = 0 and 64).
+tee_status make_tmap_cache(CUtensorMap* map, const void* base, int head_dim, const tee_cache_layout& cl,
+                           uint32_t box_rows);
 // Host: a 2-D u8 tensor map over [rows][inner] bytes, box [box_rows][box_inner],
 // no swizzle (rows land box_inner bytes apart).
 tee_status make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
