@@ -456,9 +456,14 @@ typedef struct {
     int32_t reserved;       /* 0 */
 } tee_river_layer;
 
-/* Size of `prep` (the RoPE table for positions [0, max_pos)). */
-TEE_API size_t tee_exit_river_prep_size(const tee_river_desc* desc, int32_t max_pos);
-TEE_API tee_status tee_exit_river_prepare(const tee_river_desc* desc, int32_t max_pos, void* prep,
+/* Size of `prep`: the layers' weights repacked per 128-column tile (each k
+ * block's codes, scales and zeros contiguous; about 1.1x the int4 weights) and
+ * the RoPE table for positions [0, max_pos). */
+TEE_API size_t tee_exit_river_prep_size(const tee_river_desc* desc, int32_t n_layers, int32_t max_pos);
+/* Fill `prep` for these layers (run again whenever their weights change);
+ * tee_exit_river reads it with the same desc and the same layers in order. */
+TEE_API tee_status tee_exit_river_prepare(const tee_river_desc* desc, int32_t n_layers,
+                                          const tee_river_layer* layers, int32_t max_pos, void* prep,
                                           size_t prep_bytes, void* stream);
 /* Workspace of a call with up to n_max items over caches of cache->max_pos
  * positions. */
@@ -489,7 +494,9 @@ TEE_API size_t tee_exit_river_workspace_size(const tee_river_desc* desc, int32_t
  *   h_out[i] is left as it was.
  *
  *   layers     host array of n_layers exit layers, in order
- *   prep       prepared by tee_exit_river_prepare (RoPE table)
+ *   prep       prepared by tee_exit_river_prepare for the same desc and layers
+ *              (the weights are read from there; the layers' weight pointers
+ *              are not read by this call)
  *   h          [h_rows][ld_h] bf16;  h_out [n_max][ld_out] bf16
  *   k_cache, v_cache  bf16 caches laid out as `cache` says
  */

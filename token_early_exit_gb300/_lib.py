@@ -89,8 +89,8 @@ SIGNATURES = {
     "tee_ridge_fit_workspace_size": (c_size_t, [c_int32, c_int32, c_int32]),
     "tee_ridge_fit": (c_int, [c_int32, c_int32, c_int32, _P, c_int64, _P, c_int64, c_int32, c_float, _P, c_int64, _P,
                               c_size_t, _P]),
-    "tee_exit_river_prep_size": (c_size_t, [POINTER(RiverDesc), c_int32]),
-    "tee_exit_river_prepare": (c_int, [POINTER(RiverDesc), c_int32, _P, c_size_t, _P]),
+    "tee_exit_river_prep_size": (c_size_t, [POINTER(RiverDesc), c_int32, c_int32]),
+    "tee_exit_river_prepare": (c_int, [POINTER(RiverDesc), c_int32, POINTER(RiverLayer), c_int32, _P, c_size_t, _P]),
     "tee_exit_river_workspace_size": (c_size_t, [POINTER(RiverDesc), c_int32, c_int32]),
     "tee_exit_river": (c_int, [POINTER(RiverDesc), c_int32, POINTER(RiverLayer), _P, c_size_t, c_int32, _P, _P,
                                c_int64, c_int32, _P, _P, _P, _P, _P, POINTER(CacheLayout), _P, c_int64, _P,

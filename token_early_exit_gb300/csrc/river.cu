@@ -53,24 +53,23 @@ constexpr int G_PROD_WARP = 8;   // issues the TMA / bulk copies
 constexpr int G_MMA_WARP = 9;    // issues the MMAs, owns TMEM
 constexpr int G_THREADS = 320;
 constexpr int G_EPI_THREADS = G_DQ_WARPS * 32;
-constexpr int G_S = 6;           // stages of A + codes + scales/zeros
+constexpr int G_S = 4;           // stages of two k blocks: A (TMA) + packed weights (one bulk copy)
+constexpr int G_BPS = 2;         // k blocks per stage
 constexpr int G_RB = 3;          // dequantised B buffers
 constexpr int G_A_ROWS = 128;    // A tile rows (TMEM lanes); A buffers hold 128 rows
 constexpr uint32_t G_A_BYTES = G_A_ROWS * GT_K * 2;  // 16 KB: 128 rows x 64 bf16, 128-byte swizzle
 constexpr uint32_t G_B_BYTES = GT_N * GT_K * 2;      // 16 KB
-constexpr uint32_t G_C_BYTES = 32 * GT_N;            // 4 KB: 32 packed rows x 128 columns
-constexpr uint32_t G_SZ_BYTES = 2 * GT_N * 2;        // 512 B: scales, zeros
-constexpr uint32_t G_STAGE_TX = G_A_BYTES + G_C_BYTES + G_SZ_BYTES;
+// a packed weight block: codes [32 packed rows][128 columns], then 128 fp16 scales, 128 fp16 zeros
+constexpr uint32_t G_W_BYTES = 32 * GT_N + 2 * GT_N * 2;   // 4608
 constexpr uint32_t G_OFF_A = 0;
-constexpr uint32_t G_OFF_B = G_OFF_A + G_S * G_A_BYTES;
-constexpr uint32_t G_OFF_C = G_OFF_B + G_RB * G_B_BYTES;
-constexpr uint32_t G_OFF_SZ = G_OFF_C + G_S * G_C_BYTES;
-constexpr uint32_t G_OFF_BAR = G_OFF_SZ + G_S * G_SZ_BYTES;
+constexpr uint32_t G_OFF_B = G_OFF_A + G_S * G_BPS * G_A_BYTES;
+constexpr uint32_t G_OFF_W = G_OFF_B + G_RB * G_B_BYTES;
+constexpr uint32_t G_OFF_BAR = G_OFF_W + G_S * G_BPS * G_W_BYTES;
 constexpr size_t G_SMEM = 1024 + G_OFF_BAR + (2 * G_S + 2 * G_RB + 1) * 8 + 16;
 // the CTA's partial tile after the loop: [128 rows][GT_N + 4] fp32, over the A ring
 constexpr int G_P_PITCH = GT_N + 4;
-static_assert(G_A_ROWS * G_P_PITCH * 4 <= G_S * G_A_BYTES, "partial tile fits the A ring");
-static_assert(G_OFF_B % 1024 == 0 && G_OFF_C % 16 == 0 && G_OFF_BAR % 8 == 0, "alignment");
+static_assert(G_A_ROWS * G_P_PITCH * 4 <= G_S * G_BPS * G_A_BYTES, "partial tile fits the A ring");
+static_assert(G_OFF_B % 1024 == 0 && G_OFF_W % 16 == 0 && G_OFF_BAR % 8 == 0, "alignment");
 static_assert(G_SMEM <= 232448, "shared memory");
 
 constexpr int MAX_KS = 8;        // K splits = CTAs of a cluster (portable size)
@@ -227,14 +226,15 @@ struct W4Seg {
 };
 
 struct GemmArgs {
-    CUtensorMap tm_a;       // A [128][K] bf16, box 128 x 64, 128-byte swizzle
-    CUtensorMap tm_c[3];    // codes of each segment, box 32 x 128 (GU: 32 x 64 of gate and up)
-    W4Seg seg[3];
-    int n_seg, K, N, ks;
+    CUtensorMap tm_a;       // A [128][K] bf16 as K/64 blocks, box 2 blocks x 128 rows x 64, 128-byte swizzle
+    const uint8_t* blob;    // packed weights [tile][K/64][G_W_BYTES]
+    int K, N, ks;
     int n_max;
     const int32_t* n_dev;
     const bf16* a;          // [128][lda]
     int64_t lda;
+    int a_rows;             // rows of A that TMA brings (the item bound rounded up to 8; the rest of the
+                            // 128 MMA rows read stale shared memory and feed only unused TMEM lanes)
     float* ss_zero;         // cleared by CTA (0, 0): the next producer accumulates into it
     // row scale of the normalised input: rs = 1 / sqrt(ss_in / width + eps)
     const float* ss_in;
@@ -262,36 +262,11 @@ struct GemmArgs {
     int d_ff;
 };
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(tc::smem_u32(dst)), "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
                  : "memory");
-}
-
-// Column c (0..127) of tile t -> (segment, column within it).
-template <int MODE>
-__device__ __forceinline__ void tile_col(const GemmArgs& g, int t, int c, int& s, int& col) {
-    if (MODE == M_GU) {
-        s = c >> 6;
-        col = 64 * t + (c & 63);
-    } else {
-        int c0 = t * GT_N;
-        s = 0;
-        while (s + 1 < g.n_seg && c0 >= g.seg[s].n) {
-            c0 -= g.seg[s].n;
-            ++s;
-        }
-        col = c0 + c;
-    }
 }
 
 __device__ __forceinline__ float row_scale(const GemmArgs& g, int m) {
@@ -465,81 +440,69 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     const uint32_t tmem = *tmem_slot;
 
     if (warp == G_PROD_WARP) {
-        // Block kb -> stage kb % G_S: the A tile (TMA, swizzled), the codes (TMA:
-        // one 32 x 128 box, or 32 x 64 of gate and of up) and the scale / zero rows
-        // (bulk copies), all completing on full[stage].
+        // Stage j (blocks 2j, 2j + 1) -> slot j % G_S: both A tiles in one TMA (the
+        // k-blocks map) and both packed weight blocks in one bulk copy.
         if (lane == 0) {
-            int seg0 = 0, col0 = 0;
-            tile_col<MODE>(g, t, 0, seg0, col0);
-            int kb = 0;
-            for (; kb < nkb; ++kb) {
-                const int st = kb % G_S;
-                if (kb >= G_S && !tc::mbar_wait(&empty[st], ((kb / G_S) - 1) & 1, abort, ws, 81)) break;
+            const int nst = (nkb + G_BPS - 1) / G_BPS;
+            const uint8_t* wsrc = g.blob + (static_cast<int64_t>(t) * (g.K / GT_K) + k0 / GT_K) * G_W_BYTES;
+            int j = 0;
+            for (; j < nst; ++j) {
+                const int st = j % G_S;
+                if (j >= G_S && !tc::mbar_wait(&empty[st], ((j / G_S) - 1) & 1, abort, ws, 81)) break;
+                const int nb = min(G_BPS, nkb - j * G_BPS);
                 uint64_t* bar = &full[st];
-                tc::mbar_arrive_expect_tx(bar, G_STAGE_TX);
-                const int kg = k0 + kb * GT_K;
-                tc::tma_load_2d(smem + G_OFF_A + st * G_A_BYTES, &g.tm_a, kg, 0, bar);
-                uint8_t* cdst = smem + G_OFF_C + st * G_C_BYTES;
-                __half* zdst = reinterpret_cast<__half*>(smem + G_OFF_SZ + st * G_SZ_BYTES);
-                const int64_t grow = kg / GT_K;
-                if (MODE == M_GU) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        tc::tma_load_2d(cdst + h * (G_C_BYTES / 2), &g.tm_c[h], 64 * t, kg / 2, bar);
-                        const W4Seg& sg = g.seg[h];
-                        bulk_load(zdst + 64 * h, sg.scale + grow * sg.n + 64 * t, 128, bar);
-                        bulk_load(zdst + GT_N + 64 * h, sg.zero + grow * sg.n + 64 * t, 128, bar);
-                    }
-                } else {
-                    tc::tma_load_2d(cdst, &g.tm_c[seg0], col0, kg / 2, bar);
-                    const W4Seg& sg = g.seg[seg0];
-                    bulk_load(zdst, sg.scale + grow * sg.n + col0, 256, bar);
-                    bulk_load(zdst + GT_N, sg.zero + grow * sg.n + col0, 256, bar);
-                }
+                tc::mbar_arrive_expect_tx(bar, G_BPS * g.a_rows * GT_K * 2 + nb * G_W_BYTES);
+                tc::tma_load_3d(smem + G_OFF_A + st * G_BPS * G_A_BYTES, &g.tm_a, 0, 0, k0 / GT_K + j * G_BPS, bar);
+                bulk_load(smem + G_OFF_W + st * G_BPS * G_W_BYTES, wsrc + static_cast<int64_t>(j) * G_BPS * G_W_BYTES,
+                          nb * G_W_BYTES, bar);
             }
             // stopped early: let the copies in flight land before the CTA moves on
             const uint64_t t0 = tc::globaltimer();
-            for (int j = max(0, kb - G_S); j < kb; ++j)
-                while (!tc::mbar_test_wait(&full[j % G_S], (j / G_S) & 1) && tc::globaltimer() - t0 < 200000000ull) {
+            for (int i = max(0, j - G_S); i < j; ++i)
+                while (!tc::mbar_test_wait(&full[i % G_S], (i / G_S) & 1) && tc::globaltimer() - t0 < 200000000ull) {
                 }
         }
     } else if (warp == G_MMA_WARP) {
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_bf16(128, GT_N);
             for (int kb = 0; kb < nkb; ++kb) {
-                const int st = kb % G_S, b = kb % G_RB;
-                if (!tc::mbar_wait(&full[st], (kb / G_S) & 1, abort, ws, 82)) break;
+                const int j = kb / G_BPS, st = j % G_S, b = kb % G_RB;
+                if (!tc::mbar_wait(&full[st], (j / G_S) & 1, abort, ws, 82)) break;
                 if (!tc::mbar_wait(&bfull[b], (kb / G_RB) & 1, abort, ws, 83)) break;
                 tc::tc_fence_after();
-                const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_A + st * G_A_BYTES));
+                // the stage's blocks land a_rows x 128 bytes apart (one TMA box)
+                const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_A + st * G_BPS * G_A_BYTES +
+                                                                     (kb % G_BPS) * g.a_rows * 128));
                 const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_B + b * G_B_BYTES));
 #pragma unroll
                 for (int kk = 0; kk < GT_K / 16; ++kk) tc::umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, kb | kk);
                 tc::umma_commit(&bempty[b]);
-                tc::umma_commit(&empty[st]);
+                if (kb % G_BPS == G_BPS - 1 || kb == nkb - 1) tc::umma_commit(&empty[st]);
             }
             tc::umma_commit(acc_bar);   // every MMA issued has finished (also after a stop)
         }
     } else {
         // dequantiser: column dq_n, half dq_h of each k block
         const int dq_n = tid & 127, dq_h = tid >> 7;
-        // code byte (packed row r, column dq_n) of a stage: rows 128 bytes apart, or
-        // (GU) gate columns then up columns, each [32][64]
-        const int c_off = MODE == M_GU ? (dq_n >> 6) * (G_C_BYTES / 2) + (dq_n & 63) : dq_n;
-        const int c_pitch = MODE == M_GU ? 64 : GT_N;
+        constexpr int c_pitch = GT_N;
         for (int kb = 0; kb < nkb; ++kb) {
-            const int st = kb % G_S, b = kb % G_RB;
+            const int j = kb / G_BPS, st = j % G_S, b = kb % G_RB;
             if (kb >= G_RB && !tc::mbar_wait(&bempty[b], ((kb / G_RB) - 1) & 1, abort, ws, 84)) break;
-            if (!tc::mbar_wait(&full[st], (kb / G_S) & 1, abort, ws, 85)) break;
-            const uint8_t* cs = smem + G_OFF_C + st * G_C_BYTES + c_off;
-            const __half* sz = reinterpret_cast<const __half*>(smem + G_OFF_SZ + st * G_SZ_BYTES);
+            if (!tc::mbar_wait(&full[st], (j / G_S) & 1, abort, ws, 85)) break;
+            const uint8_t* wb = smem + G_OFF_W + (st * G_BPS + kb % G_BPS) * G_W_BYTES;
+            const uint8_t* cs = wb + dq_n;
+            const __half* sz = reinterpret_cast<const __half*>(wb + 32 * GT_N);
             const float sc = __half2float(sz[dq_n]);
             const float zs = -__half2float(sz[GT_N + dq_n]) * sc;
+            // q -> float exactly as (2^23 + q) - 2^23 (a bit-or and a full-rate add, no
+            // int-to-float conversion), then (q - z) s = q s + (-z s) in one fma
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const uint32_t cb = cs[(dq_h * 16 + i) * c_pitch];
-                w[i] = pack_bf16x2(fmaf(static_cast<float>(cb & 15u), sc, zs), fmaf(static_cast<float>(cb >> 4), sc, zs));
+                const float lo = __uint_as_float(0x4B000000u | (cb & 15u)) - 8388608.0f;
+                const float hi = __uint_as_float(0x4B000000u | (cb >> 4)) - 8388608.0f;
+                w[i] = pack_bf16x2(fmaf(lo, sc, zs), fmaf(hi, sc, zs));
             }
             uint8_t* row = smem + G_OFF_B + b * G_B_BYTES + dq_n * 128;
 #pragma unroll
@@ -943,6 +906,69 @@ W4Seg seg_of(const tee_w4& w, int n) {
                  static_cast<const __half*>(w.zero), n};
 }
 
+// Packed weights of one exit layer: the q|k|v, o, gate|up and down GEMMs, each
+// [tile][K / 64][G_W_BYTES] (a tile's k blocks contiguous, so that one bulk copy
+// brings two of them).
+struct LayerPack {
+    size_t qkv, o, gu, dn, bytes;
+};
+LayerPack layer_pack(const tee_river_desc& D) {
+    const size_t qw = static_cast<size_t>(D.n_q_heads) * D.head_dim, kvw = static_cast<size_t>(D.n_kv_heads) * D.head_dim;
+    const size_t d = D.d, f = D.d_ff;
+    auto sz = [](size_t tiles, size_t K) { return round_up(tiles * (K / GT_K) * G_W_BYTES, 256); };
+    LayerPack p{};
+    size_t o = 0;
+    p.qkv = o;
+    o += sz((qw + 2 * kvw) / GT_N, d);
+    p.o = o;
+    o += sz(d / GT_N, qw);
+    p.gu = o;
+    o += sz(f / 64, d);
+    p.dn = o;
+    o += sz(d / GT_N, f);
+    p.bytes = o;
+    return p;
+}
+
+// Repack the segments of one GEMM (q|k|v, o, gate|up interleaved per tile as 64 +
+// 64 columns, down) into [tile][k block][codes 32 x 128 | scales 128 | zeros 128].
+// Grid (tiles, K / 64), 128 threads: thread c fills column c of the tile.
+__global__ void __launch_bounds__(128) w4_pack_kernel(W4Seg s0, W4Seg s1, W4Seg s2, int n_seg, int gu, int K,
+                                                      uint8_t* __restrict__ blob) {
+    const int t = blockIdx.x, kb = blockIdx.y, c = threadIdx.x;
+    int si = 0, col;
+    if (gu) {
+        si = c >> 6;
+        col = 64 * t + (c & 63);
+    } else {
+        int c0 = t * GT_N;
+        const int n0 = s0.n, n1 = s1.n;
+        if (n_seg > 1 && c0 >= n0) {
+            c0 -= n0;
+            si = 1;
+            if (n_seg > 2 && c0 >= n1) {
+                c0 -= n1;
+                si = 2;
+            }
+        }
+        col = c0 + c;
+    }
+    const W4Seg& sg = si == 0 ? s0 : (si == 1 ? s1 : s2);
+    uint8_t* out = blob + (static_cast<int64_t>(t) * (K / GT_K) + kb) * G_W_BYTES;
+#pragma unroll 4
+    for (int r = 0; r < 32; ++r) out[r * GT_N + c] = sg.codes[static_cast<int64_t>(kb * 32 + r) * sg.n + col];
+    __half* o16 = reinterpret_cast<__half*>(out + 32 * GT_N);
+    o16[c] = sg.scale[static_cast<int64_t>(kb) * sg.n + col];
+    o16[GT_N + c] = sg.zero[static_cast<int64_t>(kb) * sg.n + col];
+}
+
+tee_status pack_gemm(const W4Seg* segs, int n_seg, bool gu, int K, int tiles, uint8_t* blob, cudaStream_t s) {
+    const W4Seg none = segs[0];
+    w4_pack_kernel<<<dim3(tiles, K / GT_K), 128, 0, s>>>(segs[0], n_seg > 1 ? segs[1] : none,
+                                                       n_seg > 2 ? segs[2] : none, n_seg, gu ? 1 : 0, K, blob);
+    return launch_status();
+}
+
 // Clusters of ks GEMM CTAs that can be resident at once (one CTA per SM).
 int max_clusters(int ks) {
     static int cache[MAX_KS + 1] = {};
@@ -976,12 +1002,10 @@ int max_clusters(int ks) {
 template <int MODE>
 tee_status launch_gemm(const GemmArgs& g0, cudaStream_t s) {
     GemmArgs g = g0;
-    tee_status st = make_tmap_bf16(&g.tm_a, g.a, g.K, G_A_ROWS, static_cast<uint64_t>(g.lda) * 2, GT_K, G_A_ROWS);
+    g.a_rows = std::min(G_A_ROWS, (g.n_max + 7) / 8 * 8);
+    tee_status st = make_tmap_bf16_kblocks(&g.tm_a, g.a, G_A_ROWS, static_cast<uint64_t>(g.lda) * 2, g.K / GT_K,
+                                           g.a_rows, G_BPS);
     if (st != TEE_OK) return st;
-    for (int i = 0; i < g.n_seg; ++i) {
-        st = make_tmap_u8(&g.tm_c[i], g.seg[i].codes, g.seg[i].n, g.K / 2, g.seg[i].n, MODE == M_GU ? 64 : GT_N, 32);
-        if (st != TEE_OK) return st;
-    }
     static bool attr = false;
     if (!attr) {
         st = cuda_status(cudaFuncSetAttribute(w4_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1011,17 +1035,25 @@ tee_status launch_gemm(const GemmArgs& g0, cudaStream_t s) {
 
 using namespace tee;
 
-extern "C" size_t tee_exit_river_prep_size(const tee_river_desc* D, int32_t max_pos) {
-    if (check_desc(D) != TEE_OK || max_pos <= 0) return 0;
-    return PREP_HEADER_BYTES + rope_table_bytes(max_pos, D->head_dim);
+extern "C" size_t tee_exit_river_prep_size(const tee_river_desc* D, int32_t n_layers, int32_t max_pos) {
+    if (check_desc(D) != TEE_OK || max_pos <= 0 || n_layers < 0) return 0;
+    return PREP_HEADER_BYTES + static_cast<size_t>(n_layers) * layer_pack(*D).bytes +
+           rope_table_bytes(max_pos, D->head_dim);
 }
 
-extern "C" tee_status tee_exit_river_prepare(const tee_river_desc* D, int32_t max_pos, void* prep, size_t prep_bytes,
-                                             void* stream) {
+extern "C" tee_status tee_exit_river_prepare(const tee_river_desc* D, int32_t n_layers, const tee_river_layer* layers,
+                                             int32_t max_pos, void* prep, size_t prep_bytes, void* stream) {
     tee_status st = check_desc(D);
     if (st != TEE_OK) return st;
-    if (max_pos <= 0) return TEE_ERR_INVALID_ARG;
-    if (!prep || !aligned16(prep) || prep_bytes < tee_exit_river_prep_size(D, max_pos)) return TEE_ERR_WORKSPACE;
+    if (max_pos <= 0 || n_layers < 0 || (n_layers > 0 && !layers)) return TEE_ERR_INVALID_ARG;
+    if (!prep || !aligned16(prep) || prep_bytes < tee_exit_river_prep_size(D, n_layers, max_pos))
+        return TEE_ERR_WORKSPACE;
+    for (int l = 0; l < n_layers; ++l) {
+        const tee_river_layer& L = layers[l];
+        if (!seg_ok(L.wq) || !seg_ok(L.wk) || !seg_ok(L.wv) || !seg_ok(L.wo) || !seg_ok(L.wg) || !seg_ok(L.wu) ||
+            !seg_ok(L.wd))
+            return TEE_ERR_INVALID_ARG;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     PrepHeader h{};
     h.magic = RIVER_MAGIC;
@@ -1029,9 +1061,24 @@ extern "C" tee_status tee_exit_river_prepare(const tee_river_desc* D, int32_t ma
     h.n_kv_heads = D->n_kv_heads;
     h.head_dim = D->head_dim;
     h.max_pos = max_pos;
+    h.n_layers = n_layers;
     st = cuda_status(cudaMemcpyAsync(prep, &h, sizeof(h), cudaMemcpyHostToDevice, s));
     if (st != TEE_OK) return st;
-    float2* table = reinterpret_cast<float2*>(static_cast<char*>(prep) + PREP_HEADER_BYTES);
+    const int d = D->d, qw = D->n_q_heads * D->head_dim, kvw = D->n_kv_heads * D->head_dim, f = D->d_ff;
+    const LayerPack lp = layer_pack(*D);
+    for (int l = 0; l < n_layers; ++l) {
+        const tee_river_layer& L = layers[l];
+        uint8_t* base = static_cast<uint8_t*>(prep) + PREP_HEADER_BYTES + l * lp.bytes;
+        const W4Seg qkv[3] = {seg_of(L.wq, qw), seg_of(L.wk, kvw), seg_of(L.wv, kvw)};
+        const W4Seg o[1] = {seg_of(L.wo, d)};
+        const W4Seg gu[2] = {seg_of(L.wg, f), seg_of(L.wu, f)};
+        const W4Seg dn[1] = {seg_of(L.wd, d)};
+        if ((st = pack_gemm(qkv, 3, false, d, (qw + 2 * kvw) / GT_N, base + lp.qkv, s)) != TEE_OK) return st;
+        if ((st = pack_gemm(o, 1, false, qw, d / GT_N, base + lp.o, s)) != TEE_OK) return st;
+        if ((st = pack_gemm(gu, 2, true, d, f / 64, base + lp.gu, s)) != TEE_OK) return st;
+        if ((st = pack_gemm(dn, 1, false, f, d / GT_N, base + lp.dn, s)) != TEE_OK) return st;
+    }
+    float2* table = reinterpret_cast<float2*>(static_cast<char*>(prep) + PREP_HEADER_BYTES + n_layers * lp.bytes);
     return build_rope_table(table, max_pos, D->head_dim / 2, D->rope_base, s);
 }
 
@@ -1061,18 +1108,16 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     for (int l = 0; l < n_layers; ++l) {
         const tee_river_layer& L = layers[l];
         if (!L.attn_norm || !L.ffn_norm || !aligned16(L.attn_norm) || !aligned16(L.ffn_norm)) return TEE_ERR_INVALID_ARG;
-        if (!seg_ok(L.wq) || !seg_ok(L.wk) || !seg_ok(L.wv) || !seg_ok(L.wo) || !seg_ok(L.wg) || !seg_ok(L.wu) ||
-            !seg_ok(L.wd))
-            return TEE_ERR_INVALID_ARG;
         if (L.cache_layer < 0 || L.cache_layer >= cl.n_layers) return TEE_ERR_INVALID_ARG;
     }
-    if (!prep || !aligned16(prep) || prep_bytes < PREP_HEADER_BYTES + sizeof(float2) * (hd / 2))
-        return TEE_ERR_WORKSPACE;
+    const LayerPack lp = layer_pack(*D);
+    if (!prep || !aligned16(prep) || prep_bytes < tee_exit_river_prep_size(D, n_layers, 1)) return TEE_ERR_WORKSPACE;
     const RiverWs w = river_ws(*D, n_max, cl.max_pos);
     if (!ws || ws_bytes < w.end) return TEE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const PrepHeader* hdr = static_cast<const PrepHeader*>(prep);
-    const float2* rope = reinterpret_cast<const float2*>(static_cast<const char*>(prep) + PREP_HEADER_BYTES);
+    const float2* rope =
+        reinterpret_cast<const float2*>(static_cast<const char*>(prep) + PREP_HEADER_BYTES + n_layers * lp.bytes);
 
     float* resid = ws_at<float>(ws, w.resid);
     bf16* abuf = ws_at<bf16>(ws, w.abuf);
@@ -1156,10 +1201,8 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         const tee_river_layer& L = layers[l];
         const bool last = l == n_layers - 1;
         // q | k | v
-        g.seg[0] = seg_of(L.wq, qw);
-        g.seg[1] = seg_of(L.wk, kvw);
-        g.seg[2] = seg_of(L.wv, kvw);
-        g.n_seg = 3;
+        const uint8_t* lbase = static_cast<const uint8_t*>(prep) + PREP_HEADER_BYTES + l * lp.bytes;
+        g.blob = lbase + lp.qkv;
         g.K = d;
         g.N = qw + 2 * kvw;
         g.ks = choose_ks(g.N / GT_N, d);
@@ -1176,8 +1219,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         st = hd == 64 ? launch_attn<64>(at, rep, agrid, s) : launch_attn<128>(at, rep, agrid, s);
         if (st != TEE_OK) return st;
         // h1 = h + o Wo
-        g.seg[0] = seg_of(L.wo, d);
-        g.n_seg = 1;
+        g.blob = lbase + lp.o;
         g.K = qw;
         g.N = d;
         g.ks = choose_ks(d / GT_N, qw);
@@ -1190,9 +1232,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         g.h_out = nullptr;
         if ((st = launch_gemm<M_O>(g, s)) != TEE_OK) return st;
         // a = SiLU(x2 Wg) * (x2 Wu)
-        g.seg[0] = seg_of(L.wg, f);
-        g.seg[1] = seg_of(L.wu, f);
-        g.n_seg = 2;
+        g.blob = lbase + lp.gu;
         g.K = d;
         g.N = 2 * f;
         g.ks = choose_ks(g.N / GT_N, d);
@@ -1202,8 +1242,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         g.ss_zero = ss_a;
         if ((st = launch_gemm<M_GU>(g, s)) != TEE_OK) return st;
         // h2 = h1 + a Wd
-        g.seg[0] = seg_of(L.wd, d);
-        g.n_seg = 1;
+        g.blob = lbase + lp.dn;
         g.K = f;
         g.N = d;
         g.ks = choose_ks(d / GT_N, f);

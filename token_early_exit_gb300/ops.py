@@ -378,12 +378,13 @@ class ExitRiver:
         self.n_layers = len(layers)
         self.max_pos = int(max_pos)
         self.device = dev or torch.device("cuda")
-        nbytes = self.lib.tee_exit_river_prep_size(ctypes.byref(self.desc), self.max_pos)
+        nbytes = self.lib.tee_exit_river_prep_size(ctypes.byref(self.desc), self.n_layers, self.max_pos)
         if nbytes == 0:
             raise ValueError("invalid Exit River descriptor")
         self.prep = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
-        check("tee_exit_river_prepare", self.lib.tee_exit_river_prepare(ctypes.byref(self.desc), self.max_pos,
-                                                                        _ptr(self.prep), nbytes, _stream(self.device)))
+        check("tee_exit_river_prepare", self.lib.tee_exit_river_prepare(
+            ctypes.byref(self.desc), self.n_layers, self.layers, self.max_pos, _ptr(self.prep), nbytes,
+            _stream(self.device)))
 
     def workspace_bytes(self, n_max: int, max_pos: Optional[int] = None) -> int:
         return self.lib.tee_exit_river_workspace_size(ctypes.byref(self.desc), int(n_max),
