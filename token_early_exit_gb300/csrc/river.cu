@@ -48,10 +48,11 @@ struct RiverWs {
 
 constexpr int GT_N = 128;        // output columns per GEMM tile
 constexpr int GT_K = 64;         // inputs per k block
-constexpr int G_DQ_WARPS = 8;    // dequantising warps (then the epilogue)
-constexpr int G_PROD_WARP = 8;   // issues the TMA / bulk copies
-constexpr int G_MMA_WARP = 9;    // issues the MMAs, owns TMEM
-constexpr int G_THREADS = 320;
+constexpr int G_DQ_WARPS = 16;   // dequantising warps (then the epilogue)
+constexpr int G_PROD_WARP = G_DQ_WARPS;       // issues the TMA / bulk copies
+constexpr int G_MMA_WARP = G_DQ_WARPS + 1;    // issues the MMAs, owns TMEM
+constexpr int G_THREADS = (G_DQ_WARPS + 2) * 32;
+constexpr int G_DQ_PARTS = G_DQ_WARPS * 32 / 128;   // threads per column: each takes 32 / G_DQ_PARTS packed rows
 constexpr int G_EPI_THREADS = G_DQ_WARPS * 32;
 constexpr int G_S = 4;           // stages of two k blocks: A (TMA) + packed weights (one bulk copy)
 constexpr int G_BPS = 2;         // k blocks per stage
@@ -482,7 +483,8 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
             tc::umma_commit(acc_bar);   // every MMA issued has finished (also after a stop)
         }
     } else {
-        // dequantiser: column dq_n, half dq_h of each k block
+        // dequantiser: column dq_n, part dq_h of each k block (RPP packed rows, 2 RPP inputs)
+        constexpr int RPP = 32 / G_DQ_PARTS;
         const int dq_n = tid & 127, dq_h = tid >> 7;
         constexpr int c_pitch = GT_N;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -496,18 +498,18 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
             const float zs = -__half2float(sz[GT_N + dq_n]) * sc;
             // q -> float exactly as (2^23 + q) - 2^23 (a bit-or and a full-rate add, no
             // int-to-float conversion), then (q - z) s = q s + (-z s) in one fma
-            uint32_t w[16];
+            uint32_t w[RPP];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t cb = cs[(dq_h * 16 + i) * c_pitch];
+            for (int i = 0; i < RPP; ++i) {
+                const uint32_t cb = cs[(dq_h * RPP + i) * c_pitch];
                 const float lo = __uint_as_float(0x4B000000u | (cb & 15u)) - 8388608.0f;
                 const float hi = __uint_as_float(0x4B000000u | (cb >> 4)) - 8388608.0f;
                 w[i] = pack_bf16x2(fmaf(lo, sc, zs), fmaf(hi, sc, zs));
             }
             uint8_t* row = smem + G_OFF_B + b * G_B_BYTES + dq_n * 128;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int jj = dq_h * 4 + q;
+            for (int q = 0; q < RPP / 4; ++q) {
+                const int jj = dq_h * (RPP / 4) + q;
                 *reinterpret_cast<uint4*>(row + ((jj ^ (dq_n & 7)) << 4)) =
                     make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
@@ -525,10 +527,11 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     // lanes 32 (w % 4).., columns 64 (w / 4)..
     float* P = reinterpret_cast<float*>(smem + G_OFF_A);
     if (ok && warp < G_DQ_WARPS) {
+        constexpr int CW = GT_N / (G_DQ_WARPS / 4);   // columns per warp
         const int m = (warp & 3) * 32 + lane;
-        const int cb = (warp >> 2) * 64;
+        const int cb = (warp >> 2) * CW;
 #pragma unroll 1
-        for (int c = 0; c < 64; c += 32) {
+        for (int c = 0; c < CW; c += 32) {
             float v[32];
             tc::tmem_ld32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + cb + c, v);
             if (m < n) {
