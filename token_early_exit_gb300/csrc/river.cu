@@ -1003,7 +1003,7 @@ int max_clusters(int ks) {
 }
 
 template <int MODE>
-tee_status launch_gemm(const GemmArgs& g0, cudaStream_t s) {
+tee_status launch_gemm(const GemmArgs& g0, void* ws, cudaStream_t s) {
     GemmArgs g = g0;
     g.a_rows = std::min(G_A_ROWS, (g.n_max + 7) / 8 * 8);
     tee_status st = make_tmap_bf16_kblocks(&g.tm_a, g.a, G_A_ROWS, static_cast<uint64_t>(g.lda) * 2, g.K / GT_K,
@@ -1028,7 +1028,7 @@ tee_status launch_gemm(const GemmArgs& g0, cudaStream_t s) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = g.ks > 1 ? 1 : 0;
-    st = cuda_status(cudaLaunchKernelEx(&cfg, w4_gemm_kernel<MODE>, g, static_cast<void*>(nullptr)));
+    st = cuda_status(cudaLaunchKernelEx(&cfg, w4_gemm_kernel<MODE>, g, ws));
     return st != TEE_OK ? st : launch_status();
 }
 
@@ -1215,7 +1215,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         g.inv_width = 1.0f / d;
         g.ss_zero = nullptr;
         g.layer = L.cache_layer;
-        if ((st = launch_gemm<M_QKV>(g, s)) != TEE_OK) return st;
+        if ((st = launch_gemm<M_QKV>(g, ws, s)) != TEE_OK) return st;
         // attention
         at.layer = L.cache_layer;
         const dim3 agrid(at.chunks, D->n_kv_heads, n_max);
@@ -1233,7 +1233,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         g.next_a = abuf;
         g.ss_out = ss_f;
         g.h_out = nullptr;
-        if ((st = launch_gemm<M_O>(g, s)) != TEE_OK) return st;
+        if ((st = launch_gemm<M_O>(g, ws, s)) != TEE_OK) return st;
         // a = SiLU(x2 Wg) * (x2 Wu)
         g.blob = lbase + lp.gu;
         g.K = d;
@@ -1243,7 +1243,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         g.lda = d;
         g.ss_in = ss_f;
         g.ss_zero = ss_a;
-        if ((st = launch_gemm<M_GU>(g, s)) != TEE_OK) return st;
+        if ((st = launch_gemm<M_GU>(g, ws, s)) != TEE_OK) return st;
         // h2 = h1 + a Wd
         g.blob = lbase + lp.dn;
         g.K = f;
@@ -1264,7 +1264,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
             g.next_a = abuf;
             g.ss_out = ss_a;
         }
-        if ((st = launch_gemm<M_DOWN>(g, s)) != TEE_OK) return st;
+        if ((st = launch_gemm<M_DOWN>(g, ws, s)) != TEE_OK) return st;
     }
     return TEE_OK;
 }
