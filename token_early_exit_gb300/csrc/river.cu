@@ -442,19 +442,24 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
 
     if (warp == G_PROD_WARP) {
         // Stage j (blocks 2j, 2j + 1) -> slot j % G_S: both A tiles in one TMA (the
-        // k-blocks map) and both packed weight blocks in one bulk copy.
+        // k-blocks map) and both packed weight blocks in one bulk copy. Each tile
+        // walks its stages from a different one (when all stages hold two blocks),
+        // so that the tiles' CTAs, which all read the same A, ask for different A
+        // blocks at any time; the MMAs only sum, in that order.
         if (lane == 0) {
             const int nst = (nkb + G_BPS - 1) / G_BPS;
+            const int rot = nkb % G_BPS == 0 ? t % nst : 0;
             const uint8_t* wsrc = g.blob + (static_cast<int64_t>(t) * (g.K / GT_K) + k0 / GT_K) * G_W_BYTES;
             int j = 0;
             for (; j < nst; ++j) {
                 const int st = j % G_S;
                 if (j >= G_S && !tc::mbar_wait(&empty[st], ((j / G_S) - 1) & 1, abort, ws, 81)) break;
-                const int nb = min(G_BPS, nkb - j * G_BPS);
+                const int jr = (j + rot) % nst;   // the stage of the slice that slot j holds
+                const int nb = min(G_BPS, nkb - jr * G_BPS);
                 uint64_t* bar = &full[st];
                 tc::mbar_arrive_expect_tx(bar, G_BPS * g.a_rows * GT_K * 2 + nb * G_W_BYTES);
-                tc::tma_load_3d(smem + G_OFF_A + st * G_BPS * G_A_BYTES, &g.tm_a, 0, 0, k0 / GT_K + j * G_BPS, bar);
-                bulk_load(smem + G_OFF_W + st * G_BPS * G_W_BYTES, wsrc + static_cast<int64_t>(j) * G_BPS * G_W_BYTES,
+                tc::tma_load_3d(smem + G_OFF_A + st * G_BPS * G_A_BYTES, &g.tm_a, 0, 0, k0 / GT_K + jr * G_BPS, bar);
+                bulk_load(smem + G_OFF_W + st * G_BPS * G_W_BYTES, wsrc + static_cast<int64_t>(jr) * G_BPS * G_W_BYTES,
                           nb * G_W_BYTES, bar);
             }
             // stopped early: let the copies in flight land before the CTA moves on
