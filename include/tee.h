@@ -105,6 +105,16 @@ TEE_API tee_status tee_get_device_error(const void* ws, int32_t* code, int32_t* 
 /* Clear the device fault word of `ws` on `stream`, and every counter of the
  * header with it (the whole TEE_WS_HEADER_BYTES). */
 TEE_API tee_status tee_clear_device_error(void* ws, void* stream);
+
+/*
+ * Self-check of the failure-detection path: one block of 64 threads waits on an
+ * mbarrier that nothing completes, the same bounded wait every pipeline of the
+ * library uses, with a limit of limit_us microseconds (1 .. 100000). The waits
+ * give up, TEE_DEVERR_TIMEOUT with detail 99 is recorded in the workspace header
+ * (read it with tee_get_device_error) and the kernel returns: no fault, no hang,
+ * the context stays usable. TEE_ERR_INVALID_ARG for a limit outside the range.
+ */
+TEE_API tee_status tee_check_wait_timeout(void* ws, uint32_t limit_us, void* stream);
 /* Number of kernels this library has launched in this process (all threads). */
 TEE_API uint64_t tee_launch_count(void);
 

@@ -132,3 +132,36 @@ def test_fused_and_ridge_entry_points_check_on_the_host(lib):
     assert lib.tee_ridge_fit(64, 256, 256, fake, 256, fake, 256, _lib.TEE_BF16, 0.1, fake, 256, fake, 1024,
                              None) == _lib.TEE_ERR_WORKSPACE
     assert lib.tee_ridge_fit_workspace_size(64, 256, 256) > 256 * 256 * 4
+
+
+def test_wait_timeout_check_validates_on_the_host(lib):
+    from token_early_exit_gb300 import _lib
+    fake = ctypes.c_void_p(16)  # never dereferenced: the calls below fail their checks first
+    assert lib.tee_check_wait_timeout(None, 1000, None) == _lib.TEE_ERR_WORKSPACE
+    assert lib.tee_check_wait_timeout(fake, 0, None) == _lib.TEE_ERR_INVALID_ARG
+    assert lib.tee_check_wait_timeout(fake, 100001, None) == _lib.TEE_ERR_INVALID_ARG
+
+
+def test_exit_river_checks_on_the_host(lib):
+    from token_early_exit_gb300 import _lib
+    D = _lib.RiverDesc(d=2048, n_q_heads=32, n_kv_heads=8, head_dim=64, d_ff=8192, rope_base=5e5, eps=1e-5,
+                       group=64, flags=0)
+    assert lib.tee_exit_river_prep_size(ctypes.byref(D), 8, 4096) > 8 * 30_000_000
+    bad = _lib.RiverDesc(d=2048, n_q_heads=32, n_kv_heads=8, head_dim=96, d_ff=8192, rope_base=5e5, eps=1e-5,
+                         group=64, flags=0)
+    assert lib.tee_exit_river_prep_size(ctypes.byref(bad), 8, 4096) == 0   # head_dim 96 is not built
+    odd = _lib.RiverDesc(d=2048, n_q_heads=30, n_kv_heads=8, head_dim=64, d_ff=8192, rope_base=5e5, eps=1e-5,
+                         group=64, flags=0)
+    assert lib.tee_exit_river_prep_size(ctypes.byref(odd), 8, 4096) == 0   # q heads not a multiple of kv heads
+    layout = _lib.CacheLayout(s_layer=1 << 20, s_seq=1 << 14, s_head=4096 * 64, s_pos=64, n_layers=16, n_seq=64,
+                              n_heads=8, max_pos=4096)
+    fake = ctypes.c_void_p(16)
+    arr = (_lib.RiverLayer * 1)()
+    # more than 128 items
+    assert lib.tee_exit_river(ctypes.byref(D), 1, arr, fake, 1 << 30, 129, None, fake, 2048, 129, None, fake, None,
+                              fake, fake, ctypes.byref(layout), fake, 2048, fake, 1 << 30, None) == \
+        _lib.TEE_ERR_INVALID_ARG
+    # a layer without its norm weights
+    assert lib.tee_exit_river(ctypes.byref(D), 1, arr, fake, 1 << 30, 4, None, fake, 2048, 4, None, fake, None,
+                              fake, fake, ctypes.byref(layout), fake, 2048, fake, 1 << 30, None) == \
+        _lib.TEE_ERR_INVALID_ARG

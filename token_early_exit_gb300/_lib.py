@@ -70,6 +70,7 @@ SIGNATURES = {
     "tee_workspace_init": (c_int, [_P, c_size_t, _P]),
     "tee_get_device_error": (c_int, [_P, POINTER(c_int32), POINTER(c_int32), _P]),
     "tee_clear_device_error": (c_int, [_P, _P]),
+    "tee_check_wait_timeout": (c_int, [_P, ctypes.c_uint32, _P]),
     "tee_launch_count": (ctypes.c_uint64, []),
     "tee_exit_gate_workspace_size": (c_size_t, [POINTER(GateDesc), c_int32]),
     "tee_exit_gate": (c_int, [POINTER(GateDesc), c_int32, _P, c_int64, _P, c_int64, _P, _P, _P, _P, _P,

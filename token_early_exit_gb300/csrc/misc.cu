@@ -3,6 +3,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace tee {
 
@@ -26,6 +27,25 @@ int sm_count() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
     return n;
 }
+
+namespace {
+// The failure-detection path of the pipelines' waits: one block waits on an
+// mbarrier that nothing completes. Every wait gives up after limit_ns, the first
+// records TEE_DEVERR_TIMEOUT (detail 99) in the workspace header, and the kernel
+// returns; the context stays usable.
+constexpr int CHECK_WHERE = 99;
+__global__ void __launch_bounds__(64) wait_timeout_check_kernel(uint64_t limit_ns, void* ws) {
+    __shared__ uint64_t bar;
+    __shared__ volatile int abort;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        abort = 0;
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    (void)tc::mbar_wait_for(&bar, 0, &abort, ws, CHECK_WHERE, limit_ns, 1000);
+}
+}  // namespace
 
 }  // namespace tee
 
@@ -67,6 +87,13 @@ tee_status tee_get_device_error(const void* ws, int32_t* code, int32_t* detail, 
     if (code) *code = h[0];
     if (detail) *detail = h[1];
     return h[0] ? TEE_ERR_DEVICE : TEE_OK;
+}
+
+tee_status tee_check_wait_timeout(void* ws, uint32_t limit_us, void* stream) {
+    if (!ws) return TEE_ERR_WORKSPACE;
+    if (limit_us == 0 || limit_us > 100000) return TEE_ERR_INVALID_ARG;
+    wait_timeout_check_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(uint64_t(limit_us) * 1000, ws);
+    return launch_status();
 }
 
 tee_status tee_clear_device_error(void* ws, void* stream) {

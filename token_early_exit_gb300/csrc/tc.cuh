@@ -91,19 +91,23 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // mbarrier.try_wait (up to 20 us per attempt) instead of spinning, so that the
 // warps doing the work keep the issue slots.
 constexpr uint32_t WAIT_SUSPEND_NS = 20000;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, void* ws,
-                                          int where) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort, void* ws,
+                                              int where, uint64_t limit_ns, uint32_t suspend_ns) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait_sleep(bar, parity, WAIT_SUSPEND_NS)) return true;
+        if (mbar_try_wait_sleep(bar, parity, suspend_ns)) return true;
         if (*abort) return false;
-        if ((i & 7) == 7 && globaltimer() - t0 > WAIT_LIMIT_NS) {
+        if ((i & 7) == 7 && globaltimer() - t0 > limit_ns) {
             *abort = 1;
             record_fault(ws, TEE_DEVERR_TIMEOUT, where);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, void* ws,
+                                          int where) {
+    return mbar_wait_for(bar, parity, abort, ws, where, WAIT_LIMIT_NS, WAIT_SUSPEND_NS);
 }
 
 // ------------------------------------------------------------------ TMA

@@ -69,6 +69,12 @@ class Workspace:
             check("tee_get_device_error", st)
         return code.value, detail.value
 
+    def check_wait_timeout(self, limit_us: int = 1000):
+        """Run the library's bounded wait against a barrier that nothing completes
+        (tee_check_wait_timeout): the wait records a time-out here and returns."""
+        wp, wn = self.get(_lib.WS_HEADER_BYTES)
+        check("tee_check_wait_timeout", load().tee_check_wait_timeout(wp, int(limit_us), _stream(self.device)))
+
     def clear_error(self):
         if self.buf is not None:
             check("tee_clear_device_error", load().tee_clear_device_error(_ptr(self.buf), _stream(self.device)))
