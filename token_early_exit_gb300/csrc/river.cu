@@ -491,25 +491,32 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
         // dequantiser: column dq_n, part dq_h of each k block (RPP packed rows, 2 RPP inputs)
         constexpr int RPP = 32 / G_DQ_PARTS;
         const int dq_n = tid & 127, dq_h = tid >> 7;
-        constexpr int c_pitch = GT_N;
         for (int kb = 0; kb < nkb; ++kb) {
             const int j = kb / G_BPS, st = j % G_S, b = kb % G_RB;
             if (kb >= G_RB && !tc::mbar_wait(&bempty[b], ((kb / G_RB) - 1) & 1, abort, ws, 84)) break;
             if (!tc::mbar_wait(&full[st], (j / G_S) & 1, abort, ws, 85)) break;
             const uint8_t* wb = smem + G_OFF_W + (st * G_BPS + kb % G_BPS) * G_W_BYTES;
-            const uint8_t* cs = wb + dq_n;
             const __half* sz = reinterpret_cast<const __half*>(wb + 32 * GT_N);
             const float sc = __half2float(sz[dq_n]);
-            const float zs = -__half2float(sz[GT_N + dq_n]) * sc;
-            // q -> float exactly as (2^23 + q) - 2^23 (a bit-or and a full-rate add, no
-            // int-to-float conversion), then (q - z) s = q s + (-z s) in one fma
+            const __nv_bfloat162 s2 = __float2bfloat162_rn(sc);
+            const __nv_bfloat162 zs2 = __float2bfloat162_rn((8.0f - __half2float(sz[GT_N + dq_n])) * sc);
+            const __nv_bfloat162 k136 = __float2bfloat162_rn(136.0f);
+            // this thread's RPP packed rows of column dq_n: RPP consecutive bytes. A
+            // byte's two codes become the bf16 pair (128 + q_lo, 128 + q_hi) by a byte
+            // permute and a mask (exact), minus 136 gives q - 8 (exact), then
+            // (q - 8) s + (8 - z) s = (q - z) s in one bf16x2 fma.
             uint32_t w[RPP];
 #pragma unroll
-            for (int i = 0; i < RPP; ++i) {
-                const uint32_t cb = cs[(dq_h * RPP + i) * c_pitch];
-                const float lo = __uint_as_float(0x4B000000u | (cb & 15u)) - 8388608.0f;
-                const float hi = __uint_as_float(0x4B000000u | (cb >> 4)) - 8388608.0f;
-                w[i] = pack_bf16x2(fmaf(lo, sc, zs), fmaf(hi, sc, zs));
+            for (int wi = 0; wi < RPP / 4; ++wi) {
+                const uint32_t wl = *reinterpret_cast<const uint32_t*>(wb + dq_n * 32 + dq_h * RPP + 4 * wi);
+                const uint32_t wh = wl >> 4;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const uint32_t x = (__byte_perm(wl, wh, b | ((4 + b) << 8)) & 0x000F000Fu) | 0x43004300u;
+                    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&x);
+                    v = __hfma2(__hsub2(v, k136), s2, zs2);
+                    w[4 * wi + b] = *reinterpret_cast<const uint32_t*>(&v);
+                }
             }
             uint8_t* row = smem + G_OFF_B + b * G_B_BYTES + dq_n * 128;
 #pragma unroll
@@ -939,8 +946,9 @@ LayerPack layer_pack(const tee_river_desc& D) {
 }
 
 // Repack the segments of one GEMM (q|k|v, o, gate|up interleaved per tile as 64 +
-// 64 columns, down) into [tile][k block][codes 32 x 128 | scales 128 | zeros 128].
-// Grid (tiles, K / 64), 128 threads: thread c fills column c of the tile.
+// 64 columns, down) into [tile][k block][codes | scales 128 | zeros 128], the codes
+// of a block column by column ([128 columns][32 packed rows]: a column's 64 inputs
+// in 32 consecutive bytes). Grid (tiles, K / 64), 128 threads: thread c fills column c.
 __global__ void __launch_bounds__(128) w4_pack_kernel(W4Seg s0, W4Seg s1, W4Seg s2, int n_seg, int gu, int K,
                                                       uint8_t* __restrict__ blob) {
     const int t = blockIdx.x, kb = blockIdx.y, c = threadIdx.x;
@@ -963,8 +971,16 @@ __global__ void __launch_bounds__(128) w4_pack_kernel(W4Seg s0, W4Seg s1, W4Seg 
     }
     const W4Seg& sg = si == 0 ? s0 : (si == 1 ? s1 : s2);
     uint8_t* out = blob + (static_cast<int64_t>(t) * (K / GT_K) + kb) * G_W_BYTES;
-#pragma unroll 4
-    for (int r = 0; r < 32; ++r) out[r * GT_N + c] = sg.codes[static_cast<int64_t>(kb * 32 + r) * sg.n + col];
+    uint32_t word[8];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const uint32_t b = sg.codes[static_cast<int64_t>(kb * 32 + r) * sg.n + col];
+        if ((r & 3) == 0) word[r >> 2] = 0;
+        word[r >> 2] |= b << (8 * (r & 3));
+    }
+    uint4* oc = reinterpret_cast<uint4*>(out + c * 32);
+    oc[0] = make_uint4(word[0], word[1], word[2], word[3]);
+    oc[1] = make_uint4(word[4], word[5], word[6], word[7]);
     __half* o16 = reinterpret_cast<__half*>(out + 32 * GT_N);
     o16[c] = sg.scale[static_cast<int64_t>(kb) * sg.n + col];
     o16[GT_N + c] = sg.zero[static_cast<int64_t>(kb) * sg.n + col];
