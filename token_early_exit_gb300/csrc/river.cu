@@ -153,6 +153,7 @@ struct GatherArgs {
 };
 
 __global__ void __launch_bounds__(256) river_gather_kernel(GatherArgs a, void* ws) {
+    allow_dependents();
     const int m = blockIdx.x;
     if (m == 0)
         for (int i = threadIdx.x; i < a.n_cnt; i += blockDim.x) a.cnt[i] = 0;
@@ -416,8 +417,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t = blockIdx.x, sp = blockIdx.y;   // sp: the CTA's rank in its cluster
     const int n = item_count(g.n_max, g.n_dev);
-    if (g.ss_zero && t == 0 && sp == 0)
-        for (int i = tid; i < g.n_max; i += G_THREADS) g.ss_zero[i] = 0.f;
+    allow_dependents();   // the next kernel of the river may start launching
     if (n == 0) return;   // every CTA of the cluster leaves here
     const int kc = g.K / g.ks, k0 = sp * kc, nkb = kc / GT_K;
 
@@ -439,6 +439,12 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched early (programmatic dependent launch): the weights are constant, so
+    // the producer streams the first stages' weights before it waits for the
+    // previous kernel; everything else waits first.
+    if (!(warp == G_PROD_WARP && lane == 0)) wait_prior_grid();
+    if (g.ss_zero && t == 0 && sp == 0)
+        for (int i = tid; i < g.n_max; i += G_THREADS) g.ss_zero[i] = 0.f;
 
     if (warp == G_PROD_WARP) {
         // Stage j (blocks 2j, 2j + 1) -> slot j % G_S: both A tiles in one TMA (the
@@ -450,17 +456,28 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
             const int nst = (nkb + G_BPS - 1) / G_BPS;
             const int rot = nkb % G_BPS == 0 ? t % nst : 0;
             const uint8_t* wsrc = g.blob + (static_cast<int64_t>(t) * (g.K / GT_K) + k0 / GT_K) * G_W_BYTES;
-            int j = 0;
+            auto issue_w = [&](int j) {   // arm slot j % G_S and bring its weights
+                const int st = j % G_S, jr = (j + rot) % nst;
+                const int nb = min(G_BPS, nkb - jr * G_BPS);
+                tc::mbar_arrive_expect_tx(&full[st], G_BPS * g.a_rows * GT_K * 2 + nb * G_W_BYTES);
+                bulk_load(smem + G_OFF_W + st * G_BPS * G_W_BYTES, wsrc + static_cast<int64_t>(jr) * G_BPS * G_W_BYTES,
+                          nb * G_W_BYTES, &full[st]);
+            };
+            auto issue_a = [&](int j) {   // the stage's A tiles (written by the previous kernel)
+                const int st = j % G_S, jr = (j + rot) % nst;
+                tc::tma_load_3d(smem + G_OFF_A + st * G_BPS * G_A_BYTES, &g.tm_a, 0, 0, k0 / GT_K + jr * G_BPS,
+                                &full[st]);
+            };
+            const int pre = min(nst, G_S);
+            for (int j = 0; j < pre; ++j) issue_w(j);
+            wait_prior_grid();
+            for (int j = 0; j < pre; ++j) issue_a(j);
+            int j = pre;
             for (; j < nst; ++j) {
                 const int st = j % G_S;
-                if (j >= G_S && !tc::mbar_wait(&empty[st], ((j / G_S) - 1) & 1, abort, ws, 81)) break;
-                const int jr = (j + rot) % nst;   // the stage of the slice that slot j holds
-                const int nb = min(G_BPS, nkb - jr * G_BPS);
-                uint64_t* bar = &full[st];
-                tc::mbar_arrive_expect_tx(bar, G_BPS * g.a_rows * GT_K * 2 + nb * G_W_BYTES);
-                tc::tma_load_3d(smem + G_OFF_A + st * G_BPS * G_A_BYTES, &g.tm_a, 0, 0, k0 / GT_K + jr * G_BPS, bar);
-                bulk_load(smem + G_OFF_W + st * G_BPS * G_W_BYTES, wsrc + static_cast<int64_t>(jr) * G_BPS * G_W_BYTES,
-                          nb * G_W_BYTES, bar);
+                if (!tc::mbar_wait(&empty[st], ((j / G_S) - 1) & 1, abort, ws, 81)) break;
+                issue_w(j);
+                issue_a(j);
             }
             // stopped early: let the copies in flight land before the CTA moves on
             const uint64_t t0 = tc::globaltimer();
@@ -636,8 +653,10 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
 
     const int c = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    allow_dependents();
     const int n = item_count(a.n_max, a.n_dev);
     if (m >= n) return;
+    wait_prior_grid();   // q, the item table and the cache slots come from the q|k|v GEMM
     const int pm = a.ipos[m];
     bf16* out = a.obuf + static_cast<int64_t>(m) * a.qw + static_cast<int64_t>(g) * REP * HD;
     if (pm < 0) {   // a skipped item attends to nothing
@@ -881,8 +900,18 @@ tee_status launch_attn_rep(const AttnArgs& a, dim3 grid, cudaStream_t s) {
         if (st != TEE_OK) return st;
         attr = true;
     }
-    river_attn_kernel<HD, REP><<<grid, AT_THREADS, bytes, s>>>(a);
-    return launch_status();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(AT_THREADS);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, river_attn_kernel<HD, REP>, a));
+    return st != TEE_OK ? st : launch_status();
 }
 
 template <int HD>
@@ -1042,13 +1071,15 @@ tee_status launch_gemm(const GemmArgs& g0, void* ws, cudaStream_t s) {
     cfg.blockDim = dim3(G_THREADS);
     cfg.dynamicSmemBytes = G_SMEM;
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 1;
-    at[0].val.clusterDim.y = g.ks;
-    at[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = 1;
+    at[1].val.clusterDim.y = g.ks;
+    at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
-    cfg.numAttrs = g.ks > 1 ? 1 : 0;
+    cfg.numAttrs = g.ks > 1 ? 2 : 1;
     st = cuda_status(cudaLaunchKernelEx(&cfg, w4_gemm_kernel<MODE>, g, ws));
     return st != TEE_OK ? st : launch_status();
 }
