@@ -7,10 +7,10 @@
 //                       sum(h^2) per item; item checks; counters cleared
 //   w4_gemm<QKV>        [q|k|v] = (h * g) . [Wq|Wk|Wv], times 1/rms(h); RoPE on
 //                       q and k; q to the workspace, k and v to the cache slot
-//   river_attn          per (item, kv head, chunk of 256 / 128 positions):
-//                       scores, partial softmax and P.V on the CUDA cores (a
-//                       bandwidth-bound read of the cache); the last chunk of an
-//                       (item, kv head) merges the partials
+//   river_attn          per (item, kv head, chunk of 256 / 128 positions): TMA
+//                       brings the chunk's K and V; scores, partial softmax and
+//                       P.V on the CUDA cores; the last chunk of an (item, kv
+//                       head) merges the partials
 //   w4_gemm<O>          h1 = h + o . Wo; bf16 (h1 * ffn_norm) and sum(h1^2)
 //   w4_gemm<GU>         gate | up from (h1 * g2) . [Wg|Wu] (64 columns of each
 //                       per tile), times 1/rms(h1); a = SiLU(gate) * up (bf16)
@@ -21,13 +21,13 @@
 // kernel accumulated in fp32.
 //
 // w4_gemm (tcgen05): a CTA computes a 128-column tile for every item (M = 128
-// TMEM lanes, items <= 128) over a 1/ks slice of the inputs. cp.async brings
-// the int4 codes (a deep ring: the weights are the DRAM traffic), the fp16
-// scales/zeros and the bf16 A tile (128-byte swizzle); every thread then
-// dequantises 32 weights of the 128 x 64 B tile into shared memory, and one
-// thread issues four 128x128x16 MMAs into TMEM. Split-K partials go to the
-// workspace; the CTA that finishes a tile last (an arrival counter) sums them
-// in split order and runs the epilogue.
+// TMEM lanes, items <= 128) over a 1/ks slice of the inputs; the ks CTAs of a
+// tile are one cluster. A producer warp brings each stage of two 64-input blocks
+// (the A tiles by one TMA box, the packed int4 weights -- repacked per tile at
+// prepare time -- by one bulk copy); sixteen warps dequantise each block into a
+// B buffer; one thread issues four 128x128x16 MMAs into TMEM. The CTAs then
+// reduce their partial tiles through distributed shared memory, each finishing
+// its share of the columns with the mode's epilogue.
 #include <algorithm>
 
 #include "fill.cuh"
@@ -397,11 +397,11 @@ __device__ void finish_tile(const GemmArgs& g, const float* P, int t, int n, int
 }
 
 // One 128-column tile over a 1/ks slice of the inputs; the ks CTAs of a tile are a
-// cluster. Warp 8 streams A (TMA), the int4 codes (TMA) and scales/zeros (bulk)
-// into a G_S-stage ring; warps 0-7 dequantise each block into one of G_RB B
-// buffers; warp 9 issues the MMAs. Then every CTA stages its fp32 partial tile in
-// shared memory and, after a cluster barrier, finishes its share of the tile's
-// columns from the ks partials (DSMEM reads).
+// cluster. Warp G_PROD_WARP streams each stage (A by TMA, the packed weights by a
+// bulk copy) into a G_S-stage ring; the G_DQ_WARPS dequantising warps turn each
+// block into one of G_RB B buffers; warp G_MMA_WARP issues the MMAs. Then every
+// CTA stages its fp32 partial tile in shared memory and, after a cluster barrier,
+// finishes its share of the tile's columns from the ks partials (DSMEM reads).
 template <int MODE>
 __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_constant__ GemmArgs g, void* ws) {
     extern __shared__ uint8_t smem_raw[];
