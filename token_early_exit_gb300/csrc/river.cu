@@ -43,7 +43,7 @@ constexpr uint32_t RIVER_MAGIC = 0x54455256u;  // "TERV"
 
 // ------------------------------------------------------------------ workspace
 struct RiverWs {
-    size_t resid, abuf, qbuf, obuf, act, ss_a, ss_f, ipos, iseq, gcnt, acnt, apart, end;
+    size_t resid, abuf, qbuf, obuf, act, ss_a, ss_f, ipos, iseq, acnt, apart, end;
 };
 
 constexpr int GT_N = 128;        // output columns per GEMM tile
@@ -75,13 +75,6 @@ static_assert(G_SMEM <= 232448, "shared memory");
 
 constexpr int MAX_KS = 8;        // K splits = CTAs of a cluster (portable size)
 constexpr int MAX_ITEMS = 128;
-
-int max_tiles(const tee_river_desc& D) {
-    const int qkv = (D.n_q_heads + 2 * D.n_kv_heads) * D.head_dim / GT_N;
-    const int gu = D.d_ff / 64;
-    const int dd = D.d / GT_N;
-    return std::max(qkv, std::max(gu, dd));
-}
 
 int at_chunk(int hd) { return hd == 64 ? 256 : 128; }
 
@@ -121,7 +114,6 @@ RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
     w.ss_f = take(n * 4);
     w.ipos = take(n * 4);
     w.iseq = take(n * 4);
-    w.gcnt = take(static_cast<size_t>(max_tiles(D)) * 4);
     w.acnt = take(n * D.n_kv_heads * 4);
     w.apart = take(n * D.n_kv_heads * chunks * rep * (D.head_dim + 2) * 4);
     w.end = o;
@@ -148,7 +140,7 @@ struct GatherArgs {
     float* ss_f;
     int32_t* ipos;
     int32_t* iseq;
-    int32_t* cnt;   // GEMM tile counters then attention counters
+    int32_t* cnt;   // the attention's arrival counters
     int n_cnt;
 };
 
@@ -1183,7 +1175,6 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     float* ss_f = ws_at<float>(ws, w.ss_f);
     int32_t* ipos = ws_at<int32_t>(ws, w.ipos);
     int32_t* iseq = ws_at<int32_t>(ws, w.iseq);
-    int32_t* gcnt = ws_at<int32_t>(ws, w.gcnt);
     int32_t* acnt = ws_at<int32_t>(ws, w.acnt);
 
     GatherArgs ga{};
@@ -1205,8 +1196,8 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     ga.ss_f = ss_f;
     ga.ipos = ipos;
     ga.iseq = iseq;
-    ga.cnt = gcnt;
-    ga.n_cnt = static_cast<int>((w.acnt - w.gcnt) / 4 + static_cast<size_t>(n_max) * D->n_kv_heads);
+    ga.cnt = acnt;
+    ga.n_cnt = n_max * D->n_kv_heads;
     river_gather_kernel<<<n_max, 256, 0, s>>>(ga, ws);
     if ((st = launch_status()) != TEE_OK) return st;
 
