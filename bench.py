@@ -556,6 +556,12 @@ def max_over_ranks(x: float, world: int, dev) -> float:
     return float(t.item())
 
 
+def job_throughput(units_per_rank: float, world: int, t_ms: float) -> float:
+    """Whole-job units/s: every rank processes its own batch (weak scaling), and the
+    step time is the slowest rank's."""
+    return world * units_per_rank / (t_ms * 1e-3)
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -695,7 +701,7 @@ def run_gpu(args):
                             "frac": gbs / peaks()["hbm_gbs"], "launches": int(k1)}
     t_step = statistics.mean(step_ms)
     t_step = max_over_ranks(t_step, world, dev)
-    value = world * w.units / (t_step * 1e-3)
+    value = job_throughput(w.units, world, t_step)
 
     # end to end: pinned host inputs -> device -> step -> result back to the host, per step
     bi, bo = w.host_io()
@@ -739,7 +745,7 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "bf16" if w.config().get("workload") != configs.TINY_DECODE.name else "f32",
             "data": "synthetic", "config": w.config(), "exits_per_step": n_exit,
             "roofline": roof, "cpu_baseline": cpu,
-            "e2e": {"value": world * w.units / (t_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+            "e2e": {"value": job_throughput(w.units, world, t_e2e), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": t_e2e},
             "gpu_launches": int(launches), "launches_per_step": int(k_step), "clocks": clk,
             **({"kernels": per_kernel} if per_kernel else {}),
