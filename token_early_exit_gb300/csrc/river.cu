@@ -595,7 +595,10 @@ struct AttnArgs {
 };
 
 constexpr int AT_THREADS = 128;
-constexpr int AT_BOX = 64;   // positions per TMA box
+// positions per TMA box: the whole chunk in one copy (a copy costs about the same
+// whatever its size; the last chunk of a sequence reads up to CHUNK - 1 rows it
+// does not use)
+__host__ __device__ constexpr int at_box(int hd) { return hd == 64 ? 256 : 128; }
 
 template <int HD, int REP>
 struct AttnSmem {
@@ -664,6 +667,7 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
         tc::mbar_init(vbar, 1);
         *abort = 0;
         tc::fence_barrier_init();
+        constexpr int AT_BOX = at_box(HD);
         const int nb = (cnt + AT_BOX - 1) / AT_BOX;
         const uint32_t bytes = static_cast<uint32_t>(nb) * (HD / 64) * AT_BOX * 128;
         const int sq = a.iseq[m];
@@ -1231,8 +1235,8 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     at.qbuf = qbuf;
     at.ipos = ipos;
     at.iseq = iseq;
-    if ((st = make_tmap_cache(&at.kmap, k_cache, hd, cl, AT_BOX)) != TEE_OK) return st;
-    if ((st = make_tmap_cache(&at.vmap, v_cache, hd, cl, AT_BOX)) != TEE_OK) return st;
+    if ((st = make_tmap_cache(&at.kmap, k_cache, hd, cl, at_box(hd))) != TEE_OK) return st;
+    if ((st = make_tmap_cache(&at.vmap, v_cache, hd, cl, at_box(hd))) != TEE_OK) return st;
     at.qscale = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
     at.part = ws_at<float>(ws, w.apart);
     at.cnt = acnt;
