@@ -54,9 +54,10 @@ constexpr int G_MMA_WARP = G_DQ_WARPS + 1;    // issues the MMAs, owns TMEM
 constexpr int G_THREADS = (G_DQ_WARPS + 2) * 32;
 constexpr int G_DQ_PARTS = G_DQ_WARPS * 32 / 128;   // threads per column: each takes 32 / G_DQ_PARTS packed rows
 constexpr int G_EPI_THREADS = G_DQ_WARPS * 32;
-constexpr int G_S = 4;           // stages of two k blocks: A (TMA) + packed weights (one bulk copy)
+constexpr int G_S = 3;           // stages of two k blocks: A (TMA) + packed weights (one bulk copy)
 constexpr int G_BPS = 2;         // k blocks per stage
-constexpr int G_RB = 3;          // dequantised B buffers
+constexpr int G_BP = 2;          // B stages (a stage's k blocks dequantised), one barrier pair each
+constexpr int G_RB = G_BP * G_BPS;   // dequantised B buffers
 constexpr int G_A_ROWS = 128;    // A tile rows (TMEM lanes); A buffers hold 128 rows
 constexpr uint32_t G_A_BYTES = G_A_ROWS * GT_K * 2;  // 16 KB: 128 rows x 64 bf16, 128-byte swizzle
 constexpr uint32_t G_B_BYTES = GT_N * GT_K * 2;      // 16 KB
@@ -66,7 +67,7 @@ constexpr uint32_t G_OFF_A = 0;
 constexpr uint32_t G_OFF_B = G_OFF_A + G_S * G_BPS * G_A_BYTES;
 constexpr uint32_t G_OFF_W = G_OFF_B + G_RB * G_B_BYTES;
 constexpr uint32_t G_OFF_BAR = G_OFF_W + G_S * G_BPS * G_W_BYTES;
-constexpr size_t G_SMEM = 1024 + G_OFF_BAR + (2 * G_S + 2 * G_RB + 1) * 8 + 16;
+constexpr size_t G_SMEM = 1024 + G_OFF_BAR + (2 * G_S + 2 * G_BP + 1) * 8 + 16;
 // the CTA's partial tile after the loop: [128 rows][GT_N + 4] fp32, over the A ring
 constexpr int G_P_PITCH = GT_N + 4;
 static_assert(G_A_ROWS * G_P_PITCH * 4 <= G_S * G_BPS * G_A_BYTES, "partial tile fits the A ring");
@@ -388,10 +389,61 @@ __device__ void finish_tile(const GemmArgs& g, const float* P, int t, int n, int
     }
 }
 
+// NB consecutive packed weight blocks (G_W_BYTES apart from wst) -> NB bf16 B
+// buffers (G_B_BYTES apart from bst): this thread's RPP packed rows of column dq_n
+// in each. A byte's two codes become the bf16 pair (128 + q_lo, 128 + q_hi) by a
+// byte permute and a mask (exact), minus 136 gives q - 8 (exact), then
+// (q - 8) s + (8 - z) s = (q - z) s in one bf16x2 fma. All loads of the NB blocks
+// are issued before any arithmetic.
+template <int NB>
+__device__ __forceinline__ void dequant_blocks(const uint8_t* wst, uint8_t* bst, int dq_n, int dq_h) {
+    constexpr int RPP = 32 / G_DQ_PARTS;
+    uint32_t wl[NB][RPP / 4];
+    __half sh[NB], zh[NB];
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) {
+        const uint8_t* wb = wst + bb * G_W_BYTES;
+        const __half* sz = reinterpret_cast<const __half*>(wb + 32 * GT_N);
+        sh[bb] = sz[dq_n];
+        zh[bb] = sz[GT_N + dq_n];
+#pragma unroll
+        for (int wi = 0; wi < RPP / 4; ++wi)
+            wl[bb][wi] = *reinterpret_cast<const uint32_t*>(wb + dq_n * 32 + dq_h * RPP + 4 * wi);
+    }
+    const __nv_bfloat162 k136 = __float2bfloat162_rn(136.0f);
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) {
+        const float sc = __half2float(sh[bb]);
+        const __nv_bfloat162 s2 = __float2bfloat162_rn(sc);
+        const __nv_bfloat162 zs2 = __float2bfloat162_rn((8.0f - __half2float(zh[bb])) * sc);
+        uint32_t w[RPP];
+#pragma unroll
+        for (int wi = 0; wi < RPP / 4; ++wi) {
+            const uint32_t lo = wl[bb][wi], hi = lo >> 4;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const uint32_t x = (__byte_perm(lo, hi, b | ((4 + b) << 8)) & 0x000F000Fu) | 0x43004300u;
+                __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&x);
+                v = __hfma2(__hsub2(v, k136), s2, zs2);
+                w[4 * wi + b] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+        }
+        uint8_t* row = bst + bb * G_B_BYTES + dq_n * 128;
+#pragma unroll
+        for (int q = 0; q < RPP / 4; ++q) {
+            const int jj = dq_h * (RPP / 4) + q;
+            *reinterpret_cast<uint4*>(row + ((jj ^ (dq_n & 7)) << 4)) =
+                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+    }
+}
+
 // One 128-column tile over a 1/ks slice of the inputs; the ks CTAs of a tile are a
 // cluster. Warp G_PROD_WARP streams each stage (A by TMA, the packed weights by a
 // bulk copy) into a G_S-stage ring; the G_DQ_WARPS dequantising warps turn each
-// block into one of G_RB B buffers; warp G_MMA_WARP issues the MMAs. Then every
+// stage's blocks into one of G_BP B stages (one wait and one arrival per stage,
+// the two blocks' loads and arithmetic interleaved); warp G_MMA_WARP issues the
+// MMAs. Then every
 // CTA stages its fp32 partial tile in shared memory and, after a cluster barrier,
 // finishes its share of the tile's columns from the ks partials (DSMEM reads).
 template <int MODE>
@@ -400,9 +452,9 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + G_OFF_BAR);   // [G_S]
     uint64_t* empty = full + G_S;                                       // [G_S]
-    uint64_t* bfull = empty + G_S;                                      // [G_RB]
-    uint64_t* bempty = bfull + G_RB;                                    // [G_RB]
-    uint64_t* acc_bar = bempty + G_RB;
+    uint64_t* bfull = empty + G_S;                                      // [G_BP]
+    uint64_t* bempty = bfull + G_BP;                                    // [G_BP]
+    uint64_t* acc_bar = bempty + G_BP;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -418,7 +470,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
             tc::mbar_init(&full[i], 1);
             tc::mbar_init(&empty[i], 1);
         }
-        for (int i = 0; i < G_RB; ++i) {
+        for (int i = 0; i < G_BP; ++i) {
             tc::mbar_init(&bfull[i], G_DQ_WARPS);
             tc::mbar_init(&bempty[i], 1);
         }
@@ -480,63 +532,45 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     } else if (warp == G_MMA_WARP) {
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_bf16(128, GT_N);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int j = kb / G_BPS, st = j % G_S, b = kb % G_RB;
+            const int nst = (nkb + G_BPS - 1) / G_BPS;
+            for (int j = 0; j < nst; ++j) {
+                const int st = j % G_S, bp = j % G_BP;
                 if (!tc::mbar_wait(&full[st], (j / G_S) & 1, abort, ws, 82)) break;
-                if (!tc::mbar_wait(&bfull[b], (kb / G_RB) & 1, abort, ws, 83)) break;
+                if (!tc::mbar_wait(&bfull[bp], (j / G_BP) & 1, abort, ws, 83)) break;
                 tc::tc_fence_after();
-                // the stage's blocks land a_rows x 128 bytes apart (one TMA box)
-                const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_A + st * G_BPS * G_A_BYTES +
-                                                                     (kb % G_BPS) * g.a_rows * 128));
-                const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_B + b * G_B_BYTES));
+                for (int bb = 0; bb < G_BPS && j * G_BPS + bb < nkb; ++bb) {
+                    const int kb = j * G_BPS + bb;
+                    // the stage's blocks land a_rows x 128 bytes apart (one TMA box)
+                    const uint64_t ad = tc::smem_desc_sw128(
+                        tc::smem_u32(smem + G_OFF_A + st * G_BPS * G_A_BYTES + bb * g.a_rows * 128));
+                    const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_B + (bp * G_BPS + bb) * G_B_BYTES));
 #pragma unroll
-                for (int kk = 0; kk < GT_K / 16; ++kk) tc::umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, kb | kk);
-                tc::umma_commit(&bempty[b]);
-                if (kb % G_BPS == G_BPS - 1 || kb == nkb - 1) tc::umma_commit(&empty[st]);
+                    for (int kk = 0; kk < GT_K / 16; ++kk)
+                        tc::umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, kb | kk);
+                }
+                tc::umma_commit(&bempty[bp]);
+                tc::umma_commit(&empty[st]);
             }
             tc::umma_commit(acc_bar);   // every MMA issued has finished (also after a stop)
         }
     } else {
-        // dequantiser: column dq_n, part dq_h of each k block (RPP packed rows, 2 RPP inputs)
-        constexpr int RPP = 32 / G_DQ_PARTS;
+        // dequantiser: column dq_n, part dq_h of each k block (RPP packed rows, 2 RPP
+        // inputs), both blocks of a stage per pass
         const int dq_n = tid & 127, dq_h = tid >> 7;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int j = kb / G_BPS, st = j % G_S, b = kb % G_RB;
-            if (kb >= G_RB && !tc::mbar_wait(&bempty[b], ((kb / G_RB) - 1) & 1, abort, ws, 84)) break;
+        const int nst = (nkb + G_BPS - 1) / G_BPS;
+        for (int j = 0; j < nst; ++j) {
+            const int st = j % G_S, bp = j % G_BP;
+            if (j >= G_BP && !tc::mbar_wait(&bempty[bp], ((j / G_BP) - 1) & 1, abort, ws, 84)) break;
             if (!tc::mbar_wait(&full[st], (j / G_S) & 1, abort, ws, 85)) break;
-            const uint8_t* wb = smem + G_OFF_W + (st * G_BPS + kb % G_BPS) * G_W_BYTES;
-            const __half* sz = reinterpret_cast<const __half*>(wb + 32 * GT_N);
-            const float sc = __half2float(sz[dq_n]);
-            const __nv_bfloat162 s2 = __float2bfloat162_rn(sc);
-            const __nv_bfloat162 zs2 = __float2bfloat162_rn((8.0f - __half2float(sz[GT_N + dq_n])) * sc);
-            const __nv_bfloat162 k136 = __float2bfloat162_rn(136.0f);
-            // this thread's RPP packed rows of column dq_n: RPP consecutive bytes. A
-            // byte's two codes become the bf16 pair (128 + q_lo, 128 + q_hi) by a byte
-            // permute and a mask (exact), minus 136 gives q - 8 (exact), then
-            // (q - 8) s + (8 - z) s = (q - z) s in one bf16x2 fma.
-            uint32_t w[RPP];
-#pragma unroll
-            for (int wi = 0; wi < RPP / 4; ++wi) {
-                const uint32_t wl = *reinterpret_cast<const uint32_t*>(wb + dq_n * 32 + dq_h * RPP + 4 * wi);
-                const uint32_t wh = wl >> 4;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const uint32_t x = (__byte_perm(wl, wh, b | ((4 + b) << 8)) & 0x000F000Fu) | 0x43004300u;
-                    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&x);
-                    v = __hfma2(__hsub2(v, k136), s2, zs2);
-                    w[4 * wi + b] = *reinterpret_cast<const uint32_t*>(&v);
-                }
-            }
-            uint8_t* row = smem + G_OFF_B + b * G_B_BYTES + dq_n * 128;
-#pragma unroll
-            for (int q = 0; q < RPP / 4; ++q) {
-                const int jj = dq_h * (RPP / 4) + q;
-                *reinterpret_cast<uint4*>(row + ((jj ^ (dq_n & 7)) << 4)) =
-                    make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-            }
+            const uint8_t* wst = smem + G_OFF_W + st * G_BPS * G_W_BYTES;
+            uint8_t* bst = smem + G_OFF_B + bp * G_BPS * G_B_BYTES;
+            if (nkb - j * G_BPS >= 2)
+                dequant_blocks<2>(wst, bst, dq_n, dq_h);
+            else
+                dequant_blocks<1>(wst, bst, dq_n, dq_h);
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bfull[b]);
+            if (lane == 0) tc::mbar_arrive(&bfull[bp]);
         }
     }
     // the accumulator is final
