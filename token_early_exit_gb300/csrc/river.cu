@@ -49,28 +49,41 @@ struct RiverWs {
 constexpr int GT_N = 128;        // output columns per GEMM tile
 constexpr int GT_K = 64;         // inputs per k block
 constexpr int G_DQ_WARPS = 16;   // dequantising warps (then the epilogue)
-constexpr int G_PROD_WARP = G_DQ_WARPS;       // issues the TMA / bulk copies
+constexpr int G_PROD_WARP = G_DQ_WARPS;       // issues the weights' bulk copies
 constexpr int G_MMA_WARP = G_DQ_WARPS + 1;    // issues the MMAs, owns TMEM
-constexpr int G_THREADS = (G_DQ_WARPS + 2) * 32;
-constexpr int G_DQ_PARTS = G_DQ_WARPS * 32 / 128;   // threads per column: each takes 32 / G_DQ_PARTS packed rows
+constexpr int G_A_WARP = G_DQ_WARPS + 2;      // issues the A tiles' TMA copies
+constexpr int G_THREADS = (G_DQ_WARPS + 3) * 32;
+constexpr int G_DQ_GROUPS = 2;   // dequantising groups; group q takes the stages j with j % G_DQ_GROUPS == q
+constexpr int G_DQ_GWARPS = G_DQ_WARPS / G_DQ_GROUPS;
+constexpr int G_DQ_PARTS = G_DQ_GWARPS * 32 / 128;   // threads per column: each takes 32 / G_DQ_PARTS packed rows
 constexpr int G_EPI_THREADS = G_DQ_WARPS * 32;
-constexpr int G_S = 3;           // stages of two k blocks: A (TMA) + packed weights (one bulk copy)
+// A stage = two k blocks (G_BPS). Three rings, each with its own full / empty
+// barriers: the packed weights (G_WS stages, released by the dequantising group
+// once it has read them), the A tiles (released by the MMAs: 4 stages of two
+// tiles of up to 64 item rows, 2 stages of up to 128 rows above), and the
+// dequantised B tiles (G_BP stages, released by the MMAs). The MMA is transposed:
+// M = the tile's 128 output columns (the dequantised weights), N = the item rows
+// (a multiple of 16), so the accumulator holds [column][item], the tensor core
+// does no work for absent items and reads no rows past them.
 constexpr int G_BPS = 2;         // k blocks per stage
-constexpr int G_BP = 2;          // B stages (a stage's k blocks dequantised), one barrier pair each
+constexpr int G_WS = 6;          // weight stages
+constexpr int G_AS_MAX = 4;      // A stages (64-row tiles; 2 with 128-row tiles)
+constexpr int G_BP = 3;          // B stages
 constexpr int G_RB = G_BP * G_BPS;   // dequantised B buffers
-constexpr int G_A_ROWS = 128;    // A tile rows (TMEM lanes); A buffers hold 128 rows
-constexpr uint32_t G_A_BYTES = G_A_ROWS * GT_K * 2;  // 16 KB: 128 rows x 64 bf16, 128-byte swizzle
+constexpr int G_A_ROWS = 128;    // A tile rows (the MMA's N) at most
+constexpr uint32_t G_A_REGION = 64 * 1024;   // the A ring
 constexpr uint32_t G_B_BYTES = GT_N * GT_K * 2;      // 16 KB
 // a packed weight block: codes [32 packed rows][128 columns], then 128 fp16 scales, 128 fp16 zeros
 constexpr uint32_t G_W_BYTES = 32 * GT_N + 2 * GT_N * 2;   // 4608
 constexpr uint32_t G_OFF_A = 0;
-constexpr uint32_t G_OFF_B = G_OFF_A + G_S * G_BPS * G_A_BYTES;
+constexpr uint32_t G_OFF_B = G_OFF_A + G_A_REGION;
 constexpr uint32_t G_OFF_W = G_OFF_B + G_RB * G_B_BYTES;
-constexpr uint32_t G_OFF_BAR = G_OFF_W + G_S * G_BPS * G_W_BYTES;
-constexpr size_t G_SMEM = 1024 + G_OFF_BAR + (2 * G_S + 2 * G_BP + 1) * 8 + 16;
-// the CTA's partial tile after the loop: [128 rows][GT_N + 4] fp32, over the A ring
+constexpr uint32_t G_OFF_BAR = G_OFF_W + G_WS * G_BPS * G_W_BYTES;
+constexpr size_t G_SMEM = 1024 + G_OFF_BAR + (2 * G_WS + 2 * G_AS_MAX + 2 * G_BP + 1) * 8 + 16;
+// the CTA's partial tile after the loop: [128 rows][GT_N + 4] fp32, over the B ring
 constexpr int G_P_PITCH = GT_N + 4;
-static_assert(G_A_ROWS * G_P_PITCH * 4 <= G_S * G_BPS * G_A_BYTES, "partial tile fits the A ring");
+static_assert(G_A_ROWS * G_P_PITCH * 4 <= G_RB * G_B_BYTES, "partial tile fits the B ring");
+static_assert(G_AS_MAX * G_BPS * 64 * 128 == G_A_REGION && 2 * G_BPS * G_A_ROWS * 128 == G_A_REGION, "A ring");
 static_assert(G_OFF_B % 1024 == 0 && G_OFF_W % 16 == 0 && G_OFF_BAR % 8 == 0, "alignment");
 static_assert(G_SMEM <= 232448, "shared memory");
 
@@ -221,15 +234,15 @@ struct W4Seg {
 };
 
 struct GemmArgs {
-    CUtensorMap tm_a;       // A [128][K] bf16 as K/64 blocks, box 2 blocks x 128 rows x 64, 128-byte swizzle
+    CUtensorMap tm_a;       // A [128][K] bf16 as K/64 blocks, box 2 blocks x a_rows x 64, 128-byte swizzle
     const uint8_t* blob;    // packed weights [tile][K/64][G_W_BYTES]
     int K, N, ks;
     int n_max;
     const int32_t* n_dev;
     const bf16* a;          // [128][lda]
     int64_t lda;
-    int a_rows;             // rows of A that TMA brings (the item bound rounded up to 8; the rest of the
-                            // 128 MMA rows read stale shared memory and feed only unused TMEM lanes)
+    int a_rows;             // rows of A that TMA brings = the MMA's N (the item bound rounded up to 16;
+                            // rows past the items feed only accumulator columns that are never read)
     float* ss_zero;         // cleared by CTA (0, 0): the next producer accumulates into it
     // row scale of the normalised input: rs = 1 / sqrt(ss_in / width + eps)
     const float* ss_in;
@@ -398,6 +411,7 @@ __device__ void finish_tile(const GemmArgs& g, const float* P, int t, int n, int
 template <int NB>
 __device__ __forceinline__ void dequant_blocks(const uint8_t* wst, uint8_t* bst, int dq_n, int dq_h) {
     constexpr int RPP = 32 / G_DQ_PARTS;
+    static_assert(RPP == 16, "one 16-byte load of packed rows per block");
     uint32_t wl[NB][RPP / 4];
     __half sh[NB], zh[NB];
 #pragma unroll
@@ -406,9 +420,11 @@ __device__ __forceinline__ void dequant_blocks(const uint8_t* wst, uint8_t* bst,
         const __half* sz = reinterpret_cast<const __half*>(wb + 32 * GT_N);
         sh[bb] = sz[dq_n];
         zh[bb] = sz[GT_N + dq_n];
-#pragma unroll
-        for (int wi = 0; wi < RPP / 4; ++wi)
-            wl[bb][wi] = *reinterpret_cast<const uint32_t*>(wb + dq_n * 32 + dq_h * RPP + 4 * wi);
+        const uint4 v = *reinterpret_cast<const uint4*>(wb + dq_n * 32 + dq_h * RPP);
+        wl[bb][0] = v.x;
+        wl[bb][1] = v.y;
+        wl[bb][2] = v.z;
+        wl[bb][3] = v.w;
     }
     const __nv_bfloat162 k136 = __float2bfloat162_rn(136.0f);
 #pragma unroll
@@ -439,10 +455,14 @@ __device__ __forceinline__ void dequant_blocks(const uint8_t* wst, uint8_t* bst,
 }
 
 // One 128-column tile over a 1/ks slice of the inputs; the ks CTAs of a tile are a
-// cluster. Warp G_PROD_WARP streams each stage (A by TMA, the packed weights by a
-// bulk copy) into a G_S-stage ring; the G_DQ_WARPS dequantising warps turn each
-// stage's blocks into one of G_BP B stages (one wait and one arrival per stage,
-// the two blocks' loads and arithmetic interleaved); warp G_MMA_WARP issues the
+// cluster. Warp G_PROD_WARP streams each stage's packed weights (one bulk copy)
+// into the weight ring and warp G_A_WARP its A tiles (one TMA box) into the A
+// ring; the G_DQ_WARPS dequantising warps, in G_DQ_GROUPS groups that take
+// alternate stages (one group's waits and latencies overlap the other's work),
+// turn each stage's blocks into one of G_BP B stages (one wait and one arrival
+// per stage, the two blocks' loads and arithmetic interleaved) and release the
+// weight slot at once; warp G_MMA_WARP issues the MMAs. The weights stream
+// G_WS stages ahead of the dequantisation, bounded by it rather than by the
 // MMAs. Then every
 // CTA stages its fp32 partial tile in shared memory and, after a cluster barrier,
 // finishes its share of the tile's columns from the ks partials (DSMEM reads).
@@ -450,9 +470,11 @@ template <int MODE>
 __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_constant__ GemmArgs g, void* ws) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + G_OFF_BAR);   // [G_S]
-    uint64_t* empty = full + G_S;                                       // [G_S]
-    uint64_t* bfull = empty + G_S;                                      // [G_BP]
+    uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + G_OFF_BAR);  // [G_WS]
+    uint64_t* wempty = wfull + G_WS;                                    // [G_WS]
+    uint64_t* afull = wempty + G_WS;                                    // [G_AS_MAX]
+    uint64_t* aempty = afull + G_AS_MAX;                                // [G_AS_MAX]
+    uint64_t* bfull = aempty + G_AS_MAX;                                // [G_BP]
     uint64_t* bempty = bfull + G_BP;                                    // [G_BP]
     uint64_t* acc_bar = bempty + G_BP;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
@@ -466,12 +488,16 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     const int kc = g.K / g.ks, k0 = sp * kc, nkb = kc / GT_K;
 
     if (tid == 0) {
-        for (int i = 0; i < G_S; ++i) {
-            tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&empty[i], 1);
+        for (int i = 0; i < G_WS; ++i) {
+            tc::mbar_init(&wfull[i], 1);
+            tc::mbar_init(&wempty[i], G_DQ_GWARPS);
+        }
+        for (int i = 0; i < G_AS_MAX; ++i) {
+            tc::mbar_init(&afull[i], 1);
+            tc::mbar_init(&aempty[i], 1);
         }
         for (int i = 0; i < G_BP; ++i) {
-            tc::mbar_init(&bfull[i], G_DQ_WARPS);
+            tc::mbar_init(&bfull[i], G_DQ_GWARPS);
             tc::mbar_init(&bempty[i], 1);
         }
         tc::mbar_init(acc_bar, 1);
@@ -490,78 +516,84 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     if (g.ss_zero && t == 0 && sp == 0)
         for (int i = tid; i < g.n_max; i += G_THREADS) g.ss_zero[i] = 0.f;
 
+    // A stages: 64-row tiles up to 64 items (4 stages), else 128-row tiles (2)
+    const int as_shift = g.a_rows <= 64 ? 2 : 1;
+    const uint32_t a_stage_bytes = G_A_REGION >> as_shift;
+    const int nst = (nkb + G_BPS - 1) / G_BPS;
+    // Stage j holds blocks 2 jr, 2 jr + 1 (jr = (j + rot) % nst): each tile walks its
+    // stages from a different one (when all stages hold two blocks), so that the
+    // tiles' CTAs, which all read the same A, ask for different A blocks at any
+    // time; the MMAs only sum, in that order.
+    const int rot = nkb % G_BPS == 0 ? t % nst : 0;
+
     if (warp == G_PROD_WARP) {
-        // Stage j (blocks 2j, 2j + 1) -> slot j % G_S: both A tiles in one TMA (the
-        // k-blocks map) and both packed weight blocks in one bulk copy. Each tile
-        // walks its stages from a different one (when all stages hold two blocks),
-        // so that the tiles' CTAs, which all read the same A, ask for different A
-        // blocks at any time; the MMAs only sum, in that order.
+        // both packed weight blocks of stage j in one bulk copy into slot j % G_WS
         if (lane == 0) {
-            const int nst = (nkb + G_BPS - 1) / G_BPS;
-            const int rot = nkb % G_BPS == 0 ? t % nst : 0;
             const uint8_t* wsrc = g.blob + (static_cast<int64_t>(t) * (g.K / GT_K) + k0 / GT_K) * G_W_BYTES;
-            auto issue_w = [&](int j) {   // arm slot j % G_S and bring its weights
-                const int st = j % G_S, jr = (j + rot) % nst;
-                const int nb = min(G_BPS, nkb - jr * G_BPS);
-                tc::mbar_arrive_expect_tx(&full[st], G_BPS * g.a_rows * GT_K * 2 + nb * G_W_BYTES);
-                bulk_load(smem + G_OFF_W + st * G_BPS * G_W_BYTES, wsrc + static_cast<int64_t>(jr) * G_BPS * G_W_BYTES,
-                          nb * G_W_BYTES, &full[st]);
-            };
-            auto issue_a = [&](int j) {   // the stage's A tiles (written by the previous kernel)
-                const int st = j % G_S, jr = (j + rot) % nst;
-                tc::tma_load_3d(smem + G_OFF_A + st * G_BPS * G_A_BYTES, &g.tm_a, 0, 0, k0 / GT_K + jr * G_BPS,
-                                &full[st]);
-            };
-            const int pre = min(nst, G_S);
-            for (int j = 0; j < pre; ++j) issue_w(j);
-            wait_prior_grid();
-            for (int j = 0; j < pre; ++j) issue_a(j);
-            int j = pre;
+            int j = 0;
             for (; j < nst; ++j) {
-                const int st = j % G_S;
-                if (!tc::mbar_wait(&empty[st], ((j / G_S) - 1) & 1, abort, ws, 81)) break;
-                issue_w(j);
-                issue_a(j);
+                const int st = j % G_WS, jr = (j + rot) % nst;
+                if (j >= G_WS && !tc::mbar_wait(&wempty[st], ((j / G_WS) - 1) & 1, abort, ws, 81)) break;
+                const int nb = min(G_BPS, nkb - jr * G_BPS);
+                tc::mbar_arrive_expect_tx(&wfull[st], nb * G_W_BYTES);
+                bulk_load(smem + G_OFF_W + st * G_BPS * G_W_BYTES, wsrc + static_cast<int64_t>(jr) * G_BPS * G_W_BYTES,
+                          nb * G_W_BYTES, &wfull[st]);
             }
             // stopped early: let the copies in flight land before the CTA moves on
             const uint64_t t0 = tc::globaltimer();
-            for (int i = max(0, j - G_S); i < j; ++i)
-                while (!tc::mbar_test_wait(&full[i % G_S], (i / G_S) & 1) && tc::globaltimer() - t0 < 200000000ull) {
+            for (int i = max(0, j - G_WS); i < j; ++i)
+                while (!tc::mbar_test_wait(&wfull[i % G_WS], (i / G_WS) & 1) && tc::globaltimer() - t0 < 200000000ull) {
+                }
+        }
+    } else if (warp == G_A_WARP) {
+        // both A tiles of stage j in one TMA box (the k-blocks map) into slot j % n_as
+        if (lane == 0) {
+            const int n_as = 1 << as_shift;
+            int j = 0;
+            for (; j < nst; ++j) {
+                const int sa = j & (n_as - 1), jr = (j + rot) % nst;
+                if (j >= n_as && !tc::mbar_wait(&aempty[sa], ((j >> as_shift) - 1) & 1, abort, ws, 87)) break;
+                tc::mbar_arrive_expect_tx(&afull[sa], G_BPS * g.a_rows * GT_K * 2);
+                tc::tma_load_3d(smem + G_OFF_A + sa * a_stage_bytes, &g.tm_a, 0, 0, k0 / GT_K + jr * G_BPS, &afull[sa]);
+            }
+            const uint64_t t0 = tc::globaltimer();
+            for (int i = max(0, j - n_as); i < j; ++i)
+                while (!tc::mbar_test_wait(&afull[i & (n_as - 1)], (i >> as_shift) & 1) &&
+                       tc::globaltimer() - t0 < 200000000ull) {
                 }
         }
     } else if (warp == G_MMA_WARP) {
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_bf16(128, GT_N);
-            const int nst = (nkb + G_BPS - 1) / G_BPS;
+            const uint32_t idesc = tc::idesc_bf16(GT_N, g.a_rows);   // M = columns, N = items
             for (int j = 0; j < nst; ++j) {
-                const int st = j % G_S, bp = j % G_BP;
-                if (!tc::mbar_wait(&full[st], (j / G_S) & 1, abort, ws, 82)) break;
+                const int sa = j & ((1 << as_shift) - 1), bp = j % G_BP;
+                if (!tc::mbar_wait(&afull[sa], (j >> as_shift) & 1, abort, ws, 82)) break;
                 if (!tc::mbar_wait(&bfull[bp], (j / G_BP) & 1, abort, ws, 83)) break;
                 tc::tc_fence_after();
                 for (int bb = 0; bb < G_BPS && j * G_BPS + bb < nkb; ++bb) {
                     const int kb = j * G_BPS + bb;
                     // the stage's blocks land a_rows x 128 bytes apart (one TMA box)
-                    const uint64_t ad = tc::smem_desc_sw128(
-                        tc::smem_u32(smem + G_OFF_A + st * G_BPS * G_A_BYTES + bb * g.a_rows * 128));
+                    const uint64_t ad =
+                        tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_A + sa * a_stage_bytes + bb * g.a_rows * 128));
                     const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_B + (bp * G_BPS + bb) * G_B_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < GT_K / 16; ++kk)
-                        tc::umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, kb | kk);
+                        tc::umma_bf16(tmem, bd + 2 * kk, ad + 2 * kk, idesc, kb | kk);
                 }
                 tc::umma_commit(&bempty[bp]);
-                tc::umma_commit(&empty[st]);
+                tc::umma_commit(&aempty[sa]);
             }
             tc::umma_commit(acc_bar);   // every MMA issued has finished (also after a stop)
         }
     } else {
         // dequantiser: column dq_n, part dq_h of each k block (RPP packed rows, 2 RPP
-        // inputs), both blocks of a stage per pass
-        const int dq_n = tid & 127, dq_h = tid >> 7;
-        const int nst = (nkb + G_BPS - 1) / G_BPS;
-        for (int j = 0; j < nst; ++j) {
-            const int st = j % G_S, bp = j % G_BP;
+        // inputs), both blocks of a stage per pass, the group's stages only
+        const int gtid = tid % (G_DQ_GWARPS * 32);
+        const int dq_n = gtid & 127, dq_h = gtid >> 7;
+        for (int j = warp / G_DQ_GWARPS; j < nst; j += G_DQ_GROUPS) {
+            const int st = j % G_WS, bp = j % G_BP;
             if (j >= G_BP && !tc::mbar_wait(&bempty[bp], ((j / G_BP) - 1) & 1, abort, ws, 84)) break;
-            if (!tc::mbar_wait(&full[st], (j / G_S) & 1, abort, ws, 85)) break;
+            if (!tc::mbar_wait(&wfull[st], (j / G_WS) & 1, abort, ws, 85)) break;
             const uint8_t* wst = smem + G_OFF_W + st * G_BPS * G_W_BYTES;
             uint8_t* bst = smem + G_OFF_B + bp * G_BPS * G_B_BYTES;
             if (nkb - j * G_BPS >= 2)
@@ -570,7 +602,10 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
                 dequant_blocks<1>(wst, bst, dq_n, dq_h);
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bfull[bp]);
+            if (lane == 0) {
+                tc::mbar_arrive(&wempty[st]);   // the packed codes have been read
+                tc::mbar_arrive(&bfull[bp]);
+            }
         }
     }
     // the accumulator is final
@@ -578,22 +613,20 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     __syncthreads();
     const bool ok = !*abort;
     tc::tc_fence_after();
-    // partial tile -> shared memory (over the A ring, idle now): warp w reads TMEM
-    // lanes 32 (w % 4).., columns 64 (w / 4)..
-    float* P = reinterpret_cast<float*>(smem + G_OFF_A);
+    // partial tile -> shared memory [item][column] (over the B ring, idle now): TMEM
+    // lane = column, TMEM column = item; warp w reads lanes 32 (w % 4).. for items
+    // 32 (w / 4).., lane l stores column 32 (w % 4) + l of each
+    float* P = reinterpret_cast<float*>(smem + G_OFF_B);
+    static_assert(G_DQ_WARPS / 4 * 32 == MAX_ITEMS, "the epilogue warps cover every item");
     if (ok && warp < G_DQ_WARPS) {
-        constexpr int CW = GT_N / (G_DQ_WARPS / 4);   // columns per warp
-        const int m = (warp & 3) * 32 + lane;
-        const int cb = (warp >> 2) * CW;
-#pragma unroll 1
-        for (int c = 0; c < CW; c += 32) {
+        const int c = (warp & 3) * 32 + lane;
+        const int m0 = (warp >> 2) * 32;
+        if (m0 < n) {   // warp-uniform
             float v[32];
-            tc::tmem_ld32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + cb + c, v);
-            if (m < n) {
-                float4* dst = reinterpret_cast<float4*>(P + m * G_P_PITCH + cb + c);
+            tc::tmem_ld32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + m0, v);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
+            for (int i = 0; i < 32; ++i)
+                if (m0 + i < n) P[(m0 + i) * G_P_PITCH + c] = v[i];
         }
     }
     tc::tc_fence_before();
@@ -1085,7 +1118,7 @@ int max_clusters(int ks) {
 template <int MODE>
 tee_status launch_gemm(const GemmArgs& g0, void* ws, cudaStream_t s) {
     GemmArgs g = g0;
-    g.a_rows = std::min(G_A_ROWS, (g.n_max + 7) / 8 * 8);
+    g.a_rows = std::min(G_A_ROWS, (g.n_max + 15) / 16 * 16);   // the MMA's N: a multiple of 16
     tee_status st = make_tmap_bf16_kblocks(&g.tm_a, g.a, G_A_ROWS, static_cast<uint64_t>(g.lda) * 2, g.K / GT_K,
                                            g.a_rows, G_BPS);
     if (st != TEE_OK) return st;
