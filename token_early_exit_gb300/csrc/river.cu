@@ -20,14 +20,15 @@
 // and the epilogue multiplies by 1/rms, whose sum of squares the producing
 // kernel accumulated in fp32.
 //
-// w4_gemm (tcgen05): a CTA computes a 128-column tile for every item (M = 128
-// TMEM lanes, items <= 128) over a 1/ks slice of the inputs; the ks CTAs of a
-// tile are one cluster. A producer warp brings each stage of two 64-input blocks
-// (the A tiles by one TMA box, the packed int4 weights -- repacked per tile at
-// prepare time -- by one bulk copy); sixteen warps dequantise each block into a
-// B buffer; one thread issues four 128x128x16 MMAs into TMEM. The CTAs then
-// reduce their partial tiles through distributed shared memory, each finishing
-// its share of the columns with the mode's epilogue.
+// w4_gemm (tcgen05): a CTA computes a 128-column tile for every item (items <=
+// 128) over a 1/ks slice of the inputs; the ks CTAs of a tile are one cluster.
+// Per stage of two 64-input blocks, one warp brings the packed int4 weights
+// (repacked per tile at prepare time) by one bulk copy and another the A tiles
+// by one TMA box; two groups of eight warps, on alternate stages, dequantise the
+// weights into B tiles; one thread issues the transposed MMAs (M = the 128
+// output columns, N = the items rounded up to 16, K = 16) into TMEM. The CTAs
+// then reduce their partial tiles through distributed shared memory, each
+// finishing its share of the columns with the mode's epilogue.
 #include <algorithm>
 
 #include "fill.cuh"
