@@ -58,21 +58,21 @@ constexpr int G_DQ_GROUPS = 2;   // dequantising groups; group q takes the stage
 constexpr int G_DQ_GWARPS = G_DQ_WARPS / G_DQ_GROUPS;
 constexpr int G_DQ_PARTS = G_DQ_GWARPS * 32 / 128;   // threads per column: each takes 32 / G_DQ_PARTS packed rows
 constexpr int G_EPI_THREADS = G_DQ_WARPS * 32;
-// A stage = two k blocks (G_BPS). Three rings, each with its own full / empty
-// barriers: the packed weights (G_WS stages, released by the dequantising group
-// once it has read them), the A tiles (released by the MMAs: 4 stages of two
-// tiles of up to 64 item rows, 2 stages of up to 128 rows above), and the
-// dequantised B tiles (G_BP stages, released by the MMAs). The MMA is transposed:
+// A stage = two k blocks (G_BPS). Rings: the packed weights (G_WS stages with
+// their own full / empty barriers, released by the dequantising group once it
+// has read them), and the A tiles and dequantised B tiles (G_BP stages each, own
+// full barriers, one empty barrier per stage that the MMAs' single commit
+// releases for both). The MMA is transposed:
 // M = the tile's 128 output columns (the dequantised weights), N = the item rows
 // (a multiple of 16), so the accumulator holds [column][item], the tensor core
 // does no work for absent items and reads no rows past them.
 constexpr int G_BPS = 2;         // k blocks per stage
-constexpr int G_WS = 6;          // weight stages
-constexpr int G_AS_MAX = 4;      // A stages (64-row tiles; 2 with 128-row tiles)
-constexpr int G_BP = 3;          // B stages
+constexpr int G_WS = 3;          // weight stages
+constexpr int G_BP = 3;          // A and B stages
 constexpr int G_RB = G_BP * G_BPS;   // dequantised B buffers
 constexpr int G_A_ROWS = 128;    // A tile rows (the MMA's N) at most
-constexpr uint32_t G_A_REGION = 64 * 1024;   // the A ring
+constexpr uint32_t G_A_STAGE = G_BPS * G_A_ROWS * 128;   // 32 KB: two tiles of up to 128 rows
+constexpr uint32_t G_A_REGION = G_BP * G_A_STAGE;        // the A ring
 constexpr uint32_t G_B_BYTES = GT_N * GT_K * 2;      // 16 KB
 // a packed weight block: codes [32 packed rows][128 columns], then 128 fp16 scales, 128 fp16 zeros
 constexpr uint32_t G_W_BYTES = 32 * GT_N + 2 * GT_N * 2;   // 4608
@@ -80,11 +80,10 @@ constexpr uint32_t G_OFF_A = 0;
 constexpr uint32_t G_OFF_B = G_OFF_A + G_A_REGION;
 constexpr uint32_t G_OFF_W = G_OFF_B + G_RB * G_B_BYTES;
 constexpr uint32_t G_OFF_BAR = G_OFF_W + G_WS * G_BPS * G_W_BYTES;
-constexpr size_t G_SMEM = 1024 + G_OFF_BAR + (2 * G_WS + 2 * G_AS_MAX + 2 * G_BP + 1) * 8 + 16;
+constexpr size_t G_SMEM = 1024 + G_OFF_BAR + (2 * G_WS + 3 * G_BP + 1) * 8 + 16;
 // the CTA's partial tile after the loop: [128 rows][GT_N + 4] fp32, over the B ring
 constexpr int G_P_PITCH = GT_N + 4;
 static_assert(G_A_ROWS * G_P_PITCH * 4 <= G_RB * G_B_BYTES, "partial tile fits the B ring");
-static_assert(G_AS_MAX * G_BPS * 64 * 128 == G_A_REGION && 2 * G_BPS * G_A_ROWS * 128 == G_A_REGION, "A ring");
 static_assert(G_OFF_B % 1024 == 0 && G_OFF_W % 16 == 0 && G_OFF_BAR % 8 == 0, "alignment");
 static_assert(G_SMEM <= 232448, "shared memory");
 
@@ -462,22 +461,21 @@ __device__ __forceinline__ void dequant_blocks(const uint8_t* wst, uint8_t* bst,
 // alternate stages (one group's waits and latencies overlap the other's work),
 // turn each stage's blocks into one of G_BP B stages (one wait and one arrival
 // per stage, the two blocks' loads and arithmetic interleaved) and release the
-// weight slot at once; warp G_MMA_WARP issues the MMAs. The weights stream
-// G_WS stages ahead of the dequantisation, bounded by it rather than by the
-// MMAs. Then every
-// CTA stages its fp32 partial tile in shared memory and, after a cluster barrier,
-// finishes its share of the tile's columns from the ks partials (DSMEM reads).
+// weight slot at once; warp G_MMA_WARP issues the MMAs and one commit per stage
+// frees its A and B slots. The weights stream ahead of the dequantisation,
+// bounded by it rather than by the MMAs. Then every CTA stages its fp32 partial
+// tile in shared memory and, after a cluster barrier, finishes its share of the
+// tile's columns from the ks partials (DSMEM reads).
 template <int MODE>
 __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_constant__ GemmArgs g, void* ws) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + G_OFF_BAR);  // [G_WS]
     uint64_t* wempty = wfull + G_WS;                                    // [G_WS]
-    uint64_t* afull = wempty + G_WS;                                    // [G_AS_MAX]
-    uint64_t* aempty = afull + G_AS_MAX;                                // [G_AS_MAX]
-    uint64_t* bfull = aempty + G_AS_MAX;                                // [G_BP]
-    uint64_t* bempty = bfull + G_BP;                                    // [G_BP]
-    uint64_t* acc_bar = bempty + G_BP;
+    uint64_t* afull = wempty + G_WS;                                    // [G_BP]
+    uint64_t* bfull = afull + G_BP;                                     // [G_BP]
+    uint64_t* cempty = bfull + G_BP;                                    // [G_BP]: A and B slots consumed
+    uint64_t* acc_bar = cempty + G_BP;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -493,13 +491,10 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
             tc::mbar_init(&wfull[i], 1);
             tc::mbar_init(&wempty[i], G_DQ_GWARPS);
         }
-        for (int i = 0; i < G_AS_MAX; ++i) {
-            tc::mbar_init(&afull[i], 1);
-            tc::mbar_init(&aempty[i], 1);
-        }
         for (int i = 0; i < G_BP; ++i) {
+            tc::mbar_init(&afull[i], 1);
             tc::mbar_init(&bfull[i], G_DQ_GWARPS);
-            tc::mbar_init(&bempty[i], 1);
+            tc::mbar_init(&cempty[i], 1);
         }
         tc::mbar_init(acc_bar, 1);
         *abort = 0;
@@ -517,9 +512,6 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     if (g.ss_zero && t == 0 && sp == 0)
         for (int i = tid; i < g.n_max; i += G_THREADS) g.ss_zero[i] = 0.f;
 
-    // A stages: 64-row tiles up to 64 items (4 stages), else 128-row tiles (2)
-    const int as_shift = g.a_rows <= 64 ? 2 : 1;
-    const uint32_t a_stage_bytes = G_A_REGION >> as_shift;
     const int nst = (nkb + G_BPS - 1) / G_BPS;
     // Stage j holds blocks 2 jr, 2 jr + 1 (jr = (j + rot) % nst): each tile walks its
     // stages from a different one (when all stages hold two blocks), so that the
@@ -547,42 +539,39 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
                 }
         }
     } else if (warp == G_A_WARP) {
-        // both A tiles of stage j in one TMA box (the k-blocks map) into slot j % n_as
+        // both A tiles of stage j in one TMA box (the k-blocks map) into slot j % G_BP
         if (lane == 0) {
-            const int n_as = 1 << as_shift;
             int j = 0;
             for (; j < nst; ++j) {
-                const int sa = j & (n_as - 1), jr = (j + rot) % nst;
-                if (j >= n_as && !tc::mbar_wait(&aempty[sa], ((j >> as_shift) - 1) & 1, abort, ws, 87)) break;
+                const int sa = j % G_BP, jr = (j + rot) % nst;
+                if (j >= G_BP && !tc::mbar_wait(&cempty[sa], ((j / G_BP) - 1) & 1, abort, ws, 87)) break;
                 tc::mbar_arrive_expect_tx(&afull[sa], G_BPS * g.a_rows * GT_K * 2);
-                tc::tma_load_3d(smem + G_OFF_A + sa * a_stage_bytes, &g.tm_a, 0, 0, k0 / GT_K + jr * G_BPS, &afull[sa]);
+                tc::tma_load_3d(smem + G_OFF_A + sa * G_A_STAGE, &g.tm_a, 0, 0, k0 / GT_K + jr * G_BPS, &afull[sa]);
             }
             const uint64_t t0 = tc::globaltimer();
-            for (int i = max(0, j - n_as); i < j; ++i)
-                while (!tc::mbar_test_wait(&afull[i & (n_as - 1)], (i >> as_shift) & 1) &&
-                       tc::globaltimer() - t0 < 200000000ull) {
+            for (int i = max(0, j - G_BP); i < j; ++i)
+                while (!tc::mbar_test_wait(&afull[i % G_BP], (i / G_BP) & 1) && tc::globaltimer() - t0 < 200000000ull) {
                 }
         }
     } else if (warp == G_MMA_WARP) {
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_bf16(GT_N, g.a_rows);   // M = columns, N = items
             for (int j = 0; j < nst; ++j) {
-                const int sa = j & ((1 << as_shift) - 1), bp = j % G_BP;
-                if (!tc::mbar_wait(&afull[sa], (j >> as_shift) & 1, abort, ws, 82)) break;
+                const int bp = j % G_BP;
+                if (!tc::mbar_wait(&afull[bp], (j / G_BP) & 1, abort, ws, 82)) break;
                 if (!tc::mbar_wait(&bfull[bp], (j / G_BP) & 1, abort, ws, 83)) break;
                 tc::tc_fence_after();
                 for (int bb = 0; bb < G_BPS && j * G_BPS + bb < nkb; ++bb) {
                     const int kb = j * G_BPS + bb;
                     // the stage's blocks land a_rows x 128 bytes apart (one TMA box)
                     const uint64_t ad =
-                        tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_A + sa * a_stage_bytes + bb * g.a_rows * 128));
+                        tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_A + bp * G_A_STAGE + bb * g.a_rows * 128));
                     const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(smem + G_OFF_B + (bp * G_BPS + bb) * G_B_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < GT_K / 16; ++kk)
                         tc::umma_bf16(tmem, bd + 2 * kk, ad + 2 * kk, idesc, kb | kk);
                 }
-                tc::umma_commit(&bempty[bp]);
-                tc::umma_commit(&aempty[sa]);
+                tc::umma_commit(&cempty[bp]);   // the stage's A and B slots
             }
             tc::umma_commit(acc_bar);   // every MMA issued has finished (also after a stop)
         }
@@ -593,7 +582,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
         const int dq_n = gtid & 127, dq_h = gtid >> 7;
         for (int j = warp / G_DQ_GWARPS; j < nst; j += G_DQ_GROUPS) {
             const int st = j % G_WS, bp = j % G_BP;
-            if (j >= G_BP && !tc::mbar_wait(&bempty[bp], ((j / G_BP) - 1) & 1, abort, ws, 84)) break;
+            if (j >= G_BP && !tc::mbar_wait(&cempty[bp], ((j / G_BP) - 1) & 1, abort, ws, 84)) break;
             if (!tc::mbar_wait(&wfull[st], (j / G_WS) & 1, abort, ws, 85)) break;
             const uint8_t* wst = smem + G_OFF_W + st * G_BPS * G_W_BYTES;
             uint8_t* bst = smem + G_OFF_B + bp * G_BPS * G_B_BYTES;
