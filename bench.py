@@ -35,6 +35,7 @@ import hashlib  # noqa: E402
 import json  # noqa: E402
 import statistics  # noqa: E402
 import subprocess  # noqa: E402
+import tempfile  # noqa: E402
 import sys  # noqa: E402
 import time  # noqa: E402
 
@@ -505,8 +506,10 @@ class Clocks:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.index}.csv")
+            # the raw samples: $TEE_CLOCKS_DIR if set, else the system's temporary folder
+            d = os.environ.get("TEE_CLOCKS_DIR") or tempfile.gettempdir()
+            os.makedirs(d, exist_ok=True)
+            self.path = os.path.join(d, f"clocks_rank{self.index}.csv")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
