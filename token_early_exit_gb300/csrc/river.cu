@@ -119,7 +119,7 @@ RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
         return at;
     };
     w.resid = take(n * d * 4);
-    const size_t na = G_A_ROWS;   // the GEMMs' A operands: 128 rows, the TMA box
+    const size_t na = G_A_ROWS;   // the GEMMs' A operands: 128 rows, the TMA map's extent
     w.abuf = take(na * d * 2);
     w.qbuf = take(n * qw * 2);
     w.obuf = take(na * qw * 2);
