@@ -4,7 +4,13 @@ Gate scores: within 1e-4 absolute (fp32 accumulation). Exit masks and
 compaction indices: bit-exact, except tokens whose oracle score lies within
 1e-3 of the threshold, which are excluded and counted. Filled K/V: max-abs
 error at most 2e-2 and relative L2 error at most 1e-2 against the unrounded
-float64 oracle.
+float64 oracle (``check_kv``; every fill of the hot path).
+
+``check_kv_scaled`` is a separately named, looser max-abs bound for the fill
+variants (K/V bias, per-head K norm) and the Exit River's K/V only: there the
+reference's RMS exceeds the 0.5 that the fixed bound was set for, and the
+fill's roundings are relative errors, so the max-abs bound grows with that
+RMS while the relative-L2 bound stays 1e-2.
 """
 import numpy as np
 import torch
@@ -13,10 +19,10 @@ SCORE_TOL = 1e-4
 NEAR_BAND = 1e-3
 KV_MAX_ABS = 2e-2
 KV_REL_L2 = 1e-2
-# RMS of K and V at which KV_MAX_ABS holds (projection weights N(0, 0.25/d)): the
-# fill's roundings are relative errors, so for larger values (a per-head K norm
-# gives K an RMS near its norm weight, a bias adds to both) the bound grows with
-# the reference's RMS.
+# RMS of K and V at which KV_MAX_ABS holds (projection weights N(0, 0.25/d)).
+# check_kv_scaled only: for larger values (a per-head K norm gives K an RMS near
+# its norm weight, a bias adds to both) its max-abs bound grows with the
+# reference's RMS.
 KV_REF_RMS = 0.5
 
 
@@ -52,20 +58,34 @@ def check_mask(gpu_mask, ref_score, thr) -> int:
     return int(near.sum())
 
 
-def check_kv(gpu, ref, what="kv"):
+def _kv_errors(gpu, ref):
     g = f64(gpu)
-    diff = np.abs(g - ref)
-    mx = diff.max(initial=0.0)
+    mx = np.abs(g - ref).max(initial=0.0)
     rel = np.linalg.norm((g - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-30)
+    return mx, rel
+
+
+def check_kv(gpu, ref, what="kv"):
+    """The fill's parity rule: max-abs <= 2e-2 and relative L2 <= 1e-2."""
+    mx, rel = _kv_errors(gpu, ref)
+    assert mx <= KV_MAX_ABS and rel <= KV_REL_L2, \
+        f"{what}: max-abs {mx:.3e} (bound {KV_MAX_ABS:.1e}), rel-L2 {rel:.3e}"
+    return mx, rel
+
+
+def check_kv_scaled(gpu, ref, what="kv"):
+    """Fill variants and the Exit River only: max-abs <= 2e-2 * max(1, rms / 0.5)
+    of the reference, relative L2 <= 1e-2."""
+    mx, rel = _kv_errors(gpu, ref)
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
     lim = KV_MAX_ABS * max(1.0, rms / KV_REF_RMS)
     assert mx <= lim and rel <= KV_REL_L2, f"{what}: max-abs {mx:.3e} (bound {lim:.3e}), rel-L2 {rel:.3e}"
     return mx, rel
 
 
-def check_decode_fill(cfg, x, rows, pos, seq, sentinel):
-    """Written slots of a decode fill match the oracle; every other slot of both
-    caches still holds ``sentinel``."""
+def check_decode_fill(cfg, x, rows, pos, seq, sentinel, kv_check=check_kv):
+    """Written slots of a decode fill match the oracle (``kv_check``); every other
+    slot of both caches still holds ``sentinel``."""
     import oracle
     h = f64(x["h_cur"])
     layers = host(x["layers"])
@@ -82,7 +102,7 @@ def check_decode_fill(cfg, x, rows, pos, seq, sentinel):
         idx_p = torch.as_tensor(pos[rows], device=dev).long()
         for c, cache, ref in (("k", k_all, k_ref), ("v", v_all, v_ref)):
             if L.get("writes") in (None, "kv", c):   # a K-only / V-only layer leaves the other cache
-                check_kv(cache[j, idx_s, :, idx_p], ref, f"{c.upper()} layer {j}")
+                kv_check(cache[j, idx_s, :, idx_p], ref, f"{c.upper()} layer {j}")
                 written[c][j, idx_s, :, idx_p] = True
     for c, cache in (("k", k_all), ("v", v_all)):
         assert bool((cache[~written[c]] == sentinel).all())

@@ -2,13 +2,18 @@
 bias (QKV-bias models), a per-head RMSNorm of K before RoPE (QK-norm models),
 and layers that fill only the K or only the V cache. Each of the three fill
 paths is covered: the generic kernels (fp32), the tcgen05 prefill (dense bf16)
-and the tcgen05 decode (int4 W4A16)."""
+and the tcgen05 decode (int4 W4A16).
+
+K and V here are checked with ``check_kv_scaled``: a K bias or a per-head K
+norm lifts the reference's RMS from about 0.5 to about 1, and the fill's
+roundings are relative errors, so the max-abs bound scales with that RMS
+(relative L2 stays 1e-2)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from tests.parity import check_decode_fill, check_kv, f64, host
+from tests.parity import check_decode_fill, check_kv_scaled, f64, host
 from workloads import configs, gen
 
 pytestmark = pytest.mark.gpu
@@ -62,7 +67,8 @@ def test_generic_fill_variants(tee, kind):
     ws = tee.Workspace(DEV)
     f(x["h_cur"], x["k_cache"], x["v_cache"], rows=torch.from_numpy(rows).to(DEV), pos=x["pos"], seq=x["seq"], ws=ws)
     assert ws.device_error() == (0, 0)
-    check_decode_fill(cfg, x, rows, x["pos"].cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL)
+    check_decode_fill(cfg, x, rows, x["pos"].cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL,
+                      kv_check=check_kv_scaled)
 
 
 @pytest.mark.parametrize("kind", sorted(VARIANTS))
@@ -78,7 +84,8 @@ def test_decode_int4_fill_variants(tee, kind, n, hd, d):
     ws = tee.Workspace(DEV)
     f(x["h_cur"], x["k_cache"], x["v_cache"], rows=torch.from_numpy(rows).to(DEV), pos=x["pos"], seq=x["seq"], ws=ws)
     assert ws.device_error() == (0, 0)
-    check_decode_fill(cfg, x, rows, x["pos"].cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL)
+    check_decode_fill(cfg, x, rows, x["pos"].cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL,
+                      kv_check=check_kv_scaled)
 
 
 def test_decode_v_only_first_layer_still_records_bad_positions(tee):
@@ -94,7 +101,8 @@ def test_decode_v_only_first_layer_still_records_bad_positions(tee):
     f(x["h_cur"], x["k_cache"], x["v_cache"], rows=rows, pos=pos, seq=x["seq"], ws=ws)
     assert ws.device_error() == (2, cfg.cache_len)
     good = np.array([r for r in range(cfg.batch) if r != 9], dtype=np.int32)
-    check_decode_fill(cfg, x, good, pos.cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL)
+    check_decode_fill(cfg, x, good, pos.cpu().numpy(), x["seq"].cpu().numpy(), gen.CACHE_SENTINEL,
+                      kv_check=check_kv_scaled)
 
 
 def _tc_layers(cfg, n_layers, seed, identity):
@@ -136,7 +144,7 @@ def test_tc_prefill_fill_variants(tee, kind, hd, identity):
         for c, cache, ref in (("k", kc, k_ref), ("v", vc, v_ref)):
             got = cache[j, 0].index_select(1, p).permute(1, 0, 2)
             if L.get("writes") in (None, c):
-                check_kv(got, ref, f"{c.upper()} layer {j}")
+                check_kv_scaled(got, ref, f"{c.upper()} layer {j}")
             else:   # the other cache keeps what the backbone wrote
                 assert bool((cache[j] == gen.CACHE_SENTINEL).all())
     for cache in (kc, vc):

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from oracle import river
-from tests.parity import check_kv, f64, host
+from tests.parity import check_kv_scaled, f64, host
 from workloads import configs, gen
 
 pytestmark = pytest.mark.gpu
@@ -56,8 +56,8 @@ def _check(cfg, x, k0, v0, out, items, rows=None):
     ps, ss = torch.as_tensor(pos, device=DEV).long(), torch.as_tensor(seq, device=DEV).long()
     for L in layers:
         j = L["cache_layer"]
-        check_kv(x["k_cache"][j, ss, :, ps], kc[j, seq, :, pos], f"K layer {j}")
-        check_kv(x["v_cache"][j, ss, :, ps], vc[j, seq, :, pos], f"V layer {j}")
+        check_kv_scaled(x["k_cache"][j, ss, :, ps], kc[j, seq, :, pos], f"K layer {j}")
+        check_kv_scaled(x["v_cache"][j, ss, :, ps], vc[j, seq, :, pos], f"V layer {j}")
         written[j, ss, :, ps] = True
     assert torch.equal(x["k_cache"][~written], k0[~written])
     assert torch.equal(x["v_cache"][~written], v0[~written])
@@ -181,5 +181,5 @@ def test_llama1b_river_sampled_items(tee):
     check_h(out[torch.as_tensor(items, device=DEV)], ref, "h_out (sampled)")
     for i, j in enumerate(js):
         for b, it in enumerate(items):
-            check_kv(x["k_cache"][j, it, :, pos[it]], kc[i, b, :, pos[it]], f"K layer {j} item {it}")
-            check_kv(x["v_cache"][j, it, :, pos[it]], vc[i, b, :, pos[it]], f"V layer {j} item {it}")
+            check_kv_scaled(x["k_cache"][j, it, :, pos[it]], kc[i, b, :, pos[it]], f"K layer {j} item {it}")
+            check_kv_scaled(x["v_cache"][j, it, :, pos[it]], vc[i, b, :, pos[it]], f"V layer {j} item {it}")
