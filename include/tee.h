@@ -193,8 +193,12 @@ TEE_API tee_status tee_exit_gate(const tee_gate_desc* desc, int32_t n,
  * any stream capture. Sharing: all calls on a device use the same array and
  * it keeps the previous call's contents (each call clears the part that must
  * start at zero), so two calls that overlap on the GPU, on different streams
- * or threads, race and may return wrong results. The device fault word lives
- * in the array too; tee_get_device_error cannot read it.
+ * or threads, race and may return wrong results.
+ * Faults: a fault only the device sees (a bounded wait of the tensor-core
+ * kernel that ran out: TEE_DEVERR_TIMEOUT) is recorded in the array's own
+ * fault word, which tee_get_device_error cannot reach. It is sticky: calls do
+ * not clear it. Read it with tee_exit_gate_router_static_device_error and
+ * clear it with tee_exit_gate_router_static_clear_error.
  */
 TEE_API size_t tee_exit_gate_router_static_max_bytes(void);
 TEE_API tee_status tee_exit_gate_router_static(const tee_gate_desc* desc, int32_t n,
@@ -203,6 +207,23 @@ TEE_API tee_status tee_exit_gate_router_static(const tee_gate_desc* desc, int32_
                                                const void* w_up, const float* b_up,
                                                float* score, uint8_t* mask, int32_t* batch_flag,
                                                void* stream);
+
+/*
+ * The first device fault recorded by tee_exit_gate_router_static on the
+ * current device since the last clear (no counterpart on the source pages).
+ * Waits for `stream`, then stores the fault code (TEE_DEVERR_*, 0 if none) and
+ * its detail in *code and *detail (either may be NULL). Returns TEE_OK when no
+ * fault is recorded, TEE_ERR_DEVICE when one is, TEE_ERR_CUDA on a CUDA error.
+ * Like the gate itself, the first use on a device looks up the array's
+ * address (before any stream capture).
+ */
+TEE_API tee_status tee_exit_gate_router_static_device_error(int32_t* code, int32_t* detail, void* stream);
+
+/*
+ * Clears the fault word of tee_exit_gate_router_static's array on the current
+ * device (an asynchronous write on `stream`); no counterpart on the pages.
+ */
+TEE_API tee_status tee_exit_gate_router_static_clear_error(void* stream);
 
 /* -------------------------------------------------------- exit compaction */
 

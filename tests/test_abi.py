@@ -165,3 +165,16 @@ def test_exit_river_checks_on_the_host(lib):
     assert lib.tee_exit_river(ctypes.byref(D), 1, arr, fake, 1 << 30, 4, None, fake, 2048, 4, None, fake, None,
                               fake, fake, ctypes.byref(layout), fake, 2048, fake, 1 << 30, None) == \
         _lib.TEE_ERR_INVALID_ARG
+
+
+def test_static_router_fault_query_answers_without_a_device(lib):
+    # the fault word of the router gate's static array is read through the CUDA
+    # runtime; with no GPU the query reports a CUDA error instead of crashing
+    import torch
+    from token_early_exit_gb300 import _lib
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the GPU test reads the word")
+    code, detail = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    assert lib.tee_exit_gate_router_static_device_error(ctypes.byref(code), ctypes.byref(detail),
+                                                        None) == _lib.TEE_ERR_CUDA
+    assert lib.tee_exit_gate_router_static_clear_error(None) == _lib.TEE_ERR_CUDA

@@ -55,6 +55,12 @@ def test_static_router_gate_matches_the_workspace_entry_point(lib):
         assert (score - ref_score).abs().max().item() <= SCORE_TOL, f"call {call}"
         assert torch.equal(mask[~near], ref_mask[~near]), f"call {call}"
         assert int(flag.item()) == int(ref_flag.item()), f"call {call}"
+    # the array's sticky fault word: nothing recorded by the two clean calls
+    code, detail = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    st = lib.tee_exit_gate_router_static_device_error(ctypes.byref(code), ctypes.byref(detail), stream)
+    assert st == _lib.TEE_OK
+    assert (code.value, detail.value) == (0, 0)
+    assert lib.tee_exit_gate_router_static_clear_error(stream) == _lib.TEE_OK
 
 
 def test_static_router_gate_rejects_sizes_beyond_its_array(lib):

@@ -78,6 +78,8 @@ SIGNATURES = {
     "tee_exit_gate_router_static_max_bytes": (c_size_t, []),
     "tee_exit_gate_router_static": (c_int, [POINTER(GateDesc), c_int32, _P, c_int64, _P, _P, _P, _P, _P, _P, _P,
                                             _P, _P]),
+    "tee_exit_gate_router_static_device_error": (c_int, [POINTER(c_int32), POINTER(c_int32), _P]),
+    "tee_exit_gate_router_static_clear_error": (c_int, [_P]),
     "tee_exit_compact_workspace_size": (c_size_t, [c_int32]),
     "tee_exit_compact": (c_int, [c_int32, _P, _P, _P, c_int64, c_int32, c_int32, _P, _P, _P, _P, _P, c_int64,
                                  _P, _P, c_size_t, _P]),

@@ -513,10 +513,28 @@ extern "C" tee_status tee_exit_gate_router_static(const tee_gate_desc* g, int32_
     void* scratch = nullptr;
     tee_status st = router_static_scratch(&scratch);
     if (st != TEE_OK) return st;
-    // The array keeps the previous call's contents; the header (fault word and
-    // the last-block counter) must start at zero.
-    st = cuda_status(cudaMemsetAsync(scratch, 0, TEE_WS_HEADER_BYTES, static_cast<cudaStream_t>(stream)));
+    // The array keeps the previous call's contents. The last-block counters of
+    // the header must start at zero; the fault word (the header's first two
+    // words) is sticky, read by tee_exit_gate_router_static_device_error and
+    // cleared only by tee_exit_gate_router_static_clear_error.
+    constexpr size_t FAULT_BYTES = 2 * sizeof(int32_t);
+    st = cuda_status(cudaMemsetAsync(static_cast<unsigned char*>(scratch) + FAULT_BYTES, 0,
+                                     TEE_WS_HEADER_BYTES - FAULT_BYTES, static_cast<cudaStream_t>(stream)));
     if (st != TEE_OK) return st;
     return tee_exit_gate(g, n, h, ld, nullptr, 0, gamma, w_down, b_down, w_up, b_up, score, mask, batch_flag,
                          scratch, ROUTER_STATIC_SCRATCH_BYTES, stream);
+}
+
+extern "C" tee_status tee_exit_gate_router_static_device_error(int32_t* code, int32_t* detail, void* stream) {
+    void* scratch = nullptr;
+    tee_status st = router_static_scratch(&scratch);
+    if (st != TEE_OK) return st;
+    return tee_get_device_error(scratch, code, detail, stream);
+}
+
+extern "C" tee_status tee_exit_gate_router_static_clear_error(void* stream) {
+    void* scratch = nullptr;
+    tee_status st = router_static_scratch(&scratch);
+    if (st != TEE_OK) return st;
+    return tee_clear_device_error(scratch, stream);
 }
