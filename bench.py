@@ -26,9 +26,11 @@ from __future__ import annotations
 
 import os
 
-# The CPU oracle is timed single-threaded; fix BLAS threads before numpy loads.
+# The CPU oracle (single-threaded C++) is timed on one core; pin every BLAS /
+# OpenMP pool to one thread too (numpy only marshals arrays for it), whatever
+# the environment says.
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-    os.environ.setdefault(_v, "1")
+    os.environ[_v] = "1"
 
 import argparse  # noqa: E402
 import hashlib  # noqa: E402
@@ -48,6 +50,7 @@ sys.path.insert(0, ROOT)
 from workloads import configs, gen  # noqa: E402
 
 METRIC = "tokens/s through exit gate+compact+KV fill"
+RIVER_METRIC = "tokens/s through the Exit River (W4A16 exit layers)"
 WORKLOADS = ("decode-1b", "decode-tiny", "router-4096", "router-65536", "prefill-16k", "prefill-120k", "river-1b",
              "river-tiny")
 
@@ -80,6 +83,85 @@ def traffic(key):
 
 
 # --------------------------------------------------------------------------- workloads
+
+# --------------------------------------------------------------------------- workload descriptions
+
+def decode_config(c, case):
+    return {"workload": c.name, "tokens_per_step": c.batch, "d": c.d, "fill_layers": len(c.fill_layers),
+            "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "cache_len": c.cache_len, "gate": "cosine",
+            "rule": c.rule, "tau": c.tau, "map": c.map, "weights": c.weights, "case": case,
+            "l2": "flushed between timed steps"}
+
+
+def router_config(c, n, theta, flush):
+    return {"workload": f"{c.name}-n{n}", "tokens_per_step": n, "d": c.d, "bottleneck": c.bottleneck,
+            "theta": theta, "gate": "router", "rule": "per_token", "gather": True,
+            "l2": "flushed between timed steps" if flush else "inputs larger than L2 (no flush)"}
+
+
+def router_flush(c, n, dev):
+    """h alone twice L2 or more: no flush between steps (its lines are gone anyway)."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size if dev.type == "cuda" else 126 << 20
+    return n * c.d * 2 < 2 * l2
+
+
+def prefill_config(c, rows, n_layers):
+    name = c.name if (rows, n_layers) == (c.filled_rows, len(c.fill_layers)) else \
+        f"{c.name}-reduced-{rows}rows-{n_layers}layers"
+    return {"workload": name, "tokens_per_step": rows, "d": c.d, "fill_layers": n_layers,
+            "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "prompt_tokens": c.tokens,
+            "exact_tail": c.exact_tail, "map": "ridge (N(0,1/d)+0.5I)", "weights": "bf16 dense",
+            "l2": "inputs larger than L2; flushed between timed steps"}
+
+
+def river_cfg(cfg, rows=None, layers=None):
+    import dataclasses
+    if not (rows or layers):
+        return cfg
+    return dataclasses.replace(cfg, batch=rows or cfg.batch,
+                               river_layers=cfg.river_layers[:layers] if layers else cfg.river_layers,
+                               name=f"{cfg.name}-reduced-{rows or cfg.batch}tokens-"
+                                    f"{layers or len(cfg.river_layers)}layers")
+
+
+def river_bytes(cfg, pos):
+    """Algorithmic bytes of one Exit River call: the int4 weights (codes, scales,
+    zeros) and norm weights of every layer, the K/V rows 0..pos that the
+    attention reads, the slots written, h in and out."""
+    L = len(cfg.river_layers)
+    d, f, qw, kvw, g = cfg.d, cfg.d_ff, cfg.qw, cfg.kvw, cfg.group
+    mats = [(d, qw), (d, kvw), (d, kvw), (qw, d), (d, f), (d, f), (f, d)]
+    w_layer = sum(k * n // 2 + 2 * (k // g) * n * 2 for k, n in mats) + 2 * d * 2
+    p = pos.cpu().numpy().astype(np.int64)
+    kv_read = int((p + 1).sum()) * kvw * 2 * 2
+    kv_write = cfg.batch * kvw * 2 * 2
+    return L * (w_layer + kv_read + kv_write) + 2 * cfg.batch * d * 2
+
+
+def river_config(c, nbytes):
+    return {"workload": c.name, "tokens_per_step": c.batch, "d": c.d, "river_layers": len(c.river_layers),
+            "q_heads": c.n_q_heads, "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "d_ff": c.d_ff,
+            "cache_len": c.cache_len, "positions": "U[0, cache_len) per sequence",
+            "weights": "int4 group-64 (W4A16), every matrix", "algorithmic_bytes_per_step": nbytes,
+            "l2": "inputs larger than L2 (the KV cache read); flushed between timed steps"}
+
+
+def reference_config(name, dev, seed=0, rows=None, layers=None):
+    """The ``config`` of a workload as the GPU arm reports it, from the
+    configurations and the generator alone."""
+    if name in ("decode-1b", "decode-tiny"):
+        cfg = configs.LLAMA1B_DECODE if name == "decode-1b" else configs.TINY_DECODE
+        return decode_config(cfg, "exit" if cfg.rule == "batch_all" else "default")
+    if name in ("router-4096", "router-65536"):
+        n = 4096 if name == "router-4096" else (rows or 65536)
+        return router_config(configs.ROUTER_4096, n, 0.5, router_flush(configs.ROUTER_4096, n, dev))
+    if name in ("prefill-16k", "prefill-120k"):
+        cfg = configs.PREFILL_16K if name == "prefill-16k" else configs.PREFILL_120K
+        return prefill_config(cfg, cfg.filled_rows if rows is None else rows,
+                              len(cfg.fill_layers) if layers is None else layers)
+    cfg = river_cfg(configs.LLAMA1B_RIVER if name == "river-1b" else configs.TINY_RIVER, rows, layers)
+    return river_config(cfg, river_bytes(cfg, gen.river_positions(cfg, seed, dev)))
+
 
 class Decode:
     """gate -> compact (+gather) -> kv_fill -> scatter on one decode batch."""
@@ -175,33 +257,8 @@ class Decode:
         return int(self.c_out["counts"][1].item())
 
     def config(self):
-        c = self.cfg
-        return {"workload": c.name, "tokens_per_step": c.batch, "d": c.d, "fill_layers": len(c.fill_layers),
-                "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "cache_len": c.cache_len, "gate": "cosine",
-                "rule": c.rule, "tau": c.tau, "map": c.map, "weights": c.weights, "case": self.case,
-                "l2": "flushed between timed steps"}
+        return decode_config(self.cfg, self.case)
 
-    # ---- the oracle on the host (reference arm and cpu_baseline)
-    def oracle_sample(self):
-        import oracle
-        from tests.parity import host
-        x = self.x
-        hp, hc = host(x["h_prev"]), host(x["h_cur"])
-        layers = host(x["layers"])
-        pos, cfg = x["pos"].cpu().numpy(), self.cfg
-
-        def run():
-            s, m, f = oracle.cosine_gate(hp, hc, cfg.tau, cfg.rule)
-            part = oracle.stable_partition(m)
-            oracle.gather_rows(hc, part["cont_rows"])
-            rows = part["exit_rows"]
-            for L in layers:
-                if len(rows):
-                    oracle.fill_rows(hc[rows], L, pos[rows], cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, cfg.eps,
-                                     cfg.group)
-            oracle.exit_scatter(np.zeros_like(hc), hc, rows, rows)
-            return cfg.batch
-        return run, "one full decode step (all tokens)"
 
 
 class Router:
@@ -222,8 +279,7 @@ class Router:
         self.kernel = "exit_gate(router)"
         self.traffic_key = f"exit_gate(router)/n{n}"   # recorded ncu captures: 4096 and 65,536 tokens
         self.bound = "hbm"
-        # h alone is twice L2 or more: no flush between steps (its lines are gone anyway)
-        self.flush = n * cfg.d * 2 < 2 * torch.cuda.get_device_properties(dev).L2_cache_size
+        self.flush = router_flush(cfg, n, dev)
 
     def fill_bytes(self, n_exit):
         d, b = self.cfg.d, self.cfg.bottleneck
@@ -295,23 +351,8 @@ class Router:
         return int(self.c_out["counts"][1].item())
 
     def config(self):
-        c = self.cfg
-        return {"workload": f"{c.name}-n{self.n}", "tokens_per_step": self.n, "d": c.d, "bottleneck": c.bottleneck,
-                "theta": self.theta, "gate": "router", "rule": "per_token", "gather": True,
-                "l2": "flushed between timed steps" if self.flush else "inputs larger than L2 (no flush)"}
+        return router_config(self.cfg, self.n, self.theta, self.flush)
 
-    def oracle_sample(self):
-        import oracle
-        from tests.parity import host
-        m = 256
-        h, wd, wu = host(self.h[:m]), host(self.w["w_down"]), host(self.w["w_up"])
-
-        def run():
-            p, mask, _ = oracle.router_gate(h, wd, wu, self.theta, "per_token", eps=self.cfg.eps)
-            part = oracle.stable_partition(mask)
-            oracle.gather_rows(h, part["cont_rows"])
-            return m
-        return run, f"router gate + compaction with gather on the first {m} of {self.n} tokens"
 
 
 class Prefill:
@@ -361,27 +402,8 @@ class Prefill:
         return self.rows
 
     def config(self):
-        c = self.cfg
-        name = c.name if (self.rows, self.n_layers) == (c.filled_rows, len(c.fill_layers)) else \
-            f"{c.name}-reduced-{self.rows}rows-{self.n_layers}layers"
-        return {"workload": name, "tokens_per_step": self.rows, "d": c.d, "fill_layers": self.n_layers,
-                "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "prompt_tokens": c.tokens,
-                "exact_tail": c.exact_tail, "map": "ridge (N(0,1/d)+0.5I)", "weights": "bf16 dense",
-                "l2": "inputs larger than L2; flushed between timed steps"}
+        return prefill_config(self.cfg, self.rows, self.n_layers)
 
-    def oracle_sample(self):
-        import oracle
-        from tests.parity import host
-        rows = np.arange(16) * (self.rows // 16)
-        h = host(self.x["h_split"][torch.as_tensor(rows, device=self.dev)])
-        layers = host(self.x["layers"])
-        cfg = self.cfg
-
-        def run():
-            for L in layers:
-                oracle.fill_rows(h, L, rows, cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, cfg.eps)
-            return len(rows)
-        return run, f"fill of 16 evenly spaced rows across all {len(layers)} layers (per-row time extrapolated)"
 
 
 class River:
@@ -389,11 +411,7 @@ class River:
     remaining layers (attention over the shared cache + FFN), one call."""
 
     def __init__(self, tee, cfg, dev, seed=0, rows=None, layers=None):
-        import dataclasses
-        if rows or layers:   # a reduced case (profiling)
-            cfg = dataclasses.replace(cfg, batch=rows or cfg.batch,
-                                      river_layers=cfg.river_layers[:layers] if layers else cfg.river_layers,
-                                      name=f"{cfg.name}-reduced-{rows or cfg.batch}tokens-{layers or len(cfg.river_layers)}layers")
+        cfg = river_cfg(cfg, rows, layers)
         self.tee, self.cfg, self.dev = tee, cfg, dev
         self.x = gen.river_inputs(cfg, seed, dev)
         self.ws = tee.Workspace(dev)
@@ -403,17 +421,10 @@ class River:
         self.out = torch.empty(cfg.batch, cfg.d, dtype=torch.bfloat16, device=dev)
         self.units = cfg.batch
         self.kernel = "exit_river (all launches of the call)"
-        self.metric = "tokens/s through the Exit River (W4A16 exit layers)"
+        self.metric = RIVER_METRIC
         self.traffic_key = None
         self.bound = "hbm"
-        L = len(cfg.river_layers)
-        d, f, qw, kvw, g = cfg.d, cfg.d_ff, cfg.qw, cfg.kvw, cfg.group
-        mats = [(d, qw), (d, kvw), (d, kvw), (qw, d), (d, f), (d, f), (f, d)]
-        w_layer = sum(k * n // 2 + 2 * (k // g) * n * 2 for k, n in mats) + 2 * d * 2
-        pos = self.x["pos"].cpu().numpy().astype(np.int64)
-        kv_read = int((pos + 1).sum()) * kvw * 2 * 2         # K and V rows 0..pos of every item
-        kv_write = cfg.batch * kvw * 2 * 2
-        self._bytes = L * (w_layer + kv_read + kv_write) + 2 * cfg.batch * d * 2
+        self._bytes = river_bytes(cfg, self.x["pos"])
 
     def fill_bytes(self, n_exit):
         return self._bytes
@@ -446,23 +457,97 @@ class River:
         return self.cfg.batch
 
     def config(self):
-        c = self.cfg
-        return {"workload": c.name, "tokens_per_step": c.batch, "d": c.d, "river_layers": len(c.river_layers),
-                "q_heads": c.n_q_heads, "kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "d_ff": c.d_ff,
-                "cache_len": c.cache_len, "positions": "U[0, cache_len) per sequence",
-                "weights": "int4 group-64 (W4A16), every matrix", "algorithmic_bytes_per_step": self._bytes,
-                "l2": "inputs larger than L2 (the KV cache read); flushed between timed steps"}
+        return river_config(self.cfg, self._bytes)
 
-    def oracle_sample(self):
+
+
+# --------------------------------------------------------------------------- the oracle (CPU baseline)
+
+def _host(x):
+    """Tensors (and dicts / lists of them) -> numpy on the host: float64 for
+    floating point, as stored for integers."""
+    if torch.is_tensor(x):
+        return x.detach().double().cpu().numpy() if x.dtype.is_floating_point else x.detach().cpu().numpy()
+    if isinstance(x, dict):
+        return {k: _host(v) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [_host(v) for v in x]
+    return x
+
+
+def oracle_sample(name, dev, seed=0, rows=None, layers=None):
+    """A bounded sample of the workload for the CPU oracle: (run, description).
+
+    The inputs come from the seeded generator alone (drawn with torch on
+    ``dev``, a GPU or the CPU, and copied to the host as float64); nothing
+    here builds, loads or calls the CUDA library. ``run()`` computes the
+    sample with the C++ oracle and returns the tokens it stands for."""
+    import oracle
+    if name in ("decode-1b", "decode-tiny"):
+        cfg = configs.LLAMA1B_DECODE if name == "decode-1b" else configs.TINY_DECODE
+        case = "exit" if cfg.rule == "batch_all" else "default"
+        x = gen.decode_inputs(cfg, seed=seed, device=dev, case=case, with_cache=False)
+        hp, hc, layers_h = _host(x["h_prev"]), _host(x["h_cur"]), _host(x["layers"])
+        pos = x["pos"].cpu().numpy()
+
+        def run():
+            s, m, f = oracle.cosine_gate(hp, hc, cfg.tau, cfg.rule)
+            part = oracle.stable_partition(m)
+            oracle.gather_rows(hc, part["cont_rows"])
+            r = part["exit_rows"]
+            for L in layers_h:
+                if len(r):
+                    oracle.fill_rows(hc[r], L, pos[r], cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, cfg.eps,
+                                     cfg.group)
+            oracle.exit_scatter(np.zeros_like(hc), hc, r, r)
+            return cfg.batch
+        return run, "one full decode step (all tokens)"
+    if name in ("router-4096", "router-65536"):
+        cfg = configs.ROUTER_4096
+        n = 4096 if name == "router-4096" else (rows or 65536)
+        k, m, theta = cfg.checkpoints[0], 256, 0.5
+        w = _host(gen.router_weights(cfg, k, seed=seed, device=dev))
+        h = _host(gen.router_hidden(cfg, n, k, seed=seed, device=dev)[:m])
+
+        def run():
+            p, mask, _ = oracle.router_gate(h, w["w_down"], w["w_up"], theta, "per_token", eps=cfg.eps)
+            part = oracle.stable_partition(mask)
+            oracle.gather_rows(h, part["cont_rows"])
+            return m
+        return run, f"router gate + compaction with gather on the first {m} of {n} tokens"
+    if name in ("prefill-16k", "prefill-120k"):
+        cfg = configs.PREFILL_16K if name == "prefill-16k" else configs.PREFILL_120K
+        n_rows = cfg.filled_rows if rows is None else rows
+        x = gen.prefill_inputs(cfg, seed=seed, device=dev, rows=rows, layers=layers, with_cache=False)
+        sample = np.arange(16) * (n_rows // 16)
+        h = _host(x["h_split"][torch.as_tensor(sample, device=dev)])
+        layers_h = []
+        for L in x["layers"]:   # one layer at a time to the host
+            layers_h.append(_host(L))
+        del x
+
+        def run():
+            for L in layers_h:
+                oracle.fill_rows(h, L, sample, cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, cfg.eps)
+            return len(sample)
+        return run, (f"fill of 16 evenly spaced rows across all {len(layers_h)} layers "
+                     "(per-row time extrapolated)")
+    if name in ("river-1b", "river-tiny"):
+        import dataclasses
         from oracle import river
-        from tests.parity import host
-        cfg, x = self.cfg, self.x
-        L = host(x["layers"][0])
+        cfg = configs.LLAMA1B_RIVER if name == "river-1b" else configs.TINY_RIVER
+        if rows or layers:
+            cfg = dataclasses.replace(cfg, batch=rows or cfg.batch,
+                                      river_layers=cfg.river_layers[:layers] if layers else cfg.river_layers)
+        x = gen.river_inputs(cfg, seed, dev)
+        L = _host(x["layers"][0])
         L["cache_layer"] = 0
         p = int(x["pos"][0].item())
-        kc = host(x["k_cache"][cfg.river_layers[0]:cfg.river_layers[0] + 1, :1, :, :p + 1])
-        vc = host(x["v_cache"][cfg.river_layers[0]:cfg.river_layers[0] + 1, :1, :, :p + 1])
-        h = host(x["h"][:1])
+        j0 = cfg.river_layers[0]
+        kc = np.ascontiguousarray(_host(x["k_cache"][j0:j0 + 1, :1, :, :p + 1]))
+        vc = np.ascontiguousarray(_host(x["v_cache"][j0:j0 + 1, :1, :, :p + 1]))
+        h = _host(x["h"][:1])
+        del x
         frac = 1.0 / len(cfg.river_layers)
 
         def run():
@@ -471,6 +556,7 @@ class River:
             return frac
         return run, (f"one token through one of the {len(cfg.river_layers)} exit layers "
                      f"(position {p}; counted as 1/{len(cfg.river_layers)} token)")
+    raise SystemExit(f"unknown workload {name}")
 
 
 def make(name, tee, dev, seed, rows=None, layers=None):
@@ -585,21 +671,15 @@ def time_oracle(run, budget_s):
 # --------------------------------------------------------------------------- arms
 
 def run_reference(args):
+    """The reference arm: the C++ CPU oracle, single-threaded, on a bounded
+    sample of the workload. Its inputs come from the seeded generator only
+    (drawn on the GPU with torch when one is present, else on the CPU); the
+    CUDA library is neither built nor loaded."""
     world, rank, local = dist_env()
     if rank != 0:
         return 0
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
-    # The oracle runs on the host; inputs come from the same seeded generator.
-    tee = None
-    if dev.type == "cuda":
-        import __graft_entry__
-        __graft_entry__.build()
-        import token_early_exit_gb300 as tee
-    w = make(args.workload, tee, dev, args.seed, args.rows, args.layers) if tee is not None else None
-    if w is None:
-        print(json.dumps({"impl": "reference", "unavailable": "the reference arm needs the seeded inputs on a GPU"}))
-        return 0
-    run, sample = w.oracle_sample()
+    run, sample = oracle_sample(args.workload, dev, args.seed, args.rows, args.layers)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -608,11 +688,14 @@ def run_reference(args):
         units += run()
     el = time.perf_counter() - t0
     v = units / el
-    line = {"metric": getattr(w, "metric", METRIC), "value": v, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
+    line = {"metric": RIVER_METRIC if args.workload.startswith("river") else METRIC, "value": v,
+            "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": w.config(),
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "config": reference_config(args.workload, dev, args.seed, args.rows, args.layers),
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "impl": "C++17, single-threaded, float64", "host_cores": os.cpu_count(),
+                             "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -738,10 +821,10 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        run, sample = w.oracle_sample()
+        run, sample = oracle_sample(args.workload, dev, args.seed, args.rows, args.layers)
         v, el = time_oracle(run, args.cpu_seconds)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
-               "seconds": round(el, 2)}
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "impl": "C++17, single-threaded, float64",
+               "host_cores": os.cpu_count(), "sample": sample, "seconds": round(el, 2)}
 
     line = {"metric": getattr(w, "metric", METRIC), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",

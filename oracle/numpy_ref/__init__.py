@@ -1,24 +1,10 @@
-"""CPU oracle for the token early-exit step (test infrastructure, not product).
+"""Independent float64 numpy restatement of the oracle's definitions (test
+infrastructure, not product).
 
-A plain, slow, obviously correct float64 restatement of what the three source
-pages define: River-LLM's state-transition cosine gate, TIDE's RMSNorm router
-gate and its compaction / exit scatter, and RidgeFill's KV fill (per-layer
-linear map, that layer's own RMSNorm and K/V projection, RoPE on K, store into
-the backbone's cache slot), and River-LLM's Exit River (the W4A16 copies of
-the remaining decoder layers: attention over the shared cache and the FFN).
-Inputs stored in bf16/fp16/fp32 are widened to
-float64 exactly; nothing is rounded on the way except where a page fixes a
-precision (the exit decision, taken in fp32 like the kernels the TIDE notes
-describe).
-
-Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
-and reference arms may import this package. The CUDA library never calls it,
-and it shares no code, table or constant with the CUDA path.
-
-Every function here is pinned by the ``-m "not gpu"`` tests against closed
-forms, invariants, brute force and hand-worked examples; none is marked
-"parity unpinned".
-"""
+The oracle itself is the C++ library of the parent package. This numpy
+version (BLAS products, vectorised) computes the same definitions in a second,
+independent way; ``tests/test_oracle_cross.py`` checks that the two agree.
+Nothing else uses it. Only ``tests/`` may import it."""
 from .gate import (cosine_similarity, cosine_gate, router_probability, router_gate,
                    earliest_exit, layer_ops)  # noqa: F401
 from .compact import stable_partition, gather_rows, exit_scatter  # noqa: F401

@@ -172,6 +172,11 @@ def prefill_inputs(cfg: PrefillFillConfig, seed: int = 0, device="cpu", rows: Op
     return out
 
 
+def river_positions(cfg: RiverConfig, seed: int = 0, device="cpu") -> torch.Tensor:
+    """The exited tokens' cache positions, U[0, cache_len) per sequence."""
+    return randint((cfg.batch,), 0, cfg.cache_len, seed, "pos", device)
+
+
 def river_inputs(cfg: RiverConfig, seed: int = 0, device="cpu", with_cache: bool = True,
                  dtype=torch.bfloat16) -> Dict[str, object]:
     """Inputs of one Exit River pass: the exited tokens' hidden states, their
@@ -179,7 +184,7 @@ def river_inputs(cfg: RiverConfig, seed: int = 0, device="cpu", with_cache: bool
     (every slot) holds random values that the attention reads."""
     n, d, f = cfg.batch, cfg.d, cfg.d_ff
     h = normal((n, d), 1.0, seed, "h_exit", device, dtype)
-    pos = randint((n,), 0, cfg.cache_len, seed, "pos", device)
+    pos = river_positions(cfg, seed, device)
     layers: List[Dict[str, object]] = []
     for j in cfg.river_layers:
         L: Dict[str, object] = {"cache_layer": j}
