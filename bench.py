@@ -368,7 +368,8 @@ class Prefill:
                                rope_base=cfg.rope_base, eps=cfg.eps, dtype=torch.bfloat16, max_pos=cfg.tokens)
         self.units = self.rows
         self.kernel = "kv_fill"
-        self.traffic_key = None
+        full = (self.rows, self.n_layers) == (cfg.filled_rows, len(cfg.fill_layers))
+        self.traffic_key = "kv_fill/prefill-16k" if full and cfg is configs.PREFILL_16K else None
         self.bound = "tensor"
         d, kvw = cfg.d, cfg.kvw
         self.flops = float(self.n_layers) * self.rows * (2 * d * d + 4 * d * kvw)
@@ -784,7 +785,8 @@ def run_gpu(args):
         km = statistics.median(ts)
         gbs = nbytes / (km * 1e-3) / 1e9
         per_kernel[name] = {"us": km * 1e3, "algorithmic_bytes": nbytes, "GB/s": gbs,
-                            "frac": gbs / peaks()["hbm_gbs"], "launches": int(k1)}
+                            "frac": gbs / peaks()["hbm_gbs"], "launches": int(k1),
+                            "traffic": traffic(f"{name}/n{w.n}" if hasattr(w, "n") else None)}
     t_step = statistics.mean(step_ms)
     t_step = max_over_ranks(t_step, world, dev)
     value = job_throughput(w.units, world, t_step)
