@@ -131,15 +131,27 @@ int oc_decide(int64_t n, const double* score, double threshold, int rule, uint8_
 void oc_router_probability(int64_t n, int64_t d, int64_t b, const double* h, const double* w_down,
                            const double* w_up, const double* gamma, const double* b_down, const double* b_up,
                            double eps, double* p) {
+    // u[c] = sum_i W_down[c][i] hn[i] with W_down read through its transpose, so
+    // that the c loop is innermost; each u[c] still adds its terms in the order
+    // i = 0, 1, ...
+    vec wt = zeros(d * b);
+    for (int64_t c = 0; c < b; ++c)
+        for (int64_t i = 0; i < d; ++i) wt[size_t(i * b + c)] = w_down[c * d + i];
     vec hn = zeros(d);
+    vec u = zeros(b);
     for (int64_t t = 0; t < n; ++t) {
         rms_norm_row(h + t * d, gamma, d, eps, hn.data());
+        for (int64_t c = 0; c < b; ++c) u[size_t(c)] = 0.0;
+        for (int64_t i = 0; i < d; ++i) {
+            const double x = hn[size_t(i)];
+            const double* wi = wt.data() + i * b;
+            for (int64_t c = 0; c < b; ++c) u[size_t(c)] += wi[c] * x;
+        }
         double z = 0.0;
         for (int64_t c = 0; c < b; ++c) {
-            double u = 0.0;
-            for (int64_t i = 0; i < d; ++i) u += w_down[c * d + i] * hn[size_t(i)];
-            if (b_down) u += b_down[c];
-            z += w_up[c] * (u * sigmoid(u));
+            double uc = u[size_t(c)];
+            if (b_down) uc += b_down[c];
+            z += w_up[c] * (uc * sigmoid(uc));
         }
         if (b_up) z += b_up[0];
         p[t] = sigmoid(z);
@@ -300,18 +312,21 @@ int oc_ridge_fit(int64_t n, int64_t d, int64_t dout, const double* X, const doub
     vec A = zeros(d * d);
     vec B = zeros(d * dout);
     vec L = zeros(d * d);
-    for (int64_t i = 0; i < d; ++i)
-        for (int64_t j = 0; j < d; ++j) {
-            double s = 0.0;
-            for (int64_t r = 0; r < n; ++r) s += X[r * d + i] * X[r * d + j];
-            A[size_t(i * d + j)] = s + (i == j ? lambda : 0.0);
+    // A[i][j] = sum_r X[r][i] X[r][j], B[i][j] = sum_r X[r][i] Y[r][j]: the row loop
+    // is outermost (one row of X and Y in cache at a time), every entry still adds
+    // its terms in the order r = 0, 1, ...; lambda is added after the sum.
+    for (int64_t r = 0; r < n; ++r) {
+        const double* xr = X + r * d;
+        const double* yr = Y + r * dout;
+        for (int64_t i = 0; i < d; ++i) {
+            const double xi = xr[i];
+            double* ai = A.data() + i * d;
+            double* bi = B.data() + i * dout;
+            for (int64_t j = 0; j < d; ++j) ai[j] += xi * xr[j];
+            for (int64_t j = 0; j < dout; ++j) bi[j] += xi * yr[j];
         }
-    for (int64_t i = 0; i < d; ++i)
-        for (int64_t j = 0; j < dout; ++j) {
-            double s = 0.0;
-            for (int64_t r = 0; r < n; ++r) s += X[r * d + i] * Y[r * dout + j];
-            B[size_t(i * dout + j)] = s;
-        }
+    }
+    for (int64_t i = 0; i < d; ++i) A[size_t(i * d + i)] += lambda;
     for (int64_t j = 0; j < d; ++j) {
         double s = A[size_t(j * d + j)];
         for (int64_t k = 0; k < j; ++k) s -= L[size_t(j * d + k)] * L[size_t(j * d + k)];
@@ -324,18 +339,27 @@ int oc_ridge_fit(int64_t n, int64_t d, int64_t dout, const double* X, const doub
             L[size_t(i * d + j)] = v / ljj;
         }
     }
+    // The substitutions run on whole rows of the right-hand sides (every column
+    // c at once); each entry subtracts its terms in increasing k.
     vec Z = zeros(d * dout);
-    for (int64_t c = 0; c < dout; ++c) {
-        for (int64_t i = 0; i < d; ++i) {   // L Z = B, forward
-            double v = B[size_t(i * dout + c)];
-            for (int64_t k = 0; k < i; ++k) v -= L[size_t(i * d + k)] * Z[size_t(k * dout + c)];
-            Z[size_t(i * dout + c)] = v / L[size_t(i * d + i)];
+    vec v = zeros(dout);
+    for (int64_t i = 0; i < d; ++i) {   // L Z = B, forward
+        for (int64_t c = 0; c < dout; ++c) v[size_t(c)] = B[size_t(i * dout + c)];
+        for (int64_t k = 0; k < i; ++k) {
+            const double lik = L[size_t(i * d + k)];
+            const double* zk = Z.data() + k * dout;
+            for (int64_t c = 0; c < dout; ++c) v[size_t(c)] -= lik * zk[c];
         }
-        for (int64_t i = d - 1; i >= 0; --i) {   // L^T W = Z, backward
-            double v = Z[size_t(i * dout + c)];
-            for (int64_t k = i + 1; k < d; ++k) v -= L[size_t(k * d + i)] * W[k * dout + c];
-            W[i * dout + c] = v / L[size_t(i * d + i)];
+        for (int64_t c = 0; c < dout; ++c) Z[size_t(i * dout + c)] = v[size_t(c)] / L[size_t(i * d + i)];
+    }
+    for (int64_t i = d - 1; i >= 0; --i) {   // L^T W = Z, backward
+        for (int64_t c = 0; c < dout; ++c) v[size_t(c)] = Z[size_t(i * dout + c)];
+        for (int64_t k = i + 1; k < d; ++k) {
+            const double lki = L[size_t(k * d + i)];
+            const double* wk = W + k * dout;
+            for (int64_t c = 0; c < dout; ++c) v[size_t(c)] -= lki * wk[c];
         }
+        for (int64_t c = 0; c < dout; ++c) W[i * dout + c] = v[size_t(c)] / L[size_t(i * d + i)];
     }
     return 0;
 }
