@@ -345,7 +345,8 @@ static tee_status check_fill_desc(const tee_fill_desc* D) {
 
 extern "C" size_t tee_kv_fill_prep_size(const tee_fill_desc* D, int32_t n_layers, int32_t max_pos) {
     if (check_fill_desc(D) != TEE_OK || n_layers < 0 || max_pos <= 0) return 0;
-    return PREP_HEADER_BYTES + fill_tc_prep_bytes(*D, n_layers) + rope_table_bytes(max_pos, D->head_dim);
+    return PREP_HEADER_BYTES + fill_tc_prep_bytes(*D, n_layers) + fill_decode_prep_bytes(*D, n_layers) +
+           rope_table_bytes(max_pos, D->head_dim);
 }
 
 extern "C" tee_status tee_kv_fill_prepare(const tee_fill_desc* D, int32_t n_layers, const tee_fill_layer* layers,
@@ -363,13 +364,16 @@ extern "C" tee_status tee_kv_fill_prepare(const tee_fill_desc* D, int32_t n_laye
     h.max_pos = max_pos;
     h.n_layers = n_layers;
     h.tc_layers = fill_tc_prep_bytes(*D, n_layers) ? n_layers : 0;
+    h.dec_layers = fill_decode_prep_bytes(*D, n_layers) ? n_layers : 0;
     // The header copy is staged from pageable memory before cudaMemcpyAsync returns.
     st = cuda_status(cudaMemcpyAsync(prep, &h, sizeof(h), cudaMemcpyHostToDevice, s));
     if (st != TEE_OK) return st;
     const PrepView pv = prep_view(prep, *D, n_layers);
     st = build_rope_table(const_cast<float2*>(pv.rope), max_pos, D->head_dim / 2, D->rope_base, s);
     if (st != TEE_OK) return st;
-    return fill_tc_prepare(*D, n_layers, layers, const_cast<char*>(pv.tc), s);
+    st = fill_tc_prepare(*D, n_layers, layers, const_cast<char*>(pv.tc), s);
+    if (st != TEE_OK) return st;
+    return fill_decode_prepare(*D, n_layers, layers, const_cast<char*>(pv.dec), s);
 }
 
 extern "C" size_t tee_kv_fill_workspace_size(const tee_fill_desc* D, int32_t n_layers, int32_t n_max) {

@@ -5,15 +5,16 @@
 
 namespace tee {
 
-// Prepared state: header | tensor-core weights (size fixed by desc and layer
-// count) | RoPE table float2 {cos, sin} [max_pos][head_dim/2].
+// Prepared state: header | tensor-core weights | decode-path int4 records (the
+// sizes of both fixed by desc and layer count) | RoPE table float2 {cos, sin}
+// [max_pos][head_dim/2].
 constexpr uint32_t PREP_MAGIC = 0x54454531u;  // "TEE1"
 constexpr size_t PREP_HEADER_BYTES = 256;
 
 struct PrepHeader {
     uint32_t magic;
-    int32_t d, n_kv_heads, head_dim, max_pos, n_layers, tc_layers;
-    int32_t reserved[57];
+    int32_t d, n_kv_heads, head_dim, max_pos, n_layers, tc_layers, dec_layers;
+    int32_t reserved[56];
 };
 static_assert(sizeof(PrepHeader) == PREP_HEADER_BYTES, "prep header size");
 
@@ -43,10 +44,12 @@ struct FillCall {
 struct PrepView {
     const PrepHeader* hdr;  // device pointer
     const char* tc;         // tensor-core weights
+    const char* dec;        // decode-path int4 records
     const float2* rope;     // {cos, sin}
 };
 
 size_t fill_tc_prep_bytes(const tee_fill_desc& D, int n_layers);
+size_t fill_decode_prep_bytes(const tee_fill_desc& D, int n_layers);
 inline size_t rope_table_bytes(int max_pos, int hd) {
     return round_up(static_cast<size_t>(max_pos) * (hd / 2) * sizeof(float2), 256);
 }
@@ -54,7 +57,8 @@ inline PrepView prep_view(const void* prep, const tee_fill_desc& D, int n_layers
     PrepView v;
     v.hdr = static_cast<const PrepHeader*>(prep);
     v.tc = static_cast<const char*>(prep) + PREP_HEADER_BYTES;
-    v.rope = reinterpret_cast<const float2*>(v.tc + fill_tc_prep_bytes(D, n_layers));
+    v.dec = v.tc + fill_tc_prep_bytes(D, n_layers);
+    v.rope = reinterpret_cast<const float2*>(v.dec + fill_decode_prep_bytes(D, n_layers));
     return v;
 }
 
@@ -84,6 +88,9 @@ size_t fill_tc_ws_bytes(const tee_fill_desc& D, int n_layers, int n_max);
 tee_status fill_tc_run(const FillCall& fc);
 
 // Decode path (fill_decode.cu): small item counts; TEE_ERR_UNSUPPORTED otherwise.
+// Prepare repacks the int4 weights into the kernel's per-tile block records.
+tee_status fill_decode_prepare(const tee_fill_desc& D, int n_layers, const tee_fill_layer* layers, char* area,
+                               cudaStream_t s);
 size_t fill_decode_ws_bytes(const tee_fill_desc& D, int n_layers, int n_max);
 tee_status fill_decode_run(const FillCall& fc);
 
