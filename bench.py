@@ -747,10 +747,14 @@ def run_gpu(args):
 
     g_step, sa, sb, k_step = capture(fns)
     g_kern, ka, kb, k_kern = (capture([fns[kidx]]) if len(fns) > 1 else (None, None, None, 0))
+    # the floor of this timing method: one trivial kernel between the same two events
+    one = torch.zeros(1, device=dev)
+    g_floor, fa, fb, _ = capture([lambda: one.add_(1.0)])
     for _ in range(2):
         g_step.replay()
         if g_kern is not None:
             g_kern.replay()
+        g_floor.replay()
     torch.cuda.synchronize(dev)
 
     clocks = Clocks(dev.index)
@@ -769,6 +773,12 @@ def run_gpu(args):
     launches = args.steps * (k_step + k_kern)
     barrier(world)
     clk = clocks.stop()
+    floor_ms = []
+    for _ in range(args.steps):
+        g_floor.replay()
+        torch.cuda.synchronize(dev)
+        floor_ms.append(fa.elapsed_time(fb))
+    floor_ms = statistics.median(floor_ms)
     if g_kern is None:
         kern_ms = step_ms
     # each kernel of the path as its own call, where the workload lists them
@@ -813,13 +823,13 @@ def run_gpu(args):
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "kernel": w.kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic(w.traffic_key), "algorithmic_bytes": work, "kernel_ms": k_ms,
-                "peak_source": pk["source"]}
+                "event_floor_ms": floor_ms, "peak_source": pk["source"]}
     else:
         achieved = work / (k_ms * 1e-3) / 1e12
         peak = pk["bf16_tflops_sustained"] if k_ms > 50 else pk["bf16_tflops"]
         roof = {"bound": "tensor", "kernel": w.kernel, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic(w.traffic_key), "algorithmic_flops": work, "kernel_ms": k_ms,
-                "peak_source": pk["source"]}
+                "event_floor_ms": floor_ms, "peak_source": pk["source"]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -840,7 +850,8 @@ def run_gpu(args):
             "timing": "CUDA-graph replay per step; " + ("L2 flushed inside the graph before the step; "
                                                            if getattr(w, "flush", True) else
                                                            "no flush (every input is larger than L2); ") +
-                      "timed by device events recorded inside the graph around the step",
+                      "timed by device events recorded inside the graph around the step; roofline.event_floor_ms "
+                      "is the same interval around one trivial kernel (part of every kernel_ms)",
             "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)}}
     if rank == 0:
         print(json.dumps(line))

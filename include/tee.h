@@ -338,7 +338,7 @@ typedef struct {
     int32_t dtype;        /* h_split, w_map, gamma, dense wk/wv and the caches */
     int32_t wfmt;         /* TEE_W_DENSE or TEE_W_INT4 for wk/wv */
     int32_t group;        /* int4 group length along d (multiple of 16) */
-    int32_t flags;        /* 0, or TEE_FILL_EARLY_WEIGHTS */
+    int32_t flags;        /* 0, or TEE_FILL_EARLY_WEIGHTS and/or TEE_FILL_GENERIC */
 } tee_fill_desc;
 
 /* tee_fill_desc.flags. TEE_FILL_EARLY_WEIGHTS: the decode kernel may start while
@@ -348,6 +348,12 @@ typedef struct {
  * that kernel has completed (programmatic dependent launch). Set it only when
  * that kernel does not write the weights. Ignored by the other paths. */
 #define TEE_FILL_EARLY_WEIGHTS 1
+/* tee_fill_desc.flags. TEE_FILL_GENERIC: run the call on the generic CUDA-core
+ * kernels (a GEMM, RMS and RoPE/store launch per step and layer) even where a
+ * fused path (tensor-core prefill, int4 decode, small dense one-launch fill)
+ * takes it; same results within rounding. For checking one path against
+ * another. */
+#define TEE_FILL_GENERIC 2
 
 /* Weights of one filled layer j (device pointers). kvw = n_kv_heads*head_dim. */
 typedef struct {

@@ -178,3 +178,14 @@ def test_static_router_fault_query_answers_without_a_device(lib):
     assert lib.tee_exit_gate_router_static_device_error(ctypes.byref(code), ctypes.byref(detail),
                                                         None) == _lib.TEE_ERR_CUDA
     assert lib.tee_exit_gate_router_static_clear_error(None) == _lib.TEE_ERR_CUDA
+
+
+def test_fill_descriptor_flags(lib):
+    from token_early_exit_gb300 import _lib
+    def size(flags):
+        D = _lib.FillDesc(d=256, n_kv_heads=2, head_dim=64, rope_base=1e4, eps=1e-5, dtype=_lib.TEE_F32,
+                          wfmt=_lib.TEE_W_DENSE, group=64, flags=flags)
+        return lib.tee_kv_fill_workspace_size(ctypes.byref(D), 2, 8)
+    assert size(0) > 0
+    assert size(_lib.TEE_FILL_EARLY_WEIGHTS | _lib.TEE_FILL_GENERIC) == size(0)
+    assert size(4) == 0   # an unknown flag is rejected

@@ -52,9 +52,10 @@ def _add_variants(layers, kvw, hd, dtype, seed, kind):
     return layers
 
 
-def _make(tee, cfg, layers, dtype, max_pos, int4=False):
+def _make(tee, cfg, layers, dtype, max_pos, int4=False, generic=False):
     return tee.KVFill(layers, d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim, rope_base=cfg.rope_base,
-                      eps=cfg.eps, dtype=dtype, max_pos=max_pos, int4=int4, group=getattr(cfg, "group", 64))
+                      eps=cfg.eps, dtype=dtype, max_pos=max_pos, int4=int4, group=getattr(cfg, "group", 64),
+                      generic=generic)
 
 
 @pytest.mark.parametrize("kind", sorted(VARIANTS))
@@ -62,7 +63,7 @@ def test_generic_fill_variants(tee, kind):
     cfg = configs.TINY_DECODE
     x = gen.decode_inputs(cfg, seed=11, device=DEV)
     _add_variants(x["layers"], cfg.n_kv_heads * cfg.head_dim, cfg.head_dim, torch.float32, 11, kind)
-    f = _make(tee, cfg, x["layers"], torch.float32, cfg.cache_len)
+    f = _make(tee, cfg, x["layers"], torch.float32, cfg.cache_len, generic=True)
     rows = np.array([5, 0, 7, 2, 3], dtype=np.int32)
     ws = tee.Workspace(DEV)
     f(x["h_cur"], x["k_cache"], x["v_cache"], rows=torch.from_numpy(rows).to(DEV), pos=x["pos"], seq=x["seq"], ws=ws)

@@ -339,7 +339,7 @@ static tee_status check_fill_desc(const tee_fill_desc* D) {
     if (dtype_bytes(D->dtype) == 0) return TEE_ERR_UNSUPPORTED;
     if (D->wfmt != TEE_W_DENSE && D->wfmt != TEE_W_INT4) return TEE_ERR_UNSUPPORTED;
     if (D->wfmt == TEE_W_INT4 && (D->group <= 0 || D->group % 16 || D->d % D->group)) return TEE_ERR_INVALID_ARG;
-    if (D->flags & ~TEE_FILL_EARLY_WEIGHTS) return TEE_ERR_INVALID_ARG;
+    if (D->flags & ~(TEE_FILL_EARLY_WEIGHTS | TEE_FILL_GENERIC)) return TEE_ERR_INVALID_ARG;
     return TEE_OK;
 }
 
@@ -417,10 +417,14 @@ extern "C" tee_status tee_kv_fill(const tee_fill_desc* D, int32_t n_layers, cons
     }
     FillCall fc{D, n_layers, layers, prep, prep_bytes, n_max, n_dev, h_split, ld_h, h_rows, rows, pos, pos0, seq,
                 k_cache, v_cache, cache, ws, ws_bytes, static_cast<cudaStream_t>(stream)};
-    st = fill_tc_run(fc);
-    if (st != TEE_ERR_UNSUPPORTED) return st;
-    st = fill_decode_run(fc);
-    if (st != TEE_ERR_UNSUPPORTED) return st;
+    if (!(D->flags & TEE_FILL_GENERIC)) {
+        st = fill_tc_run(fc);
+        if (st != TEE_ERR_UNSUPPORTED) return st;
+        st = fill_decode_run(fc);
+        if (st != TEE_ERR_UNSUPPORTED) return st;
+        st = fill_small_run(fc);
+        if (st != TEE_ERR_UNSUPPORTED) return st;
+    }
     switch (D->dtype) {
         case TEE_F32: return run_generic<float>(fc);
         case TEE_F16: return run_generic<__half>(fc);

@@ -94,4 +94,8 @@ tee_status fill_decode_prepare(const tee_fill_desc& D, int n_layers, const tee_f
 size_t fill_decode_ws_bytes(const tee_fill_desc& D, int n_layers, int n_max);
 tee_status fill_decode_run(const FillCall& fc);
 
+// Small dense fill (fill_small.cu): the whole chain in one cluster launch for a
+// few items on a small model; TEE_ERR_UNSUPPORTED otherwise.
+tee_status fill_small_run(const FillCall& fc);
+
 }  // namespace tee

@@ -256,16 +256,18 @@ class KVFill:
     ``w_map`` [d][d] and, for int4, ``k_scale``, ``k_zero``, ``v_scale``,
     ``v_zero`` [d/group][kvw] fp16, plus the int ``cache_layer``. Model-family
     variants: ``k_bias``, ``v_bias`` [kvw] and ``k_norm`` [head_dim] tensors, and
-    ``writes`` = "k" or "v" to fill only one of the caches.
+    ``writes`` = "k" or "v" to fill only one of the caches. ``generic`` runs
+    every call on the generic CUDA-core kernels (for checking the fused paths).
     """
 
     def __init__(self, layers: Sequence[Dict], *, d: int, n_kv_heads: int, head_dim: int, rope_base: float,
                  eps: float, dtype: torch.dtype, max_pos: int, int4: bool = False, group: int = 64,
-                 early_weights: bool = False):
+                 early_weights: bool = False, generic: bool = False):
         self.lib = load()
         self.desc = FillDesc(d=d, n_kv_heads=n_kv_heads, head_dim=head_dim, rope_base=float(rope_base),
                              eps=float(eps), dtype=_DT[dtype], wfmt=_lib.TEE_W_INT4 if int4 else _lib.TEE_W_DENSE,
-                             group=group, flags=_lib.TEE_FILL_EARLY_WEIGHTS if early_weights else 0)
+                             group=group, flags=(_lib.TEE_FILL_EARLY_WEIGHTS if early_weights else 0)
+                             | (_lib.TEE_FILL_GENERIC if generic else 0))
         self.keep: List[torch.Tensor] = []
         arr = (FillLayer * max(1, len(layers)))()
         dev = None
