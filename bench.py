@@ -8,7 +8,8 @@ A step is one pass of the whole hot path over one batch of synthetic input:
       exit scatter (the three in one launch) -> KV fill of 8 layers (identity
       map, int4 Wk/Wv), for a 64-token Llama-3.2-1B-shaped decode batch;
   decode-tiny: the same on the tiny fp32 workload;
-  router-4096: router gate -> compaction with gather, 4096 tokens, d = 4096;
+  router-32 / router-4096: router gate -> compaction with gather, 32 or 4096
+      tokens, d = 4096;
   router-65536: the same at 65,536 tokens (inputs far larger than L2), with the
       cosine gate and the exit scatter at that batch timed alongside;
   prefill-16k / prefill-120k: the RidgeFill KV fill of every layer after the
@@ -51,7 +52,7 @@ from workloads import configs, gen  # noqa: E402
 
 METRIC = "tokens/s through exit gate+compact+KV fill"
 RIVER_METRIC = "tokens/s through the Exit River (W4A16 exit layers)"
-WORKLOADS = ("decode-1b", "decode-tiny", "router-4096", "router-65536", "prefill-16k", "prefill-120k", "river-1b",
+WORKLOADS = ("decode-1b", "decode-tiny", "router-32", "router-4096", "router-65536", "prefill-16k", "prefill-120k", "river-1b",
              "river-tiny")
 
 
@@ -152,8 +153,8 @@ def reference_config(name, dev, seed=0, rows=None, layers=None):
     if name in ("decode-1b", "decode-tiny"):
         cfg = configs.LLAMA1B_DECODE if name == "decode-1b" else configs.TINY_DECODE
         return decode_config(cfg, "exit" if cfg.rule == "batch_all" else "default")
-    if name in ("router-4096", "router-65536"):
-        n = 4096 if name == "router-4096" else (rows or 65536)
+    if name in ("router-32", "router-4096", "router-65536"):
+        n = {"router-32": 32, "router-4096": 4096}.get(name) or (rows or 65536)
         return router_config(configs.ROUTER_4096, n, 0.5, router_flush(configs.ROUTER_4096, n, dev))
     if name in ("prefill-16k", "prefill-120k"):
         cfg = configs.PREFILL_16K if name == "prefill-16k" else configs.PREFILL_120K
@@ -503,10 +504,10 @@ def oracle_sample(name, dev, seed=0, rows=None, layers=None):
             oracle.exit_scatter(np.zeros_like(hc), hc, r, r)
             return cfg.batch
         return run, "one full decode step (all tokens)"
-    if name in ("router-4096", "router-65536"):
+    if name in ("router-32", "router-4096", "router-65536"):
         cfg = configs.ROUTER_4096
-        n = 4096 if name == "router-4096" else (rows or 65536)
-        k, m, theta = cfg.checkpoints[0], 256, 0.5
+        n = {"router-32": 32, "router-4096": 4096}.get(name) or (rows or 65536)
+        k, m, theta = cfg.checkpoints[0], min(256, n), 0.5
         w = _host(gen.router_weights(cfg, k, seed=seed, device=dev))
         h = _host(gen.router_hidden(cfg, n, k, seed=seed, device=dev)[:m])
 
@@ -569,6 +570,8 @@ def make(name, tee, dev, seed, rows=None, layers=None):
         return Decode(tee, configs.LLAMA1B_DECODE, dev, seed)
     if name == "decode-tiny":
         return Decode(tee, configs.TINY_DECODE, dev, seed)
+    if name == "router-32":
+        return Router(tee, configs.ROUTER_4096, dev, seed, n=32)
     if name == "router-4096":
         return Router(tee, configs.ROUTER_4096, dev, seed)
     if name == "router-65536":
