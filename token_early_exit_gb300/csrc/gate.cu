@@ -237,21 +237,31 @@ router_dot_kernel(int n, int d, int b, const T* __restrict__ h, int64_t ldh, con
 #pragma unroll
         for (int tt = 0; tt < RT_TOK; ++tt) acc[tt] = 0.f;
         const T* wrow = wd + static_cast<int64_t>(c) * d;
-        for (int i = lane * 8; i < d; i += 256) {
-            float w[8];
-            load8(wrow + i, w);
+        // RT_WB pieces of the row per lane in flight: their loads are issued before
+        // any of them is used (one round trip per batch, not per piece)
+        constexpr int RT_WB = 4;
+        for (int i0 = lane * 8; i0 < d; i0 += 256 * RT_WB) {
+            float w[RT_WB][8];
 #pragma unroll
-            for (int tt = 0; tt < RT_TOK; ++tt) {
-                const float4 x0 = *reinterpret_cast<const float4*>(s_h + tt * d + i);
-                const float4 x1 = *reinterpret_cast<const float4*>(s_h + tt * d + i + 4);
-                acc[tt] = fmaf(w[0], x0.x, acc[tt]);
-                acc[tt] = fmaf(w[1], x0.y, acc[tt]);
-                acc[tt] = fmaf(w[2], x0.z, acc[tt]);
-                acc[tt] = fmaf(w[3], x0.w, acc[tt]);
-                acc[tt] = fmaf(w[4], x1.x, acc[tt]);
-                acc[tt] = fmaf(w[5], x1.y, acc[tt]);
-                acc[tt] = fmaf(w[6], x1.z, acc[tt]);
-                acc[tt] = fmaf(w[7], x1.w, acc[tt]);
+            for (int u = 0; u < RT_WB; ++u)
+                if (i0 + 256 * u < d) load8(wrow + i0 + 256 * u, w[u]);
+#pragma unroll
+            for (int u = 0; u < RT_WB; ++u) {
+                const int i = i0 + 256 * u;
+                if (i >= d) break;
+#pragma unroll
+                for (int tt = 0; tt < RT_TOK; ++tt) {
+                    const float4 x0 = *reinterpret_cast<const float4*>(s_h + tt * d + i);
+                    const float4 x1 = *reinterpret_cast<const float4*>(s_h + tt * d + i + 4);
+                    acc[tt] = fmaf(w[u][0], x0.x, acc[tt]);
+                    acc[tt] = fmaf(w[u][1], x0.y, acc[tt]);
+                    acc[tt] = fmaf(w[u][2], x0.z, acc[tt]);
+                    acc[tt] = fmaf(w[u][3], x0.w, acc[tt]);
+                    acc[tt] = fmaf(w[u][4], x1.x, acc[tt]);
+                    acc[tt] = fmaf(w[u][5], x1.y, acc[tt]);
+                    acc[tt] = fmaf(w[u][6], x1.z, acc[tt]);
+                    acc[tt] = fmaf(w[u][7], x1.w, acc[tt]);
+                }
             }
         }
 #pragma unroll
