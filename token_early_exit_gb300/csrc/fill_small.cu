@@ -112,11 +112,22 @@ __device__ __forceinline__ void sf_cluster_arrive() {
 __device__ __forceinline__ void sf_cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float sf_ld_peer(const float* local, int rank) {
+__device__ __forceinline__ uint32_t sf_peer(const float* local, int rank) {
     uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float sf_ld_peer(const float* local, int rank) {
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(sf_peer(local, rank)) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 sf_ld_peer4(const float* local, int rank) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(sf_peer(local, rank))
+                 : "memory");
     return v;
 }
 
@@ -318,17 +329,43 @@ fill_small_kernel(const __grid_constant__ SmallArgs a, void* ws) {
         }
         sf_cluster_arrive();
         sf_cluster_wait();   // every CTA's slice and partial sums are complete
-        if (threadIdx.x < n) {
+        if (threadIdx.x < n) {   // the eight partial sums: every load issued before the first add
             const int m = threadIdx.x;
+            float v[SF_CLUSTER];
+#pragma unroll
+            for (int q = 0; q < SF_CLUSTER; ++q) v[q] = sf_ld_peer(ssp + m, q);
             float s = 0.f;
-            for (int q = 0; q < SF_CLUSTER; ++q) s += sf_ld_peer(ssp + m, q);
+#pragma unroll
+            for (int q = 0; q < SF_CLUSTER; ++q) s += v[q];
             rs[m] = 1.0f / sqrtf(s / static_cast<float>(d) + a.eps);
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < n * d; i += SF_THREADS) {
-            const int m = i / d, k = i - m * d;
-            const int q = k / cpc;
-            As[i] = sf_ld_peer(xs + m * cpc + (k - q * cpc), q) * rs[m] * to_f32(gamma[k]);
+        // x^ rows from the eight slices: 16-byte loads, four per thread in flight
+        const int c4n = cpc / 4, per_m = SF_CLUSTER * c4n, total4 = n * per_m;
+        for (int i0 = threadIdx.x; i0 < total4; i0 += 4 * SF_THREADS) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * SF_THREADS;
+                if (i < total4) {
+                    const int m = i / per_m, r = i - m * per_m, q = r / c4n, c4 = r - q * c4n;
+                    v[u] = sf_ld_peer4(xs + m * cpc + 4 * c4, q);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * SF_THREADS;
+                if (i < total4) {
+                    const int m = i / per_m, r = i - m * per_m, q = r / c4n, c4 = r - q * c4n;
+                    const int k = q * cpc + 4 * c4;
+                    const float sc = rs[m];
+                    float* dst = As + m * d + k;
+                    dst[0] = v[u].x * sc * to_f32(gamma[k]);
+                    dst[1] = v[u].y * sc * to_f32(gamma[k + 1]);
+                    dst[2] = v[u].z * sc * to_f32(gamma[k + 2]);
+                    dst[3] = v[u].w * sc * to_f32(gamma[k + 3]);
+                }
+            }
         }
         sf_cluster_arrive();   // this CTA has read its peers' slices (waited on before exit)
     } else {
