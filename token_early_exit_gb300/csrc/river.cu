@@ -91,6 +91,7 @@ constexpr int MAX_KS = 8;        // K splits = CTAs of a cluster (portable size)
 constexpr int MAX_ITEMS = 128;
 
 int at_chunk(int hd) { return hd == 64 ? 256 : 128; }
+constexpr int KG_CNT = 64 * 8;   // counters of the two-cluster K split: tiles (<= 64) x ks (<= 8)
 
 int max_clusters(int ks);
 
@@ -104,6 +105,18 @@ int choose_ks(int tiles, int K) {
            tiles <= max_clusters(ks * 2))
         ks *= 2;
     return ks;
+}
+
+// K groups for the residual GEMMs (O, DOWN): a second cluster of ks CTAs per tile
+// when the doubled grid still fits the SMs and each split keeps eight 64-input
+// blocks (with fewer, as in the 2048-input o projection, the extra launch width
+// costs more than it brings: 13.2 us against 11.8 us measured).
+int choose_kg(int tiles, int ks, int K) {
+    const int sms = sm_count();
+    return (ks >= 2 && tiles * ks * 2 <= sms && tiles * ks <= KG_CNT && K % (ks * 2 * GT_K) == 0 &&
+            K / (ks * 2) >= 8 * GT_K)
+               ? 2
+               : 1;
 }
 
 RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
@@ -128,7 +141,7 @@ RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
     w.ss_f = take(n * 4);
     w.ipos = take(n * 4);
     w.iseq = take(n * 4);
-    w.acnt = take(n * D.n_kv_heads * 4);
+    w.acnt = take(n * D.n_kv_heads * 4 + KG_CNT * 4);   // then the K groups' counters (tiles x ks)
     w.apart = take(n * D.n_kv_heads * chunks * rep * (D.head_dim + 2) * 4);
     w.end = o;
     return w;
@@ -237,6 +250,11 @@ struct GemmArgs {
     CUtensorMap tm_a;       // A [128][K] bf16 as K/64 blocks, box 2 blocks x a_rows x 64, 128-byte swizzle
     const uint8_t* blob;    // packed weights [tile][K/64][G_W_BYTES]
     int K, N, ks;
+    // K groups: kg clusters of ks CTAs per tile, each over 1/kg of K (O and DOWN only);
+    // with kg = 2 both add their sums into the residual and the second to arrive
+    // (kg_cnt[tile][rank], zero between calls) finishes the tile's columns
+    int kg;
+    int32_t* kg_cnt;
     int n_max;
     const int32_t* n_dev;
     const bf16* a;          // [128][lda]
@@ -316,6 +334,8 @@ __device__ __forceinline__ float4 tile_sum4(const float* P, int ks, int m, int c
     return a;
 }
 
+__device__ __forceinline__ void finish_residual(const GemmArgs& g, float4 v, int m, int col, int gpr);
+
 // The tile's epilogue for this CTA's share of it (groups [rank * gpr, (rank + 1) * gpr)
 // of four consecutive columns, pairs or units); a thread takes one group of one item.
 template <int MODE>
@@ -374,32 +394,65 @@ __device__ void finish_tile(const GemmArgs& g, const float* P, int t, int n, int
             const int lc = 4 * grp, col = c0 + lc;
             float4* rp = reinterpret_cast<float4*>(g.resid + static_cast<int64_t>(m) * g.d + col);
             const float4 sum = tile_sum4(P, g.ks, m, lc);
+            if (g.kg > 1) {   // the other K group adds its part too; the second to arrive finishes below
+                atomicAdd(&rp->x, sum.x);
+                atomicAdd(&rp->y, sum.y);
+                atomicAdd(&rp->z, sum.z);
+                atomicAdd(&rp->w, sum.w);
+                continue;
+            }
             float4 v = *rp;
             v.x += sum.x;
             v.y += sum.y;
             v.z += sum.z;
             v.w += sum.w;
             *rp = v;
-            if (g.h_out) {
-                if (g.ipos[m] >= 0)
-                    *reinterpret_cast<uint2*>(g.h_out + static_cast<int64_t>(m) * g.ld_out + col) =
-                        pack4_bf16(v.x, v.y, v.z, v.w);
-            } else {
-                const uint2 gg = *reinterpret_cast<const uint2*>(g.next_gain + col);
-                float g0, g1, g2, g3;
-                unpack_bf16x2(gg.x, g0, g1);
-                unpack_bf16x2(gg.y, g2, g3);
-                *reinterpret_cast<uint2*>(g.next_a + static_cast<int64_t>(m) * g.d + col) =
-                    pack4_bf16(v.x * g0, v.y * g1, v.z * g2, v.w * g3);
-                // the item's gpr consecutive lanes (gpr a power of two <= 32) sum their squares
-                float sq = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-                const int lane = tid & 31;
-                const unsigned seg = gpr >= 32 ? 0xFFFFFFFFu : ((1u << gpr) - 1u) << (lane & ~(gpr - 1));
-                for (int o = 1; o < gpr; o <<= 1) sq += __shfl_xor_sync(seg, sq, o);
-                if ((lane & (gpr - 1)) == 0) atomicAdd(g.ss_out + m, sq);
-            }
+            finish_residual(g, v, m, col, gpr);
         }
     }
+    if ((MODE == M_O || MODE == M_DOWN) && g.kg > 1) {
+        // both K groups' sums are in the residual once the second group's CTA of this
+        // rank arrives: it writes the next normalised input (or the output)
+        __shared__ int s_second;
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"r"(G_EPI_THREADS) : "memory");
+        if (tid == 0) {
+            int32_t* ctr = g.kg_cnt + t * g.ks + rank;
+            const int prev = atomicAdd(ctr, 1);
+            s_second = prev == g.kg - 1;
+            if (s_second) *ctr = 0;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(G_EPI_THREADS) : "memory");
+        if (!s_second) return;
+        __threadfence();
+        for (int idx = tid; idx < n * gpr; idx += G_EPI_THREADS) {
+            const int m = idx / gpr, col = c0 + 4 * (rank * gpr + idx % gpr);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(g.resid + static_cast<int64_t>(m) * g.d + col));
+            finish_residual(g, v, m, col, gpr);
+        }
+    }
+}
+
+// After the residual update of (item m, columns col .. col + 3): the output row
+// (last layer), or the next normalised input and its sum of squares.
+__device__ __forceinline__ void finish_residual(const GemmArgs& g, float4 v, int m, int col, int gpr) {
+    if (g.h_out) {
+        if (g.ipos[m] >= 0)
+            *reinterpret_cast<uint2*>(g.h_out + static_cast<int64_t>(m) * g.ld_out + col) = pack4_bf16(v.x, v.y, v.z, v.w);
+        return;
+    }
+    const uint2 gg = *reinterpret_cast<const uint2*>(g.next_gain + col);
+    float g0, g1, g2, g3;
+    unpack_bf16x2(gg.x, g0, g1);
+    unpack_bf16x2(gg.y, g2, g3);
+    *reinterpret_cast<uint2*>(g.next_a + static_cast<int64_t>(m) * g.d + col) =
+        pack4_bf16(v.x * g0, v.y * g1, v.z * g2, v.w * g3);
+    // the item's gpr consecutive lanes (gpr a power of two <= 32) sum their squares
+    float sq = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    const int lane = threadIdx.x & 31;
+    const unsigned seg = gpr >= 32 ? 0xFFFFFFFFu : ((1u << gpr) - 1u) << (lane & ~(gpr - 1));
+    for (int o = 1; o < gpr; o <<= 1) sq += __shfl_xor_sync(seg, sq, o);
+    if ((lane & (gpr - 1)) == 0) atomicAdd(g.ss_out + m, sq);
 }
 
 // NB consecutive packed weight blocks (G_W_BYTES apart from wst) -> NB bf16 B
@@ -480,11 +533,12 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t = blockIdx.x, sp = blockIdx.y;   // sp: the CTA's rank in its cluster
+    const int t = blockIdx.x, sp = static_cast<int>(blockIdx.y) % g.ks;   // sp: the CTA's rank in its cluster
+    const int kgi = static_cast<int>(blockIdx.y) / g.ks;                     // its K group
     const int n = item_count(g.n_max, g.n_dev);
     allow_dependents();   // the next kernel of the river may start launching
     if (n == 0) return;   // every CTA of the cluster leaves here
-    const int kc = g.K / g.ks, k0 = sp * kc, nkb = kc / GT_K;
+    const int kc = g.K / (g.ks * g.kg), k0 = (kgi * g.ks + sp) * kc, nkb = kc / GT_K;
 
     if (tid == 0) {
         for (int i = 0; i < G_WS; ++i) {
@@ -509,7 +563,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
     // the producer streams the first stages' weights before it waits for the
     // previous kernel; everything else waits first.
     if (!(warp == G_PROD_WARP && lane == 0)) wait_prior_grid();
-    if (g.ss_zero && t == 0 && sp == 0)
+    if (g.ss_zero && t == 0 && blockIdx.y == 0)
         for (int i = tid; i < g.n_max; i += G_THREADS) g.ss_zero[i] = 0.f;
 
     const int nst = (nkb + G_BPS - 1) / G_BPS;
@@ -1120,7 +1174,7 @@ tee_status launch_gemm(const GemmArgs& g0, void* ws, cudaStream_t s) {
         attr = true;
     }
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(g.N / GT_N, g.ks);
+    cfg.gridDim = dim3(g.N / GT_N, g.ks * g.kg);
     cfg.blockDim = dim3(G_THREADS);
     cfg.dynamicSmemBytes = G_SMEM;
     cfg.stream = s;
@@ -1258,11 +1312,12 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     ga.ipos = ipos;
     ga.iseq = iseq;
     ga.cnt = acnt;
-    ga.n_cnt = n_max * D->n_kv_heads;
+    ga.n_cnt = n_max * D->n_kv_heads + KG_CNT;
     river_gather_kernel<<<n_max, 256, 0, s>>>(ga, ws);
     if ((st = launch_status()) != TEE_OK) return st;
 
     GemmArgs g{};
+    g.kg_cnt = acnt + static_cast<int64_t>(n_max) * D->n_kv_heads;   // cleared with the attention's
     g.n_max = n_max;
     g.n_dev = n_dev;
     g.eps = D->eps;
@@ -1313,6 +1368,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         g.K = d;
         g.N = qw + 2 * kvw;
         g.ks = choose_ks(g.N / GT_N, d);
+        g.kg = 1;
         g.a = abuf;
         g.lda = d;
         g.ss_in = ss_a;
@@ -1330,6 +1386,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         g.K = qw;
         g.N = d;
         g.ks = choose_ks(d / GT_N, qw);
+        g.kg = choose_kg(d / GT_N, g.ks, qw);
         g.a = obuf;
         g.lda = qw;
         g.ss_in = nullptr;
@@ -1343,6 +1400,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         g.K = d;
         g.N = 2 * f;
         g.ks = choose_ks(g.N / GT_N, d);
+        g.kg = 1;
         g.a = abuf;
         g.lda = d;
         g.ss_in = ss_f;
@@ -1353,6 +1411,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         g.K = f;
         g.N = d;
         g.ks = choose_ks(d / GT_N, f);
+        g.kg = choose_kg(d / GT_N, g.ks, f);
         g.a = act;
         g.lda = f;
         g.ss_in = nullptr;
