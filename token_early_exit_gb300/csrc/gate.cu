@@ -332,6 +332,159 @@ router_finalize_kernel(int n, int d, int b, float eps, float* __restrict__ dots,
                     ws_counter(ws, WS_CNT_ROUTER));
 }
 
+// Router gate for small batches (TIDE formula 3; module 4 "Fused LayerNorm +
+// Route") in one launch. CTA (kb, th) takes the 64 inputs [64 kb, 64 kb + 64)
+// of tokens [32 th, 32 th + 32): it stages their rows (gamma applied) and adds
+// the rows' partial sums of squares, then thread (c, half) forms channel c's
+// partial dot products with the tokens of its half (tokens 2 j + half) and adds
+// them into the workspace's dots[t][c]; the last CTA to finish (a counter)
+// finishes every token: 1/rms, b_down, SiLU, w_up, b_up, sigmoid, threshold,
+// the batch flag, and leaves dots and sums of squares cleared for the next call.
+constexpr int RS_TOK = 32, RS_K = 64, RS_THREADS = 256, RS_LD = RS_K + 4;
+constexpr int RS_MAX_TOKENS = 64;
+
+template <typename T>
+__global__ void __launch_bounds__(RS_THREADS)
+router_small_kernel(int n, int d, int b, const T* __restrict__ h, int64_t ldh, const T* __restrict__ gamma,
+                    const T* __restrict__ wd, float* __restrict__ dots, float* __restrict__ sumsq,
+                    const float* __restrict__ b_down, const T* __restrict__ w_up, const float* __restrict__ b_up,
+                    float eps, float thr, int rule, bool need_flag, float* __restrict__ score,
+                    uint8_t* __restrict__ mask, int32_t* __restrict__ flag, uint32_t* __restrict__ counter) {
+    __shared__ __align__(16) float s_h[RS_TOK][RS_LD];
+    __shared__ float s_min[RS_THREADS / 32];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int k0 = blockIdx.x * RS_K, t0 = blockIdx.y * RS_TOK;
+    const int nt = min(RS_TOK, n - t0);
+    {   // rows: eight threads per token row, eight inputs each
+        const int tt = tid >> 3, e0 = (tid & 7) * 8;
+        float x[8], g[8];
+        if (tt < nt) {
+            load8(h + static_cast<int64_t>(t0 + tt) * ldh + k0 + e0, x);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        if (gamma) {
+            load8(gamma + k0 + e0, g);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) g[e] = 1.f;
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            ss = fmaf(x[e], x[e], ss);
+            s_h[tt][e0 + e] = x[e] * g[e];
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+        if ((tid & 7) == 0 && tt < nt) atomicAdd(sumsq + t0 + tt, ss);
+    }
+    __syncthreads();
+    {   // channel c = tid / 2, tokens 2 j + (tid & 1)
+        const int c = tid >> 1, half = tid & 1;
+        if (c < b) {
+            float acc[RS_TOK / 2];
+#pragma unroll
+            for (int j = 0; j < RS_TOK / 2; ++j) acc[j] = 0.f;
+            const T* wr = wd + static_cast<int64_t>(c) * d + k0;
+            float w[RS_K / 8][8];
+#pragma unroll
+            for (int q = 0; q < RS_K / 8; ++q) load8(wr + 8 * q, w[q]);   // the whole slice in flight
+#pragma unroll
+            for (int q = 0; q < RS_K / 8; ++q)
+#pragma unroll
+                for (int j = 0; j < RS_TOK / 2; ++j) {
+                    const float4 a0 = *reinterpret_cast<const float4*>(&s_h[2 * j + half][8 * q]);
+                    const float4 a1 = *reinterpret_cast<const float4*>(&s_h[2 * j + half][8 * q + 4]);
+                    float v = acc[j];
+                    v = fmaf(w[q][0], a0.x, v);
+                    v = fmaf(w[q][1], a0.y, v);
+                    v = fmaf(w[q][2], a0.z, v);
+                    v = fmaf(w[q][3], a0.w, v);
+                    v = fmaf(w[q][4], a1.x, v);
+                    v = fmaf(w[q][5], a1.y, v);
+                    v = fmaf(w[q][6], a1.z, v);
+                    v = fmaf(w[q][7], a1.w, v);
+                    acc[j] = v;
+                }
+#pragma unroll
+            for (int j = 0; j < RS_TOK / 2; ++j)
+                if (2 * j + half < nt) atomicAdd(dots + static_cast<int64_t>(t0 + 2 * j + half) * b + c, acc[j]);
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(counter, 1u);
+        s_last = prev == gridDim.x * gridDim.y - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // the last CTA: warp w finishes tokens w, w + 8, ... (every load of them issued first)
+    float wmin = INFINITY;
+    constexpr int MAXC = 4;                                    // channels per lane (b <= 128)
+    constexpr int TPW = RS_MAX_TOKENS / (RS_THREADS / 32);     // tokens per warp
+    float wu[MAXC], bd[MAXC], u[TPW][MAXC], ssq[TPW];
+#pragma unroll
+    for (int j = 0; j < MAXC; ++j) {
+        const int c = lane + 32 * j;
+        wu[j] = c < b ? to_f32(w_up[c]) : 0.f;
+        bd[j] = (c < b && b_down) ? b_down[c] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+        const int t = warp + i * (RS_THREADS / 32);
+        ssq[i] = t < n ? __ldcg(sumsq + t) : 0.f;
+#pragma unroll
+        for (int j = 0; j < MAXC; ++j) {
+            const int c = lane + 32 * j;
+            u[i][j] = (t < n && c < b) ? __ldcg(dots + static_cast<int64_t>(t) * b + c) : 0.f;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+        const int t = warp + i * (RS_THREADS / 32);
+        if (t >= n) break;   // warp-uniform
+#pragma unroll
+        for (int j = 0; j < MAXC; ++j)
+            if (lane + 32 * j < b) dots[static_cast<int64_t>(t) * b + lane + 32 * j] = 0.f;   // cleared for the next call
+        if (lane == 0) sumsq[t] = 0.f;
+        const float r = 1.0f / sqrtf(ssq[i] / static_cast<float>(d) + eps);
+        float z = 0.f;
+#pragma unroll
+        for (int j = 0; j < MAXC; ++j) {
+            const float x = u[i][j] * r + bd[j];
+            z = fmaf(wu[j], __fdividef(x, 1.0f + __expf(-x)), z);   // SiLU
+        }
+        z = warp_sum(z);
+        if (b_up) z += b_up[0];
+        const float p = __fdividef(1.0f, 1.0f + __expf(-z));
+        if (lane == 0) {
+            score[t] = p;
+            if (rule == TEE_RULE_PER_TOKEN) mask[t] = exits(p, thr);
+        }
+        wmin = fminf(wmin, p == p ? p : -INFINITY);
+    }
+    if (tid == 0) *counter = 0u;
+    if (!need_flag) return;
+    if (lane == 0) s_min[warp] = wmin;
+    __syncthreads();
+    float m = tid < RS_THREADS / 32 ? s_min[tid] : INFINITY;
+    if (warp == 0) {
+        m = warp_min(m);
+        if (lane == 0) s_min[0] = m;
+    }
+    __syncthreads();
+    const uint8_t f = (n > 0 && s_min[0] > thr) ? 1 : 0;
+    if (tid == 0 && flag) *flag = f;
+    if (rule == TEE_RULE_BATCH_ALL)
+        for (int t = tid; t < n; t += RS_THREADS) mask[t] = f;
+}
+
 // Whole router gate on the tensor cores (router_tc.cu). Returns TEE_ERR_UNSUPPORTED
 // when the shape does not fit it, so that the CUDA-core kernels run instead.
 tee_status router_gate_tc(int n, int d, int b, int dtype, const void* h, int64_t ldh, const void* gamma,
@@ -390,6 +543,19 @@ static tee_status run_gate(const tee_gate_desc* g, int n, const void* h_cur, int
                                    ws_at<float>(ws, TEE_WS_HEADER_BYTES), ws_counter(ws, WS_CNT_ROUTER), ws,
                                    router_dots_off(), ws_bytes, stream);
     if (st != TEE_ERR_UNSUPPORTED) return st;   // the tensor-core kernel did the whole gate
+    const size_t es = sizeof(T);
+    if (n <= RS_MAX_TOKENS && b <= 128 && g->d % RS_K == 0 && aligned16(h_cur) && (ld_cur * es) % 16 == 0 &&
+        aligned16(w_down) && (!gamma || aligned16(gamma))) {
+        // one launch; its sums accumulate into dots and sumsq, which start cleared
+        st = cuda_status(cudaMemsetAsync(dots, 0, router_core_end(n, b) - router_dots_off(), stream));
+        if (st != TEE_OK) return st;
+        const dim3 grid(g->d / RS_K, (n + RS_TOK - 1) / RS_TOK);
+        router_small_kernel<T><<<grid, RS_THREADS, 0, stream>>>(
+            n, g->d, b, static_cast<const T*>(h_cur), ld_cur, static_cast<const T*>(gamma),
+            static_cast<const T*>(w_down), dots, sumsq, b_down, static_cast<const T*>(w_up), b_up, g->eps,
+            g->threshold, g->rule, need_flag, score, mask, flag, ws_counter(ws, WS_CNT_ROUTER));
+        return launch_status();
+    }
     {
         dim3 grid((n + RT_TOK - 1) / RT_TOK, (b + RT_WARPS * RT_CH_WARP - 1) / (RT_WARPS * RT_CH_WARP));
         const size_t smem = static_cast<size_t>(RT_TOK) * g->d * sizeof(float);
