@@ -189,9 +189,9 @@ class Decode:
         self.out = torch.zeros(n, d, dtype=dt, device=dev)
         self.units = n
         self.kernel = "kv_fill"
-        # the decode kernel (int4, identity map, bf16) has a recorded ncu capture
+        # the decode kernels with a recorded ncu capture: int4 (identity map, bf16) and the tiny fp32 one
         self.traffic_key = ("kv_fill/decode" if cfg.weights == "int4" and cfg.map == "identity" and cfg.dtype == "bf16"
-                            else None)
+                            else "kv_fill/decode-tiny" if cfg is configs.TINY_DECODE else None)
         # algorithmic bytes of the fill call: weights + the h rows + K/V written
         L = len(cfg.fill_layers)
         kvw = cfg.kvw
