@@ -187,6 +187,9 @@ class Decode:
         self.c_out["h_cont"] = torch.empty(n, d, dtype=dt, device=dev)
         self.c_out.update(self.g_out)   # the front writes score, mask and flag into the same dict
         self.out = torch.zeros(n, d, dtype=dt, device=dev)
+        # the end-to-end run: host buffers in, host buffers out, one library call a step
+        self.step_host = tee.DecodeStep(self.fill, n_max=n, d=d, threshold=cfg.tau, dtype=dt, rule=cfg.rule,
+                                        k_cache=self.x["k_cache"], v_cache=self.x["v_cache"])
         self.units = n
         self.kernel = "kv_fill"
         # the decode kernels with a recorded ncu capture: int4 (identity map, bf16) and the tiny fp32 one
@@ -235,7 +238,7 @@ class Decode:
     def host_io(self):
         """Pinned host copies of the step's inputs and outputs for the end-to-end run."""
         x = self.x
-        self.h_in = {k: x[k].cpu().pin_memory() for k in ("h_prev", "h_cur", "pos")}
+        self.h_in = {k: x[k].cpu().pin_memory() for k in ("h_prev", "h_cur", "pos", "seq")}
         self.h_out = {"score": torch.empty(self.cfg.batch).pin_memory(),
                       "mask": torch.empty(self.cfg.batch, dtype=torch.uint8).pin_memory(),
                       "counts": torch.empty(2, dtype=torch.int32).pin_memory(),
@@ -245,14 +248,11 @@ class Decode:
         return bi, bo
 
     def e2e_step(self):
-        x = self.x
-        for k, t in self.h_in.items():
-            x[k].copy_(t, non_blocking=True)
-        self.step()
-        self.h_out["score"].copy_(self.g_out["score"], non_blocking=True)
-        self.h_out["mask"].copy_(self.g_out["mask"], non_blocking=True)
-        self.h_out["counts"].copy_(self.c_out["counts"], non_blocking=True)
-        self.h_out["out"].copy_(self.out, non_blocking=True)
+        # tee_decode_step_run_host: the inputs' copies, the front, the fill and the
+        # results' copies in one call
+        hi, ho = self.h_in, self.h_out
+        self.step_host.run_host(hi["h_prev"], hi["h_cur"], hi["pos"], hi["seq"], score=ho["score"], mask=ho["mask"],
+                                counts=ho["counts"], out=ho["out"])
 
     def n_exit(self):
         return int(self.c_out["counts"][1].item())

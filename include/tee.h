@@ -544,6 +544,67 @@ TEE_API tee_status tee_exit_river(const tee_river_desc* desc, int32_t n_layers, 
                                   void* k_cache, void* v_cache, const tee_cache_layout* cache,
                                   void* h_out, int64_t ld_out, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------- decode step from host buffers */
+
+/*
+ * One whole decode step, host memory to host memory, in one call: River-LLM's
+ * exit decision and KV fill (method steps 1 and 3) with TIDE module 4's
+ * compaction and exit scatter. The call copies the step's inputs from host
+ * memory into the device buffers the step was created with, runs
+ * tee_exit_gate_compact_scatter (gate, compaction with the continuing rows
+ * gathered, exit scatter of token r into row r of `out`), then tee_kv_fill for
+ * the exiting tokens at their cache positions
+ * (rows = exit_rows, item count = counts[1] on the device, h_split = h_cur),
+ * and copies the score, the mask, the counts and `out` back to host memory;
+ * everything is enqueued on `stream` and the host results are valid once the
+ * stream has completed. Host buffers should be page-locked for the copies to
+ * run asynchronously. The results equal those of the two calls made on the
+ * device buffers.
+ */
+typedef struct {
+    /* device buffers owned by the caller, alive as long as the step object */
+    void* h_prev;          /* [n_max][d] gate dtype: the previous layer's states */
+    void* h_cur;           /* [n_max][d] gate dtype: the current layer's states (and the fill's h_split) */
+    int32_t* pos;          /* [n_max] cache position of each token */
+    int32_t* seq;          /* [n_max] cache sequence of each token; NULL = sequence 0 */
+    float* score;          /* [n_max] */
+    uint8_t* mask;         /* [n_max] */
+    int32_t* flag;         /* [1] batch flag, or NULL */
+    int32_t* cont_rows;    /* [n_max] */
+    int32_t* exit_rows;    /* [n_max] */
+    int32_t* cont_pos;     /* [n_max] or NULL */
+    int32_t* exit_pos;     /* [n_max] or NULL */
+    void* h_cont;          /* [n_max][d] or NULL: the continuing rows gathered */
+    void* out;             /* [n_out][d]: exiting token r's row scattered to out[r] (n_out >= n_max) */
+    int64_t n_out;
+    int32_t* counts;       /* [2] continuing, exiting */
+    void* ws;              /* workspace for both calls */
+    size_t ws_bytes;
+} tee_step_buffers;
+
+typedef struct tee_decode_step tee_decode_step;   /* opaque; host memory only */
+
+/* Check and keep the descriptors, the fill's layers (copied), its prepared
+ * state, the caches and the buffers. gate->mode must be TEE_GATE_COSINE; the
+ * gate's d and dtype must match the fill's. Errors: TEE_ERR_INVALID_ARG for a
+ * null or inconsistent argument, TEE_ERR_WORKSPACE when buf->ws is smaller
+ * than both calls need at n_max. *step is set only on success. */
+TEE_API tee_status tee_decode_step_create(const tee_gate_desc* gate, int32_t n_max, const tee_fill_desc* fill,
+                                          int32_t n_layers, const tee_fill_layer* layers, const void* fill_prep,
+                                          size_t fill_prep_bytes, void* k_cache, void* v_cache,
+                                          const tee_cache_layout* cache, const tee_step_buffers* buf,
+                                          tee_decode_step** step);
+
+/* One step over n <= n_max tokens. Host inputs: h_prev, h_cur [n][d] (gate
+ * dtype, rows contiguous), pos [n], seq [n] or NULL. Host outputs (each may be
+ * NULL to skip its copy): score [n], mask [n], counts [2], out [n_out][d]. */
+TEE_API tee_status tee_decode_step_run_host(tee_decode_step* step, int32_t n, const void* h_prev, const void* h_cur,
+                                            const int32_t* pos, const int32_t* seq, float* score, uint8_t* mask,
+                                            int32_t* counts, void* out, void* stream);
+
+/* Free the step object (not the buffers it was given). NULL is allowed. */
+TEE_API void tee_decode_step_destroy(tee_decode_step* step);
+
 #ifdef __cplusplus
 }
 #endif

@@ -189,3 +189,34 @@ def test_fill_descriptor_flags(lib):
     assert size(0) > 0
     assert size(_lib.TEE_FILL_EARLY_WEIGHTS | _lib.TEE_FILL_GENERIC) == size(0)
     assert size(4) == 0   # an unknown flag is rejected
+
+
+def test_decode_step_checks_on_the_host(lib):
+    from token_early_exit_gb300 import _lib
+    fake = ctypes.c_void_p(16)   # never dereferenced: every call below fails its checks first
+    gate = _lib.GateDesc(mode=_lib.TEE_GATE_COSINE, rule=_lib.TEE_RULE_PER_TOKEN, dtype=_lib.TEE_BF16, d=2048,
+                         bottleneck=0, threshold=0.97, eps=1e-5)
+    fill = _lib.FillDesc(d=2048, n_kv_heads=8, head_dim=64, rope_base=5e5, eps=1e-5, dtype=_lib.TEE_BF16,
+                         wfmt=_lib.TEE_W_INT4, group=64, flags=0)
+    layout = _lib.CacheLayout(s_layer=1 << 20, s_seq=1 << 14, s_head=4096 * 64, s_pos=64, n_layers=16, n_seq=64,
+                              n_heads=8, max_pos=4096)
+    layers = (_lib.FillLayer * 1)()
+    buf = _lib.StepBuffers(h_prev=16, h_cur=16, pos=16, score=16, mask=16, cont_rows=16, exit_rows=16, out=16,
+                           n_out=64, counts=16, ws=16, ws_bytes=1 << 30)
+    h = ctypes.c_void_p()
+    # the gate's d differs from the fill's
+    bad_gate = _lib.GateDesc(mode=_lib.TEE_GATE_COSINE, rule=0, dtype=_lib.TEE_BF16, d=1024, bottleneck=0,
+                             threshold=0.97, eps=1e-5)
+    assert lib.tee_decode_step_create(ctypes.byref(bad_gate), 64, ctypes.byref(fill), 1, layers, fake, 1 << 20, fake,
+                                      fake, ctypes.byref(layout), ctypes.byref(buf), ctypes.byref(h)) == \
+        _lib.TEE_ERR_INVALID_ARG
+    # a workspace smaller than the calls need
+    small = _lib.StepBuffers(h_prev=16, h_cur=16, pos=16, score=16, mask=16, cont_rows=16, exit_rows=16, out=16,
+                             n_out=64, counts=16, ws=16, ws_bytes=256)
+    assert lib.tee_decode_step_create(ctypes.byref(gate), 64, ctypes.byref(fill), 1, layers, fake, 1 << 20, fake,
+                                      fake, ctypes.byref(layout), ctypes.byref(small), ctypes.byref(h)) == \
+        _lib.TEE_ERR_WORKSPACE
+    assert h.value is None   # set only on success
+    assert lib.tee_decode_step_run_host(None, 4, fake, fake, fake, None, None, None, None, None, None) == \
+        _lib.TEE_ERR_INVALID_ARG
+    lib.tee_decode_step_destroy(None)

@@ -100,3 +100,39 @@ def test_decode_step(tee, cfg, case, seed, early, fused, record_property):
     check_decode_fill(cfg, x, part["exit_rows"], pos, seq, gen.CACHE_SENTINEL)
     o_ref = oracle.exit_scatter(np.full(hc.shape, -3.0), hc, part["exit_rows"], part["exit_pos"])
     assert np.array_equal(f64(out), o_ref)
+
+
+@pytest.mark.parametrize("cfg,case,seed", [(configs.TINY_DECODE, "default", 0), (configs.TINY_DECODE, "default", 3),
+                                           (configs.LLAMA1B_DECODE, "exit", 0), (configs.LLAMA1B_DECODE, "stay", 1)])
+def test_decode_step_from_host_buffers(tee, cfg, case, seed):
+    """tee_decode_step_run_host (host inputs copied in, front and fill, results copied
+    out, one call) gives exactly what the two device calls give on the same inputs."""
+    x = gen.decode_inputs(cfg, seed=seed, device=DEV, case=case)
+    dt = x["h_cur"].dtype
+    mk = lambda: tee.KVFill(x["layers"], d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,  # noqa: E731
+                            rope_base=cfg.rope_base, eps=cfg.eps, dtype=dt, max_pos=cfg.cache_len,
+                            int4=cfg.weights == "int4", group=cfg.group)
+    # device path on its own copies of the caches
+    k_dev, v_dev = x["k_cache"].clone(), x["v_cache"].clone()
+    ws = tee.Workspace(DEV)
+    out_dev = torch.zeros_like(x["h_cur"])
+    comp = tee.exit_gate_compact_scatter(x["h_cur"], x["h_prev"], cfg.tau, out_dev, rule=cfg.rule, ws=ws)
+    mk()(x["h_cur"], k_dev, v_dev, rows=comp["exit_rows"], pos=x["pos"], seq=x["seq"], n_dev=comp["counts"][1:],
+         n_max=cfg.batch, ws=ws)
+    # the one-call path from pinned host buffers
+    step = tee.DecodeStep(mk(), n_max=cfg.batch, d=cfg.d, threshold=cfg.tau, dtype=dt, rule=cfg.rule,
+                          k_cache=x["k_cache"], v_cache=x["v_cache"])
+    hi = {k: x[k].cpu().pin_memory() for k in ("h_prev", "h_cur", "pos", "seq")}
+    score = torch.empty(cfg.batch).pin_memory()
+    mask = torch.empty(cfg.batch, dtype=torch.uint8).pin_memory()
+    counts = torch.empty(2, dtype=torch.int32).pin_memory()
+    out = torch.empty(cfg.batch, cfg.d, dtype=dt).pin_memory()
+    step.run_host(hi["h_prev"], hi["h_cur"], hi["pos"], hi["seq"], score=score, mask=mask, counts=counts, out=out)
+    torch.cuda.synchronize()
+    assert step.ws.device_error() == (0, 0) and ws.device_error() == (0, 0)
+    assert torch.equal(score, comp["score"].cpu()) and torch.equal(mask, comp["mask"].cpu())
+    assert torch.equal(counts, comp["counts"].cpu())
+    n_exit = int(counts[1])
+    rows = comp["exit_rows"][:n_exit].long()
+    assert torch.equal(out[rows.cpu()], out_dev[rows].cpu())   # the exiting rows, scattered to their slots
+    assert torch.equal(x["k_cache"], k_dev) and torch.equal(x["v_cache"], v_dev)

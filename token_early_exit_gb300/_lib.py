@@ -63,6 +63,13 @@ class RiverLayer(ctypes.Structure):
                 ("wg", W4), ("wu", W4), ("wd", W4), ("cache_layer", c_int32), ("reserved", c_int32)]
 
 
+class StepBuffers(ctypes.Structure):
+    _fields_ = [("h_prev", c_void_p), ("h_cur", c_void_p), ("pos", c_void_p), ("seq", c_void_p), ("score", c_void_p),
+                ("mask", c_void_p), ("flag", c_void_p), ("cont_rows", c_void_p), ("exit_rows", c_void_p),
+                ("cont_pos", c_void_p), ("exit_pos", c_void_p), ("h_cont", c_void_p), ("out", c_void_p),
+                ("n_out", c_int64), ("counts", c_void_p), ("ws", c_void_p), ("ws_bytes", c_size_t)]
+
+
 _P = c_void_p
 SIGNATURES = {
     "tee_version": (c_char_p, []),
@@ -102,6 +109,10 @@ SIGNATURES = {
     "tee_exit_scatter_workspace_size": (c_size_t, [c_int32]),
     "tee_exit_scatter": (c_int, [c_int32, _P, _P, _P, _P, c_int64, _P, c_int64, c_int64, c_int32, c_int32, _P,
                                  c_float, _P, c_size_t, _P]),
+    "tee_decode_step_create": (c_int, [POINTER(GateDesc), c_int32, POINTER(FillDesc), c_int32, POINTER(FillLayer), _P,
+                                       c_size_t, _P, _P, POINTER(CacheLayout), POINTER(StepBuffers), POINTER(_P)]),
+    "tee_decode_step_run_host": (c_int, [_P, c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "tee_decode_step_destroy": (None, [_P]),
     "tee_kv_fill_prep_size": (c_size_t, [POINTER(FillDesc), c_int32, c_int32]),
     "tee_kv_fill_prepare": (c_int, [POINTER(FillDesc), c_int32, POINTER(FillLayer), c_int32, _P, c_size_t, _P]),
     "tee_kv_fill_workspace_size": (c_size_t, [POINTER(FillDesc), c_int32, c_int32]),

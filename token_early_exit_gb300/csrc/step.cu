@@ -1,0 +1,103 @@
+// A whole decode step from host buffers to host buffers in one call: the
+// inputs' host-to-device copies, the front (gate + compaction + exit scatter)
+// and the KV fill of the exiting tokens, and the results' copies back, all
+// enqueued on one stream. It only sequences the library's own calls.
+#include <new>
+
+#include "common.cuh"
+
+struct tee_decode_step {
+    tee_gate_desc gate;
+    int n_max;
+    tee_fill_desc fill;
+    int n_layers;
+    tee_fill_layer* layers;   // owned copy
+    const void* prep;
+    size_t prep_bytes;
+    void* k_cache;
+    void* v_cache;
+    tee_cache_layout cache;
+    tee_step_buffers buf;
+};
+
+using namespace tee;
+
+extern "C" tee_status tee_decode_step_create(const tee_gate_desc* gate, int32_t n_max, const tee_fill_desc* fill,
+                                             int32_t n_layers, const tee_fill_layer* layers, const void* fill_prep,
+                                             size_t fill_prep_bytes, void* k_cache, void* v_cache,
+                                             const tee_cache_layout* cache, const tee_step_buffers* buf,
+                                             tee_decode_step** step) {
+    if (!gate || !fill || !cache || !buf || !step || n_max <= 0 || n_layers < 0 || (n_layers > 0 && !layers))
+        return TEE_ERR_INVALID_ARG;
+    if (gate->mode != TEE_GATE_COSINE || gate->d != fill->d || gate->dtype != fill->dtype) return TEE_ERR_INVALID_ARG;
+    if (!buf->h_prev || !buf->h_cur || !buf->pos || !buf->score || !buf->mask || !buf->cont_rows || !buf->exit_rows ||
+        !buf->out || !buf->counts || buf->n_out < 0 || !fill_prep || !k_cache || !v_cache)
+        return TEE_ERR_INVALID_ARG;
+    const size_t need_front = tee_exit_gate_compact_scatter_workspace_size(gate, n_max);
+    const size_t need_fill = tee_kv_fill_workspace_size(fill, n_layers, n_max);
+    if (need_front == 0 || need_fill == 0) return TEE_ERR_INVALID_ARG;
+    if (!buf->ws || buf->ws_bytes < need_front || buf->ws_bytes < need_fill) return TEE_ERR_WORKSPACE;
+    tee_decode_step* s = new (std::nothrow) tee_decode_step;
+    if (!s) return TEE_ERR_INVALID_ARG;
+    s->layers = n_layers > 0 ? new (std::nothrow) tee_fill_layer[n_layers] : nullptr;
+    if (n_layers > 0 && !s->layers) {
+        delete s;
+        return TEE_ERR_INVALID_ARG;
+    }
+    for (int l = 0; l < n_layers; ++l) s->layers[l] = layers[l];
+    s->gate = *gate;
+    s->n_max = n_max;
+    s->fill = *fill;
+    s->n_layers = n_layers;
+    s->prep = fill_prep;
+    s->prep_bytes = fill_prep_bytes;
+    s->k_cache = k_cache;
+    s->v_cache = v_cache;
+    s->cache = *cache;
+    s->buf = *buf;
+    *step = s;
+    return TEE_OK;
+}
+
+extern "C" tee_status tee_decode_step_run_host(tee_decode_step* step, int32_t n, const void* h_prev, const void* h_cur,
+                                               const int32_t* pos, const int32_t* seq, float* score, uint8_t* mask,
+                                               int32_t* counts, void* out, void* stream) {
+    if (!step || n < 0 || n > step->n_max || !h_prev || !h_cur || !pos) return TEE_ERR_INVALID_ARG;
+    const tee_step_buffers& b = step->buf;
+    const int d = step->gate.d;
+    const size_t row = static_cast<size_t>(d) * dtype_bytes(step->gate.dtype);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // inputs
+    tee_status st = cuda_status(cudaMemcpyAsync(b.h_prev, h_prev, n * row, cudaMemcpyHostToDevice, s));
+    if (st == TEE_OK) st = cuda_status(cudaMemcpyAsync(b.h_cur, h_cur, n * row, cudaMemcpyHostToDevice, s));
+    if (st == TEE_OK) st = cuda_status(cudaMemcpyAsync(b.pos, pos, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    if (st == TEE_OK && seq && b.seq)
+        st = cuda_status(cudaMemcpyAsync(b.seq, seq, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    if (st != TEE_OK) return st;
+    // the front (exiting token r scattered to row r of out), then the fill of the
+    // exiting tokens at their cache positions (their count stays on the device)
+    st = tee_exit_gate_compact_scatter(&step->gate, n, b.h_cur, d, b.h_prev, d, nullptr, nullptr, nullptr, nullptr,
+                                       nullptr, nullptr, b.score, b.mask, b.flag, b.cont_rows, b.exit_rows, b.cont_pos,
+                                       b.exit_pos, b.h_cont, d, b.out, d, b.n_out, b.counts, b.ws, b.ws_bytes, stream);
+    if (st != TEE_OK) return st;
+    if (n > 0 && step->n_layers > 0) {
+        st = tee_kv_fill(&step->fill, step->n_layers, step->layers, step->prep, step->prep_bytes, n, b.counts + 1,
+                         b.h_cur, d, n, b.exit_rows, b.pos, 0, seq && b.seq ? b.seq : nullptr, step->k_cache,
+                         step->v_cache, &step->cache, b.ws, b.ws_bytes, stream);
+        if (st != TEE_OK) return st;
+    }
+    // results
+    if (score) st = cuda_status(cudaMemcpyAsync(score, b.score, n * sizeof(float), cudaMemcpyDeviceToHost, s));
+    if (st == TEE_OK && mask) st = cuda_status(cudaMemcpyAsync(mask, b.mask, n, cudaMemcpyDeviceToHost, s));
+    if (st == TEE_OK && counts)
+        st = cuda_status(cudaMemcpyAsync(counts, b.counts, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    if (st == TEE_OK && out)
+        st = cuda_status(cudaMemcpyAsync(out, b.out, static_cast<size_t>(b.n_out) * row, cudaMemcpyDeviceToHost, s));
+    return st;
+}
+
+extern "C" void tee_decode_step_destroy(tee_decode_step* step) {
+    if (!step) return;
+    delete[] step->layers;
+    delete step;
+}

@@ -13,7 +13,7 @@ from typing import Dict, List, Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import (CacheLayout, FillDesc, FillLayer, GateDesc, check, load)
+from ._lib import (CacheLayout, FillDesc, FillLayer, GateDesc, StepBuffers, check, load)
 
 _DT = {torch.float32: _lib.TEE_F32, torch.float16: _lib.TEE_F16, torch.bfloat16: _lib.TEE_BF16}
 _RULE = {"per_token": _lib.TEE_RULE_PER_TOKEN, "batch_all": _lib.TEE_RULE_BATCH_ALL}
@@ -319,6 +319,73 @@ class KVFill:
                                   _ptr(_vec(pos, "pos")), int(pos0), _ptr(_vec(seq, "seq")), _ptr(k_cache),
                                   _ptr(v_cache), ctypes.byref(layout), wp, wn, _stream(h_split.device))
         check("tee_kv_fill", st)
+
+
+class DecodeStep:
+    """A whole decode step from host buffers to host buffers in one library call
+    (tee_decode_step_run_host): the inputs' copies to the device, the cosine
+    gate with compaction and exit scatter in one launch, the KV fill of the
+    exiting tokens with ``fill`` (a prepared KVFill), and the results' copies
+    back, all on the current stream. The device buffers are allocated here and
+    kept; ``k_cache`` / ``v_cache`` are filled in place. Host tensors passed to
+    ``run_host`` should be pinned for the copies to overlap."""
+
+    def __init__(self, fill: "KVFill", *, n_max: int, d: int, threshold: float, dtype: torch.dtype,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor, rule: str = "per_token", device=None):
+        self.lib = load()
+        dev = torch.device(device or k_cache.device)
+        self.fill, self.n_max, self.d, self.dtype = fill, int(n_max), int(d), dtype
+        self.gate = GateDesc(mode=_lib.TEE_GATE_COSINE, rule=_RULE[rule], dtype=_DT[dtype], d=self.d, bottleneck=0,
+                             threshold=float(threshold), eps=1e-5)
+        n = self.n_max
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.t = {"h_prev": torch.empty(n, d, dtype=dtype, device=dev), "h_cur": torch.empty(n, d, dtype=dtype, device=dev),
+                  "pos": torch.empty(n, **i32), "seq": torch.zeros(n, **i32),
+                  "score": torch.empty(n, dtype=torch.float32, device=dev),
+                  "mask": torch.empty(n, dtype=torch.uint8, device=dev), "flag": torch.empty(1, **i32),
+                  "cont_rows": torch.empty(n, **i32), "exit_rows": torch.empty(n, **i32),
+                  "cont_pos": torch.empty(n, **i32), "exit_pos": torch.empty(n, **i32),
+                  "h_cont": torch.empty(n, d, dtype=dtype, device=dev), "out": torch.zeros(n, d, dtype=dtype, device=dev),
+                  "counts": torch.empty(2, **i32)}
+        self.ws = Workspace(dev)
+        need = max(self.lib.tee_exit_gate_compact_scatter_workspace_size(ctypes.byref(self.gate), n),
+                   fill.workspace_bytes(n))
+        wp, wn = self.ws.get(need)
+        t = self.t
+        self.buf = StepBuffers(h_prev=t["h_prev"].data_ptr(), h_cur=t["h_cur"].data_ptr(), pos=t["pos"].data_ptr(),
+                               seq=t["seq"].data_ptr(), score=t["score"].data_ptr(), mask=t["mask"].data_ptr(),
+                               flag=t["flag"].data_ptr(), cont_rows=t["cont_rows"].data_ptr(),
+                               exit_rows=t["exit_rows"].data_ptr(), cont_pos=t["cont_pos"].data_ptr(),
+                               exit_pos=t["exit_pos"].data_ptr(), h_cont=t["h_cont"].data_ptr(),
+                               out=t["out"].data_ptr(), n_out=n, counts=t["counts"].data_ptr(), ws=wp.value,
+                               ws_bytes=wn)
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.layout = cache_layout(k_cache)
+        self.handle = ctypes.c_void_p()
+        st = self.lib.tee_decode_step_create(ctypes.byref(self.gate), n, ctypes.byref(fill.desc), fill.n_layers,
+                                             fill.layers, _ptr(fill.prep), fill.prep.numel(), _ptr(k_cache),
+                                             _ptr(v_cache), ctypes.byref(self.layout), ctypes.byref(self.buf),
+                                             ctypes.byref(self.handle))
+        check("tee_decode_step_create", st)
+        self.stream = _stream(dev)
+
+    def run_host(self, h_prev: torch.Tensor, h_cur: torch.Tensor, pos: torch.Tensor,
+                 seq: Optional[torch.Tensor] = None, *, score: Optional[torch.Tensor] = None,
+                 mask: Optional[torch.Tensor] = None, counts: Optional[torch.Tensor] = None,
+                 out: Optional[torch.Tensor] = None) -> None:
+        """One step: host h_prev, h_cur [n][d], pos (and seq) [n] int32 in; host score,
+        mask, counts, out [n_max][d] written once the stream completes."""
+        n = h_cur.shape[0]
+        p = lambda t: None if t is None else t.data_ptr()   # noqa: E731 (host buffers, checked by the library)
+        st = self.lib.tee_decode_step_run_host(self.handle, n, p(h_prev), p(h_cur), p(pos), p(seq), p(score), p(mask),
+                                               p(counts), p(out), self.stream)
+        check("tee_decode_step_run_host", st)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            self.lib.tee_decode_step_destroy(h)
+            self.handle = ctypes.c_void_p()
 
 
 def kv_fill(h_split: torch.Tensor, layers: Sequence[Dict], k_cache: torch.Tensor, v_cache: torch.Tensor, *,
