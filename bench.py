@@ -16,7 +16,9 @@ A step is one pass of the whole hot path over one batch of synthetic input:
       split for all filled rows;
   river-1b / river-tiny: River-LLM's Exit River -- 64 exited tokens through the
       W4A16 copies of 8 Llama-3.2-1B-shaped layers (attention over a 4096-slot
-      cache, FFN), one call.
+      cache, FFN), one call;
+  ridge-4096: RidgeFill's closed-form map fitted on the GPU from 16,384 bf16
+      calibration rows at d = 4096 (the Gram GEMMs, the Cholesky and the solves).
 L2 is flushed (a write larger than L2) between timed steps, outside the timed
 events, except where every input is larger than L2 (router-65536). Under torchrun each rank runs its own replica (independent batches,
 no collective on the data path: weak scaling); rank 0 prints one JSON line.
@@ -52,7 +54,10 @@ from workloads import configs, gen  # noqa: E402
 
 METRIC = "tokens/s through exit gate+compact+KV fill"
 RIVER_METRIC = "tokens/s through the Exit River (W4A16 exit layers)"
-WORKLOADS = ("decode-1b", "decode-tiny", "router-32", "router-4096", "router-65536", "prefill-16k", "prefill-120k", "river-1b",
+RIDGE_METRIC = "calibration rows/s through the ridge fit (RidgeFill's closed-form map)"
+RIDGE_SHAPE = (16384, 4096)       # calibration rows, d (d_out = d)
+RIDGE_SAMPLE = (2048, 256)        # the oracle's bounded sample (the float64 fit at d = 4096 takes minutes)
+WORKLOADS = ("decode-1b", "decode-tiny", "router-32", "router-4096", "router-65536", "prefill-16k", "prefill-120k", "river-1b", "ridge-4096",
              "river-tiny")
 
 
@@ -147,6 +152,19 @@ def river_config(c, nbytes):
             "l2": "inputs larger than L2 (the KV cache read); flushed between timed steps"}
 
 
+def unit_for(name):
+    return "rows/s" if name.startswith("ridge") else "tokens/s"
+
+
+def metric_for(name):
+    return RIVER_METRIC if name.startswith("river") else RIDGE_METRIC if name.startswith("ridge") else METRIC
+
+
+def ridge_config(n, d):
+    return {"workload": f"ridge-fit-d{d}-n{n}", "rows": n, "d": d, "d_out": d, "lambda": 0.5, "inputs": "bf16",
+            "solve": "fp32 blocked Cholesky", "l2": "flushed between timed steps"}
+
+
 def reference_config(name, dev, seed=0, rows=None, layers=None):
     """The ``config`` of a workload as the GPU arm reports it, from the
     configurations and the generator alone."""
@@ -156,6 +174,8 @@ def reference_config(name, dev, seed=0, rows=None, layers=None):
     if name in ("router-32", "router-4096", "router-65536"):
         n = {"router-32": 32, "router-4096": 4096}.get(name) or (rows or 65536)
         return router_config(configs.ROUTER_4096, n, 0.5, router_flush(configs.ROUTER_4096, n, dev))
+    if name == "ridge-4096":
+        return ridge_config(*RIDGE_SHAPE)
     if name in ("prefill-16k", "prefill-120k"):
         cfg = configs.PREFILL_16K if name == "prefill-16k" else configs.PREFILL_120K
         return prefill_config(cfg, cfg.filled_rows if rows is None else rows,
@@ -463,6 +483,55 @@ class River:
 
 
 
+class Ridge:
+    """RidgeFill's map W = (X^T X + 0.5 I)^-1 X^T Y fitted on the GPU (tee_ridge_fit)."""
+
+    def __init__(self, tee, dev, seed=0):
+        n, d = RIDGE_SHAPE
+        self.tee, self.dev, self.n, self.d = tee, dev, n, d
+        self.x = gen.ridge_inputs(n, d, seed, dev)
+        self.w = torch.empty(d, d, device=dev)
+        self.ws = tee.Workspace(dev)
+        self.units = n
+        self.kernel = "ridge_fit (all launches of the call)"
+        self.metric = RIDGE_METRIC
+        self.traffic_key = None
+        self.bound = "tensor"
+
+    def fill_bytes(self, n_exit):
+        """Algorithmic FLOPs: the two Gram products (2 n d^2 each), the Cholesky (d^3 / 3)
+        and the two triangular solves (d^2 d_out each)."""
+        n, d = self.n, self.d
+        return 4.0 * n * d * d + d ** 3 / 3.0 + 2.0 * d ** 3
+
+    def parts(self):
+        def fit():
+            self.tee.ridge_fit(self.x["x"], self.x["y"], 0.5, ws=self.ws, out=self.w)
+        return [fit], 0
+
+    def step(self):
+        for f in self.parts()[0]:
+            f()
+
+    def host_io(self):
+        self.h_in = {k: self.x[k].cpu().pin_memory() for k in ("x", "y")}
+        self.h_out = {"w": torch.empty_like(self.w, device="cpu").pin_memory()}
+        return (sum(t.numel() * t.element_size() for t in self.h_in.values()),
+                sum(t.numel() * t.element_size() for t in self.h_out.values()))
+
+    def e2e_step(self):
+        for k, t in self.h_in.items():
+            self.x[k].copy_(t, non_blocking=True)
+        self.step()
+        self.h_out["w"].copy_(self.w, non_blocking=True)
+
+    def n_exit(self):
+        return self.n
+
+    def config(self):
+        return ridge_config(self.n, self.d)
+
+
 # --------------------------------------------------------------------------- the oracle (CPU baseline)
 
 def _host(x):
@@ -485,6 +554,16 @@ def oracle_sample(name, dev, seed=0, rows=None, layers=None):
     here builds, loads or calls the CUDA library. ``run()`` computes the
     sample with the C++ oracle and returns the tokens it stands for."""
     import oracle
+    if name == "ridge-4096":
+        n_s, d_s = RIDGE_SAMPLE
+        x = gen.ridge_inputs(n_s, d_s, seed, dev)
+        xh, yh = _host(x["x"]), _host(x["y"])
+
+        def run():
+            oracle.ridge_fit(xh, yh, 0.5)
+            return n_s
+        return run, (f"the oracle's fit of {n_s} rows at d = d_out = {d_s} (rows/s at that d; the float64 fit at "
+                     f"d = 4096 is a multi-minute job)")
     if name in ("decode-1b", "decode-tiny"):
         cfg = configs.LLAMA1B_DECODE if name == "decode-1b" else configs.TINY_DECODE
         case = "exit" if cfg.rule == "batch_all" else "default"
@@ -570,6 +649,8 @@ def make(name, tee, dev, seed, rows=None, layers=None):
         return Decode(tee, configs.LLAMA1B_DECODE, dev, seed)
     if name == "decode-tiny":
         return Decode(tee, configs.TINY_DECODE, dev, seed)
+    if name == "ridge-4096":
+        return Ridge(tee, dev, seed)
     if name == "router-32":
         return Router(tee, configs.ROUTER_4096, dev, seed, n=32)
     if name == "router-4096":
@@ -692,15 +773,15 @@ def run_reference(args):
         units += run()
     el = time.perf_counter() - t0
     v = units / el
-    line = {"metric": RIVER_METRIC if args.workload.startswith("river") else METRIC, "value": v,
-            "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
+    line = {"metric": metric_for(args.workload), "value": v,
+            "unit": unit_for(args.workload), "n_gpus": 0, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": reference_config(args.workload, dev, args.seed, args.rows, args.layers),
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": unit_for(args.workload), "cores": 1, "kind": "oracle",
                              "impl": "C++17, single-threaded, float64", "host_cores": os.cpu_count(),
                              "sample": sample},
-            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": v, "unit": unit_for(args.workload), "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
@@ -838,15 +919,15 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         run, sample = oracle_sample(args.workload, dev, args.seed, args.rows, args.layers)
         v, el = time_oracle(run, args.cpu_seconds)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "impl": "C++17, single-threaded, float64",
+        cpu = {"value": v, "unit": unit_for(args.workload), "cores": 1, "kind": "oracle", "impl": "C++17, single-threaded, float64",
                "host_cores": os.cpu_count(), "sample": sample, "seconds": round(el, 2)}
 
-    line = {"metric": getattr(w, "metric", METRIC), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+    line = {"metric": getattr(w, "metric", METRIC), "value": value, "unit": unit_for(args.workload), "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.config().get("workload") != configs.TINY_DECODE.name else "f32",
             "data": "synthetic", "config": w.config(), "exits_per_step": n_exit,
             "roofline": roof, "cpu_baseline": cpu,
-            "e2e": {"value": job_throughput(w.units, world, t_e2e), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+            "e2e": {"value": job_throughput(w.units, world, t_e2e), "unit": unit_for(args.workload), "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": t_e2e},
             "gpu_launches": int(launches), "launches_per_step": int(k_step), "clocks": clk,
             **({"kernels": per_kernel} if per_kernel else {}),

@@ -201,3 +201,13 @@ def river_inputs(cfg: RiverConfig, seed: int = 0, device="cpu", with_cache: bool
         out["k_cache"] = normal(shape, 0.5, seed, "k_hist", device, dtype)
         out["v_cache"] = normal(shape, 0.5, seed, "v_hist", device, dtype)
     return out
+
+
+def ridge_inputs(n: int, d: int, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
+    """Calibration rows for a ridge map: X ~ N(0, 1) [n][d] and Y = X A + 0.1 N(0, 1)
+    with A ~ N(0, 1/d) + 0.5 I (the prefill maps' distribution), both bf16."""
+    x = normal((n, d), 1.0, seed, f"ridge_x:{n}x{d}", device)
+    a = normal((d, d), 1.0 / math.sqrt(d), seed, f"ridge_a:{d}", device)
+    a += 0.5 * torch.eye(d, device=device)
+    y = x @ a + normal((n, d), 0.1, seed, f"ridge_e:{n}x{d}", device)
+    return {"x": x.to(torch.bfloat16), "y": y.to(torch.bfloat16)}
