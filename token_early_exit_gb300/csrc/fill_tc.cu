@@ -143,10 +143,12 @@ struct EpiArgs {
     const bf16* vb;
     const bf16* kn;
     // fp32 output (the ridge fit's Gram matrices): C, its row stride, and a value
-    // added where row == column
+    // added where row == column; with sub the product is subtracted from C instead
+    // (the ridge fit's substitution updates)
     float* c32;
     int64_t ldc32;
     float diag;
+    int sub;
 };
 
 __device__ __forceinline__ void store32_bf16(bf16* dst, const float (&v)[32]) {
@@ -182,11 +184,20 @@ __device__ __forceinline__ void epi_f32(const EpiArgs& ep, int row, int n, int c
         float v[32];
         tc::tmem_ld32(t_base + c * 32, v);
         if (!ok) continue;
+        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+        if (ep.sub) {
+            float4 o[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[q] = d4[q];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                d4[q] = make_float4(o[q].x - v[4 * q], o[q].y - v[4 * q + 1], o[q].z - v[4 * q + 2], o[q].w - v[4 * q + 3]);
+            continue;
+        }
         const int dc = row - (c0 + c * 32);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             if (j == dc) v[j] += ep.diag;
-        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
         for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
@@ -579,6 +590,25 @@ tee_status ridge_gram(int n, int d, int d_out, const void* x, int64_t ld_x, cons
     ep.ldc32 = ld_r;
     ep.diag = 0.f;
     return launch_gemm<EPI_F32>(tx, ty, d, nullptr, d_out, n_pad, ep, ws, s);
+}
+
+// ---- the ridge fit's substitution updates on the same GEMM: C [M][N] (row stride
+// ldc, fp32) -= A B^T with A [M][k3] and B [N][k3] bf16 (K-major rows, k3 a multiple
+// of 64): the fp32 factors split into bf16 high and low parts, laid along K so that
+// the one product carries a_hi b_hi + a_lo b_hi + a_hi b_lo.
+tee_status ridge_update_tc(int M, int N, int k3, const void* a3, const void* b3, float* c, int64_t ldc, void* ws,
+                           cudaStream_t s) {
+    if (M <= 0) return TEE_OK;
+    if (N % BN || k3 % BK) return TEE_ERR_UNSUPPORTED;
+    CUtensorMap ta, tb;
+    tee_status st = make_tmap_bf16(&ta, a3, k3, M, static_cast<uint64_t>(k3) * 2, BK, BM);
+    if (st != TEE_OK) return st;
+    if ((st = make_tmap_bf16(&tb, b3, k3, N, static_cast<uint64_t>(k3) * 2, BK, BN)) != TEE_OK) return st;
+    EpiArgs ep{};
+    ep.c32 = c;
+    ep.ldc32 = ldc;
+    ep.sub = 1;
+    return launch_gemm<EPI_F32>(ta, tb, M, nullptr, N, k3, ep, ws, s);
 }
 
 size_t fill_tc_prep_bytes(const tee_fill_desc& D, int n_layers) {

@@ -7,12 +7,16 @@
 // L L^T (blocked right-looking Cholesky in fp32, 64 x 64 tiles: the diagonal tile
 // in one CTA's shared memory, the panel below it by substitution, the trailing
 // lower triangle updated tile by tile), and W = L^-T L^-1 R is solved in place in
-// the output by block forward and backward substitution.
+// the output by block forward and backward substitution: each 64-row block solved
+// against its diagonal tile, the rest of the right-hand sides updated on the
+// tensor cores (the same GEMM, fp32 operands split into bf16 high and low parts).
 #include "common.cuh"
 
 namespace tee {
 
 size_t ridge_gram_ws_bytes(int n, int d, int d_out);
+tee_status ridge_update_tc(int M, int N, int k3, const void* a3, const void* b3, float* c, int64_t ldc, void* ws,
+                           cudaStream_t s);
 tee_status ridge_gram(int n, int d, int d_out, const void* x, int64_t ld_x, const void* y, int64_t ld_y, float lambda,
                       float* g, float* r, int64_t ld_r, char* scratch, void* ws, cudaStream_t s);
 
@@ -157,49 +161,45 @@ __global__ void __launch_bounds__(NT) trsm_rhs_kernel(const float* __restrict__ 
     for (int e = threadIdx.x; e < NB * RPC; e += NT) rk[static_cast<int64_t>(e / RPC) * ldr + e % RPC] = x[e / RPC][e % RPC];
 }
 
-// Right-hand-side update after block row k was solved. Forward: R_i -= L_ik R_k for
-// i > k. Backward: R_i -= L_ki^T R_k for i < k. Tile (i, column tile c) per CTA.
-__global__ void __launch_bounds__(NT) rhs_update_kernel(const float* __restrict__ G, int64_t ld, float* __restrict__ R,
-                                                        int64_t ldr, int k, int nb, bool upper) {
-    __shared__ float sa[NB][TLD];
-    __shared__ float sb[NB][TLD];
-    const int m = upper ? k : nb - 1 - k;   // block rows to update
-    const int bi = blockIdx.x % m, ct = blockIdx.x / m;
-    const int i = upper ? bi : k + 1 + bi;
-    float* c = R + static_cast<int64_t>(i) * NB * ldr + static_cast<int64_t>(ct) * NB;
-    const float* rk = R + static_cast<int64_t>(k) * NB * ldr + static_cast<int64_t>(ct) * NB;
-    const float* a = upper ? G + static_cast<int64_t>(k) * NB * ld + static_cast<int64_t>(i) * NB      // L_ki, used as A^T
-                           : G + static_cast<int64_t>(i) * NB * ld + static_cast<int64_t>(k) * NB;     // L_ik
-    // sa[kk][m] = the left factor's (m, kk); sb[kk][c] = R_k[kk][c]
+// fp32 -> bf16 split for the tensor-core updates: x = hi + lo with hi = bf16(x) and
+// lo = bf16(x - hi), so that a product of two split values keeps ~16 bits. A row of
+// the split operand holds 192 bf16: the 64 values' hi, lo, hi ("A form") or hi,
+// hi, lo ("B form"); A-form times B-form summed over the 192 gives
+// a_hi b_hi + a_lo b_hi + a_hi b_lo.
+constexpr int K3 = 3 * NB;
+__device__ __forceinline__ void split_store(__nv_bfloat16* row, int kk, float x, bool b_form) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+    row[kk] = hi;
+    row[NB + kk] = b_form ? hi : lo;
+    row[2 * NB + kk] = b_form ? lo : hi;
+}
+// dst[r] = split(src[r][0..64)) for r < rows (the 64 values of a row, K along the row).
+__global__ void __launch_bounds__(NT) split_rows_kernel(const float* __restrict__ src, int64_t ld, int rows,
+                                                        __nv_bfloat16* __restrict__ dst, bool b_form) {
+    const int64_t total = static_cast<int64_t>(rows) * NB;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(NT) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * NT) {
+        const int64_t r = i / NB;
+        const int kk = static_cast<int>(i % NB);
+        split_store(dst + r * K3, kk, src[r * ld + kk], b_form);
+    }
+}
+// dst[c] = split(src[0..64)[c]) for c < cols (K down the columns of a 64-row block):
+// 64 x 64 tiles through shared memory so that reads and writes stay coalesced.
+__global__ void __launch_bounds__(NT) split_cols_kernel(const float* __restrict__ src, int64_t ld, int cols,
+                                                        __nv_bfloat16* __restrict__ dst, bool b_form) {
+    __shared__ float t[NB][TLD];
+    const int c0 = blockIdx.x * NB;
     for (int e = threadIdx.x; e < NB * NB; e += NT) {
-        const int r = e / NB, cc = e % NB;
-        const float va = a[static_cast<int64_t>(r) * ld + cc];
-        if (upper)
-            sa[r][cc] = va;   // A^T: sa[kk][m] = L_ki[kk][m]
-        else
-            sa[cc][r] = va;   // sa[kk][m] = L_ik[m][kk]
-        sb[r][cc] = rk[static_cast<int64_t>(r) * ldr + cc];   // sb[kk][c] = R_k[kk][c]
+        const int kk = e / NB, c = e % NB;
+        t[kk][c] = c0 + c < cols ? src[static_cast<int64_t>(kk) * ld + c0 + c] : 0.f;
     }
     __syncthreads();
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    float acc[4][4] = {};
-#pragma unroll 8
-    for (int kk = 0; kk < NB; ++kk) {
-        float av[4], bv[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            av[q] = sa[kk][ty * 4 + q];
-            bv[q] = sb[kk][tx * 4 + q];
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int w = 0; w < 4; ++w) acc[q][w] = fmaf(av[q], bv[w], acc[q][w]);
+    for (int e = threadIdx.x; e < NB * NB; e += NT) {
+        const int c = e / NB, kk = e % NB;
+        if (c0 + c < cols) split_store(dst + static_cast<int64_t>(c0 + c) * K3, kk, t[kk][c], b_form);
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int w = 0; w < 4; ++w) c[static_cast<int64_t>(ty * 4 + q) * ldr + tx * 4 + w] -= acc[q][w];
 }
 
 }  // namespace
@@ -208,9 +208,12 @@ __global__ void __launch_bounds__(NT) rhs_update_kernel(const float* __restrict_
 
 using namespace tee;
 
+static size_t split_bytes(int rows) { return round_up(static_cast<size_t>(rows) * K3 * 2, 1024); }
+
 extern "C" size_t tee_ridge_fit_workspace_size(int32_t n, int32_t d, int32_t d_out) {
     if (n <= 0 || d <= 0 || d_out <= 0) return TEE_WS_HEADER_BYTES;
-    return TEE_WS_HEADER_BYTES + round_up(static_cast<size_t>(d) * d * 4, 1024) + ridge_gram_ws_bytes(n, d, d_out);
+    const size_t gram = ridge_gram_ws_bytes(n, d, d_out), split = split_bytes(d) + split_bytes(d_out);
+    return TEE_WS_HEADER_BYTES + round_up(static_cast<size_t>(d) * d * 4, 1024) + (gram > split ? gram : split);
 }
 
 extern "C" tee_status tee_ridge_fit(int32_t n, int32_t d, int32_t d_out, const void* x, int64_t ld_x, const void* y,
@@ -240,20 +243,40 @@ extern "C" tee_status tee_ridge_fit(int32_t n, int32_t d, int32_t d_out, const v
         syrk_kernel<<<m * (m + 1) / 2, NT, 0, s>>>(g, d, k, nb);
         if ((st = launch_status()) != TEE_OK) return st;
     }
+    // The substitutions' trailing updates run on the tensor cores with split operands
+    // (the Gram scratch is free by now): a3 [rows][192] from L, b3 [d_out][192] from
+    // the solved block row.
+    __nv_bfloat16* a3 = reinterpret_cast<__nv_bfloat16*>(scratch);
+    __nv_bfloat16* b3 = reinterpret_cast<__nv_bfloat16*>(scratch + split_bytes(d));
+    auto blocks_for = [](int64_t elems) {
+        const int64_t b = (elems + NT - 1) / NT;
+        return static_cast<int>(b < 2048 ? b : 2048);
+    };
     for (int k = 0; k < nb; ++k) {   // L Z = R
         trsm_rhs_kernel<<<d_out / RPC, NT, 0, s>>>(g, d, w, ld_w, k, false);
         if ((st = launch_status()) != TEE_OK) return st;
-        if (k + 1 < nb) {
-            rhs_update_kernel<<<(nb - 1 - k) * ncol, NT, 0, s>>>(g, d, w, ld_w, k, nb, false);
+        const int m = d - (k + 1) * NB;   // rows below: R_i -= L_ik Z_k
+        if (m > 0) {
+            split_rows_kernel<<<blocks_for(static_cast<int64_t>(m) * NB), NT, 0, s>>>(
+                g + static_cast<int64_t>(k + 1) * NB * d + static_cast<int64_t>(k) * NB, d, m, a3, false);
             if ((st = launch_status()) != TEE_OK) return st;
+            split_cols_kernel<<<ncol, NT, 0, s>>>(w + static_cast<int64_t>(k) * NB * ld_w, ld_w, d_out, b3, true);
+            if ((st = launch_status()) != TEE_OK) return st;
+            st = ridge_update_tc(m, d_out, K3, a3, b3, w + static_cast<int64_t>(k + 1) * NB * ld_w, ld_w, ws, s);
+            if (st != TEE_OK) return st;
         }
     }
     for (int k = nb - 1; k >= 0; --k) {   // L^T W = Z
         trsm_rhs_kernel<<<d_out / RPC, NT, 0, s>>>(g, d, w, ld_w, k, true);
         if ((st = launch_status()) != TEE_OK) return st;
-        if (k > 0) {
-            rhs_update_kernel<<<k * ncol, NT, 0, s>>>(g, d, w, ld_w, k, nb, true);
+        const int m = k * NB;   // rows above: R_i -= L_ki^T W_k, A[i][kk] = L[k NB + kk][i]
+        if (m > 0) {
+            split_cols_kernel<<<(m + NB - 1) / NB, NT, 0, s>>>(g + static_cast<int64_t>(k) * NB * d, d, m, a3, false);
             if ((st = launch_status()) != TEE_OK) return st;
+            split_cols_kernel<<<ncol, NT, 0, s>>>(w + static_cast<int64_t>(k) * NB * ld_w, ld_w, d_out, b3, true);
+            if ((st = launch_status()) != TEE_OK) return st;
+            st = ridge_update_tc(m, d_out, K3, a3, b3, w, ld_w, ws, s);
+            if (st != TEE_OK) return st;
         }
     }
     return TEE_OK;
