@@ -559,7 +559,11 @@ TEE_API tee_status tee_exit_river(const tee_river_desc* desc, int32_t n_layers, 
  * everything is enqueued on `stream` and the host results are valid once the
  * stream has completed. Host buffers should be page-locked for the copies to
  * run asynchronously. The results equal those of the two calls made on the
- * device buffers.
+ * device buffers. The step object captures the sequence into a CUDA graph on a
+ * stream of its own at the first call and replays it while n and the host
+ * pointers stay the same (events order it after and before `stream`); with
+ * pageable host memory, where the capture is refused, it enqueues the calls on
+ * `stream` directly. One step object must not be run from two threads at once.
  */
 typedef struct {
     /* device buffers owned by the caller, alive as long as the step object */

@@ -136,3 +136,15 @@ def test_decode_step_from_host_buffers(tee, cfg, case, seed):
     rows = comp["exit_rows"][:n_exit].long()
     assert torch.equal(out[rows.cpu()], out_dev[rows].cpu())   # the exiting rows, scattered to their slots
     assert torch.equal(x["k_cache"], k_dev) and torch.equal(x["v_cache"], v_dev)
+    # again with the same host buffers (the captured step replayed), then from pageable
+    # host memory (no capture: the calls enqueued directly); the same results each time
+    for host in (hi, {k: t.clone() for k, t in hi.items()}):
+        score2, mask2, counts2, out2 = score.clone().zero_(), mask.clone().zero_(), counts.clone().zero_(), out.clone()
+        if host is hi:
+            score2, mask2, counts2, out2 = score2.pin_memory(), mask2.pin_memory(), counts2.pin_memory(), out2.pin_memory()
+        step.run_host(host["h_prev"], host["h_cur"], host["pos"], host["seq"], score=score2, mask=mask2,
+                      counts=counts2, out=out2)
+        torch.cuda.synchronize()
+        assert torch.equal(score2, score) and torch.equal(mask2, mask) and torch.equal(counts2, counts)
+        assert torch.equal(out2[rows.cpu()], out[rows.cpu()])
+        assert torch.equal(x["k_cache"], k_dev) and torch.equal(x["v_cache"], v_dev)

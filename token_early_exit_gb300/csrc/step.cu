@@ -1,7 +1,12 @@
 // A whole decode step from host buffers to host buffers in one call: the
 // inputs' host-to-device copies, the front (gate + compaction + exit scatter)
-// and the KV fill of the exiting tokens, and the results' copies back, all
-// enqueued on one stream. It only sequences the library's own calls.
+// and the KV fill of the exiting tokens, and the results' copies back. It only
+// sequences the library's own calls. The sequence is captured once into a CUDA
+// graph on the step's own stream and replayed while the token count and the
+// host buffers stay the same (a serving loop's case), so that a step costs the
+// host one graph launch; the caller's stream and the step's stream are ordered
+// by two events. Where capture is refused (pageable host memory, for one) the
+// sequence is enqueued directly on the caller's stream instead.
 #include <new>
 
 #include "common.cuh"
@@ -18,6 +23,13 @@ struct tee_decode_step {
     void* v_cache;
     tee_cache_layout cache;
     tee_step_buffers buf;
+    // the captured sequence and the arguments it was captured for
+    cudaStream_t cap;
+    cudaEvent_t ev_in, ev_out;
+    cudaGraphExec_t exec;
+    bool graph_refused;
+    int g_n;
+    const void* g_ptr[8];
 };
 
 using namespace tee;
@@ -55,18 +67,32 @@ extern "C" tee_status tee_decode_step_create(const tee_gate_desc* gate, int32_t 
     s->v_cache = v_cache;
     s->cache = *cache;
     s->buf = *buf;
+    s->cap = nullptr;
+    s->ev_in = s->ev_out = nullptr;
+    s->exec = nullptr;
+    s->graph_refused = false;
+    s->g_n = -1;
+    if (cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s->ev_in, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s->ev_out, cudaEventDisableTiming) != cudaSuccess) {
+        const tee_status st = cuda_status(cudaGetLastError());
+        tee_decode_step_destroy(s);
+        return st == TEE_OK ? TEE_ERR_CUDA : st;
+    }
     *step = s;
     return TEE_OK;
 }
 
-extern "C" tee_status tee_decode_step_run_host(tee_decode_step* step, int32_t n, const void* h_prev, const void* h_cur,
-                                               const int32_t* pos, const int32_t* seq, float* score, uint8_t* mask,
-                                               int32_t* counts, void* out, void* stream) {
-    if (!step || n < 0 || n > step->n_max || !h_prev || !h_cur || !pos) return TEE_ERR_INVALID_ARG;
+namespace {
+
+// The step's copies and calls, enqueued on stream s.
+tee_status enqueue_step(tee_decode_step* step, int n, const void* h_prev, const void* h_cur, const int32_t* pos,
+                        const int32_t* seq, float* score, uint8_t* mask, int32_t* counts, void* out, cudaStream_t s) {
+
+    void* stream = s;
     const tee_step_buffers& b = step->buf;
     const int d = step->gate.d;
     const size_t row = static_cast<size_t>(d) * dtype_bytes(step->gate.dtype);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     // inputs
     tee_status st = cuda_status(cudaMemcpyAsync(b.h_prev, h_prev, n * row, cudaMemcpyHostToDevice, s));
     if (st == TEE_OK) st = cuda_status(cudaMemcpyAsync(b.h_cur, h_cur, n * row, cudaMemcpyHostToDevice, s));
@@ -96,8 +122,65 @@ extern "C" tee_status tee_decode_step_run_host(tee_decode_step* step, int32_t n,
     return st;
 }
 
+// Capture the sequence for these arguments into step->exec; false when the runtime
+// refuses the capture (the caller then enqueues directly).
+bool capture_step(tee_decode_step* step, int n, const void* const (&ptr)[8]) {
+    if (step->exec) {
+        cudaGraphExecDestroy(step->exec);
+        step->exec = nullptr;
+    }
+    step->g_n = -1;
+    if (cudaStreamBeginCapture(step->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    const tee_status st = enqueue_step(step, n, ptr[0], ptr[1], static_cast<const int32_t*>(ptr[2]),
+                                       static_cast<const int32_t*>(ptr[3]), static_cast<float*>(const_cast<void*>(ptr[4])),
+                                       static_cast<uint8_t*>(const_cast<void*>(ptr[5])),
+                                       static_cast<int32_t*>(const_cast<void*>(ptr[6])), const_cast<void*>(ptr[7]),
+                                       step->cap);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(step->cap, &graph);
+    bool ok = st == TEE_OK && e == cudaSuccess && graph &&
+              cudaGraphInstantiate(&step->exec, graph, 0) == cudaSuccess;
+    if (graph) cudaGraphDestroy(graph);
+    if (!ok) {
+        (void)cudaGetLastError();
+        step->exec = nullptr;
+        return false;
+    }
+    step->g_n = n;
+    for (int i = 0; i < 8; ++i) step->g_ptr[i] = ptr[i];
+    return true;
+}
+
+}  // namespace
+
+extern "C" tee_status tee_decode_step_run_host(tee_decode_step* step, int32_t n, const void* h_prev, const void* h_cur,
+                                               const int32_t* pos, const int32_t* seq, float* score, uint8_t* mask,
+                                               int32_t* counts, void* out, void* stream) {
+    if (!step || n < 0 || n > step->n_max || !h_prev || !h_cur || !pos) return TEE_ERR_INVALID_ARG;
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    const void* const ptr[8] = {h_prev, h_cur, pos, seq, score, mask, counts, out};
+    bool same = step->exec && step->g_n == n;
+    for (int i = 0; i < 8 && same; ++i) same = step->g_ptr[i] == ptr[i];
+    if (!same && !step->graph_refused && !capture_step(step, n, ptr)) step->graph_refused = true;
+    if (!step->exec || (!same && step->graph_refused))   // no graph for these arguments: enqueue directly
+        return enqueue_step(step, n, h_prev, h_cur, pos, seq, score, mask, counts, out, user);
+    tee_status st = cuda_status(cudaEventRecord(step->ev_in, user));
+    if (st == TEE_OK) st = cuda_status(cudaStreamWaitEvent(step->cap, step->ev_in, 0));
+    if (st == TEE_OK) st = cuda_status(cudaGraphLaunch(step->exec, step->cap));
+    if (st == TEE_OK) st = cuda_status(cudaEventRecord(step->ev_out, step->cap));
+    if (st == TEE_OK) st = cuda_status(cudaStreamWaitEvent(user, step->ev_out, 0));
+    return st;
+}
+
 extern "C" void tee_decode_step_destroy(tee_decode_step* step) {
     if (!step) return;
+    if (step->exec) cudaGraphExecDestroy(step->exec);
+    if (step->ev_in) cudaEventDestroy(step->ev_in);
+    if (step->ev_out) cudaEventDestroy(step->ev_out);
+    if (step->cap) cudaStreamDestroy(step->cap);
     delete[] step->layers;
     delete step;
 }
