@@ -8,9 +8,10 @@
 //   w4_gemm<QKV>        [q|k|v] = (h * g) . [Wq|Wk|Wv], times 1/rms(h); RoPE on
 //                       q and k; q to the workspace, k and v to the cache slot
 //   river_attn          per (item, kv head, chunk of 256 / 128 positions): TMA
-//                       brings the chunk's K and V; scores, partial softmax and
-//                       P.V on the CUDA cores; the last chunk of an (item, kv
-//                       head) merges the partials
+//                       brings the chunk's K and V; scores and P.V as warp-level
+//                       tensor-core products, the partial softmax on their
+//                       accumulators; the last chunk of an (item, kv head)
+//                       merges the partials
 //   w4_gemm<O>          h1 = h + o . Wo; bf16 (h1 * ffn_norm) and sum(h1^2)
 //   w4_gemm<GU>         gate | up from (h1 * g2) . [Wg|Wu] (64 columns of each
 //                       per tile), times 1/rms(h1); a = SiLU(gate) * up (bf16)
@@ -713,18 +714,18 @@ __host__ __device__ constexpr int at_box(int hd) { return hd == 64 ? 256 : 128; 
 
 template <int HD, int REP>
 struct AttnSmem {
-    static constexpr int RPT = 128 / HD;             // K rows per thread in the score pass
-    static constexpr int CHUNK = AT_THREADS * RPT;   // positions per CTA
-    static constexpr int PC = HD / 8;                // 16-byte pieces per row
-    static constexpr int RG = AT_THREADS / PC;       // row groups of the P.V pass
+    static constexpr int NW = AT_THREADS / 32;
+    static constexpr int CHUNK = at_box(HD);         // positions per CTA
+    static constexpr int WP = CHUNK / NW;            // positions per warp
+    static constexpr int MT = WP / 16;               // 16-position tiles per warp
+    static constexpr int KS = HD / 16;               // 16-column steps of a row
     static constexpr uint32_t KV_BYTES = CHUNK * HD * 2;   // 32 KB: halves of 64 columns, rows of 128 bytes
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
-    static constexpr uint32_t OFF_P = OFF_V + KV_BYTES;
-    static constexpr uint32_t OFF_RED = OFF_P + REP * CHUNK * 4;
-    static constexpr uint32_t OFF_Q = OFF_RED + (AT_THREADS / 32) * REP * HD * 4;
-    static constexpr uint32_t OFF_BAR = OFF_Q + REP * HD * 4;
+    static constexpr uint32_t OFF_RED = OFF_V + KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_RED + NW * REP * HD * 4;
     static constexpr size_t BYTES = 1024 + OFF_BAR + 64;
+    static_assert(REP <= 8 && MT >= 1 && WP % 16 == 0, "attention tiling");
 };
 
 // Byte offset of 16-byte piece q of row t in a swizzled K or V chunk: 64-column
@@ -734,31 +735,67 @@ __device__ __forceinline__ uint32_t sw_off(int t, int q) {
     return (q >> 3) * (CHUNK * 128) + t * 128 + (((q & 7) ^ (t & 7)) << 4);
 }
 
+// Warp-level bf16 products with fp32 accumulation (16 x 8 x 16 per instruction;
+// fragments as the PTX ISA's m16n8k16 layout: lane = 4 g + t holds rows g and
+// g + 8, columns 2t and 2t + 1 of a C tile).
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// bf16 pair, lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // One (chunk, kv head, item): TMA brings the chunk's K and V (swizzled) into
-// shared memory; scores, softmax statistics and P.V are computed from there on
-// the CUDA cores. The last chunk of an (item, kv head) to finish merges the
+// shared memory. Each warp takes WP positions: scores S^T = K Q^T (M = 16
+// positions, N = the kv head's query heads padded to 8, K = 16 columns of the
+// head) and O^T += V^T P^T (M = 16 columns, N = the heads, K = 16 positions) as
+// warp-level tensor-core products from registers; P^T comes from the score
+// accumulators by an in-register transpose. The softmax of a warp's positions is
+// taken on the accumulators; the warps' partial results are then merged by
+// their maxima, and the last chunk of an (item, kv head) to finish merges the
 // chunks' partials.
 template <int HD, int REP>
 __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_constant__ AttnArgs a) {
     using S = AttnSmem<HD, REP>;
-    constexpr int RPT = S::RPT, CHUNK = S::CHUNK, PC = S::PC, RG = S::RG;
-    constexpr int NW = AT_THREADS / 32;
+    constexpr int NW = S::NW, CHUNK = S::CHUNK, WP = S::WP, MT = S::MT, KS = S::KS;
     extern __shared__ uint8_t at_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
-    const uint8_t* s_k = sm + S::OFF_K;
     uint8_t* s_v = sm + S::OFF_V;
-    float (*s_p)[CHUNK] = reinterpret_cast<float (*)[CHUNK]>(sm + S::OFF_P);
     float (*s_red)[REP][HD] = reinterpret_cast<float (*)[REP][HD]>(sm + S::OFF_RED);
-    float (*s_q)[HD] = reinterpret_cast<float (*)[HD]>(sm + S::OFF_Q);
     uint64_t* kbar = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);
     uint64_t* vbar = kbar + 1;
     volatile int* abort = reinterpret_cast<volatile int*>(vbar + 1);
-    __shared__ float s_mx[REP][NW], s_l[REP][NW];
+    __shared__ float s_mw[NW][8], s_lw[NW][8], s_ww[REP][NW];
     __shared__ float s_m[REP], s_sum[REP];
     __shared__ int s_last;
 
     const int c = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lg = lane >> 2, lt = lane & 3;   // fragment row group and column pair
     allow_dependents();
     const int n = item_count(a.n_max, a.n_dev);
     if (m >= n) return;
@@ -778,155 +815,151 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
         tc::mbar_init(vbar, 1);
         *abort = 0;
         tc::fence_barrier_init();
-        constexpr int AT_BOX = at_box(HD);
-        const int nb = (cnt + AT_BOX - 1) / AT_BOX;
-        const uint32_t bytes = static_cast<uint32_t>(nb) * (HD / 64) * AT_BOX * 128;
+        const uint32_t bytes = (HD / 64) * CHUNK * 128;
         const int sq = a.iseq[m];
         tc::mbar_arrive_expect_tx(kbar, bytes);
-        for (int b = 0; b < nb; ++b)
-            for (int h = 0; h < HD / 64; ++h)
-                tc::tma_load_5d(sm + S::OFF_K + h * (CHUNK * 128) + b * (AT_BOX * 128), &a.kmap, 64 * h,
-                                t0 + b * AT_BOX, g, sq, a.layer, kbar);
+        for (int h = 0; h < HD / 64; ++h)
+            tc::tma_load_5d(sm + S::OFF_K + h * (CHUNK * 128), &a.kmap, 64 * h, t0, g, sq, a.layer, kbar);
         tc::mbar_arrive_expect_tx(vbar, bytes);
-        for (int b = 0; b < nb; ++b)
-            for (int h = 0; h < HD / 64; ++h)
-                tc::tma_load_5d(s_v + h * (CHUNK * 128) + b * (AT_BOX * 128), &a.vmap, 64 * h, t0 + b * AT_BOX, g,
-                                sq, a.layer, vbar);
+        for (int h = 0; h < HD / 64; ++h)
+            tc::tma_load_5d(s_v + h * (CHUNK * 128), &a.vmap, 64 * h, t0, g, sq, a.layer, vbar);
     }
-    for (int i = tid; i < REP * HD; i += AT_THREADS)
-        s_q[i / HD][i % HD] = __bfloat162float(a.qbuf[static_cast<int64_t>(m) * a.qw + g * REP * HD + i]) * a.qscale;
-    __syncthreads();
-    if (!tc::mbar_wait(kbar, 0, abort, a.ws, 91)) *abort = 1;
-
-    // scores: thread -> rows tid + 128 j
-    float mx[REP];
-#pragma unroll
-    for (int r = 0; r < REP; ++r) mx[r] = -INFINITY;
+    // Q^T fragments (columns 2t, 2t + 1 and 2t + 8, 2t + 9 of query head g; heads
+    // past REP are zero), unscaled bf16: the softmax scale multiplies the fp32 scores
+    uint32_t qb[KS][2];
     {
-        float acc[RPT][REP];
+        const bf16* qrow = a.qbuf + static_cast<int64_t>(m) * a.qw + (static_cast<int64_t>(g) * REP + lg) * HD;
 #pragma unroll
-        for (int j = 0; j < RPT; ++j)
-#pragma unroll
-            for (int r = 0; r < REP; ++r) acc[j][r] = 0.f;
-#pragma unroll
-        for (int q = 0; q < PC; ++q) {
-            float k8[RPT][8];
-#pragma unroll
-            for (int j = 0; j < RPT; ++j) {
-                const uint4 u = *reinterpret_cast<const uint4*>(s_k + sw_off<CHUNK>(tid + j * AT_THREADS, q));
-                unpack_bf16x2(u.x, k8[j][0], k8[j][1]);
-                unpack_bf16x2(u.y, k8[j][2], k8[j][3]);
-                unpack_bf16x2(u.z, k8[j][4], k8[j][5]);
-                unpack_bf16x2(u.w, k8[j][6], k8[j][7]);
-            }
-#pragma unroll
-            for (int r = 0; r < REP; ++r) {
-                const float4 qa = *reinterpret_cast<const float4*>(&s_q[r][8 * q]);
-                const float4 qb = *reinterpret_cast<const float4*>(&s_q[r][8 * q + 4]);
-                const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-                for (int j = 0; j < RPT; ++j)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[j][r] = fmaf(qv[e], k8[j][e], acc[j][r]);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            const int tt = tid + j * AT_THREADS;
-            if (tt >= cnt) continue;
-#pragma unroll
-            for (int r = 0; r < REP; ++r) {
-                s_p[r][tt] = acc[j][r];
-                mx[r] = fmaxf(mx[r], acc[j][r]);
-            }
+        for (int kk = 0; kk < KS; ++kk) {
+            qb[kk][0] = lg < REP ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * lt) : 0u;
+            qb[kk][1] = lg < REP ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * lt + 8) : 0u;
         }
     }
+    __syncthreads();   // the barriers' initialisation
+    const int pw = warp * WP;   // the warp's first position in the chunk
+    const float qs = a.qscale;
+    // lane l addresses row (l % 8) of matrix l / 8 of each ldmatrix; rows are 16-position tiles' rows
+    const int rr = lane & 7, mi = lane >> 3;
+    bool ok = tc::mbar_wait(kbar, 0, abort, a.ws, 91);
+    float mh[2] = {-INFINITY, -INFINITY}, lh[2] = {0.f, 0.f};   // heads 2t and 2t + 1
+    float o[KS][4];
 #pragma unroll
-    for (int r = 0; r < REP; ++r) {
-        float v = mx[r];
+    for (int j = 0; j < KS; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    uint32_t pb[MT][2];
+    if (pw < cnt) {
+        float s[MT][4];
+        const uint32_t kbase = tc::smem_u32(sm + S::OFF_K);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-        if (lane == 0) s_mx[r][warp] = v;
-    }
-    __syncthreads();
-    if (tid < REP) {
-        float v = -INFINITY;
-        for (int w = 0; w < NW; ++w) v = fmaxf(v, s_mx[tid][w]);
-        s_m[tid] = v;
-    }
-    __syncthreads();
-    {
-        float ls[REP];
+        for (int i = 0; i < MT; ++i) {
+            s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+            const int row = pw + 16 * i + ((mi & 1) << 3) + rr;   // a0 / a1: rows g, g + 8; a2 / a3: columns + 8
 #pragma unroll
-        for (int r = 0; r < REP; ++r) ls[r] = 0.f;
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t fa[4];
+                ldsm4(kbase + sw_off<CHUNK>(row, 2 * kk + (mi >> 1)), fa);
+                mma16816(s[i], fa, qb[kk][0], qb[kk][1]);
+            }
+        }
+        if (pw + WP > cnt) {   // the sequence ends inside this warp's positions
 #pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            const int tt = tid + j * AT_THREADS;
-            if (tt >= cnt) continue;
-#pragma unroll
-            for (int r = 0; r < REP; ++r) {
-                const float p = exp2f(s_p[r][tt] - s_m[r]);
-                s_p[r][tt] = p;
-                ls[r] += p;
+            for (int i = 0; i < MT; ++i) {
+                const int p0 = pw + 16 * i + lg;
+                if (p0 >= cnt) s[i][0] = s[i][1] = -INFINITY;
+                if (p0 + 8 >= cnt) s[i][2] = s[i][3] = -INFINITY;
             }
         }
 #pragma unroll
-        for (int r = 0; r < REP; ++r) {
-            const float v = warp_sum(ls[r]);
-            if (lane == 0) s_l[r][warp] = v;
+        for (int i = 0; i < MT; ++i) {
+            mh[0] = fmaxf(mh[0], fmaxf(s[i][0], s[i][2]));
+            mh[1] = fmaxf(mh[1], fmaxf(s[i][1], s[i][3]));
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) mh[e] = fmaxf(mh[e], __shfl_xor_sync(0xFFFFFFFFu, mh[e], sh));
+        // scores to the log2 domain: s * log2(e) / sqrt(head_dim); position pw is
+        // valid, so the maxima are finite
+        mh[0] *= qs;
+        mh[1] *= qs;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            const float p0 = exp2f(fmaf(s[i][0], qs, -mh[0])), p1 = exp2f(fmaf(s[i][1], qs, -mh[1]));
+            const float p2 = exp2f(fmaf(s[i][2], qs, -mh[0])), p3 = exp2f(fmaf(s[i][3], qs, -mh[1]));
+            lh[0] += p0 + p2;
+            lh[1] += p1 + p3;
+            pb[i][0] = movm_t(pack_bf16(p0, p1));   // P^T rows 2t, 2t + 1 of this tile, query head g
+            pb[i][1] = movm_t(pack_bf16(p2, p3));
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) lh[e] += __shfl_xor_sync(0xFFFFFFFFu, lh[e], sh);
+    }
+    ok = tc::mbar_wait(vbar, 0, abort, a.ws, 92) && ok;
+    ok = __all_sync(0xFFFFFFFFu, ok);   // the warp-wide instructions below run in whole warps only
+    if (pw < cnt && ok) {
+        if (pw + WP > cnt) {
+            // rows past the sequence hold whatever the cache slots hold (maybe not
+            // finite): zero them, since their weight 0 times a NaN would not vanish
+            constexpr int PR = (HD / 64) * 8;   // 16-byte pieces of a row
+            const int r0 = cnt - pw;
+            for (int idx = lane; idx < (WP - r0) * PR; idx += 32) {
+                const int row = pw + r0 + idx / PR, pc = idx % PR;
+                *reinterpret_cast<uint4*>(s_v + (pc >> 3) * (CHUNK * 128) + row * 128 + (pc & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+        const uint32_t vbase = tc::smem_u32(s_v);
+#pragma unroll
+        for (int j = 0; j < KS; ++j)
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                const int row = pw + 16 * i + ((mi >> 1) << 3) + rr;   // a0 / a2: positions 0-7 / 8-15 of the tile
+                uint32_t fa[4];
+                ldsm4_t(vbase + sw_off<CHUNK>(row, 2 * j + (mi & 1)), fa);
+                mma16816(o[j], fa, pb[i][0], pb[i][1]);
+            }
+        // O^T fragments: rows = columns 16 j + g (+ 8), columns = heads 2t, 2t + 1
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * lt + e;
+            if (h < REP)
+#pragma unroll
+                for (int j = 0; j < KS; ++j) {
+                    s_red[warp][h][16 * j + lg] = o[j][e];
+                    s_red[warp][h][16 * j + lg + 8] = o[j][2 + e];
+                }
+        }
+        if (lg == 0) {
+            s_mw[warp][2 * lt] = mh[0];
+            s_mw[warp][2 * lt + 1] = mh[1];
+            s_lw[warp][2 * lt] = lh[0];
+            s_lw[warp][2 * lt + 1] = lh[1];
         }
     }
-    if (!tc::mbar_wait(vbar, 0, abort, a.ws, 92)) *abort = 1;
+    if (!ok) *abort = 1;
     __syncthreads();
     if (*abort) return;
+    const int nwa = min(NW, (cnt + WP - 1) / WP);   // warps that saw positions
     if (tid < REP) {
-        float v = 0.f;
-        for (int w = 0; w < NW; ++w) v += s_l[tid][w];
-        s_sum[tid] = v;
-    }
-    // P.V: thread (row group rg, piece pc): rows rg, rg + RG, ...; 8 columns
-    {
-        const int rg = tid / PC, pc = tid % PC;
-        float o[REP][8];
-#pragma unroll
-        for (int r = 0; r < REP; ++r)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[r][e] = 0.f;
-#pragma unroll 4
-        for (int tt = rg; tt < cnt; tt += RG) {
-            const uint4 vr = *reinterpret_cast<const uint4*>(s_v + sw_off<CHUNK>(tt, pc));
-            float v8[8];
-            unpack_bf16x2(vr.x, v8[0], v8[1]);
-            unpack_bf16x2(vr.y, v8[2], v8[3]);
-            unpack_bf16x2(vr.z, v8[4], v8[5]);
-            unpack_bf16x2(vr.w, v8[6], v8[7]);
-#pragma unroll
-            for (int r = 0; r < REP; ++r) {
-                const float p = s_p[r][tt];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[r][e] = fmaf(p, v8[e], o[r][e]);
-            }
+        float M = -INFINITY;
+        for (int w = 0; w < nwa; ++w) M = fmaxf(M, s_mw[w][tid]);
+        float L = 0.f;
+        for (int w = 0; w < nwa; ++w) {
+            const float wt = exp2f(s_mw[w][tid] - M);
+            s_ww[tid][w] = wt;
+            L = fmaf(s_lw[w][tid], wt, L);
         }
-        // the row groups of a warp, then the warps
-#pragma unroll
-        for (int r = 0; r < REP; ++r)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-#pragma unroll
-                for (int sh = PC; sh < 32; sh <<= 1) o[r][e] += __shfl_xor_sync(0xFFFFFFFFu, o[r][e], sh);
-        if (lane < PC)
-#pragma unroll
-            for (int r = 0; r < REP; ++r)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) s_red[warp][r][8 * pc + e] = o[r][e];
+        s_m[tid] = M;
+        s_sum[tid] = L;
     }
     __syncthreads();
     if (nch == 1) {   // the whole range in this CTA: normalise and store
         for (int i = tid; i < REP * HD; i += AT_THREADS) {
             const int r = i / HD, e = i % HD;
             float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) v += s_red[w][r][e];
+            for (int w = 0; w < nwa; ++w) v = fmaf(s_red[w][r][e], s_ww[r][w], v);
             out[i] = __float2bfloat16_rn(v / s_sum[r]);
         }
         return;
@@ -935,8 +968,7 @@ __global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_con
     for (int i = tid; i < REP * HD; i += AT_THREADS) {
         const int r = i / HD, e = i % HD;
         float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) v += s_red[w][r][e];
+        for (int w = 0; w < nwa; ++w) v = fmaf(s_red[w][r][e], s_ww[r][w], v);
         pp[r * (HD + 2) + e] = v;
     }
     if (tid < REP) {
