@@ -45,7 +45,7 @@ constexpr uint32_t RIVER_MAGIC = 0x54455256u;  // "TERV"
 
 // ------------------------------------------------------------------ workspace
 struct RiverWs {
-    size_t resid, abuf, qbuf, obuf, act, ss_a, ss_f, ipos, iseq, acnt, apart, end;
+    size_t resid, abuf, qbuf, obuf, act, ss_a, ss_f, ipos, iseq, acnt, end;
 };
 
 constexpr int GT_N = 128;        // output columns per GEMM tile
@@ -91,7 +91,6 @@ static_assert(G_SMEM <= 232448, "shared memory");
 constexpr int MAX_KS = 8;        // K splits = CTAs of a cluster (portable size)
 constexpr int MAX_ITEMS = 128;
 
-int at_chunk(int hd) { return hd == 64 ? 256 : 128; }
 constexpr int KG_CNT = 64 * 8;   // counters of the two-cluster K split: tiles (<= 64) x ks (<= 8)
 
 int max_clusters(int ks);
@@ -120,11 +119,9 @@ int choose_kg(int tiles, int ks, int K) {
                : 1;
 }
 
-RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
+RiverWs river_ws(const tee_river_desc& D, int n_max) {
     const size_t n = static_cast<size_t>(n_max > 0 ? n_max : 1);
     const size_t d = D.d, qw = static_cast<size_t>(D.n_q_heads) * D.head_dim, f = D.d_ff;
-    const int rep = D.n_q_heads / std::max(1, D.n_kv_heads);
-    const size_t chunks = (static_cast<size_t>(max_pos) + at_chunk(D.head_dim) - 1) / at_chunk(D.head_dim);
     RiverWs w{};
     size_t o = TEE_WS_HEADER_BYTES;
     auto take = [&](size_t bytes) {
@@ -142,8 +139,7 @@ RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
     w.ss_f = take(n * 4);
     w.ipos = take(n * 4);
     w.iseq = take(n * 4);
-    w.acnt = take(n * D.n_kv_heads * 4 + KG_CNT * 4);   // then the K groups' counters (tiles x ks)
-    w.apart = take(n * D.n_kv_heads * chunks * rep * (D.head_dim + 2) * 4);
+    w.acnt = take(KG_CNT * 4);   // the K groups' counters (tiles x ks)
     w.end = o;
     return w;
 }
@@ -168,7 +164,7 @@ struct GatherArgs {
     float* ss_f;
     int32_t* ipos;
     int32_t* iseq;
-    int32_t* cnt;   // the attention's arrival counters
+    int32_t* cnt;   // the K-split GEMMs' arrival counters
     int n_cnt;
 };
 
@@ -691,41 +687,60 @@ __global__ void __launch_bounds__(G_THREADS, 1) w4_gemm_kernel(const __grid_cons
 
 // ------------------------------------------------------------------ attention
 struct AttnArgs {
-    CUtensorMap kmap, vmap;   // the caches, 5-D (head_dim, pos, head, seq, layer), box 64 x 64, 128-byte swizzle
+    CUtensorMap kmap, vmap;   // the caches, 5-D (head_dim, pos, head, seq, layer), box 64 x chunk, 128-byte swizzle
     int n_max;
     const int32_t* n_dev;
-    int n_kv, qw, chunks;
+    int n_kv, qw;
     const bf16* qbuf;
     const int32_t* ipos;
     const int32_t* iseq;
     int layer;
     float qscale;          // log2(e) / sqrt(head_dim)
-    float* part;           // [n][n_kv][chunks][REP][HD + 2]
-    int32_t* cnt;          // [n][n_kv]
     bf16* obuf;            // [n][qw]
     void* ws;
 };
 
-constexpr int AT_THREADS = 128;
-// positions per TMA box: the whole chunk in one copy (a copy costs about the same
-// whatever its size; the last chunk of a sequence reads up to CHUNK - 1 rows it
-// does not use)
-__host__ __device__ constexpr int at_box(int hd) { return hd == 64 ? 256 : 128; }
+// The attention is persistent: one CTA per SM, two consumer groups of four
+// warps, each fed by its own producer warp through its own ring of AT_STAGES
+// stages (a chunk of K and of V, TMA, one barrier each; the q rows, one bulk
+// copy, with a pair's first chunk). A group takes every chunk of an (item, kv
+// head) pair in order, so no chunk leaves a partial result: each warp keeps the
+// online softmax (running maximum, sum and O) of its positions of every chunk in
+// registers, and the four warps merge once, after the pair's last chunk. The
+// pairs are ranked longest first (every CTA ranks the items the same way) and
+// dealt to the groups in snake order, so that each group's chunks add up to
+// about the same.
+// In a chunk each warp takes WP positions: scores S^T = K Q^T (M = 16 positions,
+// N = the kv head's query heads padded to 8, K = 16 columns of the head) and
+// O^T += V^T P^T (M = 16 columns, N = the heads, K = 16 positions) as warp-level
+// tensor-core products from registers, P^T coming from the score accumulators
+// by an in-register transpose.
+constexpr int AT_GROUPS = 2;                              // consumer groups
+constexpr int AT_GT = 128;                                // threads of a group
+constexpr int AT_PROD_WARP = AT_GROUPS * AT_GT / 32;      // warps 8 + g issue group g's copies
+constexpr int AT_THREADS = (AT_PROD_WARP + AT_GROUPS) * 32;
+constexpr int AT_STAGES = 3;
+constexpr int AT_MAX_ITEMS = 128;
+// positions per chunk: 16 KB of K (one TMA box per 64 columns; the last chunk of
+// a sequence reads up to CHUNK - 1 rows it does not use)
+__host__ __device__ constexpr int at_box(int hd) { return 8192 / hd; }
 
 template <int HD, int REP>
 struct AttnSmem {
-    static constexpr int NW = AT_THREADS / 32;
-    static constexpr int CHUNK = at_box(HD);         // positions per CTA
+    static constexpr int NW = AT_GT / 32;            // warps of a group
+    static constexpr int CHUNK = at_box(HD);         // positions per chunk
     static constexpr int WP = CHUNK / NW;            // positions per warp
     static constexpr int MT = WP / 16;               // 16-position tiles per warp
     static constexpr int KS = HD / 16;               // 16-column steps of a row
-    static constexpr uint32_t KV_BYTES = CHUNK * HD * 2;   // 32 KB: halves of 64 columns, rows of 128 bytes
-    static constexpr uint32_t OFF_K = 0;
-    static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
-    static constexpr uint32_t OFF_RED = OFF_V + KV_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_RED + NW * REP * HD * 4;
-    static constexpr size_t BYTES = 1024 + OFF_BAR + 64;
+    static constexpr uint32_t KV_BYTES = CHUNK * HD * 2;     // 16 KB: halves of 64 columns, rows of 128 bytes
+    static constexpr uint32_t STAGE = 2 * KV_BYTES + 2048;   // K | V | q rows (stages stay 1024-aligned)
+    static constexpr uint32_t OFF_TAB = AT_GROUPS * AT_STAGES * STAGE;   // pos | seq | order, AT_MAX_ITEMS + 4 each
+    static constexpr uint32_t OFF_BAR = OFF_TAB + 3 * (AT_MAX_ITEMS + 4) * 4;
+    static constexpr size_t BYTES = 1024 + OFF_BAR + 3 * AT_GROUPS * AT_STAGES * 8 + 16;
     static_assert(REP <= 8 && MT >= 1 && WP % 16 == 0, "attention tiling");
+    static_assert(REP * HD * 2 <= 2048, "q rows fit the stage");
+    static_assert(NW * REP * HD * 4 <= KV_BYTES, "the warps' results fit the V buffer");
+    static_assert(STAGE % 1024 == 0 && BYTES <= 232448, "shared memory");
 };
 
 // Byte offset of 16-byte piece q of row t in a swizzled K or V chunk: 64-column
@@ -768,268 +783,317 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// Barrier of consumer group grp (its 128 threads) that also returns whether v
+// holds in every one of them. The aligned barrier wants each warp converged.
+__device__ __forceinline__ bool group_all(int grp, bool v) {
+    uint32_t r;
+    __syncwarp();
+    asm volatile(
+        "{\n"
+        ".reg .pred p, q;\n"
+        "setp.ne.u32 p, %1, 0;\n"
+        "bar.red.and.pred q, %2, %3, p;\n"
+        "selp.u32 %0, 1, 0, q;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(1 + grp), "r"(AT_GT)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void group_sync(int grp) {
+    __syncwarp();
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(AT_GT) : "memory");
+}
 
-// One (chunk, kv head, item): TMA brings the chunk's K and V (swizzled) into
-// shared memory. Each warp takes WP positions: scores S^T = K Q^T (M = 16
-// positions, N = the kv head's query heads padded to 8, K = 16 columns of the
-// head) and O^T += V^T P^T (M = 16 columns, N = the heads, K = 16 positions) as
-// warp-level tensor-core products from registers; P^T comes from the score
-// accumulators by an in-register transpose. The softmax of a warp's positions is
-// taken on the accumulators; the warps' partial results are then merged by
-// their maxima, and the last chunk of an (item, kv head) to finish merges the
-// chunks' partials.
+// The k-th (item, kv head) pair of group gg (of G) in snake order over the
+// ranked pairs, or -1 past the last.
+__device__ __forceinline__ int snake_pair(int k, int gg, int G, int pairs) {
+    const int p = k * G + ((k & 1) ? G - 1 - gg : gg);
+    return p < pairs ? p : -1;
+}
+
 template <int HD, int REP>
-__global__ void __launch_bounds__(AT_THREADS) river_attn_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(AT_THREADS, 1) river_attn_kernel(const __grid_constant__ AttnArgs a) {
     using S = AttnSmem<HD, REP>;
     constexpr int NW = S::NW, CHUNK = S::CHUNK, WP = S::WP, MT = S::MT, KS = S::KS;
     extern __shared__ uint8_t at_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* s_v = sm + S::OFF_V;
-    float (*s_red)[REP][HD] = reinterpret_cast<float (*)[REP][HD]>(sm + S::OFF_RED);
-    uint64_t* kbar = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);
-    uint64_t* vbar = kbar + 1;
-    volatile int* abort = reinterpret_cast<volatile int*>(vbar + 1);
-    __shared__ float s_mw[NW][8], s_lw[NW][8], s_ww[REP][NW];
-    __shared__ float s_m[REP], s_sum[REP];
-    __shared__ int s_last;
+    int* s_pos = reinterpret_cast<int*>(sm + S::OFF_TAB);
+    int* s_seq = s_pos + AT_MAX_ITEMS + 4;
+    int* s_order = s_seq + AT_MAX_ITEMS + 4;   // the items, longest sequence first; then the skipped ones
+    uint64_t* kfull = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);   // [group][stage]
+    uint64_t* vfull = kfull + AT_GROUPS * AT_STAGES;
+    uint64_t* empty = vfull + AT_GROUPS * AT_STAGES;
+    volatile int* abort = reinterpret_cast<volatile int*>(empty + AT_GROUPS * AT_STAGES);
+    __shared__ float s_mw[AT_GROUPS][NW][8], s_lw[AT_GROUPS][NW][8];   // the warps' maxima and sums per query head
+    __shared__ int s_valid;
 
-    const int c = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int lg = lane >> 2, lt = lane & 3;   // fragment row group and column pair
     allow_dependents();
-    const int n = item_count(a.n_max, a.n_dev);
-    if (m >= n) return;
-    wait_prior_grid();   // q, the item table and the cache slots come from the q|k|v GEMM
-    const int pm = a.ipos[m];
-    bf16* out = a.obuf + static_cast<int64_t>(m) * a.qw + static_cast<int64_t>(g) * REP * HD;
-    if (pm < 0) {   // a skipped item attends to nothing
-        if (c == 0)
-            for (int i = tid; i < REP * HD; i += AT_THREADS) out[i] = __float2bfloat16_rn(0.f);
-        return;
-    }
-    const int nch = pm / CHUNK + 1;
-    if (c >= nch) return;
-    const int t0 = c * CHUNK, cnt = min(CHUNK, pm + 1 - t0);
     if (tid == 0) {
-        tc::mbar_init(kbar, 1);
-        tc::mbar_init(vbar, 1);
+        for (int i = 0; i < AT_GROUPS * AT_STAGES; ++i) {
+            tc::mbar_init(&kfull[i], 1);
+            tc::mbar_init(&vfull[i], 1);
+            tc::mbar_init(&empty[i], 1);
+        }
         *abort = 0;
         tc::fence_barrier_init();
-        const uint32_t bytes = (HD / 64) * CHUNK * 128;
-        const int sq = a.iseq[m];
-        tc::mbar_arrive_expect_tx(kbar, bytes);
-        for (int h = 0; h < HD / 64; ++h)
-            tc::tma_load_5d(sm + S::OFF_K + h * (CHUNK * 128), &a.kmap, 64 * h, t0, g, sq, a.layer, kbar);
-        tc::mbar_arrive_expect_tx(vbar, bytes);
-        for (int h = 0; h < HD / 64; ++h)
-            tc::tma_load_5d(s_v + h * (CHUNK * 128), &a.vmap, 64 * h, t0, g, sq, a.layer, vbar);
     }
-    // Q^T fragments (columns 2t, 2t + 1 and 2t + 8, 2t + 9 of query head g; heads
-    // past REP are zero), unscaled bf16: the softmax scale multiplies the fp32 scores
-    uint32_t qb[KS][2];
-    {
-        const bf16* qrow = a.qbuf + static_cast<int64_t>(m) * a.qw + (static_cast<int64_t>(g) * REP + lg) * HD;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            qb[kk][0] = lg < REP ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * lt) : 0u;
-            qb[kk][1] = lg < REP ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * lt + 8) : 0u;
-        }
+    wait_prior_grid();   // q, the item table and the cache slots come from the q|k|v GEMM
+    const int n = item_count(a.n_max, a.n_dev);
+    for (int m = tid; m < n; m += AT_THREADS) {
+        s_pos[m] = a.ipos[m];
+        s_seq[m] = a.iseq[m];
     }
-    __syncthreads();   // the barriers' initialisation
-    const int pw = warp * WP;   // the warp's first position in the chunk
-    const float qs = a.qscale;
-    // lane l addresses row (l % 8) of matrix l / 8 of each ldmatrix; rows are 16-position tiles' rows
-    const int rr = lane & 7, mi = lane >> 3;
-    bool ok = tc::mbar_wait(kbar, 0, abort, a.ws, 91);
-    float mh[2] = {-INFINITY, -INFINITY}, lh[2] = {0.f, 0.f};   // heads 2t and 2t + 1
-    float o[KS][4];
-#pragma unroll
-    for (int j = 0; j < KS; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    uint32_t pb[MT][2];
-    if (pw < cnt) {
-        float s[MT][4];
-        const uint32_t kbase = tc::smem_u32(sm + S::OFF_K);
-#pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-            const int row = pw + 16 * i + ((mi & 1) << 3) + rr;   // a0 / a1: rows g, g + 8; a2 / a3: columns + 8
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                uint32_t fa[4];
-                ldsm4(kbase + sw_off<CHUNK>(row, 2 * kk + (mi >> 1)), fa);
-                mma16816(s[i], fa, qb[kk][0], qb[kk][1]);
-            }
+    __syncthreads();
+    // rank the items by chunk count, longest first (ties by index; skipped items last)
+    if (tid == 0) s_valid = 0;
+    __syncthreads();
+    for (int m = tid; m < n; m += AT_THREADS) {
+        const int km = s_pos[m] >= 0 ? s_pos[m] / CHUNK + 1 : 0;
+        int r = 0;
+        for (int j = 0; j < n; ++j) {
+            const int kj = s_pos[j] >= 0 ? s_pos[j] / CHUNK + 1 : 0;
+            r += kj > km || (kj == km && j < m);
         }
-        if (pw + WP > cnt) {   // the sequence ends inside this warp's positions
-#pragma unroll
-            for (int i = 0; i < MT; ++i) {
-                const int p0 = pw + 16 * i + lg;
-                if (p0 >= cnt) s[i][0] = s[i][1] = -INFINITY;
-                if (p0 + 8 >= cnt) s[i][2] = s[i][3] = -INFINITY;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            mh[0] = fmaxf(mh[0], fmaxf(s[i][0], s[i][2]));
-            mh[1] = fmaxf(mh[1], fmaxf(s[i][1], s[i][3]));
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-#pragma unroll
-            for (int sh = 4; sh < 32; sh <<= 1) mh[e] = fmaxf(mh[e], __shfl_xor_sync(0xFFFFFFFFu, mh[e], sh));
-        // scores to the log2 domain: s * log2(e) / sqrt(head_dim); position pw is
-        // valid, so the maxima are finite
-        mh[0] *= qs;
-        mh[1] *= qs;
-#pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            const float p0 = exp2f(fmaf(s[i][0], qs, -mh[0])), p1 = exp2f(fmaf(s[i][1], qs, -mh[1]));
-            const float p2 = exp2f(fmaf(s[i][2], qs, -mh[0])), p3 = exp2f(fmaf(s[i][3], qs, -mh[1]));
-            lh[0] += p0 + p2;
-            lh[1] += p1 + p3;
-            pb[i][0] = movm_t(pack_bf16(p0, p1));   // P^T rows 2t, 2t + 1 of this tile, query head g
-            pb[i][1] = movm_t(pack_bf16(p2, p3));
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-#pragma unroll
-            for (int sh = 4; sh < 32; sh <<= 1) lh[e] += __shfl_xor_sync(0xFFFFFFFFu, lh[e], sh);
+        s_order[r] = m;
+        if (km > 0) atomicAdd(&s_valid, 1);
     }
-    ok = tc::mbar_wait(vbar, 0, abort, a.ws, 92) && ok;
-    ok = __all_sync(0xFFFFFFFFu, ok);   // the warp-wide instructions below run in whole warps only
-    if (pw < cnt && ok) {
-        if (pw + WP > cnt) {
-            // rows past the sequence hold whatever the cache slots hold (maybe not
-            // finite): zero them, since their weight 0 times a NaN would not vanish
-            constexpr int PR = (HD / 64) * 8;   // 16-byte pieces of a row
-            const int r0 = cnt - pw;
-            for (int idx = lane; idx < (WP - r0) * PR; idx += 32) {
-                const int row = pw + r0 + idx / PR, pc = idx % PR;
-                *reinterpret_cast<uint4*>(s_v + (pc >> 3) * (CHUNK * 128) + row * 128 + (pc & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            __syncwarp();
-        }
-        const uint32_t vbase = tc::smem_u32(s_v);
+    __syncthreads();
+    const int pairs = s_valid * a.n_kv;
+    // a skipped item (position < 0) attends to nothing: its output rows are zero
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * AT_THREADS + tid; i < static_cast<int64_t>(n) * a.qw;
+         i += static_cast<int64_t>(gridDim.x) * AT_THREADS) {
+        const int m = static_cast<int>(i / a.qw);
+        if (s_pos[m] < 0) a.obuf[i] = __float2bfloat16_rn(0.f);
+    }
+    const int G = AT_GROUPS * static_cast<int>(gridDim.x);
+
+    if (warp >= AT_PROD_WARP) {   // group (warp - 8)'s copies
+        const int grp = warp - AT_PROD_WARP, gg = static_cast<int>(blockIdx.x) * AT_GROUPS + grp;
+        if (lane == 0) {
+            uint64_t* kf = kfull + grp * AT_STAGES;
+            uint64_t* vf = vfull + grp * AT_STAGES;
+            uint64_t* em = empty + grp * AT_STAGES;
+            int u = 0;   // chunks issued
+            bool go = true;
+            for (int k = 0; go; ++k) {
+                const int p = snake_pair(k, gg, G, pairs);
+                if (p < 0) break;
+                const int m = s_order[p / a.n_kv], g = p % a.n_kv;
+                const int nch = s_pos[m] / CHUNK + 1;
+                for (int c = 0; c < nch; ++c, ++u) {
+                    const int s = u % AT_STAGES;
+                    if (*abort || (u >= AT_STAGES && !tc::mbar_wait(&em[s], ((u / AT_STAGES) - 1) & 1, abort, a.ws, 93))) {
+                        go = false;
+                        break;
+                    }
+                    uint8_t* st = sm + (grp * AT_STAGES + s) * S::STAGE;
+                    const int t0 = c * CHUNK;
+                    tc::mbar_arrive_expect_tx(&kf[s], S::KV_BYTES + (c == 0 ? REP * HD * 2 : 0));
 #pragma unroll
-        for (int j = 0; j < KS; ++j)
+                    for (int h = 0; h < HD / 64; ++h)
+                        tc::tma_load_5d(st + h * (CHUNK * 128), &a.kmap, 64 * h, t0, g, s_seq[m], a.layer, &kf[s]);
+                    if (c == 0)
+                        bulk_load(st + 2 * S::KV_BYTES, a.qbuf + static_cast<int64_t>(m) * a.qw + g * REP * HD,
+                                  REP * HD * 2, &kf[s]);
+                    tc::mbar_arrive_expect_tx(&vf[s], S::KV_BYTES);
 #pragma unroll
-            for (int i = 0; i < MT; ++i) {
-                const int row = pw + 16 * i + ((mi >> 1) << 3) + rr;   // a0 / a2: positions 0-7 / 8-15 of the tile
-                uint32_t fa[4];
-                ldsm4_t(vbase + sw_off<CHUNK>(row, 2 * j + (mi & 1)), fa);
-                mma16816(o[j], fa, pb[i][0], pb[i][1]);
-            }
-        // O^T fragments: rows = columns 16 j + g (+ 8), columns = heads 2t, 2t + 1
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int h = 2 * lt + e;
-            if (h < REP)
-#pragma unroll
-                for (int j = 0; j < KS; ++j) {
-                    s_red[warp][h][16 * j + lg] = o[j][e];
-                    s_red[warp][h][16 * j + lg + 8] = o[j][2 + e];
+                    for (int h = 0; h < HD / 64; ++h)
+                        tc::tma_load_5d(st + S::KV_BYTES + h * (CHUNK * 128), &a.vmap, 64 * h, t0, g, s_seq[m],
+                                        a.layer, &vf[s]);
                 }
-        }
-        if (lg == 0) {
-            s_mw[warp][2 * lt] = mh[0];
-            s_mw[warp][2 * lt + 1] = mh[1];
-            s_lw[warp][2 * lt] = lh[0];
-            s_lw[warp][2 * lt + 1] = lh[1];
-        }
-    }
-    if (!ok) *abort = 1;
-    __syncthreads();
-    if (*abort) return;
-    const int nwa = min(NW, (cnt + WP - 1) / WP);   // warps that saw positions
-    if (tid < REP) {
-        float M = -INFINITY;
-        for (int w = 0; w < nwa; ++w) M = fmaxf(M, s_mw[w][tid]);
-        float L = 0.f;
-        for (int w = 0; w < nwa; ++w) {
-            const float wt = exp2f(s_mw[w][tid] - M);
-            s_ww[tid][w] = wt;
-            L = fmaf(s_lw[w][tid], wt, L);
-        }
-        s_m[tid] = M;
-        s_sum[tid] = L;
-    }
-    __syncthreads();
-    if (nch == 1) {   // the whole range in this CTA: normalise and store
-        for (int i = tid; i < REP * HD; i += AT_THREADS) {
-            const int r = i / HD, e = i % HD;
-            float v = 0.f;
-            for (int w = 0; w < nwa; ++w) v = fmaf(s_red[w][r][e], s_ww[r][w], v);
-            out[i] = __float2bfloat16_rn(v / s_sum[r]);
+            }
+            // leave no copy in flight: wait (bounded, whether or not the block has
+            // given up) for the last chunks issued to land
+            const uint64_t t0 = tc::globaltimer();
+            for (int j = u > AT_STAGES ? u - AT_STAGES : 0; j < u; ++j) {
+                const uint32_t ph = (j / AT_STAGES) & 1;
+                while (!(tc::mbar_test_wait(&kf[j % AT_STAGES], ph) && tc::mbar_test_wait(&vf[j % AT_STAGES], ph)) &&
+                       tc::globaltimer() - t0 < 200000000ull) {
+                }
+            }
         }
         return;
     }
-    float* pp = a.part + ((static_cast<int64_t>(m) * a.n_kv + g) * a.chunks + c) * (REP * (HD + 2));
-    for (int i = tid; i < REP * HD; i += AT_THREADS) {
-        const int r = i / HD, e = i % HD;
-        float v = 0.f;
-        for (int w = 0; w < nwa; ++w) v = fmaf(s_red[w][r][e], s_ww[r][w], v);
-        pp[r * (HD + 2) + e] = v;
-    }
-    if (tid < REP) {
-        pp[tid * (HD + 2) + HD] = s_m[tid];
-        pp[tid * (HD + 2) + HD + 1] = s_sum[tid];
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        int32_t* ctr = a.cnt + m * a.n_kv + g;
-        const int prev = atomicAdd(ctr, 1);
-        s_last = prev == nch - 1;
-        if (s_last) *ctr = 0;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    // merge the chunks: O = sum_c o_c 2^(m_c - M) / sum_c l_c 2^(m_c - M). The
-    // chunks' (m_c, l_c) go to shared memory first (one load per thread; the V
-    // buffer is free by now), then a column's o_c are loaded 16 at a time.
-    const int nc = a.chunks;
-    const float* p0 = a.part + (static_cast<int64_t>(m) * a.n_kv + g) * nc * (REP * (HD + 2));
-    float* s_ml = reinterpret_cast<float*>(s_v);   // [REP][nc][2] (the V chunk is no longer needed)
-    float* s_w = s_ml + 2 * REP * nc;              // [REP][nc]: 2^(m_c - M) / L
-    for (int i = tid; i < REP * nch; i += AT_THREADS) {
-        const int r = i / nch, cc = i % nch;
-        const float* q = p0 + cc * (REP * (HD + 2)) + r * (HD + 2) + HD;
-        s_ml[(r * nc + cc) * 2] = __ldcg(q);
-        s_ml[(r * nc + cc) * 2 + 1] = __ldcg(q + 1);
-    }
-    __syncthreads();
-    if (tid < REP) {
-        float M = -INFINITY;
-        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, s_ml[(tid * nc + cc) * 2]);
-        float L = 0.f;
-        for (int cc = 0; cc < nch; ++cc) {
-            const float w = exp2f(s_ml[(tid * nc + cc) * 2] - M);
-            s_w[tid * nc + cc] = w;
-            L = fmaf(s_ml[(tid * nc + cc) * 2 + 1], w, L);
-        }
-        for (int cc = 0; cc < nch; ++cc) s_w[tid * nc + cc] /= L;
-    }
-    __syncthreads();
-    for (int i = tid; i < REP * HD; i += AT_THREADS) {
-        const int r = i / HD, e = i % HD;
-        float O = 0.f;
-        for (int c0 = 0; c0 < nch; c0 += 16) {
-            float v[16];
+
+    // ---- consumer group grp: the chunks of its pairs, in the producer's order
+    const int grp = warp / NW, gt = tid - grp * AT_GT, gw = gt >> 5;
+    const int gg = static_cast<int>(blockIdx.x) * AT_GROUPS + grp;
+    const int lg = lane >> 2, lt = lane & 3;    // fragment row group and column pair
+    const int rr = lane & 7, mi = lane >> 3;    // lane l addresses row l % 8 of matrix l / 8 of an ldmatrix
+    const int pw = gw * WP;                     // the warp's first position in a chunk
+    const float qs = a.qscale;
+    uint64_t* kf = kfull + grp * AT_STAGES;
+    uint64_t* vf = vfull + grp * AT_STAGES;
+    uint64_t* em = empty + grp * AT_STAGES;
+    int u = 0;
+    bool go = true;
+    for (int k = 0; go; ++k) {
+        const int p = snake_pair(k, gg, G, pairs);
+        if (p < 0) break;
+        const int m = s_order[p / a.n_kv], g = p % a.n_kv;
+        const int pm = s_pos[m], nch = pm / CHUNK + 1;
+        // this warp's running softmax over the pair's chunks (log2 domain): maximum
+        // and this lane's share of the sum per query head 2t, 2t + 1, and O^T
+        float mh[2] = {-INFINITY, -INFINITY}, lh[2] = {0.f, 0.f};
+        float o[KS][4];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (c0 + j < nch) v[j] = __ldcg(p0 + (c0 + j) * (REP * (HD + 2)) + r * (HD + 2) + e);
+        for (int jj = 0; jj < KS; ++jj) o[jj][0] = o[jj][1] = o[jj][2] = o[jj][3] = 0.f;
+        uint32_t qb[KS][2];
+        for (int c = 0; c < nch; ++c, ++u) {
+            const int s = u % AT_STAGES;
+            const uint32_t ph = (u / AT_STAGES) & 1;
+            if (!group_all(grp, tc::mbar_wait(&kf[s], ph, abort, a.ws, 95))) {
+                go = false;
+                break;
+            }
+            uint8_t* st = sm + (grp * AT_STAGES + s) * S::STAGE;
+            uint8_t* s_v = st + S::KV_BYTES;
+            if (c == 0) {   // Q^T fragments (heads past REP are zero), unscaled bf16
+                const uint8_t* qrow = st + 2 * S::KV_BYTES + lg * HD * 2;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (c0 + j < nch) O = fmaf(v[j], s_w[r * nc + c0 + j], O);
+                for (int kk = 0; kk < KS; ++kk) {
+                    qb[kk][0] = lg < REP ? *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 2 * lt) * 2) : 0u;
+                    qb[kk][1] = lg < REP ? *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 2 * lt + 8) * 2) : 0u;
+                }
+            }
+            const int cnt = min(CHUNK, pm + 1 - c * CHUNK);
+            uint32_t pb[MT][2];
+            if (pw < cnt) {
+                float sc[MT][4];
+                const uint32_t kbase = tc::smem_u32(st);
+#pragma unroll
+                for (int i = 0; i < MT; ++i) {
+                    sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+                    const int row = pw + 16 * i + ((mi & 1) << 3) + rr;   // a0 / a1: rows g, g + 8; a2 / a3: columns + 8
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        uint32_t fa[4];
+                        ldsm4(kbase + sw_off<CHUNK>(row, 2 * kk + (mi >> 1)), fa);
+                        mma16816(sc[i], fa, qb[kk][0], qb[kk][1]);
+                    }
+                }
+                if (pw + WP > cnt) {   // the sequence ends inside this warp's positions
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        const int p0 = pw + 16 * i + lg;
+                        if (p0 >= cnt) sc[i][0] = sc[i][1] = -INFINITY;
+                        if (p0 + 8 >= cnt) sc[i][2] = sc[i][3] = -INFINITY;
+                    }
+                }
+                float cm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < MT; ++i) {
+                    cm[0] = fmaxf(cm[0], fmaxf(sc[i][0], sc[i][2]));
+                    cm[1] = fmaxf(cm[1], fmaxf(sc[i][1], sc[i][3]));
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                    for (int sh = 4; sh < 32; sh <<= 1) cm[e] = fmaxf(cm[e], __shfl_xor_sync(0xFFFFFFFFu, cm[e], sh));
+                    // to the log2 domain (s * log2(e) / sqrt(head_dim)); position pw is
+                    // valid, so the new maximum is finite; the old one may be -inf
+                    const float mn = fmaxf(mh[e], cm[e] * qs);
+                    const float f = exp2f(mh[e] - mn);
+                    lh[e] *= f;
+#pragma unroll
+                    for (int jj = 0; jj < KS; ++jj) {
+                        o[jj][e] *= f;
+                        o[jj][2 + e] *= f;
+                    }
+                    mh[e] = mn;
+                }
+#pragma unroll
+                for (int i = 0; i < MT; ++i) {
+                    const float p0 = exp2f(fmaf(sc[i][0], qs, -mh[0])), p1 = exp2f(fmaf(sc[i][1], qs, -mh[1]));
+                    const float p2 = exp2f(fmaf(sc[i][2], qs, -mh[0])), p3 = exp2f(fmaf(sc[i][3], qs, -mh[1]));
+                    lh[0] += p0 + p2;
+                    lh[1] += p1 + p3;
+                    pb[i][0] = movm_t(pack_bf16(p0, p1));   // P^T rows 2t, 2t + 1 of this tile, query head g
+                    pb[i][1] = movm_t(pack_bf16(p2, p3));
+                }
+            }
+            const bool vok = __all_sync(0xFFFFFFFFu, tc::mbar_wait(&vf[s], ph, abort, a.ws, 96));
+            if (pw < cnt && vok) {
+                if (pw + WP > cnt) {
+                    // rows past the sequence hold whatever the cache slots hold (maybe
+                    // not finite): zero them, since their weight 0 times a NaN would not vanish
+                    constexpr int PR = (HD / 64) * 8;   // 16-byte pieces of a row
+                    const int r0 = cnt - pw;
+                    for (int idx = lane; idx < (WP - r0) * PR; idx += 32) {
+                        const int row = pw + r0 + idx / PR, pc = idx % PR;
+                        *reinterpret_cast<uint4*>(s_v + (pc >> 3) * (CHUNK * 128) + row * 128 + (pc & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_async_smem();   // before the next copies into this stage
+                    __syncwarp();
+                }
+                const uint32_t vbase = tc::smem_u32(s_v);
+#pragma unroll
+                for (int jj = 0; jj < KS; ++jj)
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        const int row = pw + 16 * i + ((mi >> 1) << 3) + rr;   // a0 / a2: positions 0-7 / 8-15 of the tile
+                        uint32_t fa[4];
+                        ldsm4_t(vbase + sw_off<CHUNK>(row, 2 * jj + (mi & 1)), fa);
+                        mma16816(o[jj], fa, pb[i][0], pb[i][1]);
+                    }
+            }
+            if (!group_all(grp, vok)) {   // every warp's reads of the stage are done
+                go = false;
+                break;
+            }
+            if (c == nch - 1) {
+                // the pair's last chunk: merge the four warps' results by their
+                // maxima, through this stage's V buffer
+                float (*red)[REP][HD] = reinterpret_cast<float (*)[REP][HD]>(s_v);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                    for (int sh = 4; sh < 32; sh <<= 1) lh[e] += __shfl_xor_sync(0xFFFFFFFFu, lh[e], sh);
+                    const int h = 2 * lt + e;
+                    if (h < REP)
+#pragma unroll
+                        for (int jj = 0; jj < KS; ++jj) {   // O^T rows = columns 16 jj + g (+ 8)
+                            red[gw][h][16 * jj + lg] = o[jj][e];
+                            red[gw][h][16 * jj + lg + 8] = o[jj][2 + e];
+                        }
+                }
+                if (lg == 0) {
+                    s_mw[grp][gw][2 * lt] = mh[0];
+                    s_mw[grp][gw][2 * lt + 1] = mh[1];
+                    s_lw[grp][gw][2 * lt] = lh[0];
+                    s_lw[grp][gw][2 * lt + 1] = lh[1];
+                }
+                fence_async_smem();   // before the next copies into this stage
+                group_sync(grp);
+                // warp 0 saw position 0, so M is finite; a warp that saw no position
+                // has maximum -inf, weight 0 and O = 0
+                bf16* out = a.obuf + static_cast<int64_t>(m) * a.qw + static_cast<int64_t>(g) * REP * HD;
+                for (int i = gt; i < REP * HD; i += AT_GT) {
+                    const int r = i / HD, e = i % HD;
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_mw[grp][w][r]);
+                    float v = 0.f, L = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) {
+                        const float wt = exp2f(s_mw[grp][w][r] - M);
+                        v = fmaf(red[w][r][e], wt, v);
+                        L = fmaf(s_lw[grp][w][r], wt, L);
+                    }
+                    out[i] = __float2bfloat16_rn(v / L);
+                }
+                group_sync(grp);   // the merge's reads are done
+            }
+            if (gt == 0) tc::mbar_arrive(&em[s]);
         }
-        out[i] = __float2bfloat16_rn(O);
     }
 }
 
 template <int HD, int REP>
-tee_status launch_attn_rep(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+tee_status launch_attn_rep(const AttnArgs& a, cudaStream_t s) {
     static bool attr = false;
     constexpr size_t bytes = AttnSmem<HD, REP>::BYTES;
     if (!attr) {
@@ -1039,8 +1103,11 @@ tee_status launch_attn_rep(const AttnArgs& a, dim3 grid, cudaStream_t s) {
         if (st != TEE_OK) return st;
         attr = true;
     }
+    const int64_t pairs = static_cast<int64_t>(a.n_max) * a.n_kv;
+    const int grid = static_cast<int>(std::min<int64_t>(pairs, sm_count()));
+    if (grid < 1) return TEE_OK;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = grid;
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(AT_THREADS);
     cfg.dynamicSmemBytes = bytes;
     cfg.stream = s;
@@ -1054,12 +1121,12 @@ tee_status launch_attn_rep(const AttnArgs& a, dim3 grid, cudaStream_t s) {
 }
 
 template <int HD>
-tee_status launch_attn(const AttnArgs& a, int rep, dim3 grid, cudaStream_t s) {
+tee_status launch_attn(const AttnArgs& a, int rep, cudaStream_t s) {
     switch (rep) {
-        case 1: return launch_attn_rep<HD, 1>(a, grid, s);
-        case 2: return launch_attn_rep<HD, 2>(a, grid, s);
-        case 4: return launch_attn_rep<HD, 4>(a, grid, s);
-        case 8: return launch_attn_rep<HD, 8>(a, grid, s);
+        case 1: return launch_attn_rep<HD, 1>(a, s);
+        case 2: return launch_attn_rep<HD, 2>(a, s);
+        case 4: return launch_attn_rep<HD, 4>(a, s);
+        case 8: return launch_attn_rep<HD, 8>(a, s);
         default: return TEE_ERR_UNSUPPORTED;
     }
 }
@@ -1278,7 +1345,7 @@ extern "C" tee_status tee_exit_river_prepare(const tee_river_desc* D, int32_t n_
 
 extern "C" size_t tee_exit_river_workspace_size(const tee_river_desc* D, int32_t n_max, int32_t max_pos) {
     if (check_desc(D) != TEE_OK || n_max < 0 || n_max > MAX_ITEMS || max_pos <= 0) return 0;
-    return river_ws(*D, n_max, max_pos).end;
+    return river_ws(*D, n_max).end;   // the cache length does not change it
 }
 
 extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, const tee_river_layer* layers,
@@ -1306,7 +1373,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     }
     const LayerPack lp = layer_pack(*D);
     if (!prep || !aligned16(prep) || prep_bytes < tee_exit_river_prep_size(D, n_layers, 1)) return TEE_ERR_WORKSPACE;
-    const RiverWs w = river_ws(*D, n_max, cl.max_pos);
+    const RiverWs w = river_ws(*D, n_max);
     if (!ws || ws_bytes < w.end) return TEE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const PrepHeader* hdr = static_cast<const PrepHeader*>(prep);
@@ -1344,12 +1411,12 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     ga.ipos = ipos;
     ga.iseq = iseq;
     ga.cnt = acnt;
-    ga.n_cnt = n_max * D->n_kv_heads + KG_CNT;
+    ga.n_cnt = KG_CNT;
     river_gather_kernel<<<n_max, 256, 0, s>>>(ga, ws);
     if ((st = launch_status()) != TEE_OK) return st;
 
     GemmArgs g{};
-    g.kg_cnt = acnt + static_cast<int64_t>(n_max) * D->n_kv_heads;   // cleared with the attention's
+    g.kg_cnt = acnt;   // cleared by the prologue
     g.n_max = n_max;
     g.n_dev = n_dev;
     g.eps = D->eps;
@@ -1375,21 +1442,15 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     at.n_dev = n_dev;
     at.n_kv = D->n_kv_heads;
     at.qw = qw;
-    at.chunks = (cl.max_pos + at_chunk(hd) - 1) / at_chunk(hd);
     at.qbuf = qbuf;
     at.ipos = ipos;
     at.iseq = iseq;
     if ((st = make_tmap_cache(&at.kmap, k_cache, hd, cl, at_box(hd))) != TEE_OK) return st;
     if ((st = make_tmap_cache(&at.vmap, v_cache, hd, cl, at_box(hd))) != TEE_OK) return st;
     at.qscale = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
-    at.part = ws_at<float>(ws, w.apart);
-    at.cnt = acnt;
     at.obuf = obuf;
     at.ws = ws;
     const int rep = D->n_q_heads / D->n_kv_heads;
-    // the merge keeps 3 floats per (q head of a group, chunk) in the 32 KB V buffer
-    if (static_cast<size_t>(at.chunks) * rep * 3 * 4 > static_cast<size_t>(at_chunk(hd)) * hd * 2)
-        return TEE_ERR_UNSUPPORTED;
 
     for (int l = 0; l < n_layers; ++l) {
         const tee_river_layer& L = layers[l];
@@ -1410,8 +1471,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         if ((st = launch_gemm<M_QKV>(g, ws, s)) != TEE_OK) return st;
         // attention
         at.layer = L.cache_layer;
-        const dim3 agrid(at.chunks, D->n_kv_heads, n_max);
-        st = hd == 64 ? launch_attn<64>(at, rep, agrid, s) : launch_attn<128>(at, rep, agrid, s);
+        st = hd == 64 ? launch_attn<64>(at, rep, s) : launch_attn<128>(at, rep, s);
         if (st != TEE_OK) return st;
         // h1 = h + o Wo
         g.blob = lbase + lp.o;
