@@ -474,8 +474,18 @@ typedef struct {
     float rope_base;      /* RoPE base (q and k) */
     float eps;            /* epsilon of both RMSNorms */
     int32_t group;        /* int4 group length: 64 */
-    int32_t flags;        /* 0 */
+    int32_t flags;        /* 0, or one of TEE_RIVER_ATTN_BY_PAIR / TEE_RIVER_ATTN_BY_CHUNK */
 } tee_river_desc;
+
+/* tee_river_desc.flags: how the attention walks the cache; same results within
+ * rounding. By default it walks whole (item, kv head) pairs, one persistent
+ * consumer group per pair with an online softmax over the pair's chunks, when
+ * n_max * n_kv_heads fills every group (two per SM), and otherwise splits each
+ * sequence into chunks of one CTA each whose partial results a merge combines
+ * (its workspace then holds the partials: it grows with max_pos). These force
+ * one walk; the workspace size follows the flag. */
+#define TEE_RIVER_ATTN_BY_PAIR 1
+#define TEE_RIVER_ATTN_BY_CHUNK 2
 
 /* One exit layer: the W4A16 copy of decoder layer `cache_layer` (device
  * pointers). qw = n_q_heads*head_dim, kvw = n_kv_heads*head_dim. */

@@ -153,6 +153,15 @@ def test_exit_river_checks_on_the_host(lib):
     odd = _lib.RiverDesc(d=2048, n_q_heads=30, n_kv_heads=8, head_dim=64, d_ff=8192, rope_base=5e5, eps=1e-5,
                          group=64, flags=0)
     assert lib.tee_exit_river_prep_size(ctypes.byref(odd), 8, 4096) == 0   # q heads not a multiple of kv heads
+    # the attention's walk: the split walk's workspace holds the chunks' partials
+    # (it grows with the cache), the pair walk's does not; other flags are refused
+    by = {f: _lib.RiverDesc(d=2048, n_q_heads=32, n_kv_heads=8, head_dim=64, d_ff=8192, rope_base=5e5, eps=1e-5,
+                            group=64, flags=f) for f in (_lib.TEE_RIVER_ATTN_BY_PAIR, _lib.TEE_RIVER_ATTN_BY_CHUNK, 3)}
+    ws = lambda f, n, p: lib.tee_exit_river_workspace_size(ctypes.byref(by[f]), n, p)
+    pair, chunk = _lib.TEE_RIVER_ATTN_BY_PAIR, _lib.TEE_RIVER_ATTN_BY_CHUNK
+    assert ws(pair, 64, 4096) == ws(pair, 64, 131072) > 0
+    assert ws(chunk, 64, 131072) > ws(chunk, 64, 4096) > ws(pair, 64, 4096)
+    assert ws(3, 64, 4096) == 0 and lib.tee_exit_river_prep_size(ctypes.byref(by[3]), 8, 4096) == 0
     layout = _lib.CacheLayout(s_layer=1 << 20, s_seq=1 << 14, s_head=4096 * 64, s_pos=64, n_layers=16, n_seq=64,
                               n_heads=8, max_pos=4096)
     fake = ctypes.c_void_p(16)

@@ -35,9 +35,15 @@ def check_h(gpu, ref, what="h"):
     assert mx <= lim and rel <= H_REL_L2, f"{what}: max-abs {mx:.3e} (bound {lim:.3e}), rel-L2 {rel:.3e}"
 
 
-def _make(tee, cfg, layers):
+def _make(tee, cfg, layers, walk="auto"):
     return tee.ExitRiver(layers, d=cfg.d, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
-                         d_ff=cfg.d_ff, rope_base=cfg.rope_base, eps=cfg.eps, max_pos=cfg.cache_len)
+                         d_ff=cfg.d_ff, rope_base=cfg.rope_base, eps=cfg.eps, max_pos=cfg.cache_len, attn=walk)
+
+
+# the attention's two walks of the cache: whole (item, kv head) pairs, one
+# persistent consumer group each (chunks of 128 / 64 positions at head_dim 64 /
+# 128), and chunks of 256 / 128 positions, one CTA each, with a split merge
+WALKS = ["pair", "chunk"]
 
 
 def _check(cfg, x, k0, v0, out, items, rows=None):
@@ -67,42 +73,46 @@ def _cfg(**kw):
     return dataclasses.replace(configs.TINY_RIVER, **kw)
 
 
+@pytest.mark.parametrize("walk", WALKS)
 @pytest.mark.parametrize("seed", [0, 1])
-def test_tiny_river(tee, seed):
+def test_tiny_river(tee, seed, walk):
     cfg = configs.TINY_RIVER
     x = gen.river_inputs(cfg, seed, DEV)
     k0, v0 = x["k_cache"].clone(), x["v_cache"].clone()
     ws = tee.Workspace(DEV)
-    out = _make(tee, cfg, x["layers"])(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"], ws=ws)
+    out = _make(tee, cfg, x["layers"], walk)(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"], ws=ws)
     torch.cuda.synchronize()
     assert ws.device_error() == (0, 0)
     _check(cfg, x, k0, v0, out, np.arange(cfg.batch))
 
 
+@pytest.mark.parametrize("walk", WALKS)
 @pytest.mark.parametrize("n_q,n_kv,hd", [(8, 8, 64), (8, 4, 64), (16, 2, 64), (4, 2, 128), (8, 1, 128), (2, 1, 128)])
-def test_head_layouts(tee, n_q, n_kv, hd):
+def test_head_layouts(tee, n_q, n_kv, hd, walk):
     cfg = _cfg(n_q_heads=n_q, n_kv_heads=n_kv, head_dim=hd, d=512, d_ff=320, cache_len=600, batch=5)
     x = gen.river_inputs(cfg, n_q + n_kv + hd, DEV)
     k0, v0 = x["k_cache"].clone(), x["v_cache"].clone()
-    out = _make(tee, cfg, x["layers"])(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"])
+    out = _make(tee, cfg, x["layers"], walk)(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"])
     _check(cfg, x, k0, v0, out, np.arange(cfg.batch))
 
 
-@pytest.mark.parametrize("positions", [[0, 1, 2], [255, 256, 257], [511, 512, 1023], [127, 128, 129]])
-def test_chunk_boundaries(tee, positions):
-    # the attention splits positions into chunks of 256 (head_dim 64) / 128 (128)
+@pytest.mark.parametrize("walk", WALKS)
+@pytest.mark.parametrize("positions", [[0, 1, 2], [63, 64, 65], [127, 128, 129], [255, 256, 257], [511, 512, 1023]])
+def test_chunk_boundaries(tee, positions, walk):
+    # chunk edges of both walks at head_dim 64 and 128: 64, 128, 256 positions
     for hd in (64, 128):
         cfg = _cfg(head_dim=hd, n_q_heads=512 // hd, n_kv_heads=256 // hd, d=256, cache_len=1024, batch=3,
                    river_layers=(1,))
         x = gen.river_inputs(cfg, hd + positions[0], DEV)
         x["pos"] = torch.tensor(positions, dtype=torch.int32, device=DEV)
         k0, v0 = x["k_cache"].clone(), x["v_cache"].clone()
-        out = _make(tee, cfg, x["layers"])(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"])
+        out = _make(tee, cfg, x["layers"], walk)(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"])
         _check(cfg, x, k0, v0, out, np.arange(3))
 
 
+@pytest.mark.parametrize("walk", WALKS)
 @pytest.mark.parametrize("n", [1, 7, 64, 100, 128])
-def test_item_counts_rows_and_device_count(tee, n):
+def test_item_counts_rows_and_device_count(tee, n, walk):
     cfg = _cfg(batch=n, cache_len=300)
     x = gen.river_inputs(cfg, n, DEV)
     k0, v0 = x["k_cache"].clone(), x["v_cache"].clone()
@@ -111,55 +121,61 @@ def test_item_counts_rows_and_device_count(tee, n):
     n_use = max(1, n - 3)
     n_dev = torch.tensor([n_use], dtype=torch.int32, device=DEV)
     out = torch.full((n, cfg.d), 3.0, dtype=torch.bfloat16, device=DEV)
-    _make(tee, cfg, x["layers"])(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"],
-                                 rows=torch.from_numpy(rows).to(DEV), n_dev=n_dev, out=out)
+    _make(tee, cfg, x["layers"], walk)(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"],
+                                       rows=torch.from_numpy(rows).to(DEV), n_dev=n_dev, out=out)
     _check(cfg, x, k0, v0, out, np.arange(n_use), rows[:n_use])
     assert bool((out[n_use:] == 3.0).all())
 
 
-def test_bad_position_is_recorded_and_skipped(tee):
+@pytest.mark.parametrize("walk", WALKS)
+def test_bad_position_is_recorded_and_skipped(tee, walk):
     cfg = configs.TINY_RIVER
     x = gen.river_inputs(cfg, 5, DEV)
     x["pos"][4] = cfg.cache_len
     k0, v0 = x["k_cache"].clone(), x["v_cache"].clone()
     out = torch.full((cfg.batch, cfg.d), 3.0, dtype=torch.bfloat16, device=DEV)
     ws = tee.Workspace(DEV)
-    _make(tee, cfg, x["layers"])(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"], out=out, ws=ws)
+    _make(tee, cfg, x["layers"], walk)(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"], out=out, ws=ws)
     assert ws.device_error() == (2, cfg.cache_len)
     good = np.array([i for i in range(cfg.batch) if i != 4])
     _check(cfg, x, k0, v0, out, good)
     assert bool((out[4] == 3.0).all())
 
 
-def test_empty_call_is_a_no_op(tee):
+@pytest.mark.parametrize("walk", WALKS)
+def test_empty_call_is_a_no_op(tee, walk):
     cfg = configs.TINY_RIVER
     x = gen.river_inputs(cfg, 6, DEV)
     k0 = x["k_cache"].clone()
     n_dev = torch.zeros(1, dtype=torch.int32, device=DEV)
     out = torch.full((cfg.batch, cfg.d), 3.0, dtype=torch.bfloat16, device=DEV)
-    _make(tee, cfg, x["layers"])(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"], n_dev=n_dev, out=out)
+    _make(tee, cfg, x["layers"], walk)(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"], n_dev=n_dev,
+                                       out=out)
     torch.cuda.synchronize()
     assert torch.equal(x["k_cache"], k0) and bool((out == 3.0).all())
 
 
-def test_twice_reuses_the_workspace(tee):
+@pytest.mark.parametrize("walk", WALKS)
+def test_twice_reuses_the_workspace(tee, walk):
     cfg = configs.TINY_RIVER
     ws = tee.Workspace(DEV)
     for seed in (7, 8):
         x = gen.river_inputs(cfg, seed, DEV)
         k0, v0 = x["k_cache"].clone(), x["v_cache"].clone()
-        out = _make(tee, cfg, x["layers"])(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"], ws=ws)
+        out = _make(tee, cfg, x["layers"], walk)(x["h"], x["k_cache"], x["v_cache"], x["pos"], seq=x["seq"], ws=ws)
         _check(cfg, x, k0, v0, out, np.arange(cfg.batch))
     assert ws.device_error() == (0, 0)
 
 
-def test_llama1b_river_sampled_items(tee):
+@pytest.mark.parametrize("walk", ["auto", "chunk"])
+def test_llama1b_river_sampled_items(tee, walk):
     # the full workload (64 items, 8 exit layers, 4096 positions) in the launch
-    # configuration the benchmark times; the oracle runs 3 sampled items, whose
-    # sequences it reads (the items' sequences are distinct, so they do not interact)
+    # configuration the benchmark times ("auto": the pair walk, 512 pairs), and on
+    # the chunk walk; the oracle runs 3 sampled items, whose sequences it reads
+    # (the items' sequences are distinct, so they do not interact)
     cfg = configs.LLAMA1B_RIVER
     x = gen.river_inputs(cfg, 0, DEV)
-    f = _make(tee, cfg, x["layers"])
+    f = _make(tee, cfg, x["layers"], walk)
     ws = tee.Workspace(DEV)
     items = np.array([0, 31, 63])
     pos = x["pos"].cpu().numpy()

@@ -28,6 +28,8 @@ class GateDesc(ctypes.Structure):
 
 TEE_FILL_EARLY_WEIGHTS = 1
 TEE_FILL_GENERIC = 2
+TEE_RIVER_ATTN_BY_PAIR = 1
+TEE_RIVER_ATTN_BY_CHUNK = 2
 TEE_FILL_WRITE_K = 1
 TEE_FILL_WRITE_V = 2
 

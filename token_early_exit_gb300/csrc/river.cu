@@ -45,7 +45,8 @@ constexpr uint32_t RIVER_MAGIC = 0x54455256u;  // "TERV"
 
 // ------------------------------------------------------------------ workspace
 struct RiverWs {
-    size_t resid, abuf, qbuf, obuf, act, ss_a, ss_f, ipos, iseq, acnt, end;
+    size_t resid, abuf, qbuf, obuf, act, ss_a, ss_f, ipos, iseq, acnt, apart, end;
+    bool by_pair;   // the attention walks whole (item, kv head) pairs (else chunks, with partials)
 };
 
 constexpr int GT_N = 128;        // output columns per GEMM tile
@@ -92,6 +93,11 @@ constexpr int MAX_KS = 8;        // K splits = CTAs of a cluster (portable size)
 constexpr int MAX_ITEMS = 128;
 
 constexpr int KG_CNT = 64 * 8;   // counters of the two-cluster K split: tiles (<= 64) x ks (<= 8)
+// Attention chunks, one TMA box per 64 columns of K and of V (the last chunk of a
+// sequence reads up to a chunk's rows less one that it does not use): 16 KB of K
+// for the pair kernel, 32 KB for the split kernel.
+__host__ __device__ constexpr int at_pair_box(int hd) { return 8192 / hd; }
+__host__ __device__ constexpr int at_split_box(int hd) { return 16384 / hd; }
 
 int max_clusters(int ks);
 
@@ -119,9 +125,20 @@ int choose_kg(int tiles, int ks, int K) {
                : 1;
 }
 
-RiverWs river_ws(const tee_river_desc& D, int n_max) {
+// The pair kernel's consumer groups (two per SM) want a pair each at least.
+bool attn_by_pair(const tee_river_desc& D, int n_max) {
+    if (D.flags == TEE_RIVER_ATTN_BY_PAIR) return true;
+    if (D.flags == TEE_RIVER_ATTN_BY_CHUNK) return false;
+    return static_cast<int64_t>(n_max) * D.n_kv_heads >= static_cast<int64_t>(2) * sm_count();
+}
+int attn_chunks(const tee_river_desc& D, int max_pos) {
+    return (max_pos + at_split_box(D.head_dim) - 1) / at_split_box(D.head_dim);
+}
+
+RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
     const size_t n = static_cast<size_t>(n_max > 0 ? n_max : 1);
     const size_t d = D.d, qw = static_cast<size_t>(D.n_q_heads) * D.head_dim, f = D.d_ff;
+    const size_t rep = static_cast<size_t>(D.n_q_heads / std::max(1, D.n_kv_heads));
     RiverWs w{};
     size_t o = TEE_WS_HEADER_BYTES;
     auto take = [&](size_t bytes) {
@@ -139,7 +156,10 @@ RiverWs river_ws(const tee_river_desc& D, int n_max) {
     w.ss_f = take(n * 4);
     w.ipos = take(n * 4);
     w.iseq = take(n * 4);
-    w.acnt = take(KG_CNT * 4);   // the K groups' counters (tiles x ks)
+    w.by_pair = attn_by_pair(D, n_max);
+    // the K groups' counters (tiles x ks), then (split attention) the chunks' arrival counters
+    w.acnt = take((KG_CNT + (w.by_pair ? 0 : n * D.n_kv_heads)) * 4);
+    w.apart = w.by_pair ? 0 : take(n * D.n_kv_heads * attn_chunks(D, max_pos) * rep * (D.head_dim + 2) * 4);
     w.end = o;
     return w;
 }
@@ -164,7 +184,7 @@ struct GatherArgs {
     float* ss_f;
     int32_t* ipos;
     int32_t* iseq;
-    int32_t* cnt;   // the K-split GEMMs' arrival counters
+    int32_t* cnt;   // the arrival counters (K-split GEMMs, split attention)
     int n_cnt;
 };
 
@@ -698,6 +718,10 @@ struct AttnArgs {
     float qscale;          // log2(e) / sqrt(head_dim)
     bf16* obuf;            // [n][qw]
     void* ws;
+    // the split-chunk kernel only
+    int chunks;
+    float* part;           // [n][n_kv][chunks][REP][HD + 2]
+    int32_t* cnt;          // [n][n_kv]
 };
 
 // The attention is persistent: one CTA per SM, two consumer groups of four
@@ -718,17 +742,14 @@ struct AttnArgs {
 constexpr int AT_GROUPS = 2;                              // consumer groups
 constexpr int AT_GT = 128;                                // threads of a group
 constexpr int AT_PROD_WARP = AT_GROUPS * AT_GT / 32;      // warps 8 + g issue group g's copies
-constexpr int AT_THREADS = (AT_PROD_WARP + AT_GROUPS) * 32;
+constexpr int AP_THREADS = (AT_PROD_WARP + AT_GROUPS) * 32;
 constexpr int AT_STAGES = 3;
 constexpr int AT_MAX_ITEMS = 128;
-// positions per chunk: 16 KB of K (one TMA box per 64 columns; the last chunk of
-// a sequence reads up to CHUNK - 1 rows it does not use)
-__host__ __device__ constexpr int at_box(int hd) { return 8192 / hd; }
 
 template <int HD, int REP>
-struct AttnSmem {
+struct AttnPairSmem {
     static constexpr int NW = AT_GT / 32;            // warps of a group
-    static constexpr int CHUNK = at_box(HD);         // positions per chunk
+    static constexpr int CHUNK = at_pair_box(HD);    // positions per chunk
     static constexpr int WP = CHUNK / NW;            // positions per warp
     static constexpr int MT = WP / 16;               // 16-position tiles per warp
     static constexpr int KS = HD / 16;               // 16-column steps of a row
@@ -813,8 +834,8 @@ __device__ __forceinline__ int snake_pair(int k, int gg, int G, int pairs) {
 }
 
 template <int HD, int REP>
-__global__ void __launch_bounds__(AT_THREADS, 1) river_attn_kernel(const __grid_constant__ AttnArgs a) {
-    using S = AttnSmem<HD, REP>;
+__global__ void __launch_bounds__(AP_THREADS, 1) river_attn_pair_kernel(const __grid_constant__ AttnArgs a) {
+    using S = AttnPairSmem<HD, REP>;
     constexpr int NW = S::NW, CHUNK = S::CHUNK, WP = S::WP, MT = S::MT, KS = S::KS;
     extern __shared__ uint8_t at_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
@@ -841,7 +862,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) river_attn_kernel(const __grid_
     }
     wait_prior_grid();   // q, the item table and the cache slots come from the q|k|v GEMM
     const int n = item_count(a.n_max, a.n_dev);
-    for (int m = tid; m < n; m += AT_THREADS) {
+    for (int m = tid; m < n; m += AP_THREADS) {
         s_pos[m] = a.ipos[m];
         s_seq[m] = a.iseq[m];
     }
@@ -849,7 +870,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) river_attn_kernel(const __grid_
     // rank the items by chunk count, longest first (ties by index; skipped items last)
     if (tid == 0) s_valid = 0;
     __syncthreads();
-    for (int m = tid; m < n; m += AT_THREADS) {
+    for (int m = tid; m < n; m += AP_THREADS) {
         const int km = s_pos[m] >= 0 ? s_pos[m] / CHUNK + 1 : 0;
         int r = 0;
         for (int j = 0; j < n; ++j) {
@@ -862,8 +883,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1) river_attn_kernel(const __grid_
     __syncthreads();
     const int pairs = s_valid * a.n_kv;
     // a skipped item (position < 0) attends to nothing: its output rows are zero
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * AT_THREADS + tid; i < static_cast<int64_t>(n) * a.qw;
-         i += static_cast<int64_t>(gridDim.x) * AT_THREADS) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * AP_THREADS + tid; i < static_cast<int64_t>(n) * a.qw;
+         i += static_cast<int64_t>(gridDim.x) * AP_THREADS) {
         const int m = static_cast<int>(i / a.qw);
         if (s_pos[m] < 0) a.obuf[i] = __float2bfloat16_rn(0.f);
     }
@@ -1093,11 +1114,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1) river_attn_kernel(const __grid_
 }
 
 template <int HD, int REP>
-tee_status launch_attn_rep(const AttnArgs& a, cudaStream_t s) {
+tee_status launch_attn_pair(const AttnArgs& a, cudaStream_t s) {
     static bool attr = false;
-    constexpr size_t bytes = AttnSmem<HD, REP>::BYTES;
+    constexpr size_t bytes = AttnPairSmem<HD, REP>::BYTES;
     if (!attr) {
-        tee_status st = cuda_status(cudaFuncSetAttribute(river_attn_kernel<HD, REP>,
+        tee_status st = cuda_status(cudaFuncSetAttribute(river_attn_pair_kernel<HD, REP>,
                                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                          static_cast<int>(bytes)));
         if (st != TEE_OK) return st;
@@ -1108,7 +1129,7 @@ tee_status launch_attn_rep(const AttnArgs& a, cudaStream_t s) {
     if (grid < 1) return TEE_OK;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(AT_THREADS);
+    cfg.blockDim = dim3(AP_THREADS);
     cfg.dynamicSmemBytes = bytes;
     cfg.stream = s;
     cudaLaunchAttribute at[1];
@@ -1116,17 +1137,330 @@ tee_status launch_attn_rep(const AttnArgs& a, cudaStream_t s) {
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, river_attn_kernel<HD, REP>, a));
+    tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, river_attn_pair_kernel<HD, REP>, a));
     return st != TEE_OK ? st : launch_status();
 }
 
+// The split-chunk attention, for calls with fewer (item, kv head) pairs than
+// the pair kernel has consumer groups (a pair walked by one group would leave
+// most SMs idle): one CTA of four warps per (chunk of 256 / 128 positions, kv
+// head, item), the same warp-level products as above on one chunk; a sequence
+// of one chunk stores its output, otherwise the chunks' partials (o, m, l) go
+// to the workspace and the last chunk to finish (a counter) merges them.
+constexpr int AS_THREADS = 128;
+
+template <int HD, int REP>
+struct AttnSplitSmem {
+    static constexpr int NW = AS_THREADS / 32;
+    static constexpr int CHUNK = at_split_box(HD);   // positions per CTA
+    static constexpr int WP = CHUNK / NW;            // positions per warp
+    static constexpr int MT = WP / 16;               // 16-position tiles per warp
+    static constexpr int KS = HD / 16;               // 16-column steps of a row
+    static constexpr uint32_t KV_BYTES = CHUNK * HD * 2;   // 32 KB: halves of 64 columns, rows of 128 bytes
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+    static constexpr uint32_t OFF_RED = OFF_V + KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_RED + NW * REP * HD * 4;
+    static constexpr size_t BYTES = 1024 + OFF_BAR + 64;
+    static_assert(REP <= 8 && MT >= 1 && WP % 16 == 0, "attention tiling");
+};
+
+// One (chunk, kv head, item): TMA brings the chunk's K and V (swizzled) into
+// shared memory. Each warp takes WP positions: scores S^T = K Q^T (M = 16
+// positions, N = the kv head's query heads padded to 8, K = 16 columns of the
+// head) and O^T += V^T P^T (M = 16 columns, N = the heads, K = 16 positions) as
+// warp-level tensor-core products from registers; P^T comes from the score
+// accumulators by an in-register transpose. The softmax of a warp's positions is
+// taken on the accumulators; the warps' partial results are then merged by
+// their maxima, and the last chunk of an (item, kv head) to finish merges the
+// chunks' partials.
+template <int HD, int REP>
+__global__ void __launch_bounds__(AS_THREADS) river_attn_split_kernel(const __grid_constant__ AttnArgs a) {
+    using S = AttnSplitSmem<HD, REP>;
+    constexpr int NW = S::NW, CHUNK = S::CHUNK, WP = S::WP, MT = S::MT, KS = S::KS;
+    extern __shared__ uint8_t at_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* s_v = sm + S::OFF_V;
+    float (*s_red)[REP][HD] = reinterpret_cast<float (*)[REP][HD]>(sm + S::OFF_RED);
+    uint64_t* kbar = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);
+    uint64_t* vbar = kbar + 1;
+    volatile int* abort = reinterpret_cast<volatile int*>(vbar + 1);
+    __shared__ float s_mw[NW][8], s_lw[NW][8], s_ww[REP][NW];
+    __shared__ float s_m[REP], s_sum[REP];
+    __shared__ int s_last;
+
+    const int c = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lg = lane >> 2, lt = lane & 3;   // fragment row group and column pair
+    allow_dependents();
+    const int n = item_count(a.n_max, a.n_dev);
+    if (m >= n) return;
+    wait_prior_grid();   // q, the item table and the cache slots come from the q|k|v GEMM
+    const int pm = a.ipos[m];
+    bf16* out = a.obuf + static_cast<int64_t>(m) * a.qw + static_cast<int64_t>(g) * REP * HD;
+    if (pm < 0) {   // a skipped item attends to nothing
+        if (c == 0)
+            for (int i = tid; i < REP * HD; i += AS_THREADS) out[i] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const int nch = pm / CHUNK + 1;
+    if (c >= nch) return;
+    const int t0 = c * CHUNK, cnt = min(CHUNK, pm + 1 - t0);
+    if (tid == 0) {
+        tc::mbar_init(kbar, 1);
+        tc::mbar_init(vbar, 1);
+        *abort = 0;
+        tc::fence_barrier_init();
+        const uint32_t bytes = (HD / 64) * CHUNK * 128;
+        const int sq = a.iseq[m];
+        tc::mbar_arrive_expect_tx(kbar, bytes);
+        for (int h = 0; h < HD / 64; ++h)
+            tc::tma_load_5d(sm + S::OFF_K + h * (CHUNK * 128), &a.kmap, 64 * h, t0, g, sq, a.layer, kbar);
+        tc::mbar_arrive_expect_tx(vbar, bytes);
+        for (int h = 0; h < HD / 64; ++h)
+            tc::tma_load_5d(s_v + h * (CHUNK * 128), &a.vmap, 64 * h, t0, g, sq, a.layer, vbar);
+    }
+    // Q^T fragments (columns 2t, 2t + 1 and 2t + 8, 2t + 9 of query head g; heads
+    // past REP are zero), unscaled bf16: the softmax scale multiplies the fp32 scores
+    uint32_t qb[KS][2];
+    {
+        const bf16* qrow = a.qbuf + static_cast<int64_t>(m) * a.qw + (static_cast<int64_t>(g) * REP + lg) * HD;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            qb[kk][0] = lg < REP ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * lt) : 0u;
+            qb[kk][1] = lg < REP ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * lt + 8) : 0u;
+        }
+    }
+    __syncthreads();   // the barriers' initialisation
+    const int pw = warp * WP;   // the warp's first position in the chunk
+    const float qs = a.qscale;
+    // lane l addresses row (l % 8) of matrix l / 8 of each ldmatrix; rows are 16-position tiles' rows
+    const int rr = lane & 7, mi = lane >> 3;
+    bool ok = tc::mbar_wait(kbar, 0, abort, a.ws, 91);
+    float mh[2] = {-INFINITY, -INFINITY}, lh[2] = {0.f, 0.f};   // heads 2t and 2t + 1
+    float o[KS][4];
+#pragma unroll
+    for (int j = 0; j < KS; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    uint32_t pb[MT][2];
+    if (pw < cnt) {
+        float s[MT][4];
+        const uint32_t kbase = tc::smem_u32(sm + S::OFF_K);
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+            const int row = pw + 16 * i + ((mi & 1) << 3) + rr;   // a0 / a1: rows g, g + 8; a2 / a3: columns + 8
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t fa[4];
+                ldsm4(kbase + sw_off<CHUNK>(row, 2 * kk + (mi >> 1)), fa);
+                mma16816(s[i], fa, qb[kk][0], qb[kk][1]);
+            }
+        }
+        if (pw + WP > cnt) {   // the sequence ends inside this warp's positions
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                const int p0 = pw + 16 * i + lg;
+                if (p0 >= cnt) s[i][0] = s[i][1] = -INFINITY;
+                if (p0 + 8 >= cnt) s[i][2] = s[i][3] = -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            mh[0] = fmaxf(mh[0], fmaxf(s[i][0], s[i][2]));
+            mh[1] = fmaxf(mh[1], fmaxf(s[i][1], s[i][3]));
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) mh[e] = fmaxf(mh[e], __shfl_xor_sync(0xFFFFFFFFu, mh[e], sh));
+        // scores to the log2 domain: s * log2(e) / sqrt(head_dim); position pw is
+        // valid, so the maxima are finite
+        mh[0] *= qs;
+        mh[1] *= qs;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            const float p0 = exp2f(fmaf(s[i][0], qs, -mh[0])), p1 = exp2f(fmaf(s[i][1], qs, -mh[1]));
+            const float p2 = exp2f(fmaf(s[i][2], qs, -mh[0])), p3 = exp2f(fmaf(s[i][3], qs, -mh[1]));
+            lh[0] += p0 + p2;
+            lh[1] += p1 + p3;
+            pb[i][0] = movm_t(pack_bf16(p0, p1));   // P^T rows 2t, 2t + 1 of this tile, query head g
+            pb[i][1] = movm_t(pack_bf16(p2, p3));
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) lh[e] += __shfl_xor_sync(0xFFFFFFFFu, lh[e], sh);
+    }
+    ok = tc::mbar_wait(vbar, 0, abort, a.ws, 92) && ok;
+    ok = __all_sync(0xFFFFFFFFu, ok);   // the warp-wide instructions below run in whole warps only
+    if (pw < cnt && ok) {
+        if (pw + WP > cnt) {
+            // rows past the sequence hold whatever the cache slots hold (maybe not
+            // finite): zero them, since their weight 0 times a NaN would not vanish
+            constexpr int PR = (HD / 64) * 8;   // 16-byte pieces of a row
+            const int r0 = cnt - pw;
+            for (int idx = lane; idx < (WP - r0) * PR; idx += 32) {
+                const int row = pw + r0 + idx / PR, pc = idx % PR;
+                *reinterpret_cast<uint4*>(s_v + (pc >> 3) * (CHUNK * 128) + row * 128 + (pc & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+        const uint32_t vbase = tc::smem_u32(s_v);
+#pragma unroll
+        for (int j = 0; j < KS; ++j)
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                const int row = pw + 16 * i + ((mi >> 1) << 3) + rr;   // a0 / a2: positions 0-7 / 8-15 of the tile
+                uint32_t fa[4];
+                ldsm4_t(vbase + sw_off<CHUNK>(row, 2 * j + (mi & 1)), fa);
+                mma16816(o[j], fa, pb[i][0], pb[i][1]);
+            }
+        // O^T fragments: rows = columns 16 j + g (+ 8), columns = heads 2t, 2t + 1
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * lt + e;
+            if (h < REP)
+#pragma unroll
+                for (int j = 0; j < KS; ++j) {
+                    s_red[warp][h][16 * j + lg] = o[j][e];
+                    s_red[warp][h][16 * j + lg + 8] = o[j][2 + e];
+                }
+        }
+        if (lg == 0) {
+            s_mw[warp][2 * lt] = mh[0];
+            s_mw[warp][2 * lt + 1] = mh[1];
+            s_lw[warp][2 * lt] = lh[0];
+            s_lw[warp][2 * lt + 1] = lh[1];
+        }
+    }
+    if (!ok) *abort = 1;
+    __syncthreads();
+    if (*abort) return;
+    const int nwa = min(NW, (cnt + WP - 1) / WP);   // warps that saw positions
+    if (tid < REP) {
+        float M = -INFINITY;
+        for (int w = 0; w < nwa; ++w) M = fmaxf(M, s_mw[w][tid]);
+        float L = 0.f;
+        for (int w = 0; w < nwa; ++w) {
+            const float wt = exp2f(s_mw[w][tid] - M);
+            s_ww[tid][w] = wt;
+            L = fmaf(s_lw[w][tid], wt, L);
+        }
+        s_m[tid] = M;
+        s_sum[tid] = L;
+    }
+    __syncthreads();
+    if (nch == 1) {   // the whole range in this CTA: normalise and store
+        for (int i = tid; i < REP * HD; i += AS_THREADS) {
+            const int r = i / HD, e = i % HD;
+            float v = 0.f;
+            for (int w = 0; w < nwa; ++w) v = fmaf(s_red[w][r][e], s_ww[r][w], v);
+            out[i] = __float2bfloat16_rn(v / s_sum[r]);
+        }
+        return;
+    }
+    float* pp = a.part + ((static_cast<int64_t>(m) * a.n_kv + g) * a.chunks + c) * (REP * (HD + 2));
+    for (int i = tid; i < REP * HD; i += AS_THREADS) {
+        const int r = i / HD, e = i % HD;
+        float v = 0.f;
+        for (int w = 0; w < nwa; ++w) v = fmaf(s_red[w][r][e], s_ww[r][w], v);
+        pp[r * (HD + 2) + e] = v;
+    }
+    if (tid < REP) {
+        pp[tid * (HD + 2) + HD] = s_m[tid];
+        pp[tid * (HD + 2) + HD + 1] = s_sum[tid];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        int32_t* ctr = a.cnt + m * a.n_kv + g;
+        const int prev = atomicAdd(ctr, 1);
+        s_last = prev == nch - 1;
+        if (s_last) *ctr = 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // merge the chunks: O = sum_c o_c 2^(m_c - M) / sum_c l_c 2^(m_c - M). The
+    // chunks' (m_c, l_c) go to shared memory first (one load per thread; the V
+    // buffer is free by now), then a column's o_c are loaded 16 at a time.
+    const int nc = a.chunks;
+    const float* p0 = a.part + (static_cast<int64_t>(m) * a.n_kv + g) * nc * (REP * (HD + 2));
+    float* s_ml = reinterpret_cast<float*>(s_v);   // [REP][nc][2] (the V chunk is no longer needed)
+    float* s_w = s_ml + 2 * REP * nc;              // [REP][nc]: 2^(m_c - M) / L
+    for (int i = tid; i < REP * nch; i += AS_THREADS) {
+        const int r = i / nch, cc = i % nch;
+        const float* q = p0 + cc * (REP * (HD + 2)) + r * (HD + 2) + HD;
+        s_ml[(r * nc + cc) * 2] = __ldcg(q);
+        s_ml[(r * nc + cc) * 2 + 1] = __ldcg(q + 1);
+    }
+    __syncthreads();
+    if (tid < REP) {
+        float M = -INFINITY;
+        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, s_ml[(tid * nc + cc) * 2]);
+        float L = 0.f;
+        for (int cc = 0; cc < nch; ++cc) {
+            const float w = exp2f(s_ml[(tid * nc + cc) * 2] - M);
+            s_w[tid * nc + cc] = w;
+            L = fmaf(s_ml[(tid * nc + cc) * 2 + 1], w, L);
+        }
+        for (int cc = 0; cc < nch; ++cc) s_w[tid * nc + cc] /= L;
+    }
+    __syncthreads();
+    for (int i = tid; i < REP * HD; i += AS_THREADS) {
+        const int r = i / HD, e = i % HD;
+        float O = 0.f;
+        for (int c0 = 0; c0 < nch; c0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < nch) v[j] = __ldcg(p0 + (c0 + j) * (REP * (HD + 2)) + r * (HD + 2) + e);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < nch) O = fmaf(v[j], s_w[r * nc + c0 + j], O);
+        }
+        out[i] = __float2bfloat16_rn(O);
+    }
+}
+
+template <int HD, int REP>
+tee_status launch_attn_split(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+    static bool attr = false;
+    constexpr size_t bytes = AttnSplitSmem<HD, REP>::BYTES;
+    if (!attr) {
+        tee_status st = cuda_status(cudaFuncSetAttribute(river_attn_split_kernel<HD, REP>,
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         static_cast<int>(bytes)));
+        if (st != TEE_OK) return st;
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(AS_THREADS);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, river_attn_split_kernel<HD, REP>, a));
+    return st != TEE_OK ? st : launch_status();
+}
+
+template <int HD, int REP>
+tee_status launch_attn_rep(const AttnArgs& a, bool by_pair, cudaStream_t s) {
+    return by_pair ? launch_attn_pair<HD, REP>(a, s) : launch_attn_split<HD, REP>(a, dim3(a.chunks, a.n_kv, a.n_max), s);
+}
+
 template <int HD>
-tee_status launch_attn(const AttnArgs& a, int rep, cudaStream_t s) {
+tee_status launch_attn(const AttnArgs& a, int rep, bool by_pair, cudaStream_t s) {
     switch (rep) {
-        case 1: return launch_attn_rep<HD, 1>(a, s);
-        case 2: return launch_attn_rep<HD, 2>(a, s);
-        case 4: return launch_attn_rep<HD, 4>(a, s);
-        case 8: return launch_attn_rep<HD, 8>(a, s);
+        case 1: return launch_attn_rep<HD, 1>(a, by_pair, s);
+        case 2: return launch_attn_rep<HD, 2>(a, by_pair, s);
+        case 4: return launch_attn_rep<HD, 4>(a, by_pair, s);
+        case 8: return launch_attn_rep<HD, 8>(a, by_pair, s);
         default: return TEE_ERR_UNSUPPORTED;
     }
 }
@@ -1134,7 +1468,8 @@ tee_status launch_attn(const AttnArgs& a, int rep, cudaStream_t s) {
 // ------------------------------------------------------------------ host
 tee_status check_desc(const tee_river_desc* D) {
     if (!D) return TEE_ERR_INVALID_ARG;
-    if (D->d <= 0 || D->n_q_heads <= 0 || D->n_kv_heads <= 0 || D->d_ff <= 0 || D->flags != 0)
+    if (D->d <= 0 || D->n_q_heads <= 0 || D->n_kv_heads <= 0 || D->d_ff <= 0) return TEE_ERR_INVALID_ARG;
+    if (D->flags != 0 && D->flags != TEE_RIVER_ATTN_BY_PAIR && D->flags != TEE_RIVER_ATTN_BY_CHUNK)
         return TEE_ERR_INVALID_ARG;
     if (!(D->eps >= 0.f) || !(D->rope_base > 0.f)) return TEE_ERR_INVALID_ARG;
     if (D->head_dim != 64 && D->head_dim != 128) return TEE_ERR_UNSUPPORTED;
@@ -1345,7 +1680,7 @@ extern "C" tee_status tee_exit_river_prepare(const tee_river_desc* D, int32_t n_
 
 extern "C" size_t tee_exit_river_workspace_size(const tee_river_desc* D, int32_t n_max, int32_t max_pos) {
     if (check_desc(D) != TEE_OK || n_max < 0 || n_max > MAX_ITEMS || max_pos <= 0) return 0;
-    return river_ws(*D, n_max).end;   // the cache length does not change it
+    return river_ws(*D, n_max, max_pos).end;
 }
 
 extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, const tee_river_layer* layers,
@@ -1373,7 +1708,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     }
     const LayerPack lp = layer_pack(*D);
     if (!prep || !aligned16(prep) || prep_bytes < tee_exit_river_prep_size(D, n_layers, 1)) return TEE_ERR_WORKSPACE;
-    const RiverWs w = river_ws(*D, n_max);
+    const RiverWs w = river_ws(*D, n_max, cl.max_pos);
     if (!ws || ws_bytes < w.end) return TEE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const PrepHeader* hdr = static_cast<const PrepHeader*>(prep);
@@ -1411,7 +1746,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     ga.ipos = ipos;
     ga.iseq = iseq;
     ga.cnt = acnt;
-    ga.n_cnt = KG_CNT;
+    ga.n_cnt = KG_CNT + (w.by_pair ? 0 : n_max * D->n_kv_heads);
     river_gather_kernel<<<n_max, 256, 0, s>>>(ga, ws);
     if ((st = launch_status()) != TEE_OK) return st;
 
@@ -1445,12 +1780,21 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
     at.qbuf = qbuf;
     at.ipos = ipos;
     at.iseq = iseq;
-    if ((st = make_tmap_cache(&at.kmap, k_cache, hd, cl, at_box(hd))) != TEE_OK) return st;
-    if ((st = make_tmap_cache(&at.vmap, v_cache, hd, cl, at_box(hd))) != TEE_OK) return st;
+    const int box = w.by_pair ? at_pair_box(hd) : at_split_box(hd);
+    if ((st = make_tmap_cache(&at.kmap, k_cache, hd, cl, box)) != TEE_OK) return st;
+    if ((st = make_tmap_cache(&at.vmap, v_cache, hd, cl, box)) != TEE_OK) return st;
     at.qscale = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
     at.obuf = obuf;
     at.ws = ws;
     const int rep = D->n_q_heads / D->n_kv_heads;
+    if (!w.by_pair) {
+        at.chunks = attn_chunks(*D, cl.max_pos);
+        at.part = ws_at<float>(ws, w.apart);
+        at.cnt = acnt + KG_CNT;
+        // the split merge keeps 3 floats per (query head of a group, chunk) in the 32 KB V buffer
+        if (static_cast<size_t>(at.chunks) * rep * 3 * 4 > static_cast<size_t>(at_split_box(hd)) * hd * 2)
+            return TEE_ERR_UNSUPPORTED;
+    }
 
     for (int l = 0; l < n_layers; ++l) {
         const tee_river_layer& L = layers[l];
@@ -1471,7 +1815,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         if ((st = launch_gemm<M_QKV>(g, ws, s)) != TEE_OK) return st;
         // attention
         at.layer = L.cache_layer;
-        st = hd == 64 ? launch_attn<64>(at, rep, s) : launch_attn<128>(at, rep, s);
+        st = hd == 64 ? launch_attn<64>(at, rep, w.by_pair, s) : launch_attn<128>(at, rep, w.by_pair, s);
         if (st != TEE_OK) return st;
         // h1 = h + o Wo
         g.blob = lbase + lp.o;

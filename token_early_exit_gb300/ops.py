@@ -425,14 +425,17 @@ class ExitRiver:
     ``layers`` holds one dict per exit layer, in order: bf16 CUDA tensors
     ``attn_norm``, ``ffn_norm`` [d]; for each of q k v o g u d the packed int4
     codes ``w{m}`` [k_in/2][n_out] u8 and fp16 ``{m}_scale``, ``{m}_zero``
-    [k_in/64][n_out]; and the int ``cache_layer``.
+    [k_in/64][n_out]; and the int ``cache_layer``. ``attn`` forces the
+    attention's walk of the cache (``"pair"`` or ``"chunk"``, see
+    ``TEE_RIVER_ATTN_BY_PAIR``); ``"auto"`` picks it from the item count.
     """
 
     def __init__(self, layers: Sequence[Dict], *, d: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
-                 d_ff: int, rope_base: float, eps: float, max_pos: int, group: int = 64):
+                 d_ff: int, rope_base: float, eps: float, max_pos: int, group: int = 64, attn: str = "auto"):
         self.lib = load()
+        flags = {"auto": 0, "pair": _lib.TEE_RIVER_ATTN_BY_PAIR, "chunk": _lib.TEE_RIVER_ATTN_BY_CHUNK}[attn]
         self.desc = _lib.RiverDesc(d=d, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=head_dim, d_ff=d_ff,
-                                   rope_base=float(rope_base), eps=float(eps), group=group, flags=0)
+                                   rope_base=float(rope_base), eps=float(eps), group=group, flags=flags)
         self.keep: List[torch.Tensor] = []
         arr = (_lib.RiverLayer * max(1, len(layers)))()
 
