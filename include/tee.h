@@ -568,7 +568,9 @@ TEE_API tee_status tee_exit_river(const tee_river_desc* desc, int32_t n_layers, 
  * and copies the score, the mask, the counts and `out` back to host memory;
  * everything is enqueued on `stream` and the host results are valid once the
  * stream has completed. Host buffers should be page-locked for the copies to
- * run asynchronously. The results equal those of the two calls made on the
+ * run asynchronously; when every one is page-locked memory that the device
+ * reaches directly, two copy kernels move them (all inputs in one launch, all
+ * results in another) instead of one cudaMemcpyAsync per buffer. The results equal those of the two calls made on the
  * device buffers. The step object captures the sequence into a CUDA graph on a
  * stream of its own at the first call and replays it while n and the host
  * pointers stay the same (events order it after and before `stream`); with

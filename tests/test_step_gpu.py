@@ -148,3 +148,42 @@ def test_decode_step_from_host_buffers(tee, cfg, case, seed):
         assert torch.equal(score2, score) and torch.equal(mask2, mask) and torch.equal(counts2, counts)
         assert torch.equal(out2[rows.cpu()], out[rows.cpu()])
         assert torch.equal(x["k_cache"], k_dev) and torch.equal(x["v_cache"], v_dev)
+
+
+@pytest.mark.parametrize("cfg", [configs.TINY_DECODE, configs.LLAMA1B_DECODE])
+def test_decode_step_replays_read_the_rewritten_host_buffers(tee, cfg):
+    """A serving loop rewrites the same pinned host buffers every step and the
+    captured step is replayed on them: each replay must see that step's inputs
+    (the copies run in the replay, and nothing is served from a cache), equal to
+    the device calls on the same inputs."""
+    x = gen.decode_inputs(cfg, seed=11, device=DEV, case="default")
+    dt = x["h_cur"].dtype
+    mk = lambda: tee.KVFill(x["layers"], d=cfg.d, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,  # noqa: E731
+                            rope_base=cfg.rope_base, eps=cfg.eps, dtype=dt, max_pos=cfg.cache_len,
+                            int4=cfg.weights == "int4", group=cfg.group)
+    step = tee.DecodeStep(mk(), n_max=cfg.batch, d=cfg.d, threshold=cfg.tau, dtype=dt, rule=cfg.rule,
+                          k_cache=x["k_cache"], v_cache=x["v_cache"])
+    hi = {k: x[k].cpu().pin_memory() for k in ("h_prev", "h_cur", "pos", "seq")}
+    score = torch.empty(cfg.batch).pin_memory()
+    mask = torch.empty(cfg.batch, dtype=torch.uint8).pin_memory()
+    counts = torch.empty(2, dtype=torch.int32).pin_memory()
+    out = torch.empty(cfg.batch, cfg.d, dtype=dt).pin_memory()
+    fill, ws = mk(), tee.Workspace(DEV)
+    for seed in (11, 12, 13):
+        y = gen.decode_inputs(cfg, seed=seed, device=DEV, case="default")
+        for k in hi:   # this step's inputs, written in place into the same host buffers
+            hi[k].copy_(y[k].cpu())
+        k_dev, v_dev = x["k_cache"].clone(), x["v_cache"].clone()   # the caches before this step
+        out.fill_(-3.0)
+        step.run_host(hi["h_prev"], hi["h_cur"], hi["pos"], hi["seq"], score=score, mask=mask, counts=counts, out=out)
+        out_dev = torch.full_like(y["h_cur"], -3.0)
+        comp = tee.exit_gate_compact_scatter(y["h_cur"], y["h_prev"], cfg.tau, out_dev, rule=cfg.rule, ws=ws)
+        fill(y["h_cur"], k_dev, v_dev, rows=comp["exit_rows"], pos=y["pos"], seq=y["seq"], n_dev=comp["counts"][1:],
+             n_max=cfg.batch, ws=ws)
+        torch.cuda.synchronize()
+        assert step.ws.device_error() == (0, 0) and ws.device_error() == (0, 0)
+        assert torch.equal(score, comp["score"].cpu()) and torch.equal(mask, comp["mask"].cpu())
+        assert torch.equal(counts, comp["counts"].cpu())
+        rows = comp["exit_rows"][:int(counts[1])].long()
+        assert torch.equal(out[rows.cpu()], out_dev[rows].cpu())
+        assert torch.equal(x["k_cache"], k_dev) and torch.equal(x["v_cache"], v_dev)

@@ -7,6 +7,11 @@
 // host one graph launch; the caller's stream and the step's stream are ordered
 // by two events. Where capture is refused (pageable host memory, for one) the
 // sequence is enqueued directly on the caller's stream instead.
+// When every host buffer is page-locked memory that the device reaches directly
+// (mapped into its address space, as page-locked memory is under unified
+// addressing), one copy kernel reads all the inputs and another writes all the
+// results: two launches instead of eight copies, whose fixed costs would add up
+// on the step's critical path. Otherwise the copies are cudaMemcpyAsync calls.
 #include <new>
 
 #include "common.cuh"
@@ -85,20 +90,100 @@ extern "C" tee_status tee_decode_step_create(const tee_gate_desc* gate, int32_t 
 
 namespace {
 
+struct CopySeg {
+    const uint8_t* src;
+    uint8_t* dst;
+    int64_t bytes;
+};
+struct CopyList {
+    CopySeg seg[4];
+    int n;
+};
+
+// Up to four copies in one launch, 16 bytes a thread and step where both ends
+// are 16-byte aligned. Loads are volatile-cached (ld.global.cv): a replay reads
+// what the host wrote since, not a line that an earlier step left in a cache.
+__global__ void __launch_bounds__(256) step_copy_kernel(CopyList l) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int s = 0; s < l.n; ++s) {
+        const CopySeg c = l.seg[s];
+        const bool v16 = ((reinterpret_cast<uintptr_t>(c.src) | reinterpret_cast<uintptr_t>(c.dst)) & 15) == 0;
+        const int64_t n16 = v16 ? c.bytes / 16 : 0;
+        for (int64_t i = tid; i < n16; i += nth)
+            reinterpret_cast<uint4*>(c.dst)[i] = __ldcv(reinterpret_cast<const uint4*>(c.src) + i);
+        for (int64_t i = n16 * 16 + tid; i < c.bytes; i += nth) c.dst[i] = __ldcv(c.src + i);
+    }
+}
+
+// The device's address of page-locked host memory it reaches directly, or null.
+const void* device_view(const void* p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+tee_status launch_copies(const CopyList& l, cudaStream_t s) {
+    int64_t most = 0;
+    for (int i = 0; i < l.n; ++i) most = l.seg[i].bytes > most ? l.seg[i].bytes : most;
+    if (most == 0) return TEE_OK;
+    const int64_t want = (most / 16 + 255) / 256;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want > 4 * sm_count() ? 4 * sm_count() : want));
+    step_copy_kernel<<<blocks, 256, 0, s>>>(l);
+    return launch_status();
+}
+
+// The device's views of the eight host buffers (h_prev, h_cur, pos, seq, score,
+// mask, counts, out); looked up outside any stream capture.
+struct HostViews {
+    const void* v[8];
+};
+HostViews host_views(const void* const (&ptr)[8]) {
+    HostViews h{};
+    for (int i = 0; i < 8; ++i) h.v[i] = device_view(ptr[i]);
+    return h;
+}
+
 // The step's copies and calls, enqueued on stream s.
 tee_status enqueue_step(tee_decode_step* step, int n, const void* h_prev, const void* h_cur, const int32_t* pos,
-                        const int32_t* seq, float* score, uint8_t* mask, int32_t* counts, void* out, cudaStream_t s) {
+                        const int32_t* seq, float* score, uint8_t* mask, int32_t* counts, void* out,
+                        const HostViews& views, cudaStream_t s) {
 
     void* stream = s;
     const tee_step_buffers& b = step->buf;
     const int d = step->gate.d;
     const size_t row = static_cast<size_t>(d) * dtype_bytes(step->gate.dtype);
+    const bool use_seq = seq && b.seq;
+    // the device's view of every host buffer, or the copies go through cudaMemcpyAsync
+    const void* const* hv = views.v;
+    const bool mapped = hv[0] && hv[1] && hv[2] && (!use_seq || hv[3]) && (!score || hv[4]) && (!mask || hv[5]) &&
+                        (!counts || hv[6]) && (!out || hv[7]);
+    tee_status st = TEE_OK;
     // inputs
-    tee_status st = cuda_status(cudaMemcpyAsync(b.h_prev, h_prev, n * row, cudaMemcpyHostToDevice, s));
-    if (st == TEE_OK) st = cuda_status(cudaMemcpyAsync(b.h_cur, h_cur, n * row, cudaMemcpyHostToDevice, s));
-    if (st == TEE_OK) st = cuda_status(cudaMemcpyAsync(b.pos, pos, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-    if (st == TEE_OK && seq && b.seq)
-        st = cuda_status(cudaMemcpyAsync(b.seq, seq, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    if (mapped) {
+        CopyList l{};
+        l.seg[l.n++] = CopySeg{static_cast<const uint8_t*>(hv[0]), static_cast<uint8_t*>(b.h_prev),
+                               static_cast<int64_t>(n * row)};
+        l.seg[l.n++] = CopySeg{static_cast<const uint8_t*>(hv[1]), static_cast<uint8_t*>(b.h_cur),
+                               static_cast<int64_t>(n * row)};
+        l.seg[l.n++] = CopySeg{static_cast<const uint8_t*>(hv[2]), reinterpret_cast<uint8_t*>(b.pos),
+                               static_cast<int64_t>(n * sizeof(int32_t))};
+        if (use_seq)
+            l.seg[l.n++] = CopySeg{static_cast<const uint8_t*>(hv[3]), reinterpret_cast<uint8_t*>(b.seq),
+                                   static_cast<int64_t>(n * sizeof(int32_t))};
+        st = launch_copies(l, s);
+    } else {
+        st = cuda_status(cudaMemcpyAsync(b.h_prev, h_prev, n * row, cudaMemcpyHostToDevice, s));
+        if (st == TEE_OK) st = cuda_status(cudaMemcpyAsync(b.h_cur, h_cur, n * row, cudaMemcpyHostToDevice, s));
+        if (st == TEE_OK)
+            st = cuda_status(cudaMemcpyAsync(b.pos, pos, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+        if (st == TEE_OK && use_seq)
+            st = cuda_status(cudaMemcpyAsync(b.seq, seq, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    }
     if (st != TEE_OK) return st;
     // the front (exiting token r scattered to row r of out), then the fill of the
     // exiting tokens at their cache positions (their count stays on the device)
@@ -113,6 +198,21 @@ tee_status enqueue_step(tee_decode_step* step, int n, const void* h_prev, const 
         if (st != TEE_OK) return st;
     }
     // results
+    if (mapped) {
+        CopyList l{};
+        if (score)
+            l.seg[l.n++] = CopySeg{reinterpret_cast<const uint8_t*>(b.score), static_cast<uint8_t*>(const_cast<void*>(hv[4])),
+                                   static_cast<int64_t>(n * sizeof(float))};
+        if (mask)
+            l.seg[l.n++] = CopySeg{b.mask, static_cast<uint8_t*>(const_cast<void*>(hv[5])), static_cast<int64_t>(n)};
+        if (counts)
+            l.seg[l.n++] = CopySeg{reinterpret_cast<const uint8_t*>(b.counts), static_cast<uint8_t*>(const_cast<void*>(hv[6])),
+                                   static_cast<int64_t>(2 * sizeof(int32_t))};
+        if (out)
+            l.seg[l.n++] = CopySeg{static_cast<const uint8_t*>(b.out), static_cast<uint8_t*>(const_cast<void*>(hv[7])),
+                                   static_cast<int64_t>(b.n_out) * static_cast<int64_t>(row)};
+        return launch_copies(l, s);
+    }
     if (score) st = cuda_status(cudaMemcpyAsync(score, b.score, n * sizeof(float), cudaMemcpyDeviceToHost, s));
     if (st == TEE_OK && mask) st = cuda_status(cudaMemcpyAsync(mask, b.mask, n, cudaMemcpyDeviceToHost, s));
     if (st == TEE_OK && counts)
@@ -130,6 +230,7 @@ bool capture_step(tee_decode_step* step, int n, const void* const (&ptr)[8]) {
         step->exec = nullptr;
     }
     step->g_n = -1;
+    const HostViews views = host_views(ptr);
     if (cudaStreamBeginCapture(step->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
@@ -138,7 +239,7 @@ bool capture_step(tee_decode_step* step, int n, const void* const (&ptr)[8]) {
                                        static_cast<const int32_t*>(ptr[3]), static_cast<float*>(const_cast<void*>(ptr[4])),
                                        static_cast<uint8_t*>(const_cast<void*>(ptr[5])),
                                        static_cast<int32_t*>(const_cast<void*>(ptr[6])), const_cast<void*>(ptr[7]),
-                                       step->cap);
+                                       views, step->cap);
     cudaGraph_t graph = nullptr;
     const cudaError_t e = cudaStreamEndCapture(step->cap, &graph);
     bool ok = st == TEE_OK && e == cudaSuccess && graph &&
@@ -166,7 +267,7 @@ extern "C" tee_status tee_decode_step_run_host(tee_decode_step* step, int32_t n,
     for (int i = 0; i < 8 && same; ++i) same = step->g_ptr[i] == ptr[i];
     if (!same && !step->graph_refused && !capture_step(step, n, ptr)) step->graph_refused = true;
     if (!step->exec || (!same && step->graph_refused))   // no graph for these arguments: enqueue directly
-        return enqueue_step(step, n, h_prev, h_cur, pos, seq, score, mask, counts, out, user);
+        return enqueue_step(step, n, h_prev, h_cur, pos, seq, score, mask, counts, out, host_views(ptr), user);
     tee_status st = cuda_status(cudaEventRecord(step->ev_in, user));
     if (st == TEE_OK) st = cuda_status(cudaStreamWaitEvent(step->cap, step->ev_in, 0));
     if (st == TEE_OK) st = cuda_status(cudaGraphLaunch(step->exec, step->cap));
