@@ -7,9 +7,11 @@
 // L L^T (blocked right-looking Cholesky in fp32, 64 x 64 tiles: the diagonal tile
 // in one CTA's shared memory, the panel below it by substitution, the trailing
 // lower triangle updated tile by tile), and W = L^-T L^-1 R is solved in place in
-// the output by block forward and backward substitution: each 64-row block solved
-// against its diagonal tile, the rest of the right-hand sides updated on the
-// tensor cores (the same GEMM, fp32 operands split into bf16 high and low parts).
+// the output by block forward and backward substitution: each 64-row block
+// multiplied by its diagonal tile's inverse (all 64 x 64 inverses computed at
+// once after the factorisation, so a block's solve is a product with no
+// dependent steps), the rest of the right-hand sides updated on the tensor cores
+// (the same GEMM, fp32 operands split into bf16 high and low parts).
 #include "common.cuh"
 
 namespace tee {
@@ -131,34 +133,28 @@ __global__ void __launch_bounds__(NT) syrk_kernel(float* __restrict__ G, int64_t
     tile_update(c, ld, a, ld, b, ld, sa, sb);
 }
 
-// Forward substitution on block row k of the right-hand sides: R_k <- L_kk^-1 R_k,
-// 16 columns per CTA (16 threads per column, rows in order).
-// Backward (upper = true): R_k <- L_kk^-T R_k, rows in reverse.
-__global__ void __launch_bounds__(NT) trsm_rhs_kernel(const float* __restrict__ G, int64_t ld, float* __restrict__ R,
-                                                      int64_t ldr, int k, bool upper) {
+// The inverse of every diagonal tile of L at once (after the factorisation): CTA
+// k inverts L_kk into Li[k] ([64][64], lower triangular) by forward substitution
+// on the identity's columns, one column per thread (the columns are independent).
+__global__ void __launch_bounds__(NT) trtri_tiles_kernel(const float* __restrict__ G, int64_t ld, float* __restrict__ Li) {
     __shared__ float l[NB][TLD];
-    __shared__ float x[NB][RPC + 1];   // x[row][col]
+    __shared__ float x[NB][TLD];   // x[i][j]: row i of the inverse's column j
+    const int k = blockIdx.x;
     const float* lk = G + static_cast<int64_t>(k) * NB * ld + static_cast<int64_t>(k) * NB;
-    float* rk = R + static_cast<int64_t>(k) * NB * ldr + static_cast<int64_t>(blockIdx.x) * RPC;
     for (int e = threadIdx.x; e < NB * NB; e += NT) l[e / NB][e % NB] = lk[static_cast<int64_t>(e / NB) * ld + e % NB];
-    for (int e = threadIdx.x; e < NB * RPC; e += NT) x[e / RPC][e % RPC] = rk[static_cast<int64_t>(e / RPC) * ldr + e % RPC];
     __syncthreads();
-    const int col = threadIdx.x >> 4, sub = threadIdx.x & 15;
-    for (int step = 0; step < NB; ++step) {
-        const int r = upper ? NB - 1 - step : step;
-        float s = 0.f;
-        if (!upper) {
-            for (int rr = sub; rr < r; rr += 16) s = fmaf(l[r][rr], x[rr][col], s);   // L[r][rr], rr < r
-        } else {
-            for (int rr = r + 1 + sub; rr < NB; rr += 16) s = fmaf(l[rr][r], x[rr][col], s);   // L^T[r][rr] = L[rr][r]
+    const int j = threadIdx.x;
+    if (j < NB) {
+        for (int i = 0; i < j; ++i) x[i][j] = 0.f;
+        for (int i = j; i < NB; ++i) {
+            float sum = i == j ? 1.f : 0.f;
+            for (int c = j; c < i; ++c) sum = fmaf(-l[i][c], x[c][j], sum);
+            x[i][j] = sum / l[i][i];
         }
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (sub == 0) x[r][col] = (x[r][col] - s) / l[r][r];
-        __syncwarp();
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < NB * RPC; e += NT) rk[static_cast<int64_t>(e / RPC) * ldr + e % RPC] = x[e / RPC][e % RPC];
+    float* out = Li + static_cast<int64_t>(k) * NB * NB;
+    for (int e = threadIdx.x; e < NB * NB; e += NT) out[e] = x[e / NB][e % NB];
 }
 
 // fp32 -> bf16 split for the tensor-core updates: x = hi + lo with hi = bf16(x) and
@@ -202,6 +198,47 @@ __global__ void __launch_bounds__(NT) split_cols_kernel(const float* __restrict_
     }
 }
 
+// One block row of a substitution: R_k <- Li_k R_k (forward) or Li_k^T R_k
+// (backward) for the 64 columns 64 blockIdx.x .. + 63, in place (each CTA owns its
+// columns), plus the B-form split of the result for the trailing update:
+// b3[c][0..192) = split(R_k[0..64)[c]).
+__global__ void __launch_bounds__(NT) rhs_mul_kernel(const float* __restrict__ Li, float* __restrict__ R, int64_t ldr,
+                                                     int k, bool upper, __nv_bfloat16* __restrict__ b3) {
+    __shared__ float sa[NB][TLD];   // sa[kk][m] = A(m, kk): A = Li_k, or Li_k^T
+    __shared__ float sb[NB][TLD];   // sb[kk][c] = R_k(kk, c)
+    const float* lk = Li + static_cast<int64_t>(k) * NB * NB;
+    float* rk = R + static_cast<int64_t>(k) * NB * ldr + static_cast<int64_t>(blockIdx.x) * NB;
+    for (int e = threadIdx.x; e < NB * NB; e += NT) {
+        const int r = e / NB, c = e % NB;
+        sa[c][r] = upper ? lk[c * NB + r] : lk[r * NB + c];
+        sb[r][c] = rk[static_cast<int64_t>(r) * ldr + c];
+    }
+    __syncthreads();
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4] = {};
+#pragma unroll 8
+    for (int kk = 0; kk < NB; ++kk) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            av[q] = sa[kk][ty * 4 + q];
+            bv[q] = sb[kk][tx * 4 + q];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) acc[q][w] = fmaf(av[q], bv[w], acc[q][w]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const int row = ty * 4 + q, col = tx * 4 + w;
+            rk[static_cast<int64_t>(row) * ldr + col] = acc[q][w];
+            split_store(b3 + (static_cast<int64_t>(blockIdx.x) * NB + col) * K3, row, acc[q][w], true);
+        }
+}
+
 }  // namespace
 
 }  // namespace tee
@@ -213,7 +250,9 @@ static size_t split_bytes(int rows) { return round_up(static_cast<size_t>(rows) 
 extern "C" size_t tee_ridge_fit_workspace_size(int32_t n, int32_t d, int32_t d_out) {
     if (n <= 0 || d <= 0 || d_out <= 0) return TEE_WS_HEADER_BYTES;
     const size_t gram = ridge_gram_ws_bytes(n, d, d_out), split = split_bytes(d) + split_bytes(d_out);
-    return TEE_WS_HEADER_BYTES + round_up(static_cast<size_t>(d) * d * 4, 1024) + (gram > split ? gram : split);
+    // G (then L), the diagonal tiles' inverses, then the Gram's or the splits' scratch
+    return TEE_WS_HEADER_BYTES + round_up(static_cast<size_t>(d) * d * 4, 1024) +
+           round_up(static_cast<size_t>(d) * NB * 4, 1024) + (gram > split ? gram : split);
 }
 
 extern "C" tee_status tee_ridge_fit(int32_t n, int32_t d, int32_t d_out, const void* x, int64_t ld_x, const void* y,
@@ -229,7 +268,8 @@ extern "C" tee_status tee_ridge_fit(int32_t n, int32_t d, int32_t d_out, const v
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws) + TEE_WS_HEADER_BYTES;
     float* g = reinterpret_cast<float*>(base);
-    char* scratch = base + round_up(static_cast<size_t>(d) * d * 4, 1024);
+    float* li = reinterpret_cast<float*>(base + round_up(static_cast<size_t>(d) * d * 4, 1024));
+    char* scratch = reinterpret_cast<char*>(li) + round_up(static_cast<size_t>(d) * NB * 4, 1024);
     tee_status st = ridge_gram(n, d, d_out, x, ld_x, y, ld_y, lambda, g, w, ld_w, scratch, ws, s);
     if (st != TEE_OK) return st;
     const int nb = d / NB, ncol = d_out / NB;
@@ -252,28 +292,26 @@ extern "C" tee_status tee_ridge_fit(int32_t n, int32_t d, int32_t d_out, const v
         const int64_t b = (elems + NT - 1) / NT;
         return static_cast<int>(b < 2048 ? b : 2048);
     };
+    trtri_tiles_kernel<<<nb, NT, 0, s>>>(g, d, li);
+    if ((st = launch_status()) != TEE_OK) return st;
     for (int k = 0; k < nb; ++k) {   // L Z = R
-        trsm_rhs_kernel<<<d_out / RPC, NT, 0, s>>>(g, d, w, ld_w, k, false);
+        rhs_mul_kernel<<<ncol, NT, 0, s>>>(li, w, ld_w, k, false, b3);   // Z_k = L_kk^-1 R_k, and its split
         if ((st = launch_status()) != TEE_OK) return st;
         const int m = d - (k + 1) * NB;   // rows below: R_i -= L_ik Z_k
         if (m > 0) {
             split_rows_kernel<<<blocks_for(static_cast<int64_t>(m) * NB), NT, 0, s>>>(
                 g + static_cast<int64_t>(k + 1) * NB * d + static_cast<int64_t>(k) * NB, d, m, a3, false);
             if ((st = launch_status()) != TEE_OK) return st;
-            split_cols_kernel<<<ncol, NT, 0, s>>>(w + static_cast<int64_t>(k) * NB * ld_w, ld_w, d_out, b3, true);
-            if ((st = launch_status()) != TEE_OK) return st;
             st = ridge_update_tc(m, d_out, K3, a3, b3, w + static_cast<int64_t>(k + 1) * NB * ld_w, ld_w, ws, s);
             if (st != TEE_OK) return st;
         }
     }
     for (int k = nb - 1; k >= 0; --k) {   // L^T W = Z
-        trsm_rhs_kernel<<<d_out / RPC, NT, 0, s>>>(g, d, w, ld_w, k, true);
+        rhs_mul_kernel<<<ncol, NT, 0, s>>>(li, w, ld_w, k, true, b3);   // W_k = L_kk^-T Z_k, and its split
         if ((st = launch_status()) != TEE_OK) return st;
         const int m = k * NB;   // rows above: R_i -= L_ki^T W_k, A[i][kk] = L[k NB + kk][i]
         if (m > 0) {
             split_cols_kernel<<<(m + NB - 1) / NB, NT, 0, s>>>(g + static_cast<int64_t>(k) * NB * d, d, m, a3, false);
-            if ((st = launch_status()) != TEE_OK) return st;
-            split_cols_kernel<<<ncol, NT, 0, s>>>(w + static_cast<int64_t>(k) * NB * ld_w, ld_w, d_out, b3, true);
             if ((st = launch_status()) != TEE_OK) return st;
             st = ridge_update_tc(m, d_out, K3, a3, b3, w, ld_w, ws, s);
             if (st != TEE_OK) return st;
