@@ -256,6 +256,7 @@ template <bool NARROW>
 __global__ void __launch_bounds__(THREADS, 1)
 fill_decode_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ DecodeArgs a, void* ws) {
     using Lay = DLayout<NARROW>;
+    allow_dependents();   // a dependent launched after the fill waits for it before any access
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* h_full = reinterpret_cast<uint64_t*>(smem + Lay::OFF_SMALL);   // ring blocks past the first RH

@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(F_THREADS, 1) front_kernel(const __grid_consta
     __shared__ uint32_t s_pub[2];       // this CTA's minimum score (bits) and its tokens exiting on their own
     __shared__ uint32_t s_exit_bits;    // bit w: token of warp w exits on its own
     allow_dependents();
+    wait_prior_grid();   // launched as a dependent (a copy kernel before it): every access waits for it
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t cta = cluster_rank();
     const int n_ctas = static_cast<int>(gridDim.x);   // the grid is one cluster
@@ -252,13 +253,17 @@ tee_status launch_front(const FrontArgs& a, cudaStream_t stream) {
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(fw * 32);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = ctas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // it may start launching while the kernel before it runs (it waits for that
+    // kernel before any memory access)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, front_kernel<T>, a));
     return st != TEE_OK ? st : launch_status();
 }

@@ -103,7 +103,11 @@ struct CopyList {
 // Up to four copies in one launch, 16 bytes a thread and step where both ends
 // are 16-byte aligned. Loads are volatile-cached (ld.global.cv): a replay reads
 // what the host wrote since, not a line that an earlier step left in a cache.
+// The next kernel may start launching at once; launched as a dependent itself
+// (the results' copy after the fill), it waits for the kernel before it first.
 __global__ void __launch_bounds__(256) step_copy_kernel(CopyList l) {
+    allow_dependents();
+    wait_prior_grid();
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int s = 0; s < l.n; ++s) {
@@ -127,14 +131,23 @@ const void* device_view(const void* p) {
     return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
-tee_status launch_copies(const CopyList& l, cudaStream_t s) {
+tee_status launch_copies(const CopyList& l, bool dependent, cudaStream_t s) {
     int64_t most = 0;
     for (int i = 0; i < l.n; ++i) most = l.seg[i].bytes > most ? l.seg[i].bytes : most;
     if (most == 0) return TEE_OK;
     const int64_t want = (most / 16 + 255) / 256;
     const int blocks = static_cast<int>(want < 1 ? 1 : (want > 4 * sm_count() ? 4 * sm_count() : want));
-    step_copy_kernel<<<blocks, 256, 0, s>>>(l);
-    return launch_status();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    const tee_status st = cuda_status(cudaLaunchKernelEx(&cfg, step_copy_kernel, l));
+    return st != TEE_OK ? st : launch_status();
 }
 
 // The device's views of the eight host buffers (h_prev, h_cur, pos, seq, score,
@@ -175,7 +188,7 @@ tee_status enqueue_step(tee_decode_step* step, int n, const void* h_prev, const 
         if (use_seq)
             l.seg[l.n++] = CopySeg{static_cast<const uint8_t*>(hv[3]), reinterpret_cast<uint8_t*>(b.seq),
                                    static_cast<int64_t>(n * sizeof(int32_t))};
-        st = launch_copies(l, s);
+        st = launch_copies(l, false, s);
     } else {
         st = cuda_status(cudaMemcpyAsync(b.h_prev, h_prev, n * row, cudaMemcpyHostToDevice, s));
         if (st == TEE_OK) st = cuda_status(cudaMemcpyAsync(b.h_cur, h_cur, n * row, cudaMemcpyHostToDevice, s));
@@ -211,7 +224,7 @@ tee_status enqueue_step(tee_decode_step* step, int n, const void* h_prev, const 
         if (out)
             l.seg[l.n++] = CopySeg{static_cast<const uint8_t*>(b.out), static_cast<uint8_t*>(const_cast<void*>(hv[7])),
                                    static_cast<int64_t>(b.n_out) * static_cast<int64_t>(row)};
-        return launch_copies(l, s);
+        return launch_copies(l, true, s);   // a dependent of the fill (or the front)
     }
     if (score) st = cuda_status(cudaMemcpyAsync(score, b.score, n * sizeof(float), cudaMemcpyDeviceToHost, s));
     if (st == TEE_OK && mask) st = cuda_status(cudaMemcpyAsync(mask, b.mask, n, cudaMemcpyDeviceToHost, s));
