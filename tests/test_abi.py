@@ -162,6 +162,14 @@ def test_exit_river_checks_on_the_host(lib):
     assert ws(pair, 64, 4096) == ws(pair, 64, 131072) > 0
     assert ws(chunk, 64, 131072) > ws(chunk, 64, 4096) > ws(pair, 64, 4096)
     assert ws(3, 64, 4096) == 0 and lib.tee_exit_river_prep_size(ctypes.byref(by[3]), 8, 4096) == 0
+    # "auto" walks pairs when n_max x n_kv_heads fills two consumer groups per SM (on any
+    # part of up to 256 SMs, 64 items x 8 kv heads do; 16 items x 8 do not on one of more
+    # than 64 SMs, and without a device the library assumes a full-size part)
+    auto = _lib.RiverDesc(d=2048, n_q_heads=32, n_kv_heads=8, head_dim=64, d_ff=8192, rope_base=5e5, eps=1e-5,
+                          group=64, flags=0)
+    wa = lambda n, p: lib.tee_exit_river_workspace_size(ctypes.byref(auto), n, p)
+    assert wa(128, 4096) == ws(pair, 128, 4096) and wa(128, 131072) == wa(128, 4096)
+    assert wa(16, 131072) > wa(16, 4096) and wa(16, 4096) == ws(chunk, 16, 4096)
     layout = _lib.CacheLayout(s_layer=1 << 20, s_seq=1 << 14, s_head=4096 * 64, s_pos=64, n_layers=16, n_seq=64,
                               n_heads=8, max_pos=4096)
     fake = ctypes.c_void_p(16)
