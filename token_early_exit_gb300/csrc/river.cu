@@ -7,11 +7,11 @@
 //                       sum(h^2) per item; item checks; counters cleared
 //   w4_gemm<QKV>        [q|k|v] = (h * g) . [Wq|Wk|Wv], times 1/rms(h); RoPE on
 //                       q and k; q to the workspace, k and v to the cache slot
-//   river_attn          per (item, kv head, chunk of 256 / 128 positions): TMA
-//                       brings the chunk's K and V; scores and P.V as warp-level
-//                       tensor-core products, the partial softmax on their
-//                       accumulators; the last chunk of an (item, kv head)
-//                       merges the partials
+//   river_attn_pair     (or river_attn_split for few items) scores and P.V as
+//                       warp-level tensor-core products over TMA-fed K/V
+//                       chunks: persistent consumer groups each walking one
+//                       (item, kv head) pair's chunks with an online softmax, or
+//                       one CTA per chunk whose partials the last chunk merges
 //   w4_gemm<O>          h1 = h + o . Wo; bf16 (h1 * ffn_norm) and sum(h1^2)
 //   w4_gemm<GU>         gate | up from (h1 * g2) . [Wg|Wu] (64 columns of each
 //                       per tile), times 1/rms(h1); a = SiLU(gate) * up (bf16)
@@ -724,7 +724,8 @@ struct AttnArgs {
     int32_t* cnt;          // [n][n_kv]
 };
 
-// The attention is persistent: one CTA per SM, two consumer groups of four
+// The pair walk (calls whose (item, kv head) pairs fill its consumer groups) is
+// persistent: one CTA per SM, two consumer groups of four
 // warps, each fed by its own producer warp through its own ring of AT_STAGES
 // stages (a chunk of K and of V, TMA, one barrier each; the q rows, one bulk
 // copy, with a pair's first chunk). A group takes every chunk of an (item, kv
