@@ -480,10 +480,13 @@ typedef struct {
 /* tee_river_desc.flags: how the attention walks the cache; same results within
  * rounding. By default it walks whole (item, kv head) pairs, one persistent
  * consumer group per pair with an online softmax over the pair's chunks, when
- * n_max * n_kv_heads fills every group (two per SM), and otherwise splits each
- * sequence into chunks of one CTA each whose partial results a merge combines
- * (its workspace then holds the partials: it grows with max_pos). These force
- * one walk; the workspace size follows the flag. */
+ * n_max * n_kv_heads fills every group (two per SM) or the cache is too long for
+ * the other walk's merge (above ~87 K positions at head_dim 64 with 8 query
+ * heads per kv head), and otherwise splits each sequence into chunks of one CTA
+ * each whose partial results a merge combines (its workspace then holds the
+ * partials: it grows with max_pos). These force one walk; the workspace size
+ * follows the flag, and the chunk walk on a cache too long for it returns
+ * TEE_ERR_UNSUPPORTED. */
 #define TEE_RIVER_ATTN_BY_PAIR 1
 #define TEE_RIVER_ATTN_BY_CHUNK 2
 

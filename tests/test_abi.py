@@ -169,7 +169,12 @@ def test_exit_river_checks_on_the_host(lib):
                           group=64, flags=0)
     wa = lambda n, p: lib.tee_exit_river_workspace_size(ctypes.byref(auto), n, p)
     assert wa(128, 4096) == ws(pair, 128, 4096) and wa(128, 131072) == wa(128, 4096)
-    assert wa(16, 131072) > wa(16, 4096) and wa(16, 4096) == ws(chunk, 16, 4096)
+    assert wa(16, 65536) > wa(16, 4096) and wa(16, 4096) == ws(chunk, 16, 4096)
+    # a cache too long for the chunk walk's merge (3 floats per query head and chunk in a
+    # 32 KB buffer: 682 chunks of 256 positions at this descriptor's 4 query heads per kv
+    # head) takes the pair walk even for one item
+    assert wa(1, 682 * 256) == ws(chunk, 1, 682 * 256) and wa(1, 683 * 256) == ws(pair, 1, 683 * 256)
+    assert wa(1, 300000) == wa(1, 600000) == ws(pair, 1, 4096)
     layout = _lib.CacheLayout(s_layer=1 << 20, s_seq=1 << 14, s_head=4096 * 64, s_pos=64, n_layers=16, n_seq=64,
                               n_heads=8, max_pos=4096)
     fake = ctypes.c_void_p(16)

@@ -125,14 +125,23 @@ int choose_kg(int tiles, int ks, int K) {
                : 1;
 }
 
-// The pair kernel's consumer groups (two per SM) want a pair each at least.
-bool attn_by_pair(const tee_river_desc& D, int n_max) {
-    if (D.flags == TEE_RIVER_ATTN_BY_PAIR) return true;
-    if (D.flags == TEE_RIVER_ATTN_BY_CHUNK) return false;
-    return static_cast<int64_t>(n_max) * D.n_kv_heads >= static_cast<int64_t>(2) * sm_count();
-}
 int attn_chunks(const tee_river_desc& D, int max_pos) {
     return (max_pos + at_split_box(D.head_dim) - 1) / at_split_box(D.head_dim);
+}
+// The split walk's merge keeps 3 floats per (query head of a group, chunk) in the
+// 32 KB V buffer of its CTA.
+bool split_merge_fits(const tee_river_desc& D, int max_pos) {
+    const int rep = D.n_q_heads / std::max(1, D.n_kv_heads);
+    return static_cast<size_t>(attn_chunks(D, max_pos)) * rep * 3 * 4 <=
+           static_cast<size_t>(at_split_box(D.head_dim)) * D.head_dim * 2;
+}
+// The pair kernel's consumer groups (two per SM) want a pair each at least; a
+// cache too long for the split walk's merge goes to the pair walk too.
+bool attn_by_pair(const tee_river_desc& D, int n_max, int max_pos) {
+    if (D.flags == TEE_RIVER_ATTN_BY_PAIR) return true;
+    if (D.flags == TEE_RIVER_ATTN_BY_CHUNK) return false;
+    return static_cast<int64_t>(n_max) * D.n_kv_heads >= static_cast<int64_t>(2) * sm_count() ||
+           !split_merge_fits(D, max_pos);
 }
 
 RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
@@ -156,7 +165,7 @@ RiverWs river_ws(const tee_river_desc& D, int n_max, int max_pos) {
     w.ss_f = take(n * 4);
     w.ipos = take(n * 4);
     w.iseq = take(n * 4);
-    w.by_pair = attn_by_pair(D, n_max);
+    w.by_pair = attn_by_pair(D, n_max, max_pos);
     // the K groups' counters (tiles x ks), then (split attention) the chunks' arrival counters
     w.acnt = take((KG_CNT + (w.by_pair ? 0 : n * D.n_kv_heads)) * 4);
     w.apart = w.by_pair ? 0 : take(n * D.n_kv_heads * attn_chunks(D, max_pos) * rep * (D.head_dim + 2) * 4);
@@ -1792,9 +1801,7 @@ extern "C" tee_status tee_exit_river(const tee_river_desc* D, int32_t n_layers, 
         at.chunks = attn_chunks(*D, cl.max_pos);
         at.part = ws_at<float>(ws, w.apart);
         at.cnt = acnt + KG_CNT;
-        // the split merge keeps 3 floats per (query head of a group, chunk) in the 32 KB V buffer
-        if (static_cast<size_t>(at.chunks) * rep * 3 * 4 > static_cast<size_t>(at_split_box(hd)) * hd * 2)
-            return TEE_ERR_UNSUPPORTED;
+        if (!split_merge_fits(*D, cl.max_pos)) return TEE_ERR_UNSUPPORTED;   // the chunk walk forced
     }
 
     for (int l = 0; l < n_layers; ++l) {
